@@ -1,0 +1,260 @@
+"""Checks that pin the CPU oracle to facts fixed by the pages and by mathematics.
+
+Each ``pin_*`` function takes ``fwd`` (``oracle.forward`` or a build of the
+oracle with a planted mistake) and raises AssertionError when the oracle
+disagrees with the fact it checks.  None of them retypes the oracle's own
+loop: they use an independent formulation (explicit d x d matrices, products
+of explicit A_t), a library routine (numpy convolution, the normal CDF,
+scipy's logistic function, SVD, cumulative sums) or a closed form.
+
+Sources ("Technical Summary: PRISM (Parallel Residual Iterative Sequence
+Model)", gist.science/paper/2602.10796):
+  §2.1  S_t = S_{t-1} A_t + B_t, A_t rank-1 as in Gated DeltaNet
+  §2.2  anchor u_t from a ShortConv over the input; refinement loop
+        k^(l) = W_k^(l) u_t, p^(l) = W_p^(l) u_t, delta = GELU(p (.) r),
+        r^(l+1) = r^(l) - delta^(l); B_t = sum_l beta^(l) delta^(l) k^(l)^T
+  §3.3  at L = 0 PRISM reduces to Gated DeltaNet; the write has rank <= L
+        (plus the Gated DeltaNet rank-1 base write, see the design notes)
+"""
+from __future__ import annotations
+
+import numpy as np
+import scipy.special
+import scipy.stats
+import torch
+
+from linear_recurrent_sequence_causal_gb300.inputs import random_small
+
+
+def gdn_explicit(inp, T=None):
+    """Gated DeltaNet with explicit matrices: S <- S (alpha (I - beta k k^T)) + beta v k^T.
+
+    Independent of the oracle: forms every A_t as a d_k x d_k matrix.
+    Returns out [B,T,H,dv] and final state [B,H,dv,dk].
+    """
+    q, k, v = (inp[n].double().numpy() for n in ("q", "k", "v"))
+    la, be = inp["log_alpha"].double().numpy(), inp["beta"].double().numpy()
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    sl = inp.get("seq_lens")
+    out = np.zeros((B, T, H, dv))
+    fs = np.zeros((B, H, dv, dk))
+    I = np.eye(dk)
+    for b in range(B):
+        n = T if sl is None else int(sl[b])
+        for h in range(H):
+            S = np.zeros((dv, dk))
+            for t in range(n):
+                kt = k[b, t, h]
+                A = np.exp(la[b, t, h]) * (I - be[b, t, h] * np.outer(kt, kt))
+                S = S @ A + be[b, t, h] * np.outer(v[b, t, h], kt)
+                out[b, t, h] = S @ q[b, t, h]
+            fs[b, h] = S
+    return out, fs
+
+
+def _close(a, b, tol, what):
+    err = np.max(np.abs(a - b)) / max(np.max(np.abs(b)), 1e-300)
+    assert err <= tol, f"{what}: normwise error {err:.3e} > {tol:.1e}"
+
+
+def pin_l0_is_gated_deltanet(fwd):
+    """§3.3: with L = 0 the oracle must be the plain gated delta rule."""
+    inp = random_small(2, 40, 2, 5, 7, 0, 3, seed=11)
+    out, fs, _ = fwd(inp, L=0)
+    ref_o, ref_s = gdn_explicit(inp)
+    _close(out, ref_o, 1e-12, "L=0 output vs Gated DeltaNet")
+    _close(fs, ref_s, 1e-12, "L=0 final state vs Gated DeltaNet")
+
+
+def pin_zero_conv_is_gated_deltanet(fwd):
+    """conv_w = 0 => u = 0 => p = 0 => delta = GELU(0) = 0: any L gives Gated DeltaNet."""
+    inp = random_small(1, 33, 2, 6, 6, 3, 4, seed=12)
+    inp["conv_w"] = torch.zeros_like(inp["conv_w"])
+    out, fs, _ = fwd(inp)
+    ref_o, ref_s = gdn_explicit(inp)
+    _close(out, ref_o, 1e-12, "zero-conv output vs Gated DeltaNet")
+    _close(fs, ref_s, 1e-12, "zero-conv final state vs Gated DeltaNet")
+
+
+def pin_write_rank(fwd):
+    """§3.3 rank accumulation: B_t - beta_t v_t k_t^T has rank <= L (generically = L)."""
+    L = 2
+    inp = random_small(1, 24, 1, 6, 8, L, 4, seed=13)
+    _, _, tr = fwd(inp, trace=True)
+    k, v, be = inp["k"].numpy(), inp["v"].numpy(), inp["beta"].numpy()
+    for t in range(2, 24):   # from t = 2 on the anchor is non-zero
+        extra = tr["Bt"][0, t, 0] - be[0, t, 0] * np.outer(v[0, t, 0], k[0, t, 0])
+        s = np.linalg.svd(extra, compute_uv=False)
+        assert s[L] <= 1e-12 * s[0], f"t={t}: sigma_{L + 1}/sigma_1 = {s[L] / s[0]:.2e}"
+        assert s[L - 1] >= 1e-8 * s[0], f"t={t}: write rank below L"
+
+
+def pin_telescoping(fwd):
+    """§2.2: r^(l+1) = r^(l) - delta^(l) telescopes to r^(L+1) = r^(1) - sum_l delta^(l),
+    with r^(1) = v - u."""
+    inp = random_small(2, 20, 2, 5, 7, 4, 3, seed=14)
+    _, _, tr = fwd(inp, trace=True)
+    scale = np.max(np.abs(tr["r1"]))
+    np.testing.assert_allclose(tr["r_final"], tr["r1"] - tr["delta"].sum(axis=3),
+                               atol=1e-14 * scale, rtol=0)
+    np.testing.assert_allclose(tr["r1"], inp["v"].numpy() - tr["u"], atol=1e-15, rtol=0)
+
+
+def pin_brute_force_products(fwd):
+    """§2.1 for T <= 16: S_t = sum_{s<=t} B_s prod_{j=s+1..t} A_j with explicit A_j."""
+    inp = random_small(1, 16, 2, 4, 5, 2, 3, seed=15)
+    out, fs, tr = fwd(inp, trace=True)
+    q, k = inp["q"].numpy(), inp["k"].numpy()
+    la, be = inp["log_alpha"].numpy(), inp["beta"].numpy()
+    dk = k.shape[-1]
+    for h in range(2):
+        A = [np.exp(la[0, j, h]) * (np.eye(dk) - be[0, j, h] * np.outer(k[0, j, h], k[0, j, h]))
+             for j in range(16)]
+        for t in range(16):
+            S = np.zeros_like(tr["Bt"][0, 0, h])
+            for s in range(t + 1):
+                P = np.eye(dk)
+                for j in range(s + 1, t + 1):
+                    P = P @ A[j]
+                S += tr["Bt"][0, s, h] @ P
+            np.testing.assert_allclose(out[0, t, h], S @ q[0, t, h], atol=1e-12, rtol=0)
+            if t == 15:
+                np.testing.assert_allclose(fs[0, h], S, atol=1e-12, rtol=0)
+
+
+def pin_prefix_sum(fwd):
+    """alpha = 1, beta = 0: A_t = I, so S_t is the running sum of the writes B_s."""
+    inp = random_small(1, 12, 1, 4, 6, 2, 3, seed=16)
+    inp["log_alpha"].zero_()
+    inp["beta"].zero_()
+    out, _, tr = fwd(inp, trace=True)
+    S = np.cumsum(tr["Bt"][0, :, 0], axis=0)
+    np.testing.assert_allclose(out[0, :, 0], np.einsum("tij,tj->ti", S, inp["q"][0, :, 0].numpy()),
+                               atol=1e-12, rtol=0)
+
+
+def pin_no_write_no_output(fwd):
+    """L = 0 and beta = 0: nothing is ever written, so o = 0 exactly."""
+    inp = random_small(2, 10, 2, 4, 4, 0, 3, seed=17)
+    inp["beta"].zero_()
+    out, fs, _ = fwd(inp, L=0)
+    assert np.all(out == 0.0) and np.all(fs == 0.0)
+
+
+def pin_shortconv(fwd):
+    """§2.2 stage 1: u_t = sum_{j=1..w} c_j (.) v_{t-j} (strictly causal, zero history),
+    checked against numpy's full convolution with the taps shifted by one lag."""
+    w = 4
+    inp = random_small(2, 19, 3, 5, 6, 1, w, seed=18)
+    _, _, tr = fwd(inp, trace=True)
+    v, c = inp["v"].numpy(), inp["conv_w"].numpy()
+    T = v.shape[1]
+    for b in range(2):
+        for h in range(3):
+            for i in range(6):
+                taps = np.concatenate([[0.0], c[h, :, i]])   # lag 0 has no tap
+                ref = np.convolve(v[b, :, h, i], taps)[:T]
+                np.testing.assert_allclose(tr["u"][b, :, h, i], ref, atol=1e-14, rtol=0)
+
+
+def pin_direction(fwd):
+    """§2.2 direction k^(l) = normalize(W_k^(l) u): with a one-hot W_k = e_a e_c^T the
+    direction is e_a u_c / sqrt(u_c^2 + 1e-6).  Catches a transposed W_k."""
+    dk, dv = 3, 5
+    inp = random_small(1, 9, 1, dk, dv, 1, 2, seed=19)
+    Wk = torch.zeros_like(inp["Wk"])
+    Wk[0, 0, 1, 3] = 1.7   # row a = 1 (d_k side), column c = 3 (d_v side)
+    inp["Wk"] = Wk
+    _, _, tr = fwd(inp, trace=True)
+    u = tr["u"][0, :, 0]
+    kl = tr["kl"][0, :, 0, 0]
+    x = 1.7 * u[:, 3]
+    exp = np.zeros((9, dk))
+    exp[:, 1] = x / np.sqrt(x * x + 1e-6)
+    np.testing.assert_allclose(kl, exp, atol=1e-14, rtol=0)
+
+
+def pin_gain_and_gelu(fwd):
+    """§2.2 delta^(1) = GELU(p (.) r^(1)) with p = W_p u.  W_p = s I gives p = s u, and
+    GELU(x) = x Phi(x) with Phi the standard normal CDF (scipy)."""
+    dv = 6
+    inp = random_small(1, 14, 1, 4, dv, 2, 3, seed=20)
+    s = 1.9
+    inp["Wp"][0, 0] = s * torch.eye(dv, dtype=torch.float64)
+    _, _, tr = fwd(inp, trace=True)
+    u, r1 = tr["u"][0, :, 0], tr["r1"][0, :, 0]
+    x = s * u * r1
+    np.testing.assert_allclose(tr["delta"][0, :, 0, 0], x * scipy.stats.norm.cdf(x), atol=1e-14,
+                               rtol=1e-13)
+    # The second step acts on the updated residual r^(2) = r^(1) - delta^(1).
+    p2 = tr["pl"][0, :, 0, 1]
+    x2 = p2 * (r1 - tr["delta"][0, :, 0, 0])
+    np.testing.assert_allclose(tr["delta"][0, :, 0, 1], x2 * scipy.stats.norm.cdf(x2),
+                               atol=1e-14, rtol=1e-13)
+
+
+def pin_confidence_gate(fwd):
+    """§2.2 confidence gate beta^(l) = sigmoid(w_beta^(l) . u): w = 0 gives exactly 1/2;
+    w = s e_c gives expit(s u_c) (scipy).  The write factor is beta^(l) delta^(l)."""
+    dv = 5
+    inp = random_small(1, 11, 1, 4, dv, 2, 3, seed=21)
+    inp["wbeta"][0, 0].zero_()
+    inp["wbeta"][0, 1].zero_()
+    inp["wbeta"][0, 1, 3] = -2.3
+    _, _, tr = fwd(inp, trace=True)
+    assert np.all(tr["betal"][0, :, 0, 0] == 0.5)
+    np.testing.assert_allclose(tr["betal"][0, :, 0, 1], scipy.special.expit(-2.3 * tr["u"][0, :, 0, 3]),
+                               atol=1e-15, rtol=1e-14)
+    np.testing.assert_allclose(tr["dl"], tr["betal"][..., None] * tr["delta"], atol=1e-15, rtol=0)
+
+
+def pin_padding(fwd):
+    """Right padding: a length-n sequence padded to T gives the length-n result, zeros
+    after n, and a frozen final state; NaN in the padding must not leak."""
+    inp = random_small(3, 21, 2, 4, 5, 2, 3, seed=22)
+    lens = torch.tensor([21, 7, 1], dtype=torch.int32)
+    padded = {k: (v.clone() if v is not None else None) for k, v in inp.items()}
+    padded["seq_lens"] = lens
+    for b, n in enumerate(lens.tolist()):
+        for name in ("q", "k", "v", "log_alpha", "beta"):
+            padded[name][b, n:] = float("nan")
+    out, fs, _ = fwd(padded)
+    for b, n in enumerate(lens.tolist()):
+        one = {k: (v[b:b + 1, :n] if k in ("q", "k", "v", "log_alpha", "beta") else v)
+               for k, v in inp.items() if k != "seq_lens"}
+        o1, s1, _ = fwd(one)
+        np.testing.assert_allclose(out[b, :n], o1[0], atol=1e-14, rtol=0)
+        assert np.all(out[b, n:] == 0.0)
+        np.testing.assert_allclose(fs[b], s1[0], atol=1e-14, rtol=0)
+
+
+def pin_causality(fwd):
+    """Outputs before t0 do not depend on inputs at or after t0."""
+    inp = random_small(1, 30, 2, 4, 4, 3, 4, seed=23)
+    out1, _, _ = fwd(inp)
+    other = {k: (v.clone() if v is not None else None) for k, v in inp.items()}
+    g = torch.Generator().manual_seed(99)
+    for name in ("q", "k", "v", "log_alpha", "beta"):
+        other[name][:, 17:] = torch.randn(other[name][:, 17:].shape, generator=g,
+                                          dtype=torch.float64)
+    out2, _, _ = fwd(other)
+    np.testing.assert_array_equal(out1[:, :17], out2[:, :17])
+    assert not np.allclose(out1[:, 17:], out2[:, 17:])
+
+
+def pin_identity_activation(fwd):
+    """No-GELU ablation: delta^(l) = p^(l) (.) r^(l) exactly."""
+    inp = random_small(1, 12, 1, 4, 4, 3, 3, seed=24)
+    _, _, tr = fwd(inp, trace=True, identity_act=True)
+    r = tr["r1"][0, :, 0]
+    for l in range(3):
+        d = tr["pl"][0, :, 0, l] * r
+        np.testing.assert_allclose(tr["delta"][0, :, 0, l], d, atol=1e-15, rtol=0)
+        r = r - d
+
+
+ALL_PINS = [pin_l0_is_gated_deltanet, pin_zero_conv_is_gated_deltanet, pin_write_rank,
+            pin_telescoping, pin_brute_force_products, pin_prefix_sum, pin_no_write_no_output,
+            pin_shortconv, pin_direction, pin_gain_and_gelu, pin_confidence_gate, pin_padding,
+            pin_causality, pin_identity_activation]

@@ -1,0 +1,63 @@
+"""The CPU oracle against the facts that pin it (CPU only).
+
+Also plants plausible mistakes in copies of the oracle's C source and checks
+that at least one pin catches each of them.
+"""
+import functools
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "prism_oracle.c")
+
+
+@pytest.mark.parametrize("pin", oracle_pins.ALL_PINS, ids=lambda f: f.__name__)
+def test_oracle_pin(pin):
+    pin(oracle.forward)
+
+
+# (name, text in prism_oracle.c, replacement): each is a mistake a restatement of
+# the method could plausibly contain.
+MUTANTS = [
+    ("no_base_write", "Bw[(size_t)i * dk + j] = beta * vt[i] * kt[j];", "Bw[(size_t)i * dk + j] = 0.0;"),
+    ("forget_sign", "*sij - beta * Sk[i] * kt[j]", "*sij + beta * Sk[i] * kt[j]"),
+    ("forget_no_beta", "*sij - beta * Sk[i] * kt[j]", "*sij - Sk[i] * kt[j]"),
+    ("alpha_on_write", "*sij = alpha * (*sij - beta * Sk[i] * kt[j]) + Bw[(size_t)i * dk + j];",
+     "*sij = alpha * (*sij - beta * Sk[i] * kt[j] + Bw[(size_t)i * dk + j]);"),
+    ("conv_includes_current", "off_bthx(P, b, t - j, h, dv);", "off_bthx(P, b, t - j + 1, h, dv);"),
+    ("conv_tap_reversed", "((size_t)h * w + (j - 1)) * dv", "((size_t)h * w + (w - j)) * dv"),
+    ("wk_transposed", "Wk[(size_t)a * dv + c]", "Wk[(size_t)c * dk + a]"),
+    ("no_normalize", "kk[a] *= inv;", "kk[a] *= 1.0;"),
+    ("residual_not_updated", "r[i] -= dl[i];", "(void)0;"),
+    ("gelu_tanh", "return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
+     "return 0.5 * x * (1.0 + tanh(0.7978845608028654 * (x + 0.044715 * x * x * x)));"),
+    ("gate_sign", "const double bl = sigmoid(z);", "const double bl = sigmoid(-z);"),
+    ("r1_plus", "r[i] = vt[i] - u[i];", "r[i] = vt[i] + u[i];"),
+    ("write_uses_unnormalised_p", "dl[i] = P->identity_act ? x : gelu_erf(x);",
+     "dl[i] = P->identity_act ? x : gelu_erf(p[i]);"),
+    ("alpha_not_exp", "const double alpha = exp(", "const double alpha = -("),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(name, old, new, tmp_path):
+    src = open(ORACLE_SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    mutated = tmp_path / "mut.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-shared", "-fPIC", "-pthread",
+                    "-I", os.path.dirname(ORACLE_SRC), "-o", str(lib), str(mutated), "-lm"],
+                   check=True)
+    fwd = functools.partial(oracle.forward, lib_path=str(lib))
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(fwd)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"planted mistake {name} passed every pin"
