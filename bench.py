@@ -1,0 +1,391 @@
+"""Benchmark of the PRISM mixer forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one whole mixer forward pass (anchor + refinement kernel, then the
+chunkwise scan kernel) over one batch of the workload, inputs resident in HBM.
+Prints one JSON line on rank 0.  Under torchrun each rank runs its own replica
+of the workload (the (b, h) sequences are independent, so the path shards with
+no collective): weak scaling.
+
+``--impl reference`` times the fp64 CPU oracle (the only other implementation
+of the method) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from linear_recurrent_sequence_causal_gb300 import inputs as I  # noqa: E402
+
+METRIC = "PRISM mixer fwd tokens/s on 1 GB300; % of roofline (BF16 TC vs 8 TB/s HBM)"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "longctx_bf16"
+
+
+# ---------------------------------------------------------------- roofline model
+def algorithmic(wl, L):
+    """Algorithmic bytes and flops per launch of each kernel (see the design notes).
+
+    Per token-head (d = d_k = d_v, e = bytes per I/O element, C = chunk):
+      anchor/refine: bytes = d e (read v) + L 2d e (write k^(l), beta^(l) delta^(l))
+                     flops = 2 w d + L (4 d^2 + 2 d)
+      chunk scan:    bytes = 3 d e (q, k, v) + L 2d e (write factors) + d e (out) + 8 (gates)
+                     flops = C d (10 + 8L) + d^2 (6 + 2L) + C^2 / 3
+    plus the final state (d^2 fp32) once per sequence and the weights once per call.
+    """
+    d, e, C, w = wl.dk, (4 if wl.dtype == "f32" else 2), wl.chunk, wl.w
+    th = wl.B * wl.T * wl.H
+    k1_bytes = th * (d * e + L * 2 * d * e) + wl.H * (L * (2 * d * d + d) + w * d) * 4
+    k1_flops = th * (2 * w * d + L * (4 * d * d + 2 * d))
+    k2_bytes = th * (3 * d * e + L * 2 * d * e + d * e + 8) + wl.B * wl.H * d * d * 4
+    k2_flops = th * (C * d * (10 + 8 * L) + d * d * (6 + 2 * L) + C * C / 3.0)
+    return {"anchor_refine": (k1_bytes, k1_flops), "chunk_scan": (k2_bytes, k2_flops)}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_recurrent_sequence_causal_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        ent = t[kernel][workload]
+        if ent.get("source_hash") != kernel_source_hash():
+            return None
+        return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.samples = []
+        self.proc = None
+        self.sel = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            self.sel = vis.split(",")[device_index] if vis else str(device_index)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.sel, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        s = self.samples
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in s if num(p[0]) is not None]
+        mx = [num(p[1]) for p in s if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in s for i in range(4) if p[4 + i].lower().startswith("active")})
+        power = [num(p[2]) for p in s if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(s), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(inp, wl, L, target_s, threads):
+    """Time the oracle on a bounded sample of the workload's host inputs:
+    sequence 0, all heads, a prefix whose length is calibrated to about
+    ``target_s`` seconds."""
+    import oracle
+
+    def run(T):
+        sub = {k: (v[:1, :T].contiguous() if k in ("q", "k", "v", "log_alpha", "beta") else
+                   (v[:1] if k == "seq_lens" and v is not None else v)) for k, v in inp.items()}
+        t0 = time.perf_counter()
+        oracle.forward(sub, L=L, threads=threads)
+        return time.perf_counter() - t0
+
+    probe_T = min(wl.T, 256)
+    dt = run(probe_T)
+    T = max(probe_T, min(wl.T, int(probe_T * target_s / max(dt, 1e-6)) // 64 * 64))
+    dt = run(T) if T != probe_T else dt
+    return T, dt
+
+
+def reference_arm(args, wl, L):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    per_step = max(0.5, 150.0 / (args.steps + args.warmup))
+    import oracle
+    inp = I.generate(wl, L=L)
+    T, _ = oracle_sample(inp, wl, L, per_step, threads)      # calibration + first warm-up
+    sub = {k: (v[:1, :T].contiguous() if k in ("q", "k", "v", "log_alpha", "beta") else
+               (v[:1] if k == "seq_lens" and v is not None else v)) for k, v in inp.items()}
+    for _ in range(max(0, args.warmup - 1)):
+        oracle.forward(sub, L=L, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward(sub, L=L, threads=threads)
+    el = time.perf_counter() - t0
+    tok = T * args.steps
+    value = tok / el
+    sample = f"sequence 0, all {wl.H} heads, first {T} of {wl.T} tokens per step (fp64 oracle)"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "d_k": wl.dk,
+                       "d_v": wl.dv, "L": L, "conv_width": wl.w, "chunk": wl.chunk},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def our_arm(args, wl, L):
+    from linear_recurrent_sequence_causal_gb300 import build, prism
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if build.stale():
+        raise RuntimeError("libprism.so is missing or stale: run __graft_entry__.build() first")
+    prism.load()
+    dev = torch.device("cuda", local)
+    host = I.generate(wl, L=L, seed=wl.seed + rank)
+    d = prism.inputs_to_device(host, dev)
+    B, T, H, D = wl.B, wl.T, wl.H, wl.dk
+    dt = wl.torch_dtype
+    out = torch.empty((B, T, H, D), dtype=dt, device=dev)
+    fs = torch.empty((B, H, D, D), dtype=torch.float32, device=dev)
+    Kl = torch.empty((B, T, H, max(L, 1), D), dtype=dt, device=dev)
+    Dl = torch.empty((B, T, H, max(L, 1), D), dtype=dt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sl = d.get("seq_lens")
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if L > 0:
+            prism.prism_anchor_refine(d["v"], d["conv_w"], d["Wk"], d["Wp"], d["wbeta"], L,
+                                      seq_lens=sl, Kl=Kl, Dl=Dl, stream=stream, chunk=wl.chunk)
+        if ev is not None:
+            ev[1].record(stream)
+        prism.prism_chunk_scan(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], Kl, Dl, L,
+                               wl.chunk, wl.w, out=out, final_state=fs, seq_lens=sl,
+                               stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    tokens = B * T * world
+    value = tokens / (ms_per_step / 1e3)
+
+    # ---- end to end through the public API: host (pinned) inputs, copies timed
+    pinned = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
+    h_out = torch.empty((B, T, H, D), dtype=dt).pin_memory()
+    h_fs = torch.empty((B, H, D, D), dtype=torch.float32).pin_memory()
+    dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in host.items()}
+    ws = torch.empty(max(prism.workspace_bytes(prism.make_dims(B, T, H, D, D, wl.w, L, wl.chunk, dt)), 1),
+                     dtype=torch.uint8, device=dev)
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
+    d2h = h_out.numel() * h_out.element_size() + h_fs.numel() * 4
+
+    def e2e_step():
+        for k, v in pinned.items():
+            if v is not None:
+                dev_in[k].copy_(v, non_blocking=True)
+        prism.forward_inputs(dev_in, L, wl.chunk, out=out, final_state=fs, workspace=ws,
+                             stream=stream)
+        h_out.copy_(out, non_blocking=True)
+        h_fs.copy_(fs, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = tokens / (e2e_ms / 1e3)
+
+    # ---- roofline of the dominant kernel
+    hbm, tc, peak_kind = load_peaks()
+    alg = algorithmic(wl, L)
+    k1_avg = statistics.mean(k1_ms) if L > 0 else 0.0
+    k2_avg = statistics.mean(k2_ms)
+    dom = "chunk_scan" if k2_avg >= k1_avg else "anchor_refine"
+    dom_ms = k2_avg if dom == "chunk_scan" else k1_avg
+    by, fl = alg[dom]
+    t_bytes, t_flops = by / (hbm * 1e9), fl / (tc * 1e12)
+    if t_bytes >= t_flops:
+        roof = {"bound": "hbm", "achieved": by / (dom_ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": fl / (dom_ms / 1e3) / 1e12, "peak": tc,
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = committed_traffic(dom, wl.name)
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_kind} ({'MEASURED_PEAKS.json' if peak_kind == 'measured' else 'recipe fallback'})"
+    roof["kernel_ms"] = dom_ms
+    roof["algorithmic_bytes"] = by
+    roof["algorithmic_flops"] = fl
+    kernels = {"anchor_refine_ms": k1_avg, "chunk_scan_ms": k2_avg,
+               "share_chunk_scan": k2_avg / max(k1_avg + k2_avg, 1e-9)}
+    # whole-path roofline (both kernels as built) for context
+    tb = sum(v[0] for v in alg.values()) / (hbm * 1e9)
+    tf = sum(v[1] for v in alg.values()) / (tc * 1e12)
+    kernels["path_roofline_ms"] = 1e3 * max(tb, tf)
+    kernels["path_frac"] = kernels["path_roofline_ms"] / ms_per_step
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "H": wl.H, "d_k": wl.dk,
+                       "d_v": wl.dv, "L": L, "conv_width": wl.w, "chunk": wl.chunk,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (no flush)"
+                       if B * T * H * D * out.element_size() * 3 > 129e6
+                       else "inputs smaller than L2 (no flush)"},
+            "roofline": roof, "kernels": kernels, "clocks": clk,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * (2 if L > 0 else 1)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        Ts, dts = oracle_sample(host, wl, L, args.cpu_seconds, threads)
+        cb = Ts / dts
+        line["cpu_baseline"] = {"value": cb, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"sequence 0, all {wl.H} heads, first {Ts} tokens; "
+                                          f"{dts:.1f} s of fp64 oracle work on {threads} threads"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--L", type=int, default=None)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)     # at least 3 untimed warm-up steps, reported as run
+    wl = I.get_workload(args.workload)
+    L = wl.L if args.L is None else args.L
+    if args.impl == "reference":
+        reference_arm(args, wl, L)
+    else:
+        our_arm(args, wl, L)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,121 @@
+/*
+ * prism.h — C ABI of the PRISM mixer forward pass on GB300 (sm_103a).
+ *
+ * The operation ("Technical Summary: PRISM (Parallel Residual Iterative
+ * Sequence Model)", gist.science/paper/2602.10796):
+ *
+ *   §2.1  S_t = S_{t-1} A_t + B_t,  A_t = alpha_t (I - beta_t k_t k_t^T)
+ *         (the forget operator "identical to Gated DeltaNet"),
+ *         alpha_t = exp(log_alpha_t)
+ *   §2.2  stage 1: u_t = sum_{j=1..w} c_j (.) v_{t-j}    (causal ShortConv)
+ *         stage 2, l = 1..L, r^(1) = v_t - u_t:
+ *           k^(l) = normalize(W_k^(l) u_t),  p^(l) = W_p^(l) u_t,
+ *           delta^(l) = GELU(p^(l) (.) r^(l)),  r^(l+1) = r^(l) - delta^(l),
+ *           beta^(l) = sigmoid(w_beta^(l) . u_t)
+ *         write: B_t = beta_t v_t k_t^T + sum_l beta^(l) delta^(l) k^(l)^T
+ *   readout o_t = S_t q_t,  S_0 = 0.
+ *
+ * The Gated DeltaNet term beta_t v_t k_t^T of B_t is what makes L = 0 reduce to
+ * Gated DeltaNet (§3.3); normalize(x) = x / sqrt(|x|^2 + 1e-6); GELU is the
+ * exact erf form.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers, row-major and contiguous, owned by
+ *     the caller; the library allocates nothing and keeps no state.
+ *   - Every tensor pointer must be 16-byte aligned.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and runs asynchronously; errors found before launch are
+ *     returned synchronously and nothing is launched.
+ *   - Shapes (dims fields): q, k [B,T,H,d_k]; v, out [B,T,H,d_v] in `dtype`;
+ *     log_alpha, beta [B,T,H] fp32; conv_w [H,w,d_v] fp32 (row j-1 multiplies
+ *     v_{t-j}); Wk [H,L,d_k,d_v], Wp [H,L,d_v,d_v], wbeta [H,L,d_v] fp32;
+ *     final_state [B,H,d_v,d_k] fp32; seq_lens [B] int32.
+ */
+#ifndef PRISM_H
+#define PRISM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PRISM_API __attribute__((visibility("default")))
+#else
+#define PRISM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PRISM_F32 = 0, PRISM_BF16 = 1 } prism_dtype;
+
+/* flags */
+#define PRISM_FLAG_NO_GELU 1u   /* ablation: delta^(l) = p^(l) (.) r^(l) (identity activation) */
+
+typedef struct {
+    int B, T, H;          /* batch, sequence length, heads */
+    int d_k, d_v;         /* key / value head dims (supported: d_k == d_v in {16,32,64,128};
+                             fp32 also needs the working set to fit in shared memory) */
+    int conv_width;       /* w, ShortConv taps, 1..8 */
+    int L;                /* refinement steps, 0..8 */
+    int chunk;            /* scan chunk length C in {16, 32, 64} */
+    prism_dtype dtype;    /* I/O type of q, k, v, out (and of the write factors) */
+    unsigned flags;       /* PRISM_FLAG_* */
+} prism_dims;
+
+enum {
+    PRISM_OK = 0,
+    PRISM_ERR_INVALID_ARG = 1,   /* null required pointer, non-positive size, bad dtype */
+    PRISM_ERR_UNSUPPORTED = 2,   /* dims outside the supported set */
+    PRISM_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned */
+    PRISM_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than prism_workspace_bytes() */
+    PRISM_ERR_LAUNCH = 5,        /* a kernel launch failed (cudaGetLastError) */
+    PRISM_ERR_CUDA = 6           /* another CUDA runtime call failed */
+};
+
+/* Bytes of device workspace prism_forward needs for these dims (0 if the dims
+ * are invalid).  The workspace holds the per-token write factors k^(l) and
+ * beta^(l) delta^(l) between the two kernels. */
+PRISM_API size_t prism_workspace_bytes(const prism_dims* dims);
+
+/* The full mixer forward pass (anchor, refinement, write, chunkwise scan,
+ * readout) over B sequences.
+ *   seq_lens    NULL: every sequence has length T.  Otherwise tokens
+ *               t >= seq_lens[b] are padding: out is 0 there, they do not
+ *               touch the state, and their input values are never used
+ *               (NaN in padding cannot reach any output).  0 <= len <= T.
+ *   final_state NULL: not written.  Else S after each sequence's last token.
+ *   workspace   device buffer of at least prism_workspace_bytes(dims) bytes,
+ *               256-byte aligned; its contents are scratch.
+ * Returns PRISM_OK after enqueueing, or an error code (nothing launched). */
+PRISM_API int prism_forward(const prism_dims* dims,
+                  const void* q, const void* k, const void* v,
+                  const float* log_alpha, const float* beta,
+                  const float* conv_w, const float* Wk, const float* Wp, const float* wbeta,
+                  void* out, float* final_state, const int32_t* seq_lens,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Anchor + refinement only (§2.2 stages 1-2): writes the write factors
+ *   Kl [B,T,H,L,d_k] = k^(l)          (normalised directions)
+ *   Dl [B,T,H,L,d_v] = beta^(l) delta^(l)
+ * in dims->dtype, zeros at padded tokens.  Same conventions as prism_forward. */
+PRISM_API int prism_anchor_refine(const prism_dims* dims, const void* v, const float* conv_w,
+                        const float* Wk, const float* Wp, const float* wbeta,
+                        const int32_t* seq_lens, void* Kl, void* Dl, void* stream);
+
+/* Chunkwise scan only (§2.1 recurrence + readout), given write factors Kl, Dl
+ * laid out as prism_anchor_refine writes them (unused when dims->L == 0).
+ * prism_forward is prism_anchor_refine followed by this call.  Same
+ * conventions as prism_forward. */
+PRISM_API int prism_chunk_scan(const prism_dims* dims, const void* q, const void* k,
+                               const void* v, const float* log_alpha, const float* beta,
+                               const void* Kl, const void* Dl, void* out, float* final_state,
+                               const int32_t* seq_lens, void* stream);
+
+/* Static description of an error code. */
+PRISM_API const char* prism_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PRISM_H */

@@ -1,0 +1,184 @@
+"""Thin Python binding of libprism.so (the C ABI in include/prism.h).
+
+Argument marshalling only: every step of the mixer forward pass runs in the
+library's CUDA kernels.  PyTorch supplies device memory and the stream.  If the
+library has not been built (``__graft_entry__.build()`` or
+``python -m linear_recurrent_sequence_causal_gb300.build``) every call raises;
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+PRISM_F32, PRISM_BF16 = 0, 1
+PRISM_FLAG_NO_GELU = 1
+ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
+          3: "PRISM_ERR_MISALIGNED", 4: "PRISM_ERR_WORKSPACE", 5: "PRISM_ERR_LAUNCH",
+          6: "PRISM_ERR_CUDA"}
+EXPORTS = ("prism_workspace_bytes", "prism_forward", "prism_anchor_refine", "prism_chunk_scan",
+           "prism_strerror")
+
+
+class PrismError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("d_k", ctypes.c_int), ("d_v", ctypes.c_int), ("conv_width", ctypes.c_int),
+                ("L", ctypes.c_int), ("chunk", ctypes.c_int), ("dtype", ctypes.c_int),
+                ("flags", ctypes.c_uint)]
+
+
+_lock = threading.Lock()
+_lib = None
+_vp = ctypes.c_void_p
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libprism.so (raises if it is missing)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libprism.so not built ({path}); run __graft_entry__.build()")
+            lib = ctypes.CDLL(path)
+            lib.prism_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+            lib.prism_workspace_bytes.restype = ctypes.c_size_t
+            lib.prism_forward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 13 + [ctypes.c_size_t, _vp]
+            lib.prism_forward.restype = ctypes.c_int
+            lib.prism_anchor_refine.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
+            lib.prism_anchor_refine.restype = ctypes.c_int
+            lib.prism_chunk_scan.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 11
+            lib.prism_chunk_scan.restype = ctypes.c_int
+            lib.prism_strerror.argtypes = [ctypes.c_int]
+            lib.prism_strerror.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def strerror(code: int) -> str:
+    return load().prism_strerror(code).decode()
+
+
+def _check(code: int):
+    if code != 0:
+        raise PrismError(code, strerror(code))
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return PRISM_BF16
+    if t == torch.float32:
+        return PRISM_F32
+    raise PrismError(1, f"unsupported I/O dtype {t}")
+
+
+def make_dims(B, T, H, d_k, d_v, conv_width, L, chunk, dtype, no_gelu=False) -> Dims:
+    return Dims(B=B, T=T, H=H, d_k=d_k, d_v=d_v, conv_width=conv_width, L=L, chunk=chunk,
+                dtype=_dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype),
+                flags=PRISM_FLAG_NO_GELU if no_gelu else 0)
+
+
+def workspace_bytes(dims: Dims) -> int:
+    return int(load().prism_workspace_bytes(ctypes.byref(dims)))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise PrismError(1, "tensors must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def prism_forward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, out=None,
+                  final_state=None, seq_lens=None, workspace=None, stream=None,
+                  no_gelu=False, want_state=True):
+    """The mixer forward pass on CUDA tensors laid out as in include/prism.h.
+
+    Returns ``(out, final_state)``; ``final_state`` is None when
+    ``want_state`` is False and none was passed.
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    w = conv_w.shape[1]
+    dims = make_dims(B, T, H, dk, dv, w, L, chunk, q.dtype, no_gelu)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and want_state:
+        final_state = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    need = workspace_bytes(dims)
+    if workspace is None and L > 0:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = load().prism_forward(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                              _ptr(beta), _ptr(conv_w), _ptr(Wk), _ptr(Wp), _ptr(wbeta),
+                              _ptr(out), _ptr(final_state), _ptr(seq_lens), _ptr(workspace),
+                              ws_bytes, _stream_ptr(stream))
+    _check(rc)
+    return out, final_state
+
+
+def prism_anchor_refine(v, conv_w, Wk, Wp, wbeta, L, *, seq_lens=None, Kl=None, Dl=None,
+                        stream=None, no_gelu=False, chunk=64):
+    """Anchor + refinement only: returns the write factors (Kl, Dl)."""
+    B, T, H, dv = v.shape
+    dk = Wk.shape[2]
+    dims = make_dims(B, T, H, dk, dv, conv_w.shape[1], L, chunk, v.dtype, no_gelu)
+    if Kl is None:
+        Kl = torch.empty((B, T, H, L, dk), dtype=v.dtype, device=v.device)
+    if Dl is None:
+        Dl = torch.empty((B, T, H, L, dv), dtype=v.dtype, device=v.device)
+    rc = load().prism_anchor_refine(ctypes.byref(dims), _ptr(v), _ptr(conv_w), _ptr(Wk), _ptr(Wp),
+                                    _ptr(wbeta), _ptr(seq_lens), _ptr(Kl), _ptr(Dl),
+                                    _stream_ptr(stream))
+    _check(rc)
+    return Kl, Dl
+
+
+def prism_chunk_scan(q, k, v, log_alpha, beta, Kl, Dl, L, chunk, conv_width, *, out=None,
+                     final_state=None, seq_lens=None, stream=None, want_state=True):
+    """Chunkwise scan + readout only, given the write factors (Kl, Dl)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dims = make_dims(B, T, H, dk, dv, conv_width, L, chunk, q.dtype)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+    if final_state is None and want_state:
+        final_state = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    rc = load().prism_chunk_scan(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                 _ptr(beta), _ptr(Kl), _ptr(Dl), _ptr(out), _ptr(final_state),
+                                 _ptr(seq_lens), _stream_ptr(stream))
+    _check(rc)
+    return out, final_state
+
+
+def inputs_to_device(inp: dict, device="cuda") -> dict:
+    """Copy an input dict (see ``inputs.generate``) to the device, contiguous."""
+    return {k: (v.to(device).contiguous() if v is not None else None) for k, v in inp.items()}
+
+
+def forward_inputs(inp: dict, L: int, chunk: int, **kw):
+    """prism_forward on an input dict already on the device."""
+    return prism_forward(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"],
+                         inp["conv_w"], inp["Wk"], inp["Wp"], inp["wbeta"], L, chunk,
+                         seq_lens=inp.get("seq_lens"), **kw)

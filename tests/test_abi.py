@@ -1,0 +1,75 @@
+"""The C-ABI library builds, loads and exports every symbol include/prism.h
+declares; host-side argument checks answer without touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_recurrent_sequence_causal_gb300 import build, prism
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return prism.load()
+
+
+def declared_symbols():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names += re.findall(r"PRISM_API\s+[\w\s\*]+?\b(prism_\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert "prism_forward" in names and len(names) >= 5
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(names) >= set(prism.EXPORTS)
+
+
+def test_workspace_and_strerror(lib):
+    d = prism.make_dims(8, 4096, 16, 128, 128, 4, 2, 64, prism.PRISM_BF16)
+    # Kl and Dl: B*T*H*L*d*2 bytes each, 256-aligned, plus 256
+    assert prism.workspace_bytes(d) == 2 * 8 * 4096 * 16 * 2 * 128 * 2 + 256
+    assert prism.workspace_bytes(prism.make_dims(1, 8, 1, 128, 128, 4, 2, 64, prism.PRISM_F32)) == 0
+    for code in range(7):
+        assert lib.prism_strerror(code)
+    assert b"unknown" in lib.prism_strerror(99)
+
+
+def _fwd(lib, dims, ptrs, ws=0):
+    return lib.prism_forward(ctypes.byref(dims), *ptrs, ws, None)
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("B", 0, 1), ("T", -1, 1), ("d_k", 48, 2), ("chunk", 48, 2), ("L", 9, 2),
+    ("conv_width", 9, 2), ("conv_width", 0, 1), ("dtype", 7, 1), ("flags", 4, 1)])
+def test_bad_dims(lib, field, value, code):
+    d = prism.make_dims(2, 64, 2, 64, 64, 4, 2, 64, prism.PRISM_BF16)
+    if field == "d_k":
+        d.d_k = d.d_v = value
+    else:
+        setattr(d, field, value)
+    fake = [0x1000] * 13
+    assert _fwd(lib, d, fake, 1 << 40) == code
+
+
+def test_null_and_misaligned_pointers(lib):
+    d = prism.make_dims(2, 64, 2, 64, 64, 4, 2, 64, prism.PRISM_BF16)
+    good = [0x1000] * 13
+    assert _fwd(lib, d, [None] + good[1:], 1 << 40) == 1          # q NULL
+    bad = list(good); bad[2] = 0x1008                                 # v misaligned
+    assert _fwd(lib, d, bad, 1 << 40) == 3
+    assert _fwd(lib, d, good, 16) == 4                                # workspace too small
+    nows = list(good); nows[12] = None
+    assert _fwd(lib, d, nows, 1 << 40) == 4                           # workspace NULL
+    assert lib.prism_anchor_refine(ctypes.byref(d), None, *[0x1000] * 8, None) == 1
+    assert lib.prism_chunk_scan(ctypes.byref(d), *[0x1000] * 5, None, 0x1000, *[0x1000] * 3,
+                                None) == 1                            # Kl NULL with L > 0
