@@ -39,20 +39,26 @@ DEFAULT_WORKLOAD = "longctx_bf16"
 def algorithmic(wl, L):
     """Algorithmic bytes and flops per launch of each kernel (see the design notes).
 
-    Per token-head (d = d_k = d_v, e = bytes per I/O element, C = chunk):
-      anchor/refine: bytes = d e (read v) + L 2d e (write k^(l), beta^(l) delta^(l))
-                     flops = 2 w d + L (4 d^2 + 2 d)
-      chunk scan:    bytes = 3 d e (q, k, v) + L 2d e (write factors) + d e (out) + 8 (gates)
-                     flops = C d (10 + 8L) + d^2 (6 + 2L) + C^2 / 3
-    plus the final state (d^2 fp32) once per sequence and the weights once per call.
+    Per token-head (d = d_k = d_v, e = bytes per input element, C = chunk):
+      prepare: reads q, k, v, gates: 3 d e + 8; writes the chunk's factored map:
+               W, Kt, Qt_hi, Qt_lo (fp16) + U, O_intra (fp32) = 16 d, plus
+               N (d x d fp32 per chunk) = 4 d^2 / C when L > 0.
+               flops = 2 w d + L (4 d^2 + 2 d) + C d (10 + 8 L) + C^2 / 3 + 2 L d^2
+      scan:    reads that map, writes out (fp32): 16 d + 4 d^2 / C [L > 0] + 4 d
+               flops = 6 d^2
+    plus the weights once per call (prepare) and the final state (d^2 fp32) once
+    per sequence (scan).  The flop total over both kernels equals the chunk-form
+    count C d (10 + 8L) + d^2 (6 + 2L) + C^2 / 3 plus the anchor/refinement count.
     """
     d, e, C, w = wl.dk, (4 if wl.dtype == "f32" else 2), wl.chunk, wl.w
     th = wl.B * wl.T * wl.H
-    k1_bytes = th * (d * e + L * 2 * d * e) + wl.H * (L * (2 * d * d + d) + w * d) * 4
-    k1_flops = th * (2 * w * d + L * (4 * d * d + 2 * d))
-    k2_bytes = th * (3 * d * e + L * 2 * d * e + d * e + 8) + wl.B * wl.H * d * d * 4
-    k2_flops = th * (C * d * (10 + 8 * L) + d * d * (6 + 2 * L) + C * C / 3.0)
-    return {"anchor_refine": (k1_bytes, k1_flops), "chunk_scan": (k2_bytes, k2_flops)}
+    mid = 16 * d + (4 * d * d / C if L > 0 else 0) + 4.0 / C
+    k1_bytes = th * (3 * d * e + 8 + mid) + wl.H * (L * (2 * d * d + d) + w * d) * 4
+    k1_flops = th * (2 * w * d + L * (4 * d * d + 2 * d) + C * d * (10 + 8 * L) + C * C / 3.0
+                     + 2 * L * d * d)
+    k2_bytes = th * (mid + 4 * d) + wl.B * wl.H * d * d * 4
+    k2_flops = th * (6.0 * d * d)
+    return {"prepare": (k1_bytes, k1_flops), "scan": (k2_bytes, k2_flops)}
 
 
 def load_peaks():
@@ -220,27 +226,28 @@ def our_arm(args, wl, L):
     d = prism.inputs_to_device(host, dev)
     B, T, H, D = wl.B, wl.T, wl.H, wl.dk
     dt = wl.torch_dtype
-    out = torch.empty((B, T, H, D), dtype=dt, device=dev)
+    out = torch.empty((B, T, H, D), dtype=torch.float32, device=dev)
     fs = torch.empty((B, H, D, D), dtype=torch.float32, device=dev)
-    Kl = torch.empty((B, T, H, max(L, 1), D), dtype=dt, device=dev)
-    Dl = torch.empty((B, T, H, max(L, 1), D), dtype=dt, device=dev)
+    dims = prism.make_dims(B, T, H, D, D, wl.w, L, wl.chunk, dt)
+    ws = prism.alloc_workspace(dims, dev)
     stream = torch.cuda.current_stream(dev)
     sl = d.get("seq_lens")
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        if L > 0:
-            prism.prism_anchor_refine(d["v"], d["conv_w"], d["Wk"], d["Wp"], d["wbeta"], L,
-                                      seq_lens=sl, Kl=Kl, Dl=Dl, stream=stream, chunk=wl.chunk)
+        prism.prism_prepare(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"],
+                            d["Wk"], d["Wp"], d["wbeta"], L, wl.chunk, ws, seq_lens=sl,
+                            stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        prism.prism_chunk_scan(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], Kl, Dl, L,
-                               wl.chunk, wl.w, out=out, final_state=fs, seq_lens=sl,
-                               stream=stream)
+        prism.prism_scan(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], L, wl.chunk, wl.w, ws,
+                         out=out, final_state=fs, seq_lens=sl, stream=stream)
         if ev is not None:
             ev[2].record(stream)
 
+    # kernels per step: weight conversion (L > 0, bf16 path) + prepare + scan
+    launches_per_step = (1 if (L > 0 and wl.dtype == "bf16") else 0) + (1 if (L > 0 or wl.dtype == "bf16") else 0) + 1
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -274,11 +281,9 @@ def our_arm(args, wl, L):
 
     # ---- end to end through the public API: host (pinned) inputs, copies timed
     pinned = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
-    h_out = torch.empty((B, T, H, D), dtype=dt).pin_memory()
+    h_out = torch.empty((B, T, H, D), dtype=torch.float32).pin_memory()
     h_fs = torch.empty((B, H, D, D), dtype=torch.float32).pin_memory()
     dev_in = {k: (torch.empty_like(v, device=dev) if v is not None else None) for k, v in host.items()}
-    ws = torch.empty(max(prism.workspace_bytes(prism.make_dims(B, T, H, D, D, wl.w, L, wl.chunk, dt)), 1),
-                     dtype=torch.uint8, device=dev)
     h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None)
     d2h = h_out.numel() * h_out.element_size() + h_fs.numel() * 4
 
@@ -313,10 +318,10 @@ def our_arm(args, wl, L):
     # ---- roofline of the dominant kernel
     hbm, tc, peak_kind = load_peaks()
     alg = algorithmic(wl, L)
-    k1_avg = statistics.mean(k1_ms) if L > 0 else 0.0
+    k1_avg = statistics.mean(k1_ms)
     k2_avg = statistics.mean(k2_ms)
-    dom = "chunk_scan" if k2_avg >= k1_avg else "anchor_refine"
-    dom_ms = k2_avg if dom == "chunk_scan" else k1_avg
+    dom = "scan" if k2_avg >= k1_avg else "prepare"
+    dom_ms = k2_avg if dom == "scan" else k1_avg
     by, fl = alg[dom]
     t_bytes, t_flops = by / (hbm * 1e9), fl / (tc * 1e12)
     if t_bytes >= t_flops:
@@ -331,8 +336,12 @@ def our_arm(args, wl, L):
     roof["kernel_ms"] = dom_ms
     roof["algorithmic_bytes"] = by
     roof["algorithmic_flops"] = fl
-    kernels = {"anchor_refine_ms": k1_avg, "chunk_scan_ms": k2_avg,
-               "share_chunk_scan": k2_avg / max(k1_avg + k2_avg, 1e-9)}
+    kernels = {"prepare_ms": k1_avg, "scan_ms": k2_avg,
+               "share_scan": k2_avg / max(k1_avg + k2_avg, 1e-9)}
+    for name, (kb, kf) in alg.items():
+        kms = k1_avg if name == "prepare" else k2_avg
+        kernels[f"{name}_GBps"] = kb / (kms / 1e3) / 1e9
+        kernels[f"{name}_TFLOPs"] = kf / (kms / 1e3) / 1e12
     # whole-path roofline (both kernels as built) for context
     tb = sum(v[0] for v in alg.values()) / (hbm * 1e9)
     tf = sum(v[1] for v in alg.values()) / (tc * 1e12)
@@ -352,7 +361,7 @@ def our_arm(args, wl, L):
             "roofline": roof, "kernels": kernels, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps * (2 if L > 0 else 1)}
+            "gpu_launches": args.steps * launches_per_step}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         Ts, dts = oracle_sample(host, wl, L, args.cpu_seconds, threads)

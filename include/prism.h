@@ -22,14 +22,20 @@
  * Conventions for every entry point:
  *   - Tensor pointers are DEVICE pointers, row-major and contiguous, owned by
  *     the caller; the library allocates nothing and keeps no state.
- *   - Every tensor pointer must be 16-byte aligned.
+ *   - Every tensor pointer must be 16-byte aligned; the workspace 256-byte.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
  *     stream) and runs asynchronously; errors found before launch are
  *     returned synchronously and nothing is launched.
- *   - Shapes (dims fields): q, k [B,T,H,d_k]; v, out [B,T,H,d_v] in `dtype`;
+ *   - Shapes (dims fields): q, k [B,T,H,d_k]; v [B,T,H,d_v] in `dtype`;
  *     log_alpha, beta [B,T,H] fp32; conv_w [H,w,d_v] fp32 (row j-1 multiplies
  *     v_{t-j}); Wk [H,L,d_k,d_v], Wp [H,L,d_v,d_v], wbeta [H,L,d_v] fp32;
- *     final_state [B,H,d_v,d_k] fp32; seq_lens [B] int32.
+ *     out [B,T,H,d_v] fp32 (always fp32: the refinement makes outputs
+ *     heavy-tailed, and a 16-bit output rounding alone would exceed the
+ *     accuracy this library is checked to); final_state [B,H,d_v,d_k] fp32;
+ *     seq_lens [B] int32.
+ *   - dtype PRISM_BF16 runs the tensor-core path (tcgen05 prepare kernel,
+ *     fp16/fp32 split-precision products); PRISM_F32 runs an fp32 path for
+ *     small head dims (d <= 64).
  */
 #ifndef PRISM_H
 #define PRISM_H
@@ -55,11 +61,11 @@ typedef enum { PRISM_F32 = 0, PRISM_BF16 = 1 } prism_dtype;
 typedef struct {
     int B, T, H;          /* batch, sequence length, heads */
     int d_k, d_v;         /* key / value head dims (supported: d_k == d_v in {16,32,64,128};
-                             fp32 also needs the working set to fit in shared memory) */
+                             PRISM_F32: d <= 64) */
     int conv_width;       /* w, ShortConv taps, 1..8 */
     int L;                /* refinement steps, 0..8 */
     int chunk;            /* scan chunk length C in {16, 32, 64} */
-    prism_dtype dtype;    /* I/O type of q, k, v, out (and of the write factors) */
+    prism_dtype dtype;    /* I/O type of q and k and v */
     unsigned flags;       /* PRISM_FLAG_* */
 } prism_dims;
 
@@ -67,19 +73,39 @@ enum {
     PRISM_OK = 0,
     PRISM_ERR_INVALID_ARG = 1,   /* null required pointer, non-positive size, bad dtype */
     PRISM_ERR_UNSUPPORTED = 2,   /* dims outside the supported set */
-    PRISM_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned */
+    PRISM_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned (workspace: 256) */
     PRISM_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than prism_workspace_bytes() */
     PRISM_ERR_LAUNCH = 5,        /* a kernel launch failed (cudaGetLastError) */
     PRISM_ERR_CUDA = 6           /* another CUDA runtime call failed */
 };
 
-/* Bytes of device workspace prism_forward needs for these dims (0 if the dims
- * are invalid).  The workspace holds the per-token write factors k^(l) and
- * beta^(l) delta^(l) between the two kernels. */
+/* Workspace regions (see prism_workspace_layout). */
+enum {
+    PRISM_WS_STATUS = 0,   /* int32[2]: device status word (nonzero = a bounded wait gave up), flag */
+    PRISM_WS_KL = 1,       /* PRISM_F32: k^(l)              [B,T,H,L,d_k] fp32 */
+    PRISM_WS_DL = 2,       /* PRISM_F32: beta^(l) delta^(l) [B,T,H,L,d_v] fp32 */
+    PRISM_WS_WBLOCKS = 3,  /* PRISM_BF16: fp16 hi/lo weight blocks */
+    PRISM_WS_W = 4,        /* PRISM_BF16, per chunk [B,H,NC,C,d]: W = T diag(beta gamma) K   fp16 */
+    PRISM_WS_KT = 5,       /*   Kt = diag(gamma_C/gamma) K                                   fp16 */
+    PRISM_WS_QTH = 6,      /*   Qt = diag(gamma) Q - P W, hi half                            fp16 */
+    PRISM_WS_QTL = 7,      /*   Qt lo half                                                   fp16 */
+    PRISM_WS_U = 8,        /*   U = T diag(beta)(V - R)                                      fp32 */
+    PRISM_WS_OI = 9,       /*   O_intra = P U + O_l                                          fp32 */
+    PRISM_WS_N = 10,       /*   N = sum_l D_l^T diag(gamma_C/gamma) K_l, [B,H,NC,d,d]         fp32 */
+    PRISM_WS_GC = 11,      /*   gamma_C, [B,H,NC]                                            fp32 */
+    PRISM_WS_COUNT = 12
+};
+
+/* Bytes of device workspace for these dims (0 if the dims are invalid). */
 PRISM_API size_t prism_workspace_bytes(const prism_dims* dims);
 
+/* Byte offset of each PRISM_WS_* region inside the workspace (SIZE_MAX when the
+ * region is absent for these dims).  offsets must hold n >= PRISM_WS_COUNT
+ * entries.  Returns PRISM_OK or an error code. */
+PRISM_API int prism_workspace_layout(const prism_dims* dims, size_t* offsets, int n);
+
 /* The full mixer forward pass (anchor, refinement, write, chunkwise scan,
- * readout) over B sequences.
+ * readout) over B sequences = prism_prepare followed by prism_scan.
  *   seq_lens    NULL: every sequence has length T.  Otherwise tokens
  *               t >= seq_lens[b] are padding: out is 0 there, they do not
  *               touch the state, and their input values are never used
@@ -89,28 +115,30 @@ PRISM_API size_t prism_workspace_bytes(const prism_dims* dims);
  *               256-byte aligned; its contents are scratch.
  * Returns PRISM_OK after enqueueing, or an error code (nothing launched). */
 PRISM_API int prism_forward(const prism_dims* dims,
-                  const void* q, const void* k, const void* v,
-                  const float* log_alpha, const float* beta,
-                  const float* conv_w, const float* Wk, const float* Wp, const float* wbeta,
-                  void* out, float* final_state, const int32_t* seq_lens,
-                  void* workspace, size_t workspace_bytes, void* stream);
+                            const void* q, const void* k, const void* v,
+                            const float* log_alpha, const float* beta,
+                            const float* conv_w, const float* Wk, const float* Wp,
+                            const float* wbeta,
+                            float* out, float* final_state, const int32_t* seq_lens,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
-/* Anchor + refinement only (§2.2 stages 1-2): writes the write factors
- *   Kl [B,T,H,L,d_k] = k^(l)          (normalised directions)
- *   Dl [B,T,H,L,d_v] = beta^(l) delta^(l)
- * in dims->dtype, zeros at padded tokens.  Same conventions as prism_forward. */
-PRISM_API int prism_anchor_refine(const prism_dims* dims, const void* v, const float* conv_w,
-                        const float* Wk, const float* Wp, const float* wbeta,
-                        const int32_t* seq_lens, void* Kl, void* Dl, void* stream);
+/* State-independent stage (fully parallel over chunks): anchor, refinement and,
+ * on the PRISM_BF16 path, each chunk's factored affine state map; results go
+ * to the workspace regions listed above. */
+PRISM_API int prism_prepare(const prism_dims* dims,
+                            const void* q, const void* k, const void* v,
+                            const float* log_alpha, const float* beta,
+                            const float* conv_w, const float* Wk, const float* Wp,
+                            const float* wbeta, const int32_t* seq_lens,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
-/* Chunkwise scan only (§2.1 recurrence + readout), given write factors Kl, Dl
- * laid out as prism_anchor_refine writes them (unused when dims->L == 0).
- * prism_forward is prism_anchor_refine followed by this call.  Same
- * conventions as prism_forward. */
-PRISM_API int prism_chunk_scan(const prism_dims* dims, const void* q, const void* k,
-                               const void* v, const float* log_alpha, const float* beta,
-                               const void* Kl, const void* Dl, void* out, float* final_state,
-                               const int32_t* seq_lens, void* stream);
+/* Serial stage: the chunk-to-chunk state chain and the outputs, from a
+ * workspace filled by prism_prepare with the same dims and inputs. */
+PRISM_API int prism_scan(const prism_dims* dims,
+                         const void* q, const void* k, const void* v,
+                         const float* log_alpha, const float* beta,
+                         const int32_t* seq_lens, void* workspace, size_t workspace_bytes,
+                         float* out, float* final_state, void* stream);
 
 /* Static description of an error code. */
 PRISM_API const char* prism_strerror(int code);

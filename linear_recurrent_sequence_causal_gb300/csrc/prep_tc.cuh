@@ -1,0 +1,701 @@
+// Kernel A (bf16 I/O path): anchor + refinement + the chunk's rank-L write
+// summaries, on tcgen05 tensor cores.  ("Technical Summary: PRISM", §2.2
+// stages 1-2 and the injection B_t = sum_l beta^(l) delta^(l) k^(l)^T.)
+//
+// Everything here is state-independent, so it runs fully parallel: one CTA per
+// (chunk, head, batch).  For the chunk's C tokens it computes the anchor u, the
+// L refinement steps (directions K_l = k^(l), write values D_l = beta^(l) delta^(l))
+// and reduces them at once to what the state scan needs:
+//   R   = sum_l strict_tril(K K_l^T (.) Gamma) D_l      (C x d_v)  value-side correction
+//   O_l = sum_l tril(Q K_l^T (.) Gamma) D_l             (C x d_v)  intra-chunk output
+//   N_l = sum_l D_l^T diag(gamma_C / gamma) K_l          (d_v x d_k) state injection
+// with Gamma_ts = exp(g_t - g_s), g the in-chunk cumulative sum of log alpha.
+// The per-token factors never leave the SM.  The kernel then also does the
+// state-independent part of the gated delta rule for the chunk (strictly lower
+// A = beta (K K^T (.) Gamma), T = (I + A)^-1, P = tril(Q K^T (.) Gamma)) and
+// writes the chunk's affine state map in factored form for the scan kernel:
+//   E = U - W S0^T,  O = O_intra + Qt S0^T,  S1 = gamma_C S0 + E^T Kt + N
+// with W = T diag(beta gamma) K, U = T diag(beta)(V - R), Kt = diag(gamma_C/gamma) K,
+// Qt = diag(gamma) Q - P W, O_intra = P U + O_l, N = N_l.
+//
+// Precision: tensor-core operands are fp16 (q, k, v arrive as bf16 and convert
+// exactly).  Values that carry large magnitudes are split x = hi + lo into two
+// fp16 halves and multiplied in 2-3 passes (hi*hi + hi*lo + lo*hi), which keeps
+// ~fp32 accuracy: the anchor u in the projections, k^(l), D_l, the scaled
+// D_l, and the output-side scores Q K_l^T.  Accumulation is fp32 in TMEM.
+//
+// Operand orientation (all MMAs are M = 128, fp32 accumulators in TMEM):
+//   projections  [k_hat ; p]^T = W u^T : A = W (features x d_v),  B = U (tokens x d_v)
+//   scores       [G ; P]  = [K ; Q] K_l^T : A = [K ; Q] rows,   B = K_l (MN-major)
+//   corrections  [R ; O_l] += [G ; P] D_l : A = [G ; P],          B = D_l^T rows
+//   injection    N_l += Dt_l^T K_l         : A = Dt_l^T rows,     B = K_l rows
+// so each epilogue thread owns one TMEM lane (a feature or a token row).
+#pragma once
+
+#include "chunk_scan.cuh"
+#include "prism_common.cuh"
+#include "tc_common.cuh"
+
+namespace prism {
+
+struct PrepArgs {
+  int B, T, H, w, L;
+  unsigned flags;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const float* log_alpha;
+  const float* beta;
+  const float* conv_w;
+  const float* wbeta;
+  const unsigned char* wblocks;   // fp16 weight blocks laid out for the A operand
+  const int* wflag;               // nonzero: weights need their lo halves
+  const int* seq_lens;
+  // per-chunk outputs, chunk-major [B][H][NC][...]
+  __half* Wc;                     // [C][D]  W = T diag(beta gamma) K
+  __half* Kt;                     // [C][D]  Kt = diag(gamma_C / gamma) K
+  __half* Qth;                    // [C][D]  Qt = diag(gamma) Q - P W, hi half
+  __half* Qtl;                    // [C][D]  lo half
+  float* U;                       // [C][D]  U = T diag(beta) (V - R)
+  float* Oi;                      // [C][D]  O_intra = P U + O_l
+  float* Nl;                      // [D][D]  N = U^T Kt + N_l
+  float* gC;                      // [1]     gamma_C
+  int* status;                    // device error word (bounded waits)
+};
+
+// One weight block: 128 rows (features, zero beyond D) x D columns, fp16,
+// K-major with SBO = 128 and LBO = 2048:  (row, c) at (c/8)*2048 + row*16 + (c%8)*2.
+template <int D>
+struct WeightBlock {
+  static constexpr uint32_t bytes = 128u * D * 2u;
+  // block index of (h, l, which = 0 W_k / 1 W_p, part = 0 hi / 1 lo)
+  static __host__ __device__ size_t index(int h, int l, int L, int which, int part) {
+    return (((size_t)h * L + l) * 2 + which) * 2 + part;
+  }
+};
+
+// Converts W_k, W_p (fp32 [H][L][D][D]) into fp16 hi/lo blocks; sets *flag if
+// any lo half is significant (|lo| > 2^-22 of its row norm), in which case the
+// projections take a third pass with the lo halves.
+template <int D>
+__global__ void prep_weights_kernel(const float* Wk, const float* Wp, int H, int L,
+                                    unsigned char* blocks, int* flag) {
+  const int blk = blockIdx.x;              // (h*L + l)*2 + which
+  const int which = blk & 1, hl = blk >> 1;
+  const float* W = (which == 0 ? Wk : Wp) + (size_t)hl * D * D;
+  unsigned char* hi = blocks + (size_t)(blk * 2 + 0) * WeightBlock<D>::bytes;
+  unsigned char* lo = blocks + (size_t)(blk * 2 + 1) * WeightBlock<D>::bytes;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  bool need = false;
+  for (int row = warp; row < 128; row += nwarp) {
+    float n2 = 0.f;
+    if (row < D)
+      for (int c = lane; c < D; c += 32) { const float x = W[(size_t)row * D + c]; n2 = fmaf(x, x, n2); }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+    const float tol = sqrtf(n2) * 0x1p-22f;
+    for (int c = lane; c < D; c += 32) {
+      const float x = row < D ? W[(size_t)row * D + c] : 0.f;
+      __half h, l;
+      tc::split_f16(x, h, l);
+      const uint32_t off = (c / 8) * 2048u + row * 16u + (c % 8) * 2u;
+      *reinterpret_cast<__half*>(hi + off) = h;
+      *reinterpret_cast<__half*>(lo + off) = l;
+      need |= fabsf(__half2float(l)) > tol;
+    }
+  }
+  if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(flag, 1);
+}
+
+// First-fit placement helper for the tail buffers: region 1 is [r1, r1_end),
+// region 2 starts at r2 and may grow past the refinement loop's footprint.
+struct Place {
+  uint32_t o1, e1, o2;
+  constexpr Place at(uint32_t size) const {
+    return (((o1 + 127) / 128) * 128 + size <= e1)
+               ? Place{((o1 + 127) / 128) * 128 + size, e1, o2}
+               : Place{o1, e1, ((o2 + 127) / 128) * 128 + size};
+  }
+  constexpr uint32_t where(uint32_t size) const {
+    return (((o1 + 127) / 128) * 128 + size <= e1) ? ((o1 + 127) / 128) * 128 : ((o2 + 127) / 128) * 128;
+  }
+};
+
+template <int D, int C>
+struct PrepSmem {
+  static constexpr int NTH = C / 2;                      // tokens per column half
+  static constexpr uint32_t kW = WeightBlock<D>::bytes;  // 128 x D
+  static constexpr uint32_t kU = C * D * 2;              // tokens x D
+  static constexpr uint32_t kKQ = 128 * D * 2;           // 128 rows x D
+  static constexpr uint32_t kF = D * C * 2;              // features x tokens
+  static constexpr uint32_t kF128 = 128 * C * 2;         // 128 rows x tokens
+  static constexpr bool kWpInGP = kW <= 2 * kF128;       // W_p staged in the [G;P] buffers
+  // small arrays first
+  static constexpr uint32_t oG = 0;                      // f32 g[C]
+  static constexpr uint32_t oDec = oG + 4 * C;           // f32 gamma_C/gamma [C]
+  static constexpr uint32_t oBeta = oDec + 4 * C;        // f32 beta^(l) [C]
+  static constexpr uint32_t oNorm = oBeta + 4 * C;       // f32 [4][C]
+  static constexpr uint32_t oBar = oNorm + 16 * C;       // 2 mbarriers
+  static constexpr uint32_t oSlot = oBar + 16;
+  static constexpr uint32_t oTiles = ((oSlot + 16 + 127) / 128) * 128;
+  // refinement-loop tiles
+  static constexpr uint32_t oW = oTiles;
+  static constexpr uint32_t oGP = oW + kW;               // hi, lo (2 * kF128)
+  static constexpr uint32_t oWp = kWpInGP ? oGP : oGP + 2 * kF128;
+  static constexpr uint32_t oU = oGP + 2 * kF128 + (kWpInGP ? 0 : kW);   // hi, lo
+  static constexpr uint32_t oKQ = oU + 2 * kU;
+  static constexpr uint32_t oKl = oKQ + kKQ;             // hi, lo
+  static constexpr uint32_t oD = oKl + 2 * kF;           // hi, lo
+  static constexpr uint32_t oDt = oD + 2 * kF;           // hi, lo (128 rows)
+  static constexpr uint32_t loop_end = oDt + 2 * kF128;
+  // tail buffers (after the loop), placed around the [K;Q] tile which stays live
+  static constexpr uint32_t sKX = 4 * C * D, sSq = 4 * C * (C + 1), sY = 1024 * (C / 16), sB = 8 * C;
+  static constexpr Place p0{oW, oKQ, oKl};
+  static constexpr uint32_t tKX = p0.where(sKX);         // f16 [Kb | X] MN-major, C x 2D
+  static constexpr Place p1 = p0.at(sKX);
+  static constexpr uint32_t tTP = p1.where(kF128);       // f16 [T ; PT] 128 x C
+  static constexpr Place p2 = p1.at(kF128);
+  static constexpr uint32_t tA = p2.where(sSq);          // f32 [C][C+1]
+  static constexpr Place p3 = p2.at(sSq);
+  static constexpr uint32_t tP = p3.where(sSq);          // f32 [C][C+1]
+  static constexpr Place p4 = p3.at(sSq);
+  static constexpr uint32_t tT = p4.where(sSq);          // f32 [C][C+1]
+  static constexpr Place p5 = p4.at(sSq);
+  static constexpr uint32_t tY = p5.where(sY);           // f32 solve scratch
+  static constexpr Place p6 = p5.at(sY);
+  static constexpr uint32_t tB = p6.where(sB);           // f32 beta[C], gamma[C]
+  static constexpr Place p7 = p6.at(sB);
+  static constexpr uint32_t bytes = p7.o2 > loop_end ? p7.o2 : loop_end;
+  static constexpr bool kExtraX = D > 2 * C;             // U/PU need their own TMEM columns
+  static constexpr uint32_t tmem_cols_needed = 2 * C + 2 * D + (kExtraX ? D : 0);
+  static constexpr uint32_t tmem_cols =
+      tmem_cols_needed <= 32 ? 32 : tmem_cols_needed <= 64 ? 64 : tmem_cols_needed <= 128 ? 128
+                                  : tmem_cols_needed <= 256 ? 256 : 512;
+};
+
+template <int D, int C>
+__global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
+  using S = PrepSmem<D, C>;
+  constexpr int NTH = S::NTH;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  unsigned char* sW = sm + S::oW;
+  unsigned char* sWp = sm + S::oWp;
+  unsigned char* sGP = sm + S::oGP;
+  unsigned char* sU = sm + S::oU;
+  unsigned char* sKQ = sm + S::oKQ;
+  unsigned char* sKl = sm + S::oKl;
+  unsigned char* sD = sm + S::oD;
+  unsigned char* sDt = sm + S::oDt;
+  float* sg = reinterpret_cast<float*>(sm + S::oG);
+  float* sdec = reinterpret_cast<float*>(sm + S::oDec);
+  float* sbl = reinterpret_cast<float*>(sm + S::oBeta);
+  float* snorm = reinterpret_cast<float*>(sm + S::oNorm);
+  uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + S::oBar);
+  uint64_t* bar_ld = bar_mma + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::oSlot);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row = quarter * 32 + lane;         // this thread's TMEM lane
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int H = p.H, T_ = p.T, L = p.L, w = p.w;
+  const int NC = (T_ + C - 1) / C;
+  const int len = p.seq_lens ? min(max(p.seq_lens[b], 0), T_) : T_;
+  const int t0 = chunk * C;
+  const int nv = min(C, len - t0);
+  if (nv <= 0) return;                         // chunk entirely padding: never read
+  const bool need_lo = *p.wflag != 0;
+
+  // ---- setup: barriers, TMEM, gates, [K;Q] rows, zero padding rows ----
+  if (tid == 0) {
+    tc::bar_init(bar_mma, 1);
+    tc::bar_init(bar_ld, 1);
+    tc::bar_fence_init();
+  }
+  if (warp == 0) tc::alloc(tslot, S::tmem_cols);
+  if (warp == 1) {
+    // inclusive scan of log alpha over the chunk
+    float run = 0.f;
+    for (int base = 0; base < C; base += 32) {
+      const int i = base + lane;
+      float x = 0.f;
+      if (i < nv) x = p.log_alpha[((size_t)b * T_ + t0 + i) * H + h];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      x += run;
+      run = __shfl_sync(0xffffffffu, x, 31);
+      if (i < C) sg[i] = x;
+    }
+    __syncwarp();
+    for (int i = lane; i < C; i += 32) sdec[i] = expf(sg[C - 1] - sg[i]);
+  }
+  // [K ; Q] rows as fp16: (row, a) at (a/8)*2048 + row*16 + (a%8)*2
+  for (int idx = tid; idx < 128 * (D / 8); idx += 256) {
+    const int r = idx % 128, a8 = idx / 128;
+    uint4 outv = make_uint4(0u, 0u, 0u, 0u);
+    const int t = r < C ? r : r - C;
+    if (r < 2 * C && t < nv) {
+      const __nv_bfloat16* src = (r < C ? p.k : p.q) + (((size_t)b * T_ + t0 + t) * H + h) * D + a8 * 8;
+      const uint4 raw = *reinterpret_cast<const uint4*>(src);
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
+      __half hv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) hv[j] = __float2half_rn(__bfloat162float(e[j]));
+      outv = *reinterpret_cast<const uint4*>(hv);
+    }
+    *reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u) = outv;
+  }
+  // rows D..127 of the scaled-write tiles stay zero (A operand of the injection)
+  if constexpr (D < 128)
+  for (int idx = tid; idx < (128 - D) * (C / 8) * 2; idx += 256) {
+    const int part = idx / ((128 - D) * (C / 8));
+    const int rem = idx % ((128 - D) * (C / 8));
+    const int r = D + rem % (128 - D), s8 = rem / (128 - D);
+    *reinterpret_cast<uint4*>(sDt + part * S::kF128 + s8 * 2048u + r * 16u) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+
+  // ---- anchor u = sum_j c_j (.) v_{t-j}; residual r = v - u kept in registers ----
+  // thread (feature c = row, token half) owns tokens [half*NTH, half*NTH + NTH)
+  const int c = row;
+  const bool cvalid = c < D;
+  float r_reg[NTH];
+  {
+    const __nv_bfloat16* vb = p.v + ((size_t)b * T_ * H + h) * D + c;
+#pragma unroll
+    for (int j8 = 0; j8 < NTH; j8 += 8) {
+      __half uh[8], ul[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int tl = half * NTH + j8 + jj;
+        const int t = t0 + tl;
+        float u = 0.f, vt = 0.f;
+        if (cvalid) {
+          for (int j = 1; j <= w; ++j) {
+            const int ts = t - j;
+            if (ts >= 0 && ts < len)
+              u = fmaf(p.conv_w[((size_t)h * w + (j - 1)) * D + c], __bfloat162float(vb[(size_t)ts * H * D]), u);
+          }
+          if (t < len) vt = __bfloat162float(vb[(size_t)t * H * D]);
+        }
+        r_reg[j8 + jj] = (tl < nv) ? vt - u : 0.f;
+        tc::split_f16(u, uh[jj], ul[jj]);
+        if (cvalid) {
+          // U tile (B operand, N = tokens, K = features): (t, c) at (c/8)*(C*16) + t*16 + (c%8)*2
+          const uint32_t off = (c / 8) * (C * 16u) + tl * 16u + (c % 8) * 2u;
+          *reinterpret_cast<__half*>(sU + off) = uh[jj];
+          *reinterpret_cast<__half*>(sU + S::kU + off) = ul[jj];
+        }
+      }
+    }
+  }
+  tc::fence_smem_to_async();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t t_proj = tmem, t_p = tmem + C, t_ro = tmem + 2 * C, t_n = tmem + 2 * C + D;
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+
+  uint32_t ph_mma = 0, ph_ld = 0;
+  bool ok = true;
+  auto wait_mma = [&]() {
+    ok &= tc::bar_wait(bar_mma, ph_mma & 1);
+    ++ph_mma;
+    tc::fence_after();
+  };
+  auto wait_ld = [&]() {
+    ok &= tc::bar_wait(bar_ld, ph_ld & 1);
+    ++ph_ld;
+  };
+
+  constexpr uint32_t idesc_proj = tc::idesc_f16(C, false, false);
+  constexpr uint32_t idesc_gp = tc::idesc_f16(C, false, true);
+  constexpr uint32_t idesc_dd = tc::idesc_f16(D, false, false);
+  constexpr uint32_t S_s = (D / 8) * 128;      // token step of the feature x token tiles
+  const bool gelu = !(p.flags & 1u);
+
+  for (int l = 0; l < L; ++l) {
+    // [1] stage W_k^(l), W_p^(l) (hi) by bulk copy; compute beta^(l) meanwhile
+    if (l > 0) wait_mma();                      // previous l's MMAs no longer read shared tiles
+    if (tid == 0) {
+      tc::bar_expect_tx(bar_ld, 2 * S::kW);
+      tc::bulk_g2s(sW, p.wblocks + WeightBlock<D>::index(h, l, L, 0, 0) * S::kW, S::kW, bar_ld);
+      tc::bulk_g2s(sWp, p.wblocks + WeightBlock<D>::index(h, l, L, 1, 0) * S::kW, S::kW, bar_ld);
+    }
+    {
+      const float* wb = p.wbeta + ((size_t)h * L + l) * D;
+      for (int t = warp; t < C; t += 8) {
+        float z = 0.f;
+        for (int cc = lane; cc < D; cc += 32) {
+          const uint32_t off = (cc / 8) * (C * 16u) + t * 16u + (cc % 8) * 2u;
+          const float u = __half2float(*reinterpret_cast<const __half*>(sU + off)) +
+                          __half2float(*reinterpret_cast<const __half*>(sU + S::kU + off));
+          z = fmaf(wb[cc], u, z);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (lane == 0) sbl[t] = sigmoidf(z);
+      }
+    }
+    wait_ld();
+    __syncthreads();
+    // [2] projections: k_hat^T = W_k u^T, p^T = W_p u^T (u = hi + lo)
+    if (tid == 0) {
+      tc::fence_after();
+      for (int pass = 0; pass < 2; ++pass)
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t bdesc = tc::desc(sU + pass * S::kU + kk * 2 * C * 16, C * 16, 128);
+          const bool acc = pass > 0 || kk > 0;
+          tc::mma(t_proj, tc::desc(sW + kk * 4096, 2048, 128), bdesc, idesc_proj, acc);
+          tc::mma(t_p, tc::desc(sWp + kk * 4096, 2048, 128), bdesc, idesc_proj, acc);
+        }
+      tc::commit(bar_mma);
+    }
+    if (need_lo) {       // weights not exact in fp16: add W_lo u_hi
+      wait_mma();
+      if (tid == 0) {
+        tc::bar_expect_tx(bar_ld, 2 * S::kW);
+        tc::bulk_g2s(sW, p.wblocks + WeightBlock<D>::index(h, l, L, 0, 1) * S::kW, S::kW, bar_ld);
+        tc::bulk_g2s(sWp, p.wblocks + WeightBlock<D>::index(h, l, L, 1, 1) * S::kW, S::kW, bar_ld);
+      }
+      wait_ld();
+      if (tid == 0) {
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t bdesc = tc::desc(sU + kk * 2 * C * 16, C * 16, 128);
+          tc::mma(t_proj, tc::desc(sW + kk * 4096, 2048, 128), bdesc, idesc_proj, true);
+          tc::mma(t_p, tc::desc(sWp + kk * 4096, 2048, 128), bdesc, idesc_proj, true);
+        }
+        tc::commit(bar_mma);
+      }
+    }
+    wait_mma();
+    // [3] epilogue: normalise directions, residual step, write factor tiles
+    {
+      float kv[NTH];
+#pragma unroll
+      for (int j = 0; j < NTH; j += 8) {
+        float tmp[8];
+        tc::ld8(t_proj + lane_base + half * NTH + j, tmp);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) kv[j + jj] = cvalid ? tmp[jj] : 0.f;
+      }
+      // per-token sum of squares over this warp's 32 features (reduce-scatter)
+      float red[NTH];
+#pragma unroll
+      for (int j = 0; j < NTH; ++j) red[j] = kv[j] * kv[j];
+      int n = NTH;
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) {
+        if (n > 1) {
+          const int hn = n / 2;
+          const bool upper = lane & m;
+#pragma unroll
+          for (int j = 0; j < NTH / 2; ++j) {
+            if (j < hn) {
+              const float send = upper ? red[j] : red[j + hn];
+              const float keep = upper ? red[j + hn] : red[j];
+              red[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            }
+          }
+          n = hn;
+        } else {
+          red[0] += __shfl_xor_sync(0xffffffffu, red[0], m);
+        }
+      }
+      constexpr int kShift = NTH == 32 ? 0 : NTH == 16 ? 1 : NTH == 8 ? 2 : 3;
+      if ((lane & ((1 << kShift) - 1)) == 0) snorm[quarter * C + half * NTH + (lane >> kShift)] = red[0];
+      __syncthreads();
+      float pv[NTH];
+#pragma unroll
+      for (int j = 0; j < NTH; j += 8) {
+        float tmp[8];
+        tc::ld8(t_p + lane_base + half * NTH + j, tmp);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) pv[j + jj] = tmp[jj];
+      }
+      if (cvalid) {
+#pragma unroll
+        for (int j8 = 0; j8 < NTH; j8 += 8) {
+          __half kh[8], kl[8], dh[8], dlo[8], th[8], tl[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            const int j = j8 + jj, t = half * NTH + j;
+            const bool valid = t < nv;
+            float ss = 0.f;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) ss += snorm[qq * C + t];
+            const float kd = valid ? kv[j] / sqrtf(ss + 1e-6f) : 0.f;
+            const float x = pv[j] * r_reg[j];
+            const float dl = gelu ? gelu_erf(x) : x;
+            r_reg[j] -= dl;
+            const float dval = valid ? sbl[t] * dl : 0.f;
+            tc::split_f16(kd, kh[jj], kl[jj]);
+            tc::split_f16(dval, dh[jj], dlo[jj]);
+            tc::split_f16(dval * sdec[t], th[jj], tl[jj]);
+          }
+          // feature x token tiles: (f, s) at (s/8)*S_s + f*16 + (s%8)*2  (f < D)
+          const uint32_t off = ((half * NTH + j8) / 8) * S_s + c * 16u;
+          *reinterpret_cast<uint4*>(sKl + off) = *reinterpret_cast<const uint4*>(kh);
+          *reinterpret_cast<uint4*>(sKl + S::kF + off) = *reinterpret_cast<const uint4*>(kl);
+          *reinterpret_cast<uint4*>(sD + off) = *reinterpret_cast<const uint4*>(dh);
+          *reinterpret_cast<uint4*>(sD + S::kF + off) = *reinterpret_cast<const uint4*>(dlo);
+          const uint32_t off128 = ((half * NTH + j8) / 8) * 2048u + c * 16u;
+          *reinterpret_cast<uint4*>(sDt + off128) = *reinterpret_cast<const uint4*>(th);
+          *reinterpret_cast<uint4*>(sDt + S::kF128 + off128) = *reinterpret_cast<const uint4*>(tl);
+        }
+      }
+    }
+    tc::fence_smem_to_async();
+    tc::fence_before();
+    __syncthreads();
+    // [4] scores [G ; P] = [K ; Q] K_l^T   (K_l = hi + lo, MN-major B)
+    if (tid == 0) {
+      tc::fence_after();
+      for (int pass = 0; pass < 2; ++pass)
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma(t_proj, tc::desc(sKQ + kk * 4096, 2048, 128),
+                  tc::desc(sKl + pass * S::kF + kk * 256, 128, S_s), idesc_gp, pass > 0 || kk > 0);
+      tc::commit(bar_mma);
+    }
+    wait_mma();
+    // [5] epilogue: decay + causal masks; rows < C are G (strict), C..2C-1 are P (inclusive)
+    {
+      const bool isG = row < C, isP = row >= C && row < 2 * C;
+      const int t = isG ? row : row - C;
+      const float gt = (isG || isP) ? sg[t] : 0.f;
+#pragma unroll
+      for (int j8 = 0; j8 < NTH; j8 += 8) {
+        float tmp[8];
+        tc::ld8(t_proj + lane_base + half * NTH + j8, tmp);
+        __half hh[8], ll[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int s = half * NTH + j8 + jj;
+          float val = 0.f;
+          if ((isG && t > s) || (isP && t >= s)) val = expf(gt - sg[s]) * tmp[jj];
+          if (isP) {
+            tc::split_f16(val, hh[jj], ll[jj]);
+          } else {
+            hh[jj] = __float2half_rn(val);
+            ll[jj] = __float2half_rn(0.f);
+          }
+        }
+        const uint32_t off = ((half * NTH + j8) / 8) * 2048u + row * 16u;
+        *reinterpret_cast<uint4*>(sGP + off) = *reinterpret_cast<const uint4*>(hh);
+        *reinterpret_cast<uint4*>(sGP + S::kF128 + off) = *reinterpret_cast<const uint4*>(ll);
+      }
+    }
+    tc::fence_smem_to_async();
+    tc::fence_before();
+    __syncthreads();
+    // [6] [R ; O_l] += [G ; P] D_l  and  N_l += Dt_l^T K_l   (3 passes each)
+    if (tid == 0) {
+      tc::fence_after();
+      const int ap[3] = {0, 0, 1}, bp[3] = {0, 1, 0};
+      for (int ps = 0; ps < 3; ++ps)
+        for (int kk = 0; kk < C / 16; ++kk) {
+          const bool acc = l > 0 || ps > 0 || kk > 0;
+          tc::mma(t_ro, tc::desc(sGP + ap[ps] * S::kF128 + kk * 4096, 2048, 128),
+                  tc::desc(sD + bp[ps] * S::kF + kk * 2 * S_s, S_s, 128), idesc_dd, acc);
+          tc::mma(t_n, tc::desc(sDt + ap[ps] * S::kF128 + kk * 4096, 2048, 128),
+                  tc::desc(sKl + bp[ps] * S::kF + kk * 2 * S_s, S_s, 128), idesc_dd, acc);
+        }
+      tc::commit(bar_mma);
+    }
+  }
+  if (L > 0) wait_mma();
+
+  // ================= tail: gated delta rule, state-independent part =================
+  const size_t cbase = ((size_t)b * H + h) * NC + chunk;
+  float* tAf = reinterpret_cast<float*>(sm + S::tA);
+  float* tPf = reinterpret_cast<float*>(sm + S::tP);
+  float* tTf = reinterpret_cast<float*>(sm + S::tT);
+  float* tYf = reinterpret_cast<float*>(sm + S::tY);
+  float* tbeta = reinterpret_cast<float*>(sm + S::tB);
+  float* tgam = tbeta + C;
+  unsigned char* sTP = sm + S::tTP;
+  unsigned char* sKX = sm + S::tKX;
+  const uint32_t t_w = t_n;                                     // W / PW columns
+  const uint32_t t_x = S::kExtraX ? tmem + 2 * C + 2 * D : tmem; // U / PU columns
+  // (a) N = N_l to global (its TMEM columns are reused below)
+  if (L > 0) {
+    float* ndst = p.Nl + (cbase * D + row) * D;
+#pragma unroll
+    for (int j8 = 0; j8 < D / 2; j8 += 8) {
+      float tmp[8];
+      tc::ld8(t_n + lane_base + half * (D / 2) + j8, tmp);
+      if (cvalid) {
+        float4* d4 = reinterpret_cast<float4*>(ndst + half * (D / 2) + j8);
+        d4[0] = make_float4(tmp[0], tmp[1], tmp[2], tmp[3]);
+        d4[1] = make_float4(tmp[4], tmp[5], tmp[6], tmp[7]);
+      }
+    }
+  }
+  for (int i = tid; i < C; i += 256) {
+    tbeta[i] = i < nv ? p.beta[((size_t)b * T_ + t0 + i) * H + h] : 0.f;
+    tgam[i] = expf(sg[i]);
+  }
+  tc::fence_before();
+  __syncthreads();
+  // (b) [K K^T ; Q K^T] = [K ; Q] K^T   (B = the K rows of the same tile, K-major)
+  if (tid == 0) {
+    tc::fence_after();
+    for (int kk = 0; kk < D / 16; ++kk)
+      tc::mma(t_proj, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKQ + kk * 4096, 2048, 128),
+              idesc_proj, kk > 0);
+    tc::commit(bar_mma);
+  }
+  wait_mma();
+  // (c) A = strict_tril(beta (K K^T) (.) Gamma), P = tril(Q K^T (.) Gamma)   (fp32)
+  {
+    const bool isA = row < C, isP = row >= C && row < 2 * C;
+    const int t = isA ? row : row - C;
+#pragma unroll
+    for (int j8 = 0; j8 < NTH; j8 += 8) {
+      float tmp[8];
+      tc::ld8(t_proj + lane_base + half * NTH + j8, tmp);
+      if (isA || isP) {
+        const float gt = sg[t];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int s_ = half * NTH + j8 + jj;
+          if (isA) tAf[t * (C + 1) + s_] = (t > s_) ? tbeta[t] * expf(gt - sg[s_]) * tmp[jj] : 0.f;
+          else     tPf[t * (C + 1) + s_] = (t >= s_) ? expf(gt - sg[s_]) * tmp[jj] : 0.f;
+        }
+      }
+    }
+  }
+  // (d) X = beta (V - R) and Kb = beta gamma K as the MN-major B tile [Kb | X]:
+  //     (s, f) at (f/8)*(16C) + s*16 + (f%8)*2,  f < D: Kb,  f >= D: X
+  {
+    const int s_ = row;                                        // token (lanes 0..C-1)
+    const bool tok = s_ < C;
+    const float bs = tok ? tbeta[s_] : 0.f, gs = tok ? tgam[s_] : 0.f;
+    const __nv_bfloat16* vrow = p.v + (((size_t)b * T_ + t0 + (tok ? s_ : 0)) * H + h) * D;
+#pragma unroll
+    for (int j8 = 0; j8 < D / 2; j8 += 8) {
+      const int f0 = half * (D / 2) + j8;
+      float rr[8];
+      if (L > 0) {
+        tc::ld8(t_ro + lane_base + f0, rr);
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) rr[jj] = 0.f;
+      }
+      if (tok) {
+        __half xh[8], kh[8];
+        const bool valid = s_ < nv;
+        uint4 vraw = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) vraw = *reinterpret_cast<const uint4*>(vrow + f0);
+        const __nv_bfloat16* ve = reinterpret_cast<const __nv_bfloat16*>(&vraw);
+        const uint4 kraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + s_ * 16u);
+        const __half* ke = reinterpret_cast<const __half*>(&kraw);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          xh[jj] = __float2half_rn(valid ? bs * (__bfloat162float(ve[jj]) - rr[jj]) : 0.f);
+          kh[jj] = __float2half_rn(bs * gs * __half2float(ke[jj]));
+        }
+        *reinterpret_cast<uint4*>(sKX + ((D + f0) / 8) * (16u * C) + s_ * 16u) = *reinterpret_cast<const uint4*>(xh);
+        *reinterpret_cast<uint4*>(sKX + (f0 / 8) * (16u * C) + s_ * 16u) = *reinterpret_cast<const uint4*>(kh);
+      }
+    }
+  }
+  __syncthreads();
+  // (e) T = (I + A)^-1 (fp32), then PT = P T
+  solve_unit_lower<C>(tAf, tTf, tYf);
+  for (int idx = tid; idx < C * C; idx += 256) {
+    const int t = idx / C, j = idx % C;
+    float acc = 0.f;
+    for (int m = j; m <= t; ++m) acc = fmaf(tPf[t * (C + 1) + m], tTf[m * (C + 1) + j], acc);
+    tAf[t * (C + 1) + j] = acc;                                 // PT (A no longer needed)
+  }
+  __syncthreads();
+  // [T ; PT] as fp16 A tile (rows 0..C-1 = T, C..2C-1 = PT, rest 0): (r, s) at (s/8)*2048 + r*16 + (s%8)*2
+  for (int idx = tid; idx < 128 * (C / 8); idx += 256) {
+    const int r = idx % 128, s8 = idx / 128;
+    __half hv[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = s8 * 8 + jj;
+      float x = 0.f;
+      if (r < C) x = tTf[r * (C + 1) + j];
+      else if (r < 2 * C) x = tAf[(r - C) * (C + 1) + j];
+      hv[jj] = __float2half_rn(x);
+    }
+    *reinterpret_cast<uint4*>(sTP + s8 * 2048u + r * 16u) = *reinterpret_cast<const uint4*>(hv);
+  }
+  tc::fence_smem_to_async();
+  tc::fence_before();
+  __syncthreads();
+  // (f) [W ; PW] = [T ; PT] Kb,  [U ; PU] = [T ; PT] X   (B MN-major: LBO = 128, SBO = 16C)
+  if (tid == 0) {
+    tc::fence_after();
+    constexpr uint32_t idesc_tx = tc::idesc_f16(D, false, true);
+    for (int kk = 0; kk < C / 16; ++kk) {
+      const uint64_t adesc = tc::desc(sTP + kk * 4096, 2048, 128);
+      tc::mma(t_w, adesc, tc::desc(sKX + kk * 256, 128, 16 * C), idesc_tx, kk > 0);
+      tc::mma(t_x, adesc, tc::desc(sKX + (D / 8) * (16 * C) + kk * 256, 128, 16 * C), idesc_tx, kk > 0);
+    }
+    tc::commit(bar_mma);
+  }
+  wait_mma();
+  // (g) outputs.  Lanes 0..C-1: W (fp16), U (fp32), Kt (fp16).  Lanes C..2C-1:
+  //     Qt = gamma Q - PW (fp16 hi/lo), O_intra = PU + O_l (fp32).
+  {
+    const bool isT = row < C, isPT = row >= C && row < 2 * C;
+    const int t = isT ? row : row - C;
+    const size_t rbase = (cbase * C + (isT || isPT ? t : 0)) * D;
+    const float gt = (isT || isPT) ? tgam[t] : 0.f;
+    const float dct = (isT || isPT) ? sdec[t] : 0.f;
+#pragma unroll
+    for (int j8 = 0; j8 < D / 2; j8 += 8) {
+      const int f0 = half * (D / 2) + j8;
+      float wv[8], xv[8], ov[8];
+      tc::ld8(t_w + lane_base + f0, wv);
+      tc::ld8(t_x + lane_base + f0, xv);
+      if (L > 0) {
+        tc::ld8(t_ro + lane_base + f0, ov);
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) ov[jj] = 0.f;
+      }
+      if (isT) {
+        __half wh[8], kth[8];
+        const uint4 kraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + t * 16u);
+        const __half* ke = reinterpret_cast<const __half*>(&kraw);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          wh[jj] = __float2half_rn(wv[jj]);
+          kth[jj] = __float2half_rn(dct * __half2float(ke[jj]));
+        }
+        *reinterpret_cast<uint4*>(p.Wc + rbase + f0) = *reinterpret_cast<const uint4*>(wh);
+        *reinterpret_cast<uint4*>(p.Kt + rbase + f0) = *reinterpret_cast<const uint4*>(kth);
+        float4* u4 = reinterpret_cast<float4*>(p.U + rbase + f0);
+        u4[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+        u4[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+      } else if (isPT) {
+        __half qh[8], ql[8];
+        const uint4 qraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + row * 16u);
+        const __half* qe = reinterpret_cast<const __half*>(&qraw);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) tc::split_f16(gt * __half2float(qe[jj]) - wv[jj], qh[jj], ql[jj]);
+        *reinterpret_cast<uint4*>(p.Qth + rbase + f0) = *reinterpret_cast<const uint4*>(qh);
+        *reinterpret_cast<uint4*>(p.Qtl + rbase + f0) = *reinterpret_cast<const uint4*>(ql);
+        float4* o4 = reinterpret_cast<float4*>(p.Oi + rbase + f0);
+        o4[0] = make_float4(xv[0] + ov[0], xv[1] + ov[1], xv[2] + ov[2], xv[3] + ov[3]);
+        o4[1] = make_float4(xv[4] + ov[4], xv[5] + ov[5], xv[6] + ov[6], xv[7] + ov[7]);
+      }
+    }
+    if (tid == 0) p.gC[cbase] = tgam[C - 1];
+  }
+  if (!ok && lane == 0) atomicExch(p.status, 1);
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, S::tmem_cols);
+}
+
+}  // namespace prism

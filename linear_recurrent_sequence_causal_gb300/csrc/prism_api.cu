@@ -5,30 +5,67 @@
 
 #include "../../include/prism.h"
 #include "kernels.h"
+#include "kernels_tc.cuh"
 
 namespace prism {
-cudaError_t launch_k2_bf16_16(int C, const K2Args& a, cudaStream_t s);
-cudaError_t launch_k2_bf16_32(int C, const K2Args& a, cudaStream_t s);
-cudaError_t launch_k2_bf16_64(int C, const K2Args& a, cudaStream_t s);
-cudaError_t launch_k2_bf16_128(int C, const K2Args& a, cudaStream_t s);
 cudaError_t launch_k2_f32_16(int C, const K2Args& a, cudaStream_t s);
 cudaError_t launch_k2_f32_32(int C, const K2Args& a, cudaStream_t s);
 cudaError_t launch_k2_f32_64(int C, const K2Args& a, cudaStream_t s);
+#define PRISM_DECL_TC(D)                                                                        \
+  cudaError_t launch_prep_##D(int C, const PrepArgs& a, cudaStream_t s);                       \
+  cudaError_t launch_weights_##D(const float* Wk, const float* Wp, int H, int L,                \
+                                 unsigned char* blocks, int* flag, cudaStream_t s);             \
+  cudaError_t launch_scan_##D(int C, int BV, const ScanArgs& a, cudaStream_t s);                \
+  size_t prep_smem_##D(int C);
+PRISM_DECL_TC(16)
+PRISM_DECL_TC(32)
+PRISM_DECL_TC(64)
+PRISM_DECL_TC(128)
+#undef PRISM_DECL_TC
 
 cudaError_t launch_k2(int dtype, int D, int C, const K2Args& a, cudaStream_t s) {
-  if (dtype == 1) {
-    switch (D) {
-      case 16: return launch_k2_bf16_16(C, a, s);
-      case 32: return launch_k2_bf16_32(C, a, s);
-      case 64: return launch_k2_bf16_64(C, a, s);
-      case 128: return launch_k2_bf16_128(C, a, s);
-    }
-  } else {
-    switch (D) {
-      case 16: return launch_k2_f32_16(C, a, s);
-      case 32: return launch_k2_f32_32(C, a, s);
-      case 64: return launch_k2_f32_64(C, a, s);
-    }
+  if (dtype != 0) return cudaErrorInvalidValue;
+  switch (D) {
+    case 16: return launch_k2_f32_16(C, a, s);
+    case 32: return launch_k2_f32_32(C, a, s);
+    case 64: return launch_k2_f32_64(C, a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+static size_t prep_smem(int D, int C) {
+  switch (D) {
+    case 16: return prep_smem_16(C);
+    case 32: return prep_smem_32(C);
+    case 64: return prep_smem_64(C);
+    case 128: return prep_smem_128(C);
+  }
+  return 0;
+}
+static cudaError_t launch_prep(int D, int C, const PrepArgs& a, cudaStream_t s) {
+  switch (D) {
+    case 16: return launch_prep_16(C, a, s);
+    case 32: return launch_prep_32(C, a, s);
+    case 64: return launch_prep_64(C, a, s);
+    case 128: return launch_prep_128(C, a, s);
+  }
+  return cudaErrorInvalidValue;
+}
+static cudaError_t launch_weights(int D, const float* Wk, const float* Wp, int H, int L,
+                                  unsigned char* blocks, int* flag, cudaStream_t s) {
+  switch (D) {
+    case 16: return launch_weights_16(Wk, Wp, H, L, blocks, flag, s);
+    case 32: return launch_weights_32(Wk, Wp, H, L, blocks, flag, s);
+    case 64: return launch_weights_64(Wk, Wp, H, L, blocks, flag, s);
+    case 128: return launch_weights_128(Wk, Wp, H, L, blocks, flag, s);
+  }
+  return cudaErrorInvalidValue;
+}
+static cudaError_t launch_scan(int D, int C, int BV, const ScanArgs& a, cudaStream_t s) {
+  switch (D) {
+    case 16: return launch_scan_16(C, BV, a, s);
+    case 32: return launch_scan_32(C, BV, a, s);
+    case 64: return launch_scan_64(C, BV, a, s);
+    case 128: return launch_scan_128(C, BV, a, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -38,10 +75,10 @@ namespace {
 
 constexpr size_t kMaxSmem = 232448;   // 227 KB: opt-in dynamic shared memory per CTA
 constexpr int kMaxL = 8, kMaxW = 8;
+constexpr size_t kAbsent = ~size_t(0);
 
-size_t elem_size(prism_dtype t) { return t == PRISM_BF16 ? 2 : 4; }
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Shape checks shared by every entry point.
 int check_dims(const prism_dims* d) {
@@ -50,38 +87,108 @@ int check_dims(const prism_dims* d) {
   if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->d_k <= 0 || d->d_v <= 0 || d->L < 0 ||
       d->conv_width <= 0 || d->chunk <= 0)
     return PRISM_ERR_INVALID_ARG;
-  if (d->d_k != d->d_v) return PRISM_ERR_UNSUPPORTED;
-  const int D = d->d_k;
-  if (D != 16 && D != 32 && D != 64 && D != 128) return PRISM_ERR_UNSUPPORTED;
-  if (d->chunk != 16 && d->chunk != 32 && d->chunk != 64) return PRISM_ERR_UNSUPPORTED;
-  if (d->L > kMaxL || d->conv_width > kMaxW) return PRISM_ERR_UNSUPPORTED;
   if (d->flags & ~PRISM_FLAG_NO_GELU) return PRISM_ERR_INVALID_ARG;
-  const int dt = d->dtype == PRISM_BF16 ? 1 : 0;
-  const size_t s1 = prism::k1_smem_bytes(dt, D), s2 = prism::k2_smem_bytes(dt, D, d->chunk);
-  if (s1 == 0 || s2 == 0 || s1 > kMaxSmem || s2 > kMaxSmem) return PRISM_ERR_UNSUPPORTED;
-  // index arithmetic is 64-bit; keep per-dimension products within int range
+  if (d->d_k != d->d_v) return PRISM_ERR_UNSUPPORTED;
+  const int D = d->d_k, C = d->chunk;
+  if (D != 16 && D != 32 && D != 64 && D != 128) return PRISM_ERR_UNSUPPORTED;
+  if (C != 16 && C != 32 && C != 64) return PRISM_ERR_UNSUPPORTED;
+  if (d->L > kMaxL || d->conv_width > kMaxW) return PRISM_ERR_UNSUPPORTED;
+  if (d->dtype == PRISM_F32) {
+    const size_t s1 = prism::k1_smem_bytes(0, D), s2 = prism::k2_smem_bytes(0, D, C);
+    if (s1 == 0 || s2 == 0 || s1 > kMaxSmem || s2 > kMaxSmem) return PRISM_ERR_UNSUPPORTED;
+  } else {
+    const size_t s1 = prism::prep_smem(D, C);
+    if (s1 == 0 || s1 > kMaxSmem) return PRISM_ERR_UNSUPPORTED;
+  }
   if ((long long)d->B * d->T > (1LL << 31) - 1) return PRISM_ERR_UNSUPPORTED;
   return PRISM_OK;
 }
 
-size_t factor_bytes(const prism_dims* d) {
-  return (size_t)d->B * d->T * d->H * d->L * d->d_k * elem_size(d->dtype);
+struct Layout {
+  size_t off[PRISM_WS_COUNT];
+  size_t total;
+};
+
+Layout layout(const prism_dims* d) {
+  Layout Lo;
+  for (auto& o : Lo.off) o = kAbsent;
+  size_t cur = 0;
+  auto take = [&](int region, size_t bytes) {
+    Lo.off[region] = cur;
+    cur += round256(bytes);
+  };
+  const size_t D = d->d_k, C = d->chunk, NC = (d->T + C - 1) / C;
+  take(PRISM_WS_STATUS, 256);
+  if (d->dtype == PRISM_F32) {
+    const size_t f = (size_t)d->B * d->T * d->H * d->L * D * 4;
+    if (d->L > 0) {
+      take(PRISM_WS_KL, f);
+      take(PRISM_WS_DL, f);
+    }
+  } else {
+    const size_t per = (size_t)d->B * d->H * NC * C * D;
+    if (d->L > 0) take(PRISM_WS_WBLOCKS, (size_t)d->H * d->L * 4 * 128 * D * 2);
+    take(PRISM_WS_W, per * 2);
+    take(PRISM_WS_KT, per * 2);
+    take(PRISM_WS_QTH, per * 2);
+    take(PRISM_WS_QTL, per * 2);
+    take(PRISM_WS_U, per * 4);
+    take(PRISM_WS_OI, per * 4);
+    if (d->L > 0) take(PRISM_WS_N, (size_t)d->B * d->H * NC * D * D * 4);
+    take(PRISM_WS_GC, (size_t)d->B * d->H * NC * 4);
+  }
+  Lo.total = cur;
+  return Lo;
+}
+
+int check_inputs(const prism_dims* dims, const void* q, const void* k, const void* v,
+                 const float* log_alpha, const float* beta, const int32_t* seq_lens,
+                 const void* workspace, size_t workspace_bytes) {
+  if (!q || !k || !v || !log_alpha || !beta) return PRISM_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, log_alpha, beta, seq_lens};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return PRISM_ERR_MISALIGNED;
+  if (workspace && !aligned(workspace, 256)) return PRISM_ERR_MISALIGNED;
+  if (!workspace || workspace_bytes < layout(dims).total) return PRISM_ERR_WORKSPACE;
+  return PRISM_OK;
+}
+
+template <class T>
+T* region(void* ws, const Layout& Lo, int r) {
+  return Lo.off[r] == kAbsent ? nullptr
+                              : reinterpret_cast<T*>(static_cast<unsigned char*>(ws) + Lo.off[r]);
+}
+
+// Scan tile height: more, thinner tiles when there are few sequences.
+int pick_bv(const prism_dims* d) {
+  const int D = d->d_k;
+  if (D < 32) return 16;
+  const long long seqs = (long long)d->B * d->H;
+  return seqs * (D / 32) >= 2 * 152 ? 32 : 16;
 }
 
 }  // namespace
 
 extern "C" PRISM_API size_t prism_workspace_bytes(const prism_dims* dims) {
   if (check_dims(dims) != PRISM_OK) return 0;
-  // Kl then Dl (d_k == d_v), each 256-byte aligned.
-  return 2 * round256(factor_bytes(dims)) + 256;
+  return layout(dims).total;
+}
+
+extern "C" PRISM_API int prism_workspace_layout(const prism_dims* dims, size_t* offsets, int n) {
+  const int rc = check_dims(dims);
+  if (rc != PRISM_OK) return rc;
+  if (!offsets || n < PRISM_WS_COUNT) return PRISM_ERR_INVALID_ARG;
+  const Layout Lo = layout(dims);
+  for (int i = 0; i < PRISM_WS_COUNT; ++i) offsets[i] = Lo.off[i];
+  return PRISM_OK;
 }
 
 extern "C" PRISM_API const char* prism_strerror(int code) {
   switch (code) {
     case PRISM_OK: return "success";
-    case PRISM_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive size or bad dtype)";
-    case PRISM_ERR_UNSUPPORTED: return "unsupported dims (need d_k == d_v in {16,32,64,128}, chunk in {16,32,64}, L <= 8, conv width <= 8, and a working set that fits in shared memory)";
-    case PRISM_ERR_MISALIGNED: return "a tensor pointer is not 16-byte aligned";
+    case PRISM_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive size, bad dtype or flags)";
+    case PRISM_ERR_UNSUPPORTED: return "unsupported dims (need d_k == d_v in {16,32,64,128} (fp32: <= 64), chunk in {16,32,64}, L <= 8, conv width <= 8)";
+    case PRISM_ERR_MISALIGNED: return "a tensor pointer is not 16-byte aligned (workspace: 256-byte)";
     case PRISM_ERR_WORKSPACE: return "workspace missing or smaller than prism_workspace_bytes()";
     case PRISM_ERR_LAUNCH: return "kernel launch failed";
     case PRISM_ERR_CUDA: return "CUDA runtime call failed";
@@ -89,85 +196,110 @@ extern "C" PRISM_API const char* prism_strerror(int code) {
   return "unknown error code";
 }
 
-static int run_k1(const prism_dims* dims, const void* v, const float* conv_w, const float* Wk,
-                  const float* Wp, const float* wbeta, const int32_t* seq_lens, void* Kl,
-                  void* Dl, cudaStream_t s) {
-  prism::K1Args a;
+extern "C" PRISM_API int prism_prepare(const prism_dims* dims, const void* q, const void* k,
+                                       const void* v, const float* log_alpha, const float* beta,
+                                       const float* conv_w, const float* Wk, const float* Wp,
+                                       const float* wbeta, const int32_t* seq_lens,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != PRISM_OK) return rc;
+  rc = check_inputs(dims, q, k, v, log_alpha, beta, seq_lens, workspace, workspace_bytes);
+  if (rc != PRISM_OK) return rc;
+  if (dims->L > 0 && (!conv_w || !Wk || !Wp || !wbeta)) return PRISM_ERR_INVALID_ARG;
+  const void* wp[] = {conv_w, Wk, Wp, wbeta};
+  for (const void* p : wp)
+    if (p && !aligned(p, 16)) return PRISM_ERR_MISALIGNED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Layout Lo = layout(dims);
+  int* status = region<int>(workspace, Lo, PRISM_WS_STATUS);
+  if (cudaMemsetAsync(status, 0, 8, s) != cudaSuccess) return PRISM_ERR_CUDA;
+  const int D = dims->d_k, C = dims->chunk;
+  if (dims->dtype == PRISM_F32) {
+    if (dims->L == 0) return PRISM_OK;
+    prism::K1Args a;
+    a.B = dims->B; a.T = dims->T; a.H = dims->H; a.w = dims->conv_width; a.L = dims->L;
+    a.flags = dims->flags;
+    a.v = v; a.conv_w = conv_w; a.Wk = Wk; a.Wp = Wp; a.wbeta = wbeta;
+    a.seq_lens = seq_lens;
+    a.Kl = region<float>(workspace, Lo, PRISM_WS_KL);
+    a.Dl = region<float>(workspace, Lo, PRISM_WS_DL);
+    return prism::launch_k1(0, D, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
+  }
+  unsigned char* wblocks = region<unsigned char>(workspace, Lo, PRISM_WS_WBLOCKS);
+  if (dims->L > 0 &&
+      prism::launch_weights(D, Wk, Wp, dims->H, dims->L, wblocks, status + 1, s) != cudaSuccess)
+    return PRISM_ERR_LAUNCH;
+  prism::PrepArgs a;
   a.B = dims->B; a.T = dims->T; a.H = dims->H; a.w = dims->conv_width; a.L = dims->L;
   a.flags = dims->flags;
-  a.v = v; a.conv_w = conv_w; a.Wk = Wk; a.Wp = Wp; a.wbeta = wbeta;
-  a.seq_lens = seq_lens; a.Kl = Kl; a.Dl = Dl;
-  const int dt = dims->dtype == PRISM_BF16 ? 1 : 0;
-  return prism::launch_k1(dt, dims->d_k, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.log_alpha = log_alpha; a.beta = beta; a.conv_w = conv_w; a.wbeta = wbeta;
+  a.wblocks = wblocks; a.wflag = status + 1; a.seq_lens = seq_lens;
+  a.Wc = region<__half>(workspace, Lo, PRISM_WS_W);
+  a.Kt = region<__half>(workspace, Lo, PRISM_WS_KT);
+  a.Qth = region<__half>(workspace, Lo, PRISM_WS_QTH);
+  a.Qtl = region<__half>(workspace, Lo, PRISM_WS_QTL);
+  a.U = region<float>(workspace, Lo, PRISM_WS_U);
+  a.Oi = region<float>(workspace, Lo, PRISM_WS_OI);
+  a.Nl = region<float>(workspace, Lo, PRISM_WS_N);
+  a.gC = region<float>(workspace, Lo, PRISM_WS_GC);
+  a.status = status;
+  return prism::launch_prep(D, C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
 }
 
-extern "C" PRISM_API int prism_anchor_refine(const prism_dims* dims, const void* v, const float* conv_w,
-                                   const float* Wk, const float* Wp, const float* wbeta,
-                                   const int32_t* seq_lens, void* Kl, void* Dl, void* stream) {
+extern "C" PRISM_API int prism_scan(const prism_dims* dims, const void* q, const void* k,
+                                    const void* v, const float* log_alpha, const float* beta,
+                                    const int32_t* seq_lens, void* workspace,
+                                    size_t workspace_bytes, float* out, float* final_state,
+                                    void* stream) {
   int rc = check_dims(dims);
   if (rc != PRISM_OK) return rc;
-  if (dims->L == 0) return PRISM_OK;
-  if (!v || !conv_w || !Wk || !Wp || !wbeta || !Kl || !Dl) return PRISM_ERR_INVALID_ARG;
-  const void* ptrs[] = {v, conv_w, Wk, Wp, wbeta, Kl, Dl, seq_lens};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return PRISM_ERR_MISALIGNED;
-  return run_k1(dims, v, conv_w, Wk, Wp, wbeta, seq_lens, Kl, Dl,
-                static_cast<cudaStream_t>(stream));
-}
-
-extern "C" PRISM_API int prism_chunk_scan(const prism_dims* dims, const void* q, const void* k,
-                                          const void* v, const float* log_alpha,
-                                          const float* beta, const void* Kl, const void* Dl,
-                                          void* out, float* final_state, const int32_t* seq_lens,
-                                          void* stream);
-
-extern "C" PRISM_API int prism_forward(const prism_dims* dims, const void* q, const void* k, const void* v,
-                             const float* log_alpha, const float* beta, const float* conv_w,
-                             const float* Wk, const float* Wp, const float* wbeta, void* out,
-                             float* final_state, const int32_t* seq_lens, void* workspace,
-                             size_t workspace_bytes, void* stream) {
-  int rc = check_dims(dims);
+  rc = check_inputs(dims, q, k, v, log_alpha, beta, seq_lens, workspace, workspace_bytes);
   if (rc != PRISM_OK) return rc;
-  if (!q || !k || !v || !log_alpha || !beta || !out) return PRISM_ERR_INVALID_ARG;
-  if (dims->L > 0 && (!conv_w || !Wk || !Wp || !wbeta)) return PRISM_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, out, final_state,
-                        seq_lens, workspace};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return PRISM_ERR_MISALIGNED;
-  const size_t need = prism_workspace_bytes(dims);
-  if (dims->L > 0 && (!workspace || workspace_bytes < need)) return PRISM_ERR_WORKSPACE;
+  if (!out) return PRISM_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || (final_state && !aligned(final_state, 16))) return PRISM_ERR_MISALIGNED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  void* Kl = ws;
-  void* Dl = ws ? ws + round256(factor_bytes(dims)) : nullptr;
-  if (dims->L > 0) {
-    rc = run_k1(dims, v, conv_w, Wk, Wp, wbeta, seq_lens, Kl, Dl, s);
-    if (rc != PRISM_OK) return rc;
+  const Layout Lo = layout(dims);
+  const int D = dims->d_k, C = dims->chunk;
+  if (dims->dtype == PRISM_F32) {
+    prism::K2Args a;
+    a.B = dims->B; a.T = dims->T; a.H = dims->H; a.L = dims->L;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
+    a.Kl = region<float>(workspace, Lo, PRISM_WS_KL);
+    a.Dl = region<float>(workspace, Lo, PRISM_WS_DL);
+    a.seq_lens = seq_lens; a.out = out; a.final_state = final_state;
+    return prism::launch_k2(0, D, C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
   }
-  return prism_chunk_scan(dims, q, k, v, log_alpha, beta, Kl, Dl, out, final_state, seq_lens,
-                          stream);
+  prism::ScanArgs a;
+  a.B = dims->B; a.T = dims->T; a.H = dims->H; a.L = dims->L;
+  a.Wc = region<const __half>(workspace, Lo, PRISM_WS_W);
+  a.Kt = region<const __half>(workspace, Lo, PRISM_WS_KT);
+  a.Qth = region<const __half>(workspace, Lo, PRISM_WS_QTH);
+  a.Qtl = region<const __half>(workspace, Lo, PRISM_WS_QTL);
+  a.U = region<const float>(workspace, Lo, PRISM_WS_U);
+  a.Oi = region<const float>(workspace, Lo, PRISM_WS_OI);
+  a.Nl = region<const float>(workspace, Lo, PRISM_WS_N);
+  a.gC = region<const float>(workspace, Lo, PRISM_WS_GC);
+  a.seq_lens = seq_lens; a.out = out; a.final_state = final_state;
+  return prism::launch_scan(D, C, pick_bv(dims), a, s) == cudaSuccess ? PRISM_OK
+                                                                      : PRISM_ERR_LAUNCH;
 }
 
-extern "C" PRISM_API int prism_chunk_scan(const prism_dims* dims, const void* q, const void* k,
-                                          const void* v, const float* log_alpha,
-                                          const float* beta, const void* Kl, const void* Dl,
-                                          void* out, float* final_state, const int32_t* seq_lens,
-                                          void* stream) {
+extern "C" PRISM_API int prism_forward(const prism_dims* dims, const void* q, const void* k,
+                                       const void* v, const float* log_alpha, const float* beta,
+                                       const float* conv_w, const float* Wk, const float* Wp,
+                                       const float* wbeta, float* out, float* final_state,
+                                       const int32_t* seq_lens, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
   int rc = check_dims(dims);
   if (rc != PRISM_OK) return rc;
-  if (!q || !k || !v || !log_alpha || !beta || !out) return PRISM_ERR_INVALID_ARG;
-  if (dims->L > 0 && (!Kl || !Dl)) return PRISM_ERR_INVALID_ARG;
-  const void* ptrs[] = {q, k, v, log_alpha, beta, Kl, Dl, out, final_state, seq_lens};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return PRISM_ERR_MISALIGNED;
-  prism::K2Args a;
-  a.B = dims->B; a.T = dims->T; a.H = dims->H; a.L = dims->L;
-  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
-  a.Kl = Kl; a.Dl = Dl; a.seq_lens = seq_lens; a.out = out; a.final_state = final_state;
-  const int dt = dims->dtype == PRISM_BF16 ? 1 : 0;
-  return prism::launch_k2(dt, dims->d_k, dims->chunk, a, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? PRISM_OK
-             : PRISM_ERR_LAUNCH;
+  if (!out) return PRISM_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || (final_state && !aligned(final_state, 16))) return PRISM_ERR_MISALIGNED;
+  rc = prism_prepare(dims, q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, seq_lens, workspace,
+                     workspace_bytes, stream);
+  if (rc != PRISM_OK) return rc;
+  return prism_scan(dims, q, k, v, log_alpha, beta, seq_lens, workspace, workspace_bytes, out,
+                    final_state, stream);
 }

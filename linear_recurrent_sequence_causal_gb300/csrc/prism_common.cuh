@@ -10,7 +10,10 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 namespace prism {
 
@@ -40,6 +43,15 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
@@ -75,10 +87,9 @@ __device__ __forceinline__ int acc_col(int h, int e) {
 //   B_NK == false: B(k,n) = b[k*ldb + n]  (stored K x N, row-major)
 // Offsets m0, n0 are multiples of 16; K is a multiple of 16; all row strides
 // are multiples of 8 elements and the bases 16-byte aligned.
-template <bool A_T, bool B_NK>
-__device__ __forceinline__ void tile_mma(Acc16& acc, const __nv_bfloat16* a, int lda,
-                                         const __nv_bfloat16* b, int ldb, int m0, int n0,
-                                         int K) {
+template <bool A_T, bool B_NK, class H16>
+__device__ __forceinline__ void tile_mma16(Acc16& acc, const H16* a, int lda, const H16* b, int ldb,
+                                           int m0, int n0, int K) {
   const int lane = threadIdx.x & 31;
   const int j = lane >> 3;      // which 8x8 matrix this lane addresses
   const int r = lane & 7;       // which row of it
@@ -86,25 +97,41 @@ __device__ __forceinline__ void tile_mma(Acc16& acc, const __nv_bfloat16* a, int
     uint32_t af[4], bf[4];
     if (!A_T) {
       // matrices: (m+0,k+0) (m+8,k+0) (m+0,k+8) (m+8,k+8)
-      const __nv_bfloat16* p = a + (size_t)(m0 + r + 8 * (j & 1)) * lda + k0 + 8 * (j >> 1);
+      const H16* p = a + (size_t)(m0 + r + 8 * (j & 1)) * lda + k0 + 8 * (j >> 1);
       ldsm_x4(smem_u32(p), af);
     } else {
       // stored [k][m]; same four blocks, rows of the stored matrix are k
-      const __nv_bfloat16* p = a + (size_t)(k0 + r + 8 * (j >> 1)) * lda + m0 + 8 * (j & 1);
+      const H16* p = a + (size_t)(k0 + r + 8 * (j >> 1)) * lda + m0 + 8 * (j & 1);
       ldsm_x4_t(smem_u32(p), af);
     }
     if (B_NK) {
       // matrices: (n+0,k+0) (n+0,k+8) (n+8,k+0) (n+8,k+8)
-      const __nv_bfloat16* p = b + (size_t)(n0 + r + 8 * (j >> 1)) * ldb + k0 + 8 * (j & 1);
+      const H16* p = b + (size_t)(n0 + r + 8 * (j >> 1)) * ldb + k0 + 8 * (j & 1);
       ldsm_x4(smem_u32(p), bf);
     } else {
       // stored [k][n]: matrices (k+0,n+0) (k+8,n+0) (k+0,n+8) (k+8,n+8)
-      const __nv_bfloat16* p = b + (size_t)(k0 + r + 8 * (j & 1)) * ldb + n0 + 8 * (j >> 1);
+      const H16* p = b + (size_t)(k0 + r + 8 * (j & 1)) * ldb + n0 + 8 * (j >> 1);
       ldsm_x4_t(smem_u32(p), bf);
     }
-    mma_bf16_16816(acc.v[0], af, bf[0], bf[1]);
-    mma_bf16_16816(acc.v[1], af, bf[2], bf[3]);
+    if constexpr (sizeof(H16) == 2 && std::is_same<H16, __half>::value) {
+      mma_f16_16816(acc.v[0], af, bf[0], bf[1]);
+      mma_f16_16816(acc.v[1], af, bf[2], bf[3]);
+    } else {
+      mma_bf16_16816(acc.v[0], af, bf[0], bf[1]);
+      mma_bf16_16816(acc.v[1], af, bf[2], bf[3]);
+    }
   }
+}
+
+template <bool A_T, bool B_NK>
+__device__ __forceinline__ void tile_mma(Acc16& acc, const __nv_bfloat16* a, int lda,
+                                         const __nv_bfloat16* b, int ldb, int m0, int n0, int K) {
+  tile_mma16<A_T, B_NK>(acc, a, lda, b, ldb, m0, n0, K);
+}
+template <bool A_T, bool B_NK>
+__device__ __forceinline__ void tile_mma(Acc16& acc, const __half* a, int lda, const __half* b,
+                                         int ldb, int m0, int n0, int K) {
+  tile_mma16<A_T, B_NK>(acc, a, lda, b, ldb, m0, n0, K);
 }
 
 template <bool A_T, bool B_NK>
@@ -131,19 +158,19 @@ __device__ __forceinline__ void tile_mma(Acc16& acc, const float* a, int lda, co
 }
 
 // Tiles of an M x N output, numbered row-major in 16 x 16 units, dealt
-// round-robin to the kWarps warps: warp w owns tiles w, w + kWarps, ...
-template <int M, int N>
+// round-robin to the NW warps: warp w owns tiles w, w + NW, ...
+template <int M, int N, int NW = kWarps>
 struct TileMap {
   static constexpr int kTM = M / 16, kTN = N / 16, kTiles = kTM * kTN;
-  static constexpr int kPerWarp = (kTiles + kWarps - 1) / kWarps;
+  static constexpr int kPerWarp = (kTiles + NW - 1) / NW;
   static __device__ __forceinline__ bool valid(int i) {
-    return (threadIdx.x >> 5) + i * kWarps < kTiles;
+    return (threadIdx.x >> 5) + i * NW < kTiles;
   }
   static __device__ __forceinline__ int m0(int i) {
-    return (((threadIdx.x >> 5) + i * kWarps) / kTN) * 16;
+    return (((threadIdx.x >> 5) + i * NW) / kTN) * 16;
   }
   static __device__ __forceinline__ int n0(int i) {
-    return (((threadIdx.x >> 5) + i * kWarps) % kTN) * 16;
+    return (((threadIdx.x >> 5) + i * NW) % kTN) * 16;
   }
 };
 

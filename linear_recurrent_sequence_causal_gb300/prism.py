@@ -21,8 +21,9 @@ PRISM_FLAG_NO_GELU = 1
 ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
           3: "PRISM_ERR_MISALIGNED", 4: "PRISM_ERR_WORKSPACE", 5: "PRISM_ERR_LAUNCH",
           6: "PRISM_ERR_CUDA"}
-EXPORTS = ("prism_workspace_bytes", "prism_forward", "prism_anchor_refine", "prism_chunk_scan",
-           "prism_strerror")
+EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "prism_prepare",
+           "prism_scan", "prism_strerror")
+WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "W", "Kt", "Qth", "Qtl", "U", "Oi", "N", "gC")
 
 
 class PrismError(RuntimeError):
@@ -58,12 +59,15 @@ def load():
             lib = ctypes.CDLL(path)
             lib.prism_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
             lib.prism_workspace_bytes.restype = ctypes.c_size_t
+            lib.prism_workspace_layout.argtypes = [ctypes.POINTER(Dims),
+                                                   ctypes.POINTER(ctypes.c_size_t), ctypes.c_int]
+            lib.prism_workspace_layout.restype = ctypes.c_int
             lib.prism_forward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 13 + [ctypes.c_size_t, _vp]
             lib.prism_forward.restype = ctypes.c_int
-            lib.prism_anchor_refine.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 9
-            lib.prism_anchor_refine.restype = ctypes.c_int
-            lib.prism_chunk_scan.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 11
-            lib.prism_chunk_scan.restype = ctypes.c_int
+            lib.prism_prepare.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 11 + [ctypes.c_size_t, _vp]
+            lib.prism_prepare.restype = ctypes.c_int
+            lib.prism_scan.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 7 + [ctypes.c_size_t] + [_vp] * 3
+            lib.prism_scan.restype = ctypes.c_int
             lib.prism_strerror.argtypes = [ctypes.c_int]
             lib.prism_strerror.restype = ctypes.c_char_p
             _lib = lib
@@ -110,64 +114,73 @@ def _stream_ptr(stream):
     return s.cuda_stream
 
 
+def workspace_layout(dims: Dims) -> dict:
+    """Byte offsets of the workspace regions (None where absent)."""
+    offs = (ctypes.c_size_t * len(WS_REGIONS))()
+    _check(load().prism_workspace_layout(ctypes.byref(dims), offs, len(WS_REGIONS)))
+    absent = (1 << (8 * ctypes.sizeof(ctypes.c_size_t))) - 1
+    return {n: (None if offs[i] == absent else int(offs[i])) for i, n in enumerate(WS_REGIONS)}
+
+
+def _dims_for(q, v, conv_w, L, chunk, no_gelu=False) -> Dims:
+    B, T, H, dk = q.shape
+    return make_dims(B, T, H, dk, v.shape[-1], conv_w.shape[1], L, chunk, q.dtype, no_gelu)
+
+
+def alloc_workspace(dims: Dims, device) -> torch.Tensor:
+    return torch.empty(max(workspace_bytes(dims), 1), dtype=torch.uint8, device=device)
+
+
 def prism_forward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, out=None,
                   final_state=None, seq_lens=None, workspace=None, stream=None,
                   no_gelu=False, want_state=True):
     """The mixer forward pass on CUDA tensors laid out as in include/prism.h.
 
-    Returns ``(out, final_state)``; ``final_state`` is None when
+    Returns ``(out, final_state)`` (out is fp32); ``final_state`` is None when
     ``want_state`` is False and none was passed.
     """
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    w = conv_w.shape[1]
-    dims = make_dims(B, T, H, dk, dv, w, L, chunk, q.dtype, no_gelu)
+    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu)
     if out is None:
-        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+        out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
     if final_state is None and want_state:
         final_state = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
-    need = workspace_bytes(dims)
-    if workspace is None and L > 0:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if workspace is None:
+        workspace = alloc_workspace(dims, q.device)
     rc = load().prism_forward(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                               _ptr(beta), _ptr(conv_w), _ptr(Wk), _ptr(Wp), _ptr(wbeta),
                               _ptr(out), _ptr(final_state), _ptr(seq_lens), _ptr(workspace),
-                              ws_bytes, _stream_ptr(stream))
+                              workspace.numel(), _stream_ptr(stream))
     _check(rc)
     return out, final_state
 
 
-def prism_anchor_refine(v, conv_w, Wk, Wp, wbeta, L, *, seq_lens=None, Kl=None, Dl=None,
-                        stream=None, no_gelu=False, chunk=64):
-    """Anchor + refinement only: returns the write factors (Kl, Dl)."""
-    B, T, H, dv = v.shape
-    dk = Wk.shape[2]
-    dims = make_dims(B, T, H, dk, dv, conv_w.shape[1], L, chunk, v.dtype, no_gelu)
-    if Kl is None:
-        Kl = torch.empty((B, T, H, L, dk), dtype=v.dtype, device=v.device)
-    if Dl is None:
-        Dl = torch.empty((B, T, H, L, dv), dtype=v.dtype, device=v.device)
-    rc = load().prism_anchor_refine(ctypes.byref(dims), _ptr(v), _ptr(conv_w), _ptr(Wk), _ptr(Wp),
-                                    _ptr(wbeta), _ptr(seq_lens), _ptr(Kl), _ptr(Dl),
-                                    _stream_ptr(stream))
+def prism_prepare(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, workspace, *,
+                  seq_lens=None, stream=None, no_gelu=False):
+    """State-independent stage into ``workspace`` (see include/prism.h)."""
+    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu)
+    rc = load().prism_prepare(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                              _ptr(beta), _ptr(conv_w), _ptr(Wk), _ptr(Wp), _ptr(wbeta),
+                              _ptr(seq_lens), _ptr(workspace), workspace.numel(),
+                              _stream_ptr(stream))
     _check(rc)
-    return Kl, Dl
+    return workspace
 
 
-def prism_chunk_scan(q, k, v, log_alpha, beta, Kl, Dl, L, chunk, conv_width, *, out=None,
-                     final_state=None, seq_lens=None, stream=None, want_state=True):
-    """Chunkwise scan + readout only, given the write factors (Kl, Dl)."""
+def prism_scan(q, k, v, log_alpha, beta, L, chunk, conv_width, workspace, *, out=None,
+               final_state=None, seq_lens=None, stream=None, want_state=True, no_gelu=False):
+    """Serial stage from a prepared workspace; returns (out, final_state)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    dims = make_dims(B, T, H, dk, dv, conv_width, L, chunk, q.dtype)
+    dims = make_dims(B, T, H, dk, dv, conv_width, L, chunk, q.dtype, no_gelu)
     if out is None:
-        out = torch.empty((B, T, H, dv), dtype=q.dtype, device=q.device)
+        out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
     if final_state is None and want_state:
         final_state = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
-    rc = load().prism_chunk_scan(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
-                                 _ptr(beta), _ptr(Kl), _ptr(Dl), _ptr(out), _ptr(final_state),
-                                 _ptr(seq_lens), _stream_ptr(stream))
+    rc = load().prism_scan(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                           _ptr(beta), _ptr(seq_lens), _ptr(workspace), workspace.numel(),
+                           _ptr(out), _ptr(final_state), _stream_ptr(stream))
     _check(rc)
     return out, final_state
 

@@ -58,3 +58,63 @@ def check(out_gpu, fs_gpu, out_ref, fs_ref, dtype: str, *, bh=None, seq_lens=Non
         for b, n in enumerate(lens.tolist()):
             assert np.all(o[b, n:] == 0.0), f"{what}: padding of sequence {b} not zero"
     return err
+
+
+def chunk_maps(inp, kl, dl, C):
+    """fp64 reference of what the bf16 prepare stage writes per chunk:
+    W, Kt, Qt, U, O_intra ([B,H,NC,C,D]), N ([B,H,NC,D,D]) and gamma_C ([B,H,NC]),
+    from the inputs and the oracle's per-token factors k^(l), beta^(l) delta^(l)."""
+    q, k, v = (inp[n].double().numpy() for n in ("q", "k", "v"))
+    la, be = inp["log_alpha"].double().numpy(), inp["beta"].double().numpy()
+    B, T, H, D = q.shape
+    L = kl.shape[3]
+    NC = (T + C - 1) // C
+    sl = inp.get("seq_lens")
+    names = ("W", "Kt", "Qt", "U", "Oi")
+    res = {n: np.zeros((B, H, NC, C, D)) for n in names}
+    res["N"] = np.zeros((B, H, NC, D, D))
+    res["gC"] = np.ones((B, H, NC))
+    for b in range(B):
+        n_len = T if sl is None else int(sl[b])
+        for h in range(H):
+            for c in range(NC):
+                t0 = c * C
+                nv = min(C, n_len - t0)
+                if nv <= 0:
+                    continue
+                def pad(x):
+                    y = np.zeros((C,) + x.shape[1:])
+                    y[:nv] = x[:nv]
+                    return y
+                Q, K, V = (pad(a[b, t0:t0 + C, h]) for a in (q, k, v))
+                bt = pad(be[b, t0:t0 + C, h])
+                g = np.cumsum(pad(la[b, t0:t0 + C, h]))
+                gam = np.exp(g)
+                G = np.exp(np.minimum(g[:, None] - g[None, :], 0.0))
+                low, inc = np.tril(np.ones((C, C)), -1), np.tril(np.ones((C, C)))
+                Kl = [np.nan_to_num(pad(kl[b, t0:t0 + C, h, l])) for l in range(L)]
+                Dl = [np.nan_to_num(pad(dl[b, t0:t0 + C, h, l])) for l in range(L)]
+                dec = np.exp(g[-1] - g)
+                R = sum(((K @ Kl[l].T) * G * low) @ Dl[l] for l in range(L)) if L else 0.0
+                Ol = sum(((Q @ Kl[l].T) * G * inc) @ Dl[l] for l in range(L)) if L else 0.0
+                A = bt[:, None] * (K @ K.T) * G * low
+                Tm = np.linalg.inv(np.eye(C) + A)
+                P = (Q @ K.T) * G * inc
+                W = Tm @ ((bt * gam)[:, None] * K)
+                U = Tm @ (bt[:, None] * (V - R))
+                res["W"][b, h, c] = W
+                res["Kt"][b, h, c] = dec[:, None] * K
+                res["Qt"][b, h, c] = gam[:, None] * Q - P @ W
+                res["U"][b, h, c] = U
+                res["Oi"][b, h, c] = P @ U + Ol
+                if L:
+                    res["N"][b, h, c] = sum((dec[:, None] * Dl[l]).T @ Kl[l] for l in range(L))
+                res["gC"][b, h, c] = np.exp(g[-1])
+    return res
+
+
+def read_region(ws, layout, name, dtype, shape):
+    """View of one workspace region as a CPU fp64 numpy array."""
+    off = layout[name]
+    n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+    return ws[off:off + n].view(dtype).reshape(shape).double().cpu().numpy()

@@ -35,10 +35,22 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_workspace_and_strerror(lib):
-    d = prism.make_dims(8, 4096, 16, 128, 128, 4, 2, 64, prism.PRISM_BF16)
-    # Kl and Dl: B*T*H*L*d*2 bytes each, 256-aligned, plus 256
-    assert prism.workspace_bytes(d) == 2 * 8 * 4096 * 16 * 2 * 128 * 2 + 256
+    B, T, H, D, L, C = 8, 4096, 16, 128, 2, 64
+    d = prism.make_dims(B, T, H, D, D, 4, L, C, prism.PRISM_BF16)
+    NC = T // C
+    per = B * H * NC * C * D
+    expect = (256 + H * L * 4 * 128 * D * 2 + 4 * per * 2 + 2 * per * 4 + B * H * NC * D * D * 4
+              + B * H * NC * 4)
+    assert prism.workspace_bytes(d) == expect
+    lay = prism.workspace_layout(d)
+    assert lay["status"] == 0 and lay["Kl"] is None and lay["gC"] + B * H * NC * 4 == expect
+    offs = sorted(v for v in lay.values() if v is not None)
+    assert all(o % 256 == 0 for o in offs)
+    d0 = prism.make_dims(B, T, H, D, D, 4, 0, C, prism.PRISM_BF16)
+    assert prism.workspace_layout(d0)["N"] is None and prism.workspace_layout(d0)["wblocks"] is None
     assert prism.workspace_bytes(prism.make_dims(1, 8, 1, 128, 128, 4, 2, 64, prism.PRISM_F32)) == 0
+    f = prism.make_dims(1, 8, 1, 32, 32, 4, 2, 16, prism.PRISM_F32)
+    assert prism.workspace_bytes(f) == 256 + 2 * (1 * 8 * 1 * 2 * 32 * 4)   # Kl, Dl fp32
     for code in range(7):
         assert lib.prism_strerror(code)
     assert b"unknown" in lib.prism_strerror(99)
@@ -70,6 +82,11 @@ def test_null_and_misaligned_pointers(lib):
     assert _fwd(lib, d, good, 16) == 4                                # workspace too small
     nows = list(good); nows[12] = None
     assert _fwd(lib, d, nows, 1 << 40) == 4                           # workspace NULL
-    assert lib.prism_anchor_refine(ctypes.byref(d), None, *[0x1000] * 8, None) == 1
-    assert lib.prism_chunk_scan(ctypes.byref(d), *[0x1000] * 5, None, 0x1000, *[0x1000] * 3,
-                                None) == 1                            # Kl NULL with L > 0
+    big = 1 << 40
+    ws = 0x100000
+    # prepare: conv_w NULL with L > 0
+    assert lib.prism_prepare(ctypes.byref(d), *[0x1000] * 5, None, *[0x1000] * 4, ws, big, None) == 1
+    # prepare: workspace not 256-byte aligned
+    assert lib.prism_prepare(ctypes.byref(d), *[0x1000] * 10, 0x1010, big, None) == 3
+    # scan: out NULL
+    assert lib.prism_scan(ctypes.byref(d), *[0x1000] * 6, ws, big, None, None, None) == 1

@@ -154,25 +154,66 @@ def test_no_gelu_ablation():
     check(out, fs, ro, rs, "bf16", what="no-GELU ablation")
 
 
-@pytest.mark.parametrize("dtype,D", [("f32", 32), ("bf16", 128)])
-def test_write_factors(dtype, D):
-    """The anchor/refinement kernel's k^(l) and beta^(l) delta^(l) against the
-    oracle's per-token trace."""
-    wl = I.Workload("case", dtype, 2, 90, 2, D, D, 3, 4, 32, seed=9, ragged=True)
+@pytest.mark.parametrize("D,C,L,ragged", [(128, 64, 2, False), (64, 32, 3, True), (32, 16, 1, False),
+                                          (16, 64, 0, True), (128, 32, 4, True)])
+def test_prepare_stage_bf16(D, C, L, ragged):
+    """The tensor-core prepare kernel's per-chunk maps (W, Kt, Qt, U, O_intra, N,
+    gamma_C) against an fp64 numpy restatement fed with the oracle's factors."""
+    from tests.parity import chunk_maps, read_region
+    wl = I.Workload("case", "bf16", 2, 3 * C + 5, 2, D, D, L, 4, C, seed=40 + D + C, ragged=False)
+    inp = I.generate(wl)
+    if ragged:
+        inp["seq_lens"] = torch.tensor([wl.T, C + 3], dtype=torch.int32)
+    d = prism.inputs_to_device(inp)
+    dims = prism.make_dims(wl.B, wl.T, wl.H, D, D, wl.w, L, C, torch.bfloat16)
+    ws = torch.zeros(prism.workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    prism.prism_prepare(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"], d["Wk"],
+                        d["Wp"], d["wbeta"], L, C, ws, seq_lens=d.get("seq_lens"))
+    torch.cuda.synchronize()
+    lay = prism.workspace_layout(dims)
+    NC = (wl.T + C - 1) // C
+    _, _, tr = oracle.forward(inp, trace=True)
+    ref = chunk_maps(inp, tr["kl"], tr["dl"], C)
+    shp = (wl.B, wl.H, NC, C, D)
+    got = {"W": read_region(ws, lay, "W", torch.float16, shp),
+           "Kt": read_region(ws, lay, "Kt", torch.float16, shp),
+           "Qt": read_region(ws, lay, "Qth", torch.float16, shp) + read_region(ws, lay, "Qtl", torch.float16, shp),
+           "U": read_region(ws, lay, "U", torch.float32, shp),
+           "Oi": read_region(ws, lay, "Oi", torch.float32, shp),
+           "gC": read_region(ws, lay, "gC", torch.float32, (wl.B, wl.H, NC))}
+    if L:
+        got["N"] = read_region(ws, lay, "N", torch.float32, (wl.B, wl.H, NC, D, D))
+    lens = [wl.T] * wl.B if not ragged else inp["seq_lens"].tolist()
+    for name, g in got.items():
+        r = ref[name]
+        for b in range(wl.B):
+            nch = (lens[b] + C - 1) // C
+            gb, rb = g[b, :, :nch], r[b, :, :nch]
+            err = np.max(np.abs(gb - rb)) / max(np.max(np.abs(rb)), 1e-30)
+            assert err <= 5e-3, f"{name} (b={b}): normwise error {err:.3e}"
+
+
+def test_prepare_stage_f32():
+    """fp32 path: the per-token factors in the workspace against the oracle trace."""
+    from tests.parity import read_region
+    wl = I.Workload("case", "f32", 2, 90, 2, 32, 32, 3, 4, 32, seed=9)
     inp = I.generate(wl)
     inp["seq_lens"] = torch.tensor([90, 41], dtype=torch.int32)
     d = prism.inputs_to_device(inp)
-    Kl, Dl = prism.prism_anchor_refine(d["v"], d["conv_w"], d["Wk"], d["Wp"], d["wbeta"], wl.L,
-                                       seq_lens=d["seq_lens"])
+    dims = prism.make_dims(wl.B, wl.T, wl.H, 32, 32, wl.w, wl.L, wl.chunk, torch.float32)
+    ws = torch.zeros(prism.workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    prism.prism_prepare(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"], d["Wk"],
+                        d["Wp"], d["wbeta"], wl.L, wl.chunk, ws, seq_lens=d["seq_lens"])
     torch.cuda.synchronize()
+    lay = prism.workspace_layout(dims)
     _, _, tr = oracle.forward(inp, trace=True)
-    tol = 1e-5 if dtype == "f32" else 2e-2
-    for name, g, r in (("k^(l)", Kl, tr["kl"]), ("beta delta", Dl, tr["dl"])):
-        g = to64(g)
+    shp = (wl.B, wl.T, wl.H, wl.L, 32)
+    for name, key in (("Kl", "kl"), ("Dl", "dl")):
+        g = read_region(ws, lay, name, torch.float32, shp)
         for b, n in enumerate([90, 41]):
-            ref = r[b, :n]
+            ref = tr[key][b, :n]
             err = np.max(np.abs(g[b, :n] - ref)) / np.max(np.abs(ref))
-            assert err <= tol, f"{name}: {err:.3e}"
+            assert err <= 1e-5, f"{name}: {err:.3e}"
             assert np.all(g[b, n:] == 0.0)
 
 
@@ -202,7 +243,7 @@ def test_boundary_errors_on_device():
     wl = I.Workload("case", "bf16", 1, 64, 1, 64, 64, 2, 4, 64, seed=6)
     d = prism.inputs_to_device(I.generate(wl))
     # misaligned output pointer
-    buf = torch.empty(64 * 64 + 8, dtype=torch.bfloat16, device="cuda")
+    buf = torch.empty(64 * 64 + 8, dtype=torch.float32, device="cuda")
     bad_out = buf[1:1 + 64 * 64].view(1, 64, 1, 64)
     with pytest.raises(prism.PrismError) as e:
         prism.forward_inputs(d, 2, 64, out=bad_out)
