@@ -76,7 +76,9 @@ enum {
     PRISM_ERR_MISALIGNED = 3,    /* a tensor pointer is not 16-byte aligned (workspace: 256) */
     PRISM_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than prism_workspace_bytes() */
     PRISM_ERR_LAUNCH = 5,        /* a kernel launch failed (cudaGetLastError) */
-    PRISM_ERR_CUDA = 6           /* another CUDA runtime call failed */
+    PRISM_ERR_CUDA = 6,          /* another CUDA runtime call failed */
+    PRISM_ERR_SCRATCH_LIMIT = 7  /* prism_forward_static: the dims need more scratch than
+                                    PRISM_STATIC_SCRATCH_BYTES */
 };
 
 /* Workspace regions (see prism_workspace_layout). */
@@ -139,6 +141,35 @@ PRISM_API int prism_scan(const prism_dims* dims,
                          const float* log_alpha, const float* beta,
                          const int32_t* seq_lens, void* workspace, size_t workspace_bytes,
                          float* out, float* final_state, void* stream);
+
+/* Size of the library's own device scratch array used by prism_forward_static. */
+#define PRISM_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* prism_forward without a caller-provided workspace.  (The paper has no
+ * counterpart: this is a deployment convenience of this library.)
+ *
+ * For callers that cannot allocate device memory where they run the layer
+ * (pre-planned memory arenas, frameworks that forbid allocation on the hot
+ * path, plugins handed only input and output buffers).  The scratch is a
+ * fixed array of PRISM_STATIC_SCRATCH_BYTES in the library's device memory;
+ * every GPU that loads the library holds it until the process exits.  Inputs
+ * and outputs are as for prism_forward.
+ *   - Dims whose prism_workspace_bytes() exceeds PRISM_STATIC_SCRATCH_BYTES
+ *     are rejected with PRISM_ERR_SCRATCH_LIMIT before anything is launched.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current (cudaGetSymbolAddress); make that first call before
+ *     any stream capture on the device.
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents.  Calls that overlap on the GPU (other streams, or threads
+ *     without ordering between their launches) race on it: serialise them. */
+PRISM_API int prism_forward_static(const prism_dims* dims,
+                                   const void* q, const void* k, const void* v,
+                                   const float* log_alpha, const float* beta,
+                                   const float* conv_w, const float* Wk, const float* Wp,
+                                   const float* wbeta,
+                                   float* out, float* final_state, const int32_t* seq_lens,
+                                   void* stream);
 
 /* Static description of an error code. */
 PRISM_API const char* prism_strerror(int code);

@@ -192,6 +192,7 @@ extern "C" PRISM_API const char* prism_strerror(int code) {
     case PRISM_ERR_WORKSPACE: return "workspace missing or smaller than prism_workspace_bytes()";
     case PRISM_ERR_LAUNCH: return "kernel launch failed";
     case PRISM_ERR_CUDA: return "CUDA runtime call failed";
+    case PRISM_ERR_SCRATCH_LIMIT: return "dims need more scratch than PRISM_STATIC_SCRATCH_BYTES (use prism_forward with a workspace)";
   }
   return "unknown error code";
 }

@@ -20,9 +20,10 @@ PRISM_F32, PRISM_BF16 = 0, 1
 PRISM_FLAG_NO_GELU = 1
 ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
           3: "PRISM_ERR_MISALIGNED", 4: "PRISM_ERR_WORKSPACE", 5: "PRISM_ERR_LAUNCH",
-          6: "PRISM_ERR_CUDA"}
+          6: "PRISM_ERR_CUDA", 7: "PRISM_ERR_SCRATCH_LIMIT"}
+STATIC_SCRATCH_BYTES = 32 << 20
 EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "prism_prepare",
-           "prism_scan", "prism_strerror")
+           "prism_scan", "prism_forward_static", "prism_strerror")
 WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "W", "Kt", "Qth", "Qtl", "U", "Oi", "N", "gC")
 
 
@@ -68,6 +69,8 @@ def load():
             lib.prism_prepare.restype = ctypes.c_int
             lib.prism_scan.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 7 + [ctypes.c_size_t] + [_vp] * 3
             lib.prism_scan.restype = ctypes.c_int
+            lib.prism_forward_static.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 13
+            lib.prism_forward_static.restype = ctypes.c_int
             lib.prism_strerror.argtypes = [ctypes.c_int]
             lib.prism_strerror.restype = ctypes.c_char_p
             _lib = lib
@@ -152,6 +155,29 @@ def prism_forward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, 
                               _ptr(beta), _ptr(conv_w), _ptr(Wk), _ptr(Wp), _ptr(wbeta),
                               _ptr(out), _ptr(final_state), _ptr(seq_lens), _ptr(workspace),
                               workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return out, final_state
+
+
+def prism_forward_static(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, out=None,
+                         final_state=None, seq_lens=None, stream=None, no_gelu=False,
+                         want_state=True):
+    """prism_forward using the library's static device scratch (no workspace).
+
+    For callers that cannot allocate device memory on their hot path; see
+    include/prism.h for the size limit and the sharing rules.
+    """
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
+    if final_state is None and want_state:
+        final_state = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    rc = load().prism_forward_static(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v),
+                                     _ptr(log_alpha), _ptr(beta), _ptr(conv_w), _ptr(Wk), _ptr(Wp),
+                                     _ptr(wbeta), _ptr(out), _ptr(final_state), _ptr(seq_lens),
+                                     _stream_ptr(stream))
     _check(rc)
     return out, final_state
 
