@@ -134,10 +134,10 @@ struct PrepSmem {
   static constexpr uint32_t oG = 0;                      // f32 g[C]
   static constexpr uint32_t oDec = oG + 4 * C;           // f32 gamma_C/gamma [C]
   static constexpr uint32_t oBeta = oDec + 4 * C;        // f32 beta^(l) [C]
-  static constexpr uint32_t oNorm = oBeta + 4 * C;       // f32 [4][C]
-  static constexpr uint32_t oBar = oNorm + 16 * C;       // 2 mbarriers
-  static constexpr uint32_t oSlot = oBar + 16;
-  static constexpr uint32_t oTiles = ((oSlot + 16 + 127) / 128) * 128;
+  static constexpr uint32_t oInv = oBeta + 4 * C;        // f32 1/|k_hat| [C]
+  static constexpr uint32_t oBar = oInv + 4 * C;         // mbarriers: mma, W_k, W_p
+  static constexpr uint32_t oSlot = oBar + 24;
+  static constexpr uint32_t oTiles = ((oSlot + 8 + 127) / 128) * 128;
   // refinement-loop tiles
   static constexpr uint32_t oW = oTiles;
   static constexpr uint32_t oGP = oW + kW;               // hi, lo (2 * kF128)
@@ -150,10 +150,11 @@ struct PrepSmem {
   static constexpr uint32_t loop_end = oDt + 2 * kF128;
   // tail buffers (after the loop), placed around the [K;Q] tile which stays live
   static constexpr uint32_t sKX = 4 * C * D, sSq = 4 * C * (C + 1), sY = 1024 * (C / 16), sB = 8 * C;
+  static constexpr uint32_t sTB = 2 * C * C;               // f16 T as B operand (C x C)
   static constexpr Place p0{oW, oKQ, oKl};
   static constexpr uint32_t tKX = p0.where(sKX);         // f16 [Kb | X] MN-major, C x 2D
   static constexpr Place p1 = p0.at(sKX);
-  static constexpr uint32_t tTP = p1.where(kF128);       // f16 [T ; PT] 128 x C
+  static constexpr uint32_t tTP = p1.where(kF128);       // f16 [T ; PT] 128 x C  (also [I ; P])
   static constexpr Place p2 = p1.at(kF128);
   static constexpr uint32_t tA = p2.where(sSq);          // f32 [C][C+1]
   static constexpr Place p3 = p2.at(sSq);
@@ -161,10 +162,12 @@ struct PrepSmem {
   static constexpr Place p4 = p3.at(sSq);
   static constexpr uint32_t tT = p4.where(sSq);          // f32 [C][C+1]
   static constexpr Place p5 = p4.at(sSq);
-  static constexpr uint32_t tY = p5.where(sY);           // f32 solve scratch
+  static constexpr uint32_t tY = p5.where(sY);           // f32 block-solve scratch
   static constexpr Place p6 = p5.at(sY);
   static constexpr uint32_t tB = p6.where(sB);           // f32 beta[C], gamma[C]
-  static constexpr Place p7 = p6.at(sB);
+  static constexpr Place p7a = p6.at(sB);
+  static constexpr uint32_t tTB = p7a.where(sTB);        // f16 T (B operand)
+  static constexpr Place p7 = p7a.at(sTB);
   static constexpr uint32_t bytes = p7.o2 > loop_end ? p7.o2 : loop_end;
   static constexpr bool kExtraX = D > 2 * C;             // U/PU need their own TMEM columns
   static constexpr uint32_t tmem_cols_needed = 2 * C + 2 * D + (kExtraX ? D : 0);
@@ -172,6 +175,57 @@ struct PrepSmem {
       tmem_cols_needed <= 32 ? 32 : tmem_cols_needed <= 64 ? 64 : tmem_cols_needed <= 128 ? 128
                                   : tmem_cols_needed <= 256 ? 256 : 512;
 };
+
+// T = (I + A)^-1 for the strictly lower triangular C x C matrix A (fp32, row
+// stride C+1), by blocked forward substitution with 16 x 16 blocks:
+//   diagonal blocks  T_ii = (I + A_ii)^-1 : one lane per column, the column kept
+//                    in registers (row i needs only A's row i and rows < i of
+//                    the lane's own column);
+//   off-diagonal     T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, by diagonal level.
+// Result in sT (fp32, zeros above the diagonal).  All 256 threads take part.
+template <int C>
+__device__ __forceinline__ void solve_tri(const float* sA, float* sT, float* sY) {
+  constexpr int LD = C + 1, NB = C / 16;
+  const int tid = threadIdx.x;
+  for (int idx = tid; idx < C * C; idx += 256) {
+    const int i = idx / C, j = idx % C;
+    if (j / 16 != i / 16 && j > i) sT[i * LD + j] = 0.f;
+  }
+  if (tid < 16 * NB) {
+    const int blk = tid / 16, j = tid % 16, o = blk * 16;
+    float col[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float s = (i == j) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < i; ++m) s -= (m >= j) ? sA[(o + i) * LD + o + m] * col[m] : 0.f;
+      col[i] = (i >= j) ? s : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sT[(o + i) * LD + o + j] = col[i];
+  }
+  __syncthreads();
+  for (int lev = 1; lev < NB; ++lev) {
+    const int nblk = NB - lev;                       // blocks (i, j = i - lev)
+    // Y = sum_{k=j}^{i-1} A_ik T_kj
+    for (int idx = tid; idx < nblk * 256; idx += 256) {
+      const int bi = idx / 256 + lev, bj = bi - lev, r = (idx % 256) / 16, c = idx % 16;
+      float acc = 0.f;
+      for (int m = bj * 16; m < bi * 16; ++m) acc = fmaf(sA[(bi * 16 + r) * LD + m], sT[m * LD + bj * 16 + c], acc);
+      sY[idx] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nblk * 256; idx += 256) {
+      const int bi = idx / 256 + lev, bj = bi - lev, r = (idx % 256) / 16, c = idx % 16;
+      const float* Yb = sY + (idx / 256) * 256;
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) acc = fmaf(sT[(bi * 16 + r) * LD + bi * 16 + m], Yb[m * 16 + c], acc);
+      sT[(bi * 16 + r) * LD + bj * 16 + c] = -acc;
+    }
+    __syncthreads();
+  }
+}
 
 template <int D, int C>
 __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
@@ -189,9 +243,10 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   float* sg = reinterpret_cast<float*>(sm + S::oG);
   float* sdec = reinterpret_cast<float*>(sm + S::oDec);
   float* sbl = reinterpret_cast<float*>(sm + S::oBeta);
-  float* snorm = reinterpret_cast<float*>(sm + S::oNorm);
+  float* sinv = reinterpret_cast<float*>(sm + S::oInv);
   uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + S::oBar);
-  uint64_t* bar_ld = bar_mma + 1;
+  uint64_t* bar_wk = bar_mma + 1;
+  uint64_t* bar_wp = bar_mma + 2;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::oSlot);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -205,12 +260,23 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   const int nv = min(C, len - t0);
   if (nv <= 0) return;                         // chunk entirely padding: never read
   const bool need_lo = *p.wflag != 0;
+  const unsigned char* wsrc = p.wblocks;
+  auto wblock = [&](int l, int which, int part) {
+    return wsrc + WeightBlock<D>::index(h, l, L, which, part) * S::kW;
+  };
 
-  // ---- setup: barriers, TMEM, gates, [K;Q] rows, zero padding rows ----
+  // ---- setup: barriers, TMEM, first weights, gates, [K;Q] rows, v window ----
   if (tid == 0) {
     tc::bar_init(bar_mma, 1);
-    tc::bar_init(bar_ld, 1);
+    tc::bar_init(bar_wk, 1);
+    tc::bar_init(bar_wp, 1);
     tc::bar_fence_init();
+    if (L > 0) {                               // W^(0) streams in while the anchor is built
+      tc::bar_expect_tx(bar_wk, S::kW);
+      tc::bulk_g2s(sW, wblock(0, 0, 0), S::kW, bar_wk);
+      tc::bar_expect_tx(bar_wp, S::kW);
+      tc::bulk_g2s(sWp, wblock(0, 1, 0), S::kW, bar_wp);
+    }
   }
   if (warp == 0) tc::alloc(tslot, S::tmem_cols);
   if (warp == 1) {
@@ -248,39 +314,48 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     }
     *reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u) = outv;
   }
+  // v window, rows t0-w .. t0+C-1 as bf16 [C + w][D] (zero outside [0, len)), in the D tiles
+  __nv_bfloat16* vwin = reinterpret_cast<__nv_bfloat16*>(sD);
+  for (int idx = tid; idx < (C + w) * (D / 8); idx += 256) {
+    const int rr = idx / (D / 8), c8 = idx % (D / 8);
+    const int t = t0 - w + rr;
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (t >= 0 && t < len) x = *reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t) * H + h) * D + c8 * 8);
+    *reinterpret_cast<uint4*>(vwin + rr * D + c8 * 8) = x;
+  }
   // rows D..127 of the scaled-write tiles stay zero (A operand of the injection)
   if constexpr (D < 128)
-  for (int idx = tid; idx < (128 - D) * (C / 8) * 2; idx += 256) {
-    const int part = idx / ((128 - D) * (C / 8));
-    const int rem = idx % ((128 - D) * (C / 8));
-    const int r = D + rem % (128 - D), s8 = rem / (128 - D);
-    *reinterpret_cast<uint4*>(sDt + part * S::kF128 + s8 * 2048u + r * 16u) = make_uint4(0u, 0u, 0u, 0u);
-  }
+    for (int idx = tid; idx < (128 - D) * (C / 8) * 2; idx += 256) {
+      const int part = idx / ((128 - D) * (C / 8));
+      const int rem = idx % ((128 - D) * (C / 8));
+      const int r = D + rem % (128 - D), s8 = rem / (128 - D);
+      *reinterpret_cast<uint4*>(sDt + part * S::kF128 + s8 * 2048u + r * 16u) = make_uint4(0u, 0u, 0u, 0u);
+    }
   __syncthreads();
 
-  // ---- anchor u = sum_j c_j (.) v_{t-j}; residual r = v - u kept in registers ----
+  // ---- anchor u = sum_j c_j (.) v_{t-j}; u and the residual r = v - u stay in registers ----
   // thread (feature c = row, token half) owns tokens [half*NTH, half*NTH + NTH)
   const int c = row;
   const bool cvalid = c < D;
-  float r_reg[NTH];
+  float r_reg[NTH], u_reg[NTH];
   {
-    const __nv_bfloat16* vb = p.v + ((size_t)b * T_ * H + h) * D + c;
+    float taps[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) taps[j] = (cvalid && j < w) ? p.conv_w[((size_t)h * w + j) * D + c] : 0.f;
 #pragma unroll
     for (int j8 = 0; j8 < NTH; j8 += 8) {
       __half uh[8], ul[8];
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
         const int tl = half * NTH + j8 + jj;
-        const int t = t0 + tl;
         float u = 0.f, vt = 0.f;
         if (cvalid) {
-          for (int j = 1; j <= w; ++j) {
-            const int ts = t - j;
-            if (ts >= 0 && ts < len)
-              u = fmaf(p.conv_w[((size_t)h * w + (j - 1)) * D + c], __bfloat162float(vb[(size_t)ts * H * D]), u);
-          }
-          if (t < len) vt = __bfloat162float(vb[(size_t)t * H * D]);
+#pragma unroll
+          for (int j = 1; j <= 8; ++j)
+            if (j <= w) u = fmaf(taps[j - 1], __bfloat162float(vwin[(tl + w - j) * D + c]), u);
+          vt = __bfloat162float(vwin[(tl + w) * D + c]);
         }
+        u_reg[j8 + jj] = u;
         r_reg[j8 + jj] = (tl < nv) ? vt - u : 0.f;
         tc::split_f16(u, uh[jj], ul[jj]);
         if (cvalid) {
@@ -300,49 +375,38 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   const uint32_t t_proj = tmem, t_p = tmem + C, t_ro = tmem + 2 * C, t_n = tmem + 2 * C + D;
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
 
-  uint32_t ph_mma = 0, ph_ld = 0;
+  uint32_t ph_mma = 0, ph_wk = 0, ph_wp = 0;
   bool ok = true;
   auto wait_mma = [&]() {
     ok &= tc::bar_wait(bar_mma, ph_mma & 1);
     ++ph_mma;
     tc::fence_after();
   };
-  auto wait_ld = [&]() {
-    ok &= tc::bar_wait(bar_ld, ph_ld & 1);
-    ++ph_ld;
+  auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
+    ok &= tc::bar_wait(bar, ph & 1);
+    ++ph;
   };
 
   constexpr uint32_t idesc_proj = tc::idesc_f16(C, false, false);
   constexpr uint32_t idesc_gp = tc::idesc_f16(C, false, true);
   constexpr uint32_t idesc_dd = tc::idesc_f16(D, false, false);
   constexpr uint32_t S_s = (D / 8) * 128;      // token step of the feature x token tiles
+  constexpr int kShift = NTH == 32 ? 0 : NTH == 16 ? 1 : NTH == 8 ? 2 : 3;
   const bool gelu = !(p.flags & 1u);
+  float* spart = reinterpret_cast<float*>(sGP);  // per-warp partial sums during [3]
 
   for (int l = 0; l < L; ++l) {
-    // [1] stage W_k^(l), W_p^(l) (hi) by bulk copy; compute beta^(l) meanwhile
-    if (l > 0) wait_mma();                      // previous l's MMAs no longer read shared tiles
-    if (tid == 0) {
-      tc::bar_expect_tx(bar_ld, 2 * S::kW);
-      tc::bulk_g2s(sW, p.wblocks + WeightBlock<D>::index(h, l, L, 0, 0) * S::kW, S::kW, bar_ld);
-      tc::bulk_g2s(sWp, p.wblocks + WeightBlock<D>::index(h, l, L, 1, 0) * S::kW, S::kW, bar_ld);
-    }
-    {
-      const float* wb = p.wbeta + ((size_t)h * L + l) * D;
-      for (int t = warp; t < C; t += 8) {
-        float z = 0.f;
-        for (int cc = lane; cc < D; cc += 32) {
-          const uint32_t off = (cc / 8) * (C * 16u) + t * 16u + (cc % 8) * 2u;
-          const float u = __half2float(*reinterpret_cast<const __half*>(sU + off)) +
-                          __half2float(*reinterpret_cast<const __half*>(sU + S::kU + off));
-          z = fmaf(wb[cc], u, z);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        if (lane == 0) sbl[t] = sigmoidf(z);
+    // [1] W_p^(l) into the [G;P] buffers once the previous step's MMAs are done
+    //     (W_k^(l) was requested as soon as the previous projection finished)
+    if (l > 0) {
+      wait_mma();
+      if (tid == 0) {
+        tc::bar_expect_tx(bar_wp, S::kW);
+        tc::bulk_g2s(sWp, wblock(l, 1, 0), S::kW, bar_wp);
       }
     }
-    wait_ld();
-    __syncthreads();
+    wait_bar(bar_wk, ph_wk);
+    wait_bar(bar_wp, ph_wp);
     // [2] projections: k_hat^T = W_k u^T, p^T = W_p u^T (u = hi + lo)
     if (tid == 0) {
       tc::fence_after();
@@ -358,11 +422,13 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     if (need_lo) {       // weights not exact in fp16: add W_lo u_hi
       wait_mma();
       if (tid == 0) {
-        tc::bar_expect_tx(bar_ld, 2 * S::kW);
-        tc::bulk_g2s(sW, p.wblocks + WeightBlock<D>::index(h, l, L, 0, 1) * S::kW, S::kW, bar_ld);
-        tc::bulk_g2s(sWp, p.wblocks + WeightBlock<D>::index(h, l, L, 1, 1) * S::kW, S::kW, bar_ld);
+        tc::bar_expect_tx(bar_wk, S::kW);
+        tc::bulk_g2s(sW, wblock(l, 0, 1), S::kW, bar_wk);
+        tc::bar_expect_tx(bar_wp, S::kW);
+        tc::bulk_g2s(sWp, wblock(l, 1, 1), S::kW, bar_wp);
       }
-      wait_ld();
+      wait_bar(bar_wk, ph_wk);
+      wait_bar(bar_wp, ph_wp);
       if (tid == 0) {
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t bdesc = tc::desc(sU + kk * 2 * C * 16, C * 16, 128);
@@ -373,7 +439,13 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
       }
     }
     wait_mma();
-    // [3] epilogue: normalise directions, residual step, write factor tiles
+    // the projection has read W_k^(l): stream W_k^(l+1) in behind the epilogues
+    if (tid == 0 && l + 1 < L) {
+      tc::bar_expect_tx(bar_wk, S::kW);
+      tc::bulk_g2s(sW, wblock(l + 1, 0, 0), S::kW, bar_wk);
+    }
+    // [3] epilogue: |k_hat| and the gate logit w_beta . u per token (one reduction),
+    //     then the residual step and the factor tiles
     {
       float kv[NTH];
 #pragma unroll
@@ -383,10 +455,10 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) kv[j + jj] = cvalid ? tmp[jj] : 0.f;
       }
-      // per-token sum of squares over this warp's 32 features (reduce-scatter)
-      float red[NTH];
+      const float wb = cvalid ? p.wbeta[((size_t)h * L + l) * D + c] : 0.f;
+      float rn[NTH], rz[NTH];
 #pragma unroll
-      for (int j = 0; j < NTH; ++j) red[j] = kv[j] * kv[j];
+      for (int j = 0; j < NTH; ++j) { rn[j] = kv[j] * kv[j]; rz[j] = wb * u_reg[j]; }
       int n = NTH;
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1) {
@@ -396,19 +468,30 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
 #pragma unroll
           for (int j = 0; j < NTH / 2; ++j) {
             if (j < hn) {
-              const float send = upper ? red[j] : red[j + hn];
-              const float keep = upper ? red[j + hn] : red[j];
-              red[j] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+              const float sn = upper ? rn[j] : rn[j + hn], kn = upper ? rn[j + hn] : rn[j];
+              const float sz = upper ? rz[j] : rz[j + hn], kz = upper ? rz[j + hn] : rz[j];
+              rn[j] = kn + __shfl_xor_sync(0xffffffffu, sn, m);
+              rz[j] = kz + __shfl_xor_sync(0xffffffffu, sz, m);
             }
           }
           n = hn;
         } else {
-          red[0] += __shfl_xor_sync(0xffffffffu, red[0], m);
+          rn[0] += __shfl_xor_sync(0xffffffffu, rn[0], m);
+          rz[0] += __shfl_xor_sync(0xffffffffu, rz[0], m);
         }
       }
-      constexpr int kShift = NTH == 32 ? 0 : NTH == 16 ? 1 : NTH == 8 ? 2 : 3;
-      if ((lane & ((1 << kShift) - 1)) == 0) snorm[quarter * C + half * NTH + (lane >> kShift)] = red[0];
+      if ((lane & ((1 << kShift) - 1)) == 0) {
+        const int t = half * NTH + (lane >> kShift);
+        spart[quarter * C + t] = rn[0];
+        spart[4 * C + quarter * C + t] = rz[0];
+      }
       __syncthreads();
+      if (tid < C) {
+        const float ss = spart[tid] + spart[C + tid] + spart[2 * C + tid] + spart[3 * C + tid];
+        const float zz = spart[4 * C + tid] + spart[5 * C + tid] + spart[6 * C + tid] + spart[7 * C + tid];
+        sinv[tid] = 1.0f / sqrtf(ss + 1e-6f);
+        sbl[tid] = sigmoidf(zz);
+      }
       float pv[NTH];
 #pragma unroll
       for (int j = 0; j < NTH; j += 8) {
@@ -417,6 +500,7 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) pv[j + jj] = tmp[jj];
       }
+      __syncthreads();
       if (cvalid) {
 #pragma unroll
         for (int j8 = 0; j8 < NTH; j8 += 8) {
@@ -425,10 +509,7 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
           for (int jj = 0; jj < 8; ++jj) {
             const int j = j8 + jj, t = half * NTH + j;
             const bool valid = t < nv;
-            float ss = 0.f;
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) ss += snorm[qq * C + t];
-            const float kd = valid ? kv[j] / sqrtf(ss + 1e-6f) : 0.f;
+            const float kd = valid ? kv[j] * sinv[t] : 0.f;
             const float x = pv[j] * r_reg[j];
             const float dl = gelu ? gelu_erf(x) : x;
             r_reg[j] -= dl;
@@ -474,9 +555,9 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
         __half hh[8], ll[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          const int s = half * NTH + j8 + jj;
+          const int s_ = half * NTH + j8 + jj;
           float val = 0.f;
-          if ((isG && t > s) || (isP && t >= s)) val = expf(gt - sg[s]) * tmp[jj];
+          if ((isG && t > s_) || (isP && t >= s_)) val = expf(gt - sg[s_]) * tmp[jj];
           if (isP) {
             tc::split_f16(val, hh[jj], ll[jj]);
           } else {
@@ -519,8 +600,20 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   float* tgam = tbeta + C;
   unsigned char* sTP = sm + S::tTP;
   unsigned char* sKX = sm + S::tKX;
+  unsigned char* sTB = sm + S::tTB;
   const uint32_t t_w = t_n;                                     // W / PW columns
   const uint32_t t_x = S::kExtraX ? tmem + 2 * C + 2 * D : tmem; // U / PU columns
+  // V rows for X = beta (V - R): thread (token s = row, feature half) loads its 64 values now
+  const int s_tok = row;
+  const bool tok = s_tok < C;
+  const bool tok_valid = tok && s_tok < nv;
+  uint4 vpre[D / 16];
+  {
+    const __nv_bfloat16* vrow = p.v + (((size_t)b * T_ + t0 + (tok_valid ? s_tok : 0)) * H + h) * D + half * (D / 2);
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j)
+      vpre[j] = tok_valid ? *reinterpret_cast<const uint4*>(vrow + j * 8) : make_uint4(0u, 0u, 0u, 0u);
+  }
   // (a) N = N_l to global (its TMEM columns are reused below)
   if (L > 0) {
     float* ndst = p.Nl + (cbase * D + row) * D;
@@ -549,6 +642,35 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
               idesc_proj, kk > 0);
     tc::commit(bar_mma);
   }
+  // (d) meanwhile: X = beta (V - R) and Kb = beta gamma K as the MN-major B tile [Kb | X]:
+  //     (s, f) at (f/8)*(16C) + s*16 + (f%8)*2,  f < D: Kb,  f >= D: X
+  {
+    const float bs = tok ? tbeta[s_tok] : 0.f, gs = tok ? tgam[s_tok] : 0.f;
+#pragma unroll
+    for (int j8 = 0; j8 < D / 2; j8 += 8) {
+      const int f0 = half * (D / 2) + j8;
+      float rr[8];
+      if (L > 0) {
+        tc::ld8(t_ro + lane_base + f0, rr);
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) rr[jj] = 0.f;
+      }
+      if (tok) {
+        __half xh[8], kh[8];
+        const __nv_bfloat16* ve = reinterpret_cast<const __nv_bfloat16*>(&vpre[j8 / 8]);
+        const uint4 kraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + s_tok * 16u);
+        const __half* ke = reinterpret_cast<const __half*>(&kraw);
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          xh[jj] = __float2half_rn(tok_valid ? bs * (__bfloat162float(ve[jj]) - rr[jj]) : 0.f);
+          kh[jj] = __float2half_rn(bs * gs * __half2float(ke[jj]));
+        }
+        *reinterpret_cast<uint4*>(sKX + ((D + f0) / 8) * (16u * C) + s_tok * 16u) = *reinterpret_cast<const uint4*>(xh);
+        *reinterpret_cast<uint4*>(sKX + (f0 / 8) * (16u * C) + s_tok * 16u) = *reinterpret_cast<const uint4*>(kh);
+      }
+    }
+  }
   wait_mma();
   // (c) A = strict_tril(beta (K K^T) (.) Gamma), P = tril(Q K^T (.) Gamma)   (fp32)
   {
@@ -569,52 +691,11 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
       }
     }
   }
-  // (d) X = beta (V - R) and Kb = beta gamma K as the MN-major B tile [Kb | X]:
-  //     (s, f) at (f/8)*(16C) + s*16 + (f%8)*2,  f < D: Kb,  f >= D: X
-  {
-    const int s_ = row;                                        // token (lanes 0..C-1)
-    const bool tok = s_ < C;
-    const float bs = tok ? tbeta[s_] : 0.f, gs = tok ? tgam[s_] : 0.f;
-    const __nv_bfloat16* vrow = p.v + (((size_t)b * T_ + t0 + (tok ? s_ : 0)) * H + h) * D;
-#pragma unroll
-    for (int j8 = 0; j8 < D / 2; j8 += 8) {
-      const int f0 = half * (D / 2) + j8;
-      float rr[8];
-      if (L > 0) {
-        tc::ld8(t_ro + lane_base + f0, rr);
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) rr[jj] = 0.f;
-      }
-      if (tok) {
-        __half xh[8], kh[8];
-        const bool valid = s_ < nv;
-        uint4 vraw = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) vraw = *reinterpret_cast<const uint4*>(vrow + f0);
-        const __nv_bfloat16* ve = reinterpret_cast<const __nv_bfloat16*>(&vraw);
-        const uint4 kraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + s_ * 16u);
-        const __half* ke = reinterpret_cast<const __half*>(&kraw);
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          xh[jj] = __float2half_rn(valid ? bs * (__bfloat162float(ve[jj]) - rr[jj]) : 0.f);
-          kh[jj] = __float2half_rn(bs * gs * __half2float(ke[jj]));
-        }
-        *reinterpret_cast<uint4*>(sKX + ((D + f0) / 8) * (16u * C) + s_ * 16u) = *reinterpret_cast<const uint4*>(xh);
-        *reinterpret_cast<uint4*>(sKX + (f0 / 8) * (16u * C) + s_ * 16u) = *reinterpret_cast<const uint4*>(kh);
-      }
-    }
-  }
   __syncthreads();
-  // (e) T = (I + A)^-1 (fp32), then PT = P T
-  solve_unit_lower<C>(tAf, tTf, tYf);
-  for (int idx = tid; idx < C * C; idx += 256) {
-    const int t = idx / C, j = idx % C;
-    float acc = 0.f;
-    for (int m = j; m <= t; ++m) acc = fmaf(tPf[t * (C + 1) + m], tTf[m * (C + 1) + j], acc);
-    tAf[t * (C + 1) + j] = acc;                                 // PT (A no longer needed)
-  }
-  __syncthreads();
-  // [T ; PT] as fp16 A tile (rows 0..C-1 = T, C..2C-1 = PT, rest 0): (r, s) at (s/8)*2048 + r*16 + (s%8)*2
+  // (e) T = (I + A)^-1 (fp32); then [T ; PT] = [I ; P] T on the tensor core
+  solve_tri<C>(tAf, tTf, tYf);
+  // A tile [I ; P] (fp16, 128 x C, K-major (r, s) at (s/8)*2048 + r*16 + (s%8)*2), rows >= 2C zero;
+  // B tile T (N = j, K = m): (j, m) at (m/8)*(16C) + j*16 + (m%8)*2
   for (int idx = tid; idx < 128 * (C / 8); idx += 256) {
     const int r = idx % 128, s8 = idx / 128;
     __half hv[8];
@@ -622,11 +703,39 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     for (int jj = 0; jj < 8; ++jj) {
       const int j = s8 * 8 + jj;
       float x = 0.f;
-      if (r < C) x = tTf[r * (C + 1) + j];
-      else if (r < 2 * C) x = tAf[(r - C) * (C + 1) + j];
+      if (r < C) x = (r == j) ? 1.f : 0.f;
+      else if (r < 2 * C) x = tPf[(r - C) * (C + 1) + j];
       hv[jj] = __float2half_rn(x);
     }
     *reinterpret_cast<uint4*>(sTP + s8 * 2048u + r * 16u) = *reinterpret_cast<const uint4*>(hv);
+  }
+  for (int idx = tid; idx < C * (C / 8); idx += 256) {
+    const int j = idx % C, m8 = idx / C;
+    __half hv[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) hv[jj] = __float2half_rn(tTf[(m8 * 8 + jj) * (C + 1) + j]);
+    *reinterpret_cast<uint4*>(sTB + m8 * (16u * C) + j * 16u) = *reinterpret_cast<const uint4*>(hv);
+  }
+  tc::fence_smem_to_async();
+  tc::fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    tc::fence_after();
+    for (int kk = 0; kk < C / 16; ++kk)
+      tc::mma(t_proj, tc::desc(sTP + kk * 4096, 2048, 128), tc::desc(sTB + kk * 2 * 16 * C, 16 * C, 128),
+              idesc_proj, kk > 0);
+    tc::commit(bar_mma);
+  }
+  wait_mma();
+  // [T ; PT] back into the A tile (fp16)
+#pragma unroll
+  for (int j8 = 0; j8 < NTH; j8 += 8) {
+    float tmp[8];
+    tc::ld8(t_proj + lane_base + half * NTH + j8, tmp);
+    __half hv[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) hv[jj] = __float2half_rn(tmp[jj]);
+    *reinterpret_cast<uint4*>(sTP + ((half * NTH + j8) / 8) * 2048u + row * 16u) = *reinterpret_cast<const uint4*>(hv);
   }
   tc::fence_smem_to_async();
   tc::fence_before();

@@ -159,12 +159,14 @@ T* region(void* ws, const Layout& Lo, int r) {
                               : reinterpret_cast<T*>(static_cast<unsigned char*>(ws) + Lo.off[r]);
 }
 
-// Scan tile height: more, thinner tiles when there are few sequences.
+// Scan tile height (rows of S per CTA): 16-row tiles while the whole grid fits in
+// one wave of CTAs, else 32-row tiles (fewer waves, less re-reading of the
+// chunk maps shared by a head's tiles).
 int pick_bv(const prism_dims* d) {
   const int D = d->d_k;
   if (D < 32) return 16;
   const long long seqs = (long long)d->B * d->H;
-  return seqs * (D / 32) >= 2 * 152 ? 32 : 16;
+  return seqs * (D / 16) > 152 ? 32 : 16;
 }
 
 }  // namespace

@@ -40,8 +40,12 @@ template <int D, int C, int BV>
 struct ScanSmem {
   static constexpr int NW = 4;                          // warps per CTA
   static constexpr int LDD = D + 8, LDB = BV + 8;
+  static constexpr int LDU = BV + 4;                    // fp32 tile rows (U, O_intra)
+  static constexpr int LDN = D + 4;                     // fp32 tile rows (N)
   static constexpr uint32_t kTile = C * LDD * 2;        // one C x D fp16 tile
-  static constexpr uint32_t kBuf = 4 * kTile;           // W, Kt, Qt hi, Qt lo
+  static constexpr uint32_t kU = C * LDU * 4;           // C x BV fp32
+  static constexpr uint32_t kN = BV * LDN * 4;          // BV x D fp32
+  static constexpr uint32_t kBuf = 4 * kTile + 2 * kU + kN;   // W, Kt, Qt hi, Qt lo, U, O_intra, N
   static constexpr uint32_t oBuf0 = 0;
   static constexpr uint32_t oBuf1 = kBuf;
   static constexpr uint32_t oS0 = 2 * kBuf;             // hi, lo [BV][LDD]
@@ -86,10 +90,26 @@ __global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
     unsigned char* base = sm + (buf ? S::oBuf1 : S::oBuf0);
     const size_t off = (cb0 + c) * (size_t)C * D;
     const __half* src[4] = {p.Wc + off, p.Kt + off, p.Qth + off, p.Qtl + off};
-    constexpr int V = D / 8;                            // 16-byte pieces per row
+    constexpr int V = D / 8;                            // 16-byte pieces per fp16 row
     for (int idx = tid; idx < 4 * C * V; idx += NW * 32) {
       const int m = idx / (C * V), rem = idx % (C * V), r = rem / V, v8 = rem % V;
       cp_async16(base + m * S::kTile + (r * LDD + v8 * 8) * 2, src[m] + (size_t)r * D + v8 * 8);
+    }
+    // this tile's columns of U and O_intra (fp32 C x BV) and rows of N (fp32 BV x D)
+    constexpr int VU = BV / 4, VN = D / 4;
+    unsigned char* su = base + 4 * S::kTile;
+    for (int idx = tid; idx < 2 * C * VU; idx += NW * 32) {
+      const int m = idx / (C * VU), rem = idx % (C * VU), r = rem / VU, v4 = rem % VU;
+      const float* g = (m == 0 ? p.U : p.Oi) + off + (size_t)r * D + r0 + v4 * 4;
+      cp_async16(su + m * S::kU + (r * S::LDU + v4 * 4) * 4, g);
+    }
+    if (p.Nl) {
+      unsigned char* sn = su + 2 * S::kU;
+      const float* g0 = p.Nl + ((cb0 + c) * D + r0) * (size_t)D;
+      for (int idx = tid; idx < BV * VN; idx += NW * 32) {
+        const int r = idx / VN, v4 = idx % VN;
+        cp_async16(sn + (r * S::LDN + v4 * 4) * 4, g0 + (size_t)r * D + v4 * 4);
+      }
     }
   };
 
@@ -117,6 +137,12 @@ __global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
           sS0l[o] = __float2half_rn(x - __half2float(hi));
         }
     }
+    cp_async_wait<1>();
+    __syncthreads();
+    const unsigned char* bufp = sm + (buf ? S::oBuf1 : S::oBuf0);
+    const float* sUt = reinterpret_cast<const float*>(bufp + 4 * S::kTile);
+    const float* sOt = sUt + C * S::LDU;
+    const float* sNt = sOt + C * S::LDU;
     // S <- gamma_C S0 + N (the E^T Kt term is added below)
     const float gC = p.gC[cbase];
 #pragma unroll
@@ -128,14 +154,11 @@ __global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
 #pragma unroll
         for (int e = 0; e < 4; e += 2) {
           float2 nn = make_float2(0.f, 0.f);
-          if (p.Nl) nn = *reinterpret_cast<const float2*>(
-                        p.Nl + (cbase * D + r0 + m0 + acc_row(e)) * D + n0 + acc_col(hh, e));
+          if (p.Nl) nn = *reinterpret_cast<const float2*>(sNt + (m0 + acc_row(e)) * S::LDN + n0 + acc_col(hh, e));
           accS[i].v[hh][e] = fmaf(gC, accS[i].v[hh][e], nn.x);
           accS[i].v[hh][e + 1] = fmaf(gC, accS[i].v[hh][e + 1], nn.y);
         }
     }
-    cp_async_wait<1>();
-    __syncthreads();
     const __half* sW = reinterpret_cast<const __half*>(sm + (buf ? S::oBuf1 : S::oBuf0));
     const __half* sKt = sW + C * LDD;
     const __half* sQh = sKt + C * LDD;
@@ -158,9 +181,8 @@ __global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
 #pragma unroll
         for (int e2 = 0; e2 < 4; e2 += 2) {
           const int t = m0 + acc_row(e2), col = n0 + acc_col(hh, e2);
-          const size_t g = (cbase * C + t) * D + r0 + col;
-          const float2 u = *reinterpret_cast<const float2*>(p.U + g);
-          const float2 oi = *reinterpret_cast<const float2*>(p.Oi + g);
+          const float2 u = *reinterpret_cast<const float2*>(sUt + t * S::LDU + col);
+          const float2 oi = *reinterpret_cast<const float2*>(sOt + t * S::LDU + col);
           sE[t * LDB + col] = __float2half_rn(u.x - e.v[hh][e2]);
           sE[t * LDB + col + 1] = __float2half_rn(u.y - e.v[hh][e2 + 1]);
           if (t < nv) {
