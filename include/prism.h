@@ -98,6 +98,10 @@ enum {
     PRISM_WS_COUNT = 12
 };
 
+/* Inside one chunk, the PRISM_BF16 per-chunk arrays (R rows x d features) are
+ * stored in 16-byte column pieces: element (r, f) at ((f / V) * R + r) * V + f % V
+ * with V = 16 / element size (8 for fp16, 4 for fp32); N uses R = d. */
+
 /* Bytes of device workspace for these dims (0 if the dims are invalid). */
 PRISM_API size_t prism_workspace_bytes(const prism_dims* dims);
 

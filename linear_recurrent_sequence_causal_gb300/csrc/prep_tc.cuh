@@ -51,7 +51,10 @@ struct PrepArgs {
   const unsigned char* wblocks;   // fp16 weight blocks laid out for the A operand
   const int* wflag;               // nonzero: weights need their lo halves
   const int* seq_lens;
-  // per-chunk outputs, chunk-major [B][H][NC][...]
+  // Per-chunk outputs, chunk-major [B][H][NC][...].  Inside a chunk each array is
+  // stored "piece-major": 16-byte column pieces, rows contiguous within a piece:
+  // element (r, f) of an R-row array at ((f / V) * R + r) * V + f % V, V = 16 / elem
+  // size.  A warp whose lanes hold consecutive rows then writes 512 contiguous bytes.
   __half* Wc;                     // [C][D]  W = T diag(beta gamma) K
   __half* Kt;                     // [C][D]  Kt = diag(gamma_C / gamma) K
   __half* Qth;                    // [C][D]  Qt = diag(gamma) Q - P W, hi half
@@ -170,7 +173,8 @@ struct PrepSmem {
   static constexpr Place p7 = p7a.at(sTB);
   static constexpr uint32_t bytes = p7.o2 > loop_end ? p7.o2 : loop_end;
   static constexpr bool kExtraX = D > 2 * C;             // U/PU need their own TMEM columns
-  static constexpr uint32_t tmem_cols_needed = 2 * C + 2 * D + (kExtraX ? D : 0);
+  // columns: k_hat | p | [R;O_l] | N_l | r, u (refinement loop) or U/PU (tail, when D > 2C)
+  static constexpr uint32_t tmem_cols_needed = 2 * C + 2 * D + (kExtraX ? D : 2 * C);
   static constexpr uint32_t tmem_cols =
       tmem_cols_needed <= 32 ? 32 : tmem_cols_needed <= 64 ? 64 : tmem_cols_needed <= 128 ? 128
                                   : tmem_cols_needed <= 256 ? 256 : 512;
@@ -205,23 +209,46 @@ __device__ __forceinline__ void solve_tri(const float* sA, float* sT, float* sY)
     for (int i = 0; i < 16; ++i) sT[(o + i) * LD + o + j] = col[i];
   }
   __syncthreads();
+  // Off-diagonal blocks by level (distance lev = i - j).  At one level every
+  // block has the same inner length 16*lev, so a thread walks its (up to
+  // NB-1) elements in lockstep: independent FMA chains instead of one long one.
+  const int r = (tid & 255) / 16, cc = tid % 16;
   for (int lev = 1; lev < NB; ++lev) {
-    const int nblk = NB - lev;                       // blocks (i, j = i - lev)
-    // Y = sum_{k=j}^{i-1} A_ik T_kj
-    for (int idx = tid; idx < nblk * 256; idx += 256) {
-      const int bi = idx / 256 + lev, bj = bi - lev, r = (idx % 256) / 16, c = idx % 16;
-      float acc = 0.f;
-      for (int m = bj * 16; m < bi * 16; ++m) acc = fmaf(sA[(bi * 16 + r) * LD + m], sT[m * LD + bj * 16 + c], acc);
-      sY[idx] = acc;
+    const int nblk = NB - lev;                       // blocks (i = lev + e, j = e)
+    if (tid < 256) {
+      float acc[NB > 1 ? NB - 1 : 1];
+#pragma unroll
+      for (int e = 0; e < NB - 1; ++e) acc[e] = 0.f;
+#pragma unroll 4
+      for (int mo = 0; mo < 16 * lev; ++mo) {
+#pragma unroll
+        for (int e = 0; e < NB - 1; ++e)
+          if (e < nblk) {
+            const int bi = lev + e, bj = e;
+            acc[e] = fmaf(sA[(bi * 16 + r) * LD + bj * 16 + mo], sT[(bj * 16 + mo) * LD + bj * 16 + cc], acc[e]);
+          }
+      }
+#pragma unroll
+      for (int e = 0; e < NB - 1; ++e)
+        if (e < nblk) sY[e * 256 + r * 16 + cc] = acc[e];
     }
     __syncthreads();
-    for (int idx = tid; idx < nblk * 256; idx += 256) {
-      const int bi = idx / 256 + lev, bj = bi - lev, r = (idx % 256) / 16, c = idx % 16;
-      const float* Yb = sY + (idx / 256) * 256;
-      float acc = 0.f;
+    if (tid < 256) {
+      float acc[NB > 1 ? NB - 1 : 1];
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc = fmaf(sT[(bi * 16 + r) * LD + bi * 16 + m], Yb[m * 16 + c], acc);
-      sT[(bi * 16 + r) * LD + bj * 16 + c] = -acc;
+      for (int e = 0; e < NB - 1; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+#pragma unroll
+        for (int e = 0; e < NB - 1; ++e)
+          if (e < nblk) {
+            const int bi = lev + e;
+            acc[e] = fmaf(sT[(bi * 16 + r) * LD + bi * 16 + m], sY[e * 256 + m * 16 + cc], acc[e]);
+          }
+      }
+#pragma unroll
+      for (int e = 0; e < NB - 1; ++e)
+        if (e < nblk) sT[((lev + e) * 16 + r) * LD + e * 16 + cc] = -acc[e];
     }
     __syncthreads();
   }
@@ -298,30 +325,46 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     __syncwarp();
     for (int i = lane; i < C; i += 32) sdec[i] = expf(sg[C - 1] - sg[i]);
   }
-  // [K ; Q] rows as fp16: (row, a) at (a/8)*2048 + row*16 + (a%8)*2
-  for (int idx = tid; idx < 128 * (D / 8); idx += 256) {
-    const int r = idx % 128, a8 = idx / 128;
-    uint4 outv = make_uint4(0u, 0u, 0u, 0u);
-    const int t = r < C ? r : r - C;
-    if (r < 2 * C && t < nv) {
-      const __nv_bfloat16* src = (r < C ? p.k : p.q) + (((size_t)b * T_ + t0 + t) * H + h) * D + a8 * 8;
-      const uint4 raw = *reinterpret_cast<const uint4*>(src);
-      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
-      __half hv[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) hv[j] = __float2half_rn(__bfloat162float(e[j]));
-      outv = *reinterpret_cast<const uint4*>(hv);
-    }
-    *reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u) = outv;
-  }
-  // v window, rows t0-w .. t0+C-1 as bf16 [C + w][D] (zero outside [0, len)), in the D tiles
+  // [K ; Q] rows as fp16: (row, a) at (a/8)*2048 + row*16 + (a%8)*2, and the v window,
+  // rows t0-w .. t0+C-1 as bf16 [C + w][D] (zero outside [0, len)), in the D tiles.
+  // All global loads are issued before any is used.
   __nv_bfloat16* vwin = reinterpret_cast<__nv_bfloat16*>(sD);
-  for (int idx = tid; idx < (C + w) * (D / 8); idx += 256) {
-    const int rr = idx / (D / 8), c8 = idx % (D / 8);
-    const int t = t0 - w + rr;
-    uint4 x = make_uint4(0u, 0u, 0u, 0u);
-    if (t >= 0 && t < len) x = *reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t) * H + h) * D + c8 * 8);
-    *reinterpret_cast<uint4*>(vwin + rr * D + c8 * 8) = x;
+  {
+    constexpr int NKQ = (128 * (D / 8) + 255) / 256;
+    constexpr int NVW = ((C + 8) * (D / 8) + 255) / 256;
+    uint4 kq[NKQ], vw[NVW];
+#pragma unroll
+    for (int i = 0; i < NKQ; ++i) {
+      const int idx = tid + i * 256, r = idx % 128, a8 = idx / 128;
+      const int t = r < C ? r : r - C;
+      kq[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (idx < 128 * (D / 8) && r < 2 * C && t < nv)
+        kq[i] = *reinterpret_cast<const uint4*>((r < C ? p.k : p.q) + (((size_t)b * T_ + t0 + t) * H + h) * D + a8 * 8);
+    }
+#pragma unroll
+    for (int i = 0; i < NVW; ++i) {
+      const int idx = tid + i * 256, rr = idx / (D / 8), c8 = idx % (D / 8);
+      const int t = t0 - w + rr;
+      vw[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (rr < C + w && t >= 0 && t < len)
+        vw[i] = *reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t) * H + h) * D + c8 * 8);
+    }
+#pragma unroll
+    for (int i = 0; i < NKQ; ++i) {
+      const int idx = tid + i * 256, r = idx % 128, a8 = idx / 128;
+      if (idx < 128 * (D / 8)) {
+        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&kq[i]);
+        __half hv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) hv[j] = __float2half_rn(__bfloat162float(e[j]));
+        *reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u) = *reinterpret_cast<const uint4*>(hv);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NVW; ++i) {
+      const int idx = tid + i * 256, rr = idx / (D / 8), c8 = idx % (D / 8);
+      if (rr < C + w) *reinterpret_cast<uint4*>(vwin + rr * D + c8 * 8) = vw[i];
+    }
   }
   // rows D..127 of the scaled-write tiles stay zero (A operand of the injection)
   if constexpr (D < 128)
@@ -331,19 +374,26 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
       const int r = D + rem % (128 - D), s8 = rem / (128 - D);
       *reinterpret_cast<uint4*>(sDt + part * S::kF128 + s8 * 2048u + r * 16u) = make_uint4(0u, 0u, 0u, 0u);
     }
+  tc::fence_before();
   __syncthreads();
 
-  // ---- anchor u = sum_j c_j (.) v_{t-j}; u and the residual r = v - u stay in registers ----
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t t_proj = tmem, t_p = tmem + C, t_ro = tmem + 2 * C, t_n = tmem + 2 * C + D;
+  const uint32_t t_r = tmem + 2 * C + 2 * D, t_u = t_r + C;   // residual r and anchor u
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+
+  // ---- anchor u = sum_j c_j (.) v_{t-j} and residual r = v - u, kept in TMEM ----
   // thread (feature c = row, token half) owns tokens [half*NTH, half*NTH + NTH)
   const int c = row;
   const bool cvalid = c < D;
-  float r_reg[NTH], u_reg[NTH];
   {
     float taps[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) taps[j] = (cvalid && j < w) ? p.conv_w[((size_t)h * w + j) * D + c] : 0.f;
-#pragma unroll
+#pragma unroll 1
     for (int j8 = 0; j8 < NTH; j8 += 8) {
+      float uu[8], rr[8];
       __half uh[8], ul[8];
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) {
@@ -355,8 +405,8 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
             if (j <= w) u = fmaf(taps[j - 1], __bfloat162float(vwin[(tl + w - j) * D + c]), u);
           vt = __bfloat162float(vwin[(tl + w) * D + c]);
         }
-        u_reg[j8 + jj] = u;
-        r_reg[j8 + jj] = (tl < nv) ? vt - u : 0.f;
+        uu[jj] = u;
+        rr[jj] = (tl < nv) ? vt - u : 0.f;
         tc::split_f16(u, uh[jj], ul[jj]);
         if (cvalid) {
           // U tile (B operand, N = tokens, K = features): (t, c) at (c/8)*(C*16) + t*16 + (c%8)*2
@@ -365,15 +415,14 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
           *reinterpret_cast<__half*>(sU + S::kU + off) = ul[jj];
         }
       }
+      tc::st8(t_u + lane_base + half * NTH + j8, uu);
+      tc::st8(t_r + lane_base + half * NTH + j8, rr);
     }
   }
   tc::fence_smem_to_async();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  const uint32_t tmem = *tslot;
-  const uint32_t t_proj = tmem, t_p = tmem + C, t_ro = tmem + 2 * C, t_n = tmem + 2 * C + D;
-  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
 
   uint32_t ph_mma = 0, ph_wk = 0, ph_wp = 0;
   bool ok = true;
@@ -391,7 +440,6 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   constexpr uint32_t idesc_gp = tc::idesc_f16(C, false, true);
   constexpr uint32_t idesc_dd = tc::idesc_f16(D, false, false);
   constexpr uint32_t S_s = (D / 8) * 128;      // token step of the feature x token tiles
-  constexpr int kShift = NTH == 32 ? 0 : NTH == 16 ? 1 : NTH == 8 ? 2 : 3;
   const bool gelu = !(p.flags & 1u);
   float* spart = reinterpret_cast<float*>(sGP);  // per-warp partial sums during [3]
 
@@ -444,46 +492,46 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
       tc::bar_expect_tx(bar_wk, S::kW);
       tc::bulk_g2s(sW, wblock(l + 1, 0, 0), S::kW, bar_wk);
     }
-    // [3] epilogue: |k_hat| and the gate logit w_beta . u per token (one reduction),
-    //     then the residual step and the factor tiles
+    // [3] epilogue.  Pass A: per token |k_hat|^2 and the gate logit w_beta . u,
+    //     summed over this warp's 32 features (reduce-scatter over 8-token groups).
     {
-      float kv[NTH];
-#pragma unroll
-      for (int j = 0; j < NTH; j += 8) {
-        float tmp[8];
-        tc::ld8(t_proj + lane_base + half * NTH + j, tmp);
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) kv[j + jj] = cvalid ? tmp[jj] : 0.f;
-      }
       const float wb = cvalid ? p.wbeta[((size_t)h * L + l) * D + c] : 0.f;
-      float rn[NTH], rz[NTH];
+#pragma unroll 1
+      for (int j8 = 0; j8 < NTH; j8 += 8) {
+        float kv[8], uv[8], rn[8], rz[8];
+        tc::ld8(t_proj + lane_base + half * NTH + j8, kv);
+        tc::ld8(t_u + lane_base + half * NTH + j8, uv);
 #pragma unroll
-      for (int j = 0; j < NTH; ++j) { rn[j] = kv[j] * kv[j]; rz[j] = wb * u_reg[j]; }
-      int n = NTH;
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) {
-        if (n > 1) {
-          const int hn = n / 2;
-          const bool upper = lane & m;
-#pragma unroll
-          for (int j = 0; j < NTH / 2; ++j) {
-            if (j < hn) {
-              const float sn = upper ? rn[j] : rn[j + hn], kn = upper ? rn[j + hn] : rn[j];
-              const float sz = upper ? rz[j] : rz[j + hn], kz = upper ? rz[j + hn] : rz[j];
-              rn[j] = kn + __shfl_xor_sync(0xffffffffu, sn, m);
-              rz[j] = kz + __shfl_xor_sync(0xffffffffu, sz, m);
-            }
-          }
-          n = hn;
-        } else {
-          rn[0] += __shfl_xor_sync(0xffffffffu, rn[0], m);
-          rz[0] += __shfl_xor_sync(0xffffffffu, rz[0], m);
+        for (int jj = 0; jj < 8; ++jj) {
+          rn[jj] = cvalid ? kv[jj] * kv[jj] : 0.f;
+          rz[jj] = wb * uv[jj];
         }
-      }
-      if ((lane & ((1 << kShift) - 1)) == 0) {
-        const int t = half * NTH + (lane >> kShift);
-        spart[quarter * C + t] = rn[0];
-        spart[4 * C + quarter * C + t] = rz[0];
+        int n = 8;
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+          if (n > 1) {
+            const int hn = n / 2;
+            const bool upper = lane & m;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (j < hn) {
+                const float sn = upper ? rn[j] : rn[j + hn], kn = upper ? rn[j + hn] : rn[j];
+                const float sz = upper ? rz[j] : rz[j + hn], kz = upper ? rz[j + hn] : rz[j];
+                rn[j] = kn + __shfl_xor_sync(0xffffffffu, sn, m);
+                rz[j] = kz + __shfl_xor_sync(0xffffffffu, sz, m);
+              }
+            }
+            n = hn;
+          } else {
+            rn[0] += __shfl_xor_sync(0xffffffffu, rn[0], m);
+            rz[0] += __shfl_xor_sync(0xffffffffu, rz[0], m);
+          }
+        }
+        if ((lane & 3) == 0) {                  // lane holds token j8 + lane/4 of its half
+          const int t = half * NTH + j8 + (lane >> 2);
+          spart[quarter * C + t] = rn[0];
+          spart[4 * C + quarter * C + t] = rz[0];
+        }
       }
       __syncthreads();
       if (tid < C) {
@@ -492,32 +540,30 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
         sinv[tid] = 1.0f / sqrtf(ss + 1e-6f);
         sbl[tid] = sigmoidf(zz);
       }
-      float pv[NTH];
-#pragma unroll
-      for (int j = 0; j < NTH; j += 8) {
-        float tmp[8];
-        tc::ld8(t_p + lane_base + half * NTH + j, tmp);
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) pv[j + jj] = tmp[jj];
-      }
       __syncthreads();
-      if (cvalid) {
+      // Pass B: directions, residual step, factor tiles
+#pragma unroll 1
+      for (int j8 = 0; j8 < NTH; j8 += 8) {
+        float kv[8], pv[8], rr[8];
+        tc::ld8(t_proj + lane_base + half * NTH + j8, kv);
+        tc::ld8(t_p + lane_base + half * NTH + j8, pv);
+        tc::ld8(t_r + lane_base + half * NTH + j8, rr);
+        __half kh[8], kl[8], dh[8], dlo[8], th[8], tl[8];
 #pragma unroll
-        for (int j8 = 0; j8 < NTH; j8 += 8) {
-          __half kh[8], kl[8], dh[8], dlo[8], th[8], tl[8];
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int j = j8 + jj, t = half * NTH + j;
-            const bool valid = t < nv;
-            const float kd = valid ? kv[j] * sinv[t] : 0.f;
-            const float x = pv[j] * r_reg[j];
-            const float dl = gelu ? gelu_erf(x) : x;
-            r_reg[j] -= dl;
-            const float dval = valid ? sbl[t] * dl : 0.f;
-            tc::split_f16(kd, kh[jj], kl[jj]);
-            tc::split_f16(dval, dh[jj], dlo[jj]);
-            tc::split_f16(dval * sdec[t], th[jj], tl[jj]);
-          }
+        for (int jj = 0; jj < 8; ++jj) {
+          const int t = half * NTH + j8 + jj;
+          const bool valid = cvalid && t < nv;
+          const float kd = valid ? kv[jj] * sinv[t] : 0.f;
+          const float x = pv[jj] * rr[jj];
+          const float dl = gelu ? gelu_erf(x) : x;
+          rr[jj] -= dl;
+          const float dval = valid ? sbl[t] * dl : 0.f;
+          tc::split_f16(kd, kh[jj], kl[jj]);
+          tc::split_f16(dval, dh[jj], dlo[jj]);
+          tc::split_f16(dval * sdec[t], th[jj], tl[jj]);
+        }
+        tc::st8(t_r + lane_base + half * NTH + j8, rr);
+        if (cvalid) {
           // feature x token tiles: (f, s) at (s/8)*S_s + f*16 + (s%8)*2  (f < D)
           const uint32_t off = ((half * NTH + j8) / 8) * S_s + c * 16u;
           *reinterpret_cast<uint4*>(sKl + off) = *reinterpret_cast<const uint4*>(kh);
@@ -548,7 +594,7 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
       const bool isG = row < C, isP = row >= C && row < 2 * C;
       const int t = isG ? row : row - C;
       const float gt = (isG || isP) ? sg[t] : 0.f;
-#pragma unroll
+#pragma unroll 1
       for (int j8 = 0; j8 < NTH; j8 += 8) {
         float tmp[8];
         tc::ld8(t_proj + lane_base + half * NTH + j8, tmp);
@@ -603,28 +649,20 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   unsigned char* sTB = sm + S::tTB;
   const uint32_t t_w = t_n;                                     // W / PW columns
   const uint32_t t_x = S::kExtraX ? tmem + 2 * C + 2 * D : tmem; // U / PU columns
-  // V rows for X = beta (V - R): thread (token s = row, feature half) loads its 64 values now
   const int s_tok = row;
   const bool tok = s_tok < C;
   const bool tok_valid = tok && s_tok < nv;
-  uint4 vpre[D / 16];
-  {
-    const __nv_bfloat16* vrow = p.v + (((size_t)b * T_ + t0 + (tok_valid ? s_tok : 0)) * H + h) * D + half * (D / 2);
-#pragma unroll
-    for (int j = 0; j < D / 16; ++j)
-      vpre[j] = tok_valid ? *reinterpret_cast<const uint4*>(vrow + j * 8) : make_uint4(0u, 0u, 0u, 0u);
-  }
   // (a) N = N_l to global (its TMEM columns are reused below)
   if (L > 0) {
-    float* ndst = p.Nl + (cbase * D + row) * D;
-#pragma unroll
+    float* nbase = p.Nl + cbase * D * D;      // piece-major: (c, a) at ((a/4)*D + c)*4 + a%4
+#pragma unroll 1
     for (int j8 = 0; j8 < D / 2; j8 += 8) {
       float tmp[8];
       tc::ld8(t_n + lane_base + half * (D / 2) + j8, tmp);
       if (cvalid) {
-        float4* d4 = reinterpret_cast<float4*>(ndst + half * (D / 2) + j8);
-        d4[0] = make_float4(tmp[0], tmp[1], tmp[2], tmp[3]);
-        d4[1] = make_float4(tmp[4], tmp[5], tmp[6], tmp[7]);
+        const int a0 = half * (D / 2) + j8;
+        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4) * D + row) * 4) = make_float4(tmp[0], tmp[1], tmp[2], tmp[3]);
+        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4 + 1) * D + row) * 4) = make_float4(tmp[4], tmp[5], tmp[6], tmp[7]);
       }
     }
   }
@@ -646,7 +684,7 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   //     (s, f) at (f/8)*(16C) + s*16 + (f%8)*2,  f < D: Kb,  f >= D: X
   {
     const float bs = tok ? tbeta[s_tok] : 0.f, gs = tok ? tgam[s_tok] : 0.f;
-#pragma unroll
+#pragma unroll 1
     for (int j8 = 0; j8 < D / 2; j8 += 8) {
       const int f0 = half * (D / 2) + j8;
       float rr[8];
@@ -658,7 +696,9 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
       }
       if (tok) {
         __half xh[8], kh[8];
-        const __nv_bfloat16* ve = reinterpret_cast<const __nv_bfloat16*>(&vpre[j8 / 8]);
+        uint4 vraw = make_uint4(0u, 0u, 0u, 0u);
+        if (tok_valid) vraw = *reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t0 + s_tok) * H + h) * D + f0);
+        const __nv_bfloat16* ve = reinterpret_cast<const __nv_bfloat16*>(&vraw);
         const uint4 kraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + s_tok * 16u);
         const __half* ke = reinterpret_cast<const __half*>(&kraw);
 #pragma unroll
@@ -676,7 +716,7 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   {
     const bool isA = row < C, isP = row >= C && row < 2 * C;
     const int t = isA ? row : row - C;
-#pragma unroll
+#pragma unroll 1
     for (int j8 = 0; j8 < NTH; j8 += 8) {
       float tmp[8];
       tc::ld8(t_proj + lane_base + half * NTH + j8, tmp);
@@ -728,7 +768,7 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   }
   wait_mma();
   // [T ; PT] back into the A tile (fp16)
-#pragma unroll
+#pragma unroll 1
   for (int j8 = 0; j8 < NTH; j8 += 8) {
     float tmp[8];
     tc::ld8(t_proj + lane_base + half * NTH + j8, tmp);
@@ -757,10 +797,11 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   {
     const bool isT = row < C, isPT = row >= C && row < 2 * C;
     const int t = isT ? row : row - C;
-    const size_t rbase = (cbase * C + (isT || isPT ? t : 0)) * D;
+    const size_t cb = cbase * C * D;         // piece-major chunk base
+    const int tr = (isT || isPT) ? t : 0;
     const float gt = (isT || isPT) ? tgam[t] : 0.f;
     const float dct = (isT || isPT) ? sdec[t] : 0.f;
-#pragma unroll
+#pragma unroll 1
     for (int j8 = 0; j8 < D / 2; j8 += 8) {
       const int f0 = half * (D / 2) + j8;
       float wv[8], xv[8], ov[8];
@@ -781,22 +822,24 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
           wh[jj] = __float2half_rn(wv[jj]);
           kth[jj] = __float2half_rn(dct * __half2float(ke[jj]));
         }
-        *reinterpret_cast<uint4*>(p.Wc + rbase + f0) = *reinterpret_cast<const uint4*>(wh);
-        *reinterpret_cast<uint4*>(p.Kt + rbase + f0) = *reinterpret_cast<const uint4*>(kth);
-        float4* u4 = reinterpret_cast<float4*>(p.U + rbase + f0);
-        u4[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
-        u4[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+        const size_t o16 = cb + ((size_t)(f0 / 8) * C + tr) * 8;     // fp16 piece (8 values)
+        *reinterpret_cast<uint4*>(p.Wc + o16) = *reinterpret_cast<const uint4*>(wh);
+        *reinterpret_cast<uint4*>(p.Kt + o16) = *reinterpret_cast<const uint4*>(kth);
+        *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4) * C + tr) * 4) = make_float4(xv[0], xv[1], xv[2], xv[3]);
+        *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4 + 1) * C + tr) * 4) = make_float4(xv[4], xv[5], xv[6], xv[7]);
       } else if (isPT) {
         __half qh[8], ql[8];
         const uint4 qraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + row * 16u);
         const __half* qe = reinterpret_cast<const __half*>(&qraw);
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) tc::split_f16(gt * __half2float(qe[jj]) - wv[jj], qh[jj], ql[jj]);
-        *reinterpret_cast<uint4*>(p.Qth + rbase + f0) = *reinterpret_cast<const uint4*>(qh);
-        *reinterpret_cast<uint4*>(p.Qtl + rbase + f0) = *reinterpret_cast<const uint4*>(ql);
-        float4* o4 = reinterpret_cast<float4*>(p.Oi + rbase + f0);
-        o4[0] = make_float4(xv[0] + ov[0], xv[1] + ov[1], xv[2] + ov[2], xv[3] + ov[3]);
-        o4[1] = make_float4(xv[4] + ov[4], xv[5] + ov[5], xv[6] + ov[6], xv[7] + ov[7]);
+        const size_t o16 = cb + ((size_t)(f0 / 8) * C + tr) * 8;
+        *reinterpret_cast<uint4*>(p.Qth + o16) = *reinterpret_cast<const uint4*>(qh);
+        *reinterpret_cast<uint4*>(p.Qtl + o16) = *reinterpret_cast<const uint4*>(ql);
+        *reinterpret_cast<float4*>(p.Oi + cb + ((size_t)(f0 / 4) * C + tr) * 4) =
+            make_float4(xv[0] + ov[0], xv[1] + ov[1], xv[2] + ov[2], xv[3] + ov[3]);
+        *reinterpret_cast<float4*>(p.Oi + cb + ((size_t)(f0 / 4 + 1) * C + tr) * 4) =
+            make_float4(xv[4] + ov[4], xv[5] + ov[5], xv[6] + ov[6], xv[7] + ov[7]);
       }
     }
     if (tid == 0) p.gC[cbase] = tgam[C - 1];

@@ -123,6 +123,27 @@ __device__ __forceinline__ void tile_mma16(Acc16& acc, const H16* a, int lda, co
   }
 }
 
+// Same product with operands addressed through functors: a(m0_row, k_col) and
+// b(...) return the shared address of the 16-byte ldmatrix row the lane loads.
+//   AMode 0: A row-major,  address of (row m, cols k..k+7)    -> ldmatrix
+//   AMode 1: A transposed, address of (row k, cols m..m+7)    -> ldmatrix.trans
+//   BMode 0: B stored N x K, address of (row n, cols k..k+7)  -> ldmatrix
+//   BMode 1: B stored K x N, address of (row k, cols n..n+7)  -> ldmatrix.trans
+template <int AMode, int BMode, class AF, class BF>
+__device__ __forceinline__ void tile_mma_f16(Acc16& acc, AF a, BF b, int m0, int n0, int K) {
+  const int lane = threadIdx.x & 31;
+  const int j = lane >> 3, r = lane & 7;
+  for (int k0 = 0; k0 < K; k0 += 16) {
+    uint32_t af[4], bf[4];
+    if (AMode == 0) ldsm_x4(a(m0 + r + 8 * (j & 1), k0 + 8 * (j >> 1)), af);
+    else            ldsm_x4_t(a(k0 + r + 8 * (j >> 1), m0 + 8 * (j & 1)), af);
+    if (BMode == 0) ldsm_x4(b(n0 + r + 8 * (j >> 1), k0 + 8 * (j & 1)), bf);
+    else            ldsm_x4_t(b(k0 + r + 8 * (j & 1), n0 + 8 * (j >> 1)), bf);
+    mma_f16_16816(acc.v[0], af, bf[0], bf[1]);
+    mma_f16_16816(acc.v[1], af, bf[2], bf[3]);
+  }
+}
+
 template <bool A_T, bool B_NK>
 __device__ __forceinline__ void tile_mma(Acc16& acc, const __nv_bfloat16* a, int lda,
                                          const __nv_bfloat16* b, int ldb, int m0, int n0, int K) {

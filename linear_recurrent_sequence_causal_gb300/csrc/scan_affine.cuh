@@ -9,8 +9,13 @@
 //   S1  = gamma_C S0 + E^T Kt + N         (d_v x d_k)
 // Rows of S evolve independently (A_t acts from the right), so one CTA owns a
 // tile of BV rows of S for one (b, h) and walks the chunks in order; W, Qt and
-// Kt are shared by the tiles of a head through L2.  The next chunk's shared
-// operands stream in with cp.async while the current one is computed.
+// Kt are shared by the tiles of a head through L2.  The next chunk's operands
+// stream in with cp.async while the current one is computed.
+//
+// The chunk maps arrive piece-major (16-byte column pieces, rows contiguous in
+// a piece) and are kept that way in shared memory: every ldmatrix row is one
+// 16-byte piece-row, so the copies are linear and the fragment loads are free
+// of bank conflicts.
 //
 // Precision: fp16 operands with fp32 accumulation; the entering state S0 and
 // Qt are split into fp16 hi + lo halves (S0 can carry large values written by
@@ -39,12 +44,10 @@ struct ScanArgs {
 template <int D, int C, int BV>
 struct ScanSmem {
   static constexpr int NW = 4;                          // warps per CTA
-  static constexpr int LDD = D + 8, LDB = BV + 8;
-  static constexpr int LDU = BV + 4;                    // fp32 tile rows (U, O_intra)
-  static constexpr int LDN = D + 4;                     // fp32 tile rows (N)
-  static constexpr uint32_t kTile = C * LDD * 2;        // one C x D fp16 tile
-  static constexpr uint32_t kU = C * LDU * 4;           // C x BV fp32
-  static constexpr uint32_t kN = BV * LDN * 4;          // BV x D fp32
+  static constexpr int LDD = D + 8, LDB = BV + 8;       // padded row-major tiles (S0, E)
+  static constexpr uint32_t kTile = C * D * 2;          // one piece-major C x D fp16 map
+  static constexpr uint32_t kU = C * BV * 4;            // C x BV fp32, piece-major
+  static constexpr uint32_t kN = BV * D * 4;            // BV x D fp32, piece-major
   static constexpr uint32_t kBuf = 4 * kTile + 2 * kU + kN;   // W, Kt, Qt hi, Qt lo, U, O_intra, N
   static constexpr uint32_t oBuf0 = 0;
   static constexpr uint32_t oBuf1 = kBuf;
@@ -86,29 +89,32 @@ __global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
 #pragma unroll
   for (int i = 0; i < MapS::kPerWarp; ++i) accS[i].zero();
 
+  // Chunk maps are piece-major: fp16 (r, f) at ((f/8)*R + r)*8 + f%8, fp32 at
+  // ((f/4)*R + r)*4 + f%4 (R = C for the token-row maps, D for N).
   auto issue_loads = [&](int c, int buf) {
     unsigned char* base = sm + (buf ? S::oBuf1 : S::oBuf0);
     const size_t off = (cb0 + c) * (size_t)C * D;
     const __half* src[4] = {p.Wc + off, p.Kt + off, p.Qth + off, p.Qtl + off};
-    constexpr int V = D / 8;                            // 16-byte pieces per fp16 row
-    for (int idx = tid; idx < 4 * C * V; idx += NW * 32) {
-      const int m = idx / (C * V), rem = idx % (C * V), r = rem / V, v8 = rem % V;
-      cp_async16(base + m * S::kTile + (r * LDD + v8 * 8) * 2, src[m] + (size_t)r * D + v8 * 8);
+    constexpr int NP = C * D / 8;                       // 16-byte pieces per map
+    for (int idx = tid; idx < 4 * NP; idx += NW * 32) {
+      const int m = idx / NP, q = idx % NP;
+      cp_async16(base + m * S::kTile + q * 16, src[m] + (size_t)q * 8);
     }
-    // this tile's columns of U and O_intra (fp32 C x BV) and rows of N (fp32 BV x D)
-    constexpr int VU = BV / 4, VN = D / 4;
+    // this tile's columns of U and O_intra (pieces r0/4 .. r0/4 + BV/4 - 1, C rows each)
     unsigned char* su = base + 4 * S::kTile;
-    for (int idx = tid; idx < 2 * C * VU; idx += NW * 32) {
-      const int m = idx / (C * VU), rem = idx % (C * VU), r = rem / VU, v4 = rem % VU;
-      const float* g = (m == 0 ? p.U : p.Oi) + off + (size_t)r * D + r0 + v4 * 4;
-      cp_async16(su + m * S::kU + (r * S::LDU + v4 * 4) * 4, g);
+    constexpr int NU = (BV / 4) * C;
+    for (int idx = tid; idx < 2 * NU; idx += NW * 32) {
+      const int m = idx / NU, q = idx % NU;
+      const float* g = (m == 0 ? p.U : p.Oi) + off + ((size_t)(r0 / 4) * C + q) * 4;
+      cp_async16(su + m * S::kU + q * 16, g);
     }
     if (p.Nl) {
+      // this tile's rows of N: in every piece a4 the rows r0 .. r0+BV-1 are contiguous
       unsigned char* sn = su + 2 * S::kU;
-      const float* g0 = p.Nl + ((cb0 + c) * D + r0) * (size_t)D;
-      for (int idx = tid; idx < BV * VN; idx += NW * 32) {
-        const int r = idx / VN, v4 = idx % VN;
-        cp_async16(sn + (r * S::LDN + v4 * 4) * 4, g0 + (size_t)r * D + v4 * 4);
+      const float* g0 = p.Nl + (cb0 + c) * (size_t)D * D;
+      for (int idx = tid; idx < BV * (D / 4); idx += NW * 32) {
+        const int a4 = idx / BV, r = idx % BV;
+        cp_async16(sn + idx * 16, g0 + ((size_t)a4 * D + r0 + r) * 4);
       }
     }
   };
@@ -140,9 +146,13 @@ __global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
     cp_async_wait<1>();
     __syncthreads();
     const unsigned char* bufp = sm + (buf ? S::oBuf1 : S::oBuf0);
+    const unsigned char* sW = bufp;
+    const unsigned char* sKt = bufp + S::kTile;
+    const unsigned char* sQh = bufp + 2 * S::kTile;
+    const unsigned char* sQl = bufp + 3 * S::kTile;
     const float* sUt = reinterpret_cast<const float*>(bufp + 4 * S::kTile);
-    const float* sOt = sUt + C * S::LDU;
-    const float* sNt = sOt + C * S::LDU;
+    const float* sOt = sUt + C * BV;
+    const float* sNt = sOt + C * BV;
     // S <- gamma_C S0 + N (the E^T Kt term is added below)
     const float gC = p.gC[cbase];
 #pragma unroll
@@ -154,15 +164,18 @@ __global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
 #pragma unroll
         for (int e = 0; e < 4; e += 2) {
           float2 nn = make_float2(0.f, 0.f);
-          if (p.Nl) nn = *reinterpret_cast<const float2*>(sNt + (m0 + acc_row(e)) * S::LDN + n0 + acc_col(hh, e));
+          const int r = m0 + acc_row(e), a = n0 + acc_col(hh, e);
+          if (p.Nl) nn = *reinterpret_cast<const float2*>(sNt + ((a / 4) * BV + r) * 4 + a % 4);
           accS[i].v[hh][e] = fmaf(gC, accS[i].v[hh][e], nn.x);
           accS[i].v[hh][e + 1] = fmaf(gC, accS[i].v[hh][e + 1], nn.y);
         }
     }
-    const __half* sW = reinterpret_cast<const __half*>(sm + (buf ? S::oBuf1 : S::oBuf0));
-    const __half* sKt = sW + C * LDD;
-    const __half* sQh = sKt + C * LDD;
-    const __half* sQl = sQh + C * LDD;
+    auto pm = [](const unsigned char* base) {           // piece-major C-row fp16 map
+      return [base](int row, int col) { return smem_u32(base + ((col / 8) * C + row) * 16); };
+    };
+    auto rm = [](const __half* base, int ld) {          // padded row-major fp16 tile
+      return [base, ld](int row, int col) { return smem_u32(base + row * ld + col); };
+    };
     // E = U - W S0^T  and  O = O_intra + Qt S0^T   (tile columns r0 .. r0+BV-1)
 #pragma unroll
     for (int i = 0; i < MapE::kPerWarp; ++i) {
@@ -171,18 +184,19 @@ __global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
       Acc16 e, o;
       e.zero();
       o.zero();
-      tile_mma<false, true>(e, sW, LDD, sS0h, LDD, m0, n0, D);
-      tile_mma<false, true>(e, sW, LDD, sS0l, LDD, m0, n0, D);
-      tile_mma<false, true>(o, sQh, LDD, sS0h, LDD, m0, n0, D);
-      tile_mma<false, true>(o, sQh, LDD, sS0l, LDD, m0, n0, D);
-      tile_mma<false, true>(o, sQl, LDD, sS0h, LDD, m0, n0, D);
+      tile_mma_f16<0, 0>(e, pm(sW), rm(sS0h, LDD), m0, n0, D);
+      tile_mma_f16<0, 0>(e, pm(sW), rm(sS0l, LDD), m0, n0, D);
+      tile_mma_f16<0, 0>(o, pm(sQh), rm(sS0h, LDD), m0, n0, D);
+      tile_mma_f16<0, 0>(o, pm(sQh), rm(sS0l, LDD), m0, n0, D);
+      tile_mma_f16<0, 0>(o, pm(sQl), rm(sS0h, LDD), m0, n0, D);
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
         for (int e2 = 0; e2 < 4; e2 += 2) {
           const int t = m0 + acc_row(e2), col = n0 + acc_col(hh, e2);
-          const float2 u = *reinterpret_cast<const float2*>(sUt + t * S::LDU + col);
-          const float2 oi = *reinterpret_cast<const float2*>(sOt + t * S::LDU + col);
+          const int uo = ((col / 4) * C + t) * 4 + col % 4;
+          const float2 u = *reinterpret_cast<const float2*>(sUt + uo);
+          const float2 oi = *reinterpret_cast<const float2*>(sOt + uo);
           sE[t * LDB + col] = __float2half_rn(u.x - e.v[hh][e2]);
           sE[t * LDB + col + 1] = __float2half_rn(u.y - e.v[hh][e2 + 1]);
           if (t < nv) {
@@ -196,7 +210,7 @@ __global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
 #pragma unroll
     for (int i = 0; i < MapS::kPerWarp; ++i) {
       if (!MapS::valid(i)) continue;
-      tile_mma<true, false>(accS[i], sE, LDB, sKt, LDD, MapS::m0(i), MapS::n0(i), C);
+      tile_mma_f16<1, 1>(accS[i], rm(sE, LDB), pm(sKt), MapS::m0(i), MapS::n0(i), C);
     }
     __syncthreads();
   }

@@ -113,8 +113,17 @@ def chunk_maps(inp, kl, dl, C):
     return res
 
 
-def read_region(ws, layout, name, dtype, shape):
-    """View of one workspace region as a CPU fp64 numpy array."""
+def read_region(ws, layout, name, dtype, shape, piece_major=True):
+    """One workspace region as a CPU fp64 numpy array.  Per-chunk arrays
+    (shape [..., R, F]) are stored piece-major: 16-byte column pieces, rows
+    contiguous inside a piece; they are returned in plain [..., R, F] order."""
     off = layout[name]
-    n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
-    return ws[off:off + n].view(dtype).reshape(shape).double().cpu().numpy()
+    esz = torch.tensor([], dtype=dtype).element_size()
+    n = int(np.prod(shape)) * esz
+    flat = ws[off:off + n].view(dtype).double().cpu().numpy()
+    if len(shape) < 2 or not piece_major:
+        return flat.reshape(shape)
+    R, F = shape[-2], shape[-1]
+    V = 16 // esz
+    x = flat.reshape(shape[:-2] + (F // V, R, V))
+    return np.moveaxis(x, -3, -2).reshape(shape)

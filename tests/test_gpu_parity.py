@@ -209,7 +209,7 @@ def test_prepare_stage_f32():
     _, _, tr = oracle.forward(inp, trace=True)
     shp = (wl.B, wl.T, wl.H, wl.L, 32)
     for name, key in (("Kl", "kl"), ("Dl", "dl")):
-        g = read_region(ws, lay, name, torch.float32, shp)
+        g = read_region(ws, lay, name, torch.float32, shp, piece_major=False)
         for b, n in enumerate([90, 41]):
             ref = tr[key][b, :n]
             err = np.max(np.abs(g[b, :n] - ref)) / np.max(np.abs(ref))
