@@ -25,7 +25,7 @@ cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s) {
   auto fn = scan_affine_kernel<D, C, BV>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
   if (e != cudaSuccess) return e;
-  fn<<<a.B * a.H * (D / BV), 128, S::bytes, s>>>(a);
+  fn<<<a.B * a.H * (D / BV), S::NW * 32, S::bytes, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -43,7 +43,7 @@ struct ScanArgs {
 
 template <int D, int C, int BV>
 struct ScanSmem {
-  static constexpr int NW = 4;                          // warps per CTA
+  static constexpr int NW = 8;                          // warps per CTA
   static constexpr int LDD = D + 8, LDB = BV + 8;       // padded row-major tiles (S0, E)
   static constexpr uint32_t kTile = C * D * 2;          // one piece-major C x D fp16 map
   static constexpr uint32_t kU = C * BV * 4;            // C x BV fp32, piece-major
@@ -64,7 +64,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 template <int D, int C, int BV>
-__global__ void __launch_bounds__(128) scan_affine_kernel(ScanArgs p) {
+__global__ void __launch_bounds__(256) scan_affine_kernel(ScanArgs p) {
   using S = ScanSmem<D, C, BV>;
   constexpr int NW = S::NW, LDD = S::LDD, LDB = S::LDB;
   constexpr int NT = D / BV;                            // tiles per head
