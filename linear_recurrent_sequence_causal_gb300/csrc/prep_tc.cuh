@@ -32,13 +32,17 @@
 // so each epilogue thread owns one TMEM lane (a feature or a token row).
 #pragma once
 
-#include "chunk_scan.cuh"
+#include <cuda.h>
+
 #include "prism_common.cuh"
 #include "tc_common.cuh"
 
 namespace prism {
 
 struct PrepArgs {
+  // TMA maps of q, k, v as 4-D bf16 tensors (d, H, T, B); boxes of (d, 1, C, 1) rows for
+  // q and k and (d, 1, C + 8, 1) for the v window.
+  CUtensorMap tm_q, tm_k, tm_v;
   int B, T, H, w, L;
   unsigned flags;
   const __nv_bfloat16* q;
@@ -126,7 +130,14 @@ struct Place {
 
 template <int D, int C>
 struct PrepSmem {
-  static constexpr int NTH = C / 2;                      // tokens per column half
+  // Threads: 4 warps per TMEM lane quarter when the column counts allow it.
+  // Warp w reads lane quarter w % 4 and column group w / 4 of every TMEM tile.
+  static constexpr int CG = (C % 32 == 0 && D % 32 == 0) ? 4 : 2;   // column groups
+  static constexpr int NW = 4 * CG;
+  static constexpr int NT = 32 * NW;
+  static constexpr int NTH = C / CG;                     // token columns per thread
+  static constexpr int NFD = D / CG;                     // feature columns per thread
+  static constexpr int NQ = (D + 31) / 32;               // lane quarters that hold features
   static constexpr uint32_t kW = WeightBlock<D>::bytes;  // 128 x D
   static constexpr uint32_t kU = C * D * 2;              // tokens x D
   static constexpr uint32_t kKQ = 128 * D * 2;           // 128 rows x D
@@ -136,10 +147,10 @@ struct PrepSmem {
   // small arrays first
   static constexpr uint32_t oG = 0;                      // f32 g[C]
   static constexpr uint32_t oDec = oG + 4 * C;           // f32 gamma_C/gamma [C]
-  static constexpr uint32_t oBeta = oDec + 4 * C;        // f32 beta^(l) [C]
-  static constexpr uint32_t oInv = oBeta + 4 * C;        // f32 1/|k_hat| [C]
-  static constexpr uint32_t oBar = oInv + 4 * C;         // mbarriers: mma, W_k, W_p
-  static constexpr uint32_t oSlot = oBar + 24;
+  static constexpr uint32_t oBeta = oDec + 4 * C;        // f32 beta^(l) [C] (0 past the sequence end)
+  static constexpr uint32_t oInv = oBeta + 4 * C;        // f32 1/|k_hat| [C] (0 past the sequence end)
+  static constexpr uint32_t oBar = oInv + 4 * C;         // mbarriers: mma, W_k, W_p, inputs
+  static constexpr uint32_t oSlot = oBar + 32;
   static constexpr uint32_t oTiles = ((oSlot + 8 + 127) / 128) * 128;
   // refinement-loop tiles
   static constexpr uint32_t oW = oTiles;
@@ -152,112 +163,172 @@ struct PrepSmem {
   static constexpr uint32_t oDt = oD + 2 * kF;           // hi, lo (128 rows)
   static constexpr uint32_t loop_end = oDt + 2 * kF128;
   // tail buffers (after the loop), placed around the [K;Q] tile which stays live
-  static constexpr uint32_t sKX = 4 * C * D, sSq = 4 * C * (C + 1), sY = 1024 * (C / 16), sB = 8 * C;
-  static constexpr uint32_t sTB = 2 * C * C;               // f16 T as B operand (C x C)
+  static constexpr uint32_t sKX = 4 * C * D, sSq = 4 * C * (C + 4), sB = 8 * C;
+  static constexpr uint32_t sZ = 4 * 32 * 36;                                   // block-solve scratch
+  static constexpr uint32_t sTB = 2 * C * C;             // f16 T as B operand (C x C)
   static constexpr Place p0{oW, oKQ, oKl};
   static constexpr uint32_t tKX = p0.where(sKX);         // f16 [Kb | X] MN-major, C x 2D
   static constexpr Place p1 = p0.at(sKX);
-  static constexpr uint32_t tTP = p1.where(kF128);       // f16 [T ; PT] 128 x C  (also [I ; P])
+  static constexpr uint32_t tTP = p1.where(kF128);       // f16 [I ; P], then [T ; PT], 128 x C
   static constexpr Place p2 = p1.at(kF128);
-  static constexpr uint32_t tA = p2.where(sSq);          // f32 [C][C+1]
+  static constexpr uint32_t tA = p2.where(sSq);          // f32 A [C][C+4]
   static constexpr Place p3 = p2.at(sSq);
-  static constexpr uint32_t tP = p3.where(sSq);          // f32 [C][C+1]
+  static constexpr uint32_t tT = p3.where(sSq);          // f32 T [C][C+4]
   static constexpr Place p4 = p3.at(sSq);
-  static constexpr uint32_t tT = p4.where(sSq);          // f32 [C][C+1]
-  static constexpr Place p5 = p4.at(sSq);
-  static constexpr uint32_t tY = p5.where(sY);           // f32 block-solve scratch
-  static constexpr Place p6 = p5.at(sY);
-  static constexpr uint32_t tB = p6.where(sB);           // f32 beta[C], gamma[C]
-  static constexpr Place p7a = p6.at(sB);
-  static constexpr uint32_t tTB = p7a.where(sTB);        // f16 T (B operand)
-  static constexpr Place p7 = p7a.at(sTB);
+  static constexpr uint32_t tZ = p4.where(sZ);           // f32 block-solve scratch
+  static constexpr Place p5 = p4.at(sZ);
+  static constexpr uint32_t tB = p5.where(sB);           // f32 beta[C], gamma[C]
+  static constexpr Place p6 = p5.at(sB);
+  static constexpr uint32_t tTB = p6.where(sTB);         // f16 T (B operand)
+  static constexpr Place p7 = p6.at(sTB);
   static constexpr uint32_t bytes = p7.o2 > loop_end ? p7.o2 : loop_end;
   static constexpr bool kExtraX = D > 2 * C;             // U/PU need their own TMEM columns
-  // columns: k_hat | p | [R;O_l] | N_l | r, u (refinement loop) or U/PU (tail, when D > 2C)
-  static constexpr uint32_t tmem_cols_needed = 2 * C + 2 * D + (kExtraX ? D : 2 * C);
+  // columns: k_hat | p | [R;O_l] | N_l | u (refinement loop), or U/PU there (tail, when D > 2C)
+  static constexpr uint32_t tmem_cols_needed = 2 * C + 2 * D + (kExtraX ? D : C);
   static constexpr uint32_t tmem_cols =
       tmem_cols_needed <= 32 ? 32 : tmem_cols_needed <= 64 ? 64 : tmem_cols_needed <= 128 ? 128
                                   : tmem_cols_needed <= 256 ? 256 : 512;
+  static_assert(NTH % 8 == 0 && NFD % 8 == 0, "column groups of 8");
 };
 
-// T = (I + A)^-1 for the strictly lower triangular C x C matrix A (fp32, row
-// stride C+1), by blocked forward substitution with 16 x 16 blocks:
-//   diagonal blocks  T_ii = (I + A_ii)^-1 : one lane per column, the column kept
-//                    in registers (row i needs only A's row i and rows < i of
-//                    the lane's own column);
-//   off-diagonal     T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj, by diagonal level.
-// Result in sT (fp32, zeros above the diagonal).  All 256 threads take part.
-template <int C>
-__device__ __forceinline__ void solve_tri(const float* sA, float* sT, float* sY) {
-  constexpr int LD = C + 1, NB = C / 16;
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < C * C; idx += 256) {
-    const int i = idx / C, j = idx % C;
-    if (j / 16 != i / 16 && j > i) sT[i * LD + j] = 0.f;
-  }
-  if (tid < 16 * NB) {
-    const int blk = tid / 16, j = tid % 16, o = blk * 16;
-    float col[16];
+// One warp: acc = X[16 x K] Y[K x 16] (fp32, shared memory; row strides ldx and
+// ldy, multiples of 4 floats; X 16-byte aligned, Y 8-byte aligned).  Lane
+// (rg = lane/8, cg = lane%8) owns rows rg + 4i (i < 4) and columns 2cg, 2cg+1:
+// acc[2i + c].  X is read as 4-wide k vectors, Y as column pairs, so one
+// shared-memory wavefront feeds 128 FMAs.
+__device__ __forceinline__ void warp_blk16(const float* X, int ldx, const float* Y, int ldy, int K,
+                                           float (&acc)[8]) {
+  const int lane = threadIdx.x & 31, rg = lane >> 3, cg = lane & 7;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float s = (i == j) ? 1.f : 0.f;
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 2
+  for (int k = 0; k < K; k += 4) {
+    float4 xa[4];
 #pragma unroll
-      for (int m = 0; m < i; ++m) s -= (m >= j) ? sA[(o + i) * LD + o + m] * col[m] : 0.f;
-      col[i] = (i >= j) ? s : 0.f;
-    }
+    for (int i = 0; i < 4; ++i) xa[i] = *reinterpret_cast<const float4*>(X + (rg + 4 * i) * ldx + k);
+    float2 yb[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) sT[(o + i) * LD + o + j] = col[i];
-  }
-  __syncthreads();
-  // Off-diagonal blocks by level (distance lev = i - j).  At one level every
-  // block has the same inner length 16*lev, so a thread walks its (up to
-  // NB-1) elements in lockstep: independent FMA chains instead of one long one.
-  const int r = (tid & 255) / 16, cc = tid % 16;
-  for (int lev = 1; lev < NB; ++lev) {
-    const int nblk = NB - lev;                       // blocks (i = lev + e, j = e)
-    if (tid < 256) {
-      float acc[NB > 1 ? NB - 1 : 1];
+    for (int q = 0; q < 4; ++q) yb[q] = *reinterpret_cast<const float2*>(Y + (k + q) * ldy + 2 * cg);
 #pragma unroll
-      for (int e = 0; e < NB - 1; ++e) acc[e] = 0.f;
-#pragma unroll 4
-      for (int mo = 0; mo < 16 * lev; ++mo) {
+    for (int i = 0; i < 4; ++i) {
+      const float xv[4] = {xa[i].x, xa[i].y, xa[i].z, xa[i].w};
 #pragma unroll
-        for (int e = 0; e < NB - 1; ++e)
-          if (e < nblk) {
-            const int bi = lev + e, bj = e;
-            acc[e] = fmaf(sA[(bi * 16 + r) * LD + bj * 16 + mo], sT[(bj * 16 + mo) * LD + bj * 16 + cc], acc[e]);
-          }
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * i] = fmaf(xv[q], yb[q].x, acc[2 * i]);
+        acc[2 * i + 1] = fmaf(xv[q], yb[q].y, acc[2 * i + 1]);
       }
-#pragma unroll
-      for (int e = 0; e < NB - 1; ++e)
-        if (e < nblk) sY[e * 256 + r * 16 + cc] = acc[e];
     }
-    __syncthreads();
-    if (tid < 256) {
-      float acc[NB > 1 ? NB - 1 : 1];
-#pragma unroll
-      for (int e = 0; e < NB - 1; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-#pragma unroll
-        for (int e = 0; e < NB - 1; ++e)
-          if (e < nblk) {
-            const int bi = lev + e;
-            acc[e] = fmaf(sT[(bi * 16 + r) * LD + bi * 16 + m], sY[e * 256 + m * 16 + cc], acc[e]);
-          }
-      }
-#pragma unroll
-      for (int e = 0; e < NB - 1; ++e)
-        if (e < nblk) sT[((lev + e) * 16 + r) * LD + e * 16 + cc] = -acc[e];
-    }
-    __syncthreads();
   }
 }
 
+// Stores -acc of warp_blk16 as block (row0, col0) of T: fp32 into sT (stride ld)
+// and fp16 into the B tile sTB ((j, m) -> T[m][j] at (m/8)*16C + j*16 + (m%8)*2).
+template <int C>
+__device__ __forceinline__ void store_tblk(const float (&acc)[8], float* sT, int ld, unsigned char* sTB,
+                                           int row0, int col0) {
+  const int lane = threadIdx.x & 31, rg = lane >> 3, cg = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = row0 + rg + 4 * i, j = col0 + 2 * cg;
+    const float v0 = -acc[2 * i], v1 = -acc[2 * i + 1];
+    *reinterpret_cast<float2*>(sT + m * ld + j) = make_float2(v0, v1);
+    *reinterpret_cast<__half*>(sTB + (m / 8) * (16u * C) + j * 16u + (m % 8) * 2u) = __float2half_rn(v0);
+    *reinterpret_cast<__half*>(sTB + (m / 8) * (16u * C) + (j + 1) * 16u + (m % 8) * 2u) = __float2half_rn(v1);
+  }
+}
+
+// T = (I + A)^-1 for the strictly lower triangular C x C matrix A (fp32, row
+// stride LD = C + 4) by block doubling.  With blocks of 16:
+//   diagonal blocks   T_ii = (I + A_ii)^-1, one thread per column: once entry m
+//                     of the column is final it is eliminated from all rows
+//                     below it (15 dependent steps of independent FMAs);
+//   16 -> 32          T_(2p+1)(2p) = -T_(2p+1)(2p+1) (A_(2p+1)(2p) T_(2p)(2p));
+//   32 -> 64          [T_20 T_21; T_30 T_31] = -T_hi (A_lo T_lo), with T_lo, T_hi
+//                     the 32 x 32 diagonal halves (lower triangular, so the
+//                     zero blocks drop out of the sums).
+// Each product Y = X Z of 16 x 16 blocks is one warp's job (warp_blk16).
+// Results: sT (fp32, stride LD; blocks above the diagonal not written) and sTB,
+// T as the fp16 B operand of the [I ; P] T product, K-major: (j, m) -> T[m][j]
+// at (m/8)*16C + j*16 + (m%8)*2, zero above the diagonal.  sY: 32 x 36 floats.
+template <int C, int NT>
+__device__ __forceinline__ void solve_tri(const float* sA, float* sT, unsigned char* sTB, float* sY) {
+  constexpr int LD = C + 4, NB = C / 16, LDY = 36;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  for (int idx = tid; idx < (C / 8) * C; idx += NT) {   // pieces wholly above the diagonal blocks
+    const int m8 = idx / C, j = idx % C;
+    if (m8 / 2 < j / 16) *reinterpret_cast<uint4*>(sTB + m8 * (16u * C) + j * 16u) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (tid < C) {
+    const int o = (tid / 16) * 16, j = tid % 16;
+    float col[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) col[i] = (i == j) ? 1.f : 0.f;
+#pragma unroll
+    for (int m = 0; m < 15; ++m) {
+      const float cm = col[m];
+#pragma unroll
+      for (int i = m + 1; i < 16; ++i) col[i] = fmaf(-sA[(o + i) * LD + o + m], cm, col[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sT[(o + i) * LD + o + j] = col[i];
+    float a[8], b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { a[i] = col[i]; b[i] = col[8 + i]; }
+    *reinterpret_cast<uint4*>(sTB + (o / 8) * (16u * C) + (o + j) * 16u) = tc::cvt8(a);
+    *reinterpret_cast<uint4*>(sTB + (o / 8 + 1) * (16u * C) + (o + j) * 16u) = tc::cvt8(b);
+  }
+  if constexpr (NB >= 2) {
+    __syncthreads();
+    // 16 -> 32: Y_p = A_(2p+1)(2p) T_(2p)(2p), then T_(2p+1)(2p) = -T_(2p+1)(2p+1) Y_p
+    float acc[8];
+    if (warp < NB / 2) {
+      const int p = warp, r = (2 * p + 1) * 16, c = 2 * p * 16;
+      warp_blk16(sA + r * LD + c, LD, sT + c * LD + c, LD, 16, acc);
+      const int lane = tid & 31, rg = lane >> 3, cg = lane & 7;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float2*>(sY + p * 16 * LDY + (rg + 4 * i) * LDY + 2 * cg) = make_float2(acc[2 * i], acc[2 * i + 1]);
+    }
+    __syncthreads();
+    if (warp < NB / 2) {
+      const int p = warp, r = (2 * p + 1) * 16, c = 2 * p * 16;
+      warp_blk16(sT + r * LD + r, LD, sY + p * 16 * LDY, LDY, 16, acc);
+      store_tblk<C>(acc, sT, LD, sTB, r, c);
+    }
+  }
+  if constexpr (NB == 4) {
+    __syncthreads();
+    // Y = A_lo T_lo  (rows 32..63, cols 0..31):  Y_(bi)(bj) = sum_{k = bj}^{1} A_(bi)(k) T_(k)(bj)
+    float acc[8];
+    if (warp < 4) {
+      const int bi = 2 + (warp >> 1), bj = warp & 1;
+      warp_blk16(sA + (bi * 16) * LD + bj * 16, LD, sT + (bj * 16) * LD + bj * 16, LD, 16 * (2 - bj), acc);
+      const int lane = tid & 31, rg = lane >> 3, cg = lane & 7;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float2*>(sY + ((bi - 2) * 16 + rg + 4 * i) * LDY + bj * 16 + 2 * cg) =
+            make_float2(acc[2 * i], acc[2 * i + 1]);
+    }
+    __syncthreads();
+    // T_(bi)(bj) = -sum_{k = 2}^{bi} T_(bi)(k) Y_(k)(bj)
+    if (warp < 4) {
+      const int bi = 2 + (warp >> 1), bj = warp & 1;
+      warp_blk16(sT + (bi * 16) * LD + 32, LD, sY + bj * 16, LDY, 16 * (bi - 1), acc);
+      store_tblk<C>(acc, sT, LD, sTB, bi * 16, bj * 16);
+    }
+  }
+}
+
+__device__ __forceinline__ void ld_f8(const float* p, float (&v)[8]) {   // 32-byte aligned
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
 template <int D, int C>
-__global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
+__global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __grid_constant__ PrepArgs p) {
   using S = PrepSmem<D, C>;
-  constexpr int NTH = S::NTH;
+  constexpr int NT = S::NT, NTH = S::NTH, NFD = S::NFD, NQ = S::NQ;
   extern __shared__ __align__(1024) unsigned char sm[];
   unsigned char* sW = sm + S::oW;
   unsigned char* sWp = sm + S::oWp;
@@ -274,11 +345,14 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + S::oBar);
   uint64_t* bar_wk = bar_mma + 1;
   uint64_t* bar_wp = bar_mma + 2;
+  uint64_t* bar_in = bar_mma + 3;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::oSlot);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int quarter = warp & 3, half = warp >> 2;
+  const int quarter = warp & 3, cg = warp >> 2;
   const int row = quarter * 32 + lane;         // this thread's TMEM lane
+  const int tb0 = cg * NTH;                    // first of this thread's token columns
+  const int fb0 = cg * NFD;                    // first of this thread's feature columns
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int H = p.H, T_ = p.T, L = p.L, w = p.w;
   const int NC = (T_ + C - 1) / C;
@@ -292,27 +366,57 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     return wsrc + WeightBlock<D>::index(h, l, L, which, part) * S::kW;
   };
 
-  // ---- setup: barriers, TMEM, first weights, gates, [K;Q] rows, v window ----
-  if (tid == 0) {
-    tc::bar_init(bar_mma, 1);
-    tc::bar_init(bar_wk, 1);
-    tc::bar_init(bar_wp, 1);
-    tc::bar_fence_init();
-    if (L > 0) {                               // W^(0) streams in while the anchor is built
-      tc::bar_expect_tx(bar_wk, S::kW);
-      tc::bulk_g2s(sW, wblock(0, 0, 0), S::kW, bar_wk);
-      tc::bar_expect_tx(bar_wp, S::kW);
-      tc::bulk_g2s(sWp, wblock(0, 1, 0), S::kW, bar_wp);
+  // ---- setup: warp 0 starts the tile copies (K, Q rows and the v window by TMA,
+  //      W^(0) by bulk copy) and allocates TMEM; meanwhile the small parameters are
+  //      fetched and warp 1 scans the gates ----
+  __nv_bfloat16* kqraw = reinterpret_cast<__nv_bfloat16*>(sKl);   // [2C][D]: K rows, then Q rows
+  __nv_bfloat16* vwin = reinterpret_cast<__nv_bfloat16*>(sD);     // [C + 8][D]: tokens t0-8 .. t0+C-1
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::bar_init(bar_mma, 1);
+      tc::bar_init(bar_wk, 1);
+      tc::bar_init(bar_wp, 1);
+      tc::bar_init(bar_in, 1);
+      tc::bar_fence_init();
+      tc::bar_expect_tx(bar_in, (uint32_t)(3 * C + 8) * D * 2);
+      tc::tma_load_4d(kqraw, &p.tm_k, 0, h, t0, b, bar_in);
+      tc::tma_load_4d(kqraw + C * D, &p.tm_q, 0, h, t0, b, bar_in);
+      tc::tma_load_4d(vwin, &p.tm_v, 0, h, t0 - 8, b, bar_in);
+      if (L > 0) {                             // W^(0) streams in while the anchor is built
+        tc::bar_expect_tx(bar_wk, S::kW);
+        tc::bulk_g2s(sW, wblock(0, 0, 0), S::kW, bar_wk);
+        tc::bar_expect_tx(bar_wp, S::kW);
+        tc::bulk_g2s(sWp, wblock(0, 1, 0), S::kW, bar_wp);
+      }
     }
+    __syncwarp();
+    tc::alloc(tslot, S::tmem_cols);
   }
-  if (warp == 0) tc::alloc(tslot, S::tmem_cols);
+  // small per-thread parameters: conv taps (ca[m] multiplies v_{t-8+m}), w_beta^(0) of
+  // this thread's feature, beta of token tid (used in the tail)
+  const bool cvalid = row < D;
+  float ca[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int j = 8 - m;
+    ca[m] = (cvalid && j <= w) ? tc::ldg_early(p.conv_w + ((size_t)h * w + (j - 1)) * D + row) : 0.f;
+  }
+  float wb_next = (L > 0 && cvalid) ? tc::ldg_early(p.wbeta + (size_t)h * L * D + row) : 0.f;
+  const float beta_tok = (tid < nv) ? tc::ldg_early(p.beta + ((size_t)b * T_ + t0 + tid) * H + h) : 0.f;
   if (warp == 1) {
-    // inclusive scan of log alpha over the chunk
+    // inclusive scan of log alpha over the chunk (all loads issued first)
+    constexpr int NG = (C + 31) / 32;
+    float la[NG];
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+      const int i = q * 32 + lane;
+      la[q] = (i < nv) ? tc::ldg_early(p.log_alpha + ((size_t)b * T_ + t0 + i) * H + h) : 0.f;
+    }
     float run = 0.f;
-    for (int base = 0; base < C; base += 32) {
-      const int i = base + lane;
-      float x = 0.f;
-      if (i < nv) x = p.log_alpha[((size_t)b * T_ + t0 + i) * H + h];
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+      const int i = q * 32 + lane;
+      float x = la[q];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const float y = __shfl_up_sync(0xffffffffu, x, o);
@@ -325,50 +429,9 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     __syncwarp();
     for (int i = lane; i < C; i += 32) sdec[i] = expf(sg[C - 1] - sg[i]);
   }
-  // [K ; Q] rows as fp16: (row, a) at (a/8)*2048 + row*16 + (a%8)*2, and the v window,
-  // rows t0-w .. t0+C-1 as bf16 [C + w][D] (zero outside [0, len)), in the D tiles.
-  // All global loads are issued before any is used.
-  __nv_bfloat16* vwin = reinterpret_cast<__nv_bfloat16*>(sD);
-  {
-    constexpr int NKQ = (128 * (D / 8) + 255) / 256;
-    constexpr int NVW = ((C + 8) * (D / 8) + 255) / 256;
-    uint4 kq[NKQ], vw[NVW];
-#pragma unroll
-    for (int i = 0; i < NKQ; ++i) {
-      const int idx = tid + i * 256, r = idx % 128, a8 = idx / 128;
-      const int t = r < C ? r : r - C;
-      kq[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (idx < 128 * (D / 8) && r < 2 * C && t < nv)
-        kq[i] = *reinterpret_cast<const uint4*>((r < C ? p.k : p.q) + (((size_t)b * T_ + t0 + t) * H + h) * D + a8 * 8);
-    }
-#pragma unroll
-    for (int i = 0; i < NVW; ++i) {
-      const int idx = tid + i * 256, rr = idx / (D / 8), c8 = idx % (D / 8);
-      const int t = t0 - w + rr;
-      vw[i] = make_uint4(0u, 0u, 0u, 0u);
-      if (rr < C + w && t >= 0 && t < len)
-        vw[i] = *reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t) * H + h) * D + c8 * 8);
-    }
-#pragma unroll
-    for (int i = 0; i < NKQ; ++i) {
-      const int idx = tid + i * 256, r = idx % 128, a8 = idx / 128;
-      if (idx < 128 * (D / 8)) {
-        const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&kq[i]);
-        __half hv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) hv[j] = __float2half_rn(__bfloat162float(e[j]));
-        *reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u) = *reinterpret_cast<const uint4*>(hv);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < NVW; ++i) {
-      const int idx = tid + i * 256, rr = idx / (D / 8), c8 = idx % (D / 8);
-      if (rr < C + w) *reinterpret_cast<uint4*>(vwin + rr * D + c8 * 8) = vw[i];
-    }
-  }
   // rows D..127 of the scaled-write tiles stay zero (A operand of the injection)
   if constexpr (D < 128)
-    for (int idx = tid; idx < (128 - D) * (C / 8) * 2; idx += 256) {
+    for (int idx = tid; idx < (128 - D) * (C / 8) * 2; idx += NT) {
       const int part = idx / ((128 - D) * (C / 8));
       const int rem = idx % ((128 - D) * (C / 8));
       const int r = D + rem % (128 - D), s8 = rem / (128 - D);
@@ -376,47 +439,83 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     }
   tc::fence_before();
   __syncthreads();
+  bool ok = tc::bar_wait(bar_in, 0);
+  // [K ; Q] rows as fp16: (row, a) at (a/8)*2048 + row*16 + (a%8)*2; rows of tokens past
+  // the sequence end and rows >= 2C zero.  v rows past the sequence end are cleared too.
+  for (int idx = tid; idx < 128 * (D / 8); idx += NT) {
+    const int r = idx % 128, a8 = idx / 128;
+    const int t = r < C ? r : r - C;
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (r < 2 * C && t < nv) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(kqraw + r * D + a8 * 8);
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
+      float f[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
+      o = tc::cvt8(f);
+    }
+    *reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u) = o;
+  }
+  if (t0 + C > len) {
+    const int r0 = len - (t0 - 8);             // first v-window row past the end (>= 9)
+    for (int idx = tid; idx < (C + 8 - r0) * (D / 8); idx += NT)
+      *reinterpret_cast<uint4*>(vwin + (r0 + idx / (D / 8)) * D + (idx % (D / 8)) * 8) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
 
   tc::fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t t_proj = tmem, t_p = tmem + C, t_ro = tmem + 2 * C, t_n = tmem + 2 * C + D;
-  const uint32_t t_r = tmem + 2 * C + 2 * D, t_u = t_r + C;   // residual r and anchor u
+  const uint32_t t_u = tmem + 2 * C + 2 * D;   // anchor u (refinement loop)
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-
-  // ---- anchor u = sum_j c_j (.) v_{t-j} and residual r = v - u, kept in TMEM ----
-  // thread (feature c = row, token half) owns tokens [half*NTH, half*NTH + NTH)
   const int c = row;
-  const bool cvalid = c < D;
+  const bool fwarp = quarter < NQ;             // warp holds feature rows
+
+  // Decay mask of this thread's token row for the score tiles (fixed for the
+  // chunk): rows < C strictly causal (G, A), rows C..2C-1 inclusive (P).
+  float gm[NTH];
   {
-    float taps[8];
+    const bool isG = row < C, isP = row >= C && row < 2 * C;
+    const int t = isG ? row : row - C;
+    const float gt = (isG || isP) ? sg[t] : 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) taps[j] = (cvalid && j < w) ? p.conv_w[((size_t)h * w + j) * D + c] : 0.f;
-#pragma unroll 1
+    for (int jj = 0; jj < NTH; ++jj) {
+      const int s_ = tb0 + jj;
+      gm[jj] = ((isG && t > s_) || (isP && t >= s_)) ? __expf(gt - sg[s_]) : 0.f;
+    }
+  }
+
+  // ---- anchor u = sum_j c_j (.) v_{t-j} (TMEM and the U tile) and residual r = v - u
+  //      (registers); thread (feature c, column group) owns tokens tb0 .. tb0+NTH-1 ----
+  float rres[NTH];
+  {
+#pragma unroll
     for (int j8 = 0; j8 < NTH; j8 += 8) {
-      float uu[8], rr[8];
-      __half uh[8], ul[8];
+      if (fwarp) {
+        float win[16], uu[8];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int tl = half * NTH + j8 + jj;
-        float u = 0.f, vt = 0.f;
-        if (cvalid) {
+        for (int i = 0; i < 16; ++i) win[i] = cvalid ? __bfloat162float(vwin[(tb0 + j8 + i) * D + c]) : 0.f;
 #pragma unroll
-          for (int j = 1; j <= 8; ++j)
-            if (j <= w) u = fmaf(taps[j - 1], __bfloat162float(vwin[(tl + w - j) * D + c]), u);
-          vt = __bfloat162float(vwin[(tl + w) * D + c]);
+        for (int jj = 0; jj < 8; ++jj) {
+          float u = 0.f;
+#pragma unroll
+          for (int m = 0; m < 8; ++m) u = fmaf(ca[m], win[jj + m], u);
+          uu[jj] = u;
+          rres[j8 + jj] = (tb0 + j8 + jj < nv) ? win[jj + 8] - u : 0.f;
         }
-        uu[jj] = u;
-        rr[jj] = (tl < nv) ? vt - u : 0.f;
-        tc::split_f16(u, uh[jj], ul[jj]);
         if (cvalid) {
-          // U tile (B operand, N = tokens, K = features): (t, c) at (c/8)*(C*16) + t*16 + (c%8)*2
-          const uint32_t off = (c / 8) * (C * 16u) + tl * 16u + (c % 8) * 2u;
-          *reinterpret_cast<__half*>(sU + off) = uh[jj];
-          *reinterpret_cast<__half*>(sU + S::kU + off) = ul[jj];
+          // U tile, MN-major B operand (K = features, N = tokens): (c, t) at (t/8)*16D + c*16 + (t%8)*2
+          uint4 uh, ul;
+          tc::split8(uu, uh, ul);
+          const uint32_t off = ((tb0 + j8) / 8) * (16u * D) + c * 16u;
+          *reinterpret_cast<uint4*>(sU + off) = uh;
+          *reinterpret_cast<uint4*>(sU + S::kU + off) = ul;
         }
+        tc::st8(t_u + lane_base + tb0 + j8, uu);
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) rres[j8 + jj] = 0.f;
       }
-      tc::st8(t_u + lane_base + half * NTH + j8, uu);
-      tc::st8(t_r + lane_base + half * NTH + j8, rr);
     }
   }
   tc::fence_smem_to_async();
@@ -425,7 +524,6 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   tc::fence_after();
 
   uint32_t ph_mma = 0, ph_wk = 0, ph_wp = 0;
-  bool ok = true;
   auto wait_mma = [&]() {
     ok &= tc::bar_wait(bar_mma, ph_mma & 1);
     ++ph_mma;
@@ -436,8 +534,9 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     ++ph;
   };
 
-  constexpr uint32_t idesc_proj = tc::idesc_f16(C, false, false);
+  constexpr uint32_t idesc_proj = tc::idesc_f16(C, false, true);   // B = U, MN-major
   constexpr uint32_t idesc_gp = tc::idesc_f16(C, false, true);
+  constexpr uint32_t idesc_cc = tc::idesc_f16(C, false, false);
   constexpr uint32_t idesc_dd = tc::idesc_f16(D, false, false);
   constexpr uint32_t S_s = (D / 8) * 128;      // token step of the feature x token tiles
   const bool gelu = !(p.flags & 1u);
@@ -460,7 +559,7 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
       tc::fence_after();
       for (int pass = 0; pass < 2; ++pass)
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t bdesc = tc::desc(sU + pass * S::kU + kk * 2 * C * 16, C * 16, 128);
+          const uint64_t bdesc = tc::desc(sU + pass * S::kU + kk * 256, 128, 16 * D);
           const bool acc = pass > 0 || kk > 0;
           tc::mma(t_proj, tc::desc(sW + kk * 4096, 2048, 128), bdesc, idesc_proj, acc);
           tc::mma(t_p, tc::desc(sWp + kk * 4096, 2048, 128), bdesc, idesc_proj, acc);
@@ -479,7 +578,7 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
       wait_bar(bar_wp, ph_wp);
       if (tid == 0) {
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t bdesc = tc::desc(sU + kk * 2 * C * 16, C * 16, 128);
+          const uint64_t bdesc = tc::desc(sU + kk * 256, 128, 16 * D);
           tc::mma(t_proj, tc::desc(sW + kk * 4096, 2048, 128), bdesc, idesc_proj, true);
           tc::mma(t_p, tc::desc(sWp + kk * 4096, 2048, 128), bdesc, idesc_proj, true);
         }
@@ -495,84 +594,100 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     // [3] epilogue.  Pass A: per token |k_hat|^2 and the gate logit w_beta . u,
     //     summed over this warp's 32 features (reduce-scatter over 8-token groups).
     {
-      const float wb = cvalid ? p.wbeta[((size_t)h * L + l) * D + c] : 0.f;
+      const float wb = wb_next;
+      if (l + 1 < L && cvalid) wb_next = tc::ldg_early(p.wbeta + ((size_t)h * L + l + 1) * D + c);   // next step's
+      if (fwarp) {
 #pragma unroll 1
-      for (int j8 = 0; j8 < NTH; j8 += 8) {
-        float kv[8], uv[8], rn[8], rz[8];
-        tc::ld8(t_proj + lane_base + half * NTH + j8, kv);
-        tc::ld8(t_u + lane_base + half * NTH + j8, uv);
+        for (int j8 = 0; j8 < NTH; j8 += 8) {
+          uint32_t kr[8], ur[8];
+          tc::ld8a(t_proj + lane_base + tb0 + j8, kr);
+          tc::ld8a(t_u + lane_base + tb0 + j8, ur);
+          tc::wait_ld(kr, ur);
+          float rn[8], rz[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          rn[jj] = cvalid ? kv[jj] * kv[jj] : 0.f;
-          rz[jj] = wb * uv[jj];
-        }
-        int n = 8;
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-          if (n > 1) {
-            const int hn = n / 2;
-            const bool upper = lane & m;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (j < hn) {
-                const float sn = upper ? rn[j] : rn[j + hn], kn = upper ? rn[j + hn] : rn[j];
-                const float sz = upper ? rz[j] : rz[j + hn], kz = upper ? rz[j + hn] : rz[j];
-                rn[j] = kn + __shfl_xor_sync(0xffffffffu, sn, m);
-                rz[j] = kz + __shfl_xor_sync(0xffffffffu, sz, m);
-              }
-            }
-            n = hn;
-          } else {
-            rn[0] += __shfl_xor_sync(0xffffffffu, rn[0], m);
-            rz[0] += __shfl_xor_sync(0xffffffffu, rz[0], m);
+          for (int jj = 0; jj < 8; ++jj) {
+            rn[jj] = u2f(kr[jj]) * u2f(kr[jj]);
+            rz[jj] = wb * u2f(ur[jj]);
           }
-        }
-        if ((lane & 3) == 0) {                  // lane holds token j8 + lane/4 of its half
-          const int t = half * NTH + j8 + (lane >> 2);
-          spart[quarter * C + t] = rn[0];
-          spart[4 * C + quarter * C + t] = rz[0];
+          int n = 8;
+#pragma unroll
+          for (int m = 16; m >= 1; m >>= 1) {
+            if (n > 1) {
+              const int hn = n / 2;
+              const bool upper = lane & m;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                if (j < hn) {
+                  const float sn = upper ? rn[j] : rn[j + hn], kn = upper ? rn[j + hn] : rn[j];
+                  const float sz = upper ? rz[j] : rz[j + hn], kz = upper ? rz[j + hn] : rz[j];
+                  rn[j] = kn + __shfl_xor_sync(0xffffffffu, sn, m);
+                  rz[j] = kz + __shfl_xor_sync(0xffffffffu, sz, m);
+                }
+              }
+              n = hn;
+            } else {
+              rn[0] += __shfl_xor_sync(0xffffffffu, rn[0], m);
+              rz[0] += __shfl_xor_sync(0xffffffffu, rz[0], m);
+            }
+          }
+          if ((lane & 3) == 0) {                // lane holds token j8 + lane/4 of its group
+            const int t = tb0 + j8 + (lane >> 2);
+            spart[quarter * C + t] = rn[0];
+            spart[4 * C + quarter * C + t] = rz[0];
+          }
         }
       }
       __syncthreads();
       if (tid < C) {
-        const float ss = spart[tid] + spart[C + tid] + spart[2 * C + tid] + spart[3 * C + tid];
-        const float zz = spart[4 * C + tid] + spart[5 * C + tid] + spart[6 * C + tid] + spart[7 * C + tid];
-        sinv[tid] = 1.0f / sqrtf(ss + 1e-6f);
-        sbl[tid] = sigmoidf(zz);
+        float ss = 0.f, zz = 0.f;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          ss += spart[q * C + tid];
+          zz += spart[4 * C + q * C + tid];
+        }
+        const bool tv = tid < nv;
+        sinv[tid] = tv ? 1.0f / sqrtf(ss + 1e-6f) : 0.f;
+        sbl[tid] = tv ? sigmoidf(zz) : 0.f;
       }
       __syncthreads();
       // Pass B: directions, residual step, factor tiles
-#pragma unroll 1
-      for (int j8 = 0; j8 < NTH; j8 += 8) {
-        float kv[8], pv[8], rr[8];
-        tc::ld8(t_proj + lane_base + half * NTH + j8, kv);
-        tc::ld8(t_p + lane_base + half * NTH + j8, pv);
-        tc::ld8(t_r + lane_base + half * NTH + j8, rr);
-        __half kh[8], kl[8], dh[8], dlo[8], th[8], tl[8];
+      if (fwarp) {
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int t = half * NTH + j8 + jj;
-          const bool valid = cvalid && t < nv;
-          const float kd = valid ? kv[jj] * sinv[t] : 0.f;
-          const float x = pv[jj] * rr[jj];
-          const float dl = gelu ? gelu_erf(x) : x;
-          rr[jj] -= dl;
-          const float dval = valid ? sbl[t] * dl : 0.f;
-          tc::split_f16(kd, kh[jj], kl[jj]);
-          tc::split_f16(dval, dh[jj], dlo[jj]);
-          tc::split_f16(dval * sdec[t], th[jj], tl[jj]);
-        }
-        tc::st8(t_r + lane_base + half * NTH + j8, rr);
-        if (cvalid) {
-          // feature x token tiles: (f, s) at (s/8)*S_s + f*16 + (s%8)*2  (f < D)
-          const uint32_t off = ((half * NTH + j8) / 8) * S_s + c * 16u;
-          *reinterpret_cast<uint4*>(sKl + off) = *reinterpret_cast<const uint4*>(kh);
-          *reinterpret_cast<uint4*>(sKl + S::kF + off) = *reinterpret_cast<const uint4*>(kl);
-          *reinterpret_cast<uint4*>(sD + off) = *reinterpret_cast<const uint4*>(dh);
-          *reinterpret_cast<uint4*>(sD + S::kF + off) = *reinterpret_cast<const uint4*>(dlo);
-          const uint32_t off128 = ((half * NTH + j8) / 8) * 2048u + c * 16u;
-          *reinterpret_cast<uint4*>(sDt + off128) = *reinterpret_cast<const uint4*>(th);
-          *reinterpret_cast<uint4*>(sDt + S::kF128 + off128) = *reinterpret_cast<const uint4*>(tl);
+        for (int j8 = 0; j8 < NTH; j8 += 8) {
+          uint32_t kr[8], pr[8];
+          tc::ld8a(t_proj + lane_base + tb0 + j8, kr);
+          tc::ld8a(t_p + lane_base + tb0 + j8, pr);
+          const int tb = tb0 + j8;
+          float si[8], sb[8], sd[8];
+          ld_f8(sinv + tb, si);
+          ld_f8(sbl + tb, sb);
+          ld_f8(sdec + tb, sd);
+          tc::wait_ld(kr, pr);
+          float kd[8], dv[8], dt[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            kd[jj] = u2f(kr[jj]) * si[jj];
+            const float x = u2f(pr[jj]) * rres[j8 + jj];
+            const float dl = gelu ? gelu_erf(x) : x;
+            rres[j8 + jj] -= dl;
+            dv[jj] = sb[jj] * dl;
+            dt[jj] = dv[jj] * sd[jj];
+          }
+          if (cvalid) {
+            uint4 hi, lo;
+            // feature x token tiles: (f, s) at (s/8)*S_s + f*16 + (s%8)*2  (f < D)
+            const uint32_t off = (tb / 8) * S_s + c * 16u;
+            const uint32_t off128 = (tb / 8) * 2048u + c * 16u;
+            tc::split8(kd, hi, lo);
+            *reinterpret_cast<uint4*>(sKl + off) = hi;
+            *reinterpret_cast<uint4*>(sKl + S::kF + off) = lo;
+            tc::split8(dv, hi, lo);
+            *reinterpret_cast<uint4*>(sD + off) = hi;
+            *reinterpret_cast<uint4*>(sD + S::kF + off) = lo;
+            tc::split8(dt, hi, lo);
+            *reinterpret_cast<uint4*>(sDt + off128) = hi;
+            *reinterpret_cast<uint4*>(sDt + S::kF128 + off128) = lo;
+          }
         }
       }
     }
@@ -589,31 +704,23 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
       tc::commit(bar_mma);
     }
     wait_mma();
-    // [5] epilogue: decay + causal masks; rows < C are G (strict), C..2C-1 are P (inclusive)
-    {
-      const bool isG = row < C, isP = row >= C && row < 2 * C;
-      const int t = isG ? row : row - C;
-      const float gt = (isG || isP) ? sg[t] : 0.f;
-#pragma unroll 1
-      for (int j8 = 0; j8 < NTH; j8 += 8) {
-        float tmp[8];
-        tc::ld8(t_proj + lane_base + half * NTH + j8, tmp);
-        __half hh[8], ll[8];
+    // [5] epilogue: decay and causal mask, then hi/lo split; rows < C are G, C..2C-1 are P
+    if (quarter * 32 < 2 * C) {
+      uint32_t gr[NTH / 8][8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          const int s_ = half * NTH + j8 + jj;
-          float val = 0.f;
-          if ((isG && t > s_) || (isP && t >= s_)) val = expf(gt - sg[s_]) * tmp[jj];
-          if (isP) {
-            tc::split_f16(val, hh[jj], ll[jj]);
-          } else {
-            hh[jj] = __float2half_rn(val);
-            ll[jj] = __float2half_rn(0.f);
-          }
-        }
-        const uint32_t off = ((half * NTH + j8) / 8) * 2048u + row * 16u;
-        *reinterpret_cast<uint4*>(sGP + off) = *reinterpret_cast<const uint4*>(hh);
-        *reinterpret_cast<uint4*>(sGP + S::kF128 + off) = *reinterpret_cast<const uint4*>(ll);
+      for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_proj + lane_base + tb0 + 8 * g, gr[g]);
+      tc::wait_ld();
+#pragma unroll
+      for (int g = 0; g < NTH / 8; ++g) {
+        tc::pin(gr[g]);
+        float val[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) val[jj] = gm[8 * g + jj] * u2f(gr[g][jj]);
+        uint4 hi, lo;
+        tc::split8(val, hi, lo);
+        const uint32_t off = ((tb0 + 8 * g) / 8) * 2048u + row * 16u;
+        *reinterpret_cast<uint4*>(sGP + off) = hi;
+        *reinterpret_cast<uint4*>(sGP + S::kF128 + off) = lo;
       }
     }
     tc::fence_smem_to_async();
@@ -639,9 +746,8 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   // ================= tail: gated delta rule, state-independent part =================
   const size_t cbase = ((size_t)b * H + h) * NC + chunk;
   float* tAf = reinterpret_cast<float*>(sm + S::tA);
-  float* tPf = reinterpret_cast<float*>(sm + S::tP);
   float* tTf = reinterpret_cast<float*>(sm + S::tT);
-  float* tYf = reinterpret_cast<float*>(sm + S::tY);
+  float* tZf = reinterpret_cast<float*>(sm + S::tZ);
   float* tbeta = reinterpret_cast<float*>(sm + S::tB);
   float* tgam = tbeta + C;
   unsigned char* sTP = sm + S::tTP;
@@ -652,23 +758,34 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   const int s_tok = row;
   const bool tok = s_tok < C;
   const bool tok_valid = tok && s_tok < nv;
+  // v rows for (d), fetched now so the latency overlaps (a)
+  uint4 vr[NFD / 8];
+#pragma unroll
+  for (int g = 0; g < NFD / 8; ++g)
+    vr[g] = tok_valid ? tc::ldg_early(reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t0 + s_tok) * H + h) * D + fb0 + 8 * g))
+                      : make_uint4(0u, 0u, 0u, 0u);
   // (a) N = N_l to global (its TMEM columns are reused below)
-  if (L > 0) {
+  if (L > 0 && fwarp) {
     float* nbase = p.Nl + cbase * D * D;      // piece-major: (c, a) at ((a/4)*D + c)*4 + a%4
-#pragma unroll 1
-    for (int j8 = 0; j8 < D / 2; j8 += 8) {
-      float tmp[8];
-      tc::ld8(t_n + lane_base + half * (D / 2) + j8, tmp);
+    uint32_t nr[NFD / 8][8];
+#pragma unroll
+    for (int g = 0; g < NFD / 8; ++g) tc::ld8a(t_n + lane_base + fb0 + 8 * g, nr[g]);
+    tc::wait_ld();
+#pragma unroll
+    for (int g = 0; g < NFD / 8; ++g) {
+      tc::pin(nr[g]);
       if (cvalid) {
-        const int a0 = half * (D / 2) + j8;
-        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4) * D + row) * 4) = make_float4(tmp[0], tmp[1], tmp[2], tmp[3]);
-        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4 + 1) * D + row) * 4) = make_float4(tmp[4], tmp[5], tmp[6], tmp[7]);
+        const int a0 = fb0 + 8 * g;
+        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4) * D + row) * 4) =
+            make_float4(u2f(nr[g][0]), u2f(nr[g][1]), u2f(nr[g][2]), u2f(nr[g][3]));
+        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4 + 1) * D + row) * 4) =
+            make_float4(u2f(nr[g][4]), u2f(nr[g][5]), u2f(nr[g][6]), u2f(nr[g][7]));
       }
     }
   }
-  for (int i = tid; i < C; i += 256) {
-    tbeta[i] = i < nv ? p.beta[((size_t)b * T_ + t0 + i) * H + h] : 0.f;
-    tgam[i] = expf(sg[i]);
+  if (tid < C) {
+    tbeta[tid] = beta_tok;
+    tgam[tid] = expf(sg[tid]);
   }
   tc::fence_before();
   __syncthreads();
@@ -677,85 +794,79 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     tc::fence_after();
     for (int kk = 0; kk < D / 16; ++kk)
       tc::mma(t_proj, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKQ + kk * 4096, 2048, 128),
-              idesc_proj, kk > 0);
+              idesc_cc, kk > 0);
     tc::commit(bar_mma);
   }
   // (d) meanwhile: X = beta (V - R) and Kb = beta gamma K as the MN-major B tile [Kb | X]:
   //     (s, f) at (f/8)*(16C) + s*16 + (f%8)*2,  f < D: Kb,  f >= D: X
-  {
+  if (quarter * 32 < C) {
     const float bs = tok ? tbeta[s_tok] : 0.f, gs = tok ? tgam[s_tok] : 0.f;
-#pragma unroll 1
-    for (int j8 = 0; j8 < D / 2; j8 += 8) {
-      const int f0 = half * (D / 2) + j8;
-      float rr[8];
-      if (L > 0) {
-        tc::ld8(t_ro + lane_base + f0, rr);
-      } else {
+    uint32_t rr[NFD / 8][8];
+    if (L > 0) {
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) rr[jj] = 0.f;
-      }
-      if (tok) {
-        __half xh[8], kh[8];
-        uint4 vraw = make_uint4(0u, 0u, 0u, 0u);
-        if (tok_valid) vraw = *reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t0 + s_tok) * H + h) * D + f0);
-        const __nv_bfloat16* ve = reinterpret_cast<const __nv_bfloat16*>(&vraw);
+      for (int g = 0; g < NFD / 8; ++g) tc::ld8a(t_ro + lane_base + fb0 + 8 * g, rr[g]);
+      tc::wait_ld();
+#pragma unroll
+      for (int g = 0; g < NFD / 8; ++g) tc::pin(rr[g]);
+    } else {
+#pragma unroll
+      for (int g = 0; g < NFD / 8; ++g)
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) rr[g][jj] = 0u;
+    }
+    if (tok) {
+#pragma unroll
+      for (int g = 0; g < NFD / 8; ++g) {
+        const int f0 = fb0 + 8 * g;
+        const __nv_bfloat16* ve = reinterpret_cast<const __nv_bfloat16*>(&vr[g]);
         const uint4 kraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + s_tok * 16u);
         const __half* ke = reinterpret_cast<const __half*>(&kraw);
+        float xf[8], kf[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          xh[jj] = __float2half_rn(tok_valid ? bs * (__bfloat162float(ve[jj]) - rr[jj]) : 0.f);
-          kh[jj] = __float2half_rn(bs * gs * __half2float(ke[jj]));
+          xf[jj] = tok_valid ? bs * (__bfloat162float(ve[jj]) - u2f(rr[g][jj])) : 0.f;
+          kf[jj] = bs * gs * __half2float(ke[jj]);
         }
-        *reinterpret_cast<uint4*>(sKX + ((D + f0) / 8) * (16u * C) + s_tok * 16u) = *reinterpret_cast<const uint4*>(xh);
-        *reinterpret_cast<uint4*>(sKX + (f0 / 8) * (16u * C) + s_tok * 16u) = *reinterpret_cast<const uint4*>(kh);
+        *reinterpret_cast<uint4*>(sKX + ((D + f0) / 8) * (16u * C) + s_tok * 16u) = tc::cvt8(xf);
+        *reinterpret_cast<uint4*>(sKX + (f0 / 8) * (16u * C) + s_tok * 16u) = tc::cvt8(kf);
       }
     }
   }
   wait_mma();
-  // (c) A = strict_tril(beta (K K^T) (.) Gamma), P = tril(Q K^T (.) Gamma)   (fp32)
-  {
-    const bool isA = row < C, isP = row >= C && row < 2 * C;
+  // (c) A = strict_tril(beta (K K^T) (.) Gamma) (fp32) and the A tile [I ; P] of the
+  //     [T ; PT] product (fp16, K-major (r, s) at (s/8)*2048 + r*16 + (s%8)*2; rows >= 2C zero)
+  if (quarter * 32 < 2 * C) {
+    const bool isA = row < C;
     const int t = isA ? row : row - C;
-#pragma unroll 1
-    for (int j8 = 0; j8 < NTH; j8 += 8) {
-      float tmp[8];
-      tc::ld8(t_proj + lane_base + half * NTH + j8, tmp);
-      if (isA || isP) {
-        const float gt = sg[t];
+    const float bt = isA ? tbeta[t] : 0.f;
+    uint32_t ar[NTH / 8][8];
+#pragma unroll
+    for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_proj + lane_base + tb0 + 8 * g, ar[g]);
+    tc::wait_ld();
+#pragma unroll
+    for (int g = 0; g < NTH / 8; ++g) {
+      tc::pin(ar[g]);
+      const int s0 = tb0 + 8 * g;
+      float v8[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) v8[jj] = gm[8 * g + jj] * u2f(ar[g][jj]);
+      if (isA) {
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          const int s_ = half * NTH + j8 + jj;
-          if (isA) tAf[t * (C + 1) + s_] = (t > s_) ? tbeta[t] * expf(gt - sg[s_]) * tmp[jj] : 0.f;
-          else     tPf[t * (C + 1) + s_] = (t >= s_) ? expf(gt - sg[s_]) * tmp[jj] : 0.f;
+          tAf[t * (C + 4) + s0 + jj] = bt * v8[jj];
+          v8[jj] = (s0 + jj == t) ? 1.f : 0.f;
         }
       }
+      *reinterpret_cast<uint4*>(sTP + (s0 / 8) * 2048u + row * 16u) = tc::cvt8(v8);
     }
+  } else {
+#pragma unroll
+    for (int g = 0; g < NTH / 8; ++g)
+      *reinterpret_cast<uint4*>(sTP + ((tb0 + 8 * g) / 8) * 2048u + row * 16u) = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
-  // (e) T = (I + A)^-1 (fp32); then [T ; PT] = [I ; P] T on the tensor core
-  solve_tri<C>(tAf, tTf, tYf);
-  // A tile [I ; P] (fp16, 128 x C, K-major (r, s) at (s/8)*2048 + r*16 + (s%8)*2), rows >= 2C zero;
-  // B tile T (N = j, K = m): (j, m) at (m/8)*(16C) + j*16 + (m%8)*2
-  for (int idx = tid; idx < 128 * (C / 8); idx += 256) {
-    const int r = idx % 128, s8 = idx / 128;
-    __half hv[8];
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const int j = s8 * 8 + jj;
-      float x = 0.f;
-      if (r < C) x = (r == j) ? 1.f : 0.f;
-      else if (r < 2 * C) x = tPf[(r - C) * (C + 1) + j];
-      hv[jj] = __float2half_rn(x);
-    }
-    *reinterpret_cast<uint4*>(sTP + s8 * 2048u + r * 16u) = *reinterpret_cast<const uint4*>(hv);
-  }
-  for (int idx = tid; idx < C * (C / 8); idx += 256) {
-    const int j = idx % C, m8 = idx / C;
-    __half hv[8];
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) hv[jj] = __float2half_rn(tTf[(m8 * 8 + jj) * (C + 1) + j]);
-    *reinterpret_cast<uint4*>(sTB + m8 * (16u * C) + j * 16u) = *reinterpret_cast<const uint4*>(hv);
-  }
+  // (e) T = (I + A)^-1 (fp32, and the fp16 B tile); then [T ; PT] = [I ; P] T on the tensor core
+  solve_tri<C, NT>(tAf, tTf, sTB, tZf);
   tc::fence_smem_to_async();
   tc::fence_before();
   __syncthreads();
@@ -763,19 +874,24 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     tc::fence_after();
     for (int kk = 0; kk < C / 16; ++kk)
       tc::mma(t_proj, tc::desc(sTP + kk * 4096, 2048, 128), tc::desc(sTB + kk * 2 * 16 * C, 16 * C, 128),
-              idesc_proj, kk > 0);
+              idesc_cc, kk > 0);
     tc::commit(bar_mma);
   }
   wait_mma();
   // [T ; PT] back into the A tile (fp16)
-#pragma unroll 1
-  for (int j8 = 0; j8 < NTH; j8 += 8) {
-    float tmp[8];
-    tc::ld8(t_proj + lane_base + half * NTH + j8, tmp);
-    __half hv[8];
+  {
+    uint32_t tr[NTH / 8][8];
 #pragma unroll
-    for (int jj = 0; jj < 8; ++jj) hv[jj] = __float2half_rn(tmp[jj]);
-    *reinterpret_cast<uint4*>(sTP + ((half * NTH + j8) / 8) * 2048u + row * 16u) = *reinterpret_cast<const uint4*>(hv);
+    for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_proj + lane_base + tb0 + 8 * g, tr[g]);
+    tc::wait_ld();
+#pragma unroll
+    for (int g = 0; g < NTH / 8; ++g) {
+      tc::pin(tr[g]);
+      float v8[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) v8[jj] = u2f(tr[g][jj]);
+      *reinterpret_cast<uint4*>(sTP + ((tb0 + 8 * g) / 8) * 2048u + row * 16u) = tc::cvt8(v8);
+    }
   }
   tc::fence_smem_to_async();
   tc::fence_before();
@@ -794,7 +910,7 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
   wait_mma();
   // (g) outputs.  Lanes 0..C-1: W (fp16), U (fp32), Kt (fp16).  Lanes C..2C-1:
   //     Qt = gamma Q - PW (fp16 hi/lo), O_intra = PU + O_l (fp32).
-  {
+  if (quarter * 32 < 2 * C) {
     const bool isT = row < C, isPT = row >= C && row < 2 * C;
     const int t = isT ? row : row - C;
     const size_t cb = cbase * C * D;         // piece-major chunk base
@@ -802,48 +918,56 @@ __global__ void __launch_bounds__(256, 1) prep_tc_kernel(PrepArgs p) {
     const float gt = (isT || isPT) ? tgam[t] : 0.f;
     const float dct = (isT || isPT) ? sdec[t] : 0.f;
 #pragma unroll 1
-    for (int j8 = 0; j8 < D / 2; j8 += 8) {
-      const int f0 = half * (D / 2) + j8;
-      float wv[8], xv[8], ov[8];
-      tc::ld8(t_w + lane_base + f0, wv);
-      tc::ld8(t_x + lane_base + f0, xv);
+    for (int j8 = 0; j8 < NFD; j8 += 8) {
+      const int f0 = fb0 + j8;
+      uint32_t wr[8], xr[8], orr[8];
+      tc::ld8a(t_w + lane_base + f0, wr);
+      tc::ld8a(t_x + lane_base + f0, xr);
       if (L > 0) {
-        tc::ld8(t_ro + lane_base + f0, ov);
+        tc::ld8a(t_ro + lane_base + f0, orr);
+        tc::wait_ld(wr, xr, orr);
       } else {
+        tc::wait_ld(wr, xr);
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) ov[jj] = 0.f;
+        for (int jj = 0; jj < 8; ++jj) orr[jj] = 0u;
       }
       if (isT) {
-        __half wh[8], kth[8];
         const uint4 kraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + t * 16u);
         const __half* ke = reinterpret_cast<const __half*>(&kraw);
+        float wv[8], kt[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          wh[jj] = __float2half_rn(wv[jj]);
-          kth[jj] = __float2half_rn(dct * __half2float(ke[jj]));
+          wv[jj] = u2f(wr[jj]);
+          kt[jj] = dct * __half2float(ke[jj]);
         }
         const size_t o16 = cb + ((size_t)(f0 / 8) * C + tr) * 8;     // fp16 piece (8 values)
-        *reinterpret_cast<uint4*>(p.Wc + o16) = *reinterpret_cast<const uint4*>(wh);
-        *reinterpret_cast<uint4*>(p.Kt + o16) = *reinterpret_cast<const uint4*>(kth);
-        *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4) * C + tr) * 4) = make_float4(xv[0], xv[1], xv[2], xv[3]);
-        *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4 + 1) * C + tr) * 4) = make_float4(xv[4], xv[5], xv[6], xv[7]);
+        *reinterpret_cast<uint4*>(p.Wc + o16) = tc::cvt8(wv);
+        *reinterpret_cast<uint4*>(p.Kt + o16) = tc::cvt8(kt);
+        *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4) * C + tr) * 4) =
+            make_float4(u2f(xr[0]), u2f(xr[1]), u2f(xr[2]), u2f(xr[3]));
+        *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4 + 1) * C + tr) * 4) =
+            make_float4(u2f(xr[4]), u2f(xr[5]), u2f(xr[6]), u2f(xr[7]));
       } else if (isPT) {
-        __half qh[8], ql[8];
         const uint4 qraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + row * 16u);
         const __half* qe = reinterpret_cast<const __half*>(&qraw);
+        float qv[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) tc::split_f16(gt * __half2float(qe[jj]) - wv[jj], qh[jj], ql[jj]);
+        for (int jj = 0; jj < 8; ++jj) qv[jj] = gt * __half2float(qe[jj]) - u2f(wr[jj]);
+        uint4 hi, lo;
+        tc::split8(qv, hi, lo);
         const size_t o16 = cb + ((size_t)(f0 / 8) * C + tr) * 8;
-        *reinterpret_cast<uint4*>(p.Qth + o16) = *reinterpret_cast<const uint4*>(qh);
-        *reinterpret_cast<uint4*>(p.Qtl + o16) = *reinterpret_cast<const uint4*>(ql);
+        *reinterpret_cast<uint4*>(p.Qth + o16) = hi;
+        *reinterpret_cast<uint4*>(p.Qtl + o16) = lo;
         *reinterpret_cast<float4*>(p.Oi + cb + ((size_t)(f0 / 4) * C + tr) * 4) =
-            make_float4(xv[0] + ov[0], xv[1] + ov[1], xv[2] + ov[2], xv[3] + ov[3]);
+            make_float4(u2f(xr[0]) + u2f(orr[0]), u2f(xr[1]) + u2f(orr[1]), u2f(xr[2]) + u2f(orr[2]),
+                        u2f(xr[3]) + u2f(orr[3]));
         *reinterpret_cast<float4*>(p.Oi + cb + ((size_t)(f0 / 4 + 1) * C + tr) * 4) =
-            make_float4(xv[4] + ov[4], xv[5] + ov[5], xv[6] + ov[6], xv[7] + ov[7]);
+            make_float4(u2f(xr[4]) + u2f(orr[4]), u2f(xr[5]) + u2f(orr[5]), u2f(xr[6]) + u2f(orr[6]),
+                        u2f(xr[7]) + u2f(orr[7]));
       }
     }
-    if (tid == 0) p.gC[cbase] = tgam[C - 1];
   }
+  if (tid == 0) p.gC[cbase] = tgam[C - 1];
   if (!ok && lane == 0) atomicExch(p.status, 1);
   tc::fence_before();
   __syncthreads();

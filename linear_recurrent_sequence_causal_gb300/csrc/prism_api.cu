@@ -1,7 +1,11 @@
 // C ABI of the PRISM mixer forward pass: argument checks, workspace layout and
 // kernel dispatch.  See include/prism.h for the contract of each entry point.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "../../include/prism.h"
 #include "kernels.h"
@@ -78,6 +82,36 @@ constexpr int kMaxL = 8, kMaxW = 8;
 constexpr size_t kAbsent = ~size_t(0);
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link to the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// TMA map of a bf16 [B][T][H][d] tensor as 4-D (d, H, T, B) with boxes of `rows` tokens
+// of one head: (d, 1, rows, 1).
+bool make_row_map(CUtensorMap* m, const void* base, const prism_dims* d, int rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t D = (cuuint64_t)d->d_k, H = (cuuint64_t)d->H, T = (cuuint64_t)d->T;
+  const cuuint64_t dim[4] = {D, H, T, (cuuint64_t)d->B};
+  const cuuint64_t stride[3] = {D * 2, H * D * 2, T * H * D * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)D, 1, (cuuint32_t)rows, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dim, stride, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Shape checks shared by every entry point.
@@ -233,6 +267,9 @@ extern "C" PRISM_API int prism_prepare(const prism_dims* dims, const void* q, co
       prism::launch_weights(D, Wk, Wp, dims->H, dims->L, wblocks, status + 1, s) != cudaSuccess)
     return PRISM_ERR_LAUNCH;
   prism::PrepArgs a;
+  if (!make_row_map(&a.tm_q, q, dims, C) || !make_row_map(&a.tm_k, k, dims, C) ||
+      !make_row_map(&a.tm_v, v, dims, C + 8))
+    return PRISM_ERR_CUDA;
   a.B = dims->B; a.T = dims->T; a.H = dims->H; a.w = dims->conv_width; a.L = dims->L;
   a.flags = dims->flags;
   a.q = static_cast<const __nv_bfloat16*>(q);

@@ -12,6 +12,7 @@
 
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <string.h>
 
 namespace prism {
 namespace tc {
@@ -85,6 +86,27 @@ __device__ __forceinline__ void ld8(uint32_t taddr, float (&v)[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Asynchronous form of ld8: several loads may be in flight; wait_ld(regs...)
+// then waits for all of them and ties the named registers to the wait, so no
+// use of a loaded value can be scheduled before it.
+__device__ __forceinline__ void ld8a(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "r"(taddr));
+}
+template <int N>
+__device__ __forceinline__ void pin(uint32_t (&r)[N]) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+__device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+template <typename... R>
+__device__ __forceinline__ void wait_ld(R&... regs) {
+  wait_ld();
+  (pin(regs), ...);
+}
+
 // 32 lanes x 8 columns of fp32 into TMEM; waits for completion.
 __device__ __forceinline__ void st8(uint32_t taddr, const float (&v)[8]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
@@ -116,6 +138,31 @@ __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, uint32_
   return false;
 }
 
+// Global loads that stay where they are written (a volatile asm is not moved
+// past other volatile asm), so a value can be fetched well before its first use.
+__device__ __forceinline__ float ldg_early(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];\n" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ldg_early(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// 4-D tiled tensor copy global -> shared (TMA), completing its box's bytes on `bar`.
+// `map` is the address of a CUtensorMap kernel parameter; coordinates may lie
+// outside the tensor (those elements read as zero).
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];\n"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` of transaction on `bar`.
 // Both addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -130,6 +177,30 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ void split_f16(float x, __half& hi, __half& lo) {
   hi = __float2half_rn(x);
   lo = __float2half_rn(x - __half2float(hi));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) {
+  uint32_t u;
+  memcpy(&u, &h, 4);
+  return u;
+}
+// Eight fp32 values -> one 16-byte piece of fp16 (element 0 at the lowest address).
+__device__ __forceinline__ uint4 cvt8(const float (&x)[8]) {
+  return make_uint4(h2_bits(__floats2half2_rn(x[0], x[1])), h2_bits(__floats2half2_rn(x[2], x[3])),
+                    h2_bits(__floats2half2_rn(x[4], x[5])), h2_bits(__floats2half2_rn(x[6], x[7])));
+}
+// Eight fp32 values -> hi and lo pieces, hi = rn(x), lo = rn(x - hi), in pairs.
+__device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 a = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+    const float2 f = __half22float2(a);
+    h[i] = h2_bits(a);
+    l[i] = h2_bits(__floats2half2_rn(x[2 * i] - f.x, x[2 * i + 1] - f.y));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 }  // namespace tc
