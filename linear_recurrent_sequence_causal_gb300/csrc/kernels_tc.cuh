@@ -15,7 +15,7 @@ cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
   if (e != cudaSuccess) return e;
   dim3 grid((a.T + C - 1) / C, a.H, a.B);
-  fn<<<grid, S::NT, S::bytes, s>>>(a);
+  fn<<<grid, S::NTA, S::bytes, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -130,11 +130,13 @@ struct Place {
 
 template <int D, int C>
 struct PrepSmem {
-  // Threads: 4 warps per TMEM lane quarter when the column counts allow it.
-  // Warp w reads lane quarter w % 4 and column group w / 4 of every TMEM tile.
+  // Consumer threads: 4 warps per TMEM lane quarter when the column counts allow it;
+  // warp w reads lane quarter w % 4 and column group w / 4 of every TMEM tile.  One more
+  // warp (the producer) issues the tile copies and the MMAs of the refinement loop.
   static constexpr int CG = (C % 32 == 0 && D % 32 == 0) ? 4 : 2;   // column groups
-  static constexpr int NW = 4 * CG;
-  static constexpr int NT = 32 * NW;
+  static constexpr int NW = 4 * CG;                      // consumer warps
+  static constexpr int NT = 32 * NW;                     // consumer threads
+  static constexpr int NTA = NT + 32;                    // all threads (with the producer warp)
   static constexpr int NTH = C / CG;                     // token columns per thread
   static constexpr int NFD = D / CG;                     // feature columns per thread
   static constexpr int NQ = (D + 31) / 32;               // lane quarters that hold features
@@ -143,20 +145,22 @@ struct PrepSmem {
   static constexpr uint32_t kKQ = 128 * D * 2;           // 128 rows x D
   static constexpr uint32_t kF = D * C * 2;              // features x tokens
   static constexpr uint32_t kF128 = 128 * C * 2;         // 128 rows x tokens
-  static constexpr bool kWpInGP = kW <= 2 * kF128;       // W_p staged in the [G;P] buffers
+  static constexpr uint32_t kX = kW > 2 * kF128 ? kW : 2 * kF128;   // W_k, or the [G;P] hi/lo tiles
   // small arrays first
   static constexpr uint32_t oG = 0;                      // f32 g[C]
   static constexpr uint32_t oDec = oG + 4 * C;           // f32 gamma_C/gamma [C]
   static constexpr uint32_t oBeta = oDec + 4 * C;        // f32 beta^(l) [C] (0 past the sequence end)
   static constexpr uint32_t oInv = oBeta + 4 * C;        // f32 1/|k_hat| [C] (0 past the sequence end)
-  static constexpr uint32_t oBar = oInv + 4 * C;         // mbarriers: mma, W_k, W_p, inputs
-  static constexpr uint32_t oSlot = oBar + 32;
+  static constexpr uint32_t oPart = oInv + 4 * C;        // f32 per-quarter partial sums, quarters 1..3:
+                                                         //   [3][2][C] (|k_hat|^2, w_beta . u)
+  static constexpr int kBars = 13;
+  static constexpr uint32_t oBar = oPart + 24 * C;       // mbarriers
+  static constexpr uint32_t oSlot = oBar + 8 * kBars;
   static constexpr uint32_t oTiles = ((oSlot + 8 + 127) / 128) * 128;
   // refinement-loop tiles
-  static constexpr uint32_t oW = oTiles;
-  static constexpr uint32_t oGP = oW + kW;               // hi, lo (2 * kF128)
-  static constexpr uint32_t oWp = kWpInGP ? oGP : oGP + 2 * kF128;
-  static constexpr uint32_t oU = oGP + 2 * kF128 + (kWpInGP ? 0 : kW);   // hi, lo
+  static constexpr uint32_t oX = oTiles;                 // W_k^(l+1) / [G;P]_l hi, lo
+  static constexpr uint32_t oY = oX + kX;                // W_p
+  static constexpr uint32_t oU = oY + kW;                // u hi, lo
   static constexpr uint32_t oKQ = oU + 2 * kU;
   static constexpr uint32_t oKl = oKQ + kKQ;             // hi, lo
   static constexpr uint32_t oD = oKl + 2 * kF;           // hi, lo
@@ -164,9 +168,9 @@ struct PrepSmem {
   static constexpr uint32_t loop_end = oDt + 2 * kF128;
   // tail buffers (after the loop), placed around the [K;Q] tile which stays live
   static constexpr uint32_t sKX = 4 * C * D, sSq = 4 * C * (C + 4), sB = 8 * C;
-  static constexpr uint32_t sZ = 4 * 32 * 36;                                   // block-solve scratch
+  static constexpr uint32_t sZ = 4 * 32 * 36;            // block-solve scratch
   static constexpr uint32_t sTB = 2 * C * C;             // f16 T as B operand (C x C)
-  static constexpr Place p0{oW, oKQ, oKl};
+  static constexpr Place p0{oX, oKQ, oKl};
   static constexpr uint32_t tKX = p0.where(sKX);         // f16 [Kb | X] MN-major, C x 2D
   static constexpr Place p1 = p0.at(sKX);
   static constexpr uint32_t tTP = p1.where(kF128);       // f16 [I ; P], then [T ; PT], 128 x C
@@ -182,14 +186,22 @@ struct PrepSmem {
   static constexpr uint32_t tTB = p6.where(sTB);         // f16 T (B operand)
   static constexpr Place p7 = p6.at(sTB);
   static constexpr uint32_t bytes = p7.o2 > loop_end ? p7.o2 : loop_end;
-  static constexpr bool kExtraX = D > 2 * C;             // U/PU need their own TMEM columns
-  // columns: k_hat | p | [R;O_l] | N_l | u (refinement loop), or U/PU there (tail, when D > 2C)
-  static constexpr uint32_t tmem_cols_needed = 2 * C + 2 * D + (kExtraX ? D : C);
+  // TMEM columns: k_hat of even / odd steps (reused for the scores [G;P]) | p | u | [R;O_l] | N_l,
+  // and in the tail U/PU over the first 4C columns, or after N_l when D > 4C.
+  static constexpr bool kExtraX = D > 4 * C;
+  static constexpr uint32_t tmem_cols_needed = 4 * C + 2 * D + (kExtraX ? D : 0);
   static constexpr uint32_t tmem_cols =
       tmem_cols_needed <= 32 ? 32 : tmem_cols_needed <= 64 ? 64 : tmem_cols_needed <= 128 ? 128
                                   : tmem_cols_needed <= 256 ? 256 : 512;
   static_assert(NTH % 8 == 0 && NFD % 8 == 0, "column groups of 8");
+  static_assert(tmem_cols_needed <= 512, "TMEM");
 };
+
+// Barrier among the consumer warps only (the producer warp does not take part).
+template <int NT>
+__device__ __forceinline__ void csync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(NT) : "memory");
+}
 
 // One warp: acc = X[16 x K] Y[K x 16] (fp32, shared memory; row strides ldx and
 // ldy, multiples of 4 floats; X 16-byte aligned, Y 8-byte aligned).  Lane
@@ -278,7 +290,7 @@ __device__ __forceinline__ void solve_tri(const float* sA, float* sT, unsigned c
     *reinterpret_cast<uint4*>(sTB + (o / 8 + 1) * (16u * C) + (o + j) * 16u) = tc::cvt8(b);
   }
   if constexpr (NB >= 2) {
-    __syncthreads();
+    csync<NT>();
     // 16 -> 32: Y_p = A_(2p+1)(2p) T_(2p)(2p), then T_(2p+1)(2p) = -T_(2p+1)(2p+1) Y_p
     float acc[8];
     if (warp < NB / 2) {
@@ -289,7 +301,7 @@ __device__ __forceinline__ void solve_tri(const float* sA, float* sT, unsigned c
       for (int i = 0; i < 4; ++i)
         *reinterpret_cast<float2*>(sY + p * 16 * LDY + (rg + 4 * i) * LDY + 2 * cg) = make_float2(acc[2 * i], acc[2 * i + 1]);
     }
-    __syncthreads();
+    csync<NT>();
     if (warp < NB / 2) {
       const int p = warp, r = (2 * p + 1) * 16, c = 2 * p * 16;
       warp_blk16(sT + r * LD + r, LD, sY + p * 16 * LDY, LDY, 16, acc);
@@ -297,7 +309,7 @@ __device__ __forceinline__ void solve_tri(const float* sA, float* sT, unsigned c
     }
   }
   if constexpr (NB == 4) {
-    __syncthreads();
+    csync<NT>();
     // Y = A_lo T_lo  (rows 32..63, cols 0..31):  Y_(bi)(bj) = sum_{k = bj}^{1} A_(bi)(k) T_(k)(bj)
     float acc[8];
     if (warp < 4) {
@@ -309,7 +321,7 @@ __device__ __forceinline__ void solve_tri(const float* sA, float* sT, unsigned c
         *reinterpret_cast<float2*>(sY + ((bi - 2) * 16 + rg + 4 * i) * LDY + bj * 16 + 2 * cg) =
             make_float2(acc[2 * i], acc[2 * i + 1]);
     }
-    __syncthreads();
+    csync<NT>();
     // T_(bi)(bj) = -sum_{k = 2}^{bi} T_(bi)(k) Y_(k)(bj)
     if (warp < 4) {
       const int bi = 2 + (warp >> 1), bj = warp & 1;
@@ -326,13 +338,12 @@ __device__ __forceinline__ void ld_f8(const float* p, float (&v)[8]) {   // 32-b
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
 template <int D, int C>
-__global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __grid_constant__ PrepArgs p) {
+__global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const __grid_constant__ PrepArgs p) {
   using S = PrepSmem<D, C>;
-  constexpr int NT = S::NT, NTH = S::NTH, NFD = S::NFD, NQ = S::NQ;
+  constexpr int NT = S::NT, NW = S::NW, NTH = S::NTH, NFD = S::NFD, NQ = S::NQ;
   extern __shared__ __align__(1024) unsigned char sm[];
-  unsigned char* sW = sm + S::oW;
-  unsigned char* sWp = sm + S::oWp;
-  unsigned char* sGP = sm + S::oGP;
+  unsigned char* sX = sm + S::oX;
+  unsigned char* sY = sm + S::oY;
   unsigned char* sU = sm + S::oU;
   unsigned char* sKQ = sm + S::oKQ;
   unsigned char* sKl = sm + S::oKl;
@@ -342,13 +353,29 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
   float* sdec = reinterpret_cast<float*>(sm + S::oDec);
   float* sbl = reinterpret_cast<float*>(sm + S::oBeta);
   float* sinv = reinterpret_cast<float*>(sm + S::oInv);
-  uint64_t* bar_mma = reinterpret_cast<uint64_t*>(sm + S::oBar);
-  uint64_t* bar_wk = bar_mma + 1;
-  uint64_t* bar_wp = bar_mma + 2;
-  uint64_t* bar_in = bar_mma + 3;
+  float* spart = reinterpret_cast<float*>(sm + S::oPart);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::oBar);
+  // mbarriers.  Tile copies: bar_wk (W_k into X), bar_wp (W_p into Y), bar_in (K, Q, v).
+  // MMA completion (tcgen05.commit): bar_k[l % 2] (k_hat^(l)), bar_p (p^(l)), bar_gp (scores
+  // of step l), bar_6 (step l's [R;O_l], N_l updates), bar_x (internal), bar_mma (tail).
+  // Consumer warps -> producer (one arrival per warp): bar_u (u tiles written), bar_rb
+  // (pass B done: K_l, D_l tiles written, k_hat and p read), bar_r5 ([G;P] tiles written).
+  uint64_t* bar_mma = bars + 0;
+  uint64_t* bar_wk = bars + 1;
+  uint64_t* bar_wp = bars + 2;
+  uint64_t* bar_in = bars + 3;
+  uint64_t* bar_k = bars + 4;                  // [2]
+  uint64_t* bar_p = bars + 6;
+  uint64_t* bar_gp = bars + 7;
+  uint64_t* bar_6 = bars + 8;
+  uint64_t* bar_rb = bars + 9;
+  uint64_t* bar_r5 = bars + 10;
+  uint64_t* bar_x = bars + 11;
+  uint64_t* bar_u = bars + 12;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::oSlot);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool producer = warp == NW;
   const int quarter = warp & 3, cg = warp >> 2;
   const int row = quarter * 32 + lane;         // this thread's TMEM lane
   const int tb0 = cg * NTH;                    // first of this thread's token columns
@@ -366,17 +393,15 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
     return wsrc + WeightBlock<D>::index(h, l, L, which, part) * S::kW;
   };
 
-  // ---- setup: warp 0 starts the tile copies (K, Q rows and the v window by TMA,
-  //      W^(0) by bulk copy) and allocates TMEM; meanwhile the small parameters are
-  //      fetched and warp 1 scans the gates ----
+  // ---- setup: warp 0 starts every tile copy (K, Q rows and the v window by TMA, W_k^(0)
+  //      and W_p^(0) by bulk copy) and allocates TMEM; meanwhile the consumers fetch
+  //      their small parameters and warp 1 scans the gates ----
   __nv_bfloat16* kqraw = reinterpret_cast<__nv_bfloat16*>(sKl);   // [2C][D]: K rows, then Q rows
   __nv_bfloat16* vwin = reinterpret_cast<__nv_bfloat16*>(sD);     // [C + 8][D]: tokens t0-8 .. t0+C-1
   if (warp == 0) {
     if (lane == 0) {
-      tc::bar_init(bar_mma, 1);
-      tc::bar_init(bar_wk, 1);
-      tc::bar_init(bar_wp, 1);
-      tc::bar_init(bar_in, 1);
+      for (int i = 0; i < S::kBars; ++i)
+        tc::bar_init(bars + i, (bars + i == bar_u || bars + i == bar_rb || bars + i == bar_r5) ? NW : 1);
       tc::bar_fence_init();
       tc::bar_expect_tx(bar_in, (uint32_t)(3 * C + 8) * D * 2);
       tc::tma_load_4d(kqraw, &p.tm_k, 0, h, t0, b, bar_in);
@@ -384,9 +409,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
       tc::tma_load_4d(vwin, &p.tm_v, 0, h, t0 - 8, b, bar_in);
       if (L > 0) {                             // W^(0) streams in while the anchor is built
         tc::bar_expect_tx(bar_wk, S::kW);
-        tc::bulk_g2s(sW, wblock(0, 0, 0), S::kW, bar_wk);
+        tc::bulk_g2s(sX, wblock(0, 0, 0), S::kW, bar_wk);
         tc::bar_expect_tx(bar_wp, S::kW);
-        tc::bulk_g2s(sWp, wblock(0, 1, 0), S::kW, bar_wp);
+        tc::bulk_g2s(sY, wblock(0, 1, 0), S::kW, bar_wp);
       }
     }
     __syncwarp();
@@ -394,7 +419,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
   }
   // small per-thread parameters: conv taps (ca[m] multiplies v_{t-8+m}), w_beta^(0) of
   // this thread's feature, beta of token tid (used in the tail)
-  const bool cvalid = row < D;
+  const bool cvalid = row < D && !producer;
   float ca[8];
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
@@ -431,7 +456,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
   }
   // rows D..127 of the scaled-write tiles stay zero (A operand of the injection)
   if constexpr (D < 128)
-    for (int idx = tid; idx < (128 - D) * (C / 8) * 2; idx += NT) {
+    for (int idx = tid; idx < (128 - D) * (C / 8) * 2; idx += S::NTA) {
       const int part = idx / ((128 - D) * (C / 8));
       const int rem = idx % ((128 - D) * (C / 8));
       const int r = D + rem % (128 - D), s8 = rem / (128 - D);
@@ -439,7 +464,102 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
     }
   tc::fence_before();
   __syncthreads();
-  bool ok = tc::bar_wait(bar_in, 0);
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+  // TMEM columns: k_hat (even steps) | k_hat (odd steps) | p | u | [R;O_l] | N_l
+  const uint32_t t_k0 = tmem, t_p = tmem + 2 * C, t_u = tmem + 3 * C;
+  const uint32_t t_ro = tmem + 4 * C, t_n = tmem + 4 * C + D;
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  constexpr uint32_t idesc_proj = tc::idesc_f16(C, false, true);   // B = U, MN-major
+  constexpr uint32_t idesc_gp = tc::idesc_f16(C, false, true);
+  constexpr uint32_t idesc_cc = tc::idesc_f16(C, false, false);
+  constexpr uint32_t idesc_dd = tc::idesc_f16(D, false, false);
+  constexpr uint32_t S_s = (D / 8) * 128;      // token step of the feature x token tiles
+  bool ok = true;
+
+  if (producer) {
+    // ================= producer: tile copies and MMAs of the refinement loop =================
+    if (lane == 0 && L > 0) {
+      uint32_t ph_wk = 0, ph_wp = 0, ph_rb = 0, ph_r5 = 0, ph_x = 0;
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        ok &= tc::bar_wait(bar, parity);
+        tc::fence_after();
+      };
+      // projection W u^T of step l (which 0: W_k from X into the k_hat columns, 1: W_p from
+      // Y into the p columns): hi weights against u hi + lo, then (weights not exact in
+      // fp16) the lo weights against u hi; completion on `done`
+      auto proj = [&](int l, int which, uint32_t dst, unsigned char* wbuf, uint64_t* ldbar, uint32_t& ldph,
+                      uint64_t* done) {
+        for (int pass = 0; pass < 2; ++pass)
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc::mma(dst, tc::desc(wbuf + kk * 4096, 2048, 128), tc::desc(sU + pass * S::kU + kk * 256, 128, 16 * D),
+                    idesc_proj, pass > 0 || kk > 0);
+        if (need_lo) {
+          tc::commit(bar_x);
+          wait(bar_x, ph_x++ & 1);
+          tc::bar_expect_tx(ldbar, S::kW);
+          tc::bulk_g2s(wbuf, wblock(l, which, 1), S::kW, ldbar);
+          wait(ldbar, ldph++ & 1);
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc::mma(dst, tc::desc(wbuf + kk * 4096, 2048, 128), tc::desc(sU + kk * 256, 128, 16 * D), idesc_proj, true);
+        }
+        tc::commit(done);
+      };
+      wait(bar_u, 0);
+      wait(bar_wk, ph_wk++ & 1);
+      proj(0, 0, t_k0, sX, bar_wk, ph_wk, bar_k);
+      wait(bar_wp, ph_wp++ & 1);
+      proj(0, 1, t_p, sY, bar_wp, ph_wp, bar_p);
+      for (int l = 0; l < L; ++l) {
+        const uint32_t t_kl = t_k0 + (l & 1) * C;
+        if (l + 1 < L) {
+          // W_p^(l+1) into Y once p^(l) is done; W_k^(l+1) into X once k_hat^(l) is done and
+          // step l-1's [G;P] tiles have been read; then k_hat^(l+1) into the other columns
+          wait(bar_p, l & 1);
+          tc::bar_expect_tx(bar_wp, S::kW);
+          tc::bulk_g2s(sY, wblock(l + 1, 1, 0), S::kW, bar_wp);
+          wait(bar_k + (l & 1), (l >> 1) & 1);
+          if (l > 0) wait(bar_6, (l - 1) & 1);
+          tc::bar_expect_tx(bar_wk, S::kW);
+          tc::bulk_g2s(sX, wblock(l + 1, 0, 0), S::kW, bar_wk);
+          wait(bar_wk, ph_wk++ & 1);
+          proj(l + 1, 0, t_k0 + ((l + 1) & 1) * C, sX, bar_wk, ph_wk, bar_k + ((l + 1) & 1));
+        }
+        // [4] scores [G ; P] = [K ; Q] K_l^T (K_l = hi + lo) once pass B has written K_l
+        wait(bar_rb, ph_rb++ & 1);
+        for (int pass = 0; pass < 2; ++pass)
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc::mma(t_kl, tc::desc(sKQ + kk * 4096, 2048, 128),
+                    tc::desc(sKl + pass * S::kF + kk * 256, 128, S_s), idesc_gp, pass > 0 || kk > 0);
+        tc::commit(bar_gp);
+        // [6a] N_l += Dt_l^T K_l (3 passes)
+        {
+          const int ap[3] = {0, 0, 1}, bp[3] = {0, 1, 0};
+          for (int ps = 0; ps < 3; ++ps)
+            for (int kk = 0; kk < C / 16; ++kk)
+              tc::mma(t_n, tc::desc(sDt + ap[ps] * S::kF128 + kk * 4096, 2048, 128),
+                      tc::desc(sKl + bp[ps] * S::kF + kk * 2 * S_s, S_s, 128), idesc_dd, l > 0 || ps > 0 || kk > 0);
+        }
+        if (l + 1 < L) {                       // p^(l+1): pass B has read p^(l)
+          wait(bar_wp, ph_wp++ & 1);
+          proj(l + 1, 1, t_p, sY, bar_wp, ph_wp, bar_p);
+        }
+        // [6b] [R ; O_l] += [G ; P] D_l (3 passes) once the [G;P] tiles are in X
+        wait(bar_r5, ph_r5++ & 1);
+        {
+          const int ap[3] = {0, 0, 1}, bp[3] = {0, 1, 0};
+          for (int ps = 0; ps < 3; ++ps)
+            for (int kk = 0; kk < C / 16; ++kk)
+              tc::mma(t_ro, tc::desc(sX + ap[ps] * S::kF128 + kk * 4096, 2048, 128),
+                      tc::desc(sD + bp[ps] * S::kF + kk * 2 * S_s, S_s, 128), idesc_dd, l > 0 || ps > 0 || kk > 0);
+        }
+        tc::commit(bar_6);
+      }
+    }
+    __syncwarp();
+  } else {
+  // ================= consumers =================
+  ok = tc::bar_wait(bar_in, 0);
   // [K ; Q] rows as fp16: (row, a) at (a/8)*2048 + row*16 + (a%8)*2; rows of tokens past
   // the sequence end and rows >= 2C zero.  v rows past the sequence end are cleared too.
   for (int idx = tid; idx < 128 * (D / 8); idx += NT) {
@@ -461,13 +581,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
     for (int idx = tid; idx < (C + 8 - r0) * (D / 8); idx += NT)
       *reinterpret_cast<uint4*>(vwin + (r0 + idx / (D / 8)) * D + (idx % (D / 8)) * 8) = make_uint4(0u, 0u, 0u, 0u);
   }
-  __syncthreads();
-
-  tc::fence_after();
-  const uint32_t tmem = *tslot;
-  const uint32_t t_proj = tmem, t_p = tmem + C, t_ro = tmem + 2 * C, t_n = tmem + 2 * C + D;
-  const uint32_t t_u = tmem + 2 * C + 2 * D;   // anchor u (refinement loop)
-  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  csync<NT>();
   const int c = row;
   const bool fwarp = quarter < NQ;             // warp holds feature rows
 
@@ -518,89 +632,29 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
       }
     }
   }
+  // u tiles written: the producer may start the projections
   tc::fence_smem_to_async();
   tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
+  __syncwarp();
+  if (lane == 0) tc::bar_arrive(bar_u);
 
-  uint32_t ph_mma = 0, ph_wk = 0, ph_wp = 0;
-  auto wait_mma = [&]() {
-    ok &= tc::bar_wait(bar_mma, ph_mma & 1);
-    ++ph_mma;
-    tc::fence_after();
-  };
-  auto wait_bar = [&](uint64_t* bar, uint32_t& ph) {
-    ok &= tc::bar_wait(bar, ph & 1);
-    ++ph;
-  };
-
-  constexpr uint32_t idesc_proj = tc::idesc_f16(C, false, true);   // B = U, MN-major
-  constexpr uint32_t idesc_gp = tc::idesc_f16(C, false, true);
-  constexpr uint32_t idesc_cc = tc::idesc_f16(C, false, false);
-  constexpr uint32_t idesc_dd = tc::idesc_f16(D, false, false);
-  constexpr uint32_t S_s = (D / 8) * 128;      // token step of the feature x token tiles
   const bool gelu = !(p.flags & 1u);
-  float* spart = reinterpret_cast<float*>(sGP);  // per-warp partial sums during [3]
-
   for (int l = 0; l < L; ++l) {
-    // [1] W_p^(l) into the [G;P] buffers once the previous step's MMAs are done
-    //     (W_k^(l) was requested as soon as the previous projection finished)
-    if (l > 0) {
-      wait_mma();
-      if (tid == 0) {
-        tc::bar_expect_tx(bar_wp, S::kW);
-        tc::bulk_g2s(sWp, wblock(l, 1, 0), S::kW, bar_wp);
-      }
-    }
-    wait_bar(bar_wk, ph_wk);
-    wait_bar(bar_wp, ph_wp);
-    // [2] projections: k_hat^T = W_k u^T, p^T = W_p u^T (u = hi + lo)
-    if (tid == 0) {
-      tc::fence_after();
-      for (int pass = 0; pass < 2; ++pass)
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t bdesc = tc::desc(sU + pass * S::kU + kk * 256, 128, 16 * D);
-          const bool acc = pass > 0 || kk > 0;
-          tc::mma(t_proj, tc::desc(sW + kk * 4096, 2048, 128), bdesc, idesc_proj, acc);
-          tc::mma(t_p, tc::desc(sWp + kk * 4096, 2048, 128), bdesc, idesc_proj, acc);
-        }
-      tc::commit(bar_mma);
-    }
-    if (need_lo) {       // weights not exact in fp16: add W_lo u_hi
-      wait_mma();
-      if (tid == 0) {
-        tc::bar_expect_tx(bar_wk, S::kW);
-        tc::bulk_g2s(sW, wblock(l, 0, 1), S::kW, bar_wk);
-        tc::bar_expect_tx(bar_wp, S::kW);
-        tc::bulk_g2s(sWp, wblock(l, 1, 1), S::kW, bar_wp);
-      }
-      wait_bar(bar_wk, ph_wk);
-      wait_bar(bar_wp, ph_wp);
-      if (tid == 0) {
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t bdesc = tc::desc(sU + kk * 256, 128, 16 * D);
-          tc::mma(t_proj, tc::desc(sW + kk * 4096, 2048, 128), bdesc, idesc_proj, true);
-          tc::mma(t_p, tc::desc(sWp + kk * 4096, 2048, 128), bdesc, idesc_proj, true);
-        }
-        tc::commit(bar_mma);
-      }
-    }
-    wait_mma();
-    // the projection has read W_k^(l): stream W_k^(l+1) in behind the epilogues
-    if (tid == 0 && l + 1 < L) {
-      tc::bar_expect_tx(bar_wk, S::kW);
-      tc::bulk_g2s(sW, wblock(l + 1, 0, 0), S::kW, bar_wk);
-    }
+    const uint32_t t_kl = t_k0 + (l & 1) * C;  // k_hat^(l), then the scores of step l
+    ok &= tc::bar_wait(bar_k + (l & 1), (l >> 1) & 1);
+    tc::fence_after();
     // [3] epilogue.  Pass A: per token |k_hat|^2 and the gate logit w_beta . u,
-    //     summed over this warp's 32 features (reduce-scatter over 8-token groups).
+    //     summed over this warp's 32 features (reduce-scatter over 8-token groups); the
+    //     quarter-0 warps keep their sums, the others leave them in shared memory.
     {
       const float wb = wb_next;
       if (l + 1 < L && cvalid) wb_next = tc::ldg_early(p.wbeta + ((size_t)h * L + l + 1) * D + c);   // next step's
+      float keep_n[NTH / 8], keep_z[NTH / 8];
       if (fwarp) {
-#pragma unroll 1
+#pragma unroll
         for (int j8 = 0; j8 < NTH; j8 += 8) {
           uint32_t kr[8], ur[8];
-          tc::ld8a(t_proj + lane_base + tb0 + j8, kr);
+          tc::ld8a(t_kl + lane_base + tb0 + j8, kr);
           tc::ld8a(t_u + lane_base + tb0 + j8, ur);
           tc::wait_ld(kr, ur);
           float rn[8], rz[8];
@@ -632,30 +686,43 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
           }
           if ((lane & 3) == 0) {                // lane holds token j8 + lane/4 of its group
             const int t = tb0 + j8 + (lane >> 2);
-            spart[quarter * C + t] = rn[0];
-            spart[4 * C + quarter * C + t] = rz[0];
+            if (quarter == 0) {
+              keep_n[j8 / 8] = rn[0];
+              keep_z[j8 / 8] = rz[0];
+            } else {
+              spart[(quarter - 1) * 2 * C + t] = rn[0];
+              spart[(quarter - 1) * 2 * C + C + t] = rz[0];
+            }
           }
         }
       }
-      __syncthreads();
-      if (tid < C) {
-        float ss = 0.f, zz = 0.f;
+      csync<NT>();
+      if (quarter == 0 && (lane & 3) == 0) {   // sums over the quarters, in quarter order
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-          ss += spart[q * C + tid];
-          zz += spart[4 * C + q * C + tid];
+        for (int g = 0; g < NTH / 8; ++g) {
+          const int t = tb0 + 8 * g + (lane >> 2);
+          float ss = keep_n[g], zz = keep_z[g];
+#pragma unroll
+          for (int q = 1; q < NQ; ++q) {
+            ss += spart[(q - 1) * 2 * C + t];
+            zz += spart[(q - 1) * 2 * C + C + t];
+          }
+          const bool tv = t < nv;
+          sinv[t] = tv ? 1.0f / sqrtf(ss + 1e-6f) : 0.f;
+          sbl[t] = tv ? sigmoidf(zz) : 0.f;
         }
-        const bool tv = tid < nv;
-        sinv[tid] = tv ? 1.0f / sqrtf(ss + 1e-6f) : 0.f;
-        sbl[tid] = tv ? sigmoidf(zz) : 0.f;
       }
-      __syncthreads();
+      csync<NT>();
+      // p^(l) ready, and step l-1's MMAs have read the K_l, D_l tiles about to be rewritten
+      ok &= tc::bar_wait(bar_p, l & 1);
+      if (l > 0) ok &= tc::bar_wait(bar_6, (l - 1) & 1);
+      tc::fence_after();
       // Pass B: directions, residual step, factor tiles
       if (fwarp) {
 #pragma unroll
         for (int j8 = 0; j8 < NTH; j8 += 8) {
           uint32_t kr[8], pr[8];
-          tc::ld8a(t_proj + lane_base + tb0 + j8, kr);
+          tc::ld8a(t_kl + lane_base + tb0 + j8, kr);
           tc::ld8a(t_p + lane_base + tb0 + j8, pr);
           const int tb = tb0 + j8;
           float si[8], sb[8], sd[8];
@@ -693,22 +760,15 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
     }
     tc::fence_smem_to_async();
     tc::fence_before();
-    __syncthreads();
-    // [4] scores [G ; P] = [K ; Q] K_l^T   (K_l = hi + lo, MN-major B)
-    if (tid == 0) {
-      tc::fence_after();
-      for (int pass = 0; pass < 2; ++pass)
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma(t_proj, tc::desc(sKQ + kk * 4096, 2048, 128),
-                  tc::desc(sKl + pass * S::kF + kk * 256, 128, S_s), idesc_gp, pass > 0 || kk > 0);
-      tc::commit(bar_mma);
-    }
-    wait_mma();
+    __syncwarp();
+    if (lane == 0) tc::bar_arrive(bar_rb);
+    ok &= tc::bar_wait(bar_gp, l & 1);
+    tc::fence_after();
     // [5] epilogue: decay and causal mask, then hi/lo split; rows < C are G, C..2C-1 are P
     if (quarter * 32 < 2 * C) {
       uint32_t gr[NTH / 8][8];
 #pragma unroll
-      for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_proj + lane_base + tb0 + 8 * g, gr[g]);
+      for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_kl + lane_base + tb0 + 8 * g, gr[g]);
       tc::wait_ld();
 #pragma unroll
       for (int g = 0; g < NTH / 8; ++g) {
@@ -719,29 +779,25 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
         uint4 hi, lo;
         tc::split8(val, hi, lo);
         const uint32_t off = ((tb0 + 8 * g) / 8) * 2048u + row * 16u;
-        *reinterpret_cast<uint4*>(sGP + off) = hi;
-        *reinterpret_cast<uint4*>(sGP + S::kF128 + off) = lo;
+        *reinterpret_cast<uint4*>(sX + off) = hi;
+        *reinterpret_cast<uint4*>(sX + S::kF128 + off) = lo;
       }
     }
     tc::fence_smem_to_async();
     tc::fence_before();
-    __syncthreads();
-    // [6] [R ; O_l] += [G ; P] D_l  and  N_l += Dt_l^T K_l   (3 passes each)
-    if (tid == 0) {
-      tc::fence_after();
-      const int ap[3] = {0, 0, 1}, bp[3] = {0, 1, 0};
-      for (int ps = 0; ps < 3; ++ps)
-        for (int kk = 0; kk < C / 16; ++kk) {
-          const bool acc = l > 0 || ps > 0 || kk > 0;
-          tc::mma(t_ro, tc::desc(sGP + ap[ps] * S::kF128 + kk * 4096, 2048, 128),
-                  tc::desc(sD + bp[ps] * S::kF + kk * 2 * S_s, S_s, 128), idesc_dd, acc);
-          tc::mma(t_n, tc::desc(sDt + ap[ps] * S::kF128 + kk * 4096, 2048, 128),
-                  tc::desc(sKl + bp[ps] * S::kF + kk * 2 * S_s, S_s, 128), idesc_dd, acc);
-        }
-      tc::commit(bar_mma);
-    }
+    __syncwarp();
+    if (lane == 0) tc::bar_arrive(bar_r5);
   }
-  if (L > 0) wait_mma();
+  if (L > 0) {
+    ok &= tc::bar_wait(bar_6, (L - 1) & 1);
+    tc::fence_after();
+  }
+  uint32_t ph_mma = 0;
+  auto wait_mma = [&]() {
+    ok &= tc::bar_wait(bar_mma, ph_mma & 1);
+    ++ph_mma;
+    tc::fence_after();
+  };
 
   // ================= tail: gated delta rule, state-independent part =================
   const size_t cbase = ((size_t)b * H + h) * NC + chunk;
@@ -754,7 +810,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
   unsigned char* sKX = sm + S::tKX;
   unsigned char* sTB = sm + S::tTB;
   const uint32_t t_w = t_n;                                     // W / PW columns
-  const uint32_t t_x = S::kExtraX ? tmem + 2 * C + 2 * D : tmem; // U / PU columns
+  const uint32_t t_x = S::kExtraX ? tmem + 4 * C + 2 * D : tmem; // U / PU columns
   const int s_tok = row;
   const bool tok = s_tok < C;
   const bool tok_valid = tok && s_tok < nv;
@@ -788,12 +844,12 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
     tgam[tid] = expf(sg[tid]);
   }
   tc::fence_before();
-  __syncthreads();
+  csync<NT>();
   // (b) [K K^T ; Q K^T] = [K ; Q] K^T   (B = the K rows of the same tile, K-major)
   if (tid == 0) {
     tc::fence_after();
     for (int kk = 0; kk < D / 16; ++kk)
-      tc::mma(t_proj, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKQ + kk * 4096, 2048, 128),
+      tc::mma(t_k0, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKQ + kk * 4096, 2048, 128),
               idesc_cc, kk > 0);
     tc::commit(bar_mma);
   }
@@ -841,7 +897,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
     const float bt = isA ? tbeta[t] : 0.f;
     uint32_t ar[NTH / 8][8];
 #pragma unroll
-    for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_proj + lane_base + tb0 + 8 * g, ar[g]);
+    for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_k0 + lane_base + tb0 + 8 * g, ar[g]);
     tc::wait_ld();
 #pragma unroll
     for (int g = 0; g < NTH / 8; ++g) {
@@ -864,16 +920,16 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
     for (int g = 0; g < NTH / 8; ++g)
       *reinterpret_cast<uint4*>(sTP + ((tb0 + 8 * g) / 8) * 2048u + row * 16u) = make_uint4(0u, 0u, 0u, 0u);
   }
-  __syncthreads();
+  csync<NT>();
   // (e) T = (I + A)^-1 (fp32, and the fp16 B tile); then [T ; PT] = [I ; P] T on the tensor core
   solve_tri<C, NT>(tAf, tTf, sTB, tZf);
   tc::fence_smem_to_async();
   tc::fence_before();
-  __syncthreads();
+  csync<NT>();
   if (tid == 0) {
     tc::fence_after();
     for (int kk = 0; kk < C / 16; ++kk)
-      tc::mma(t_proj, tc::desc(sTP + kk * 4096, 2048, 128), tc::desc(sTB + kk * 2 * 16 * C, 16 * C, 128),
+      tc::mma(t_k0, tc::desc(sTP + kk * 4096, 2048, 128), tc::desc(sTB + kk * 2 * 16 * C, 16 * C, 128),
               idesc_cc, kk > 0);
     tc::commit(bar_mma);
   }
@@ -882,7 +938,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
   {
     uint32_t tr[NTH / 8][8];
 #pragma unroll
-    for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_proj + lane_base + tb0 + 8 * g, tr[g]);
+    for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_k0 + lane_base + tb0 + 8 * g, tr[g]);
     tc::wait_ld();
 #pragma unroll
     for (int g = 0; g < NTH / 8; ++g) {
@@ -895,7 +951,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
   }
   tc::fence_smem_to_async();
   tc::fence_before();
-  __syncthreads();
+  csync<NT>();
   // (f) [W ; PW] = [T ; PT] Kb,  [U ; PU] = [T ; PT] X   (B MN-major: LBO = 128, SBO = 16C)
   if (tid == 0) {
     tc::fence_after();
@@ -968,7 +1024,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NT, 1) prep_tc_kernel(const __
     }
   }
   if (tid == 0) p.gC[cbase] = tgam[C - 1];
-  if (!ok && lane == 0) atomicExch(p.status, 1);
+  }  // consumers
+  if (!ok) atomicExch(p.status, 1);
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, S::tmem_cols);

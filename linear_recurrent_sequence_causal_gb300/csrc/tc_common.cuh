@@ -124,6 +124,9 @@ __device__ __forceinline__ void bar_fence_init() { asm volatile("fence.mbarrier_
 __device__ __forceinline__ void bar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(bytes));
 }
+__device__ __forceinline__ void bar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
 // Bounded wait for the phase with parity `parity` to complete.  Returns false
 // (and the caller records an error) if it did not complete in `limit` polls.
 __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, uint32_t limit = (1u << 22)) {
