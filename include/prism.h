@@ -87,20 +87,23 @@ enum {
     PRISM_WS_KL = 1,       /* PRISM_F32: k^(l)              [B,T,H,L,d_k] fp32 */
     PRISM_WS_DL = 2,       /* PRISM_F32: beta^(l) delta^(l) [B,T,H,L,d_v] fp32 */
     PRISM_WS_WBLOCKS = 3,  /* PRISM_BF16: fp16 hi/lo weight blocks */
-    PRISM_WS_W = 4,        /* PRISM_BF16, per chunk [B,H,NC,C,d]: W = T diag(beta gamma) K   fp16 */
-    PRISM_WS_KT = 5,       /*   Kt = diag(gamma_C/gamma) K                                   fp16 */
-    PRISM_WS_QTH = 6,      /*   Qt = diag(gamma) Q - P W, hi half                            fp16 */
-    PRISM_WS_QTL = 7,      /*   Qt lo half                                                   fp16 */
-    PRISM_WS_U = 8,        /*   U = T diag(beta)(V - R)                                      fp32 */
-    PRISM_WS_OI = 9,       /*   O_intra = P U + O_l                                          fp32 */
-    PRISM_WS_N = 10,       /*   N = sum_l D_l^T diag(gamma_C/gamma) K_l, [B,H,NC,d,d]         fp32 */
-    PRISM_WS_GC = 11,      /*   gamma_C, [B,H,NC]                                            fp32 */
-    PRISM_WS_COUNT = 12
+    PRISM_WS_WQ = 4,       /* PRISM_BF16, per chunk [B,H,NC,2C,d]: W = T diag(beta gamma) K and
+                              Qt = diag(gamma) Q - P W (hi half), fp16, interleaved (below) */
+    PRISM_WS_QK = 5,       /*   Qt lo half and Kt = diag(gamma_C/gamma) K, fp16, interleaved   */
+    PRISM_WS_U = 6,        /*   U = T diag(beta)(V - R)                          [C,d]  fp32 */
+    PRISM_WS_OI = 7,       /*   O_intra = P U + O_l                              [C,d]  fp32 */
+    PRISM_WS_N = 8,        /*   N^T, N = sum_l D_l^T diag(gamma_C/gamma) K_l     [d,d]  fp32 */
+    PRISM_WS_GC = 9,       /*   gamma_C, [B,H,NC]                                       fp32 */
+    PRISM_WS_COUNT = 10
 };
 
 /* Inside one chunk, the PRISM_BF16 per-chunk arrays (R rows x d features) are
  * stored in 16-byte column pieces: element (r, f) at ((f / V) * R + r) * V + f % V
- * with V = 16 / element size (8 for fp16, 4 for fp32); N uses R = d. */
+ * with V = 16 / element size (8 for fp16, 4 for fp32).  U and O_intra use R = C; N^T
+ * (rows k, features v) uses R = d.  WQ and QK hold two fp16 maps each, sharing the
+ * pieces: in piece f / 8, first the C rows of W (resp. Qt lo), then the C rows of
+ * Qt hi (resp. Kt), so W(r, f) is at ((f / 8) * 2C + r) * 8 + f % 8 and
+ * Qt_hi(r, f) at ((f / 8) * 2C + C + r) * 8 + f % 8. */
 
 /* Bytes of device workspace for these dims (0 if the dims are invalid). */
 PRISM_API size_t prism_workspace_bytes(const prism_dims* dims);

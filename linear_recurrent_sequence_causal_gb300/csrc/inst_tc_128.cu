@@ -24,6 +24,11 @@ cudaError_t launch_scan_128(int C, int BV, const ScanArgs& a, cudaStream_t s) {
   if (C == 64 && BV == 32) return launch_scan_t<128, 64, 32>(a, s);
   return cudaErrorInvalidValue;
 }
+cudaError_t launch_scan_tc_128(int C, const ScanTcArgs& a, cudaStream_t s) {
+  if (C == 32) return launch_scan_tc_t<32>(a, s);
+  if (C == 64) return launch_scan_tc_t<64>(a, s);
+  return cudaErrorInvalidValue;
+}
 size_t prep_smem_128(int C) {
   switch (C) {
     case 16: return PrepSmem<128, 16>::bytes;

@@ -5,6 +5,7 @@
 
 #include "prep_tc.cuh"
 #include "scan_affine.cuh"
+#include "scan_tc.cuh"
 
 namespace prism {
 
@@ -26,6 +27,16 @@ cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
   if (e != cudaSuccess) return e;
   fn<<<a.B * a.H * (D / BV), S::NW * 32, S::bytes, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int C>
+cudaError_t launch_scan_tc_t(const ScanTcArgs& a, cudaStream_t s) {
+  using S = ScanTcSmem<C>;
+  auto fn = scan_tc_kernel<C>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
+  if (e != cudaSuccess) return e;
+  fn<<<a.B * a.H * (S::D / S::BV), S::NT, S::bytes, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -59,13 +59,15 @@ struct PrepArgs {
   // stored "piece-major": 16-byte column pieces, rows contiguous within a piece:
   // element (r, f) of an R-row array at ((f / V) * R + r) * V + f % V, V = 16 / elem
   // size.  A warp whose lanes hold consecutive rows then writes 512 contiguous bytes.
-  __half* Wc;                     // [C][D]  W = T diag(beta gamma) K
-  __half* Kt;                     // [C][D]  Kt = diag(gamma_C / gamma) K
-  __half* Qth;                    // [C][D]  Qt = diag(gamma) Q - P W, hi half
-  __half* Qtl;                    // [C][D]  lo half
+  // Two fp16 maps share each piece: WQ holds, per 8-feature piece, the C rows of W
+  // then the C rows of Qt_hi ([D/8][2][C][8]); QK the rows of Qt_lo then of Kt.
+  //   W  = T diag(beta gamma) K,   Qt = diag(gamma) Q - P W (hi + lo),
+  //   Kt = diag(gamma_C / gamma) K
+  __half* WQ;                     // [D/8][2][C][8]
+  __half* QK;                     // [D/8][2][C][8]
   float* U;                       // [C][D]  U = T diag(beta) (V - R)
   float* Oi;                      // [C][D]  O_intra = P U + O_l
-  float* Nl;                      // [D][D]  N = U^T Kt + N_l
+  float* Nt;                      // [D][D]  N^T (d_k x d_v), piece-major over d_v
   float* gC;                      // [1]     gamma_C
   int* status;                    // device error word (bounded waits)
 };
@@ -532,13 +534,13 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
             tc::mma(t_kl, tc::desc(sKQ + kk * 4096, 2048, 128),
                     tc::desc(sKl + pass * S::kF + kk * 256, 128, S_s), idesc_gp, pass > 0 || kk > 0);
         tc::commit(bar_gp);
-        // [6a] N_l += Dt_l^T K_l (3 passes)
+        // [6a] N_l^T += K_l^T Dt_l (3 passes; rows of N^T are k features, columns v features)
         {
-          const int ap[3] = {0, 0, 1}, bp[3] = {0, 1, 0};
+          const int ap[3] = {0, 1, 0}, bp[3] = {0, 0, 1};
           for (int ps = 0; ps < 3; ++ps)
             for (int kk = 0; kk < C / 16; ++kk)
-              tc::mma(t_n, tc::desc(sDt + ap[ps] * S::kF128 + kk * 4096, 2048, 128),
-                      tc::desc(sKl + bp[ps] * S::kF + kk * 2 * S_s, S_s, 128), idesc_dd, l > 0 || ps > 0 || kk > 0);
+              tc::mma(t_n, tc::desc(sKl + ap[ps] * S::kF + kk * 2 * S_s, S_s, 128),
+                      tc::desc(sDt + bp[ps] * S::kF128 + kk * 4096, 2048, 128), idesc_dd, l > 0 || ps > 0 || kk > 0);
         }
         if (l + 1 < L) {                       // p^(l+1): pass B has read p^(l)
           wait(bar_wp, ph_wp++ & 1);
@@ -632,11 +634,13 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       }
     }
   }
-  // u tiles written: the producer may start the projections
+  // u tiles written: the producer may start the projections.  The barrier keeps every
+  // lane's anchor writes ahead of the tail, whose buffers reuse this memory (L = 0).
   tc::fence_smem_to_async();
   tc::fence_before();
   __syncwarp();
   if (lane == 0) tc::bar_arrive(bar_u);
+  csync<NT>();
 
   const bool gelu = !(p.flags & 1u);
   for (int l = 0; l < L; ++l) {
@@ -820,9 +824,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   for (int g = 0; g < NFD / 8; ++g)
     vr[g] = tok_valid ? tc::ldg_early(reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t0 + s_tok) * H + h) * D + fb0 + 8 * g))
                       : make_uint4(0u, 0u, 0u, 0u);
-  // (a) N = N_l to global (its TMEM columns are reused below)
+  // (a) N^T to global (its TMEM columns are reused below)
   if (L > 0 && fwarp) {
-    float* nbase = p.Nl + cbase * D * D;      // piece-major: (c, a) at ((a/4)*D + c)*4 + a%4
+    float* nbase = p.Nt + cbase * D * D;      // piece-major over v: (k, v) at ((v/4)*D + k)*4 + v%4
     uint32_t nr[NFD / 8][8];
 #pragma unroll
     for (int g = 0; g < NFD / 8; ++g) tc::ld8a(t_n + lane_base + fb0 + 8 * g, nr[g]);
@@ -969,7 +973,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   if (quarter * 32 < 2 * C) {
     const bool isT = row < C, isPT = row >= C && row < 2 * C;
     const int t = isT ? row : row - C;
-    const size_t cb = cbase * C * D;         // piece-major chunk base
+    const size_t cb = cbase * C * D;         // piece-major chunk base (fp32 maps)
+    const size_t cb2 = cbase * 2 * C * D;    // interleaved fp16 maps
     const int tr = (isT || isPT) ? t : 0;
     const float gt = (isT || isPT) ? tgam[t] : 0.f;
     const float dct = (isT || isPT) ? sdec[t] : 0.f;
@@ -996,9 +1001,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
           wv[jj] = u2f(wr[jj]);
           kt[jj] = dct * __half2float(ke[jj]);
         }
-        const size_t o16 = cb + ((size_t)(f0 / 8) * C + tr) * 8;     // fp16 piece (8 values)
-        *reinterpret_cast<uint4*>(p.Wc + o16) = tc::cvt8(wv);
-        *reinterpret_cast<uint4*>(p.Kt + o16) = tc::cvt8(kt);
+        const size_t o16 = cb2 + ((size_t)(f0 / 8) * 2 * C + tr) * 8;   // fp16 piece (8 values)
+        *reinterpret_cast<uint4*>(p.WQ + o16) = tc::cvt8(wv);
+        *reinterpret_cast<uint4*>(p.QK + o16 + C * 8) = tc::cvt8(kt);
         *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4) * C + tr) * 4) =
             make_float4(u2f(xr[0]), u2f(xr[1]), u2f(xr[2]), u2f(xr[3]));
         *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4 + 1) * C + tr) * 4) =
@@ -1011,9 +1016,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
         for (int jj = 0; jj < 8; ++jj) qv[jj] = gt * __half2float(qe[jj]) - u2f(wr[jj]);
         uint4 hi, lo;
         tc::split8(qv, hi, lo);
-        const size_t o16 = cb + ((size_t)(f0 / 8) * C + tr) * 8;
-        *reinterpret_cast<uint4*>(p.Qth + o16) = hi;
-        *reinterpret_cast<uint4*>(p.Qtl + o16) = lo;
+        const size_t o16 = cb2 + ((size_t)(f0 / 8) * 2 * C + tr) * 8;
+        *reinterpret_cast<uint4*>(p.WQ + o16 + C * 8) = hi;
+        *reinterpret_cast<uint4*>(p.QK + o16) = lo;
         *reinterpret_cast<float4*>(p.Oi + cb + ((size_t)(f0 / 4) * C + tr) * 4) =
             make_float4(u2f(xr[0]) + u2f(orr[0]), u2f(xr[1]) + u2f(orr[1]), u2f(xr[2]) + u2f(orr[2]),
                         u2f(xr[3]) + u2f(orr[3]));

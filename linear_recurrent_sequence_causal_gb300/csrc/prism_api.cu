@@ -26,6 +26,7 @@ PRISM_DECL_TC(32)
 PRISM_DECL_TC(64)
 PRISM_DECL_TC(128)
 #undef PRISM_DECL_TC
+cudaError_t launch_scan_tc_128(int C, const ScanTcArgs& a, cudaStream_t s);
 
 cudaError_t launch_k2(int dtype, int D, int C, const K2Args& a, cudaStream_t s) {
   if (dtype != 0) return cudaErrorInvalidValue;
@@ -162,10 +163,8 @@ Layout layout(const prism_dims* d) {
   } else {
     const size_t per = (size_t)d->B * d->H * NC * C * D;
     if (d->L > 0) take(PRISM_WS_WBLOCKS, (size_t)d->H * d->L * 4 * 128 * D * 2);
-    take(PRISM_WS_W, per * 2);
-    take(PRISM_WS_KT, per * 2);
-    take(PRISM_WS_QTH, per * 2);
-    take(PRISM_WS_QTL, per * 2);
+    take(PRISM_WS_WQ, per * 4);
+    take(PRISM_WS_QK, per * 4);
     take(PRISM_WS_U, per * 4);
     take(PRISM_WS_OI, per * 4);
     if (d->L > 0) take(PRISM_WS_N, (size_t)d->B * d->H * NC * D * D * 4);
@@ -277,13 +276,11 @@ extern "C" PRISM_API int prism_prepare(const prism_dims* dims, const void* q, co
   a.v = static_cast<const __nv_bfloat16*>(v);
   a.log_alpha = log_alpha; a.beta = beta; a.conv_w = conv_w; a.wbeta = wbeta;
   a.wblocks = wblocks; a.wflag = status + 1; a.seq_lens = seq_lens;
-  a.Wc = region<__half>(workspace, Lo, PRISM_WS_W);
-  a.Kt = region<__half>(workspace, Lo, PRISM_WS_KT);
-  a.Qth = region<__half>(workspace, Lo, PRISM_WS_QTH);
-  a.Qtl = region<__half>(workspace, Lo, PRISM_WS_QTL);
+  a.WQ = region<__half>(workspace, Lo, PRISM_WS_WQ);
+  a.QK = region<__half>(workspace, Lo, PRISM_WS_QK);
   a.U = region<float>(workspace, Lo, PRISM_WS_U);
   a.Oi = region<float>(workspace, Lo, PRISM_WS_OI);
-  a.Nl = region<float>(workspace, Lo, PRISM_WS_N);
+  a.Nt = region<float>(workspace, Lo, PRISM_WS_N);
   a.gC = region<float>(workspace, Lo, PRISM_WS_GC);
   a.status = status;
   return prism::launch_prep(D, C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
@@ -312,15 +309,26 @@ extern "C" PRISM_API int prism_scan(const prism_dims* dims, const void* q, const
     a.seq_lens = seq_lens; a.out = out; a.final_state = final_state;
     return prism::launch_k2(0, D, C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
   }
+  if (D == 128 && (C == 32 || C == 64)) {   // tensor-core scan
+    prism::ScanTcArgs a;
+    a.B = dims->B; a.T = dims->T; a.H = dims->H;
+    a.WQ = region<const __half>(workspace, Lo, PRISM_WS_WQ);
+    a.QK = region<const __half>(workspace, Lo, PRISM_WS_QK);
+    a.U = region<const float>(workspace, Lo, PRISM_WS_U);
+    a.Oi = region<const float>(workspace, Lo, PRISM_WS_OI);
+    a.Nt = region<const float>(workspace, Lo, PRISM_WS_N);
+    a.gC = region<const float>(workspace, Lo, PRISM_WS_GC);
+    a.seq_lens = seq_lens; a.out = out; a.final_state = final_state;
+    a.status = region<int>(workspace, Lo, PRISM_WS_STATUS);
+    return prism::launch_scan_tc_128(C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
+  }
   prism::ScanArgs a;
   a.B = dims->B; a.T = dims->T; a.H = dims->H; a.L = dims->L;
-  a.Wc = region<const __half>(workspace, Lo, PRISM_WS_W);
-  a.Kt = region<const __half>(workspace, Lo, PRISM_WS_KT);
-  a.Qth = region<const __half>(workspace, Lo, PRISM_WS_QTH);
-  a.Qtl = region<const __half>(workspace, Lo, PRISM_WS_QTL);
+  a.WQ = region<const __half>(workspace, Lo, PRISM_WS_WQ);
+  a.QK = region<const __half>(workspace, Lo, PRISM_WS_QK);
   a.U = region<const float>(workspace, Lo, PRISM_WS_U);
   a.Oi = region<const float>(workspace, Lo, PRISM_WS_OI);
-  a.Nl = region<const float>(workspace, Lo, PRISM_WS_N);
+  a.Nt = region<const float>(workspace, Lo, PRISM_WS_N);
   a.gC = region<const float>(workspace, Lo, PRISM_WS_GC);
   a.seq_lens = seq_lens; a.out = out; a.final_state = final_state;
   return prism::launch_scan(D, C, pick_bv(dims), a, s) == cudaSuccess ? PRISM_OK

@@ -28,13 +28,11 @@ namespace prism {
 
 struct ScanArgs {
   int B, T, H, L;
-  const __half* Wc;
-  const __half* Kt;
-  const __half* Qth;
-  const __half* Qtl;
+  const __half* WQ;      // per chunk [d/8][2][C][8]: W rows, then Qt hi rows
+  const __half* QK;      // per chunk [d/8][2][C][8]: Qt lo rows, then Kt rows
   const float* U;
   const float* Oi;
-  const float* Nl;       // null when L == 0
+  const float* Nt;       // per chunk N^T piece-major over d_v; null when L == 0
   const float* gC;
   const int* seq_lens;
   float* out;            // [B][T][H][D] fp32
@@ -90,15 +88,19 @@ __global__ void __launch_bounds__(256) scan_affine_kernel(ScanArgs p) {
   for (int i = 0; i < MapS::kPerWarp; ++i) accS[i].zero();
 
   // Chunk maps are piece-major: fp16 (r, f) at ((f/8)*R + r)*8 + f%8, fp32 at
-  // ((f/4)*R + r)*4 + f%4 (R = C for the token-row maps, D for N).
+  // ((f/4)*R + r)*4 + f%4 (R = C for the token-row maps).  The fp16 maps come two to a
+  // piece (W then Qt hi, Qt lo then Kt) and are split into one tile each here; N
+  // arrives transposed, piece-major over its rows: (a, r) at ((r/4)*D + a)*4 + r%4.
   auto issue_loads = [&](int c, int buf) {
     unsigned char* base = sm + (buf ? S::oBuf1 : S::oBuf0);
     const size_t off = (cb0 + c) * (size_t)C * D;
-    const __half* src[4] = {p.Wc + off, p.Kt + off, p.Qth + off, p.Qtl + off};
+    // tiles W, Kt, Qt hi, Qt lo: source map and row offset inside its pieces
+    const __half* src[4] = {p.WQ + 2 * off, p.QK + 2 * off, p.WQ + 2 * off, p.QK + 2 * off};
+    const int roff[4] = {0, C, C, 0};
     constexpr int NP = C * D / 8;                       // 16-byte pieces per map
     for (int idx = tid; idx < 4 * NP; idx += NW * 32) {
       const int m = idx / NP, q = idx % NP;
-      cp_async16(base + m * S::kTile + q * 16, src[m] + (size_t)q * 8);
+      cp_async16(base + m * S::kTile + q * 16, src[m] + ((size_t)(q / C) * 2 * C + roff[m] + q % C) * 8);
     }
     // this tile's columns of U and O_intra (pieces r0/4 .. r0/4 + BV/4 - 1, C rows each)
     unsigned char* su = base + 4 * S::kTile;
@@ -108,14 +110,11 @@ __global__ void __launch_bounds__(256) scan_affine_kernel(ScanArgs p) {
       const float* g = (m == 0 ? p.U : p.Oi) + off + ((size_t)(r0 / 4) * C + q) * 4;
       cp_async16(su + m * S::kU + q * 16, g);
     }
-    if (p.Nl) {
-      // this tile's rows of N: in every piece a4 the rows r0 .. r0+BV-1 are contiguous
+    if (p.Nt) {
+      // this tile's rows of N: pieces r0/4 .. r0/4 + BV/4 - 1 of N^T, contiguous
       unsigned char* sn = su + 2 * S::kU;
-      const float* g0 = p.Nl + (cb0 + c) * (size_t)D * D;
-      for (int idx = tid; idx < BV * (D / 4); idx += NW * 32) {
-        const int a4 = idx / BV, r = idx % BV;
-        cp_async16(sn + idx * 16, g0 + ((size_t)a4 * D + r0 + r) * 4);
-      }
+      const float* g0 = p.Nt + (cb0 + c) * (size_t)D * D + (size_t)(r0 / 4) * D * 4;
+      for (int idx = tid; idx < BV * (D / 4); idx += NW * 32) cp_async16(sn + idx * 16, g0 + (size_t)idx * 4);
     }
   };
 
@@ -165,7 +164,10 @@ __global__ void __launch_bounds__(256) scan_affine_kernel(ScanArgs p) {
         for (int e = 0; e < 4; e += 2) {
           float2 nn = make_float2(0.f, 0.f);
           const int r = m0 + acc_row(e), a = n0 + acc_col(hh, e);
-          if (p.Nl) nn = *reinterpret_cast<const float2*>(sNt + ((a / 4) * BV + r) * 4 + a % 4);
+          if (p.Nt) {                                   // (r, a) of this tile's rows at ((r/4)*D + a)*4 + r%4
+            nn.x = sNt[((r / 4) * D + a) * 4 + r % 4];
+            nn.y = sNt[((r / 4) * D + a + 1) * 4 + r % 4];
+          }
           accS[i].v[hh][e] = fmaf(gC, accS[i].v[hh][e], nn.x);
           accS[i].v[hh][e + 1] = fmaf(gC, accS[i].v[hh][e + 1], nn.y);
         }

@@ -1,0 +1,290 @@
+// Kernel B on tcgen05 (bf16 I/O path, d = 128, chunk 32 or 64): the serial chain of
+// the chunkwise scan ("Technical Summary: PRISM", §2.1, S_t = S_{t-1} A_t + B_t
+// composed over a chunk), one CTA per (b, h, BV-wide slice of d_v):
+//   E   = U - W S0^T                      (C x BV)
+//   O   = O_intra + Qt S0^T               (C x BV), the chunk's outputs o_t = S_t q_t
+//   S1  = gamma_C S0 + E^T Kt + N         (BV x d_k)
+// Both products per chunk run on the tensor core with fp32 accumulators in TMEM:
+//   MMA1  [W ; Qt_hi] [S0_hi | S0_lo]^T   (128 x 2BV, K = d_k)   and
+//         [Qt_lo ; *] S0_hi^T              (128 x BV)
+//   MMA2  Kt^T [E_hi | E_lo]               (d_k x 2BV, K = C)
+// so W S0^T and Qt S0^T keep ~fp32 accuracy (hi*hi + hi*lo + lo*hi) and E enters
+// in two fp16 halves.  The chunk maps arrive in the layout prepare writes (16-byte
+// column pieces, in each piece W rows then Qt_hi rows, or Qt_lo rows then Kt rows),
+// which is exactly the K-major (resp. MN-major) operand layout, so every chunk is
+// five bulk copies into a double buffer.
+//
+// Threads: warps 0..3 own TMEM lanes 0..127 (thread k keeps row k of S^T, i.e.
+// column k of this slice of S, in fp32 registers across chunks); warp 4 issues the
+// copies and the MMAs.
+#pragma once
+
+#include "prism_common.cuh"
+#include "tc_common.cuh"
+
+namespace prism {
+
+struct ScanTcArgs {
+  int B, T, H;
+  const __half* WQ;      // per chunk [d/8][2][C][8]: W rows, then Qt hi rows
+  const __half* QK;      // per chunk [d/8][2][C][8]: Qt lo rows, then Kt rows
+  const float* U;        // per chunk piece-major [d/4][C][4]
+  const float* Oi;       // per chunk piece-major [d/4][C][4]
+  const float* Nt;       // per chunk N^T piece-major over d_v: [d/4][d_k][4]; null when L == 0
+  const float* gC;       // per chunk gamma_C
+  const int* seq_lens;
+  float* out;            // [B][T][H][d] fp32
+  float* final_state;    // [B][H][d_v][d_k] or null
+  int* status;           // device error word (bounded waits)
+};
+
+template <int C>
+struct ScanTcSmem {
+  static constexpr int D = 128, BV = 32;
+  static constexpr uint32_t kMap = 2 * C * D * 2;        // one interleaved fp16 map (WQ or QK)
+  static constexpr uint32_t kU = C * BV * 4;             // BV columns of U (or O_intra)
+  static constexpr uint32_t kN = BV * D * 4;             // BV rows of N
+  static constexpr uint32_t oWQ = 0, oQK = kMap, oU = 2 * kMap, oOi = oU + kU, oN = oOi + kU;
+  static constexpr uint32_t kBuf = oN + kN;
+  static constexpr uint32_t oBuf0 = 0, oBuf1 = kBuf;
+  static constexpr uint32_t oS = 2 * kBuf;               // [S_hi | S_lo]^T, MN-major B (K = d_k, N = 2BV)
+  static constexpr uint32_t kS = D * 2 * BV * 2;
+  static constexpr uint32_t oE = oS + kS;                // [E_hi | E_lo], MN-major B (K = C, N = 2BV)
+  static constexpr uint32_t kE = C * 2 * BV * 2;
+  static constexpr uint32_t oX = oE + kE;                // Qt_lo S0_hi^T rows, handed to the output rows
+  static constexpr uint32_t kX = C * BV * 4;
+  static constexpr uint32_t oBar = oX + kX;              // full[2], mma1, e_ready, mma2, s_ready
+  static constexpr uint32_t oSlot = oBar + 6 * 8;
+  static constexpr uint32_t bytes = oSlot + 16;
+  static constexpr int NT = 5 * 32;
+};
+
+template <int C>
+__global__ void __launch_bounds__(160, 1) scan_tc_kernel(ScanTcArgs p) {
+  using S = ScanTcSmem<C>;
+  constexpr int D = S::D, BV = S::BV, NSL = D / BV;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + S::oBar);   // [2]
+  uint64_t* bar_mma1 = bar_full + 2;
+  uint64_t* bar_e = bar_full + 3;
+  uint64_t* bar_mma2 = bar_full + 4;
+  uint64_t* bar_s = bar_full + 5;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::oSlot);
+  unsigned char* sS = sm + S::oS;
+  unsigned char* sE = sm + S::oE;
+  float* sX = reinterpret_cast<float*>(sm + S::oX);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slice = blockIdx.x % NSL, bh = blockIdx.x / NSL;
+  const int h = bh % p.H, b = bh / p.H;
+  const int v0 = slice * BV;
+  const int H = p.H, T_ = p.T;
+  const int NC = (T_ + C - 1) / C;
+  const int len = p.seq_lens ? min(max(p.seq_lens[b], 0), T_) : T_;
+  const int nchunks = (len + C - 1) / C;
+  const size_t cb0 = ((size_t)b * H + h) * NC;
+
+  if (tid == 0) {
+    tc::bar_init(bar_full, 1);
+    tc::bar_init(bar_full + 1, 1);
+    tc::bar_init(bar_mma1, 1);
+    tc::bar_init(bar_e, 4);
+    tc::bar_init(bar_mma2, 1);
+    tc::bar_init(bar_s, 4);
+    tc::bar_fence_init();
+  }
+  if (warp == 0) tc::alloc(tslot, 256);
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tmem = *tslot;
+  const uint32_t t_d1 = tmem, t_d2 = tmem + 2 * BV, t_d3 = tmem + 128;   // 64, 32 and 64 columns
+  bool ok = true;
+
+  if (warp == 4) {
+    // ================= issuer: chunk copies and MMAs =================
+    if (lane == 0) {
+      auto load = [&](int c, int buf) {
+        unsigned char* base = sm + (buf ? S::oBuf1 : S::oBuf0);
+        const size_t cb = cb0 + c;
+        tc::bar_expect_tx(bar_full + buf, 2 * S::kMap + 2 * S::kU + (p.Nt ? S::kN : 0));
+        tc::bulk_g2s(base + S::oWQ, p.WQ + cb * 2 * C * D, S::kMap, bar_full + buf);
+        tc::bulk_g2s(base + S::oQK, p.QK + cb * 2 * C * D, S::kMap, bar_full + buf);
+        tc::bulk_g2s(base + S::oU, p.U + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, bar_full + buf);
+        tc::bulk_g2s(base + S::oOi, p.Oi + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, bar_full + buf);
+        if (p.Nt) tc::bulk_g2s(base + S::oN, p.Nt + cb * D * D + (size_t)(v0 / 4) * D * 4, S::kN, bar_full + buf);
+      };
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        ok &= tc::bar_wait(bar, parity);
+        tc::fence_after();
+      };
+      constexpr uint32_t idesc_q2 = tc::idesc_f16(2 * BV, false, true);   // [W;Qt_hi] x [S_hi|S_lo]^T
+      constexpr uint32_t idesc_q1 = tc::idesc_f16(BV, false, true);       // [Qt_lo;*] x S_hi^T
+      constexpr uint32_t idesc_k = tc::idesc_f16(2 * BV, true, true);     // Kt^T x [E_hi|E_lo]
+      if (nchunks > 0) load(0, 0);
+      if (nchunks > 1) load(1, 1);
+      for (int c = 0; c < nchunks; ++c) {
+        const int buf = c & 1;
+        const unsigned char* base = sm + (buf ? S::oBuf1 : S::oBuf0);
+        wait(bar_s, c & 1);                    // state tile of chunk c written, chunk c-1 consumed
+        if (c >= 1 && c + 1 < nchunks) load(c + 1, (c + 1) & 1);
+        wait(bar_full + buf, (c >> 1) & 1);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t bs = tc::desc(sS + kk * 256, 128, 16 * D);
+          tc::mma(t_d1, tc::desc(base + S::oWQ + kk * 2 * (2 * C * 16), 2 * C * 16, 128), bs, idesc_q2, kk > 0);
+          tc::mma(t_d2, tc::desc(base + S::oQK + kk * 2 * (2 * C * 16), 2 * C * 16, 128), bs, idesc_q1, kk > 0);
+        }
+        tc::commit(bar_mma1);
+        wait(bar_e, c & 1);                    // E tile written
+        for (int kk = 0; kk < C / 16; ++kk)
+          tc::mma(t_d3, tc::desc(base + S::oQK + C * 16 + kk * 256, 128, 2 * C * 16),
+                  tc::desc(sE + kk * 256, 128, 16 * C), idesc_k, kk > 0);
+        tc::commit(bar_mma2);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= lanes: epilogues, state in registers =================
+    const int k = tid;                         // TMEM lane: row of [W;Qt], of E, of S^T
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float st[BV];                              // S^T[k][v0 .. v0+BV-1]
+#pragma unroll
+    for (int v = 0; v < BV; ++v) st[v] = 0.f;
+    auto write_state = [&]() {                 // [S_hi | S_lo]^T rows: (k, n) at (n/8)*16D + k*16 + (n%8)*2
+#pragma unroll
+      for (int g = 0; g < BV / 8; ++g) {
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = st[8 * g + j];
+        uint4 hi, lo;
+        tc::split8(x, hi, lo);
+        *reinterpret_cast<uint4*>(sS + g * (16u * D) + k * 16u) = hi;
+        *reinterpret_cast<uint4*>(sS + (BV / 8 + g) * (16u * D) + k * 16u) = lo;
+      }
+      tc::fence_smem_to_async();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(bar_s);
+    };
+    write_state();
+    for (int c = 0; c < nchunks; ++c) {
+      const int buf = c & 1;
+      const unsigned char* base = sm + (buf ? S::oBuf1 : S::oBuf0);
+      const float* sU = reinterpret_cast<const float*>(base + S::oU);
+      const float* sOi = reinterpret_cast<const float*>(base + S::oOi);
+      const float* sN = reinterpret_cast<const float*>(base + S::oN);
+      const size_t cbase = cb0 + c;
+      const int t0 = c * C, nv = min(C, len - t0);
+      const float gC = tc::ldg_early(p.gC + cbase);
+      ok &= tc::bar_wait(bar_mma1, c & 1);
+      tc::fence_after();
+      // ---- E = U - W S0^T (lanes < C); O = O_intra + Qt_hi S0^T (lanes C..2C-1) ----
+      float ov[BV];
+      if (warp * 32 < 2 * C) {
+        uint32_t d1[8][8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) tc::ld8a(t_d1 + lane_base + 8 * g, d1[g]);
+        tc::wait_ld();
+#pragma unroll
+        for (int g = 0; g < 8; ++g) tc::pin(d1[g]);
+        if (k < C) {
+          uint32_t d2[4][8];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) tc::ld8a(t_d2 + lane_base + 8 * g, d2[g]);
+          tc::wait_ld();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            tc::pin(d2[g]);
+            float uu[8], e8[8];
+            const float4 u0 = *reinterpret_cast<const float4*>(sU + ((2 * g) * C + k) * 4);
+            const float4 u1 = *reinterpret_cast<const float4*>(sU + ((2 * g + 1) * C + k) * 4);
+            uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
+            uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              e8[j] = uu[j] - (__uint_as_float(d1[g][j]) + __uint_as_float(d1[4 + g][j]));
+            uint4 hi, lo;
+            tc::split8(e8, hi, lo);
+            // [E_hi | E_lo]: (r, n) at (n/8)*16C + r*16 + (n%8)*2
+            *reinterpret_cast<uint4*>(sE + g * (16u * C) + k * 16u) = hi;
+            *reinterpret_cast<uint4*>(sE + (BV / 8 + g) * (16u * C) + k * 16u) = lo;
+            *reinterpret_cast<float4*>(sX + k * BV + 8 * g) =
+                make_float4(__uint_as_float(d2[g][0]), __uint_as_float(d2[g][1]), __uint_as_float(d2[g][2]), __uint_as_float(d2[g][3]));
+            *reinterpret_cast<float4*>(sX + k * BV + 8 * g + 4) =
+                make_float4(__uint_as_float(d2[g][4]), __uint_as_float(d2[g][5]), __uint_as_float(d2[g][6]), __uint_as_float(d2[g][7]));
+          }
+        } else if (k < 2 * C) {
+          const int r = k - C;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float4 o0 = *reinterpret_cast<const float4*>(sOi + ((2 * g) * C + r) * 4);
+            const float4 o1 = *reinterpret_cast<const float4*>(sOi + ((2 * g + 1) * C + r) * 4);
+            const float oi[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              ov[8 * g + j] = oi[j] + (__uint_as_float(d1[g][j]) + __uint_as_float(d1[4 + g][j]));
+          }
+        }
+      }
+      tc::fence_smem_to_async();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(bar_e);
+      asm volatile("bar.sync 1, 128;\n" ::: "memory");   // lanes: the Qt_lo rows are in sX
+      if (k >= C && k < 2 * C) {
+        const int r = k - C;
+        if (r < nv) {
+          float* dst = p.out + (((size_t)b * T_ + t0 + r) * H + h) * D + v0;
+#pragma unroll
+          for (int g = 0; g < BV / 4; ++g) {
+            const float4 x = *reinterpret_cast<const float4*>(sX + r * BV + 4 * g);
+            *reinterpret_cast<float4*>(dst + 4 * g) =
+                make_float4(ov[4 * g] + x.x, ov[4 * g + 1] + x.y, ov[4 * g + 2] + x.z, ov[4 * g + 3] + x.w);
+          }
+        }
+      }
+      // ---- S1^T = gamma_C S0^T + Kt^T E + N^T  (lane k) ----
+      ok &= tc::bar_wait(bar_mma2, c & 1);
+      tc::fence_after();
+      {
+        uint32_t d3[8][8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) tc::ld8a(t_d3 + lane_base + 8 * g, d3[g]);
+        tc::wait_ld();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          tc::pin(d3[g]);
+          tc::pin(d3[4 + g]);
+          float nn[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (p.Nt) {
+            const float4 n0 = *reinterpret_cast<const float4*>(sN + ((2 * g) * D + k) * 4);
+            const float4 n1 = *reinterpret_cast<const float4*>(sN + ((2 * g + 1) * D + k) * 4);
+            nn[0] = n0.x; nn[1] = n0.y; nn[2] = n0.z; nn[3] = n0.w;
+            nn[4] = n1.x; nn[5] = n1.y; nn[6] = n1.z; nn[7] = n1.w;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st[8 * g + j] = fmaf(gC, st[8 * g + j],
+                                 (__uint_as_float(d3[g][j]) + __uint_as_float(d3[4 + g][j])) + nn[j]);
+        }
+      }
+      write_state();
+    }
+    // padded tokens: zero output columns of this slice
+    for (size_t idx = tid; idx < (size_t)(T_ - len) * BV; idx += 128) {
+      const int t = len + (int)(idx / BV), col = (int)(idx % BV);
+      p.out[(((size_t)b * T_ + t) * H + h) * D + v0 + col] = 0.f;
+    }
+    if (p.final_state) {
+      float* fs = p.final_state + ((size_t)b * H + h) * D * D;
+#pragma unroll
+      for (int v = 0; v < BV; ++v) fs[(size_t)(v0 + v) * D + k] = st[v];
+    }
+  }
+  if (!ok) atomicExch(p.status, 1);
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tmem, 256);
+}
+
+}  // namespace prism

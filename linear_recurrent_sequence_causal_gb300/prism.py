@@ -24,7 +24,7 @@ ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
 STATIC_SCRATCH_BYTES = 32 << 20
 EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "prism_prepare",
            "prism_scan", "prism_forward_static", "prism_strerror")
-WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "W", "Kt", "Qth", "Qtl", "U", "Oi", "N", "gC")
+WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC")
 
 
 class PrismError(RuntimeError):

@@ -113,6 +113,19 @@ def chunk_maps(inp, kl, dl, C):
     return res
 
 
+def read_pair(ws, layout, name, shape):
+    """An interleaved fp16 region (two [..., C, F] maps sharing 16-byte column pieces:
+    in each piece the C rows of the first map, then the C rows of the second) as two
+    CPU fp64 numpy arrays in plain [..., C, F] order."""
+    off = layout[name]
+    C, F = shape[-2], shape[-1]
+    n = int(np.prod(shape)) * 2 * 2
+    flat = ws[off:off + n].view(torch.float16).double().cpu().numpy()
+    x = flat.reshape(tuple(shape[:-2]) + (F // 8, 2, C, 8))
+    first, second = x[..., 0, :, :], x[..., 1, :, :]
+    return (np.moveaxis(first, -3, -2).reshape(shape), np.moveaxis(second, -3, -2).reshape(shape))
+
+
 def read_region(ws, layout, name, dtype, shape, piece_major=True):
     """One workspace region as a CPU fp64 numpy array.  Per-chunk arrays
     (shape [..., R, F]) are stored piece-major: 16-byte column pieces, rows

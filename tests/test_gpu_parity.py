@@ -155,11 +155,12 @@ def test_no_gelu_ablation():
 
 
 @pytest.mark.parametrize("D,C,L,ragged", [(128, 64, 2, False), (64, 32, 3, True), (32, 16, 1, False),
-                                          (16, 64, 0, True), (128, 32, 4, True)])
+                                          (16, 64, 0, True), (128, 32, 4, True), (32, 64, 0, False),
+                                          (128, 64, 0, False)])
 def test_prepare_stage_bf16(D, C, L, ragged):
     """The tensor-core prepare kernel's per-chunk maps (W, Kt, Qt, U, O_intra, N,
     gamma_C) against an fp64 numpy restatement fed with the oracle's factors."""
-    from tests.parity import chunk_maps, read_region
+    from tests.parity import chunk_maps, read_pair, read_region
     wl = I.Workload("case", "bf16", 2, 3 * C + 5, 2, D, D, L, 4, C, seed=40 + D + C, ragged=False)
     inp = I.generate(wl)
     if ragged:
@@ -175,14 +176,14 @@ def test_prepare_stage_bf16(D, C, L, ragged):
     _, _, tr = oracle.forward(inp, trace=True)
     ref = chunk_maps(inp, tr["kl"], tr["dl"], C)
     shp = (wl.B, wl.H, NC, C, D)
-    got = {"W": read_region(ws, lay, "W", torch.float16, shp),
-           "Kt": read_region(ws, lay, "Kt", torch.float16, shp),
-           "Qt": read_region(ws, lay, "Qth", torch.float16, shp) + read_region(ws, lay, "Qtl", torch.float16, shp),
+    W, Qth = read_pair(ws, lay, "WQ", shp)
+    Qtl, Kt = read_pair(ws, lay, "QK", shp)
+    got = {"W": W, "Kt": Kt, "Qt": Qth + Qtl,
            "U": read_region(ws, lay, "U", torch.float32, shp),
            "Oi": read_region(ws, lay, "Oi", torch.float32, shp),
            "gC": read_region(ws, lay, "gC", torch.float32, (wl.B, wl.H, NC))}
-    if L:
-        got["N"] = read_region(ws, lay, "N", torch.float32, (wl.B, wl.H, NC, D, D))
+    if L:   # stored transposed: rows k, features v
+        got["N"] = np.swapaxes(read_region(ws, lay, "N", torch.float32, (wl.B, wl.H, NC, D, D)), -1, -2)
     lens = [wl.T] * wl.B if not ragged else inp["seq_lens"].tolist()
     for name, g in got.items():
         r = ref[name]
