@@ -14,9 +14,9 @@
 // which is exactly the K-major (resp. MN-major) operand layout, so every chunk is
 // five bulk copies into a double buffer.
 //
-// Threads: warps 0..3 own TMEM lanes 0..127 (thread k keeps row k of S^T, i.e.
-// column k of this slice of S, in fp32 registers across chunks); warp 4 issues the
-// copies and the MMAs.
+// Threads: warps 0..7 read TMEM lane quarter w % 4 and column half w / 4 (16 of the
+// slice's BV = 32 columns); thread (k, half) keeps those 16 entries of row k of S^T in
+// fp32 registers across chunks.  Warp 8 issues the copies and the MMAs.
 #pragma once
 
 #include "prism_common.cuh"
@@ -56,13 +56,14 @@ struct ScanTcSmem {
   static constexpr uint32_t oBar = oX + kX;              // full[2], mma1, e_ready, mma2, s_ready
   static constexpr uint32_t oSlot = oBar + 6 * 8;
   static constexpr uint32_t bytes = oSlot + 16;
-  static constexpr int NT = 5 * 32;
+  static constexpr int NW = 8;                          // epilogue warps
+  static constexpr int NT = (NW + 1) * 32;
 };
 
 template <int C>
-__global__ void __launch_bounds__(160, 1) scan_tc_kernel(ScanTcArgs p) {
+__global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArgs p) {
   using S = ScanTcSmem<C>;
-  constexpr int D = S::D, BV = S::BV, NSL = D / BV;
+  constexpr int D = S::D, BV = S::BV, NSL = D / BV, NW = S::NW, HB = BV / 2;
   extern __shared__ __align__(1024) unsigned char sm[];
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + S::oBar);   // [2]
   uint64_t* bar_mma1 = bar_full + 2;
@@ -88,9 +89,9 @@ __global__ void __launch_bounds__(160, 1) scan_tc_kernel(ScanTcArgs p) {
     tc::bar_init(bar_full, 1);
     tc::bar_init(bar_full + 1, 1);
     tc::bar_init(bar_mma1, 1);
-    tc::bar_init(bar_e, 4);
+    tc::bar_init(bar_e, NW);
     tc::bar_init(bar_mma2, 1);
-    tc::bar_init(bar_s, 4);
+    tc::bar_init(bar_s, NW);
     tc::bar_fence_init();
   }
   if (warp == 0) tc::alloc(tslot, 256);
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(160, 1) scan_tc_kernel(ScanTcArgs p) {
   const uint32_t t_d1 = tmem, t_d2 = tmem + 2 * BV, t_d3 = tmem + 128;   // 64, 32 and 64 columns
   bool ok = true;
 
-  if (warp == 4) {
+  if (warp == NW) {
     // ================= issuer: chunk copies and MMAs =================
     if (lane == 0) {
       auto load = [&](int c, int buf) {
@@ -127,7 +128,6 @@ __global__ void __launch_bounds__(160, 1) scan_tc_kernel(ScanTcArgs p) {
         const int buf = c & 1;
         const unsigned char* base = sm + (buf ? S::oBuf1 : S::oBuf0);
         wait(bar_s, c & 1);                    // state tile of chunk c written, chunk c-1 consumed
-        if (c >= 1 && c + 1 < nchunks) load(c + 1, (c + 1) & 1);
         wait(bar_full + buf, (c >> 1) & 1);
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t bs = tc::desc(sS + kk * 256, 128, 16 * D);
@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(160, 1) scan_tc_kernel(ScanTcArgs p) {
           tc::mma(t_d2, tc::desc(base + S::oQK + kk * 2 * (2 * C * 16), 2 * C * 16, 128), bs, idesc_q1, kk > 0);
         }
         tc::commit(bar_mma1);
+        if (c >= 1 && c + 1 < nchunks) load(c + 1, (c + 1) & 1);   // chunk c-1's buffer is free
         wait(bar_e, c & 1);                    // E tile written
         for (int kk = 0; kk < C / 16; ++kk)
           tc::mma(t_d3, tc::desc(base + S::oQK + C * 16 + kk * 256, 128, 2 * C * 16),
@@ -145,21 +146,23 @@ __global__ void __launch_bounds__(160, 1) scan_tc_kernel(ScanTcArgs p) {
     __syncwarp();
   } else {
     // ================= lanes: epilogues, state in registers =================
-    const int k = tid;                         // TMEM lane: row of [W;Qt], of E, of S^T
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float st[BV];                              // S^T[k][v0 .. v0+BV-1]
+    const int k = (warp & 3) * 32 + lane;      // TMEM lane: row of [W;Qt], of E, of S^T
+    const int hf = warp >> 2;                  // column half: slice columns hf*16 .. hf*16+15
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    float st[HB];                              // S^T[k][v0 + hf*16 ..]
 #pragma unroll
-    for (int v = 0; v < BV; ++v) st[v] = 0.f;
+    for (int v = 0; v < HB; ++v) st[v] = 0.f;
     auto write_state = [&]() {                 // [S_hi | S_lo]^T rows: (k, n) at (n/8)*16D + k*16 + (n%8)*2
 #pragma unroll
-      for (int g = 0; g < BV / 8; ++g) {
+      for (int g = 0; g < HB / 8; ++g) {
         float x[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) x[j] = st[8 * g + j];
         uint4 hi, lo;
         tc::split8(x, hi, lo);
-        *reinterpret_cast<uint4*>(sS + g * (16u * D) + k * 16u) = hi;
-        *reinterpret_cast<uint4*>(sS + (BV / 8 + g) * (16u * D) + k * 16u) = lo;
+        const int n8 = 2 * hf + g;             // column group of the slice
+        *reinterpret_cast<uint4*>(sS + n8 * (16u * D) + k * 16u) = hi;
+        *reinterpret_cast<uint4*>(sS + (BV / 8 + n8) * (16u * D) + k * 16u) = lo;
       }
       tc::fence_smem_to_async();
       tc::fence_before();
@@ -179,50 +182,61 @@ __global__ void __launch_bounds__(160, 1) scan_tc_kernel(ScanTcArgs p) {
       ok &= tc::bar_wait(bar_mma1, c & 1);
       tc::fence_after();
       // ---- E = U - W S0^T (lanes < C); O = O_intra + Qt_hi S0^T (lanes C..2C-1) ----
-      float ov[BV];
-      if (warp * 32 < 2 * C) {
-        uint32_t d1[8][8];
+      float ov[HB];
+      if ((warp & 3) * 32 < 2 * C) {
+        uint32_t d1[4][8];                     // hi columns hf*16.., lo columns 32 + hf*16..
 #pragma unroll
-        for (int g = 0; g < 8; ++g) tc::ld8a(t_d1 + lane_base + 8 * g, d1[g]);
-        tc::wait_ld();
-#pragma unroll
-        for (int g = 0; g < 8; ++g) tc::pin(d1[g]);
+        for (int g = 0; g < 2; ++g) {
+          tc::ld8a(t_d1 + lane_base + hf * HB + 8 * g, d1[g]);
+          tc::ld8a(t_d1 + lane_base + BV + hf * HB + 8 * g, d1[2 + g]);
+        }
         if (k < C) {
-          uint32_t d2[4][8];
+          uint32_t d2[2][8];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) tc::ld8a(t_d2 + lane_base + 8 * g, d2[g]);
+          for (int g = 0; g < 2; ++g) tc::ld8a(t_d2 + lane_base + hf * HB + 8 * g, d2[g]);
           tc::wait_ld();
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int g = 0; g < 2; ++g) {
+            tc::pin(d1[g]);
+            tc::pin(d1[2 + g]);
             tc::pin(d2[g]);
+            const int pc = 4 * hf + 2 * g;     // U piece (4 columns) of this group
             float uu[8], e8[8];
-            const float4 u0 = *reinterpret_cast<const float4*>(sU + ((2 * g) * C + k) * 4);
-            const float4 u1 = *reinterpret_cast<const float4*>(sU + ((2 * g + 1) * C + k) * 4);
+            const float4 u0 = *reinterpret_cast<const float4*>(sU + (pc * C + k) * 4);
+            const float4 u1 = *reinterpret_cast<const float4*>(sU + ((pc + 1) * C + k) * 4);
             uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
             uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              e8[j] = uu[j] - (__uint_as_float(d1[g][j]) + __uint_as_float(d1[4 + g][j]));
+              e8[j] = uu[j] - (__uint_as_float(d1[g][j]) + __uint_as_float(d1[2 + g][j]));
             uint4 hi, lo;
             tc::split8(e8, hi, lo);
             // [E_hi | E_lo]: (r, n) at (n/8)*16C + r*16 + (n%8)*2
-            *reinterpret_cast<uint4*>(sE + g * (16u * C) + k * 16u) = hi;
-            *reinterpret_cast<uint4*>(sE + (BV / 8 + g) * (16u * C) + k * 16u) = lo;
-            *reinterpret_cast<float4*>(sX + k * BV + 8 * g) =
+            const int n8 = 2 * hf + g;
+            *reinterpret_cast<uint4*>(sE + n8 * (16u * C) + k * 16u) = hi;
+            *reinterpret_cast<uint4*>(sE + (BV / 8 + n8) * (16u * C) + k * 16u) = lo;
+            float* xr = sX + k * BV + hf * HB + 8 * g;
+            *reinterpret_cast<float4*>(xr) =
                 make_float4(__uint_as_float(d2[g][0]), __uint_as_float(d2[g][1]), __uint_as_float(d2[g][2]), __uint_as_float(d2[g][3]));
-            *reinterpret_cast<float4*>(sX + k * BV + 8 * g + 4) =
+            *reinterpret_cast<float4*>(xr + 4) =
                 make_float4(__uint_as_float(d2[g][4]), __uint_as_float(d2[g][5]), __uint_as_float(d2[g][6]), __uint_as_float(d2[g][7]));
           }
-        } else if (k < 2 * C) {
-          const int r = k - C;
+        } else {
+          tc::wait_ld();
+          if (k < 2 * C) {
+            const int r = k - C;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const float4 o0 = *reinterpret_cast<const float4*>(sOi + ((2 * g) * C + r) * 4);
-            const float4 o1 = *reinterpret_cast<const float4*>(sOi + ((2 * g + 1) * C + r) * 4);
-            const float oi[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+            for (int g = 0; g < 2; ++g) {
+              tc::pin(d1[g]);
+              tc::pin(d1[2 + g]);
+              const int pc = 4 * hf + 2 * g;
+              const float4 o0 = *reinterpret_cast<const float4*>(sOi + (pc * C + r) * 4);
+              const float4 o1 = *reinterpret_cast<const float4*>(sOi + ((pc + 1) * C + r) * 4);
+              const float oi[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              ov[8 * g + j] = oi[j] + (__uint_as_float(d1[g][j]) + __uint_as_float(d1[4 + g][j]));
+              for (int j = 0; j < 8; ++j)
+                ov[8 * g + j] = oi[j] + (__uint_as_float(d1[g][j]) + __uint_as_float(d1[2 + g][j]));
+            }
           }
         }
       }
@@ -230,55 +244,59 @@ __global__ void __launch_bounds__(160, 1) scan_tc_kernel(ScanTcArgs p) {
       tc::fence_before();
       __syncwarp();
       if (lane == 0) tc::bar_arrive(bar_e);
-      asm volatile("bar.sync 1, 128;\n" ::: "memory");   // lanes: the Qt_lo rows are in sX
+      asm volatile("bar.sync 1, %0;\n" ::"n"(NW * 32) : "memory");   // the Qt_lo rows are in sX
       if (k >= C && k < 2 * C) {
         const int r = k - C;
         if (r < nv) {
-          float* dst = p.out + (((size_t)b * T_ + t0 + r) * H + h) * D + v0;
+          float* dst = p.out + (((size_t)b * T_ + t0 + r) * H + h) * D + v0 + hf * HB;
 #pragma unroll
-          for (int g = 0; g < BV / 4; ++g) {
-            const float4 x = *reinterpret_cast<const float4*>(sX + r * BV + 4 * g);
+          for (int g = 0; g < HB / 4; ++g) {
+            const float4 x = *reinterpret_cast<const float4*>(sX + r * BV + hf * HB + 4 * g);
             *reinterpret_cast<float4*>(dst + 4 * g) =
                 make_float4(ov[4 * g] + x.x, ov[4 * g + 1] + x.y, ov[4 * g + 2] + x.z, ov[4 * g + 3] + x.w);
           }
         }
       }
-      // ---- S1^T = gamma_C S0^T + Kt^T E + N^T  (lane k) ----
+      // ---- S1^T = gamma_C S0^T + Kt^T E + N^T  (lane k, this column half) ----
       ok &= tc::bar_wait(bar_mma2, c & 1);
       tc::fence_after();
       {
-        uint32_t d3[8][8];
+        uint32_t d3[4][8];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) tc::ld8a(t_d3 + lane_base + 8 * g, d3[g]);
+        for (int g = 0; g < 2; ++g) {
+          tc::ld8a(t_d3 + lane_base + hf * HB + 8 * g, d3[g]);
+          tc::ld8a(t_d3 + lane_base + BV + hf * HB + 8 * g, d3[2 + g]);
+        }
         tc::wait_ld();
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < 2; ++g) {
           tc::pin(d3[g]);
-          tc::pin(d3[4 + g]);
+          tc::pin(d3[2 + g]);
           float nn[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           if (p.Nt) {
-            const float4 n0 = *reinterpret_cast<const float4*>(sN + ((2 * g) * D + k) * 4);
-            const float4 n1 = *reinterpret_cast<const float4*>(sN + ((2 * g + 1) * D + k) * 4);
+            const int pc = 4 * hf + 2 * g;
+            const float4 n0 = *reinterpret_cast<const float4*>(sN + (pc * D + k) * 4);
+            const float4 n1 = *reinterpret_cast<const float4*>(sN + ((pc + 1) * D + k) * 4);
             nn[0] = n0.x; nn[1] = n0.y; nn[2] = n0.z; nn[3] = n0.w;
             nn[4] = n1.x; nn[5] = n1.y; nn[6] = n1.z; nn[7] = n1.w;
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             st[8 * g + j] = fmaf(gC, st[8 * g + j],
-                                 (__uint_as_float(d3[g][j]) + __uint_as_float(d3[4 + g][j])) + nn[j]);
+                                 (__uint_as_float(d3[g][j]) + __uint_as_float(d3[2 + g][j])) + nn[j]);
         }
       }
       write_state();
     }
     // padded tokens: zero output columns of this slice
-    for (size_t idx = tid; idx < (size_t)(T_ - len) * BV; idx += 128) {
+    for (size_t idx = tid; idx < (size_t)(T_ - len) * BV; idx += NW * 32) {
       const int t = len + (int)(idx / BV), col = (int)(idx % BV);
       p.out[(((size_t)b * T_ + t) * H + h) * D + v0 + col] = 0.f;
     }
     if (p.final_state) {
       float* fs = p.final_state + ((size_t)b * H + h) * D * D;
 #pragma unroll
-      for (int v = 0; v < BV; ++v) fs[(size_t)(v0 + v) * D + k] = st[v];
+      for (int v = 0; v < HB; ++v) fs[(size_t)(v0 + hf * HB + v) * D + k] = st[v];
     }
   }
   if (!ok) atomicExch(p.status, 1);
