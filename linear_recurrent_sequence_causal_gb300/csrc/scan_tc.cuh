@@ -51,8 +51,9 @@ struct ScanTcSmem {
   static constexpr uint32_t kS = D * 2 * BV * 2;
   static constexpr uint32_t oE = oS + kS;                // [E_hi | E_lo], MN-major B (K = C, N = 2BV)
   static constexpr uint32_t kE = C * 2 * BV * 2;
+  static constexpr int LDX = BV + 4;                     // padded row (conflict-free 16-byte accesses)
   static constexpr uint32_t oX = oE + kE;                // Qt_lo S0_hi^T rows, handed to the output rows
-  static constexpr uint32_t kX = C * BV * 4;
+  static constexpr uint32_t kX = C * LDX * 4;
   static constexpr uint32_t oBar = oX + kX;              // full[2], mma1, e_ready, mma2, s_ready
   static constexpr uint32_t oSlot = oBar + 6 * 8;
   static constexpr uint32_t bytes = oSlot + 16;
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
             const int n8 = 2 * hf + g;
             *reinterpret_cast<uint4*>(sE + n8 * (16u * C) + k * 16u) = hi;
             *reinterpret_cast<uint4*>(sE + (BV / 8 + n8) * (16u * C) + k * 16u) = lo;
-            float* xr = sX + k * BV + hf * HB + 8 * g;
+            float* xr = sX + k * S::LDX + hf * HB + 8 * g;
             *reinterpret_cast<float4*>(xr) =
                 make_float4(__uint_as_float(d2[g][0]), __uint_as_float(d2[g][1]), __uint_as_float(d2[g][2]), __uint_as_float(d2[g][3]));
             *reinterpret_cast<float4*>(xr + 4) =
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
           float* dst = p.out + (((size_t)b * T_ + t0 + r) * H + h) * D + v0 + hf * HB;
 #pragma unroll
           for (int g = 0; g < HB / 4; ++g) {
-            const float4 x = *reinterpret_cast<const float4*>(sX + r * BV + hf * HB + 4 * g);
+            const float4 x = *reinterpret_cast<const float4*>(sX + r * S::LDX + hf * HB + 4 * g);
             *reinterpret_cast<float4*>(dst + 4 * g) =
                 make_float4(ov[4 * g] + x.x, ov[4 * g + 1] + x.y, ov[4 * g + 2] + x.z, ov[4 * g + 3] + x.w);
           }
