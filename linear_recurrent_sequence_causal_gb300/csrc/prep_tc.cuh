@@ -188,6 +188,11 @@ struct PrepSmem {
   static constexpr uint32_t tTB = p6.where(sTB);         // f16 T (B operand)
   static constexpr Place p7 = p6.at(sTB);
   static constexpr uint32_t bytes = p7.o2 > loop_end ? p7.o2 : loop_end;
+  // N^T leaves through a shared-memory staging area and an asynchronous bulk store
+  // (draining while the tail computes) where the tail's own buffers leave the K_l / D /
+  // Dt region free.
+  static constexpr uint32_t kNT = D * D * 4;
+  static constexpr bool kStageN = p7.o2 <= oKl && oKl + kNT <= loop_end;
   // TMEM columns: k_hat of even / odd steps (reused for the scores [G;P]) | p | u | [R;O_l] | N_l,
   // and in the tail U/PU over the first 4C columns, or after N_l when D > 4C.
   static constexpr bool kExtraX = D > 4 * C;
@@ -700,7 +705,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
           }
         }
       }
-      csync<NT>();
+      // the four warps of this column group (one per lane quarter) hold all partial sums
+      // of its tokens: they synchronise among themselves
+      asm volatile("bar.sync %0, 128;\n" ::"r"(2 + cg) : "memory");
       if (quarter == 0 && (lane & 3) == 0) {   // sums over the quarters, in quarter order
 #pragma unroll
         for (int g = 0; g < NTH / 8; ++g) {
@@ -716,7 +723,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
           sbl[t] = tv ? sigmoidf(zz) : 0.f;
         }
       }
-      csync<NT>();
+      asm volatile("bar.sync %0, 128;\n" ::"r"(2 + cg) : "memory");
       // p^(l) ready, and step l-1's MMAs have read the K_l, D_l tiles about to be rewritten
       ok &= tc::bar_wait(bar_p, l & 1);
       if (l > 0) ok &= tc::bar_wait(bar_6, (l - 1) & 1);
@@ -826,7 +833,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
                       : make_uint4(0u, 0u, 0u, 0u);
   // (a) N^T to global (its TMEM columns are reused below)
   if (L > 0 && fwarp) {
-    float* nbase = p.Nt + cbase * D * D;      // piece-major over v: (k, v) at ((v/4)*D + k)*4 + v%4
+    // piece-major over v: (k, v) at ((v/4)*D + k)*4 + v%4, staged in shared memory when room
+    float* nbase = S::kStageN ? reinterpret_cast<float*>(sm + S::oKl) : p.Nt + cbase * D * D;
     uint32_t nr[NFD / 8][8];
 #pragma unroll
     for (int g = 0; g < NFD / 8; ++g) tc::ld8a(t_n + lane_base + fb0 + 8 * g, nr[g]);
@@ -847,8 +855,14 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     tbeta[tid] = beta_tok;
     tgam[tid] = expf(sg[tid]);
   }
+  if constexpr (S::kStageN) tc::fence_smem_to_async();
   tc::fence_before();
   csync<NT>();
+  if constexpr (S::kStageN)
+    if (L > 0 && tid == 0) {                 // N^T out while the tail runs
+      tc::bulk_s2g(p.Nt + cbase * D * D, sm + S::oKl, S::kNT);
+      tc::bulk_commit();
+    }
   // (b) [K K^T ; Q K^T] = [K ; Q] K^T   (B = the K rows of the same tile, K-major)
   if (tid == 0) {
     tc::fence_after();
@@ -970,11 +984,13 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   wait_mma();
   // (g) outputs.  Lanes 0..C-1: W (fp16), U (fp32), Kt (fp16).  Lanes C..2C-1:
   //     Qt = gamma Q - PW (fp16 hi/lo), O_intra = PU + O_l (fp32).
+  __half* oWQ = p.WQ + cbase * 2 * C * D;
+  __half* oQK = p.QK + cbase * 2 * C * D;
+  float* oU = p.U + cbase * C * D;
+  float* oOi = p.Oi + cbase * C * D;
   if (quarter * 32 < 2 * C) {
     const bool isT = row < C, isPT = row >= C && row < 2 * C;
     const int t = isT ? row : row - C;
-    const size_t cb = cbase * C * D;         // piece-major chunk base (fp32 maps)
-    const size_t cb2 = cbase * 2 * C * D;    // interleaved fp16 maps
     const int tr = (isT || isPT) ? t : 0;
     const float gt = (isT || isPT) ? tgam[t] : 0.f;
     const float dct = (isT || isPT) ? sdec[t] : 0.f;
@@ -1001,12 +1017,12 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
           wv[jj] = u2f(wr[jj]);
           kt[jj] = dct * __half2float(ke[jj]);
         }
-        const size_t o16 = cb2 + ((size_t)(f0 / 8) * 2 * C + tr) * 8;   // fp16 piece (8 values)
-        *reinterpret_cast<uint4*>(p.WQ + o16) = tc::cvt8(wv);
-        *reinterpret_cast<uint4*>(p.QK + o16 + C * 8) = tc::cvt8(kt);
-        *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4) * C + tr) * 4) =
+        const int o16 = ((f0 / 8) * 2 * C + tr) * 8;   // fp16 piece (8 values)
+        *reinterpret_cast<uint4*>(oWQ + o16) = tc::cvt8(wv);
+        *reinterpret_cast<uint4*>(oQK + o16 + C * 8) = tc::cvt8(kt);
+        *reinterpret_cast<float4*>(oU + ((f0 / 4) * C + tr) * 4) =
             make_float4(u2f(xr[0]), u2f(xr[1]), u2f(xr[2]), u2f(xr[3]));
-        *reinterpret_cast<float4*>(p.U + cb + ((size_t)(f0 / 4 + 1) * C + tr) * 4) =
+        *reinterpret_cast<float4*>(oU + ((f0 / 4 + 1) * C + tr) * 4) =
             make_float4(u2f(xr[4]), u2f(xr[5]), u2f(xr[6]), u2f(xr[7]));
       } else if (isPT) {
         const uint4 qraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + row * 16u);
@@ -1016,19 +1032,21 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
         for (int jj = 0; jj < 8; ++jj) qv[jj] = gt * __half2float(qe[jj]) - u2f(wr[jj]);
         uint4 hi, lo;
         tc::split8(qv, hi, lo);
-        const size_t o16 = cb2 + ((size_t)(f0 / 8) * 2 * C + tr) * 8;
-        *reinterpret_cast<uint4*>(p.WQ + o16 + C * 8) = hi;
-        *reinterpret_cast<uint4*>(p.QK + o16) = lo;
-        *reinterpret_cast<float4*>(p.Oi + cb + ((size_t)(f0 / 4) * C + tr) * 4) =
+        const int o16 = ((f0 / 8) * 2 * C + tr) * 8;
+        *reinterpret_cast<uint4*>(oWQ + o16 + C * 8) = hi;
+        *reinterpret_cast<uint4*>(oQK + o16) = lo;
+        *reinterpret_cast<float4*>(oOi + ((f0 / 4) * C + tr) * 4) =
             make_float4(u2f(xr[0]) + u2f(orr[0]), u2f(xr[1]) + u2f(orr[1]), u2f(xr[2]) + u2f(orr[2]),
                         u2f(xr[3]) + u2f(orr[3]));
-        *reinterpret_cast<float4*>(p.Oi + cb + ((size_t)(f0 / 4 + 1) * C + tr) * 4) =
+        *reinterpret_cast<float4*>(oOi + ((f0 / 4 + 1) * C + tr) * 4) =
             make_float4(u2f(xr[4]) + u2f(orr[4]), u2f(xr[5]) + u2f(orr[5]), u2f(xr[6]) + u2f(orr[6]),
                         u2f(xr[7]) + u2f(orr[7]));
       }
     }
   }
   if (tid == 0) p.gC[cbase] = tgam[C - 1];
+  if constexpr (S::kStageN)                  // the copy must have read N^T before the CTA exits
+    if (tid == 0) tc::bulk_wait_read();
   }  // consumers
   if (!ok) atomicExch(p.status, 1);
   tc::fence_before();
