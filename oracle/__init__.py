@@ -45,7 +45,7 @@ class _Problem(ctypes.Structure):
                 + [(n, _dp) for n in ("q", "k", "v", "log_alpha", "beta", "conv_w", "Wk", "Wp",
                                       "wbeta")]
                 + [("seq_lens", _ip), ("out", _dp), ("final_state", _dp),
-                   ("trace", ctypes.POINTER(_Trace))])
+                   ("trace", ctypes.POINTER(_Trace)), ("initial_state", _dp), ("v_hist", _dp)])
 
 
 def build(force: bool = False) -> str:
@@ -95,12 +95,15 @@ def _ptr(a):
 
 
 def forward(inp: dict, *, L: int | None = None, trace: bool = False, bh_items=None,
-            threads: int | None = None, identity_act: bool = False, lib_path=None):
+            threads: int | None = None, identity_act: bool = False, lib_path=None,
+            initial_state=None, v_hist=None):
     """Run the oracle on one input dict (see ``inputs.generate``).
 
     Returns ``(out [B,T,H,dv], final_state [B,H,dv,dk], trace_dict_or_None)``
     as fp64 numpy arrays.  ``bh_items`` restricts the work to a list of (b, h)
-    pairs; rows of the other pairs are left as NaN.
+    pairs; rows of the other pairs are left as NaN.  ``initial_state``
+    [B,H,dv,dk] and ``v_hist`` [B,H,w,dv] (the v rows of the w tokens before
+    t = 0, oldest first) resume a sequence; None means zeros.
     """
     lib = _load(lib_path)
     q, k, v = _f64(inp["q"]), _f64(inp["k"]), _f64(inp["v"])
@@ -117,6 +120,10 @@ def forward(inp: dict, *, L: int | None = None, trace: bool = False, bh_items=No
     sl = None if sl is None else np.ascontiguousarray(np.asarray(sl, dtype=np.int32))
     assert k.shape == q.shape and v.shape[:3] == (B, T, H) and la.shape == (B, T, H)
     assert conv_w.shape == (H, w, dv) and Wk.shape == (H, L, dk, dv) and Wp.shape == (H, L, dv, dv)
+    s0 = _f64(initial_state)
+    vh = _f64(v_hist)
+    assert s0 is None or s0.shape == (B, H, dv, dk)
+    assert vh is None or vh.shape == (B, H, w, dv)
     out = np.full((B, T, H, dv), np.nan)
     fs = np.full((B, H, dv, dk), np.nan)
     tr_arrays = None
@@ -134,7 +141,8 @@ def forward(inp: dict, *, L: int | None = None, trace: bool = False, bh_items=No
                  conv_w=_ptr(conv_w), Wk=_ptr(Wk), Wp=_ptr(Wp), wbeta=_ptr(wb),
                  seq_lens=sl.ctypes.data_as(_ip) if sl is not None else None,
                  out=_ptr(out), final_state=_ptr(fs),
-                 trace=ctypes.pointer(tr) if tr is not None else None)
+                 trace=ctypes.pointer(tr) if tr is not None else None,
+                 initial_state=_ptr(s0), v_hist=_ptr(vh))
     items = None
     n_items = 0
     if bh_items is not None:

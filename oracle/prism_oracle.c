@@ -28,7 +28,9 @@
  *     model could not reduce to Gated DeltaNet there.
  *   - normalize(x) = x / sqrt(|x|^2 + 1e-6); GELU is the exact erf form.
  *   - beta^(l) = sigmoid(w_beta^(l) . u_t) without bias; alpha_t = exp(log_alpha_t).
- *   - Readout o_t = S_t q_t (post-update, no scaling); S_0 = 0.
+ *   - Readout o_t = S_t q_t (post-update, no scaling); S_0 = 0 unless an initial
+ *     state is given, and the anchor of the first tokens reads zeros before t = 0
+ *     unless the v rows of the preceding tokens are given (resuming a sequence).
  *   - Right padding: for t >= len_b the output is 0 and the state is frozen.
  *
  * S is d_v x d_k.  The product S_{t-1} A_t is formed as
@@ -82,6 +84,8 @@ static int run_sequence(const oracle_problem* P, int b, int h) {
         return -1;
     }
     const oracle_trace* tr = P->trace;
+    if (P->initial_state)
+        memcpy(S, P->initial_state + ((size_t)b * P->H + h) * dv * dk, sizeof(double) * dv * dk);
 
     for (int t = 0; t < T; ++t) {
         double* o = P->out + off_bthx(P, b, t, h, dv);
@@ -95,11 +99,17 @@ static int run_sequence(const oracle_problem* P, int b, int h) {
         const double alpha = exp(P->log_alpha[((size_t)b * T + t) * P->H + h]);
         const double beta = P->beta[((size_t)b * T + t) * P->H + h];
 
-        /* Stage 1: anchor u_t = sum_{j=1..w} c_j (.) v_{t-j}, zero before t = 0. */
+        /* Stage 1: anchor u_t = sum_{j=1..w} c_j (.) v_{t-j}; before t = 0 the given
+           history (row w + t - j of v_hist), else zero. */
         for (int i = 0; i < dv; ++i) u[i] = 0.0;
         for (int j = 1; j <= w; ++j) {
-            if (t - j < 0) break;
-            const double* vp = P->v + off_bthx(P, b, t - j, h, dv);
+            const double* vp;
+            if (t - j >= 0)
+                vp = P->v + off_bthx(P, b, t - j, h, dv);
+            else if (P->v_hist)
+                vp = P->v_hist + (((size_t)b * P->H + h) * w + (w + t - j)) * dv;
+            else
+                break;
             const double* c = P->conv_w + ((size_t)h * w + (j - 1)) * dv;
             for (int i = 0; i < dv; ++i) u[i] += c[i] * vp[i];
         }

@@ -8,7 +8,10 @@
  *   conv_w [H,w,dv] (row j-1 multiplies v_{t-j});
  *   Wk [H,L,dk,dv]; Wp [H,L,dv,dv]; wbeta [H,L,dv];
  *   seq_lens [B] int32 or NULL (all sequences have length T);
- *   out [B,T,H,dv]; final_state [B,H,dv,dk] or NULL.
+ *   out [B,T,H,dv]; final_state [B,H,dv,dk] or NULL;
+ *   initial_state [B,H,dv,dk] or NULL (S_0 = 0);
+ *   v_hist [B,H,w,dv] or NULL: v of the w tokens before t = 0, oldest first, which
+ *   the anchor of the first tokens reads (zero history when NULL).
  */
 #ifndef PRISM_ORACLE_H
 #define PRISM_ORACLE_H
@@ -38,6 +41,8 @@ typedef struct {
     double* out;
     double* final_state;
     const oracle_trace* trace;
+    const double* initial_state;
+    const double* v_hist;
 } oracle_problem;
 
 /* Runs the (b,h) sequences listed in bh_items (index b*H+h; NULL = all) on

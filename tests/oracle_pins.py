@@ -26,8 +26,9 @@ import torch
 from linear_recurrent_sequence_causal_gb300.inputs import random_small
 
 
-def gdn_explicit(inp, T=None):
-    """Gated DeltaNet with explicit matrices: S <- S (alpha (I - beta k k^T)) + beta v k^T.
+def gdn_explicit(inp, T=None, S0=None):
+    """Gated DeltaNet with explicit matrices: S <- S (alpha (I - beta k k^T)) + beta v k^T,
+    starting from S0 [B,H,dv,dk] (zero when None).
 
     Independent of the oracle: forms every A_t as a d_k x d_k matrix.
     Returns out [B,T,H,dv] and final state [B,H,dv,dk].
@@ -43,7 +44,7 @@ def gdn_explicit(inp, T=None):
     for b in range(B):
         n = T if sl is None else int(sl[b])
         for h in range(H):
-            S = np.zeros((dv, dk))
+            S = np.zeros((dv, dk)) if S0 is None else np.array(S0[b, h], dtype=np.float64)
             for t in range(n):
                 kt = k[b, t, h]
                 A = np.exp(la[b, t, h]) * (I - be[b, t, h] * np.outer(kt, kt))
@@ -254,7 +255,43 @@ def pin_identity_activation(fwd):
         r = r - d
 
 
+def _slice_tokens(inp, t0, t1):
+    out = dict(inp)
+    for n in ("q", "k", "v", "log_alpha", "beta"):
+        out[n] = inp[n][:, t0:t1].contiguous()
+    return out
+
+
+def pin_resume_is_markov(fwd):
+    """The recurrence is Markov in (S, the last w values of v): running tokens
+    [0, T1), then [T1, T) from the reached state and the last w rows of v, gives the
+    outputs and final state of one run over [0, T) (split at several points)."""
+    inp = random_small(2, 29, 2, 5, 4, 2, 3, seed=25)
+    out, fs, _ = fwd(inp)
+    w = inp["conv_w"].shape[1]
+    for T1 in (1, 2, 11, 28):
+        o1, s1, _ = fwd(_slice_tokens(inp, 0, T1))
+        t0 = max(T1 - w, 0)
+        hist = np.zeros((2, 2, w, 4))
+        hist[:, :, w - (T1 - t0):] = inp["v"][:, t0:T1].double().numpy().transpose(0, 2, 1, 3)
+        o2, s2, _ = fwd(_slice_tokens(inp, T1, 29), initial_state=s1, v_hist=hist)
+        _close(o1, out[:, :T1], 1e-12, f"prefix outputs (T1={T1})")
+        _close(o2, out[:, T1:], 1e-12, f"resumed outputs (T1={T1})")
+        _close(s2, fs, 1e-12, f"resumed final state (T1={T1})")
+
+
+def pin_initial_state_gated_deltanet(fwd):
+    """L = 0 from a given state: the explicit-matrix Gated DeltaNet started at S0."""
+    inp = random_small(2, 17, 2, 6, 5, 0, 3, seed=26)
+    S0 = np.random.default_rng(3).standard_normal((2, 2, 5, 6))
+    out, fs, _ = fwd(inp, initial_state=S0)
+    ref_o, ref_s = gdn_explicit(inp, S0=S0)
+    _close(out, ref_o, 1e-12, "outputs")
+    _close(fs, ref_s, 1e-12, "final state")
+
+
 ALL_PINS = [pin_l0_is_gated_deltanet, pin_zero_conv_is_gated_deltanet, pin_write_rank,
             pin_telescoping, pin_brute_force_products, pin_prefix_sum, pin_no_write_no_output,
             pin_shortconv, pin_direction, pin_gain_and_gelu, pin_confidence_gate, pin_padding,
-            pin_causality, pin_identity_activation]
+            pin_causality, pin_identity_activation, pin_resume_is_markov,
+            pin_initial_state_gated_deltanet]

@@ -40,6 +40,9 @@ MUTANTS = [
     ("write_uses_unnormalised_p", "dl[i] = P->identity_act ? x : gelu_erf(x);",
      "dl[i] = P->identity_act ? x : gelu_erf(p[i]);"),
     ("alpha_not_exp", "const double alpha = exp(", "const double alpha = -("),
+    ("initial_state_ignored", "if (P->initial_state)\n        memcpy(", "if (0)\n        memcpy("),
+    ("history_ignored", "else if (P->v_hist)", "else if (0)"),
+    ("history_reversed", "(w + t - j)) * dv;", "(-1 - t + j)) * dv;"),
 ]
 
 
