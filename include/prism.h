@@ -131,6 +131,41 @@ PRISM_API int prism_forward(const prism_dims* dims,
                             float* out, float* final_state, const int32_t* seq_lens,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* prism_forward resuming sequences (for instance a long sequence processed in
+ * pieces): the chunkwise scan starts from initial_state [B,H,d_v,d_k] fp32 (NULL:
+ * zero), and the anchor of tokens 0..w-1 reads v_hist [B,H,w,d_v] in `dtype` — the
+ * v rows of the w tokens before t = 0, oldest first (NULL: zeros).  Running a
+ * sequence in two pieces, the second from the first's final_state and last w v
+ * rows, gives the one-piece result up to rounding.  The pages' layer has S_0 = 0
+ * and no history; these arguments only extend it to sequences that continue. */
+PRISM_API int prism_forward_from(const prism_dims* dims,
+                                 const void* q, const void* k, const void* v,
+                                 const float* log_alpha, const float* beta,
+                                 const float* conv_w, const float* Wk, const float* Wp,
+                                 const float* wbeta,
+                                 const float* initial_state, const void* v_hist,
+                                 float* out, float* final_state, const int32_t* seq_lens,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* One token of every sequence (dims->T must be 1; chunk is ignored): the
+ * recurrence of §2.1-2.2 of "Technical Summary: PRISM" applied to a single token,
+ * for streaming generation after a prism_forward_from / prism_forward prefix.
+ *   q, k, v     [B,H,d] in `dtype` (the token's rows)
+ *   log_alpha, beta [B,H] fp32
+ *   state       [B,H,d_v,d_k] fp32: S before the token on entry, after it on return
+ *   v_hist      [B,H,w,d_v] in `dtype`: the v rows of the w previous tokens, oldest
+ *               first; on return it has moved by one token (v appended)
+ *   out         [B,H,d_v] fp32, o_t = S_t q_t
+ * No workspace; every sequence advances (no seq_lens).  Arithmetic is fp32 on the
+ * CUDA cores.  The pages describe no decoding procedure; this entry point has no
+ * counterpart there beyond the recurrence itself. */
+PRISM_API int prism_decode_step(const prism_dims* dims,
+                                const void* q, const void* k, const void* v,
+                                const float* log_alpha, const float* beta,
+                                const float* conv_w, const float* Wk, const float* Wp,
+                                const float* wbeta,
+                                float* state, void* v_hist, float* out, void* stream);
+
 /* State-independent stage (fully parallel over chunks): anchor, refinement and,
  * on the PRISM_BF16 path, each chunk's factored affine state map; results go
  * to the workspace regions listed above. */

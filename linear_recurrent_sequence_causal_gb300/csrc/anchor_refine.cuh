@@ -44,6 +44,7 @@ struct K1Args {
   const float* Wp;
   const float* wbeta;
   const int* seq_lens;
+  const void* vhist;     // [B][H][w][D] v of the w tokens before t = 0 (oldest first), or null
   void* Kl;
   void* Dl;
 };
@@ -69,12 +70,15 @@ __global__ void __launch_bounds__(kThreads, 1) anchor_refine_kernel(K1Args p) {
   const T* v = static_cast<const T*>(p.v);
 
   // 1. v window: rows t0-w .. t0+TT-1 -> sVw[(i + w)][c] for token t0 + i.
-  //    Tokens outside [0, len) read as 0 (padding is selected away, never used).
+  //    Tokens outside [0, len) read as 0 (padding is selected away, never used); tokens
+  //    before t = 0 come from the history when one is given.
   for (int idx = tid; idx < (TT + w) * D; idx += kThreads) {
     const int rr = idx / D, c = idx % D;
     const int t = t0 - w + rr;
     float x = 0.f;
     if (t >= 0 && t < len) x = Elem<T>::to_f(v[(((size_t)b * T_ + t) * H + h) * D + c]);
+    else if (t < 0 && p.vhist)
+      x = Elem<T>::to_f(static_cast<const T*>(p.vhist)[(((size_t)b * H + h) * w + (w + t)) * D + c]);
     sVw[rr * D + c] = x;
   }
   __syncthreads();

@@ -68,6 +68,7 @@ struct K2Args {
   const int* seq_lens;
   void* out;
   float* final_state;
+  const float* initial_state;   // [B][H][D][D] entering state, or null (zero)
 };
 
 // Load rows [0, n_valid) of a C x D tile from global rows spaced `stride`
@@ -186,6 +187,18 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_scan_kernel(K2Args p) {
   Acc16 accS[MapDD::kPerWarp];
 #pragma unroll
   for (int i = 0; i < MapDD::kPerWarp; ++i) accS[i].zero();
+  if (p.initial_state) {
+    const float* s0 = p.initial_state + ((size_t)b * H + h) * D * D;
+#pragma unroll
+    for (int i = 0; i < MapDD::kPerWarp; ++i) {
+      if (!MapDD::valid(i)) continue;
+      const int m0 = MapDD::m0(i), n0 = MapDD::n0(i);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) accS[i].v[hh][e] = s0[(m0 + acc_row(e)) * D + n0 + acc_col(hh, e)];
+    }
+  }
 
   for (int c0 = 0; c0 < len; c0 += C) {
     const int nv = min(C, len - c0);

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "../../include/prism.h"
+#include "decode.cuh"
 #include "kernels.h"
 #include "kernels_tc.cuh"
 
@@ -27,6 +28,7 @@ PRISM_DECL_TC(64)
 PRISM_DECL_TC(128)
 #undef PRISM_DECL_TC
 cudaError_t launch_scan_tc_128(int C, const ScanTcArgs& a, cudaStream_t s);
+cudaError_t launch_decode(int dtype, int D, const DecodeArgs& a, cudaStream_t s);
 
 cudaError_t launch_k2(int dtype, int D, int C, const K2Args& a, cudaStream_t s) {
   if (dtype != 0) return cudaErrorInvalidValue;
@@ -232,17 +234,17 @@ extern "C" PRISM_API const char* prism_strerror(int code) {
   return "unknown error code";
 }
 
-extern "C" PRISM_API int prism_prepare(const prism_dims* dims, const void* q, const void* k,
-                                       const void* v, const float* log_alpha, const float* beta,
-                                       const float* conv_w, const float* Wk, const float* Wp,
-                                       const float* wbeta, const int32_t* seq_lens,
-                                       void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+int prepare_impl(const prism_dims* dims, const void* q, const void* k, const void* v,
+                 const float* log_alpha, const float* beta, const float* conv_w, const float* Wk,
+                 const float* Wp, const float* wbeta, const int32_t* seq_lens, const void* v_hist,
+                 void* workspace, size_t workspace_bytes, void* stream) {
   int rc = check_dims(dims);
   if (rc != PRISM_OK) return rc;
   rc = check_inputs(dims, q, k, v, log_alpha, beta, seq_lens, workspace, workspace_bytes);
   if (rc != PRISM_OK) return rc;
   if (dims->L > 0 && (!conv_w || !Wk || !Wp || !wbeta)) return PRISM_ERR_INVALID_ARG;
-  const void* wp[] = {conv_w, Wk, Wp, wbeta};
+  const void* wp[] = {conv_w, Wk, Wp, wbeta, v_hist};
   for (const void* p : wp)
     if (p && !aligned(p, 16)) return PRISM_ERR_MISALIGNED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -256,7 +258,7 @@ extern "C" PRISM_API int prism_prepare(const prism_dims* dims, const void* q, co
     a.B = dims->B; a.T = dims->T; a.H = dims->H; a.w = dims->conv_width; a.L = dims->L;
     a.flags = dims->flags;
     a.v = v; a.conv_w = conv_w; a.Wk = Wk; a.Wp = Wp; a.wbeta = wbeta;
-    a.seq_lens = seq_lens;
+    a.seq_lens = seq_lens; a.vhist = v_hist;
     a.Kl = region<float>(workspace, Lo, PRISM_WS_KL);
     a.Dl = region<float>(workspace, Lo, PRISM_WS_DL);
     return prism::launch_k1(0, D, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
@@ -276,6 +278,7 @@ extern "C" PRISM_API int prism_prepare(const prism_dims* dims, const void* q, co
   a.v = static_cast<const __nv_bfloat16*>(v);
   a.log_alpha = log_alpha; a.beta = beta; a.conv_w = conv_w; a.wbeta = wbeta;
   a.wblocks = wblocks; a.wflag = status + 1; a.seq_lens = seq_lens;
+  a.vhist = static_cast<const __nv_bfloat16*>(v_hist);
   a.WQ = region<__half>(workspace, Lo, PRISM_WS_WQ);
   a.QK = region<__half>(workspace, Lo, PRISM_WS_QK);
   a.U = region<float>(workspace, Lo, PRISM_WS_U);
@@ -285,18 +288,30 @@ extern "C" PRISM_API int prism_prepare(const prism_dims* dims, const void* q, co
   a.status = status;
   return prism::launch_prep(D, C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
 }
+}  // namespace
 
-extern "C" PRISM_API int prism_scan(const prism_dims* dims, const void* q, const void* k,
-                                    const void* v, const float* log_alpha, const float* beta,
-                                    const int32_t* seq_lens, void* workspace,
-                                    size_t workspace_bytes, float* out, float* final_state,
-                                    void* stream) {
+extern "C" PRISM_API int prism_prepare(const prism_dims* dims, const void* q, const void* k,
+                                       const void* v, const float* log_alpha, const float* beta,
+                                       const float* conv_w, const float* Wk, const float* Wp,
+                                       const float* wbeta, const int32_t* seq_lens,
+                                       void* workspace, size_t workspace_bytes, void* stream) {
+  return prepare_impl(dims, q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, seq_lens, nullptr,
+                      workspace, workspace_bytes, stream);
+}
+
+namespace {
+int scan_impl(const prism_dims* dims, const void* q, const void* k, const void* v,
+              const float* log_alpha, const float* beta, const int32_t* seq_lens,
+              const float* initial_state, void* workspace, size_t workspace_bytes, float* out,
+              float* final_state, void* stream) {
   int rc = check_dims(dims);
   if (rc != PRISM_OK) return rc;
   rc = check_inputs(dims, q, k, v, log_alpha, beta, seq_lens, workspace, workspace_bytes);
   if (rc != PRISM_OK) return rc;
   if (!out) return PRISM_ERR_INVALID_ARG;
-  if (!aligned(out, 16) || (final_state && !aligned(final_state, 16))) return PRISM_ERR_MISALIGNED;
+  if (!aligned(out, 16) || (final_state && !aligned(final_state, 16)) ||
+      (initial_state && !aligned(initial_state, 16)))
+    return PRISM_ERR_MISALIGNED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout Lo = layout(dims);
   const int D = dims->d_k, C = dims->chunk;
@@ -306,7 +321,7 @@ extern "C" PRISM_API int prism_scan(const prism_dims* dims, const void* q, const
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
     a.Kl = region<float>(workspace, Lo, PRISM_WS_KL);
     a.Dl = region<float>(workspace, Lo, PRISM_WS_DL);
-    a.seq_lens = seq_lens; a.out = out; a.final_state = final_state;
+    a.seq_lens = seq_lens; a.out = out; a.final_state = final_state; a.initial_state = initial_state;
     return prism::launch_k2(0, D, C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
   }
   if (D == 128 && (C == 32 || C == 64)) {   // tensor-core scan
@@ -318,7 +333,7 @@ extern "C" PRISM_API int prism_scan(const prism_dims* dims, const void* q, const
     a.Oi = region<const float>(workspace, Lo, PRISM_WS_OI);
     a.Nt = region<const float>(workspace, Lo, PRISM_WS_N);
     a.gC = region<const float>(workspace, Lo, PRISM_WS_GC);
-    a.seq_lens = seq_lens; a.out = out; a.final_state = final_state;
+    a.seq_lens = seq_lens; a.out = out; a.final_state = final_state; a.initial_state = initial_state;
     a.status = region<int>(workspace, Lo, PRISM_WS_STATUS);
     return prism::launch_scan_tc_128(C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
   }
@@ -330,9 +345,38 @@ extern "C" PRISM_API int prism_scan(const prism_dims* dims, const void* q, const
   a.Oi = region<const float>(workspace, Lo, PRISM_WS_OI);
   a.Nt = region<const float>(workspace, Lo, PRISM_WS_N);
   a.gC = region<const float>(workspace, Lo, PRISM_WS_GC);
-  a.seq_lens = seq_lens; a.out = out; a.final_state = final_state;
+  a.seq_lens = seq_lens; a.out = out; a.final_state = final_state; a.initial_state = initial_state;
   return prism::launch_scan(D, C, pick_bv(dims), a, s) == cudaSuccess ? PRISM_OK
                                                                       : PRISM_ERR_LAUNCH;
+}
+}  // namespace
+
+extern "C" PRISM_API int prism_scan(const prism_dims* dims, const void* q, const void* k,
+                                    const void* v, const float* log_alpha, const float* beta,
+                                    const int32_t* seq_lens, void* workspace,
+                                    size_t workspace_bytes, float* out, float* final_state,
+                                    void* stream) {
+  return scan_impl(dims, q, k, v, log_alpha, beta, seq_lens, nullptr, workspace, workspace_bytes,
+                   out, final_state, stream);
+}
+
+extern "C" PRISM_API int prism_forward_from(const prism_dims* dims, const void* q, const void* k,
+                                            const void* v, const float* log_alpha,
+                                            const float* beta, const float* conv_w,
+                                            const float* Wk, const float* Wp, const float* wbeta,
+                                            const float* initial_state, const void* v_hist,
+                                            float* out, float* final_state,
+                                            const int32_t* seq_lens, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
+  int rc = check_dims(dims);
+  if (rc != PRISM_OK) return rc;
+  if (!out) return PRISM_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || (final_state && !aligned(final_state, 16))) return PRISM_ERR_MISALIGNED;
+  rc = prepare_impl(dims, q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, seq_lens, v_hist,
+                    workspace, workspace_bytes, stream);
+  if (rc != PRISM_OK) return rc;
+  return scan_impl(dims, q, k, v, log_alpha, beta, seq_lens, initial_state, workspace,
+                   workspace_bytes, out, final_state, stream);
 }
 
 extern "C" PRISM_API int prism_forward(const prism_dims* dims, const void* q, const void* k,
@@ -341,13 +385,37 @@ extern "C" PRISM_API int prism_forward(const prism_dims* dims, const void* q, co
                                        const float* wbeta, float* out, float* final_state,
                                        const int32_t* seq_lens, void* workspace,
                                        size_t workspace_bytes, void* stream) {
-  int rc = check_dims(dims);
-  if (rc != PRISM_OK) return rc;
-  if (!out) return PRISM_ERR_INVALID_ARG;
-  if (!aligned(out, 16) || (final_state && !aligned(final_state, 16))) return PRISM_ERR_MISALIGNED;
-  rc = prism_prepare(dims, q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, seq_lens, workspace,
-                     workspace_bytes, stream);
-  if (rc != PRISM_OK) return rc;
-  return prism_scan(dims, q, k, v, log_alpha, beta, seq_lens, workspace, workspace_bytes, out,
-                    final_state, stream);
+  return prism_forward_from(dims, q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, nullptr, nullptr,
+                            out, final_state, seq_lens, workspace, workspace_bytes, stream);
+}
+
+extern "C" PRISM_API int prism_decode_step(const prism_dims* dims, const void* q, const void* k,
+                                           const void* v, const float* log_alpha,
+                                           const float* beta, const float* conv_w,
+                                           const float* Wk, const float* Wp, const float* wbeta,
+                                           float* state, void* v_hist, float* out, void* stream) {
+  if (!dims) return PRISM_ERR_INVALID_ARG;
+  if (dims->dtype != PRISM_F32 && dims->dtype != PRISM_BF16) return PRISM_ERR_INVALID_ARG;
+  if (dims->B <= 0 || dims->H <= 0 || dims->d_k <= 0 || dims->d_v <= 0 || dims->L < 0 ||
+      dims->conv_width <= 0 || dims->T != 1)
+    return PRISM_ERR_INVALID_ARG;
+  if (dims->flags & ~PRISM_FLAG_NO_GELU) return PRISM_ERR_INVALID_ARG;
+  const int D = dims->d_k;
+  if (dims->d_k != dims->d_v || (D != 16 && D != 32 && D != 64 && D != 128) || dims->L > kMaxL ||
+      dims->conv_width > kMaxW)
+    return PRISM_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !log_alpha || !beta || !conv_w || !state || !v_hist || !out)
+    return PRISM_ERR_INVALID_ARG;
+  if (dims->L > 0 && (!Wk || !Wp || !wbeta)) return PRISM_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, state, v_hist, out};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return PRISM_ERR_MISALIGNED;
+  prism::DecodeArgs a;
+  a.B = dims->B; a.H = dims->H; a.w = dims->conv_width; a.L = dims->L; a.flags = dims->flags;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.conv_w = conv_w;
+  a.Wk = Wk; a.Wp = Wp; a.wbeta = wbeta; a.state = state; a.vhist = v_hist; a.out = out;
+  return prism::launch_decode(dims->dtype == PRISM_F32 ? 0 : 1, D, a, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PRISM_OK
+             : PRISM_ERR_LAUNCH;
 }

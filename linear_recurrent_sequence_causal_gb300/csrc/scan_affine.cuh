@@ -37,6 +37,7 @@ struct ScanArgs {
   const int* seq_lens;
   float* out;            // [B][T][H][D] fp32
   float* final_state;    // [B][H][D][D] or null
+  const float* initial_state;   // [B][H][D][D] entering state, or null (zero)
 };
 
 template <int D, int C, int BV>
@@ -86,6 +87,18 @@ __global__ void __launch_bounds__(256) scan_affine_kernel(ScanArgs p) {
   Acc16 accS[MapS::kPerWarp];
 #pragma unroll
   for (int i = 0; i < MapS::kPerWarp; ++i) accS[i].zero();
+  if (p.initial_state) {
+    const float* s0 = p.initial_state + ((size_t)b * p.H + h) * D * D;
+#pragma unroll
+    for (int i = 0; i < MapS::kPerWarp; ++i) {
+      if (!MapS::valid(i)) continue;
+      const int m0 = MapS::m0(i), n0 = MapS::n0(i);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) accS[i].v[hh][e] = s0[(size_t)(r0 + m0 + acc_row(e)) * D + n0 + acc_col(hh, e)];
+    }
+  }
 
   // Chunk maps are piece-major: fp16 (r, f) at ((f/8)*R + r)*8 + f%8, fp32 at
   // ((f/4)*R + r)*4 + f%4 (R = C for the token-row maps).  The fp16 maps come two to a

@@ -35,6 +35,7 @@ struct ScanTcArgs {
   const int* seq_lens;
   float* out;            // [B][T][H][d] fp32
   float* final_state;    // [B][H][d_v][d_k] or null
+  const float* initial_state;   // [B][H][d_v][d_k] entering state, or null (zero)
   int* status;           // device error word (bounded waits)
 };
 
@@ -151,8 +152,9 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
     const int hf = warp >> 2;                  // column half: slice columns hf*16 .. hf*16+15
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float st[HB];                              // S^T[k][v0 + hf*16 ..]
+    const float* s0 = p.initial_state ? p.initial_state + ((size_t)b * H + h) * D * D : nullptr;
 #pragma unroll
-    for (int v = 0; v < HB; ++v) st[v] = 0.f;
+    for (int v = 0; v < HB; ++v) st[v] = s0 ? s0[(size_t)(v0 + hf * HB + v) * D + k] : 0.f;
     auto write_state = [&]() {                 // [S_hi | S_lo]^T rows: (k, n) at (n/8)*16D + k*16 + (n%8)*2
 #pragma unroll
       for (int g = 0; g < HB / 8; ++g) {

@@ -23,7 +23,8 @@ ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
           6: "PRISM_ERR_CUDA", 7: "PRISM_ERR_SCRATCH_LIMIT"}
 STATIC_SCRATCH_BYTES = 32 << 20
 EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "prism_prepare",
-           "prism_scan", "prism_forward_static", "prism_strerror")
+           "prism_scan", "prism_forward_static", "prism_strerror", "prism_forward_from",
+           "prism_decode_step")
 WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC")
 
 
@@ -70,6 +71,10 @@ def load():
             lib.prism_scan.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 7 + [ctypes.c_size_t] + [_vp] * 3
             lib.prism_scan.restype = ctypes.c_int
             lib.prism_forward_static.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 13
+            lib.prism_forward_from.restype = ctypes.c_int
+            lib.prism_forward_from.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 15 + [ctypes.c_size_t, _vp]
+            lib.prism_decode_step.restype = ctypes.c_int
+            lib.prism_decode_step.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 13
             lib.prism_forward_static.restype = ctypes.c_int
             lib.prism_strerror.argtypes = [ctypes.c_int]
             lib.prism_strerror.restype = ctypes.c_char_p
@@ -157,6 +162,58 @@ def prism_forward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, 
                               workspace.numel(), _stream_ptr(stream))
     _check(rc)
     return out, final_state
+
+
+def prism_forward_from(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *,
+                       initial_state=None, v_hist=None, out=None, final_state=None,
+                       seq_lens=None, workspace=None, stream=None, no_gelu=False, want_state=True):
+    """prism_forward resuming from ``initial_state`` [B,H,dv,dk] fp32 and ``v_hist``
+    [B,H,w,dv] (I/O dtype; the v rows of the w tokens before t = 0, oldest first)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu)
+    if out is None:
+        out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
+    if final_state is None and want_state:
+        final_state = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(dims, q.device)
+    rc = load().prism_forward_from(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                   _ptr(beta), _ptr(conv_w), _ptr(Wk), _ptr(Wp), _ptr(wbeta),
+                                   _ptr(initial_state), _ptr(v_hist), _ptr(out), _ptr(final_state),
+                                   _ptr(seq_lens), _ptr(workspace), workspace.numel(),
+                                   _stream_ptr(stream))
+    _check(rc)
+    return out, final_state
+
+
+def prism_decode_step(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, state, v_hist, *,
+                      out=None, stream=None, no_gelu=False):
+    """One token for every (b, h): q, k, v [B,H,d]; log_alpha, beta [B,H]; ``state``
+    [B,H,dv,dk] fp32 and ``v_hist`` [B,H,w,dv] are updated in place.  Returns out
+    [B,H,dv] fp32."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dims = make_dims(B, 1, H, dk, dv, conv_w.shape[1], L, 16, q.dtype, no_gelu)
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=torch.float32, device=q.device)
+    rc = load().prism_decode_step(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                  _ptr(beta), _ptr(conv_w), _ptr(Wk), _ptr(Wp), _ptr(wbeta),
+                                  _ptr(state), _ptr(v_hist), _ptr(out), _stream_ptr(stream))
+    _check(rc)
+    return out
+
+
+def v_history(v, w, end=None):
+    """The v rows of the w tokens before ``end`` (default: the end), oldest first, as a
+    contiguous [B,H,w,dv] tensor; rows before token 0 are zero."""
+    B, T, H, dv = v.shape
+    end = T if end is None else end
+    hist = torch.zeros((B, H, w, dv), dtype=v.dtype, device=v.device)
+    n = min(w, end)
+    if n > 0:
+        hist[:, :, w - n:] = v[:, end - n:end].permute(0, 2, 1, 3)
+    return hist.contiguous()
 
 
 def prism_forward_static(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, out=None,

@@ -90,3 +90,22 @@ def test_null_and_misaligned_pointers(lib):
     assert lib.prism_prepare(ctypes.byref(d), *[0x1000] * 10, 0x1010, big, None) == 3
     # scan: out NULL
     assert lib.prism_scan(ctypes.byref(d), *[0x1000] * 6, ws, big, None, None, None) == 1
+
+
+def test_decode_step_argument_errors(lib):
+    """prism_decode_step rejects bad dims and pointers before any launch."""
+    d = prism.Dims(B=2, T=1, H=2, d_k=32, d_v=32, conv_width=4, L=2, chunk=16, dtype=1, flags=0)
+    ok = [0x1000] * 12
+    d.T = 2
+    assert lib.prism_decode_step(ctypes.byref(d), *ok, None) == 1          # T must be 1
+    d.T = 1
+    d.d_k = 48
+    assert lib.prism_decode_step(ctypes.byref(d), *ok, None) == 2          # d_k != d_v
+    d.d_k = d.d_v = 96
+    assert lib.prism_decode_step(ctypes.byref(d), *ok, None) == 2          # unsupported head dim
+    d.d_k = d.d_v = 32
+    bad = list(ok); bad[9] = None                                          # no state
+    assert lib.prism_decode_step(ctypes.byref(d), *bad, None) == 1
+    bad = list(ok); bad[10] = 0x1008                                       # misaligned history
+    assert lib.prism_decode_step(ctypes.byref(d), *bad, None) == 3
+
