@@ -194,8 +194,9 @@ struct PrepSmem {
   // Dt region free.
   static constexpr uint32_t kNT = D * D * 4;
   static constexpr bool kStageN = p7.o2 <= oKl && oKl + kNT <= loop_end;
-  // TMEM columns: k_hat of even / odd steps (reused for the scores [G;P]) | p | u | [R;O_l] | N_l,
-  // and in the tail U/PU over the first 4C columns, or after N_l when D > 4C.
+  // TMEM columns: k_hat of even / odd steps (reused for the scores [G;P]) | p (the u hi and u lo
+  // products side by side) | [R;O_l] | N_l, and in the tail [W | U] over the first 4C columns
+  // (or W over N_l and U after it when D > 2C).
   static constexpr bool kExtraX = D > 4 * C;
   static constexpr uint32_t tmem_cols_needed = 4 * C + 2 * D + (kExtraX ? D : 0);
   static constexpr uint32_t tmem_cols =
@@ -344,6 +345,16 @@ __device__ __forceinline__ void ld_f8(const float* p, float (&v)[8]) {   // 32-b
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+// Eight fp16 values (one 16-byte piece) to fp32.
+__device__ __forceinline__ void h8_to_f(uint4 x, float (&f)[8]) {
+  const __half2* h = reinterpret_cast<const __half2*>(&x);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 t = __half22float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
 
 template <int D, int C>
 __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const __grid_constant__ PrepArgs p) {
@@ -474,11 +485,12 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tslot;
-  // TMEM columns: k_hat (even steps) | k_hat (odd steps) | p | u | [R;O_l] | N_l
-  const uint32_t t_k0 = tmem, t_p = tmem + 2 * C, t_u = tmem + 3 * C;
+  // TMEM columns: k_hat (even steps) | k_hat (odd steps) | p (W_p u_hi, W_p u_lo) | [R;O_l] | N_l
+  const uint32_t t_k0 = tmem, t_p = tmem + 2 * C;
   const uint32_t t_ro = tmem + 4 * C, t_n = tmem + 4 * C + D;
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   constexpr uint32_t idesc_proj = tc::idesc_f16(C, false, true);   // B = U, MN-major
+  constexpr uint32_t idesc_proj2 = tc::idesc_f16(2 * C, false, true);   // B = [u_hi | u_lo]
   constexpr uint32_t idesc_gp = tc::idesc_f16(C, false, true);
   constexpr uint32_t idesc_cc = tc::idesc_f16(C, false, false);
   constexpr uint32_t idesc_dd = tc::idesc_f16(D, false, false);
@@ -495,13 +507,22 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       };
       // projection W u^T of step l (which 0: W_k from X into the k_hat columns, 1: W_p from
       // Y into the p columns): hi weights against u hi + lo, then (weights not exact in
-      // fp16) the lo weights against u hi; completion on `done`
+      // fp16) the lo weights against u hi; completion on `done`.  k_hat accumulates both
+      // halves of u in one set of C columns (two MMAs per K step); p takes [u_hi | u_lo] as
+      // one N = 2C operand (one MMA per K step: an MMA costs about the same for any N up
+      // to 256) and leaves the two products side by side for the epilogue to add.
       auto proj = [&](int l, int which, uint32_t dst, unsigned char* wbuf, uint64_t* ldbar, uint32_t& ldph,
                       uint64_t* done) {
-        for (int pass = 0; pass < 2; ++pass)
+        if (which == 0) {
+          for (int pass = 0; pass < 2; ++pass)
+            for (int kk = 0; kk < D / 16; ++kk)
+              tc::mma(dst, tc::desc(wbuf + kk * 4096, 2048, 128), tc::desc(sU + pass * S::kU + kk * 256, 128, 16 * D),
+                      idesc_proj, pass > 0 || kk > 0);
+        } else {
           for (int kk = 0; kk < D / 16; ++kk)
-            tc::mma(dst, tc::desc(wbuf + kk * 4096, 2048, 128), tc::desc(sU + pass * S::kU + kk * 256, 128, 16 * D),
-                    idesc_proj, pass > 0 || kk > 0);
+            tc::mma(dst, tc::desc(wbuf + kk * 4096, 2048, 128), tc::desc(sU + kk * 256, 128, 16 * D), idesc_proj2,
+                    kk > 0);
+        }
         if (need_lo) {
           tc::commit(bar_x);
           wait(bar_x, ph_x++ & 1);
@@ -570,8 +591,10 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   ok = tc::bar_wait(bar_in, 0);
   // [K ; Q] rows as fp16: (row, a) at (a/8)*2048 + row*16 + (a%8)*2; rows of tokens past
   // the sequence end and rows >= 2C zero.  v rows past the sequence end are cleared too.
+  // (the piece index is rotated by the row so that eight consecutive lanes read eight
+  //  different bank groups of the raw rows and write eight different ones of the tile)
   for (int idx = tid; idx < 128 * (D / 8); idx += NT) {
-    const int r = idx % 128, a8 = idx / 128;
+    const int r = idx % 128, a8 = (idx / 128 + r) % (D / 8);
     const int t = r < C ? r : r - C;
     uint4 o = make_uint4(0u, 0u, 0u, 0u);
     if (r < 2 * C && t < nv) {
@@ -613,7 +636,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     }
   }
 
-  // ---- anchor u = sum_j c_j (.) v_{t-j} (TMEM and the U tile) and residual r = v - u
+  // ---- anchor u = sum_j c_j (.) v_{t-j} (the U tile, hi + lo) and residual r = v - u
   //      (registers); thread (feature c, column group) owns tokens tb0 .. tb0+NTH-1 ----
   float rres[NTH];
   {
@@ -639,7 +662,6 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
           *reinterpret_cast<uint4*>(sU + off) = uh;
           *reinterpret_cast<uint4*>(sU + S::kU + off) = ul;
         }
-        tc::st8(t_u + lane_base + tb0 + j8, uu);
       } else {
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) rres[j8 + jj] = 0.f;
@@ -669,15 +691,26 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       if (fwarp) {
 #pragma unroll
         for (int j8 = 0; j8 < NTH; j8 += 8) {
-          uint32_t kr[8], ur[8];
+          uint32_t kr[8];
           tc::ld8a(t_kl + lane_base + tb0 + j8, kr);
-          tc::ld8a(t_u + lane_base + tb0 + j8, ur);
-          tc::wait_ld(kr, ur);
+          float uf[8];                            // u = hi + lo from the U tile
+          if (cvalid) {
+            const uint32_t off = ((tb0 + j8) / 8) * (16u * D) + c * 16u;
+            float uh[8], ul[8];
+            h8_to_f(*reinterpret_cast<const uint4*>(sU + off), uh);
+            h8_to_f(*reinterpret_cast<const uint4*>(sU + S::kU + off), ul);
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) uf[jj] = uh[jj] + ul[jj];
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) uf[jj] = 0.f;
+          }
+          tc::wait_ld(kr);
           float rn[8], rz[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
             rn[jj] = u2f(kr[jj]) * u2f(kr[jj]);
-            rz[jj] = wb * u2f(ur[jj]);
+            rz[jj] = wb * uf[jj];
           }
           int n = 8;
 #pragma unroll
@@ -739,20 +772,21 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       if (fwarp) {
 #pragma unroll
         for (int j8 = 0; j8 < NTH; j8 += 8) {
-          uint32_t kr[8], pr[8];
+          uint32_t kr[8], pr[8], pl[8];
           tc::ld8a(t_kl + lane_base + tb0 + j8, kr);
           tc::ld8a(t_p + lane_base + tb0 + j8, pr);
+          tc::ld8a(t_p + C + lane_base + tb0 + j8, pl);
           const int tb = tb0 + j8;
           float si[8], sb[8], sd[8];
           ld_f8(sinv + tb, si);
           ld_f8(sbl + tb, sb);
           ld_f8(sdec + tb, sd);
-          tc::wait_ld(kr, pr);
+          tc::wait_ld(kr, pr, pl);
           float kd[8], dv[8], dt[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
             kd[jj] = u2f(kr[jj]) * si[jj];
-            const float x = u2f(pr[jj]) * rres[j8 + jj];
+            const float x = (u2f(pr[jj]) + u2f(pl[jj])) * rres[j8 + jj];
             const float dl = gelu ? gelu_erf(x) : x;
             rres[j8 + jj] -= dl;
             dv[jj] = sb[jj] * dl;
@@ -827,8 +861,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   unsigned char* sTP = sm + S::tTP;
   unsigned char* sKX = sm + S::tKX;
   unsigned char* sTB = sm + S::tTB;
-  const uint32_t t_w = t_n;                                     // W / PW columns
-  const uint32_t t_x = S::kExtraX ? tmem + 4 * C + 2 * D : tmem; // U / PU columns
+  // [W | U] side by side from column 0 when they fit below [R;O_l] (one N = 2D MMA per K
+  // step); otherwise W over N_l and U at column 0 (or after N_l when D > 4C)
+  constexpr bool kMergeWX = 2 * D <= 4 * C;
+  const uint32_t t_w = kMergeWX ? tmem : t_n;                                      // W / PW
+  const uint32_t t_x = kMergeWX ? tmem + D : (S::kExtraX ? tmem + 4 * C + 2 * D : tmem);   // U / PU
   const int s_tok = row;
   const bool tok = s_tok < C;
   const bool tok_valid = tok && s_tok < nv;
@@ -981,10 +1018,15 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   if (tid == 0) {
     tc::fence_after();
     constexpr uint32_t idesc_tx = tc::idesc_f16(D, false, true);
+    constexpr uint32_t idesc_tx2 = tc::idesc_f16(kMergeWX ? 2 * D : D, false, true);
     for (int kk = 0; kk < C / 16; ++kk) {
       const uint64_t adesc = tc::desc(sTP + kk * 4096, 2048, 128);
-      tc::mma(t_w, adesc, tc::desc(sKX + kk * 256, 128, 16 * C), idesc_tx, kk > 0);
-      tc::mma(t_x, adesc, tc::desc(sKX + (D / 8) * (16 * C) + kk * 256, 128, 16 * C), idesc_tx, kk > 0);
+      if constexpr (kMergeWX) {                // B = [Kb | X] as one N = 2D operand
+        tc::mma(t_w, adesc, tc::desc(sKX + kk * 256, 128, 16 * C), idesc_tx2, kk > 0);
+      } else {
+        tc::mma(t_w, adesc, tc::desc(sKX + kk * 256, 128, 16 * C), idesc_tx, kk > 0);
+        tc::mma(t_x, adesc, tc::desc(sKX + (D / 8) * (16 * C) + kk * 256, 128, 16 * C), idesc_tx, kk > 0);
+      }
     }
     tc::commit(bar_mma);
   }
