@@ -194,8 +194,8 @@ struct PrepSmem {
   // Dt region free.
   static constexpr uint32_t kNT = D * D * 4;
   static constexpr bool kStageN = p7.o2 <= oKl && oKl + kNT <= loop_end;
-  // TMEM columns: k_hat of even / odd steps (reused for the scores [G;P]) | p (the u hi and u lo
-  // products side by side) | [R;O_l] | N_l, and in the tail [W | U] over the first 4C columns
+  // TMEM columns: k_hat of even / odd steps | p (the u hi and u lo products side by side; the
+  // scores [G;P] of K_l hi and lo once p has been read) | [R;O_l] | N_l, and in the tail [W | U] over the first 4C columns
   // (or W over N_l and U after it when D > 2C).
   static constexpr bool kExtraX = D > 4 * C;
   static constexpr uint32_t tmem_cols_needed = 4 * C + 2 * D + (kExtraX ? D : 0);
@@ -491,7 +491,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   constexpr uint32_t idesc_proj = tc::idesc_f16(C, false, true);   // B = U, MN-major
   constexpr uint32_t idesc_proj2 = tc::idesc_f16(2 * C, false, true);   // B = [u_hi | u_lo]
-  constexpr uint32_t idesc_gp = tc::idesc_f16(C, false, true);
+  constexpr uint32_t idesc_gp2 = tc::idesc_f16(2 * C, false, true);
   constexpr uint32_t idesc_cc = tc::idesc_f16(C, false, false);
   constexpr uint32_t idesc_dd = tc::idesc_f16(D, false, false);
   constexpr uint32_t S_s = (D / 8) * 128;      // token step of the feature x token tiles
@@ -554,12 +554,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
           wait(bar_wk, ph_wk++ & 1);
           proj(l + 1, 0, t_k0 + ((l + 1) & 1) * C, sX, bar_wk, ph_wk, bar_k + ((l + 1) & 1));
         }
-        // [4] scores [G ; P] = [K ; Q] K_l^T (K_l = hi + lo) once pass B has written K_l
+        // [4] scores [G ; P] = [K ; Q] [K_l,hi | K_l,lo]^T into the p columns (pass B has read
+        //     p^(l)) as one N = 2C operand; the epilogue adds the two halves
         wait(bar_rb, ph_rb++ & 1);
-        for (int pass = 0; pass < 2; ++pass)
-          for (int kk = 0; kk < D / 16; ++kk)
-            tc::mma(t_kl, tc::desc(sKQ + kk * 4096, 2048, 128),
-                    tc::desc(sKl + pass * S::kF + kk * 256, 128, S_s), idesc_gp, pass > 0 || kk > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma(t_p, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKl + kk * 256, 128, S_s), idesc_gp2, kk > 0);
         tc::commit(bar_gp);
         // [6a] N_l^T += K_l^T Dt_l (3 passes; rows of N^T are k features, columns v features)
         {
@@ -569,12 +568,13 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
               tc::mma(t_n, tc::desc(sKl + ap[ps] * S::kF + kk * 2 * S_s, S_s, 128),
                       tc::desc(sDt + bp[ps] * S::kF128 + kk * 4096, 2048, 128), idesc_dd, l > 0 || ps > 0 || kk > 0);
         }
-        if (l + 1 < L) {                       // p^(l+1): pass B has read p^(l)
+        // [6b] [R ; O_l] += [G ; P] D_l (3 passes) once the [G;P] tiles are in X; before it
+        //      p^(l+1) into the p columns, which the [5] epilogue has read
+        wait(bar_r5, ph_r5++ & 1);
+        if (l + 1 < L) {
           wait(bar_wp, ph_wp++ & 1);
           proj(l + 1, 1, t_p, sY, bar_wp, ph_wp, bar_p);
         }
-        // [6b] [R ; O_l] += [G ; P] D_l (3 passes) once the [G;P] tiles are in X
-        wait(bar_r5, ph_r5++ & 1);
         {
           const int ap[3] = {0, 0, 1}, bp[3] = {0, 1, 0};
           for (int ps = 0; ps < 3; ++ps)
@@ -678,7 +678,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
 
   const bool gelu = !(p.flags & 1u);
   for (int l = 0; l < L; ++l) {
-    const uint32_t t_kl = t_k0 + (l & 1) * C;  // k_hat^(l), then the scores of step l
+    const uint32_t t_kl = t_k0 + (l & 1) * C;  // k_hat^(l)
     ok &= tc::bar_wait(bar_k + (l & 1), (l >> 1) & 1);
     tc::fence_after();
     // [3] epilogue.  Pass A: per token |k_hat|^2 and the gate logit w_beta . u,
@@ -759,8 +759,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
             zz += spart[(q - 1) * 2 * C + C + t];
           }
           const bool tv = t < nv;
-          sinv[t] = tv ? 1.0f / sqrtf(ss + 1e-6f) : 0.f;
-          sbl[t] = tv ? sigmoidf(zz) : 0.f;
+          sinv[t] = tv ? rsqrtf(ss + 1e-6f) : 0.f;
+          sbl[t] = tv ? __frcp_rn(1.0f + __expf(-zz)) : 0.f;
         }
       }
       asm volatile("bar.sync %0, 128;\n" ::"r"(2 + cg) : "memory");
@@ -818,16 +818,20 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     tc::fence_after();
     // [5] epilogue: decay and causal mask, then hi/lo split; rows < C are G, C..2C-1 are P
     if (quarter * 32 < 2 * C) {
-      uint32_t gr[NTH / 8][8];
+      uint32_t gr[NTH / 8][8], gl[NTH / 8][8];
 #pragma unroll
-      for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_kl + lane_base + tb0 + 8 * g, gr[g]);
+      for (int g = 0; g < NTH / 8; ++g) {
+        tc::ld8a(t_p + lane_base + tb0 + 8 * g, gr[g]);
+        tc::ld8a(t_p + C + lane_base + tb0 + 8 * g, gl[g]);
+      }
       tc::wait_ld();
 #pragma unroll
       for (int g = 0; g < NTH / 8; ++g) {
         tc::pin(gr[g]);
+        tc::pin(gl[g]);
         float val[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) val[jj] = gm[8 * g + jj] * u2f(gr[g][jj]);
+        for (int jj = 0; jj < 8; ++jj) val[jj] = gm[8 * g + jj] * (u2f(gr[g][jj]) + u2f(gl[g][jj]));
         uint4 hi, lo;
         tc::split8(val, hi, lo);
         const uint32_t off = ((tb0 + 8 * g) / 8) * 2048u + row * 16u;
