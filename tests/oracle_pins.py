@@ -295,3 +295,67 @@ ALL_PINS = [pin_l0_is_gated_deltanet, pin_zero_conv_is_gated_deltanet, pin_write
             pin_shortconv, pin_direction, pin_gain_and_gelu, pin_confidence_gate, pin_padding,
             pin_causality, pin_identity_activation, pin_resume_is_markov,
             pin_initial_state_gated_deltanet]
+
+
+# ---- gradients (oracle.grad): pinned to the C oracle above, an independent implementation ----
+
+def _grad_case(seed, L=2, ragged=True, T=13):
+    inp = random_small(2, T, 2, 4, 4, L, 3, seed=seed, ragged=ragged)
+    rng = np.random.default_rng(seed)
+    d_out = rng.standard_normal((2, T, 2, 4))
+    d_fs = rng.standard_normal((2, 2, 4, 4))
+    return inp, d_out, d_fs
+
+
+def pin_grad_forward_matches(fwd, grad_mod):
+    """The differentiable restatement gives the C oracle's outputs and final state."""
+    for seed, L, ragged, act in ((40, 2, True, False), (41, 0, False, False), (42, 3, True, True)):
+        inp, _, _ = _grad_case(seed, L, ragged)
+        p = {n: inp[n].double() for n in grad_mod.GRAD_KEYS}
+        with torch.no_grad():
+            o, s = grad_mod.forward_torch(p, L, seq_lens=inp.get("seq_lens"), identity_act=act)
+        ro, rs, _ = fwd(inp, identity_act=act)
+        _close(o.numpy(), ro, 1e-12, f"outputs (L={L})")
+        _close(s.numpy(), rs, 1e-12, f"final state (L={L})")
+
+
+def pin_grad_finite_difference(fwd, grad_mod):
+    """Every gradient along a random direction equals the central difference of the
+    C oracle's  sum(out * d_out) + sum(final_state * d_fs)  (step 1e-5, fp64)."""
+    for seed, L, act in ((43, 2, False), (44, 3, True)):
+        inp, d_out, d_fs = _grad_case(seed, L)
+        g = grad_mod.backward(inp, d_out, d_fs, identity_act=act)
+
+        def f(x):
+            o, s, _ = fwd(x, identity_act=act)
+            return float(np.sum(o * d_out) + np.sum(s * d_fs))
+        rng = np.random.default_rng(seed + 100)
+        eps = 1e-5
+        for n in grad_mod.GRAD_KEYS:
+            base = inp[n].double()
+            delta = torch.from_numpy(rng.standard_normal(tuple(base.shape)))
+            xp, xm = dict(inp), dict(inp)
+            xp[n] = base + eps * delta
+            xm[n] = base - eps * delta
+            fd = (f(xp) - f(xm)) / (2 * eps)
+            an = float(np.sum(g[n] * delta.numpy()))
+            assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), f"d/d{n} (L={L}): fd {fd:.9e} vs {an:.9e}"
+
+
+def pin_grad_dq_closed_form(fwd, grad_mod):
+    """o_t = S_t q_t, so dq_t = S_t^T do_t, with S_t the final state of the C oracle run
+    on tokens [0, t] (zero for padding tokens, whose output is fixed at 0)."""
+    inp, d_out, _ = _grad_case(45, 2, True, T=9)
+    g = grad_mod.backward(inp, d_out, None)
+    lens = inp["seq_lens"].numpy()
+    for t in range(9):
+        _, s, _ = fwd(_slice_tokens(inp, 0, t + 1))
+        for b in range(2):
+            for h in range(2):
+                if t < lens[b]:
+                    _close(g["q"][b, t, h], s[b, h].T @ d_out[b, t, h], 1e-12, f"dq (t={t})")
+                else:
+                    assert not np.any(g["q"][b, t, h]), f"dq of a padding token (t={t})"
+
+
+GRAD_PINS = [pin_grad_forward_matches, pin_grad_finite_difference, pin_grad_dq_closed_form]

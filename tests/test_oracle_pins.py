@@ -6,10 +6,12 @@ that at least one pin catches each of them.
 import functools
 import os
 import subprocess
+import types
 
 import pytest
 
 import oracle
+from oracle import grad
 from tests import oracle_pins
 
 ORACLE_SRC = os.path.join(os.path.dirname(oracle.__file__), "prism_oracle.c")
@@ -64,3 +66,40 @@ def test_planted_mistake_is_caught(name, old, new, tmp_path):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"planted mistake {name} passed every pin"
+
+
+# ---- the gradient oracle (oracle/grad.py) ----
+
+@pytest.mark.parametrize("pin", oracle_pins.GRAD_PINS, ids=lambda f: f.__name__)
+def test_grad_pin(pin):
+    pin(oracle.forward, grad)
+
+
+# mistakes planted in the differentiable restatement: each must fail a gradient pin
+GRAD_MUTANTS = [
+    ("no_base_write", "Bw = be[:, t].view(B, H, 1, 1) * vt.unsqueeze(-1) * kt.unsqueeze(-2)",
+     "Bw = 0.0 * vt.unsqueeze(-1) * kt.unsqueeze(-2)"),
+    ("no_normalize", "kl = kh / torch.sqrt((kh * kh).sum(-1, keepdim=True) + NORM_EPS)", "kl = kh"),
+    ("gelu_tanh", "0.5 * x * (1.0 + torch.erf(x / math.sqrt(2.0)))",
+     "0.5 * x * (1.0 + torch.tanh(0.7978845608028654 * (x + 0.044715 * x ** 3)))"),
+    ("write_transposed", "S_new = S @ A + Bw", "S_new = S @ A + Bw.transpose(-1, -2)"),
+    ("output_before_update", "o = torch.einsum(\"xhab,xhb->xha\", S, qt)",
+     "o = torch.einsum(\"xhab,xhb->xha\", torch.where(live, S @ A, S), qt)"),
+    ("padding_not_frozen", "S = torch.where(live, S_new, S)", "S = S_new"),
+    ("decay_not_exp", "A = torch.exp(la[:, t]).view(B, H, 1, 1) * (", "A = (1.0 + la[:, t]).view(B, H, 1, 1) * ("),
+]
+
+
+@pytest.mark.parametrize("name,old,new", GRAD_MUTANTS, ids=[m[0] for m in GRAD_MUTANTS])
+def test_grad_planted_mistake_is_caught(name, old, new):
+    src = open(grad.__file__).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    mod = types.ModuleType(f"grad_mut_{name}")
+    exec(compile(src.replace(old, new), f"<grad {name}>", "exec"), mod.__dict__)
+    caught = []
+    for pin in oracle_pins.GRAD_PINS:
+        try:
+            pin(oracle.forward, mod)
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"planted mistake {name} passed every gradient pin"
