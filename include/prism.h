@@ -213,6 +213,39 @@ PRISM_API int prism_forward_static(const prism_dims* dims,
                                    float* out, float* final_state, const int32_t* seq_lens,
                                    void* stream);
 
+/* ---- Backward pass ----
+ * Gradients of a scalar loss through prism_forward ("Technical Summary: PRISM",
+ * §2.1-2.2: the anchor, the refinement, the rank-L write and the gated delta-rule
+ * recurrence from a zero state), given
+ *   d_out          [B,T,H,d_v] fp32: dLoss/d out (ignored at padding tokens)
+ *   d_final_state  [B,H,d_v,d_k] fp32: dLoss/d final_state, or NULL (zero)
+ * Outputs (fp32, every element overwritten; zero at padding tokens):
+ *   dq, dk, dv     [B,T,H,d]
+ *   dlog_alpha, dbeta [B,T,H]
+ *   dconv_w        [H,w,d_v]
+ *   dWk, dWp       [H,L,d,d]      (not written when L = 0)
+ *   dwbeta         [H,L,d_v]      (not written when L = 0)
+ * Inputs are those of prism_forward; d_k must equal d_v.  dims->chunk is ignored.
+ * Arithmetic is fp32 on the CUDA cores: the refinement per token (recomputed), the
+ * state forward with a checkpoint every 16 tokens and then backwards block by block
+ * (the block's states recomputed from its checkpoint), the refinement chain backwards,
+ * and token sums for the weight gradients.  Deterministic (no atomics).  The workspace
+ * (prism_backward_workspace_bytes) holds per-token factors and the checkpoints; it is
+ * caller-owned, 256-byte aligned, and needs no initialisation.  Errors as for
+ * prism_forward; asynchronous on `stream`. */
+PRISM_API size_t prism_backward_workspace_bytes(const prism_dims* dims);
+PRISM_API int prism_backward(const prism_dims* dims,
+                             const void* q, const void* k, const void* v,
+                             const float* log_alpha, const float* beta,
+                             const float* conv_w, const float* Wk, const float* Wp,
+                             const float* wbeta,
+                             const float* d_out, const float* d_final_state,
+                             float* dq, float* dk, float* dv,
+                             float* dlog_alpha, float* dbeta,
+                             float* dconv_w, float* dWk, float* dWp, float* dwbeta,
+                             const int32_t* seq_lens, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
 /* Static description of an error code. */
 PRISM_API const char* prism_strerror(int code);
 

@@ -1,0 +1,754 @@
+// Backward pass of the PRISM mixer ("Technical Summary: PRISM", §2.1 and §2.2, read as the
+// forward kernels read them): the gradients of a scalar loss with respect to q, k, v,
+// log_alpha, beta and the per-head parameters (conv taps, W_k, W_p, w_beta), given the
+// loss's gradient with respect to the outputs (and, optionally, the final state).
+//
+// All arithmetic is fp32 on the CUDA cores; five kernels, in launch order:
+//   A  bwd_refine_fwd   per tile of tokens: anchor u, the L refinement steps; keeps u,
+//                       k^(l), D^(l) = beta^(l) delta^(l), p^(l), 1/|k_hat^(l)|, z^(l)
+//   B  bwd_state        per (b, h): the state S_t forward (checkpoints every kBwdCK tokens),
+//                       then backward block by block, recomputing the block's states from
+//                       its checkpoint: dS_(t-1) = alpha (dS_t - beta (dS_t k) k^T) with
+//                       dS_t += do_t q_t^T, and the per-token gradients of q, k, v (base
+//                       write), beta, log_alpha, D^(l) and k^(l)
+//   C  bwd_refine       per tile of tokens: the refinement chain backwards (GELU, the
+//                       residual, the normalisation, the gate), du_t, dv_t (residual part)
+//   D  bwd_weights      dW_k, dW_p (token-sum outer products), dw_beta, dconv_w
+//   E  bwd_conv_dv      dv_t += sum_j c_j (.) du_(t+j)  (the anchor's taps, transposed)
+#pragma once
+
+#include "prism_common.cuh"
+
+namespace prism {
+
+constexpr int kBwdTT = 32;        // tokens per tile, kernel A
+constexpr int kBwdTC = 16;        // tokens per tile, kernel C
+constexpr int kBwdCK = 16;        // tokens between state checkpoints, kernel B
+constexpr int kBwdLmax = 8;
+constexpr int kBwdThreads = 256;
+
+struct BwdArgs {
+  int B, T, H, L, w;
+  unsigned flags;                 // bit 0: identity in place of GELU
+  const void* q;                  // [B][T][H][D] (I/O dtype)
+  const void* k;
+  const void* v;
+  const float* log_alpha;         // [B][T][H]
+  const float* beta;
+  const float* conv_w;            // [H][w][D]
+  const float* Wk;                // [H][L][D][D]
+  const float* Wp;
+  const float* wbeta;             // [H][L][D]
+  const float* d_out;             // [B][T][H][D]
+  const float* d_fs;              // [B][H][D][D] or null
+  const int* seq_lens;
+  float* dq;                      // [B][T][H][D]
+  float* dk;
+  float* dv;
+  float* dla;                     // [B][T][H]
+  float* dbeta;
+  float* dconv;                   // [H][w][D]
+  float* dWk;                     // [H][L][D][D]
+  float* dWp;
+  float* dwb;                     // [H][L][D]
+  // workspace (token-head n = (b T + t) H + h)
+  float* U;                       // [n][D]
+  float* KL;                      // [n][L][D]  k^(l)
+  float* DL;                      // [n][L][D]  D^(l); then dp^(l) (kernel C)
+  float* P;                       // [n][L][D]  p^(l)
+  float* NRM;                     // [n][L]     1 / sqrt(|k_hat|^2 + eps)
+  float* Z;                       // [n][L]     w_beta^(l) . u
+  float* dDL;                     // [n][L][D]
+  float* dKL;                     // [n][L][D]
+  float* dKH;                     // [n][L][D]  gradient of k_hat^(l)
+  float* dZ;                      // [n][L]
+  float* dU;                      // [n][D]
+  float* CK;                      // [B][H][ceil(T/kBwdCK)][D][D] states before each block
+  float* SCR;                     // [B][H][kBwdCK][D][D] states of the block being reversed
+};
+
+__device__ __forceinline__ int bwd_len(const BwdArgs& p, int b) {
+  return p.seq_lens ? min(max(p.seq_lens[b], 0), p.T) : p.T;
+}
+
+__device__ __forceinline__ float gelu_grad(float x) {     // d/dx of x Phi(x)
+  return 0.5f * (1.0f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * expf(-0.5f * x * x);
+}
+
+// ------------------------------------------------------------------------------------
+// A: refinement forward for kBwdTT tokens of one (b, h)
+
+template <int D>
+struct BwdASmem {
+  static constexpr int LDW = D + 1;
+  static constexpr size_t oW = 0;                                   // W [D][D+1]
+  static constexpr size_t oV = oW + 4u * D * LDW;                   // v rows t0-8 .. t0+TT-1
+  static constexpr size_t oU = oV + 4u * (kBwdTT + 8) * D;          // u  [TT][D]
+  static constexpr size_t oR = oU + 4u * kBwdTT * D;                // r  [TT][D]
+  static constexpr size_t oK = oR + 4u * kBwdTT * D;                // k_hat [TT][D]
+  static constexpr size_t oP = oK + 4u * kBwdTT * D;                // p [TT][D]
+  static constexpr size_t oS = oP + 4u * kBwdTT * D;                // 1/|k_hat| [TT], beta^(l) [TT]
+  static constexpr size_t bytes = oS + 4u * 2 * kBwdTT;
+};
+
+// W [D][D] (row-major, global) into shared memory rows of D + 1.
+template <int D>
+__device__ __forceinline__ void bwd_load_w(float* sW, const float* W) {
+  for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) sW[(idx / D) * (D + 1) + idx % D] = W[idx];
+}
+
+// Y[i][a] = sum_c W[a][c] X[i][a'=c] for the NTOK token rows of X (shared memory).
+template <int D, int NTOK>
+__device__ __forceinline__ void bwd_matvec(const float* sW, const float* X, float* Y) {
+  constexpr int NG = kBwdThreads / D, TPG = NTOK / NG;
+  const int a = threadIdx.x % D, g = threadIdx.x / D;
+  float acc[TPG];
+#pragma unroll
+  for (int i = 0; i < TPG; ++i) acc[i] = 0.f;
+  for (int c = 0; c < D; ++c) {
+    const float wv = sW[a * (D + 1) + c];
+#pragma unroll
+    for (int i = 0; i < TPG; ++i) acc[i] = fmaf(wv, X[(g * TPG + i) * D + c], acc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < TPG; ++i) Y[(g * TPG + i) * D + a] = acc[i];
+}
+
+// Y[i][c] += sum_a W[a][c] X[i][a] (the transposed product), NTOK token rows.
+template <int D, int NTOK>
+__device__ __forceinline__ void bwd_matvec_t_add(const float* sW, const float* X, float* Y) {
+  constexpr int NG = kBwdThreads / D, TPG = NTOK / NG;
+  const int c = threadIdx.x % D, g = threadIdx.x / D;
+  float acc[TPG];
+#pragma unroll
+  for (int i = 0; i < TPG; ++i) acc[i] = 0.f;
+  for (int a = 0; a < D; ++a) {
+    const float wv = sW[a * (D + 1) + c];
+#pragma unroll
+    for (int i = 0; i < TPG; ++i) acc[i] = fmaf(wv, X[(g * TPG + i) * D + a], acc[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < TPG; ++i) Y[(g * TPG + i) * D + c] += acc[i];
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+template <class T, int D>
+__global__ void __launch_bounds__(kBwdThreads) bwd_refine_fwd_kernel(BwdArgs p) {
+  using S = BwdASmem<D>;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  float* sW = reinterpret_cast<float*>(sm + S::oW);
+  float* sV = reinterpret_cast<float*>(sm + S::oV);
+  float* sU = reinterpret_cast<float*>(sm + S::oU);
+  float* sR = reinterpret_cast<float*>(sm + S::oR);
+  float* sK = reinterpret_cast<float*>(sm + S::oK);
+  float* sP = reinterpret_cast<float*>(sm + S::oP);
+  float* sInv = reinterpret_cast<float*>(sm + S::oS);
+  float* sBl = sInv + kBwdTT;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * kBwdTT, h = blockIdx.y, b = blockIdx.z;
+  const int H = p.H, T_ = p.T, L = p.L, w = p.w;
+  const int len = bwd_len(p, b);
+  const T* v = static_cast<const T*>(p.v);
+  const bool gelu = !(p.flags & 1u);
+
+  for (int idx = tid; idx < (kBwdTT + 8) * D; idx += kBwdThreads) {
+    const int t = t0 - 8 + idx / D;
+    sV[idx] = (t >= 0 && t < len) ? Elem<T>::to_f(v[(((size_t)b * T_ + t) * H + h) * D + idx % D]) : 0.f;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < kBwdTT * D; idx += kBwdThreads) {
+    const int i = idx / D, c = idx % D, t = t0 + i;
+    float u = 0.f;
+    for (int j = 1; j <= w; ++j) u = fmaf(p.conv_w[((size_t)h * w + (j - 1)) * D + c], sV[(i + 8 - j) * D + c], u);
+    const bool valid = t < len;
+    sU[idx] = valid ? u : 0.f;
+    sR[idx] = valid ? sV[(i + 8) * D + c] - u : 0.f;
+    if (t < T_) p.U[(((size_t)b * T_ + t) * H + h) * D + c] = valid ? u : 0.f;
+  }
+  __syncthreads();
+  for (int l = 0; l < L; ++l) {
+    bwd_load_w<D>(sW, p.Wk + ((size_t)h * L + l) * D * D);
+    __syncthreads();
+    bwd_matvec<D, kBwdTT>(sW, sU, sK);
+    __syncthreads();
+    bwd_load_w<D>(sW, p.Wp + ((size_t)h * L + l) * D * D);
+    __syncthreads();
+    bwd_matvec<D, kBwdTT>(sW, sU, sP);
+    for (int i = warp; i < kBwdTT; i += kBwdThreads / 32) {   // reads sK, sU (ready)
+      float n2 = 0.f, z = 0.f;
+      for (int a = lane; a < D; a += 32) {
+        const float kk = sK[i * D + a];
+        n2 = fmaf(kk, kk, n2);
+        z = fmaf(p.wbeta[((size_t)h * L + l) * D + a], sU[i * D + a], z);
+      }
+      n2 = warp_sum(n2);
+      z = warp_sum(z);
+      const int t = t0 + i;
+      const bool valid = t < len;
+      const float inv = 1.0f / sqrtf(n2 + 1e-6f);
+      if (lane == 0) {
+        sInv[i] = inv;
+        sBl[i] = sigmoidf(z);
+        if (t < T_) {
+          const size_t n = ((size_t)b * T_ + t) * H + h;
+          p.NRM[n * L + l] = valid ? inv : 0.f;
+          p.Z[n * L + l] = valid ? z : 0.f;
+        }
+      }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < kBwdTT * D; idx += kBwdThreads) {
+      const int i = idx / D, a = idx % D, t = t0 + i;
+      if (t >= T_) continue;
+      const size_t o = ((((size_t)b * T_ + t) * H + h) * L + l) * D + a;
+      if (t < len) {
+        const float x = sP[idx] * sR[idx];
+        const float dl = gelu ? gelu_erf(x) : x;
+        sR[idx] -= dl;
+        p.KL[o] = sK[idx] * sInv[i];
+        p.DL[o] = sBl[i] * dl;
+        p.P[o] = sP[idx];
+      } else {
+        p.KL[o] = 0.f;
+        p.DL[o] = 0.f;
+        p.P[o] = 0.f;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// B: the state, forward with checkpoints and backward block by block (one CTA per (b, h),
+// 4 D threads).  Row mapping: thread (r = tid / 4, cq = tid % 4) owns columns cq + 4 i of
+// row r; column mapping: thread (c = tid % D, rq = tid / D) owns rows rq D/4 + i of column c.
+
+template <int D>
+struct BwdBSmem {
+  static constexpr int LDS = D + 4;                                 // 16-byte rows, no bank conflicts
+  static constexpr int NT = 4 * D, NW = NT / 32;
+  static constexpr size_t oDS = 0;                                  // dS [D][D+4]
+  static constexpr size_t oS = oDS + 4u * D * LDS;                  // S  [D][D+4]
+  static constexpr size_t oVec = oS + 4u * D * LDS;                 // k, q, do, v, y: 5 x D
+  static constexpr size_t oKL = oVec + 4u * 5 * D;                  // k^(l) [Lmax][D]
+  static constexpr size_t oDL = oKL + 4u * kBwdLmax * D;            // D^(l) [Lmax][D]
+  static constexpr size_t oZS = oDL + 4u * kBwdLmax * D;            // S_(t-1) k_t of the block [CK][D]
+  static constexpr size_t oAS = oZS + 4u * kBwdCK * D;              // S_(t-1)^T do_t of the block [CK][D]
+  static constexpr size_t oPart = oAS + 4u * kBwdCK * D;            // column partial sums [4][2 + Lmax][D]
+  static constexpr size_t oRed = oPart + 4u * 4 * (2 + kBwdLmax) * D;   // scalar partials [NW][16]
+  static constexpr size_t oSc = oRed + 4u * NW * 16;                // alpha, beta of the token
+  static constexpr size_t bytes = oSc + 16;
+};
+
+__device__ __forceinline__ void bwd_cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void bwd_cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bwd_cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+template <int D>
+__device__ __forceinline__ void bwd_state_load_async(float* sS, const float* g) {
+  using S = BwdBSmem<D>;
+  for (int idx = threadIdx.x; idx < D * D / 4; idx += S::NT) {
+    const int r = (idx * 4) / D, c = (idx * 4) % D;
+    bwd_cp_async16(sS + r * S::LDS + c, g + (size_t)idx * 4);
+  }
+  bwd_cp_async_commit();
+}
+template <int D>
+__device__ __forceinline__ void bwd_state_store(const float* sS, float* g) {
+  using S = BwdBSmem<D>;
+  for (int idx = threadIdx.x; idx < D * D / 4; idx += S::NT) {
+    const int r = (idx * 4) / D, c = (idx * 4) % D;
+    *reinterpret_cast<float4*>(g + (size_t)idx * 4) = *reinterpret_cast<const float4*>(sS + r * S::LDS + c);
+  }
+}
+
+template <class T, int D>
+__global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
+  using S = BwdBSmem<D>;
+  constexpr int LDS = S::LDS, NT = S::NT, NW = S::NW, CPT = D / 4;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  float* sDS = reinterpret_cast<float*>(sm + S::oDS);
+  float* sS = reinterpret_cast<float*>(sm + S::oS);
+  float* sk = reinterpret_cast<float*>(sm + S::oVec);
+  float* sq = sk + D;
+  float* sdo = sq + D;
+  float* sv = sdo + D;
+  float* sy = sv + D;
+  float* skl = reinterpret_cast<float*>(sm + S::oKL);
+  float* sdl = reinterpret_cast<float*>(sm + S::oDL);
+  float* sZS = reinterpret_cast<float*>(sm + S::oZS);
+  float* sAS = reinterpret_cast<float*>(sm + S::oAS);
+  float* sPart = reinterpret_cast<float*>(sm + S::oPart);
+  float* sRed = reinterpret_cast<float*>(sm + S::oRed);
+  float* sSc = reinterpret_cast<float*>(sm + S::oSc);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int r = tid >> 2, cq = tid & 3;              // row mapping
+  const int cc = tid % D, rq = tid / D;              // column mapping
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int H = p.H, T_ = p.T, L = p.L;
+  const int len = bwd_len(p, b);
+  const int NCK = (T_ + kBwdCK - 1) / kBwdCK;
+  const T* qg = static_cast<const T*>(p.q);
+  const T* kg = static_cast<const T*>(p.k);
+  const T* vg = static_cast<const T*>(p.v);
+  float* ck = p.CK + ((size_t)b * H + h) * NCK * D * D;
+  float* scr = p.SCR + ((size_t)b * H + h) * kBwdCK * D * D;
+  auto tok = [&](int t) { return ((size_t)b * T_ + t) * H + h; };
+
+  // padding tokens: every per-token gradient is zero
+  for (int t = len; t < T_; ++t) {
+    const size_t n = tok(t);
+    for (int idx = tid; idx < D; idx += NT) {
+      p.dq[n * D + idx] = 0.f;
+      p.dk[n * D + idx] = 0.f;
+      p.dv[n * D + idx] = 0.f;
+    }
+    for (int idx = tid; idx < L * D; idx += NT) {
+      p.dDL[n * L * D + idx] = 0.f;
+      p.dKL[n * L * D + idx] = 0.f;
+    }
+    if (tid == 0) {
+      p.dla[n] = 0.f;
+      p.dbeta[n] = 0.f;
+    }
+  }
+  if (len <= 0) return;
+
+  // token t's vectors into shared memory (k, v and the refinement factors; q and do too)
+  auto load_token = [&](int t, bool with_q) {
+    const size_t n = tok(t);
+    for (int idx = tid; idx < D; idx += NT) {
+      sk[idx] = Elem<T>::to_f(kg[n * D + idx]);
+      sv[idx] = Elem<T>::to_f(vg[n * D + idx]);
+      sdo[idx] = p.d_out[n * D + idx];
+      if (with_q) sq[idx] = Elem<T>::to_f(qg[n * D + idx]);
+    }
+    for (int idx = tid; idx < L * D; idx += NT) {
+      skl[idx] = p.KL[n * L * D + idx];
+      sdl[idx] = p.DL[n * L * D + idx];
+    }
+    if (tid == 0) {
+      sSc[0] = expf(p.log_alpha[n]);
+      sSc[1] = p.beta[n];
+    }
+  };
+  // z_r = S[r] . k (row mapping; every thread of the row gets it)
+  auto row_dot_k = [&]() {
+    float z = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < CPT; ++i) z = fmaf(sS[r * LDS + cq + 4 * i], sk[cq + 4 * i], z);
+    z += __shfl_xor_sync(0xffffffffu, z, 1);
+    z += __shfl_xor_sync(0xffffffffu, z, 2);
+    return z;
+  };
+  // S <- alpha (S - beta z k^T) + beta v k^T + sum_l D^(l) k^(l)^T on this thread's elements
+  auto row_update = [&](float z) {
+    const float al = sSc[0], be = sSc[1];
+#pragma unroll 4
+    for (int i = 0; i < CPT; ++i) {
+      const int c = cq + 4 * i;
+      float x = al * (sS[r * LDS + c] - be * z * sk[c]) + be * sv[r] * sk[c];
+      for (int l = 0; l < L; ++l) x = fmaf(sdl[l * D + r], skl[l * D + c], x);
+      sS[r * LDS + c] = x;
+    }
+  };
+
+  // ---- forward: checkpoints (the state before tokens 0, CK, 2 CK, ...) ----
+  for (int idx = tid; idx < D * LDS; idx += NT) sS[idx] = 0.f;
+  __syncthreads();
+  bwd_state_store<D>(sS, ck);
+  for (int t = 0; t < len; ++t) {
+    load_token(t, false);
+    __syncthreads();
+    const float z = row_dot_k();
+    row_update(z);
+    __syncthreads();
+    if ((t + 1) % kBwdCK == 0 && t + 1 < len) bwd_state_store<D>(sS, ck + (size_t)((t + 1) / kBwdCK) * D * D);
+  }
+
+  // ---- backward ----
+  for (int idx = tid; idx < D * LDS; idx += NT) {
+    const int rr = idx / LDS, c = idx % LDS;
+    sDS[idx] = (p.d_fs && c < D) ? p.d_fs[(((size_t)b * H + h) * D + rr) * D + c] : 0.f;
+  }
+  const int nblk = (len + kBwdCK - 1) / kBwdCK;
+  for (int blk = nblk - 1; blk >= 0; --blk) {
+    const int c0 = blk * kBwdCK, c1 = min(c0 + kBwdCK, len);
+    __syncthreads();
+    bwd_state_load_async<D>(sS, ck + (size_t)blk * D * D);
+    bwd_cp_async_wait_all();
+    __syncthreads();
+    // recompute the block: z_t = S_(t-1) k_t, a_t = S_(t-1)^T do_t, and the states after
+    // tokens c0 .. c1-2 into the scratch
+    for (int t = c0; t < c1; ++t) {
+      load_token(t, false);
+      __syncthreads();
+      const float z = row_dot_k();
+      if (cq == 0) sZS[(t - c0) * D + r] = z;
+      {
+        float a = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < CPT; ++i) {
+          const int rr = rq * CPT + i;
+          a = fmaf(sS[rr * LDS + cc], sdo[rr], a);
+        }
+        sPart[rq * D + cc] = a;
+      }
+      __syncthreads();
+      if (tid < D) sAS[(t - c0) * D + tid] = sPart[tid] + sPart[D + tid] + sPart[2 * D + tid] + sPart[3 * D + tid];
+      row_update(z);
+      __syncthreads();
+      if (t < c1 - 1) bwd_state_store<D>(sS, scr + (size_t)(t - c0) * D * D);
+    }
+    // reverse through the block
+    for (int t = c1 - 1; t >= c0; --t) {
+      __syncthreads();                                 // previous token done with the buffers
+      bwd_state_load_async<D>(sS, t > c0 ? scr + (size_t)(t - 1 - c0) * D * D : ck + (size_t)blk * D * D);
+      load_token(t, true);
+      __syncthreads();
+      const size_t n = tok(t);
+      const float al = sSc[0], be = sSc[1];
+      const float* zs = sZS + (t - c0) * D;
+      // phase 1 (rows): dS += do q^T; y = dS k; y_l = dS k^(l)
+      float y = 0.f, yl[kBwdLmax];
+#pragma unroll
+      for (int l = 0; l < kBwdLmax; ++l) yl[l] = 0.f;
+      {
+        const float dor = sdo[r];
+#pragma unroll 4
+        for (int i = 0; i < CPT; ++i) {
+          const int c = cq + 4 * i;
+          const float ds = fmaf(dor, sq[c], sDS[r * LDS + c]);
+          sDS[r * LDS + c] = ds;
+          y = fmaf(ds, sk[c], y);
+          for (int l = 0; l < L; ++l) yl[l] = fmaf(ds, skl[l * D + c], yl[l]);
+        }
+      }
+      y += __shfl_xor_sync(0xffffffffu, y, 1);
+      y += __shfl_xor_sync(0xffffffffu, y, 2);
+#pragma unroll
+      for (int l = 0; l < kBwdLmax; ++l) {
+        if (l < L) {
+          yl[l] += __shfl_xor_sync(0xffffffffu, yl[l], 1);
+          yl[l] += __shfl_xor_sync(0xffffffffu, yl[l], 2);
+        }
+      }
+      // per-row scalars (summed over rows below): v.y, z.y, z.do, v.do, D^(l).do
+      float sc[4 + kBwdLmax];
+      {
+        const bool own = cq == 0;
+        const float zr = zs[r], vr = sv[r], dor = sdo[r];
+        sc[0] = own ? vr * y : 0.f;
+        sc[1] = own ? zr * y : 0.f;
+        sc[2] = own ? zr * dor : 0.f;
+        sc[3] = own ? vr * dor : 0.f;
+#pragma unroll
+        for (int l = 0; l < kBwdLmax; ++l) sc[4 + l] = (own && l < L) ? sdl[l * D + r] * dor : 0.f;
+        if (own) {
+          sy[r] = y;
+          p.dv[n * D + r] = be * y;
+          for (int l = 0; l < L; ++l) p.dDL[(n * L + l) * D + r] = yl[l];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4 + kBwdLmax; ++j) {
+        if (j < 4 + L) {
+          const float s = warp_sum(sc[j]);
+          if (lane == 0) sRed[warp * 16 + j] = s;
+        }
+      }
+      bwd_cp_async_wait_all();
+      __syncthreads();
+      // phase 2 (columns): S_(t-1)^T y, dS^T (beta v - alpha beta z), dS^T D^(l), <S_(t-1), dS>;
+      // then dS <- alpha (dS - beta y k^T)
+      {
+        float bS = 0.f, e = 0.f, fro = 0.f, f[kBwdLmax];
+#pragma unroll
+        for (int l = 0; l < kBwdLmax; ++l) f[l] = 0.f;
+        const float kc = sk[cc];
+#pragma unroll 4
+        for (int i = 0; i < CPT; ++i) {
+          const int rr = rq * CPT + i;
+          const float s = sS[rr * LDS + cc], ds = sDS[rr * LDS + cc], yr = sy[rr];
+          bS = fmaf(s, yr, bS);
+          e = fmaf(ds, be * (sv[rr] - al * zs[rr]), e);
+          fro = fmaf(s, ds, fro);
+          for (int l = 0; l < L; ++l) f[l] = fmaf(ds, sdl[l * D + rr], f[l]);
+          sDS[rr * LDS + cc] = al * (ds - be * yr * kc);
+        }
+        sPart[(rq * (2 + kBwdLmax) + 0) * D + cc] = bS;
+        sPart[(rq * (2 + kBwdLmax) + 1) * D + cc] = e;
+        for (int l = 0; l < L; ++l) sPart[(rq * (2 + kBwdLmax) + 2 + l) * D + cc] = f[l];
+        fro = warp_sum(fro);
+        if (lane == 0) sRed[warp * 16 + 15] = fro;
+      }
+      __syncthreads();
+      // phase 3: per-token gradients
+      if (tid < D) {
+        const int c = tid;
+        float tot[2 + kBwdLmax];
+#pragma unroll
+        for (int j = 0; j < 2 + kBwdLmax; ++j) tot[j] = 0.f;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          tot[0] += sPart[(q4 * (2 + kBwdLmax) + 0) * D + c];
+          tot[1] += sPart[(q4 * (2 + kBwdLmax) + 1) * D + c];
+          for (int l = 0; l < L; ++l) tot[2 + l] += sPart[(q4 * (2 + kBwdLmax) + 2 + l) * D + c];
+        }
+        float zd = 0.f, vd = 0.f;
+        for (int wv = 0; wv < NW; ++wv) {
+          zd += sRed[wv * 16 + 2];
+          vd += sRed[wv * 16 + 3];
+        }
+        p.dk[n * D + c] = tot[1] - al * be * tot[0];
+        float dqc = al * (sAS[(t - c0) * D + c] - be * zd * sk[c]) + be * vd * sk[c];
+        for (int l = 0; l < L; ++l) {
+          float ddl = 0.f;
+          for (int wv = 0; wv < NW; ++wv) ddl += sRed[wv * 16 + 4 + l];
+          dqc = fmaf(ddl, skl[l * D + c], dqc);
+          p.dKL[(n * L + l) * D + c] = tot[2 + l];
+        }
+        p.dq[n * D + c] = dqc;
+        if (c == 0) {
+          float vy = 0.f, zy = 0.f, fr = 0.f;
+          for (int wv = 0; wv < NW; ++wv) {
+            vy += sRed[wv * 16 + 0];
+            zy += sRed[wv * 16 + 1];
+            fr += sRed[wv * 16 + 15];
+          }
+          p.dbeta[n] = vy - al * zy;
+          p.dla[n] = al * (fr - be * zy);
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// C: the refinement chain backwards for kBwdTC tokens of one (b, h)
+
+template <int D>
+struct BwdCSmem {
+  static constexpr size_t oW = 0;                                       // W [D][D+1]
+  static constexpr size_t oR = oW + 4u * D * (D + 1);                   // r^(l) [Lmax][TC][D]
+  static constexpr size_t oDR = oR + 4u * kBwdLmax * kBwdTC * D;        // dr [TC][D]
+  static constexpr size_t oDU = oDR + 4u * kBwdTC * D;                  // du [TC][D]
+  static constexpr size_t oG = oDU + 4u * kBwdTC * D;                   // d k_hat [TC][D]
+  static constexpr size_t oH = oG + 4u * kBwdTC * D;                    // dp [TC][D]
+  static constexpr size_t oZ = oH + 4u * kBwdTC * D;                    // dz [TC]
+  static constexpr size_t bytes = oZ + 4u * kBwdTC;
+};
+
+template <class T, int D>
+__global__ void __launch_bounds__(kBwdThreads) bwd_refine_kernel(BwdArgs p) {
+  using S = BwdCSmem<D>;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  float* sW = reinterpret_cast<float*>(sm + S::oW);
+  float* sR = reinterpret_cast<float*>(sm + S::oR);
+  float* sDR = reinterpret_cast<float*>(sm + S::oDR);
+  float* sDU = reinterpret_cast<float*>(sm + S::oDU);
+  float* sG = reinterpret_cast<float*>(sm + S::oG);
+  float* sH = reinterpret_cast<float*>(sm + S::oH);
+  float* sZ = reinterpret_cast<float*>(sm + S::oZ);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t0 = blockIdx.x * kBwdTC, h = blockIdx.y, b = blockIdx.z;
+  const int H = p.H, T_ = p.T, L = p.L;
+  const int len = bwd_len(p, b);
+  const T* vg = static_cast<const T*>(p.v);
+  const bool gelu = !(p.flags & 1u);
+  auto tok = [&](int t) { return ((size_t)b * T_ + t) * H + h; };
+
+  // forward recompute of the residual chain: r^(1) = v - u, r^(l+1) = r^(l) - delta^(l)
+  for (int idx = tid; idx < kBwdTC * D; idx += kBwdThreads) {
+    const int i = idx / D, c = idx % D, t = t0 + i;
+    float rr = 0.f;
+    if (t < len) {
+      const size_t n = tok(t);
+      rr = Elem<T>::to_f(vg[n * D + c]) - p.U[n * D + c];
+      for (int l = 0; l < L; ++l) {
+        sR[(l * kBwdTC + i) * D + c] = rr;
+        const float x = p.P[(n * L + l) * D + c] * rr;
+        rr -= gelu ? gelu_erf(x) : x;
+      }
+    } else {
+      for (int l = 0; l < L; ++l) sR[(l * kBwdTC + i) * D + c] = 0.f;
+    }
+    sDR[idx] = 0.f;
+    sDU[idx] = 0.f;
+  }
+  __syncthreads();
+  for (int l = L - 1; l >= 0; --l) {
+    // elementwise: dp, dr, and per token d beta^(l) (-> dz) and k^(l) . dk^(l) (-> d k_hat)
+    for (int i = warp; i < kBwdTC; i += kBwdThreads / 32) {
+      const int t = t0 + i;
+      const bool valid = t < len;
+      const size_t n = valid ? tok(t) : 0;
+      const float bl = valid ? sigmoidf(p.Z[n * L + l]) : 0.f;
+      const float inv = valid ? p.NRM[n * L + l] : 0.f;
+      float sdb = 0.f, skd = 0.f;
+      for (int a = lane; a < D; a += 32) {
+        if (!valid) {
+          sH[i * D + a] = 0.f;
+          continue;
+        }
+        const float rr = sR[(l * kBwdTC + i) * D + a];
+        const float pp = p.P[(n * L + l) * D + a];
+        const float x = pp * rr;
+        const float dl = gelu ? gelu_erf(x) : x;
+        const float dD = p.dDL[(n * L + l) * D + a];
+        const float ddel = bl * dD - sDR[i * D + a];
+        const float dx = ddel * (gelu ? gelu_grad(x) : 1.0f);
+        sH[i * D + a] = dx * rr;
+        sDR[i * D + a] += dx * pp;
+        sdb = fmaf(dl, dD, sdb);
+        skd = fmaf(p.KL[(n * L + l) * D + a], p.dKL[(n * L + l) * D + a], skd);
+      }
+      sdb = warp_sum(sdb);
+      skd = warp_sum(skd);
+      const float dz = sdb * bl * (1.0f - bl);
+      if (lane == 0) sZ[i] = valid ? dz : 0.f;
+      for (int a = lane; a < D; a += 32) {
+        const float g = valid ? (p.dKL[(n * L + l) * D + a] - p.KL[(n * L + l) * D + a] * skd) * inv : 0.f;
+        sG[i * D + a] = g;
+        if (t < T_) {
+          const size_t o = (tok(t) * L + l) * D + a;
+          p.dKH[o] = g;
+          p.DL[o] = sH[i * D + a];          // dp^(l) (the forward's D^(l) is no longer needed)
+        }
+      }
+      if (lane == 0 && t < T_) p.dZ[tok(t) * L + l] = valid ? dz : 0.f;
+    }
+    __syncthreads();
+    // du += W_k^T d k_hat + W_p^T dp + dz w_beta
+    bwd_load_w<D>(sW, p.Wk + ((size_t)h * L + l) * D * D);
+    __syncthreads();
+    bwd_matvec_t_add<D, kBwdTC>(sW, sG, sDU);
+    __syncthreads();
+    bwd_load_w<D>(sW, p.Wp + ((size_t)h * L + l) * D * D);
+    __syncthreads();
+    bwd_matvec_t_add<D, kBwdTC>(sW, sH, sDU);
+    __syncthreads();
+    for (int idx = tid; idx < kBwdTC * D; idx += kBwdThreads)
+      sDU[idx] = fmaf(sZ[idx / D], p.wbeta[((size_t)h * L + l) * D + idx % D], sDU[idx]);
+    __syncthreads();
+  }
+  // r^(1) = v - u: dv += dr^(1), du -= dr^(1)
+  for (int idx = tid; idx < kBwdTC * D; idx += kBwdThreads) {
+    const int i = idx / D, c = idx % D, t = t0 + i;
+    if (t >= T_) continue;
+    const size_t n = tok(t);
+    if (t < len) {
+      p.dv[n * D + c] += sDR[idx];
+      p.dU[n * D + c] = sDU[idx] - sDR[idx];
+    } else {
+      p.dU[n * D + c] = 0.f;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// D: dW_k^(l), dW_p^(l) (one CTA per TW x TW output tile: sum over the head's tokens of
+// d k_hat u^T and dp u^T), then dw_beta and the conv taps.
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads) bwd_weight_kernel(BwdArgs p) {
+  constexpr int TW = D < 32 ? D : 32;                // tile width
+  constexpr int OPT = TW * TW / kBwdThreads;         // outputs per thread (1 or 4)
+  __shared__ float sA[32][TW + 1], sUt[32][TW + 1];
+  const int tid = threadIdx.x;
+  const int tile = blockIdx.x, which = blockIdx.y % 2, l = blockIdx.y / 2, h = blockIdx.z;
+  const int a0 = (tile / (D / TW)) * TW, c0 = (tile % (D / TW)) * TW;
+  const int H = p.H, L = p.L, NTOK = p.B * p.T;
+  const float* src = which == 0 ? p.dKH : p.DL;      // DL holds dp^(l) after kernel C
+  const int ta = tid / (TW / OPT), tc = (tid % (TW / OPT)) * OPT;   // output (a0 + ta, c0 + tc ..)
+  float acc[OPT];
+#pragma unroll
+  for (int e = 0; e < OPT; ++e) acc[e] = 0.f;
+  for (int m0 = 0; m0 < NTOK; m0 += 32) {
+    for (int idx = tid; idx < 32 * TW; idx += kBwdThreads) {
+      const int i = idx / TW, j = idx % TW, m = m0 + i;
+      const size_t n = (size_t)m * H + h;
+      sA[i][j] = m < NTOK ? src[(n * L + l) * D + a0 + j] : 0.f;
+      sUt[i][j] = m < NTOK ? p.U[n * D + c0 + j] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+      const float av = sA[i][ta];
+#pragma unroll
+      for (int e = 0; e < OPT; ++e) acc[e] = fmaf(av, sUt[i][tc + e], acc[e]);
+    }
+    __syncthreads();
+  }
+  float* dst = (which == 0 ? p.dWk : p.dWp) + (((size_t)h * L + l) * D + a0 + ta) * D + c0 + tc;
+#pragma unroll
+  for (int e = 0; e < OPT; ++e) dst[e] = acc[e];
+}
+
+// dw_beta^(l)[c] = sum_tokens dz^(l) u[c];  dconv[j-1][c] = sum_tokens du_t[c] v_(t-j)[c].
+// One CTA per (32 channels, head); thread (channel, token lane) over every 8th token.
+template <class T, int D>
+__global__ void __launch_bounds__(kBwdThreads) bwd_small_weight_kernel(BwdArgs p) {
+  __shared__ float sRed[8][32][kBwdLmax + 8 + 1];
+  const int tid = threadIdx.x, cl = tid % 32, tl = tid / 32;
+  const int c = blockIdx.x * 32 + cl, h = blockIdx.y;
+  const int H = p.H, T_ = p.T, L = p.L, w = p.w;
+  const T* vg = static_cast<const T*>(p.v);
+  float acc[kBwdLmax + 8];
+#pragma unroll
+  for (int j = 0; j < kBwdLmax + 8; ++j) acc[j] = 0.f;
+  for (int b = 0; b < p.B && c < D; ++b) {
+    const int len = bwd_len(p, b);
+    for (int t = tl; t < len; t += 8) {
+      const size_t n = ((size_t)b * T_ + t) * H + h;
+      const float uc = p.U[n * D + c], du = p.dU[n * D + c];
+      for (int l = 0; l < L; ++l) acc[l] = fmaf(p.dZ[n * L + l], uc, acc[l]);
+      for (int j = 1; j <= w && j <= t; ++j)
+        acc[kBwdLmax + j - 1] = fmaf(du, Elem<T>::to_f(vg[(((size_t)b * T_ + t - j) * H + h) * D + c]), acc[kBwdLmax + j - 1]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kBwdLmax + 8; ++j) sRed[tl][cl][j] = acc[j];
+  __syncthreads();
+  if (tl == 0 && c < D) {
+    for (int l = 0; l < L; ++l) {
+      float s = 0.f;
+      for (int q = 0; q < 8; ++q) s += sRed[q][cl][l];
+      p.dwb[((size_t)h * L + l) * D + c] = s;
+    }
+    for (int j = 1; j <= w; ++j) {
+      float s = 0.f;
+      for (int q = 0; q < 8; ++q) s += sRed[q][cl][kBwdLmax + j - 1];
+      p.dconv[((size_t)h * w + j - 1) * D + c] = s;
+    }
+  }
+}
+
+// E: dv_t += sum_{j=1..w} c_j (.) du_(t+j) over tokens t + j inside the sequence.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads) bwd_conv_dv_kernel(BwdArgs p) {
+  const size_t total = (size_t)p.B * p.T * p.H * D;
+  for (size_t idx = (size_t)blockIdx.x * kBwdThreads + threadIdx.x; idx < total; idx += (size_t)gridDim.x * kBwdThreads) {
+    const int c = idx % D;
+    const size_t n = idx / D;
+    const int h = n % p.H;
+    const size_t bt = n / p.H;
+    const int t = bt % p.T, b = bt / p.T;
+    const int len = bwd_len(p, b);
+    if (t >= len) continue;
+    float s = 0.f;
+    for (int j = 1; j <= p.w && t + j < len; ++j)
+      s = fmaf(p.conv_w[((size_t)h * p.w + j - 1) * D + c], p.dU[(n + (size_t)j * p.H) * D + c], s);
+    p.dv[idx] += s;
+  }
+}
+
+}  // namespace prism

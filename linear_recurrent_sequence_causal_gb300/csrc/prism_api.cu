@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "../../include/prism.h"
+#include "backward.cuh"
 #include "decode.cuh"
 #include "kernels.h"
 #include "kernels_tc.cuh"
@@ -29,6 +30,7 @@ PRISM_DECL_TC(128)
 #undef PRISM_DECL_TC
 cudaError_t launch_scan_tc_128(int C, const ScanTcArgs& a, cudaStream_t s);
 cudaError_t launch_decode(int dtype, int D, const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_backward(int dtype, int D, const BwdArgs& a, cudaStream_t s);
 
 cudaError_t launch_k2(int dtype, int D, int C, const K2Args& a, cudaStream_t s) {
   if (dtype != 0) return cudaErrorInvalidValue;
@@ -416,6 +418,102 @@ extern "C" PRISM_API int prism_decode_step(const prism_dims* dims, const void* q
   a.Wk = Wk; a.Wp = Wp; a.wbeta = wbeta; a.state = state; a.vhist = v_hist; a.out = out;
   return prism::launch_decode(dims->dtype == PRISM_F32 ? 0 : 1, D, a, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
+             ? PRISM_OK
+             : PRISM_ERR_LAUNCH;
+}
+
+namespace {
+
+// Backward-pass workspace: per token-head factors, then the state checkpoints and the
+// block scratch.  Offsets in floats of each region, 256-byte aligned.
+struct BwdLayout {
+  size_t U, KL, DL, P, NRM, Z, dDL, dKL, dKH, dZ, dU, CK, SCR, total;
+};
+
+BwdLayout bwd_layout(const prism_dims* d) {
+  BwdLayout Lo;
+  size_t cur = 0;
+  auto take = [&](size_t floats) {
+    const size_t o = cur;
+    cur += round256(floats * 4) / 4;
+    return o;
+  };
+  const size_t D = d->d_k, L = d->L, NTH = (size_t)d->B * d->T * d->H;
+  const size_t NCK = (d->T + prism::kBwdCK - 1) / prism::kBwdCK;
+  Lo.U = take(NTH * D);
+  Lo.KL = take(NTH * L * D);
+  Lo.DL = take(NTH * L * D);
+  Lo.P = take(NTH * L * D);
+  Lo.NRM = take(NTH * L);
+  Lo.Z = take(NTH * L);
+  Lo.dDL = take(NTH * L * D);
+  Lo.dKL = take(NTH * L * D);
+  Lo.dKH = take(NTH * L * D);
+  Lo.dZ = take(NTH * L);
+  Lo.dU = take(NTH * D);
+  Lo.CK = take((size_t)d->B * d->H * NCK * D * D);
+  Lo.SCR = take((size_t)d->B * d->H * prism::kBwdCK * D * D);
+  Lo.total = cur * 4;
+  return Lo;
+}
+
+int check_bwd_dims(const prism_dims* d) {
+  if (!d) return PRISM_ERR_INVALID_ARG;
+  if (d->dtype != PRISM_F32 && d->dtype != PRISM_BF16) return PRISM_ERR_INVALID_ARG;
+  if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->d_k <= 0 || d->d_v <= 0 || d->L < 0 || d->conv_width <= 0)
+    return PRISM_ERR_INVALID_ARG;
+  if (d->flags & ~PRISM_FLAG_NO_GELU) return PRISM_ERR_INVALID_ARG;
+  const int D = d->d_k;
+  if (d->d_k != d->d_v || (D != 16 && D != 32 && D != 64 && D != 128) || d->L > kMaxL ||
+      d->conv_width > kMaxW)
+    return PRISM_ERR_UNSUPPORTED;
+  if ((long long)d->B * d->T > (1LL << 31) - 1 || d->H > 65535 || d->B > 65535) return PRISM_ERR_UNSUPPORTED;
+  return PRISM_OK;
+}
+
+}  // namespace
+
+extern "C" PRISM_API size_t prism_backward_workspace_bytes(const prism_dims* dims) {
+  if (check_bwd_dims(dims) != PRISM_OK) return 0;
+  return bwd_layout(dims).total;
+}
+
+extern "C" PRISM_API int prism_backward(const prism_dims* dims, const void* q, const void* k,
+                                        const void* v, const float* log_alpha, const float* beta,
+                                        const float* conv_w, const float* Wk, const float* Wp,
+                                        const float* wbeta, const float* d_out,
+                                        const float* d_final_state, float* dq, float* dk, float* dv,
+                                        float* dlog_alpha, float* dbeta, float* dconv_w, float* dWk,
+                                        float* dWp, float* dwbeta, const int32_t* seq_lens,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_bwd_dims(dims);
+  if (rc != PRISM_OK) return rc;
+  const bool hasL = dims->L > 0;
+  if (!q || !k || !v || !log_alpha || !beta || !conv_w || !d_out || !dq || !dk || !dv || !dlog_alpha ||
+      !dbeta || !dconv_w)
+    return PRISM_ERR_INVALID_ARG;
+  if (hasL && (!Wk || !Wp || !wbeta || !dWk || !dWp || !dwbeta)) return PRISM_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, d_out, d_final_state, dq, dk, dv,
+                        dlog_alpha, dbeta, dconv_w, dWk, dWp, dwbeta, seq_lens};
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return PRISM_ERR_MISALIGNED;
+  if (workspace && !aligned(workspace, 256)) return PRISM_ERR_MISALIGNED;
+  const BwdLayout Lo = bwd_layout(dims);
+  if (!workspace || workspace_bytes < Lo.total) return PRISM_ERR_WORKSPACE;
+  float* ws = static_cast<float*>(workspace);
+  prism::BwdArgs a;
+  a.B = dims->B; a.T = dims->T; a.H = dims->H; a.L = dims->L; a.w = dims->conv_width;
+  a.flags = dims->flags;
+  a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.conv_w = conv_w;
+  a.Wk = Wk; a.Wp = Wp; a.wbeta = wbeta; a.d_out = d_out; a.d_fs = d_final_state;
+  a.seq_lens = seq_lens;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dla = dlog_alpha; a.dbeta = dbeta; a.dconv = dconv_w;
+  a.dWk = dWk; a.dWp = dWp; a.dwb = dwbeta;
+  a.U = ws + Lo.U; a.KL = ws + Lo.KL; a.DL = ws + Lo.DL; a.P = ws + Lo.P; a.NRM = ws + Lo.NRM;
+  a.Z = ws + Lo.Z; a.dDL = ws + Lo.dDL; a.dKL = ws + Lo.dKL; a.dKH = ws + Lo.dKH; a.dZ = ws + Lo.dZ;
+  a.dU = ws + Lo.dU; a.CK = ws + Lo.CK; a.SCR = ws + Lo.SCR;
+  return prism::launch_backward(dims->dtype == PRISM_F32 ? 0 : 1, dims->d_k, a,
+                                static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PRISM_OK
              : PRISM_ERR_LAUNCH;
 }

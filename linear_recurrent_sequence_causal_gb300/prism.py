@@ -24,7 +24,7 @@ ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
 STATIC_SCRATCH_BYTES = 32 << 20
 EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "prism_prepare",
            "prism_scan", "prism_forward_static", "prism_strerror", "prism_forward_from",
-           "prism_decode_step")
+           "prism_decode_step", "prism_backward_workspace_bytes", "prism_backward")
 WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC")
 
 
@@ -76,6 +76,10 @@ def load():
             lib.prism_decode_step.restype = ctypes.c_int
             lib.prism_decode_step.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 13
             lib.prism_forward_static.restype = ctypes.c_int
+            lib.prism_backward_workspace_bytes.argtypes = [ctypes.POINTER(Dims)]
+            lib.prism_backward_workspace_bytes.restype = ctypes.c_size_t
+            lib.prism_backward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 21 + [ctypes.c_size_t, _vp]
+            lib.prism_backward.restype = ctypes.c_int
             lib.prism_strerror.argtypes = [ctypes.c_int]
             lib.prism_strerror.restype = ctypes.c_char_p
             _lib = lib
@@ -185,6 +189,42 @@ def prism_forward_from(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk
                                    _stream_ptr(stream))
     _check(rc)
     return out, final_state
+
+
+def prism_backward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, d_out, *,
+                   d_final_state=None, seq_lens=None, workspace=None, grads=None, stream=None,
+                   no_gelu=False):
+    """Gradients through prism_forward given ``d_out`` [B,T,H,dv] fp32 (and optionally
+    ``d_final_state`` [B,H,dv,dk] fp32).  Returns a dict of fp32 CUDA tensors keyed q, k,
+    v, log_alpha, beta, conv_w, Wk, Wp, wbeta (shapes of the inputs; Wk, Wp, wbeta are
+    None when L = 0).  ``grads`` may pass preallocated outputs with the same keys."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dims = _dims_for(q, v, conv_w, L, 64, no_gelu)
+    dev = q.device
+    g = dict(grads) if grads else {}
+    shapes = {"q": (B, T, H, dk), "k": (B, T, H, dk), "v": (B, T, H, dv), "log_alpha": (B, T, H),
+              "beta": (B, T, H), "conv_w": tuple(conv_w.shape)}
+    if L > 0:
+        shapes.update(Wk=(H, L, dk, dv), Wp=(H, L, dv, dv), wbeta=(H, L, dv))
+    for n, shp in shapes.items():
+        if g.get(n) is None:
+            g[n] = torch.empty(shp, dtype=torch.float32, device=dev)
+    for n in ("Wk", "Wp", "wbeta"):
+        g.setdefault(n, None)
+    if workspace is None:
+        nbytes = load().prism_backward_workspace_bytes(ctypes.byref(dims))
+        if nbytes == 0:
+            raise PrismError(2, "prism_backward_workspace_bytes rejected the dims")
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    rc = load().prism_backward(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                               _ptr(beta), _ptr(conv_w), _ptr(Wk), _ptr(Wp), _ptr(wbeta),
+                               _ptr(d_out), _ptr(d_final_state), _ptr(g["q"]), _ptr(g["k"]),
+                               _ptr(g["v"]), _ptr(g["log_alpha"]), _ptr(g["beta"]), _ptr(g["conv_w"]),
+                               _ptr(g["Wk"]), _ptr(g["Wp"]), _ptr(g["wbeta"]), _ptr(seq_lens),
+                               _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _check(rc)
+    return g
 
 
 def prism_decode_step(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, state, v_hist, *,

@@ -1,0 +1,92 @@
+"""GPU parity of the backward pass (prism_backward) against the gradient oracle
+(oracle/grad.py: autograd of the fp64 token recurrence, pinned to the C oracle by finite
+differences).
+
+Tolerance: the GPU computes every gradient in fp32 from the same (bf16-exact or fp32)
+inputs, so the gap to the fp64 reference is fp32 rounding carried through the backward
+recurrence and the token sums of the weight gradients.  Each gradient tensor is compared
+normwise, max|g_gpu - g_ref| / max|g_ref| <= 2e-4 (the forward's fp32 bound of 1e-4,
+doubled for the second pass over the same operations); padding tokens' gradients are
+exactly zero.
+"""
+import numpy as np
+import pytest
+import torch
+
+from linear_recurrent_sequence_causal_gb300 import inputs as I
+from linear_recurrent_sequence_causal_gb300 import prism
+from oracle import grad as G
+
+pytestmark = pytest.mark.gpu
+
+GRAD_TOL = 2e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU required for -m gpu tests")
+    prism.load()
+
+
+def _run(dtype, D, L, T, B, H, w, ragged, no_gelu, with_fs, seed):
+    wl = I.Workload("bwd", dtype, B, T, H, D, D, L, w, 16, seed=seed, ragged=ragged)
+    inp = I.generate(wl)
+    if ragged:                                   # lengths over the whole range, one full
+        g = torch.Generator().manual_seed(seed)
+        lens = torch.randint(1, T + 1, (B,), generator=g, dtype=torch.int32)
+        lens[0] = T
+        inp["seq_lens"] = lens
+    rng = np.random.default_rng(seed)
+    d_out = rng.standard_normal((B, T, H, D)).astype(np.float32)
+    d_fs = rng.standard_normal((B, H, D, D)).astype(np.float32) if with_fs else None
+    ref = G.backward(inp, d_out.astype(np.float64), None if d_fs is None else d_fs.astype(np.float64),
+                     identity_act=no_gelu)
+    d = prism.inputs_to_device(inp)
+    gg = prism.prism_backward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"],
+                              d["Wk"], d["Wp"], d["wbeta"], L, torch.from_numpy(d_out).cuda(),
+                              d_final_state=None if d_fs is None else torch.from_numpy(d_fs).cuda(),
+                              seq_lens=d.get("seq_lens"), no_gelu=no_gelu)
+    torch.cuda.synchronize()
+    return inp, ref, gg
+
+
+CASES = [
+    # dtype, D, L, T, B, H, w, ragged, no_gelu, d_final_state
+    ("f32", 16, 2, 37, 2, 2, 4, True, False, True),
+    ("bf16", 32, 3, 50, 2, 2, 3, True, True, False),
+    ("bf16", 64, 0, 33, 1, 2, 4, False, False, True),
+    ("bf16", 128, 2, 40, 1, 2, 4, False, False, True),
+    ("f32", 64, 4, 21, 2, 1, 8, True, False, False),
+    ("bf16", 128, 1, 17, 1, 1, 1, False, False, False),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "-".join(map(str, c)))
+def test_backward_matches_oracle(case):
+    dtype, D, L, T, B, H, w, ragged, no_gelu, with_fs = case
+    inp, ref, gg = _run(dtype, D, L, T, B, H, w, ragged, no_gelu, with_fs, seed=90 + D + L + T)
+    errs = {}
+    for n in G.GRAD_KEYS:
+        if L == 0 and n in ("Wk", "Wp", "wbeta"):
+            continue
+        gpu = gg[n].double().cpu().numpy()
+        r = ref[n]
+        if n in ("Wk", "Wp", "wbeta"):
+            r = r[:, :L]
+        assert np.all(np.isfinite(gpu)), f"d{n}: non-finite"
+        scale = max(np.max(np.abs(r)), 1e-30)
+        errs[n] = np.max(np.abs(gpu - r)) / scale
+    bad = {n: e for n, e in errs.items() if e > GRAD_TOL}
+    assert not bad, f"gradient errors above {GRAD_TOL}: {bad} (all: {errs})"
+    if inp.get("seq_lens") is not None:
+        for b, n in enumerate(inp["seq_lens"].tolist()):
+            for key in ("q", "k", "v", "log_alpha", "beta"):
+                assert not torch.any(gg[key][b, n:]), f"d{key} of padding tokens in sequence {b}"
+
+
+def test_backward_is_deterministic():
+    _, _, g1 = _run("bf16", 64, 2, 45, 2, 2, 4, True, False, True, seed=7)
+    _, _, g2 = _run("bf16", 64, 2, 45, 2, 2, 4, True, False, True, seed=7)
+    for n in G.GRAD_KEYS:
+        assert torch.equal(g1[n], g2[n]), f"d{n} differs between two identical calls"
