@@ -10,6 +10,9 @@ no collective): weak scaling.
 
 ``--impl reference`` times the fp64 CPU oracle (the only other implementation
 of the method) on the host cores, on a bounded sample of the same workload.
+
+``--backward`` times the backward pass instead (prism_backward: all gradients given
+d_out and d_final_state), with the gradient oracle as its CPU baseline.
 """
 from __future__ import annotations
 
@@ -376,6 +379,159 @@ def our_arm(args, wl, L):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------- backward arm
+BWD_METRIC = "PRISM mixer bwd tokens/s on 1 GB300 (all gradients, fp32 CUDA-core kernels)"
+# FP32 FMA rate of the CUDA cores: 152 SMs x 128 lanes x 2 flop x 2.07 GHz (unit counts and
+# the maximum SM clock); the backward kernels are fp32 arithmetic, not tensor-core work.
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def bwd_algorithmic(wl, L):
+    """Flops and unavoidable bytes of one backward pass (per token-head, d = d_k = d_v):
+    flops d^2 (28 + 20 L): the state sweep forward, its block recompute and the reverse
+    step (2 d^2 (14 + 4 L)), the refinement projections and their transposes (8 L d^2),
+    the weight-gradient outer products (4 L d^2); bytes: q, k, v, gates and d_out read,
+    dq, dk, dv, dlog_alpha, dbeta written (fp32): 3 d e + 4 d + 8 + 12 d + 8."""
+    d, e = wl.dk, (4 if wl.dtype == "f32" else 2)
+    th = wl.B * wl.T * wl.H
+    flops = th * d * d * (28.0 + 20.0 * L)
+    by = th * (3 * d * e + 16 * d + 16) + wl.H * (2 * L * d * d + L * d + wl.w * d) * 4 * 2
+    return by, flops
+
+
+def grad_oracle_sample(host, wl, L, target_s):
+    """Time the gradient oracle on a bounded sample: sequence 0, one head, a prefix
+    calibrated to about ``target_s`` seconds."""
+    from oracle import grad as G
+
+    def run(T):
+        sub = {}
+        for k, v in host.items():
+            if k in ("q", "k", "v", "log_alpha", "beta"):
+                sub[k] = v[:1, :T, :1].contiguous()
+            elif k in ("conv_w", "Wk", "Wp", "wbeta"):
+                sub[k] = v[:1].contiguous()
+            else:
+                sub[k] = None
+        d_out = torch.ones((1, T, 1, wl.dv), dtype=torch.float64)
+        t0 = time.perf_counter()
+        G.backward(sub, d_out, None, L=L)
+        return time.perf_counter() - t0
+
+    probe = min(wl.T, 32)
+    dt = run(probe)
+    T = max(probe, min(wl.T, int(probe * target_s / max(dt, 1e-6))))
+    dt = run(T) if T != probe else dt
+    return T, dt
+
+
+def backward_arm(args, wl, L):
+    from linear_recurrent_sequence_causal_gb300 import build, prism
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if build.stale():
+        raise RuntimeError("libprism.so is missing or stale: run __graft_entry__.build() first")
+    prism.load()
+    dev = torch.device("cuda", local)
+    host = I.generate(wl, L=L, seed=wl.seed)
+    d = prism.inputs_to_device(host, dev)
+    B, T, H, D = wl.B, wl.T, wl.H, wl.dk
+    g = torch.Generator().manual_seed(wl.seed + 1)
+    h_dout = torch.randn((B, T, H, D), generator=g, dtype=torch.float32)
+    h_dfs = torch.randn((B, H, D, D), generator=g, dtype=torch.float32)
+    d_out, d_fs = h_dout.to(dev), h_dfs.to(dev)
+    dims = prism.make_dims(B, T, H, D, D, wl.w, L, wl.chunk, wl.torch_dtype)
+    ws = torch.empty(prism.load().prism_backward_workspace_bytes(ctypes_byref(dims)), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+    grads = prism.prism_backward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"], d["Wk"],
+                                 d["Wp"], d["wbeta"], L, d_out, d_final_state=d_fs,
+                                 seq_lens=d.get("seq_lens"), workspace=ws, stream=stream)
+
+    def step():
+        prism.prism_backward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"], d["Wk"],
+                             d["Wp"], d["wbeta"], L, d_out, d_final_state=d_fs,
+                             seq_lens=d.get("seq_lens"), workspace=ws, grads=grads, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = a.elapsed_time(b) / args.steps
+    tokens = B * T
+    value = tokens / (ms / 1e3)
+
+    # end to end: inputs and d_out from pinned host memory, every gradient back to the host
+    pinned = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
+    p_dout, p_dfs = h_dout.pin_memory(), h_dfs.pin_memory()
+    host_g = {k: (torch.empty(v.shape, dtype=v.dtype).pin_memory() if v is not None else None)
+              for k, v in grads.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values() if v is not None) \
+        + p_dout.numel() * 4 + p_dfs.numel() * 4
+    d2h = sum(v.numel() * 4 for v in host_g.values() if v is not None)
+
+    def e2e_step():
+        for k, v in pinned.items():
+            if v is not None:
+                d[k].copy_(v, non_blocking=True)
+        d_out.copy_(p_dout, non_blocking=True)
+        d_fs.copy_(p_dfs, non_blocking=True)
+        step()
+        for k, v in host_g.items():
+            if v is not None:
+                v.copy_(grads[k], non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a.elapsed_time(b) / e2e_steps
+
+    hbm, _, peak_kind = load_peaks()
+    by, fl = bwd_algorithmic(wl, L)
+    roof = {"bound": "alu", "achieved": fl / (ms / 1e3) / 1e12, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+            "traffic": None, "kernel": "prism_backward (five kernels, timed as one call)",
+            "peak_source": "fp32 FMA lanes x maximum SM clock (derived; not in MEASURED_PEAKS.json)",
+            "algorithmic_flops": fl, "algorithmic_bytes": by,
+            "hbm_view": {"achieved_GBps": by / (ms / 1e3) / 1e9, "peak_GBps": hbm, "peak_kind": peak_kind}}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    line = {"metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "B": B, "T": T, "H": H, "d_k": D, "d_v": D, "L": L,
+                       "conv_width": wl.w, "pass": "backward"},
+            "roofline": roof, "clocks": clk,
+            "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * (5 + (1 if L > 0 else 0))}
+    if not args.no_cpu_baseline:
+        Ts, dts = grad_oracle_sample(host, wl, L, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": Ts / dts / H, "unit": UNIT, "cores": torch.get_num_threads(),
+                                "kind": "oracle",
+                                "sample": f"gradient oracle (torch fp64 autograd), sequence 0, head 0 of "
+                                          f"{H}, first {Ts} tokens: {dts:.1f} s; scaled to tokens of all "
+                                          f"{H} heads"}
+    print(json.dumps(line), flush=True)
+
+
+def ctypes_byref(x):
+    import ctypes
+    return ctypes.byref(x)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -386,11 +542,14 @@ def main():
     ap.add_argument("--L", type=int, default=None)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)     # at least 3 untimed warm-up steps, reported as run
     wl = I.get_workload(args.workload)
     L = wl.L if args.L is None else args.L
-    if args.impl == "reference":
+    if args.backward:
+        backward_arm(args, wl, L)
+    elif args.impl == "reference":
         reference_arm(args, wl, L)
     else:
         our_arm(args, wl, L)

@@ -417,62 +417,63 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
       const size_t n = tok(t);
       const float al = sSc[0], be = sSc[1];
       const float* zs = sZS + (t - c0) * D;
-      // phase 1 (rows): dS += do q^T; y = dS k; y_l = dS k^(l)
-      float y = 0.f, yl[kBwdLmax];
-#pragma unroll
-      for (int l = 0; l < kBwdLmax; ++l) yl[l] = 0.f;
-      {
-        const float dor = sdo[r];
+      // phase 1 (rows): dS += do q^T; y = dS k; y_l = dS k^(l)  (loops over l outside the
+      // column loops: no per-l arrays in registers)
+      const float dor = sdo[r];
+      float y = 0.f;
 #pragma unroll 4
-        for (int i = 0; i < CPT; ++i) {
-          const int c = cq + 4 * i;
-          const float ds = fmaf(dor, sq[c], sDS[r * LDS + c]);
-          sDS[r * LDS + c] = ds;
-          y = fmaf(ds, sk[c], y);
-          for (int l = 0; l < L; ++l) yl[l] = fmaf(ds, skl[l * D + c], yl[l]);
-        }
+      for (int i = 0; i < CPT; ++i) {
+        const int c = cq + 4 * i;
+        const float ds = fmaf(dor, sq[c], sDS[r * LDS + c]);
+        sDS[r * LDS + c] = ds;
+        y = fmaf(ds, sk[c], y);
       }
       y += __shfl_xor_sync(0xffffffffu, y, 1);
       y += __shfl_xor_sync(0xffffffffu, y, 2);
-#pragma unroll
-      for (int l = 0; l < kBwdLmax; ++l) {
-        if (l < L) {
-          yl[l] += __shfl_xor_sync(0xffffffffu, yl[l], 1);
-          yl[l] += __shfl_xor_sync(0xffffffffu, yl[l], 2);
-        }
+      const bool own = cq == 0;
+      for (int l = 0; l < L; ++l) {
+        float yl = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < CPT; ++i) yl = fmaf(sDS[r * LDS + cq + 4 * i], skl[l * D + cq + 4 * i], yl);
+        yl += __shfl_xor_sync(0xffffffffu, yl, 1);
+        yl += __shfl_xor_sync(0xffffffffu, yl, 2);
+        if (own) p.dDL[(n * L + l) * D + r] = yl;
+        const float s = warp_sum(own ? sdl[l * D + r] * dor : 0.f);   // D^(l) . do
+        if (lane == 0) sRed[warp * 16 + 4 + l] = s;
       }
-      // per-row scalars (summed over rows below): v.y, z.y, z.do, v.do, D^(l).do
-      float sc[4 + kBwdLmax];
       {
-        const bool own = cq == 0;
-        const float zr = zs[r], vr = sv[r], dor = sdo[r];
-        sc[0] = own ? vr * y : 0.f;
-        sc[1] = own ? zr * y : 0.f;
-        sc[2] = own ? zr * dor : 0.f;
-        sc[3] = own ? vr * dor : 0.f;
-#pragma unroll
-        for (int l = 0; l < kBwdLmax; ++l) sc[4 + l] = (own && l < L) ? sdl[l * D + r] * dor : 0.f;
+        // per-row scalars summed over rows: v.y, z.y, z.do, v.do
+        const float zr = zs[r], vr = sv[r];
+        const float s0 = warp_sum(own ? vr * y : 0.f);
+        const float s1 = warp_sum(own ? zr * y : 0.f);
+        const float s2 = warp_sum(own ? zr * dor : 0.f);
+        const float s3 = warp_sum(own ? vr * dor : 0.f);
+        if (lane == 0) {
+          sRed[warp * 16 + 0] = s0;
+          sRed[warp * 16 + 1] = s1;
+          sRed[warp * 16 + 2] = s2;
+          sRed[warp * 16 + 3] = s3;
+        }
         if (own) {
           sy[r] = y;
           p.dv[n * D + r] = be * y;
-          for (int l = 0; l < L; ++l) p.dDL[(n * L + l) * D + r] = yl[l];
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 4 + kBwdLmax; ++j) {
-        if (j < 4 + L) {
-          const float s = warp_sum(sc[j]);
-          if (lane == 0) sRed[warp * 16 + j] = s;
         }
       }
       bwd_cp_async_wait_all();
       __syncthreads();
-      // phase 2 (columns): S_(t-1)^T y, dS^T (beta v - alpha beta z), dS^T D^(l), <S_(t-1), dS>;
+      // phase 2 (columns): dS^T D^(l); S_(t-1)^T y, dS^T (beta v - alpha beta z), <S_(t-1), dS>;
       // then dS <- alpha (dS - beta y k^T)
+      for (int l = 0; l < L; ++l) {
+        float f = 0.f;
+#pragma unroll 4
+        for (int i = 0; i < CPT; ++i) {
+          const int rr = rq * CPT + i;
+          f = fmaf(sDS[rr * LDS + cc], sdl[l * D + rr], f);
+        }
+        sPart[(rq * (2 + kBwdLmax) + 2 + l) * D + cc] = f;
+      }
       {
-        float bS = 0.f, e = 0.f, fro = 0.f, f[kBwdLmax];
-#pragma unroll
-        for (int l = 0; l < kBwdLmax; ++l) f[l] = 0.f;
+        float bS = 0.f, e = 0.f, fro = 0.f;
         const float kc = sk[cc];
 #pragma unroll 4
         for (int i = 0; i < CPT; ++i) {
@@ -481,12 +482,10 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
           bS = fmaf(s, yr, bS);
           e = fmaf(ds, be * (sv[rr] - al * zs[rr]), e);
           fro = fmaf(s, ds, fro);
-          for (int l = 0; l < L; ++l) f[l] = fmaf(ds, sdl[l * D + rr], f[l]);
           sDS[rr * LDS + cc] = al * (ds - be * yr * kc);
         }
         sPart[(rq * (2 + kBwdLmax) + 0) * D + cc] = bS;
         sPart[(rq * (2 + kBwdLmax) + 1) * D + cc] = e;
-        for (int l = 0; l < L; ++l) sPart[(rq * (2 + kBwdLmax) + 2 + l) * D + cc] = f[l];
         fro = warp_sum(fro);
         if (lane == 0) sRed[warp * 16 + 15] = fro;
       }
@@ -494,27 +493,25 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
       // phase 3: per-token gradients
       if (tid < D) {
         const int c = tid;
-        float tot[2 + kBwdLmax];
-#pragma unroll
-        for (int j = 0; j < 2 + kBwdLmax; ++j) tot[j] = 0.f;
+        float t0s = 0.f, t1s = 0.f, zd = 0.f, vd = 0.f;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          tot[0] += sPart[(q4 * (2 + kBwdLmax) + 0) * D + c];
-          tot[1] += sPart[(q4 * (2 + kBwdLmax) + 1) * D + c];
-          for (int l = 0; l < L; ++l) tot[2 + l] += sPart[(q4 * (2 + kBwdLmax) + 2 + l) * D + c];
+          t0s += sPart[(q4 * (2 + kBwdLmax) + 0) * D + c];
+          t1s += sPart[(q4 * (2 + kBwdLmax) + 1) * D + c];
         }
-        float zd = 0.f, vd = 0.f;
         for (int wv = 0; wv < NW; ++wv) {
           zd += sRed[wv * 16 + 2];
           vd += sRed[wv * 16 + 3];
         }
-        p.dk[n * D + c] = tot[1] - al * be * tot[0];
+        p.dk[n * D + c] = t1s - al * be * t0s;
         float dqc = al * (sAS[(t - c0) * D + c] - be * zd * sk[c]) + be * vd * sk[c];
         for (int l = 0; l < L; ++l) {
-          float ddl = 0.f;
+          float ddl = 0.f, tl = 0.f;
           for (int wv = 0; wv < NW; ++wv) ddl += sRed[wv * 16 + 4 + l];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) tl += sPart[(q4 * (2 + kBwdLmax) + 2 + l) * D + c];
           dqc = fmaf(ddl, skl[l * D + c], dqc);
-          p.dKL[(n * L + l) * D + c] = tot[2 + l];
+          p.dKL[(n * L + l) * D + c] = tl;
         }
         p.dq[n * D + c] = dqc;
         if (c == 0) {
