@@ -232,17 +232,16 @@ template <int D>
 struct BwdBSmem {
   static constexpr int LDS = D + 4;                                 // 16-byte rows, no bank conflicts
   static constexpr int NT = 4 * D, NW = NT / 32;
+  static constexpr int TOKF = (4 + 2 * kBwdLmax) * D + 2;           // floats of one token's vectors
+  static constexpr int PF = (TOKF + NT - 1) / NT;                   // of them per thread
   static constexpr size_t oDS = 0;                                  // dS [D][D+4]
   static constexpr size_t oS = oDS + 4u * D * LDS;                  // S  [D][D+4]
-  static constexpr size_t oVec = oS + 4u * D * LDS;                 // k, q, do, v, y: 5 x D
-  static constexpr size_t oKL = oVec + 4u * 5 * D;                  // k^(l) [Lmax][D]
-  static constexpr size_t oDL = oKL + 4u * kBwdLmax * D;            // D^(l) [Lmax][D]
-  static constexpr size_t oZS = oDL + 4u * kBwdLmax * D;            // S_(t-1) k_t of the block [CK][D]
-  static constexpr size_t oAS = oZS + 4u * kBwdCK * D;              // S_(t-1)^T do_t of the block [CK][D]
-  static constexpr size_t oPart = oAS + 4u * kBwdCK * D;            // column partial sums [4][2 + Lmax][D]
-  static constexpr size_t oRed = oPart + 4u * 4 * (2 + kBwdLmax) * D;   // scalar partials [NW][16]
-  static constexpr size_t oSc = oRed + 4u * NW * 16;                // alpha, beta of the token
-  static constexpr size_t bytes = oSc + 16;
+  static constexpr size_t oVec = oS + 4u * D * LDS;                 // k | v | do | q | k^(l) | D^(l) | la, beta
+  static constexpr size_t oY = oVec + 4u * ((TOKF + 3) / 4 * 4);    // y [D]
+  static constexpr size_t oZS = oY + 4u * D;                        // S_(t-1) k_t of the block [CK][D]
+  static constexpr size_t oPart = oZS + 4u * kBwdCK * D;            // column partial sums [4][3 + Lmax][D]
+  static constexpr size_t oRed = oPart + 4u * 4 * (3 + kBwdLmax) * D;   // scalar partials [NW][16]
+  static constexpr size_t bytes = oRed + 4u * NW * 16;
 };
 
 __device__ __forceinline__ void bwd_cp_async16(void* dst, const void* src) {
@@ -260,34 +259,20 @@ __device__ __forceinline__ void bwd_state_load_async(float* sS, const float* g) 
   }
   bwd_cp_async_commit();
 }
-template <int D>
-__device__ __forceinline__ void bwd_state_store(const float* sS, float* g) {
-  using S = BwdBSmem<D>;
-  for (int idx = threadIdx.x; idx < D * D / 4; idx += S::NT) {
-    const int r = (idx * 4) / D, c = (idx * 4) % D;
-    *reinterpret_cast<float4*>(g + (size_t)idx * 4) = *reinterpret_cast<const float4*>(sS + r * S::LDS + c);
-  }
-}
 
 template <class T, int D>
 __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
   using S = BwdBSmem<D>;
-  constexpr int LDS = S::LDS, NT = S::NT, NW = S::NW, CPT = D / 4;
+  constexpr int LDS = S::LDS, NT = S::NT, NW = S::NW, CPT = D / 4, PF = S::PF;
+  constexpr int NSLOT = 3 + kBwdLmax;
   extern __shared__ __align__(1024) unsigned char sm[];
   float* sDS = reinterpret_cast<float*>(sm + S::oDS);
   float* sS = reinterpret_cast<float*>(sm + S::oS);
-  float* sk = reinterpret_cast<float*>(sm + S::oVec);
-  float* sq = sk + D;
-  float* sdo = sq + D;
-  float* sv = sdo + D;
-  float* sy = sv + D;
-  float* skl = reinterpret_cast<float*>(sm + S::oKL);
-  float* sdl = reinterpret_cast<float*>(sm + S::oDL);
+  float* svec = reinterpret_cast<float*>(sm + S::oVec);
+  float* sy = reinterpret_cast<float*>(sm + S::oY);
   float* sZS = reinterpret_cast<float*>(sm + S::oZS);
-  float* sAS = reinterpret_cast<float*>(sm + S::oAS);
   float* sPart = reinterpret_cast<float*>(sm + S::oPart);
   float* sRed = reinterpret_cast<float*>(sm + S::oRed);
-  float* sSc = reinterpret_cast<float*>(sm + S::oSc);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = tid >> 2, cq = tid & 3;              // row mapping
@@ -296,11 +281,19 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
   const int H = p.H, T_ = p.T, L = p.L;
   const int len = bwd_len(p, b);
   const int NCK = (T_ + kBwdCK - 1) / kBwdCK;
+  const int TOK = (4 + 2 * L) * D + 2;               // floats of a token's vectors at this L
   const T* qg = static_cast<const T*>(p.q);
   const T* kg = static_cast<const T*>(p.k);
   const T* vg = static_cast<const T*>(p.v);
   float* ck = p.CK + ((size_t)b * H + h) * NCK * D * D;
   float* scr = p.SCR + ((size_t)b * H + h) * kBwdCK * D * D;
+  float* sk = svec;
+  float* sv = svec + D;
+  float* sdo = svec + 2 * D;
+  float* sq = svec + 3 * D;
+  float* skl = svec + 4 * D;
+  float* sdl = skl + L * D;
+  const float* sgate = sdl + L * D;                  // log alpha, beta
   auto tok = [&](int t) { return ((size_t)b * T_ + t) * H + h; };
 
   // padding tokens: every per-token gradient is zero
@@ -322,23 +315,31 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
   }
   if (len <= 0) return;
 
-  // token t's vectors into shared memory (k, v and the refinement factors; q and do too)
-  auto load_token = [&](int t, bool with_q) {
+  // A token's vectors are fetched into registers one token ahead (the loads overlap the
+  // current token's work) and committed to shared memory at the next token's start.
+  float pf[PF];
+  auto fetch = [&](int t) {
     const size_t n = tok(t);
-    for (int idx = tid; idx < D; idx += NT) {
-      sk[idx] = Elem<T>::to_f(kg[n * D + idx]);
-      sv[idx] = Elem<T>::to_f(vg[n * D + idx]);
-      sdo[idx] = p.d_out[n * D + idx];
-      if (with_q) sq[idx] = Elem<T>::to_f(qg[n * D + idx]);
+#pragma unroll
+    for (int j = 0; j < PF; ++j) {
+      int e = tid + j * NT;
+      float x = 0.f;
+      if (e < TOK) {
+        if (e < D) x = Elem<T>::to_f(kg[n * D + e]);
+        else if ((e -= D) < D) x = Elem<T>::to_f(vg[n * D + e]);
+        else if ((e -= D) < D) x = p.d_out[n * D + e];
+        else if ((e -= D) < D) x = Elem<T>::to_f(qg[n * D + e]);
+        else if ((e -= D) < L * D) x = p.KL[n * L * D + e];
+        else if ((e -= L * D) < L * D) x = p.DL[n * L * D + e];
+        else x = (e - L * D == 0) ? p.log_alpha[n] : p.beta[n];
+      }
+      pf[j] = x;
     }
-    for (int idx = tid; idx < L * D; idx += NT) {
-      skl[idx] = p.KL[n * L * D + idx];
-      sdl[idx] = p.DL[n * L * D + idx];
-    }
-    if (tid == 0) {
-      sSc[0] = expf(p.log_alpha[n]);
-      sSc[1] = p.beta[n];
-    }
+  };
+  auto commit = [&]() {
+#pragma unroll
+    for (int j = 0; j < PF; ++j)
+      if (tid + j * NT < TOK) svec[tid + j * NT] = pf[j];
   };
   // z_r = S[r] . k (row mapping; every thread of the row gets it)
   auto row_dot_k = [&]() {
@@ -350,8 +351,9 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
     return z;
   };
   // S <- alpha (S - beta z k^T) + beta v k^T + sum_l D^(l) k^(l)^T on this thread's elements
+  // (rows of S evolve independently: no barrier between tokens)
   auto row_update = [&](float z) {
-    const float al = sSc[0], be = sSc[1];
+    const float al = expf(sgate[0]), be = sgate[1];
 #pragma unroll 4
     for (int i = 0; i < CPT; ++i) {
       const int c = cq + 4 * i;
@@ -360,18 +362,23 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
       sS[r * LDS + c] = x;
     }
   };
+  auto row_store = [&](float* g) {                   // this thread's elements of S to global
+#pragma unroll 4
+    for (int i = 0; i < CPT; ++i) g[r * D + cq + 4 * i] = sS[r * LDS + cq + 4 * i];
+  };
 
   // ---- forward: checkpoints (the state before tokens 0, CK, 2 CK, ...) ----
   for (int idx = tid; idx < D * LDS; idx += NT) sS[idx] = 0.f;
   __syncthreads();
-  bwd_state_store<D>(sS, ck);
+  row_store(ck);
+  fetch(0);
   for (int t = 0; t < len; ++t) {
-    load_token(t, false);
     __syncthreads();
-    const float z = row_dot_k();
-    row_update(z);
+    commit();
     __syncthreads();
-    if ((t + 1) % kBwdCK == 0 && t + 1 < len) bwd_state_store<D>(sS, ck + (size_t)((t + 1) / kBwdCK) * D * D);
+    if (t + 1 < len) fetch(t + 1);
+    row_update(row_dot_k());
+    if ((t + 1) % kBwdCK == 0 && t + 1 < len) row_store(ck + (size_t)((t + 1) / kBwdCK) * D * D);
   }
 
   // ---- backward ----
@@ -385,40 +392,32 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
     __syncthreads();
     bwd_state_load_async<D>(sS, ck + (size_t)blk * D * D);
     bwd_cp_async_wait_all();
-    __syncthreads();
-    // recompute the block: z_t = S_(t-1) k_t, a_t = S_(t-1)^T do_t, and the states after
-    // tokens c0 .. c1-2 into the scratch
+    fetch(c0);
+    // recompute the block: z_t = S_(t-1) k_t, and the states after tokens c0 .. c1-2
     for (int t = c0; t < c1; ++t) {
-      load_token(t, false);
       __syncthreads();
+      commit();
+      __syncthreads();
+      if (t + 1 < c1) fetch(t + 1);
       const float z = row_dot_k();
       if (cq == 0) sZS[(t - c0) * D + r] = z;
-      {
-        float a = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < CPT; ++i) {
-          const int rr = rq * CPT + i;
-          a = fmaf(sS[rr * LDS + cc], sdo[rr], a);
-        }
-        sPart[rq * D + cc] = a;
+      if (t < c1 - 1) {
+        row_update(z);
+        row_store(scr + (size_t)(t - c0) * D * D);
       }
-      __syncthreads();
-      if (tid < D) sAS[(t - c0) * D + tid] = sPart[tid] + sPart[D + tid] + sPart[2 * D + tid] + sPart[3 * D + tid];
-      row_update(z);
-      __syncthreads();
-      if (t < c1 - 1) bwd_state_store<D>(sS, scr + (size_t)(t - c0) * D * D);
     }
     // reverse through the block
+    fetch(c1 - 1);
     for (int t = c1 - 1; t >= c0; --t) {
       __syncthreads();                                 // previous token done with the buffers
+      commit();
       bwd_state_load_async<D>(sS, t > c0 ? scr + (size_t)(t - 1 - c0) * D * D : ck + (size_t)blk * D * D);
-      load_token(t, true);
       __syncthreads();
+      if (t - 1 >= c0) fetch(t - 1);
       const size_t n = tok(t);
-      const float al = sSc[0], be = sSc[1];
+      const float al = expf(sgate[0]), be = sgate[1];
       const float* zs = sZS + (t - c0) * D;
-      // phase 1 (rows): dS += do q^T; y = dS k; y_l = dS k^(l)  (loops over l outside the
-      // column loops: no per-l arrays in registers)
+      // phase 1 (rows): dS += do q^T; y = dS k; y_l = dS k^(l)
       const float dor = sdo[r];
       float y = 0.f;
 #pragma unroll 4
@@ -461,8 +460,8 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
       }
       bwd_cp_async_wait_all();
       __syncthreads();
-      // phase 2 (columns): dS^T D^(l); S_(t-1)^T y, dS^T (beta v - alpha beta z), <S_(t-1), dS>;
-      // then dS <- alpha (dS - beta y k^T)
+      // phase 2 (columns): dS^T D^(l); S_(t-1)^T y, S_(t-1)^T do, dS^T (beta v - alpha beta z),
+      // <S_(t-1), dS>; then dS <- alpha (dS - beta y k^T)
       for (int l = 0; l < L; ++l) {
         float f = 0.f;
 #pragma unroll 4
@@ -470,22 +469,24 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
           const int rr = rq * CPT + i;
           f = fmaf(sDS[rr * LDS + cc], sdl[l * D + rr], f);
         }
-        sPart[(rq * (2 + kBwdLmax) + 2 + l) * D + cc] = f;
+        sPart[(rq * NSLOT + 3 + l) * D + cc] = f;
       }
       {
-        float bS = 0.f, e = 0.f, fro = 0.f;
+        float bS = 0.f, e = 0.f, a = 0.f, fro = 0.f;
         const float kc = sk[cc];
 #pragma unroll 4
         for (int i = 0; i < CPT; ++i) {
           const int rr = rq * CPT + i;
           const float s = sS[rr * LDS + cc], ds = sDS[rr * LDS + cc], yr = sy[rr];
           bS = fmaf(s, yr, bS);
+          a = fmaf(s, sdo[rr], a);
           e = fmaf(ds, be * (sv[rr] - al * zs[rr]), e);
           fro = fmaf(s, ds, fro);
           sDS[rr * LDS + cc] = al * (ds - be * yr * kc);
         }
-        sPart[(rq * (2 + kBwdLmax) + 0) * D + cc] = bS;
-        sPart[(rq * (2 + kBwdLmax) + 1) * D + cc] = e;
+        sPart[(rq * NSLOT + 0) * D + cc] = bS;
+        sPart[(rq * NSLOT + 1) * D + cc] = e;
+        sPart[(rq * NSLOT + 2) * D + cc] = a;
         fro = warp_sum(fro);
         if (lane == 0) sRed[warp * 16 + 15] = fro;
       }
@@ -493,23 +494,24 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
       // phase 3: per-token gradients
       if (tid < D) {
         const int c = tid;
-        float t0s = 0.f, t1s = 0.f, zd = 0.f, vd = 0.f;
+        float t0s = 0.f, t1s = 0.f, t2s = 0.f, zd = 0.f, vd = 0.f;
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
-          t0s += sPart[(q4 * (2 + kBwdLmax) + 0) * D + c];
-          t1s += sPart[(q4 * (2 + kBwdLmax) + 1) * D + c];
+          t0s += sPart[(q4 * NSLOT + 0) * D + c];
+          t1s += sPart[(q4 * NSLOT + 1) * D + c];
+          t2s += sPart[(q4 * NSLOT + 2) * D + c];
         }
         for (int wv = 0; wv < NW; ++wv) {
           zd += sRed[wv * 16 + 2];
           vd += sRed[wv * 16 + 3];
         }
         p.dk[n * D + c] = t1s - al * be * t0s;
-        float dqc = al * (sAS[(t - c0) * D + c] - be * zd * sk[c]) + be * vd * sk[c];
+        float dqc = al * (t2s - be * zd * sk[c]) + be * vd * sk[c];
         for (int l = 0; l < L; ++l) {
           float ddl = 0.f, tl = 0.f;
           for (int wv = 0; wv < NW; ++wv) ddl += sRed[wv * 16 + 4 + l];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) tl += sPart[(q4 * (2 + kBwdLmax) + 2 + l) * D + c];
+          for (int q4 = 0; q4 < 4; ++q4) tl += sPart[(q4 * NSLOT + 3 + l) * D + c];
           dqc = fmaf(ddl, skl[l * D + c], dqc);
           p.dKL[(n * L + l) * D + c] = tl;
         }
