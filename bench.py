@@ -74,12 +74,19 @@ def load_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+# Sources of the forward kernels (the backward and decode kernels do not change them).
+FORWARD_SOURCES = ("prep_tc.cuh", "scan_tc.cuh", "scan_affine.cuh", "tc_common.cuh", "prism_common.cuh",
+                   "kernels_tc.cuh", "inst_tc_16.cu", "inst_tc_32.cu", "inst_tc_64.cu", "inst_tc_128.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_recurrent_sequence_causal_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+    for f in FORWARD_SOURCES:
+        path = os.path.join(csrc, f)
+        if os.path.exists(path):
+            with open(path, "rb") as fh:
+                h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
