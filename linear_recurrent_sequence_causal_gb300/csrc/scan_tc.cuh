@@ -5,9 +5,10 @@
 //   O   = O_intra + Qt S0^T               (C x BV), the chunk's outputs o_t = S_t q_t
 //   S1  = gamma_C S0 + E^T Kt + N         (BV x d_k)
 // Both products per chunk run on the tensor core with fp32 accumulators in TMEM:
-//   MMA1  [W ; Qt_hi] [S0_hi | S0_lo]^T   (128 x 2BV, K = d_k)   and
-//         [Qt_lo ; *] S0_hi^T              (128 x BV)
+//   MMA1  [W ; Qt_hi] [S0_hi | S0_lo]^T   (128 x 2BV, K = d_k)
 //   MMA2  Kt^T [E_hi | E_lo]               (d_k x 2BV, K = C)
+//   MMA1b [Qt_lo ; *] S0_hi^T              (128 x BV), issued after MMA2: it feeds only
+//         the outputs, so it runs while the epilogue updates the state
 // so W S0^T and Qt S0^T keep ~fp32 accuracy (hi*hi + hi*lo + lo*hi) and E enters
 // in two fp16 halves.  The chunk maps arrive in the layout prepare writes (16-byte
 // column pieces, in each piece W rows then Qt_hi rows, or Qt_lo rows then Kt rows),
@@ -55,8 +56,8 @@ struct ScanTcSmem {
   static constexpr int LDX = BV + 4;                     // padded row (conflict-free 16-byte accesses)
   static constexpr uint32_t oX = oE + kE;                // Qt_lo S0_hi^T rows, handed to the output rows
   static constexpr uint32_t kX = C * LDX * 4;
-  static constexpr uint32_t oBar = oX + kX;              // full[2], mma1, e_ready, mma2, s_ready
-  static constexpr uint32_t oSlot = oBar + 6 * 8;
+  static constexpr uint32_t oBar = oX + kX;              // full[2], mma1, e_ready, mma2, s_ready, mma1b
+  static constexpr uint32_t oSlot = oBar + 7 * 8;
   static constexpr uint32_t bytes = oSlot + 16;
   static constexpr int NW = 8;                          // epilogue warps
   static constexpr int NT = (NW + 1) * 32;
@@ -72,6 +73,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
   uint64_t* bar_e = bar_full + 3;
   uint64_t* bar_mma2 = bar_full + 4;
   uint64_t* bar_s = bar_full + 5;
+  uint64_t* bar_mma1b = bar_full + 6;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::oSlot);
   unsigned char* sS = sm + S::oS;
   unsigned char* sE = sm + S::oE;
@@ -94,6 +96,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
     tc::bar_init(bar_e, NW);
     tc::bar_init(bar_mma2, 1);
     tc::bar_init(bar_s, NW);
+    tc::bar_init(bar_mma1b, 1);
     tc::bar_fence_init();
   }
   if (warp == 0) tc::alloc(tslot, 256);
@@ -131,11 +134,11 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
         const unsigned char* base = sm + (buf ? S::oBuf1 : S::oBuf0);
         wait(bar_s, c & 1);                    // state tile of chunk c written, chunk c-1 consumed
         wait(bar_full + buf, (c >> 1) & 1);
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t bs = tc::desc(sS + kk * 256, 128, 16 * D);
-          tc::mma(t_d1, tc::desc(base + S::oWQ + kk * 2 * (2 * C * 16), 2 * C * 16, 128), bs, idesc_q2, kk > 0);
-          tc::mma(t_d2, tc::desc(base + S::oQK + kk * 2 * (2 * C * 16), 2 * C * 16, 128), bs, idesc_q1, kk > 0);
-        }
+        // MMA1a on the state chain; MMA1b (the Qt_lo rows, outputs only) after MMA2, so it
+        // runs while the epilogue updates the state
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma(t_d1, tc::desc(base + S::oWQ + kk * 2 * (2 * C * 16), 2 * C * 16, 128),
+                  tc::desc(sS + kk * 256, 128, 16 * D), idesc_q2, kk > 0);
         tc::commit(bar_mma1);
         if (c >= 1 && c + 1 < nchunks) load(c + 1, (c + 1) & 1);   // chunk c-1's buffer is free
         wait(bar_e, c & 1);                    // E tile written
@@ -143,6 +146,10 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
           tc::mma(t_d3, tc::desc(base + S::oQK + C * 16 + kk * 256, 128, 2 * C * 16),
                   tc::desc(sE + kk * 256, 128, 16 * C), idesc_k, kk > 0);
         tc::commit(bar_mma2);
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma(t_d2, tc::desc(base + S::oQK + kk * 2 * (2 * C * 16), 2 * C * 16, 128),
+                  tc::desc(sS + kk * 256, 128, 16 * D), idesc_q1, kk > 0);
+        tc::commit(bar_mma1b);
       }
     }
     __syncwarp();
@@ -193,16 +200,12 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
           tc::ld8a(t_d1 + lane_base + hf * HB + 8 * g, d1[g]);
           tc::ld8a(t_d1 + lane_base + BV + hf * HB + 8 * g, d1[2 + g]);
         }
+        tc::wait_ld();
         if (k < C) {
-          uint32_t d2[2][8];
-#pragma unroll
-          for (int g = 0; g < 2; ++g) tc::ld8a(t_d2 + lane_base + hf * HB + 8 * g, d2[g]);
-          tc::wait_ld();
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
             tc::pin(d1[g]);
             tc::pin(d1[2 + g]);
-            tc::pin(d2[g]);
             const int pc = 4 * hf + 2 * g;     // U piece (4 columns) of this group
             float uu[8], e8[8];
             const float4 u0 = *reinterpret_cast<const float4*>(sU + (pc * C + k) * 4);
@@ -218,28 +221,20 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
             const int n8 = 2 * hf + g;
             *reinterpret_cast<uint4*>(sE + n8 * (16u * C) + k * 16u) = hi;
             *reinterpret_cast<uint4*>(sE + (BV / 8 + n8) * (16u * C) + k * 16u) = lo;
-            float* xr = sX + k * S::LDX + hf * HB + 8 * g;
-            *reinterpret_cast<float4*>(xr) =
-                make_float4(__uint_as_float(d2[g][0]), __uint_as_float(d2[g][1]), __uint_as_float(d2[g][2]), __uint_as_float(d2[g][3]));
-            *reinterpret_cast<float4*>(xr + 4) =
-                make_float4(__uint_as_float(d2[g][4]), __uint_as_float(d2[g][5]), __uint_as_float(d2[g][6]), __uint_as_float(d2[g][7]));
           }
-        } else {
-          tc::wait_ld();
-          if (k < 2 * C) {
-            const int r = k - C;
+        } else if (k < 2 * C) {
+          const int r = k - C;
 #pragma unroll
-            for (int g = 0; g < 2; ++g) {
-              tc::pin(d1[g]);
-              tc::pin(d1[2 + g]);
-              const int pc = 4 * hf + 2 * g;
-              const float4 o0 = *reinterpret_cast<const float4*>(sOi + (pc * C + r) * 4);
-              const float4 o1 = *reinterpret_cast<const float4*>(sOi + ((pc + 1) * C + r) * 4);
-              const float oi[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+          for (int g = 0; g < 2; ++g) {
+            tc::pin(d1[g]);
+            tc::pin(d1[2 + g]);
+            const int pc = 4 * hf + 2 * g;
+            const float4 o0 = *reinterpret_cast<const float4*>(sOi + (pc * C + r) * 4);
+            const float4 o1 = *reinterpret_cast<const float4*>(sOi + ((pc + 1) * C + r) * 4);
+            const float oi[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                ov[8 * g + j] = oi[j] + (__uint_as_float(d1[g][j]) + __uint_as_float(d1[2 + g][j]));
-            }
+            for (int j = 0; j < 8; ++j)
+              ov[8 * g + j] = oi[j] + (__uint_as_float(d1[g][j]) + __uint_as_float(d1[2 + g][j]));
           }
         }
       }
@@ -247,19 +242,6 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
       tc::fence_before();
       __syncwarp();
       if (lane == 0) tc::bar_arrive(bar_e);
-      asm volatile("bar.sync 1, %0;\n" ::"n"(NW * 32) : "memory");   // the Qt_lo rows are in sX
-      if (k >= C && k < 2 * C) {
-        const int r = k - C;
-        if (r < nv) {
-          float* dst = p.out + (((size_t)b * T_ + t0 + r) * H + h) * D + v0 + hf * HB;
-#pragma unroll
-          for (int g = 0; g < HB / 4; ++g) {
-            const float4 x = *reinterpret_cast<const float4*>(sX + r * S::LDX + hf * HB + 4 * g);
-            *reinterpret_cast<float4*>(dst + 4 * g) =
-                make_float4(ov[4 * g] + x.x, ov[4 * g + 1] + x.y, ov[4 * g + 2] + x.z, ov[4 * g + 3] + x.w);
-          }
-        }
-      }
       // ---- S1^T = gamma_C S0^T + Kt^T E + N^T  (lane k, this column half) ----
       ok &= tc::bar_wait(bar_mma2, c & 1);
       tc::fence_after();
@@ -289,7 +271,39 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
                                  (__uint_as_float(d3[g][j]) + __uint_as_float(d3[2 + g][j])) + nn[j]);
         }
       }
+      // MMA1b (Qt_lo S0_hi^T) has read the state tile: the new state may replace it; the
+      // Qt_lo rows go to the output rows through sX
+      ok &= tc::bar_wait(bar_mma1b, c & 1);
+      tc::fence_after();
+      if ((warp & 3) * 32 < C && k < C) {
+        uint32_t d2[2][8];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) tc::ld8a(t_d2 + lane_base + hf * HB + 8 * g, d2[g]);
+        tc::wait_ld();
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          tc::pin(d2[g]);
+          float* xr = sX + k * S::LDX + hf * HB + 8 * g;
+          *reinterpret_cast<float4*>(xr) =
+              make_float4(__uint_as_float(d2[g][0]), __uint_as_float(d2[g][1]), __uint_as_float(d2[g][2]), __uint_as_float(d2[g][3]));
+          *reinterpret_cast<float4*>(xr + 4) =
+              make_float4(__uint_as_float(d2[g][4]), __uint_as_float(d2[g][5]), __uint_as_float(d2[g][6]), __uint_as_float(d2[g][7]));
+        }
+      }
       write_state();
+      asm volatile("bar.sync 1, %0;\n" ::"n"(NW * 32) : "memory");   // the Qt_lo rows are in sX
+      if (k >= C && k < 2 * C) {
+        const int r = k - C;
+        if (r < nv) {
+          float* dst = p.out + (((size_t)b * T_ + t0 + r) * H + h) * D + v0 + hf * HB;
+#pragma unroll
+          for (int g = 0; g < HB / 4; ++g) {
+            const float4 x = *reinterpret_cast<const float4*>(sX + r * S::LDX + hf * HB + 4 * g);
+            *reinterpret_cast<float4*>(dst + 4 * g) =
+                make_float4(ov[4 * g] + x.x, ov[4 * g + 1] + x.y, ov[4 * g + 2] + x.z, ov[4 * g + 3] + x.w);
+          }
+        }
+      }
     }
     // padded tokens: zero output columns of this slice
     for (size_t idx = tid; idx < (size_t)(T_ - len) * BV; idx += NW * 32) {
