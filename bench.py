@@ -74,15 +74,16 @@ def load_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-# Sources of the forward kernels (the backward and decode kernels do not change them).
-FORWARD_SOURCES = ("prep_tc.cuh", "scan_tc.cuh", "scan_affine.cuh", "tc_common.cuh", "prism_common.cuh",
-                   "kernels_tc.cuh", "inst_tc_16.cu", "inst_tc_32.cu", "inst_tc_64.cu", "inst_tc_128.cu")
+# Sources of each forward kernel (the backward and decode kernels do not change them).
+_COMMON = ("tc_common.cuh", "prism_common.cuh", "kernels_tc.cuh", "inst_tc_16.cu", "inst_tc_32.cu",
+           "inst_tc_64.cu", "inst_tc_128.cu")
+KERNEL_SOURCES = {"prepare": ("prep_tc.cuh",) + _COMMON, "scan": ("scan_tc.cuh", "scan_affine.cuh") + _COMMON}
 
 
-def kernel_source_hash():
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_recurrent_sequence_causal_gb300", "csrc")
-    for f in FORWARD_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         path = os.path.join(csrc, f)
         if os.path.exists(path):
             with open(path, "rb") as fh:
@@ -98,7 +99,7 @@ def committed_traffic(kernel, workload):
         with open(path) as f:
             t = json.load(f)
         ent = t[kernel][workload]
-        if ent.get("source_hash") != kernel_source_hash():
+        if ent.get("source_hash") != kernel_source_hash(kernel):
             return None
         return float(ent["dram_bytes_per_launch"])
     except Exception:
