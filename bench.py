@@ -218,6 +218,28 @@ def reference_arm(args, wl, L):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- ranks
+def replica_seed(wl, rank):
+    """Each rank times its own replica of the workload (independent sequences): the
+    inputs differ by rank through the seed."""
+    return wl.seed + rank
+
+
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time (the whole job ends when it does); ``ms`` unchanged on one
+    process."""
+    if dist is None:
+        return ms
+    t = torch.tensor([float(ms)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, ms_per_step):
+    """Whole-job tokens/s: the units all ranks processed over the slowest rank's time."""
+    return tokens_per_rank * world / (ms_per_step / 1e3)
+
+
 # ---------------------------------------------------------------- our arm
 def our_arm(args, wl, L):
     from linear_recurrent_sequence_causal_gb300 import build, prism
@@ -233,7 +255,7 @@ def our_arm(args, wl, L):
         raise RuntimeError("libprism.so is missing or stale: run __graft_entry__.build() first")
     prism.load()
     dev = torch.device("cuda", local)
-    host = I.generate(wl, L=L, seed=wl.seed + rank)
+    host = I.generate(wl, L=L, seed=replica_seed(wl, rank))
     d = prism.inputs_to_device(host, dev)
     B, T, H, D = wl.B, wl.T, wl.H, wl.dk
     dt = wl.torch_dtype
@@ -282,13 +304,10 @@ def our_arm(args, wl, L):
     elapsed_ms = t_start.elapsed_time(t_end)
     k1_ms = [e[0].elapsed_time(e[1]) for e in evs]
     k2_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     ms_per_step = elapsed_ms / args.steps
     tokens = B * T * world
-    value = tokens / (ms_per_step / 1e3)
+    value = job_throughput(B * T, world, ms_per_step)
 
     # ---- end to end through the public API: host (pinned) inputs, copies timed
     pinned = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
@@ -320,11 +339,8 @@ def our_arm(args, wl, L):
     b.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = a.elapsed_time(b) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = tokens / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    e2e_value = job_throughput(B * T, world, e2e_ms)
 
     # ---- roofline of the dominant kernel
     hbm, tc, peak_kind = load_peaks()
