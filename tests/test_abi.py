@@ -109,3 +109,35 @@ def test_decode_step_argument_errors(lib):
     bad = list(ok); bad[10] = 0x1008                                       # misaligned history
     assert lib.prism_decode_step(ctypes.byref(d), *bad, None) == 3
 
+
+
+def test_backward_argument_errors(lib):
+    """prism_backward and its workspace query reject bad dims and pointers before any
+    launch."""
+    d = prism.make_dims(2, 64, 2, 32, 32, 4, 2, 64, prism.PRISM_BF16)
+    nbytes = lib.prism_backward_workspace_bytes(ctypes.byref(d))
+    assert nbytes > 0 and nbytes % 256 == 0
+    d2 = prism.make_dims(2, 128, 2, 32, 32, 4, 2, 64, prism.PRISM_BF16)
+    assert lib.prism_backward_workspace_bytes(ctypes.byref(d2)) > nbytes     # grows with T
+    ok = [0x1000] * 21
+    ws = 0x100000
+
+    def call(dims, ptrs, wsb=1 << 40, w=ws):
+        return lib.prism_backward(ctypes.byref(dims), *ptrs, w, wsb, None)
+
+    bad = prism.make_dims(2, 64, 2, 32, 64, 4, 2, 64, prism.PRISM_BF16)       # d_k != d_v
+    assert lib.prism_backward_workspace_bytes(ctypes.byref(bad)) == 0
+    assert call(bad, ok) == 2
+    big_l = prism.make_dims(2, 64, 2, 32, 32, 4, 9, 64, prism.PRISM_BF16)     # L > 8
+    assert call(big_l, ok) == 2
+    for i in (0, 9, 11, 15):                       # q, d_out, dq, dbeta NULL
+        p = list(ok)
+        p[i] = None
+        assert call(d, p) == 1, f"pointer {i} NULL accepted"
+    p = list(ok)
+    p[10] = None                                   # d_final_state may be NULL
+    assert call(d, p, wsb=16) == 4                 # ... then the small workspace is reported
+    p = list(ok)
+    p[12] = 0x1004                                 # dk misaligned
+    assert call(d, p) == 3
+    assert call(d, ok, wsb=nbytes - 1) == 4        # workspace too small
