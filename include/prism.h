@@ -57,6 +57,9 @@ typedef enum { PRISM_F32 = 0, PRISM_BF16 = 1 } prism_dtype;
 
 /* flags */
 #define PRISM_FLAG_NO_GELU 1u   /* ablation: delta^(l) = p^(l) (.) r^(l) (identity activation) */
+#define PRISM_FLAG_VHIST_TOKEN_MAJOR 2u  /* prism_forward_from: v_hist is [B,w,H,d_v], the layout of
+                                            v itself (so the last w token rows of the previous
+                                            segment's v serve directly when B = 1) */
 
 typedef struct {
     int B, T, H;          /* batch, sequence length, heads */

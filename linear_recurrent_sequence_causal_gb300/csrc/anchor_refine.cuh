@@ -77,8 +77,9 @@ __global__ void __launch_bounds__(kThreads, 1) anchor_refine_kernel(K1Args p) {
     const int t = t0 - w + rr;
     float x = 0.f;
     if (t >= 0 && t < len) x = Elem<T>::to_f(v[(((size_t)b * T_ + t) * H + h) * D + c]);
-    else if (t < 0 && p.vhist)
-      x = Elem<T>::to_f(static_cast<const T*>(p.vhist)[(((size_t)b * H + h) * w + (w + t)) * D + c]);
+    else if (t < 0 && p.vhist)                 // [B][H][w][D], or [B][w][H][D] (token-major flag)
+      x = Elem<T>::to_f(static_cast<const T*>(p.vhist)[(p.flags & 2u) ? (((size_t)b * w + (w + t)) * H + h) * D + c
+                                                                     : (((size_t)b * H + h) * w + (w + t)) * D + c]);
     sVw[rr * D + c] = x;
   }
   __syncthreads();

@@ -55,7 +55,8 @@ struct PrepArgs {
   const unsigned char* wblocks;   // fp16 weight blocks laid out for the A operand
   const int* wflag;               // nonzero: weights need their lo halves
   const int* seq_lens;
-  const __nv_bfloat16* vhist;     // [B][H][w][D] v of the w tokens before t = 0 (oldest first), or null
+  const __nv_bfloat16* vhist;     // [B][H][w][D] (or [B][w][H][D] with flag bit 1) v of the w tokens
+                                  // before t = 0 (oldest first), or null
   // Per-chunk outputs, chunk-major [B][H][NC][...].  Inside a chunk each array is
   // stored "piece-major": 16-byte column pieces, rows contiguous within a piece:
   // element (r, f) of an R-row array at ((f / V) * R + r) * V + f % V, V = 16 / elem
@@ -613,10 +614,12 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       *reinterpret_cast<uint4*>(vwin + (r0 + idx / (D / 8)) * D + (idx % (D / 8)) * 8) = make_uint4(0u, 0u, 0u, 0u);
   }
   if (t0 == 0 && p.vhist) {                    // tokens -w .. -1 of a resumed sequence (rows 8-w .. 7)
-    const __nv_bfloat16* hs = p.vhist + ((size_t)b * H + h) * w * D;
-    for (int idx = tid; idx < w * (D / 8); idx += NT)
-      *reinterpret_cast<uint4*>(vwin + (8 - w + idx / (D / 8)) * D + (idx % (D / 8)) * 8) =
-          *reinterpret_cast<const uint4*>(hs + idx * 8);
+    const bool tmaj = p.flags & 2u;
+    for (int idx = tid; idx < w * (D / 8); idx += NT) {
+      const int rr = idx / (D / 8), pc = idx % (D / 8);
+      const __nv_bfloat16* src = p.vhist + (tmaj ? (((size_t)b * w + rr) * H + h) * D : (((size_t)b * H + h) * w + rr) * D) + pc * 8;
+      *reinterpret_cast<uint4*>(vwin + (8 - w + rr) * D + pc * 8) = *reinterpret_cast<const uint4*>(src);
+    }
   }
   csync<NT>();
   const int c = row;

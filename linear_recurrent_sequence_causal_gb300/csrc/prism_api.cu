@@ -126,7 +126,7 @@ int check_dims(const prism_dims* d) {
   if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->d_k <= 0 || d->d_v <= 0 || d->L < 0 ||
       d->conv_width <= 0 || d->chunk <= 0)
     return PRISM_ERR_INVALID_ARG;
-  if (d->flags & ~PRISM_FLAG_NO_GELU) return PRISM_ERR_INVALID_ARG;
+  if (d->flags & ~(PRISM_FLAG_NO_GELU | PRISM_FLAG_VHIST_TOKEN_MAJOR)) return PRISM_ERR_INVALID_ARG;
   if (d->d_k != d->d_v) return PRISM_ERR_UNSUPPORTED;
   const int D = d->d_k, C = d->chunk;
   if (D != 16 && D != 32 && D != 64 && D != 128) return PRISM_ERR_UNSUPPORTED;

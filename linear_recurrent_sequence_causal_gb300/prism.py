@@ -18,6 +18,7 @@ from . import build as _build
 
 PRISM_F32, PRISM_BF16 = 0, 1
 PRISM_FLAG_NO_GELU = 1
+PRISM_FLAG_VHIST_TOKEN_MAJOR = 2
 ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
           3: "PRISM_ERR_MISALIGNED", 4: "PRISM_ERR_WORKSPACE", 5: "PRISM_ERR_LAUNCH",
           6: "PRISM_ERR_CUDA", 7: "PRISM_ERR_SCRATCH_LIMIT"}
@@ -103,10 +104,10 @@ def _dtype_code(t: torch.dtype) -> int:
     raise PrismError(1, f"unsupported I/O dtype {t}")
 
 
-def make_dims(B, T, H, d_k, d_v, conv_width, L, chunk, dtype, no_gelu=False) -> Dims:
+def make_dims(B, T, H, d_k, d_v, conv_width, L, chunk, dtype, no_gelu=False, flags=0) -> Dims:
     return Dims(B=B, T=T, H=H, d_k=d_k, d_v=d_v, conv_width=conv_width, L=L, chunk=chunk,
                 dtype=_dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype),
-                flags=PRISM_FLAG_NO_GELU if no_gelu else 0)
+                flags=(PRISM_FLAG_NO_GELU if no_gelu else 0) | flags)
 
 
 def workspace_bytes(dims: Dims) -> int:
@@ -134,9 +135,9 @@ def workspace_layout(dims: Dims) -> dict:
     return {n: (None if offs[i] == absent else int(offs[i])) for i, n in enumerate(WS_REGIONS)}
 
 
-def _dims_for(q, v, conv_w, L, chunk, no_gelu=False) -> Dims:
+def _dims_for(q, v, conv_w, L, chunk, no_gelu=False, flags=0) -> Dims:
     B, T, H, dk = q.shape
-    return make_dims(B, T, H, dk, v.shape[-1], conv_w.shape[1], L, chunk, q.dtype, no_gelu)
+    return make_dims(B, T, H, dk, v.shape[-1], conv_w.shape[1], L, chunk, q.dtype, no_gelu, flags)
 
 
 def alloc_workspace(dims: Dims, device) -> torch.Tensor:
@@ -170,12 +171,15 @@ def prism_forward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, 
 
 def prism_forward_from(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *,
                        initial_state=None, v_hist=None, out=None, final_state=None,
-                       seq_lens=None, workspace=None, stream=None, no_gelu=False, want_state=True):
+                       seq_lens=None, workspace=None, stream=None, no_gelu=False, want_state=True,
+                       v_hist_token_major=False):
     """prism_forward resuming from ``initial_state`` [B,H,dv,dk] fp32 and ``v_hist``
-    [B,H,w,dv] (I/O dtype; the v rows of the w tokens before t = 0, oldest first)."""
+    [B,H,w,dv] (I/O dtype; the v rows of the w tokens before t = 0, oldest first), or
+    [B,w,H,dv] (the layout of v) with ``v_hist_token_major``."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu)
+    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu,
+                     PRISM_FLAG_VHIST_TOKEN_MAJOR if v_hist_token_major else 0)
     if out is None:
         out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
     if final_state is None and want_state:
@@ -318,3 +322,102 @@ def forward_inputs(inp: dict, L: int, chunk: int, **kw):
     return prism_forward(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"],
                          inp["conv_w"], inp["Wk"], inp["Wp"], inp["wbeta"], L, chunk,
                          seq_lens=inp.get("seq_lens"), **kw)
+
+
+class HostPipeline:
+    """The forward pass from host (pinned) inputs to host outputs, with the copies overlapped
+    with the kernels: the work is cut into pieces (groups of sequences when B > 1; token
+    segments when B = 1, each resumed from the previous segment's final state and its last
+    w v rows with prism_forward_from), copied in on one stream, computed on a second and
+    copied out on a third.  Device buffers, streams and the workspace are kept across calls.
+    """
+
+    def __init__(self, shapes: dict, dtype, L, chunk, *, pieces=8, device="cuda", no_gelu=False,
+                 min_piece_bytes=32 << 20):
+        self.L, self.chunk, self.no_gelu = L, chunk, no_gelu
+        self.dev = torch.device(device)
+        B, T, H, D = shapes["q"]
+        # pieces small enough to overlap, large enough that copies and launches stay efficient
+        moved = B * T * H * D * (3 * torch.tensor([], dtype=dtype).element_size() + 4)
+        if min_piece_bytes > 0:
+            pieces = max(1, min(pieces, moved // min_piece_bytes))
+        self.B, self.T, self.H, self.D = B, T, H, D
+        self.w = shapes["conv_w"][1]
+        self.buf = {n: torch.empty(shp, dtype=(dtype if n in ("q", "k", "v") else torch.float32),
+                                   device=self.dev) for n, shp in shapes.items() if n != "seq_lens"}
+        self.out = torch.empty((B, T, H, D), dtype=torch.float32, device=self.dev)
+        self.states = [torch.empty((B, H, D, D), dtype=torch.float32, device=self.dev) for _ in range(2)]
+        if B > 1:
+            n = min(pieces, B)
+            step = -(-B // n)
+            self.pieces = [(b0, min(b0 + step, B)) for b0 in range(0, B, step)]
+            pdims = make_dims(step, T, H, D, D, self.w, L, chunk, dtype, no_gelu)
+        else:
+            n = max(1, min(pieces, T // max(chunk, self.w)))
+            step = -(-T // n)
+            step = -(-step // chunk) * chunk          # chunk-aligned segments
+            self.pieces = [(t0, min(t0 + step, T)) for t0 in range(0, T, step)]
+            pdims = make_dims(1, step, H, D, D, self.w, L, chunk, dtype, no_gelu, PRISM_FLAG_VHIST_TOKEN_MAJOR)
+        self.ws = alloc_workspace(pdims, self.dev)
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(self.dev) for _ in range(3))
+        self.ev_in = [torch.cuda.Event() for _ in self.pieces]
+        self.ev_comp = [torch.cuda.Event() for _ in self.pieces]
+        self.lens_dev = None                        # one buffer per piece (16-byte aligned)
+
+    def h2d_bytes(self, host: dict) -> int:
+        return sum(t.numel() * t.element_size() for n, t in host.items() if t is not None)
+
+    def run(self, host: dict, host_out, host_fs, stream=None):
+        """host: pinned CPU tensors keyed like ``inputs.generate``; host_out [B,T,H,D] fp32 and
+        host_fs [B,H,D,D] fp32 pinned.  Ordered after ``stream`` (default: current) and
+        finished before later work on it."""
+        caller = stream or torch.cuda.current_stream(self.dev)
+        start = torch.cuda.Event()
+        start.record(caller)
+        for s in (self.s_in, self.s_comp, self.s_out):
+            s.wait_event(start)
+        b = self.buf
+        lens = host.get("seq_lens")
+        with torch.cuda.stream(self.s_in):
+            for n in ("conv_w", "Wk", "Wp", "wbeta"):
+                b[n].copy_(host[n], non_blocking=True)
+            if lens is not None and self.B > 1:
+                if self.lens_dev is None:
+                    self.lens_dev = [torch.empty((a1 - a0,), dtype=torch.int32, device=self.dev)
+                                     for a0, a1 in self.pieces]
+                for (a0, a1), buf in zip(self.pieces, self.lens_dev):
+                    buf.copy_(lens[a0:a1], non_blocking=True)
+        for i, (a0, a1) in enumerate(self.pieces):
+            sl = (slice(a0, a1),) if self.B > 1 else (slice(None), slice(a0, a1))
+            with torch.cuda.stream(self.s_in):
+                for n in ("q", "k", "v", "log_alpha", "beta"):
+                    b[n][sl].copy_(host[n][sl], non_blocking=True)
+                self.ev_in[i].record(self.s_in)
+            self.s_comp.wait_event(self.ev_in[i])
+            with torch.cuda.stream(self.s_comp):
+                if self.B > 1:
+                    lv = self.lens_dev[i] if lens is not None else None
+                    prism_forward(b["q"][sl], b["k"][sl], b["v"][sl], b["log_alpha"][sl], b["beta"][sl],
+                                  b["conv_w"], b["Wk"], b["Wp"], b["wbeta"], self.L, self.chunk,
+                                  out=self.out[sl], final_state=self.states[0][a0:a1], seq_lens=lv,
+                                  workspace=self.ws, stream=self.s_comp, no_gelu=self.no_gelu)
+                else:
+                    if lens is not None:
+                        raise PrismError(1, "HostPipeline: seq_lens with B = 1 is not supported")
+                    hist = b["v"][:, a0 - self.w:a0] if a0 >= self.w else None
+                    prism_forward_from(b["q"][sl], b["k"][sl], b["v"][sl], b["log_alpha"][sl],
+                                       b["beta"][sl], b["conv_w"], b["Wk"], b["Wp"], b["wbeta"],
+                                       self.L, self.chunk,
+                                       initial_state=self.states[i % 2] if i > 0 else None,
+                                       v_hist=hist, v_hist_token_major=True, out=self.out[sl],
+                                       final_state=self.states[(i + 1) % 2], workspace=self.ws,
+                                       stream=self.s_comp, no_gelu=self.no_gelu)
+                self.ev_comp[i].record(self.s_comp)
+            self.s_out.wait_event(self.ev_comp[i])
+            with torch.cuda.stream(self.s_out):
+                host_out[sl].copy_(self.out[sl], non_blocking=True)
+        with torch.cuda.stream(self.s_out):
+            fs = self.states[0] if self.B > 1 else self.states[len(self.pieces) % 2]
+            host_fs.copy_(fs, non_blocking=True)
+        for s in (self.s_in, self.s_comp, self.s_out):
+            caller.wait_stream(s)

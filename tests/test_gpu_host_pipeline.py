@@ -1,0 +1,44 @@
+"""GPU: the host-to-host forward (prism.HostPipeline: copies overlapped with the kernels)
+gives the results of one prism_forward call on the same inputs, and the oracle's."""
+import pytest
+import torch
+
+import oracle
+from linear_recurrent_sequence_causal_gb300 import inputs as I
+from linear_recurrent_sequence_causal_gb300 import prism
+from tests.parity import check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA GPU required for -m gpu tests")
+    prism.load()
+
+
+@pytest.mark.parametrize("B,T,H,D,L,chunk,ragged,pieces", [
+    (6, 300, 2, 64, 2, 64, True, 4),      # groups of sequences
+    (1, 1000, 3, 128, 4, 64, False, 5),   # token segments resumed from the previous state
+    (1, 77, 2, 32, 1, 32, False, 3),
+])
+def test_host_pipeline_equals_one_call(B, T, H, D, L, chunk, ragged, pieces):
+    wl = I.Workload("hp", "bf16", B, T, H, D, D, L, 4, chunk, seed=11 + B + D, ragged=ragged)
+    host = I.generate(wl)
+    pinned = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
+    shapes = {k: tuple(v.shape) for k, v in host.items() if v is not None}
+    pipe = prism.HostPipeline(shapes, torch.bfloat16, L, chunk, pieces=pieces, min_piece_bytes=0)
+    assert len(pipe.pieces) > 1
+    h_out = torch.empty((B, T, H, D), dtype=torch.float32).pin_memory()
+    h_fs = torch.empty((B, H, D, D), dtype=torch.float32).pin_memory()
+    pipe.run(pinned, h_out, h_fs)
+    torch.cuda.synchronize()
+    d = prism.inputs_to_device(host)
+    ref_out, ref_fs = prism.forward_inputs(d, L, chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(h_out, ref_out.cpu()), "outputs differ from one prism_forward call"
+    assert torch.equal(h_fs, ref_fs.cpu()), "final state differs from one prism_forward call"
+    if T <= 300 or B == 1:
+        ro, rs, _ = oracle.forward(host)
+        check(h_out, h_fs, ro, rs, "bf16", seq_lens=host.get("seq_lens"), what="host pipeline")
