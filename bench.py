@@ -13,6 +13,9 @@ of the method) on the host cores, on a bounded sample of the same workload.
 
 ``--backward`` times the backward pass instead (prism_backward: all gradients given
 d_out and d_final_state), with the gradient oracle as its CPU baseline.
+
+``--decode`` times the single-token step (prism_decode_step) for every sequence of the
+workload from a resident state, with the oracle's one-token forward as its CPU baseline.
 """
 from __future__ import annotations
 
@@ -549,6 +552,124 @@ def backward_arm(args, wl, L):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- decode arm
+DEC_METRIC = "PRISM mixer decode tokens/s on 1 GB300 (one token for every sequence, fp32 state)"
+
+
+def dec_algorithmic(wl, L):
+    """Bytes and flops of one decode step (every (b, h) advances one token), d = d_k = d_v,
+    e = I/O bytes: per (b, h) the state read and written (8 d^2), q, k, v in (3 d e), the
+    gates (8), out (4 d), the history read and rewritten (2 w d e); per head the L-step
+    weights once (4 L (2 d^2 + d)) and the taps (4 w d).  Flops per (b, h): the
+    projections 4 L d^2, S k and S q 4 d^2, the rank-(L+2) update 2 (L + 2) d^2."""
+    d, e, w = wl.dk, (4 if wl.dtype == "f32" else 2), wl.w
+    bh = wl.B * wl.H
+    by = bh * (8 * d * d + 3 * d * e + 8 + 4 * d + 2 * w * d * e) + wl.H * 4 * (L * (2 * d * d + d) + w * d)
+    fl = bh * (4 * L * d * d + 4 * d * d + 2 * (L + 2) * d * d)
+    return by, fl
+
+
+def decode_arm(args, wl, L):
+    from linear_recurrent_sequence_causal_gb300 import build, prism
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if build.stale():
+        raise RuntimeError("libprism.so is missing or stale: run __graft_entry__.build() first")
+    prism.load()
+    dev = torch.device("cuda", local)
+    B, H, D, w = wl.B, wl.H, wl.dk, wl.w
+    one = wl.with_(T=1, ragged=False)
+    host = I.generate(one, L=L, seed=wl.seed)
+    g = torch.Generator().manual_seed(wl.seed + 2)
+    h_state = torch.randn((B, H, D, D), generator=g) * 0.1
+    h_hist = torch.randn((B, H, w, D), generator=g).to(wl.torch_dtype)
+    tok = {n: host[n][:, 0].contiguous() for n in ("q", "k", "v", "log_alpha", "beta")}
+    d_tok = {n: t.to(dev) for n, t in tok.items()}
+    par = {n: host[n].to(dev) for n in ("conv_w", "Wk", "Wp", "wbeta")}
+    state, hist = h_state.to(dev), h_hist.to(dev)
+    out = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        prism.prism_decode_step(d_tok["q"], d_tok["k"], d_tok["v"], d_tok["log_alpha"], d_tok["beta"],
+                                par["conv_w"], par["Wk"], par["Wp"], par["wbeta"], L, state, hist, out=out,
+                                stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    steps = max(args.steps, 100)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = a.elapsed_time(b) / steps
+    value = B / (ms / 1e3)
+
+    # end to end: the token's q, k, v and gates from pinned host memory, out back to the host
+    p_tok = {n: t.pin_memory() for n, t in tok.items()}
+    h_out = torch.empty((B, H, D), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in p_tok.values())
+    d2h = h_out.numel() * 4
+
+    def e2e_step():
+        for n, t in p_tok.items():
+            d_tok[n].copy_(t, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a.elapsed_time(b) / steps
+
+    hbm, _, peak_kind = load_peaks()
+    by, fl = dec_algorithmic(wl, L)
+    roof = {"bound": "hbm", "achieved": by / (ms / 1e3) / 1e9, "peak": hbm, "unit": "GB/s", "traffic": None,
+            "kernel": "decode_kernel", "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)",
+            "kernel_ms": ms, "algorithmic_bytes": by, "algorithmic_flops": fl}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    line = {"metric": DEC_METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "B": B, "H": H, "d_k": D, "d_v": D, "L": L, "conv_width": w,
+                       "pass": "decode (one token per sequence)",
+                       "l2": "state larger than L2 (no flush)" if B * H * D * D * 4 > 129e6
+                       else "state smaller than L2 (no flush)"},
+            "roofline": roof, "clocks": clk,
+            "e2e": {"value": B / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": steps}
+    if not args.no_cpu_baseline:
+        import oracle
+        inp1 = dict(host)
+        inp1["seq_lens"] = None
+        s0 = h_state.double().numpy()
+        vh = h_hist.float().double().numpy()
+        threads = os.cpu_count() or 1
+        t0 = time.perf_counter()
+        n = 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 5.0):
+            oracle.forward(inp1, L=L, initial_state=s0, v_hist=vh, threads=threads)
+            n += 1
+        dt = (time.perf_counter() - t0) / n
+        line["cpu_baseline"] = {"value": B / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": f"the fp64 oracle's forward on one token of all {B} x {H} "
+                                          f"sequences from the same state, {n} runs"}
+    print(json.dumps(line), flush=True)
+
+
 def ctypes_byref(x):
     import ctypes
     return ctypes.byref(x)
@@ -565,12 +686,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true")
+    ap.add_argument("--decode", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)     # at least 3 untimed warm-up steps, reported as run
     wl = I.get_workload(args.workload)
     L = wl.L if args.L is None else args.L
     if args.backward:
         backward_arm(args, wl, L)
+    elif args.decode:
+        decode_arm(args, wl, L)
     elif args.impl == "reference":
         reference_arm(args, wl, L)
     else:
