@@ -27,8 +27,16 @@ constexpr int kBwdCK = 16;        // tokens between state checkpoints, kernel B
 constexpr int kBwdLmax = 8;
 constexpr int kBwdThreads = 256;
 
+// Rows-of-S slices per (b, h) in the state kernel: enough CTAs to fill the SMs twice over.
+inline int bwd_pick_rs(long long BH, int D) {
+  if (BH >= 152) return 1;
+  if (BH >= 76) return 2;
+  return D >= 32 ? 4 : 2;
+}
+
 struct BwdArgs {
   int B, T, H, L, w;
+  int rs;                         // rows-of-S slices per (b, h) in the state kernel
   unsigned flags;                 // bit 0: identity in place of GELU
   const void* q;                  // [B][T][H][D] (I/O dtype)
   const void* k;
@@ -63,8 +71,14 @@ struct BwdArgs {
   float* dKH;                     // [n][L][D]  gradient of k_hat^(l)
   float* dZ;                      // [n][L]
   float* dU;                      // [n][D]
-  float* CK;                      // [B][H][ceil(T/kBwdCK)][D][D] states before each block
-  float* SCR;                     // [B][H][kBwdCK][D][D] states of the block being reversed
+  float* CK;                      // [B][H][RS][ceil(T/kBwdCK)][D/RS][D] states before each block
+  float* SCR;                     // [B][H][RS][kBwdCK][D/RS][D] states of the block being reversed
+  // per-slice partial column sums when the state kernel splits rows over RS CTAs
+  float* PQ;                      // [RS][n][D]
+  float* PK;                      // [RS][n][D]
+  float* PKL;                     // [RS][n][L][D]
+  float* PB;                      // [RS][n]
+  float* PA;                      // [RS][n]
 };
 
 __device__ __forceinline__ int bwd_len(const BwdArgs& p, int b) {
@@ -228,42 +242,60 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_refine_fwd_kernel(BwdArgs p) 
 // 4 D threads).  Row mapping: thread (r = tid / 4, cq = tid % 4) owns columns cq + 4 i of
 // row r; column mapping: thread (c = tid % D, rq = tid / D) owns rows rq D/4 + i of column c.
 
-template <int D>
+// RS CTAs share a (b, h): each owns R = D / RS rows of S and dS (rows evolve independently)
+// and writes its part of the column sums (dq, dk, dk^(l), dbeta, dlog_alpha) to per-slice
+// partial arrays, which bwd_state_reduce adds in slice order (RS = 1 writes them directly).
+template <int D, int RS>
 struct BwdBSmem {
+  static constexpr int R = D / RS;                                  // rows of S in this CTA
   static constexpr int LDS = D + 4;                                 // 16-byte rows, no bank conflicts
-  static constexpr int NT = 4 * D, NW = NT / 32;
+  static constexpr int NT = 4 * R, NW = NT / 32;
+  static constexpr int NGRP = NT / D;                               // row groups of the column mapping
+  static constexpr int RPG = R / NGRP;                              // rows per group (= D / 4)
   static constexpr int TOKF = (4 + 2 * kBwdLmax) * D + 2;           // floats of one token's vectors
-  static constexpr int PF = (TOKF + NT - 1) / NT;                   // of them per thread
-  static constexpr size_t oDS = 0;                                  // dS [D][D+4]
-  static constexpr size_t oS = oDS + 4u * D * LDS;                  // S  [D][D+4]
-  static constexpr size_t oVec = oS + 4u * D * LDS;                 // k | v | do | q | k^(l) | D^(l) | la, beta
-  static constexpr size_t oY = oVec + 4u * ((TOKF + 3) / 4 * 4);    // y [D]
-  static constexpr size_t oZS = oY + 4u * D;                        // S_(t-1) k_t of the block [CK][D]
-  static constexpr size_t oPart = oZS + 4u * kBwdCK * D;            // column partial sums [4][3 + Lmax][D]
-  static constexpr size_t oRed = oPart + 4u * 4 * (3 + kBwdLmax) * D;   // scalar partials [NW][16]
-  static constexpr size_t bytes = oRed + 4u * NW * 16;
+  static constexpr size_t oDS = 0;                                  // dS [R][D+4]
+  static constexpr size_t oS = oDS + 4u * R * LDS;                  // S  [R][D+4]
+  static constexpr size_t oVec = oS + 4u * R * LDS;                 // k | v | do | q | k^(l) | D^(l) | la, beta
+  static constexpr size_t oY = oVec + 4u * ((TOKF + 3) / 4 * 4);    // y [R]
+  static constexpr size_t oZS = oY + 4u * R;                        // S_(t-1) k_t of the block [CK][R]
+  static constexpr size_t oPart = oZS + 4u * kBwdCK * R;            // column partial sums [NGRP][3 + Lmax][D]
+  static constexpr size_t oRed = oPart + 4u * NGRP * (3 + kBwdLmax) * D;   // scalar partials [NW][16]
+  static constexpr size_t oRing = (oRed + 4u * NW * 16 + 15) / 16 * 16;     // raw token vectors [NSTAGE]
+  static constexpr int NSTAGE = 4;                                  // tokens in flight
+  // raw bytes of one token's vectors at L steps (k, v, q in the I/O type, do, k^(l), D^(l), gates)
+  static __host__ __device__ constexpr size_t tok_bytes(int L, int esz) {
+    return (size_t)3 * D * esz + 4u * D + 8u * L * D + 16;
+  }
+  static __host__ __device__ constexpr size_t bytes(int L, int esz) { return oRing + NSTAGE * tok_bytes(L, esz); }
+  static_assert(NT >= D && NT % D == 0 && NT % 32 == 0, "row slice too small");
 };
 
 __device__ __forceinline__ void bwd_cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+__device__ __forceinline__ void bwd_cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
 __device__ __forceinline__ void bwd_cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bwd_cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bwd_cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
-template <int D>
+template <int D, int RS>
 __device__ __forceinline__ void bwd_state_load_async(float* sS, const float* g) {
-  using S = BwdBSmem<D>;
-  for (int idx = threadIdx.x; idx < D * D / 4; idx += S::NT) {
+  using S = BwdBSmem<D, RS>;
+  for (int idx = threadIdx.x; idx < S::R * D / 4; idx += S::NT) {
     const int r = (idx * 4) / D, c = (idx * 4) % D;
     bwd_cp_async16(sS + r * S::LDS + c, g + (size_t)idx * 4);
   }
   bwd_cp_async_commit();
 }
 
-template <class T, int D>
-__global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
-  using S = BwdBSmem<D>;
-  constexpr int LDS = S::LDS, NT = S::NT, NW = S::NW, CPT = D / 4, PF = S::PF;
+template <class T, int D, int RS>
+__global__ void __launch_bounds__(4 * (D / RS)) bwd_state_kernel(BwdArgs p) {
+  using S = BwdBSmem<D, RS>;
+  constexpr int R = S::R, LDS = S::LDS, NT = S::NT, NW = S::NW, CPT = D / 4;
+  constexpr int RPG = S::RPG;
   constexpr int NSLOT = 3 + kBwdLmax;
   extern __shared__ __align__(1024) unsigned char sm[];
   float* sDS = reinterpret_cast<float*>(sm + S::oDS);
@@ -275,18 +307,25 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
   float* sRed = reinterpret_cast<float*>(sm + S::oRed);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = tid >> 2, cq = tid & 3;              // row mapping
-  const int cc = tid % D, rq = tid / D;              // column mapping
-  const int h = blockIdx.x, b = blockIdx.y;
+  const int r = tid >> 2, cq = tid & 3;              // row mapping (local row r of the slice)
+  const int cc = tid % D, rq = tid / D;              // column mapping (row group rq)
+  const int h = blockIdx.x, b = blockIdx.y, slice = blockIdx.z;
+  const int r0 = slice * R;                          // first row of S owned here
   const int H = p.H, T_ = p.T, L = p.L;
   const int len = bwd_len(p, b);
   const int NCK = (T_ + kBwdCK - 1) / kBwdCK;
-  const int TOK = (4 + 2 * L) * D + 2;               // floats of a token's vectors at this L
+  const size_t NTH = (size_t)p.B * T_ * H;
   const T* qg = static_cast<const T*>(p.q);
   const T* kg = static_cast<const T*>(p.k);
   const T* vg = static_cast<const T*>(p.v);
-  float* ck = p.CK + ((size_t)b * H + h) * NCK * D * D;
-  float* scr = p.SCR + ((size_t)b * H + h) * kBwdCK * D * D;
+  float* ck = p.CK + (((size_t)b * H + h) * RS + slice) * NCK * R * D;
+  float* scr = p.SCR + (((size_t)b * H + h) * RS + slice) * kBwdCK * R * D;
+  // column-sum outputs: the final arrays (RS = 1) or this slice's partial arrays
+  float* oq = RS > 1 ? p.PQ + slice * NTH * D : p.dq;
+  float* ok_ = RS > 1 ? p.PK + slice * NTH * D : p.dk;
+  float* okl = RS > 1 ? p.PKL + slice * NTH * L * D : p.dKL;
+  float* ob = RS > 1 ? p.PB + slice * NTH : p.dbeta;
+  float* oa = RS > 1 ? p.PA + slice * NTH : p.dla;
   float* sk = svec;
   float* sv = svec + D;
   float* sdo = svec + 2 * D;
@@ -296,69 +335,101 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
   const float* sgate = sdl + L * D;                  // log alpha, beta
   auto tok = [&](int t) { return ((size_t)b * T_ + t) * H + h; };
 
-  // padding tokens: every per-token gradient is zero
+  // padding tokens: every per-token gradient is zero (this slice's rows and partials)
   for (int t = len; t < T_; ++t) {
     const size_t n = tok(t);
     for (int idx = tid; idx < D; idx += NT) {
-      p.dq[n * D + idx] = 0.f;
-      p.dk[n * D + idx] = 0.f;
-      p.dv[n * D + idx] = 0.f;
+      oq[n * D + idx] = 0.f;
+      ok_[n * D + idx] = 0.f;
     }
-    for (int idx = tid; idx < L * D; idx += NT) {
-      p.dDL[n * L * D + idx] = 0.f;
-      p.dKL[n * L * D + idx] = 0.f;
-    }
+    for (int idx = tid; idx < R; idx += NT) p.dv[n * D + r0 + idx] = 0.f;
+    for (int idx = tid; idx < L * D; idx += NT) okl[n * L * D + idx] = 0.f;
+    for (int idx = tid; idx < L * R; idx += NT) p.dDL[(n * L + idx / R) * D + r0 + idx % R] = 0.f;
     if (tid == 0) {
-      p.dla[n] = 0.f;
-      p.dbeta[n] = 0.f;
+      oa[n] = 0.f;
+      ob[n] = 0.f;
     }
   }
   if (len <= 0) return;
 
-  // A token's vectors are fetched into registers one token ahead (the loads overlap the
-  // current token's work) and committed to shared memory at the next token's start.
-  float pf[PF];
-  auto fetch = [&](int t) {
-    const size_t n = tok(t);
-#pragma unroll
-    for (int j = 0; j < PF; ++j) {
-      int e = tid + j * NT;
-      float x = 0.f;
-      if (e < TOK) {
-        if (e < D) x = Elem<T>::to_f(kg[n * D + e]);
-        else if ((e -= D) < D) x = Elem<T>::to_f(vg[n * D + e]);
-        else if ((e -= D) < D) x = p.d_out[n * D + e];
-        else if ((e -= D) < D) x = Elem<T>::to_f(qg[n * D + e]);
-        else if ((e -= D) < L * D) x = p.KL[n * L * D + e];
-        else if ((e -= L * D) < L * D) x = p.DL[n * L * D + e];
-        else x = (e - L * D == 0) ? p.log_alpha[n] : p.beta[n];
+  // A token's vectors stream through a ring of NSTAGE raw buffers (cp.async, one group per
+  // token, issued NSTAGE - 1 tokens ahead so the loads' latency overlaps the work) and are
+  // converted to fp32 vectors in svec when the token's turn comes.
+  constexpr int NSTAGE = S::NSTAGE;
+  constexpr int ESZ = sizeof(T);
+  const size_t TB = S::tok_bytes(L, ESZ);
+  unsigned char* ring = sm + S::oRing;
+  const int nk16 = D * ESZ / 16, nf16 = D / 4, nl16 = L * D / 4;   // 16-byte pieces per vector
+  auto issue = [&](int t, bool valid) {          // token t into stage t % NSTAGE (empty if !valid)
+    if (valid) {
+      unsigned char* st = ring + (size_t)(t % NSTAGE) * TB;
+      const size_t n = tok(t);
+      const int total = 3 * nk16 + nf16 + 2 * nl16;
+      for (int i = tid; i < total; i += NT) {
+        int j = i;
+        const void* src;
+        if (j < nk16) src = kg + n * D + j * (16 / ESZ);
+        else if ((j -= nk16) < nk16) src = vg + n * D + j * (16 / ESZ);
+        else if ((j -= nk16) < nk16) src = qg + n * D + j * (16 / ESZ);
+        else if ((j -= nk16) < nf16) src = p.d_out + n * D + j * 4;
+        else if ((j -= nf16) < nl16) src = p.KL + n * L * D + j * 4;
+        else src = p.DL + n * L * D + (j - nl16) * 4;
+        bwd_cp_async16(st + (size_t)i * 16, src);
       }
-      pf[j] = x;
+      if (tid == 0) {
+        bwd_cp_async4(st + TB - 16, p.log_alpha + n);
+        bwd_cp_async4(st + TB - 12, p.beta + n);
+      }
     }
+    bwd_cp_async_commit();
   };
-  auto commit = [&]() {
-#pragma unroll
-    for (int j = 0; j < PF; ++j)
-      if (tid + j * NT < TOK) svec[tid + j * NT] = pf[j];
+  auto convert = [&](int t) {                    // stage of token t -> svec (k | v | do | q | k^(l) | D^(l) | gates)
+    const unsigned char* st = ring + (size_t)(t % NSTAGE) * TB;
+    const T* rk = reinterpret_cast<const T*>(st);
+    const T* rv = rk + D;
+    const T* rqq = rv + D;
+    const float* rf = reinterpret_cast<const float*>(st + 3 * D * ESZ);   // do | k^(l) | D^(l)
+    for (int i = tid; i < D; i += NT) {
+      sk[i] = Elem<T>::to_f(rk[i]);
+      sv[i] = Elem<T>::to_f(rv[i]);
+      sq[i] = Elem<T>::to_f(rqq[i]);
+      sdo[i] = rf[i];
+    }
+    for (int i = tid; i < 2 * L * D; i += NT) skl[i] = rf[D + i];     // k^(l) then D^(l): contiguous
+    if (tid < 2) svec[(4 + 2 * L) * D + tid] = reinterpret_cast<const float*>(st + TB - 16)[tid];
   };
   // z_r = S[r] . k (row mapping; every thread of the row gets it)
   auto row_dot_k = [&]() {
-    float z = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < CPT; ++i) z = fmaf(sS[r * LDS + cq + 4 * i], sk[cq + 4 * i], z);
+    float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;      // four independent chains
+#pragma unroll
+    for (int i = 0; i < CPT; i += 4) {
+      z0 = fmaf(sS[r * LDS + cq + 4 * i], sk[cq + 4 * i], z0);
+      if (i + 1 < CPT) z1 = fmaf(sS[r * LDS + cq + 4 * (i + 1)], sk[cq + 4 * (i + 1)], z1);
+      if (i + 2 < CPT) z2 = fmaf(sS[r * LDS + cq + 4 * (i + 2)], sk[cq + 4 * (i + 2)], z2);
+      if (i + 3 < CPT) z3 = fmaf(sS[r * LDS + cq + 4 * (i + 3)], sk[cq + 4 * (i + 3)], z3);
+    }
+    float z = (z0 + z1) + (z2 + z3);
     z += __shfl_xor_sync(0xffffffffu, z, 1);
     z += __shfl_xor_sync(0xffffffffu, z, 2);
     return z;
   };
   // S <- alpha (S - beta z k^T) + beta v k^T + sum_l D^(l) k^(l)^T on this thread's elements
   // (rows of S evolve independently: no barrier between tokens)
+  // (the row's coefficients in registers: alpha, beta v - alpha beta z, D^(l)[r])
   auto row_update = [&](float z) {
     const float al = expf(sgate[0]), be = sgate[1];
+    const int gr = r0 + r;
+    const float a0 = be * sv[gr] - al * be * z;
+    float al_[kBwdLmax];
+#pragma unroll
+    for (int l = 0; l < kBwdLmax; ++l) al_[l] = l < L ? sdl[l * D + gr] : 0.f;
 #pragma unroll 4
     for (int i = 0; i < CPT; ++i) {
       const int c = cq + 4 * i;
-      float x = al * (sS[r * LDS + c] - be * z * sk[c]) + be * sv[r] * sk[c];
-      for (int l = 0; l < L; ++l) x = fmaf(sdl[l * D + r], skl[l * D + c], x);
+      float x = fmaf(al, sS[r * LDS + c], a0 * sk[c]);
+#pragma unroll
+      for (int l = 0; l < kBwdLmax; ++l)
+        if (l < L) x = fmaf(al_[l], skl[l * D + c], x);
       sS[r * LDS + c] = x;
     }
   };
@@ -368,57 +439,64 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
   };
 
   // ---- forward: checkpoints (the state before tokens 0, CK, 2 CK, ...) ----
-  for (int idx = tid; idx < D * LDS; idx += NT) sS[idx] = 0.f;
+  for (int idx = tid; idx < R * LDS; idx += NT) sS[idx] = 0.f;
   __syncthreads();
   row_store(ck);
-  fetch(0);
+  for (int j = 0; j < NSTAGE - 1; ++j) issue(j, j < len);
   for (int t = 0; t < len; ++t) {
+    issue(t + NSTAGE - 1, t + NSTAGE - 1 < len);
+    bwd_cp_async_wait<NSTAGE - 1>();
     __syncthreads();
-    commit();
+    convert(t);
     __syncthreads();
-    if (t + 1 < len) fetch(t + 1);
     row_update(row_dot_k());
-    if ((t + 1) % kBwdCK == 0 && t + 1 < len) row_store(ck + (size_t)((t + 1) / kBwdCK) * D * D);
+    if ((t + 1) % kBwdCK == 0 && t + 1 < len) row_store(ck + (size_t)((t + 1) / kBwdCK) * R * D);
   }
 
   // ---- backward ----
-  for (int idx = tid; idx < D * LDS; idx += NT) {
+  for (int idx = tid; idx < R * LDS; idx += NT) {
     const int rr = idx / LDS, c = idx % LDS;
-    sDS[idx] = (p.d_fs && c < D) ? p.d_fs[(((size_t)b * H + h) * D + rr) * D + c] : 0.f;
+    sDS[idx] = (p.d_fs && c < D) ? p.d_fs[(((size_t)b * H + h) * D + r0 + rr) * D + c] : 0.f;
   }
   const int nblk = (len + kBwdCK - 1) / kBwdCK;
   for (int blk = nblk - 1; blk >= 0; --blk) {
     const int c0 = blk * kBwdCK, c1 = min(c0 + kBwdCK, len);
     __syncthreads();
-    bwd_state_load_async<D>(sS, ck + (size_t)blk * D * D);
+    bwd_state_load_async<D, RS>(sS, ck + (size_t)blk * R * D);
     bwd_cp_async_wait_all();
-    fetch(c0);
+    for (int j = 0; j < NSTAGE - 1; ++j) issue(c0 + j, c0 + j < c1);
     // recompute the block: z_t = S_(t-1) k_t, and the states after tokens c0 .. c1-2
     for (int t = c0; t < c1; ++t) {
+      issue(t + NSTAGE - 1, t + NSTAGE - 1 < c1);
+      bwd_cp_async_wait<NSTAGE - 1>();
       __syncthreads();
-      commit();
+      convert(t);
       __syncthreads();
-      if (t + 1 < c1) fetch(t + 1);
       const float z = row_dot_k();
-      if (cq == 0) sZS[(t - c0) * D + r] = z;
+      if (cq == 0) sZS[(t - c0) * R + r] = z;
       if (t < c1 - 1) {
         row_update(z);
-        row_store(scr + (size_t)(t - c0) * D * D);
+        row_store(scr + (size_t)(t - c0) * R * D);
       }
     }
-    // reverse through the block
-    fetch(c1 - 1);
+    // reverse through the block (tokens in decreasing order through the same ring)
+    bwd_cp_async_wait<0>();
+    __syncthreads();
+    for (int j = 0; j < NSTAGE - 1; ++j) issue(c1 - 1 - j, c1 - 1 - j >= c0);
     for (int t = c1 - 1; t >= c0; --t) {
       __syncthreads();                                 // previous token done with the buffers
-      commit();
-      bwd_state_load_async<D>(sS, t > c0 ? scr + (size_t)(t - 1 - c0) * D * D : ck + (size_t)blk * D * D);
+      bwd_state_load_async<D, RS>(sS, t > c0 ? scr + (size_t)(t - 1 - c0) * R * D : ck + (size_t)blk * R * D);
+      issue(t - (NSTAGE - 1), t - (NSTAGE - 1) >= c0);
+      bwd_cp_async_wait<2>();                          // token t's vectors (older groups) landed
       __syncthreads();
-      if (t - 1 >= c0) fetch(t - 1);
+      convert(t);
+      __syncthreads();
       const size_t n = tok(t);
       const float al = expf(sgate[0]), be = sgate[1];
-      const float* zs = sZS + (t - c0) * D;
+      const float* zs = sZS + (t - c0) * R;
       // phase 1 (rows): dS += do q^T; y = dS k; y_l = dS k^(l)
-      const float dor = sdo[r];
+      const int gr = r0 + r;
+      const float dor = sdo[gr];
       float y = 0.f;
 #pragma unroll 4
       for (int i = 0; i < CPT; ++i) {
@@ -436,13 +514,13 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
         for (int i = 0; i < CPT; ++i) yl = fmaf(sDS[r * LDS + cq + 4 * i], skl[l * D + cq + 4 * i], yl);
         yl += __shfl_xor_sync(0xffffffffu, yl, 1);
         yl += __shfl_xor_sync(0xffffffffu, yl, 2);
-        if (own) p.dDL[(n * L + l) * D + r] = yl;
-        const float s = warp_sum(own ? sdl[l * D + r] * dor : 0.f);   // D^(l) . do
+        if (own) p.dDL[(n * L + l) * D + gr] = yl;
+        const float s = warp_sum(own ? sdl[l * D + gr] * dor : 0.f);   // D^(l) . do over these rows
         if (lane == 0) sRed[warp * 16 + 4 + l] = s;
       }
       {
-        // per-row scalars summed over rows: v.y, z.y, z.do, v.do
-        const float zr = zs[r], vr = sv[r];
+        // per-row scalars summed over this slice's rows: v.y, z.y, z.do, v.do
+        const float zr = zs[r], vr = sv[gr];
         const float s0 = warp_sum(own ? vr * y : 0.f);
         const float s1 = warp_sum(own ? zr * y : 0.f);
         const float s2 = warp_sum(own ? zr * dor : 0.f);
@@ -455,19 +533,19 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
         }
         if (own) {
           sy[r] = y;
-          p.dv[n * D + r] = be * y;
+          p.dv[n * D + gr] = be * y;
         }
       }
-      bwd_cp_async_wait_all();
+      bwd_cp_async_wait<1>();                          // S_(t-1) landed (only the newest prefetch may pend)
       __syncthreads();
-      // phase 2 (columns): dS^T D^(l); S_(t-1)^T y, S_(t-1)^T do, dS^T (beta v - alpha beta z),
-      // <S_(t-1), dS>; then dS <- alpha (dS - beta y k^T)
+      // phase 2 (columns, this slice's rows): dS^T D^(l); S_(t-1)^T y, S_(t-1)^T do,
+      // dS^T (beta v - alpha beta z), <S_(t-1), dS>; then dS <- alpha (dS - beta y k^T)
       for (int l = 0; l < L; ++l) {
         float f = 0.f;
 #pragma unroll 4
-        for (int i = 0; i < CPT; ++i) {
-          const int rr = rq * CPT + i;
-          f = fmaf(sDS[rr * LDS + cc], sdl[l * D + rr], f);
+        for (int i = 0; i < RPG; ++i) {
+          const int rr = rq * RPG + i;
+          f = fmaf(sDS[rr * LDS + cc], sdl[l * D + r0 + rr], f);
         }
         sPart[(rq * NSLOT + 3 + l) * D + cc] = f;
       }
@@ -475,12 +553,12 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
         float bS = 0.f, e = 0.f, a = 0.f, fro = 0.f;
         const float kc = sk[cc];
 #pragma unroll 4
-        for (int i = 0; i < CPT; ++i) {
-          const int rr = rq * CPT + i;
+        for (int i = 0; i < RPG; ++i) {
+          const int rr = rq * RPG + i;
           const float s = sS[rr * LDS + cc], ds = sDS[rr * LDS + cc], yr = sy[rr];
           bS = fmaf(s, yr, bS);
-          a = fmaf(s, sdo[rr], a);
-          e = fmaf(ds, be * (sv[rr] - al * zs[rr]), e);
+          a = fmaf(s, sdo[r0 + rr], a);
+          e = fmaf(ds, be * (sv[r0 + rr] - al * zs[rr]), e);
           fro = fmaf(s, ds, fro);
           sDS[rr * LDS + cc] = al * (ds - be * yr * kc);
         }
@@ -491,12 +569,12 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
         if (lane == 0) sRed[warp * 16 + 15] = fro;
       }
       __syncthreads();
-      // phase 3: per-token gradients
+      // phase 3: this slice's part of the per-token gradients
       if (tid < D) {
         const int c = tid;
         float t0s = 0.f, t1s = 0.f, t2s = 0.f, zd = 0.f, vd = 0.f;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < S::NGRP; ++q4) {
           t0s += sPart[(q4 * NSLOT + 0) * D + c];
           t1s += sPart[(q4 * NSLOT + 1) * D + c];
           t2s += sPart[(q4 * NSLOT + 2) * D + c];
@@ -505,17 +583,17 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
           zd += sRed[wv * 16 + 2];
           vd += sRed[wv * 16 + 3];
         }
-        p.dk[n * D + c] = t1s - al * be * t0s;
+        ok_[n * D + c] = t1s - al * be * t0s;
         float dqc = al * (t2s - be * zd * sk[c]) + be * vd * sk[c];
         for (int l = 0; l < L; ++l) {
           float ddl = 0.f, tl = 0.f;
           for (int wv = 0; wv < NW; ++wv) ddl += sRed[wv * 16 + 4 + l];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) tl += sPart[(q4 * NSLOT + 3 + l) * D + c];
+          for (int q4 = 0; q4 < S::NGRP; ++q4) tl += sPart[(q4 * NSLOT + 3 + l) * D + c];
           dqc = fmaf(ddl, skl[l * D + c], dqc);
-          p.dKL[(n * L + l) * D + c] = tl;
+          okl[(n * L + l) * D + c] = tl;
         }
-        p.dq[n * D + c] = dqc;
+        oq[n * D + c] = dqc;
         if (c == 0) {
           float vy = 0.f, zy = 0.f, fr = 0.f;
           for (int wv = 0; wv < NW; ++wv) {
@@ -523,10 +601,42 @@ __global__ void __launch_bounds__(4 * D) bwd_state_kernel(BwdArgs p) {
             zy += sRed[wv * 16 + 1];
             fr += sRed[wv * 16 + 15];
           }
-          p.dbeta[n] = vy - al * zy;
-          p.dla[n] = al * (fr - be * zy);
+          ob[n] = vy - al * zy;
+          oa[n] = al * (fr - be * zy);
         }
       }
+    }
+  }
+  bwd_cp_async_wait<0>();
+}
+
+// Sum of the RS slices' partial column sums, in slice order.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads) bwd_state_reduce_kernel(BwdArgs p, int RS) {
+  const size_t NTH = (size_t)p.B * p.T * p.H;
+  const int L = p.L;
+  const size_t per = (size_t)(2 + L) * D + 2;        // outputs per token-head
+  for (size_t idx = (size_t)blockIdx.x * kBwdThreads + threadIdx.x; idx < NTH * per;
+       idx += (size_t)gridDim.x * kBwdThreads) {
+    const size_t n = idx / per;
+    const int j = (int)(idx % per);
+    float s = 0.f;
+    if (j < D) {
+      for (int r = 0; r < RS; ++r) s += p.PQ[(r * NTH + n) * D + j];
+      p.dq[n * D + j] = s;
+    } else if (j < 2 * D) {
+      for (int r = 0; r < RS; ++r) s += p.PK[(r * NTH + n) * D + j - D];
+      p.dk[n * D + j - D] = s;
+    } else if (j < (2 + L) * D) {
+      const int e = j - 2 * D;
+      for (int r = 0; r < RS; ++r) s += p.PKL[(r * NTH + n) * L * D + e];
+      p.dKL[n * L * D + e] = s;
+    } else if (j == (2 + L) * D) {
+      for (int r = 0; r < RS; ++r) s += p.PB[r * NTH + n];
+      p.dbeta[n] = s;
+    } else {
+      for (int r = 0; r < RS; ++r) s += p.PA[r * NTH + n];
+      p.dla[n] = s;
     }
   }
 }

@@ -5,6 +5,17 @@
 
 namespace prism {
 
+template <class T, int D, int RS>
+cudaError_t launch_state(const BwdArgs& a, cudaStream_t s) {
+  using S = BwdBSmem<D, RS>;
+  auto fn = bwd_state_kernel<T, D, RS>;
+  const size_t bytes = S::bytes(a.L, (int)sizeof(T));
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  fn<<<dim3(a.H, a.B, RS), S::NT, bytes, s>>>(a);
+  return cudaGetLastError();
+}
+
 template <class T, int D>
 cudaError_t launch_backward_t(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e;
@@ -16,11 +27,17 @@ cudaError_t launch_backward_t(const BwdArgs& a, cudaStream_t s) {
     fn<<<dim3((a.T + kBwdTT - 1) / kBwdTT, a.H, a.B), kBwdThreads, BwdASmem<D>::bytes, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  {
-    auto fn = bwd_state_kernel<T, D>;
-    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)BwdBSmem<D>::bytes)) != cudaSuccess)
-      return e;
-    fn<<<dim3(a.H, a.B), 4 * D, BwdBSmem<D>::bytes, s>>>(a);
+  switch (a.rs) {
+    case 1: e = launch_state<T, D, 1>(a, s); break;
+    case 2: e = launch_state<T, D, 2>(a, s); break;
+    case 4: e = (D >= 32) ? launch_state<T, D, (D >= 32 ? 4 : 2)>(a, s) : cudaErrorInvalidValue; break;
+    default: e = cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  if (a.rs > 1) {
+    const size_t total = (size_t)a.B * a.T * a.H * ((2 + L) * D + 2);
+    const size_t blocks = (total + kBwdThreads - 1) / kBwdThreads;
+    bwd_state_reduce_kernel<D><<<(unsigned)(blocks < 4864 ? blocks : 4864), kBwdThreads, 0, s>>>(a, a.rs);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {

@@ -427,7 +427,8 @@ namespace {
 // Backward-pass workspace: per token-head factors, then the state checkpoints and the
 // block scratch.  Offsets in floats of each region, 256-byte aligned.
 struct BwdLayout {
-  size_t U, KL, DL, P, NRM, Z, dDL, dKL, dKH, dZ, dU, CK, SCR, total;
+  size_t U, KL, DL, P, NRM, Z, dDL, dKL, dKH, dZ, dU, CK, SCR, PQ, PK, PKL, PB, PA, total;
+  int rs;
 };
 
 BwdLayout bwd_layout(const prism_dims* d) {
@@ -453,6 +454,13 @@ BwdLayout bwd_layout(const prism_dims* d) {
   Lo.dU = take(NTH * D);
   Lo.CK = take((size_t)d->B * d->H * NCK * D * D);
   Lo.SCR = take((size_t)d->B * d->H * prism::kBwdCK * D * D);
+  Lo.rs = prism::bwd_pick_rs((long long)d->B * d->H, (int)D);
+  const size_t RSp = Lo.rs > 1 ? (size_t)Lo.rs : 0;   // partial sums only when rows are split
+  Lo.PQ = take(RSp * NTH * D);
+  Lo.PK = take(RSp * NTH * D);
+  Lo.PKL = take(RSp * NTH * L * D);
+  Lo.PB = take(RSp * NTH);
+  Lo.PA = take(RSp * NTH);
   Lo.total = cur * 4;
   return Lo;
 }
@@ -512,6 +520,8 @@ extern "C" PRISM_API int prism_backward(const prism_dims* dims, const void* q, c
   a.U = ws + Lo.U; a.KL = ws + Lo.KL; a.DL = ws + Lo.DL; a.P = ws + Lo.P; a.NRM = ws + Lo.NRM;
   a.Z = ws + Lo.Z; a.dDL = ws + Lo.dDL; a.dKL = ws + Lo.dKL; a.dKH = ws + Lo.dKH; a.dZ = ws + Lo.dZ;
   a.dU = ws + Lo.dU; a.CK = ws + Lo.CK; a.SCR = ws + Lo.SCR;
+  a.rs = Lo.rs;
+  a.PQ = ws + Lo.PQ; a.PK = ws + Lo.PK; a.PKL = ws + Lo.PKL; a.PB = ws + Lo.PB; a.PA = ws + Lo.PA;
   return prism::launch_backward(dims->dtype == PRISM_F32 ? 0 : 1, dims->d_k, a,
                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PRISM_OK

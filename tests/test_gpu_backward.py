@@ -59,6 +59,8 @@ CASES = [
     ("bf16", 128, 2, 40, 1, 2, 4, False, False, True),
     ("f32", 64, 4, 21, 2, 1, 8, True, False, False),
     ("bf16", 128, 1, 17, 1, 1, 1, False, False, False),
+    ("bf16", 16, 1, 20, 20, 8, 4, True, False, True),     # 160 sequences: one CTA per (b, h)
+    ("f32", 32, 2, 24, 10, 10, 3, False, False, True),    # 100 sequences: two row slices
 ]
 
 
