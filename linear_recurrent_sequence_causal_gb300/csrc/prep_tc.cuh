@@ -590,24 +590,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   } else {
   // ================= consumers =================
   ok = tc::bar_wait(bar_in, 0);
-  // [K ; Q] rows as fp16: (row, a) at (a/8)*2048 + row*16 + (a%8)*2; rows of tokens past
-  // the sequence end and rows >= 2C zero.  v rows past the sequence end are cleared too.
-  // (the piece index is rotated by the row so that eight consecutive lanes read eight
-  //  different bank groups of the raw rows and write eight different ones of the tile)
-  for (int idx = tid; idx < 128 * (D / 8); idx += NT) {
-    const int r = idx % 128, a8 = (idx / 128 + r) % (D / 8);
-    const int t = r < C ? r : r - C;
-    uint4 o = make_uint4(0u, 0u, 0u, 0u);
-    if (r < 2 * C && t < nv) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(kqraw + r * D + a8 * 8);
-      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
-      float f[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
-      o = tc::cvt8(f);
-    }
-    *reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u) = o;
-  }
+  // v rows past the sequence end are cleared.
   if (t0 + C > len) {
     const int r0 = len - (t0 - 8);             // first v-window row past the end (>= 9)
     for (int idx = tid; idx < (C + 8 - r0) * (D / 8); idx += NT)
@@ -624,20 +607,6 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   csync<NT>();
   const int c = row;
   const bool fwarp = quarter < NQ;             // warp holds feature rows
-
-  // Decay mask of this thread's token row for the score tiles (fixed for the
-  // chunk): rows < C strictly causal (G, A), rows C..2C-1 inclusive (P).
-  float gm[NTH];
-  {
-    const bool isG = row < C, isP = row >= C && row < 2 * C;
-    const int t = isG ? row : row - C;
-    const float gt = (isG || isP) ? sg[t] : 0.f;
-#pragma unroll
-    for (int jj = 0; jj < NTH; ++jj) {
-      const int s_ = tb0 + jj;
-      gm[jj] = ((isG && t > s_) || (isP && t >= s_)) ? __expf(gt - sg[s_]) : 0.f;
-    }
-  }
 
   // ---- anchor u = sum_j c_j (.) v_{t-j} (the U tile, hi + lo) and residual r = v - u
   //      (registers); thread (feature c, column group) owns tokens tb0 .. tb0+NTH-1 ----
@@ -678,6 +647,41 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   __syncwarp();
   if (lane == 0) tc::bar_arrive(bar_u);
   csync<NT>();
+  // [K ; Q] rows as fp16: (row, a) at (a/8)*2048 + row*16 + (a%8)*2; rows of tokens past
+  // the sequence end and rows >= 2C zero.  This and the decay mask run while the first
+  // projection is on the tensor core (nothing before the scores of step 0 reads them).
+  // (the piece index is rotated by the row so that eight consecutive lanes read eight
+  //  different bank groups of the raw rows and write eight different ones of the tile)
+  for (int idx = tid; idx < 128 * (D / 8); idx += NT) {
+    const int r = idx % 128, a8 = (idx / 128 + r) % (D / 8);
+    const int t = r < C ? r : r - C;
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (r < 2 * C && t < nv) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(kqraw + r * D + a8 * 8);
+      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&raw);
+      float f[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
+      o = tc::cvt8(f);
+    }
+    *reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u) = o;
+  }
+  // Decay mask of this thread's token row for the score tiles (fixed for the
+  // chunk): rows < C strictly causal (G, A), rows C..2C-1 inclusive (P).
+  float gm[NTH];
+  {
+    const bool isG = row < C, isP = row >= C && row < 2 * C;
+    const int t = isG ? row : row - C;
+    const float gt = (isG || isP) ? sg[t] : 0.f;
+#pragma unroll
+    for (int jj = 0; jj < NTH; ++jj) {
+      const int s_ = tb0 + jj;
+      gm[jj] = ((isG && t > s_) || (isP && t >= s_)) ? __expf(gt - sg[s_]) : 0.f;
+    }
+  }
+
+  tc::fence_smem_to_async();                   // the [K ; Q] tile is a tensor-core operand
+  csync<NT>();                                 // the raw K/Q rows (in the K_l tile) are read
 
   const bool gelu = !(p.flags & 1u);
   for (int l = 0; l < L; ++l) {
