@@ -364,6 +364,24 @@ class HostPipeline:
         self.ev_comp = [torch.cuda.Event() for _ in self.pieces]
         self.lens_dev = None                        # one buffer per piece (16-byte aligned)
 
+    def _run_one(self, host, host_out, host_fs, stream):
+        b = self.buf
+        with torch.cuda.stream(stream):
+            for n in ("q", "k", "v", "log_alpha", "beta", "conv_w", "Wk", "Wp", "wbeta"):
+                b[n].copy_(host[n], non_blocking=True)
+            lens = host.get("seq_lens")
+            lv = None
+            if lens is not None:
+                if self.lens_dev is None:
+                    self.lens_dev = [torch.empty(tuple(lens.shape), dtype=torch.int32, device=self.dev)]
+                self.lens_dev[0].copy_(lens, non_blocking=True)
+                lv = self.lens_dev[0]
+            prism_forward(b["q"], b["k"], b["v"], b["log_alpha"], b["beta"], b["conv_w"], b["Wk"],
+                          b["Wp"], b["wbeta"], self.L, self.chunk, out=self.out, final_state=self.states[0],
+                          seq_lens=lv, workspace=self.ws, stream=stream, no_gelu=self.no_gelu)
+            host_out.copy_(self.out, non_blocking=True)
+            host_fs.copy_(self.states[0], non_blocking=True)
+
     def h2d_bytes(self, host: dict) -> int:
         return sum(t.numel() * t.element_size() for n, t in host.items() if t is not None)
 
@@ -372,6 +390,8 @@ class HostPipeline:
         host_fs [B,H,D,D] fp32 pinned.  Ordered after ``stream`` (default: current) and
         finished before later work on it."""
         caller = stream or torch.cuda.current_stream(self.dev)
+        if len(self.pieces) == 1:                  # nothing to overlap: one stream, no events
+            return self._run_one(host, host_out, host_fs, caller)
         start = torch.cuda.Event()
         start.record(caller)
         for s in (self.s_in, self.s_comp, self.s_out):

@@ -22,6 +22,7 @@ def _cuda():
     (6, 300, 2, 64, 2, 64, True, 4),      # groups of sequences
     (1, 1000, 3, 128, 4, 64, False, 5),   # token segments resumed from the previous state
     (1, 77, 2, 32, 1, 32, False, 3),
+    (3, 90, 2, 32, 2, 32, True, 1),       # one piece: a single stream
 ])
 def test_host_pipeline_equals_one_call(B, T, H, D, L, chunk, ragged, pieces):
     wl = I.Workload("hp", "bf16", B, T, H, D, D, L, 4, chunk, seed=11 + B + D, ragged=ragged)
@@ -29,7 +30,7 @@ def test_host_pipeline_equals_one_call(B, T, H, D, L, chunk, ragged, pieces):
     pinned = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
     shapes = {k: tuple(v.shape) for k, v in host.items() if v is not None}
     pipe = prism.HostPipeline(shapes, torch.bfloat16, L, chunk, pieces=pieces, min_piece_bytes=0)
-    assert len(pipe.pieces) > 1
+    assert (len(pipe.pieces) > 1) == (pieces > 1)
     h_out = torch.empty((B, T, H, D), dtype=torch.float32).pin_memory()
     h_fs = torch.empty((B, H, D, D), dtype=torch.float32).pin_memory()
     pipe.run(pinned, h_out, h_fs)
