@@ -43,7 +43,7 @@ DEFAULT_WORKLOAD = "longctx_bf16"
 
 # ---------------------------------------------------------------- roofline model
 def algorithmic(wl, L):
-    """Algorithmic bytes and flops per launch of each kernel (see the design notes).
+    """Algorithmic bytes and flops per launch of each kernel.
 
     Per token-head (d = d_k = d_v, e = bytes per input element, C = chunk):
       prepare: reads q, k, v, gates: 3 d e + 8; writes the chunk's factored map:

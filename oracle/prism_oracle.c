@@ -21,7 +21,7 @@
  *   §2.2 final injection: B_t = sum_l beta^(l) delta^(l) k^(l)^T
  *   §3.3 (contribution 3): at L = 0 the model is Gated DeltaNet.
  *
- * Readings where the summary is silent (each is listed in the design notes):
+ * Readings where the summary is silent:
  *   - r^(1) = v_t - u_t.
  *   - The Gated DeltaNet write beta_t v_t k_t^T is always part of B_t and the
  *     L refinement terms add to it; otherwise B_t is empty at L = 0 and the

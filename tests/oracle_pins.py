@@ -14,7 +14,8 @@ Model)", gist.science/paper/2602.10796):
         k^(l) = W_k^(l) u_t, p^(l) = W_p^(l) u_t, delta = GELU(p (.) r),
         r^(l+1) = r^(l) - delta^(l); B_t = sum_l beta^(l) delta^(l) k^(l)^T
   §3.3  at L = 0 PRISM reduces to Gated DeltaNet; the write has rank <= L
-        (plus the Gated DeltaNet rank-1 base write, see the design notes)
+        (plus the Gated DeltaNet rank-1 base write, which is kept in B_t so that
+        L = 0 gives Gated DeltaNet)
 """
 from __future__ import annotations
 

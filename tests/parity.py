@@ -1,7 +1,7 @@
 """Helpers shared by the GPU parity tests: run the CUDA path through the C ABI,
-run the oracle on the same host inputs, and compare with the tolerances of the
-design notes (fp32: normwise 1e-4; bf16: max|d| <= 2e-2 RMS(o_ref) and
-relative Frobenius error of the final state <= 1e-2; padding exactly 0)."""
+run the oracle on the same host inputs, and compare with the specified tolerances
+(fp32: normwise 1e-4; bf16: max|d| <= 2e-2 RMS(o_ref) and relative Frobenius error
+of the final state <= 1e-2; padding exactly 0)."""
 from __future__ import annotations
 
 import numpy as np
