@@ -324,6 +324,23 @@ def forward_inputs(inp: dict, L: int, chunk: int, **kw):
                          seq_lens=inp.get("seq_lens"), **kw)
 
 
+def plan_pieces(B, T, chunk, w, moved_bytes, pieces=8, min_piece_bytes=32 << 20):
+    """How HostPipeline cuts the work: a list of (start, end) ranges of sequences when B > 1,
+    or of chunk-aligned token ranges when B = 1 (each at least max(chunk, w) tokens so the
+    next segment's history lies inside its predecessor), at most ``pieces`` of them and,
+    when ``min_piece_bytes`` > 0, none moving fewer bytes than that."""
+    if min_piece_bytes > 0:
+        pieces = max(1, min(pieces, moved_bytes // min_piece_bytes))
+    if B > 1:
+        n = min(pieces, B)
+        step = -(-B // n)
+        return [(b0, min(b0 + step, B)) for b0 in range(0, B, step)]
+    n = max(1, min(pieces, T // max(chunk, w)))
+    step = -(-T // n)
+    step = -(-step // chunk) * chunk
+    return [(t0, min(t0 + step, T)) for t0 in range(0, T, step)]
+
+
 class HostPipeline:
     """The forward pass from host (pinned) inputs to host outputs, with the copies overlapped
     with the kernels: the work is cut into pieces (groups of sequences when B > 1; token
@@ -339,8 +356,8 @@ class HostPipeline:
         B, T, H, D = shapes["q"]
         # pieces small enough to overlap, large enough that copies and launches stay efficient
         moved = B * T * H * D * (3 * torch.tensor([], dtype=dtype).element_size() + 4)
-        if min_piece_bytes > 0:
-            pieces = max(1, min(pieces, moved // min_piece_bytes))
+        self.pieces = plan_pieces(B, T, chunk, shapes["conv_w"][1], moved, pieces, min_piece_bytes)
+        step = max(a1 - a0 for a0, a1 in self.pieces)
         self.B, self.T, self.H, self.D = B, T, H, D
         self.w = shapes["conv_w"][1]
         self.buf = {n: torch.empty(shp, dtype=(dtype if n in ("q", "k", "v") else torch.float32),
@@ -348,15 +365,8 @@ class HostPipeline:
         self.out = torch.empty((B, T, H, D), dtype=torch.float32, device=self.dev)
         self.states = [torch.empty((B, H, D, D), dtype=torch.float32, device=self.dev) for _ in range(2)]
         if B > 1:
-            n = min(pieces, B)
-            step = -(-B // n)
-            self.pieces = [(b0, min(b0 + step, B)) for b0 in range(0, B, step)]
             pdims = make_dims(step, T, H, D, D, self.w, L, chunk, dtype, no_gelu)
         else:
-            n = max(1, min(pieces, T // max(chunk, self.w)))
-            step = -(-T // n)
-            step = -(-step // chunk) * chunk          # chunk-aligned segments
-            self.pieces = [(t0, min(t0 + step, T)) for t0 in range(0, T, step)]
             pdims = make_dims(1, step, H, D, D, self.w, L, chunk, dtype, no_gelu, PRISM_FLAG_VHIST_TOKEN_MAJOR)
         self.ws = alloc_workspace(pdims, self.dev)
         self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(self.dev) for _ in range(3))
