@@ -6,7 +6,9 @@
 //          delta^(l) = GELU(p^(l) (.) r), r -= delta^(l)
 //   S <- alpha (S - beta (S k) k^T) + beta v k^T + sum_l beta^(l) delta^(l) k^(l)^T,   o = S q,
 // then the history moves by one token.  Everything is fp32 (one token is small:
-// matrix-vector products on the CUDA cores), one CTA per (b, h).
+// matrix-vector products on the CUDA cores), one CTA per (b, h); the 2L weight matrices
+// stream through two shared-memory buffers (cp.async, the next one loading while the
+// current one is used) and every product reads shared memory.
 #pragma once
 
 #include "prism_common.cuh"
@@ -35,8 +37,10 @@ constexpr int kDecodeThreads = 256, kDecodeLmax = 8;
 template <int D>
 struct DecodeSmem {
   static constexpr int LDS = D + 1;                       // padded state rows
+  static constexpr int LDW = D + 4;                       // weight rows (16-byte aligned)
   static constexpr size_t oS = 0;                         // f32 [D][LDS]
-  static constexpr size_t oVec = oS + sizeof(float) * D * LDS;   // v, k, q, u, r, p, Sk: 7 x D
+  static constexpr size_t oW = (sizeof(float) * D * LDS + 15) / 16 * 16;   // f32 [2][D][LDW]
+  static constexpr size_t oVec = oW + sizeof(float) * 2 * D * LDW;         // v, k, q, u, r, p, Sk: 7 x D
   static constexpr size_t oKl = oVec + sizeof(float) * 7 * D;    // [Lmax][D] directions
   static constexpr size_t oDl = oKl + sizeof(float) * kDecodeLmax * D;   // [Lmax][D] beta^(l) delta^(l)
   static constexpr size_t oRed = oDl + sizeof(float) * kDecodeLmax * D;  // block-reduction scratch
@@ -57,18 +61,39 @@ __device__ __forceinline__ float block_sum(float x, float* red) {
   return s;
 }
 
-// y[a] = sum_c M[a][c] x[c] for a < D (M row-major D x D in global memory), one warp per
-// row, lanes along the row (coalesced).
+// y[a] = sum_c M[a][c] x[c] for a < D (M in shared memory, rows `ld` floats apart): a warp
+// takes four rows at a time (four independent reductions), lanes along the row.
 template <int D>
-__device__ __forceinline__ void matvec_rows(const float* M, const float* x, float* y) {
+__device__ __forceinline__ void matvec_smem(const float* M, int ld, const float* x, float* y) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int a = warp; a < D; a += kDecodeThreads / 32) {
-    float s = 0.f;
-    for (int c = lane; c < D; c += 32) s = fmaf(M[(size_t)a * D + c], x[c], s);
+  constexpr int NWp = kDecodeThreads / 32;
+  for (int a0 = warp * 4; a0 < D; a0 += NWp * 4) {
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int c = lane; c < D; c += 32) {
+      const float xc = x[c];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) y[a] = s;
+      for (int q = 0; q < 4; ++q) s[q] = fmaf(M[(a0 + q) * ld + c], xc, s[q]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) s[q] += __shfl_xor_sync(0xffffffffu, s[q], o);
+    if (lane < 4) y[a0 + lane] = lane == 0 ? s[0] : lane == 1 ? s[1] : lane == 2 ? s[2] : s[3];
   }
+}
+
+// Weight matrix m (W_k^(l) for m = 2l, W_p^(l) for m = 2l + 1) into buffer m % 2.
+template <int D>
+__device__ __forceinline__ void decode_load_w(const DecodeArgs& p, int h, int m, float* sW) {
+  const int l = m >> 1;
+  const float* g = ((m & 1) ? p.Wp : p.Wk) + ((size_t)h * p.L + l) * D * D;
+  float* dst = sW + (size_t)(m & 1) * D * DecodeSmem<D>::LDW;
+  for (int i = threadIdx.x; i < D * D / 4; i += kDecodeThreads) {
+    const int a = (i * 4) / D, c = (i * 4) % D;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst + a * DecodeSmem<D>::LDW + c)),
+                 "l"(g + (size_t)i * 4) : "memory");
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
 
 template <class T, int D>
@@ -77,6 +102,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(DecodeArgs p) {
   constexpr int LDS = S::LDS;
   extern __shared__ __align__(128) unsigned char smem[];
   float* sS = reinterpret_cast<float*>(smem + S::oS);
+  float* sW = reinterpret_cast<float*>(smem + S::oW);
   float* sv = reinterpret_cast<float*>(smem + S::oVec);
   float* sk = sv + D;
   float* sq = sk + D;
@@ -98,6 +124,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(DecodeArgs p) {
   float* st = p.state + (size_t)bh * D * D;
   const float alpha = expf(p.log_alpha[bh]), beta = p.beta[bh];
 
+  if (L > 0) decode_load_w<D>(p, h, 0, sW);          // W_k^(0) streams in meanwhile
   for (int idx = tid; idx < D * D; idx += kDecodeThreads) sS[(idx / D) * LDS + idx % D] = st[idx];
   for (int c = tid; c < D; c += kDecodeThreads) {
     sv[c] = Elem<T>::to_f(v[c]);
@@ -114,9 +141,19 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(DecodeArgs p) {
   const bool gelu = !(p.flags & 1u);
   for (int l = 0; l < L; ++l) {
     float* kl = skl + l * D;
-    matvec_rows<D>(p.Wk + ((size_t)h * L + l) * D * D, su, kl);
-    matvec_rows<D>(p.Wp + ((size_t)h * L + l) * D * D, su, sp);
-    __syncthreads();
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {        // W_k^(l) then W_p^(l)
+      const int m = 2 * l + which;
+      if (m + 1 < 2 * L) {
+        decode_load_w<D>(p, h, m + 1, sW);           // the next matrix into the other buffer
+        asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+      } else {
+        asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+      }
+      __syncthreads();
+      matvec_smem<D>(sW + (size_t)(m & 1) * D * S::LDW, S::LDW, su, which ? sp : kl);
+      __syncthreads();                               // buffer m % 2 free for matrix m + 2
+    }
     float n2 = 0.f, z = 0.f;
     for (int c = tid; c < D; c += kDecodeThreads) {
       n2 = fmaf(kl[c], kl[c], n2);
@@ -135,13 +172,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(DecodeArgs p) {
   }
 
   // S k, then S <- alpha (S - beta (S k) k^T) + beta v k^T + sum_l D^(l) k^(l)^T, then o = S q
-  for (int i = warp; i < D; i += kDecodeThreads / 32) {
-    float s = 0.f;
-    for (int j = lane; j < D; j += 32) s = fmaf(sS[i * LDS + j], sk[j], s);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) sSk[i] = s;
-  }
+  matvec_smem<D>(sS, LDS, sk, sSk);
   __syncthreads();
   for (int idx = tid; idx < D * D; idx += kDecodeThreads) {
     const int i = idx / D, j = idx % D;
@@ -151,13 +182,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_kernel(DecodeArgs p) {
     st[idx] = x;
   }
   __syncthreads();
-  for (int i = warp; i < D; i += kDecodeThreads / 32) {
-    float s = 0.f;
-    for (int j = lane; j < D; j += 32) s = fmaf(sS[i * LDS + j], sq[j], s);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) p.out[(size_t)bh * D + i] = s;
-  }
+  matvec_smem<D>(sS, LDS, sq, p.out + (size_t)bh * D);
   // history: drop the oldest row, append v_t (all reads before any write)
   T keep[(kDecodeLmax * 128 + kDecodeThreads - 1) / kDecodeThreads];
   int n = 0;
