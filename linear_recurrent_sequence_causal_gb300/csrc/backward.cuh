@@ -89,14 +89,24 @@ __device__ __forceinline__ float gelu_grad(float x) {     // d/dx of x Phi(x)
   return 0.5f * (1.0f + erff(x * 0.70710678118654752f)) + x * 0.39894228040143268f * expf(-0.5f * x * x);
 }
 
+__device__ __forceinline__ void bwd_cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void bwd_cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void bwd_cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bwd_cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void bwd_cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
 // ------------------------------------------------------------------------------------
 // A: refinement forward for kBwdTT tokens of one (b, h)
 
 template <int D>
 struct BwdASmem {
-  static constexpr int LDW = D + 1;
-  static constexpr size_t oW = 0;                                   // W [D][D+1]
-  static constexpr size_t oV = oW + 4u * D * LDW;                   // v rows t0-8 .. t0+TT-1
+  static constexpr size_t oW = 0;                                   // W [2][D][D] (swizzled pieces)
+  static constexpr size_t oV = oW + 4u * 2 * D * D;                 // v rows t0-8 .. t0+TT-1
   static constexpr size_t oU = oV + 4u * (kBwdTT + 8) * D;          // u  [TT][D]
   static constexpr size_t oR = oU + 4u * kBwdTT * D;                // r  [TT][D]
   static constexpr size_t oK = oR + 4u * kBwdTT * D;                // k_hat [TT][D]
@@ -105,10 +115,21 @@ struct BwdASmem {
   static constexpr size_t bytes = oS + 4u * 2 * kBwdTT;
 };
 
-// W [D][D] (row-major, global) into shared memory rows of D + 1.
+// W [D][D] (row-major, global) into shared memory asynchronously (one cp.async group):
+// row a's 16-byte piece j lands at piece j ^ (a mod D/4) of the row, so threads reading
+// one column (consecutive a) or one row (consecutive c) hit different banks.
 template <int D>
-__device__ __forceinline__ void bwd_load_w(float* sW, const float* W) {
-  for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) sW[(idx / D) * (D + 1) + idx % D] = W[idx];
+__device__ __forceinline__ void bwd_load_w_async(float* sW, const float* W) {
+  constexpr int NP = D / 4;
+  for (int i = threadIdx.x; i < D * NP; i += blockDim.x) {
+    const int a = i / NP, j = i % NP;
+    bwd_cp_async16(sW + a * D + ((j ^ (a & (NP - 1))) << 2), W + (size_t)i * 4);
+  }
+  bwd_cp_async_commit();
+}
+template <int D>
+__device__ __forceinline__ float bwd_w(const float* sW, int a, int c) {
+  return sW[a * D + (((c >> 2) ^ (a & (D / 4 - 1))) << 2) + (c & 3)];
 }
 
 // Y[i][a] = sum_c W[a][c] X[i][a'=c] for the NTOK token rows of X (shared memory).
@@ -120,7 +141,7 @@ __device__ __forceinline__ void bwd_matvec(const float* sW, const float* X, floa
 #pragma unroll
   for (int i = 0; i < TPG; ++i) acc[i] = 0.f;
   for (int c = 0; c < D; ++c) {
-    const float wv = sW[a * (D + 1) + c];
+    const float wv = bwd_w<D>(sW, a, c);
 #pragma unroll
     for (int i = 0; i < TPG; ++i) acc[i] = fmaf(wv, X[(g * TPG + i) * D + c], acc[i]);
   }
@@ -137,7 +158,7 @@ __device__ __forceinline__ void bwd_matvec_t_add(const float* sW, const float* X
 #pragma unroll
   for (int i = 0; i < TPG; ++i) acc[i] = 0.f;
   for (int a = 0; a < D; ++a) {
-    const float wv = sW[a * (D + 1) + c];
+    const float wv = bwd_w<D>(sW, a, c);
 #pragma unroll
     for (int i = 0; i < TPG; ++i) acc[i] = fmaf(wv, X[(g * TPG + i) * D + a], acc[i]);
   }
@@ -150,6 +171,8 @@ __device__ __forceinline__ float warp_sum(float x) {
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;
 }
+
+
 
 template <class T, int D>
 __global__ void __launch_bounds__(kBwdThreads) bwd_refine_fwd_kernel(BwdArgs p) {
@@ -170,6 +193,9 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_refine_fwd_kernel(BwdArgs p) 
   const T* v = static_cast<const T*>(p.v);
   const bool gelu = !(p.flags & 1u);
 
+  // the 2L weight matrices (W_k^(0), W_p^(0), W_k^(1), ...) stream through two buffers
+  auto wmat = [&](int m) { return ((m & 1) ? p.Wp : p.Wk) + ((size_t)h * L + (m >> 1)) * D * D; };
+  if (L > 0) bwd_load_w_async<D>(sW, wmat(0));
   for (int idx = tid; idx < (kBwdTT + 8) * D; idx += kBwdThreads) {
     const int t = t0 - 8 + idx / D;
     sV[idx] = (t >= 0 && t < len) ? Elem<T>::to_f(v[(((size_t)b * T_ + t) * H + h) * D + idx % D]) : 0.f;
@@ -186,13 +212,19 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_refine_fwd_kernel(BwdArgs p) 
   }
   __syncthreads();
   for (int l = 0; l < L; ++l) {
-    bwd_load_w<D>(sW, p.Wk + ((size_t)h * L + l) * D * D);
-    __syncthreads();
-    bwd_matvec<D, kBwdTT>(sW, sU, sK);
-    __syncthreads();
-    bwd_load_w<D>(sW, p.Wp + ((size_t)h * L + l) * D * D);
-    __syncthreads();
-    bwd_matvec<D, kBwdTT>(sW, sU, sP);
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const int m = 2 * l + which;
+      if (m + 1 < 2 * L) {
+        bwd_load_w_async<D>(sW + (size_t)((m + 1) & 1) * D * D, wmat(m + 1));
+        bwd_cp_async_wait<1>();
+      } else {
+        bwd_cp_async_wait<0>();
+      }
+      __syncthreads();
+      bwd_matvec<D, kBwdTT>(sW + (size_t)(m & 1) * D * D, sU, which ? sP : sK);
+      __syncthreads();                               // buffer m % 2 free for matrix m + 2
+    }
     for (int i = warp; i < kBwdTT; i += kBwdThreads / 32) {   // reads sK, sU (ready)
       float n2 = 0.f, z = 0.f;
       for (int a = lane; a < D; a += 32) {
@@ -270,16 +302,6 @@ struct BwdBSmem {
   static_assert(NT >= D && NT % D == 0 && NT % 32 == 0, "row slice too small");
 };
 
-__device__ __forceinline__ void bwd_cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void bwd_cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void bwd_cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void bwd_cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void bwd_cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 template <int D, int RS>
 __device__ __forceinline__ void bwd_state_load_async(float* sS, const float* g) {
@@ -646,8 +668,8 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_state_reduce_kernel(BwdArgs p
 
 template <int D>
 struct BwdCSmem {
-  static constexpr size_t oW = 0;                                       // W [D][D+1]
-  static constexpr size_t oR = oW + 4u * D * (D + 1);                   // r^(l) [Lmax][TC][D]
+  static constexpr size_t oW = 0;                                       // W [2][D][D] (swizzled pieces)
+  static constexpr size_t oR = oW + 4u * 2 * D * D;                     // r^(l) [Lmax][TC][D]
   static constexpr size_t oDR = oR + 4u * kBwdLmax * kBwdTC * D;        // dr [TC][D]
   static constexpr size_t oDU = oDR + 4u * kBwdTC * D;                  // du [TC][D]
   static constexpr size_t oG = oDU + 4u * kBwdTC * D;                   // d k_hat [TC][D]
@@ -675,6 +697,12 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_refine_kernel(BwdArgs p) {
   const bool gelu = !(p.flags & 1u);
   auto tok = [&](int t) { return ((size_t)b * T_ + t) * H + h; };
 
+  // the weight matrices in the order they are used: W_k^(L-1), W_p^(L-1), W_k^(L-2), ...
+  auto wmat = [&](int m) {
+    const int l = L - 1 - (m >> 1);
+    return ((m & 1) ? p.Wp : p.Wk) + ((size_t)h * L + l) * D * D;
+  };
+  if (L > 0) bwd_load_w_async<D>(sW, wmat(0));
   // forward recompute of the residual chain: r^(1) = v - u, r^(l+1) = r^(l) - delta^(l)
   for (int idx = tid; idx < kBwdTC * D; idx += kBwdThreads) {
     const int i = idx / D, c = idx % D, t = t0 + i;
@@ -737,14 +765,19 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_refine_kernel(BwdArgs p) {
     }
     __syncthreads();
     // du += W_k^T d k_hat + W_p^T dp + dz w_beta
-    bwd_load_w<D>(sW, p.Wk + ((size_t)h * L + l) * D * D);
-    __syncthreads();
-    bwd_matvec_t_add<D, kBwdTC>(sW, sG, sDU);
-    __syncthreads();
-    bwd_load_w<D>(sW, p.Wp + ((size_t)h * L + l) * D * D);
-    __syncthreads();
-    bwd_matvec_t_add<D, kBwdTC>(sW, sH, sDU);
-    __syncthreads();
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const int m = 2 * (L - 1 - l) + which;
+      if (m + 1 < 2 * L) {
+        bwd_load_w_async<D>(sW + (size_t)((m + 1) & 1) * D * D, wmat(m + 1));
+        bwd_cp_async_wait<1>();
+      } else {
+        bwd_cp_async_wait<0>();
+      }
+      __syncthreads();
+      bwd_matvec_t_add<D, kBwdTC>(sW + (size_t)(m & 1) * D * D, which ? sH : sG, sDU);
+      __syncthreads();                               // buffer m % 2 free for matrix m + 2
+    }
     for (int idx = tid; idx < kBwdTC * D; idx += kBwdThreads)
       sDU[idx] = fmaf(sZ[idx / D], p.wbeta[((size_t)h * L + l) * D + idx % D], sDU[idx]);
     __syncthreads();
