@@ -92,3 +92,29 @@ def test_backward_is_deterministic():
     _, _, g2 = _run("bf16", 64, 2, 45, 2, 2, 4, True, False, True, seed=7)
     for n in G.GRAD_KEYS:
         assert torch.equal(g1[n], g2[n]), f"d{n} differs between two identical calls"
+
+
+def test_backward_short_sequences_and_an_empty_one():
+    """T shorter than a checkpoint block, one sequence of length 0 and one of length 1: the
+    gradients of the others match the oracle and the empty one's are exactly zero."""
+    B, T, H, D, L = 4, 7, 2, 32, 2
+    wl = I.Workload("bwd", "bf16", B, T, H, D, D, L, 4, 16, seed=5, ragged=True)
+    inp = I.generate(wl)
+    inp["seq_lens"] = torch.tensor([T, 0, 1, 5], dtype=torch.int32)
+    rng = np.random.default_rng(5)
+    d_out = rng.standard_normal((B, T, H, D)).astype(np.float32)
+    d_fs = rng.standard_normal((B, H, D, D)).astype(np.float32)
+    ref = G.backward(inp, d_out.astype(np.float64), d_fs.astype(np.float64))
+    d = prism.inputs_to_device(inp)
+    gg = prism.prism_backward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"],
+                              d["Wk"], d["Wp"], d["wbeta"], L, torch.from_numpy(d_out).cuda(),
+                              d_final_state=torch.from_numpy(d_fs).cuda(), seq_lens=d["seq_lens"])
+    torch.cuda.synchronize()
+    for n in G.GRAD_KEYS:
+        gpu = gg[n].double().cpu().numpy()
+        r = ref[n]
+        assert np.all(np.isfinite(gpu)), f"d{n}: non-finite"
+        err = np.max(np.abs(gpu - r)) / max(np.max(np.abs(r)), 1e-30)
+        assert err <= GRAD_TOL, f"d{n}: {err:.3e}"
+    for key in ("q", "k", "v", "log_alpha", "beta"):
+        assert not torch.any(gg[key][1]), f"d{key} of the empty sequence"
