@@ -162,53 +162,82 @@ def pin_shortconv(fwd):
 
 def pin_direction(fwd):
     """§2.2 direction k^(l) = normalize(W_k^(l) u): with a one-hot W_k = e_a e_c^T the
-    direction is e_a u_c / sqrt(u_c^2 + 1e-6).  Catches a transposed W_k."""
+    direction is e_a g u_c / sqrt((g u_c)^2 + 1e-6).  Each head has its own (a, c, g), so
+    a transposed W_k or one head's W_k used for another is caught."""
     dk, dv = 3, 5
-    inp = random_small(1, 9, 1, dk, dv, 1, 2, seed=19)
+    inp = random_small(1, 9, 2, dk, dv, 1, 2, seed=19)
     Wk = torch.zeros_like(inp["Wk"])
-    Wk[0, 0, 1, 3] = 1.7   # row a = 1 (d_k side), column c = 3 (d_v side)
+    per_head = [(1, 3, 1.7), (2, 0, -0.8)]   # (row a on the d_k side, column c on d_v, gain)
+    for h, (a, c, g) in enumerate(per_head):
+        Wk[h, 0, a, c] = g
     inp["Wk"] = Wk
     _, _, tr = fwd(inp, trace=True)
-    u = tr["u"][0, :, 0]
-    kl = tr["kl"][0, :, 0, 0]
-    x = 1.7 * u[:, 3]
-    exp = np.zeros((9, dk))
-    exp[:, 1] = x / np.sqrt(x * x + 1e-6)
-    np.testing.assert_allclose(kl, exp, atol=1e-14, rtol=0)
+    for h, (a, c, g) in enumerate(per_head):
+        x = g * tr["u"][0, :, h, c]
+        exp = np.zeros((9, dk))
+        exp[:, a] = x / np.sqrt(x * x + 1e-6)
+        np.testing.assert_allclose(tr["kl"][0, :, h, 0], exp, atol=1e-14, rtol=0)
 
 
 def pin_gain_and_gelu(fwd):
     """§2.2 delta^(1) = GELU(p (.) r^(1)) with p = W_p u.  W_p = s I gives p = s u, and
-    GELU(x) = x Phi(x) with Phi the standard normal CDF (scipy)."""
+    GELU(x) = x Phi(x) with Phi the standard normal CDF (scipy).  The two heads take
+    different gains s."""
     dv = 6
-    inp = random_small(1, 14, 1, 4, dv, 2, 3, seed=20)
-    s = 1.9
-    inp["Wp"][0, 0] = s * torch.eye(dv, dtype=torch.float64)
+    inp = random_small(1, 14, 2, 4, dv, 2, 3, seed=20)
+    gains = (1.9, -0.6)
+    for h, s in enumerate(gains):
+        inp["Wp"][h, 0] = s * torch.eye(dv, dtype=torch.float64)
     _, _, tr = fwd(inp, trace=True)
-    u, r1 = tr["u"][0, :, 0], tr["r1"][0, :, 0]
-    x = s * u * r1
-    np.testing.assert_allclose(tr["delta"][0, :, 0, 0], x * scipy.stats.norm.cdf(x), atol=1e-14,
-                               rtol=1e-13)
-    # The second step acts on the updated residual r^(2) = r^(1) - delta^(1).
-    p2 = tr["pl"][0, :, 0, 1]
-    x2 = p2 * (r1 - tr["delta"][0, :, 0, 0])
-    np.testing.assert_allclose(tr["delta"][0, :, 0, 1], x2 * scipy.stats.norm.cdf(x2),
-                               atol=1e-14, rtol=1e-13)
+    for h, s in enumerate(gains):
+        u, r1 = tr["u"][0, :, h], tr["r1"][0, :, h]
+        x = s * u * r1
+        np.testing.assert_allclose(tr["delta"][0, :, h, 0], x * scipy.stats.norm.cdf(x),
+                                   atol=1e-14, rtol=1e-13)
+        # The second step acts on the updated residual r^(2) = r^(1) - delta^(1).
+        p2 = tr["pl"][0, :, h, 1]
+        x2 = p2 * (r1 - tr["delta"][0, :, h, 0])
+        np.testing.assert_allclose(tr["delta"][0, :, h, 1], x2 * scipy.stats.norm.cdf(x2),
+                                   atol=1e-14, rtol=1e-13)
 
 
 def pin_confidence_gate(fwd):
     """§2.2 confidence gate beta^(l) = sigmoid(w_beta^(l) . u): w = 0 gives exactly 1/2;
-    w = s e_c gives expit(s u_c) (scipy).  The write factor is beta^(l) delta^(l)."""
+    w = s e_c gives expit(s u_c) (scipy).  The write factor is beta^(l) delta^(l).  The
+    second head takes another (s, c)."""
     dv = 5
-    inp = random_small(1, 11, 1, 4, dv, 2, 3, seed=21)
-    inp["wbeta"][0, 0].zero_()
-    inp["wbeta"][0, 1].zero_()
-    inp["wbeta"][0, 1, 3] = -2.3
+    inp = random_small(1, 11, 2, 4, dv, 2, 3, seed=21)
+    inp["wbeta"].zero_()
+    per_head = [(3, -2.3), (1, 1.4)]
+    for h, (c, s) in enumerate(per_head):
+        inp["wbeta"][h, 1, c] = s
     _, _, tr = fwd(inp, trace=True)
-    assert np.all(tr["betal"][0, :, 0, 0] == 0.5)
-    np.testing.assert_allclose(tr["betal"][0, :, 0, 1], scipy.special.expit(-2.3 * tr["u"][0, :, 0, 3]),
-                               atol=1e-15, rtol=1e-14)
+    assert np.all(tr["betal"][0, :, :, 0] == 0.5)
+    for h, (c, s) in enumerate(per_head):
+        np.testing.assert_allclose(tr["betal"][0, :, h, 1], scipy.special.expit(s * tr["u"][0, :, h, c]),
+                                   atol=1e-15, rtol=1e-14)
     np.testing.assert_allclose(tr["dl"], tr["betal"][..., None] * tr["delta"], atol=1e-15, rtol=0)
+
+
+def pin_gate_scales_write(fwd):
+    """§2.2 final injection B_t = sum_l beta^(l) delta^(l) k^(l)^T: delta^(l) and k^(l) do
+    not depend on w_beta, so the refinement part of the write the state receives, B_t minus
+    the L = 0 write, scales with the gate.  At L = 1 a run with w_beta = s e_c has
+    2 expit(s u_c) times the refinement write of a run with w_beta = 0 (gate 1/2)."""
+    inp = random_small(1, 13, 2, 4, 5, 1, 3, seed=27)
+    c, s = 2, 1.6
+    half = {k: (v.clone() if v is not None else None) for k, v in inp.items()}
+    half["wbeta"].zero_()
+    gated = {k: (v.clone() if v is not None else None) for k, v in half.items()}
+    gated["wbeta"][:, 0, c] = s
+    _, _, tr0 = fwd(inp, trace=True, L=0)
+    _, _, trh = fwd(half, trace=True)
+    _, _, trg = fwd(gated, trace=True)
+    base = tr0["Bt"]
+    dh, dg = trh["Bt"] - base, trg["Bt"] - base
+    assert np.max(np.abs(dh)) > 1e-3, "refinement write vanished"
+    ratio = 2.0 * scipy.special.expit(s * trh["u"][..., c])       # [B, T, H]
+    np.testing.assert_allclose(dg, ratio[..., None, None] * dh, atol=1e-14, rtol=1e-12)
 
 
 def pin_padding(fwd):
@@ -293,7 +322,8 @@ def pin_initial_state_gated_deltanet(fwd):
 
 ALL_PINS = [pin_l0_is_gated_deltanet, pin_zero_conv_is_gated_deltanet, pin_write_rank,
             pin_telescoping, pin_brute_force_products, pin_prefix_sum, pin_no_write_no_output,
-            pin_shortconv, pin_direction, pin_gain_and_gelu, pin_confidence_gate, pin_padding,
+            pin_shortconv, pin_direction, pin_gain_and_gelu, pin_confidence_gate,
+            pin_gate_scales_write, pin_padding,
             pin_causality, pin_identity_activation, pin_resume_is_markov,
             pin_initial_state_gated_deltanet]
 

@@ -22,6 +22,30 @@ def test_oracle_pin(pin):
     pin(oracle.forward)
 
 
+# The state update and the readout of one token, as they stand in prism_oracle.c: the
+# "output_before_update" mistake swaps them.
+_UPDATE = (
+    '        /* S <- S A_t + B_t, with S A_t = alpha (S - beta (S k) k^T). */\n'
+    '        for (int i = 0; i < dv; ++i) {\n'
+    '            double s = 0.0;\n'
+    '            for (int j = 0; j < dk; ++j) s += S[(size_t)i * dk + j] * kt[j];\n'
+    '            Sk[i] = s;\n'
+    '        }\n'
+    '        for (int i = 0; i < dv; ++i)\n'
+    '            for (int j = 0; j < dk; ++j) {\n'
+    '                double* sij = &S[(size_t)i * dk + j];\n'
+    '                *sij = alpha * (*sij - beta * Sk[i] * kt[j]) + Bw[(size_t)i * dk + j];\n'
+    '            }\n'
+)
+_READOUT = (
+    '        /* o_t = S_t q_t */\n'
+    '        for (int i = 0; i < dv; ++i) {\n'
+    '            double s = 0.0;\n'
+    '            for (int j = 0; j < dk; ++j) s += S[(size_t)i * dk + j] * qt[j];\n'
+    '            o[i] = s;\n'
+    '        }\n'
+)
+
 # (name, text in prism_oracle.c, replacement): each is a mistake a restatement of
 # the method could plausibly contain.
 MUTANTS = [
@@ -45,6 +69,24 @@ MUTANTS = [
     ("initial_state_ignored", "if (P->initial_state)\n        memcpy(", "if (0)\n        memcpy("),
     ("history_ignored", "else if (P->v_hist)", "else if (0)"),
     ("history_reversed", "(w + t - j)) * dv;", "(-1 - t + j)) * dv;"),
+    ("k_from_residual", "s += Wk[(size_t)a * dv + c] * u[c];", "s += Wk[(size_t)a * dv + c] * r[c];"),
+    ("p_from_residual", "s += Wp[(size_t)a * dv + c] * u[c];", "s += Wp[(size_t)a * dv + c] * r[c];"),
+    ("gate_from_residual", "z += wb[c] * u[c];", "z += wb[c] * r[c];"),
+    ("gate_dropped_from_write", "Bw[(size_t)i * dk + j] += bl * dl[i] * kk[j];",
+     "Bw[(size_t)i * dk + j] += dl[i] * kk[j];"),
+    ("wk_of_first_step", "P->Wk + ((size_t)h * L + l)", "P->Wk + ((size_t)h * L + 0)"),
+    ("wp_of_first_step", "P->Wp + ((size_t)h * L + l)", "P->Wp + ((size_t)h * L + 0)"),
+    ("wbeta_of_first_step", "P->wbeta + ((size_t)h * L + l)", "P->wbeta + ((size_t)h * L + 0)"),
+    ("wk_of_head_zero", "P->Wk + ((size_t)h * L + l)", "P->Wk + ((size_t)0 * L + l)"),
+    ("wp_of_head_zero", "P->Wp + ((size_t)h * L + l)", "P->Wp + ((size_t)0 * L + l)"),
+    ("wbeta_of_head_zero", "P->wbeta + ((size_t)h * L + l)", "P->wbeta + ((size_t)0 * L + l)"),
+    ("conv_of_head_zero", "P->conv_w + ((size_t)h * w", "P->conv_w + ((size_t)0 * w"),
+    ("readout_with_k", "s += S[(size_t)i * dk + j] * qt[j];", "s += S[(size_t)i * dk + j] * kt[j];"),
+    ("beta_of_previous_token", "const double beta = P->beta[((size_t)b * T + t) * P->H + h];",
+     "const double beta = P->beta[((size_t)b * T + (t > 0 ? t - 1 : 0)) * P->H + h];"),
+    ("padding_processed", "if (t >= len) {", "if (0) {"),
+    ("r1_without_anchor", "r[i] = vt[i] - u[i];", "r[i] = vt[i];"),
+    ("output_before_update", _UPDATE + _READOUT, _READOUT + _UPDATE),
 ]
 
 
