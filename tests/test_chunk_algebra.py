@@ -16,6 +16,12 @@ log alpha inside the chunk, gamma = exp(g), Gamma_ts = exp(g_t - g_s):
 where K_l, D_l are the per-token refinement directions k^(l) and write values
 beta^(l) delta^(l) ("Technical Summary: PRISM", §2.2), and the Gated DeltaNet
 write beta v k^T is the E part.
+
+S1 is affine in S0: S1 = S0 M + c with M = gamma_C I - W^T diag(gamma_C/gamma) K and
+c = U^T diag(gamma_C/gamma) K + sum_l D_l^T diag(gamma_C/gamma) K_l.  Maps compose as
+(M1, c1) o (M2, c2) = (M1 M2, c1 M2 + c2), which is what a sequence split into segments
+scanned in parallel would exchange (the §2.1 recurrence is an affine scan); the last test
+checks that combine against the oracle.
 """
 import numpy as np
 import pytest
@@ -24,12 +30,44 @@ import oracle
 from linear_recurrent_sequence_causal_gb300.inputs import random_small
 
 
-def chunk_form(inp, kl, dl, C):
+def one_chunk(S, Q, K, V, bt, la, Kl, Dl):
+    """One chunk from entering state S: returns (O, S1, M, c) with S1 = S M + c."""
+    n_c, dk = K.shape
+    g = np.cumsum(la)
+    gam = np.exp(g)
+    G = np.exp(g[:, None] - g[None, :])
+    low = np.tril(np.ones((n_c, n_c)), -1)
+    inc = np.tril(np.ones((n_c, n_c)))
+    A = bt[:, None] * (K @ K.T) * G * low
+    Tm = np.linalg.inv(np.eye(n_c) + A)
+    L = len(Kl)
+    R = sum(((K @ Kl[l].T) * G * low) @ Dl[l] for l in range(L)) if L else 0.0
+    W = Tm @ ((bt * gam)[:, None] * K)
+    U = Tm @ (bt[:, None] * (V - R))
+    E = U - W @ S.T
+    O = gam[:, None] * (Q @ S.T) + ((Q @ K.T) * G * inc) @ E
+    for l in range(L):
+        O += ((Q @ Kl[l].T) * G * inc) @ Dl[l]
+    dec = np.exp(g[-1] - g)
+    c = U.T @ (dec[:, None] * K)
+    for l in range(L):
+        c += Dl[l].T @ (dec[:, None] * Kl[l])
+    M = np.exp(g[-1]) * np.eye(dk) - W.T @ (dec[:, None] * K)
+    return O, S @ M + c, M, c
+
+
+def _chunk_inputs(inp, kl, dl, b, h, c0, c1):
     q, k, v = (inp[n].double().numpy() for n in ("q", "k", "v"))
     la, be = inp["log_alpha"].double().numpy(), inp["beta"].double().numpy()
-    B, T, H, dk = q.shape
-    dv = v.shape[-1]
     L = kl.shape[3]
+    return (q[b, c0:c1, h], k[b, c0:c1, h], v[b, c0:c1, h], be[b, c0:c1, h], la[b, c0:c1, h],
+            [np.nan_to_num(kl[b, c0:c1, h, l]) for l in range(L)],
+            [np.nan_to_num(dl[b, c0:c1, h, l]) for l in range(L)])
+
+
+def chunk_form(inp, kl, dl, C):
+    B, T, H, dk = inp["q"].shape
+    dv = inp["v"].shape[-1]
     sl = inp.get("seq_lens")
     out = np.zeros((B, T, H, dv))
     fs = np.zeros((B, H, dv, dk))
@@ -39,31 +77,8 @@ def chunk_form(inp, kl, dl, C):
             S = np.zeros((dv, dk))
             for c0 in range(0, n, C):
                 c1 = min(c0 + C, n)
-                Q, K, V = q[b, c0:c1, h], k[b, c0:c1, h], v[b, c0:c1, h]
-                bt = be[b, c0:c1, h]
-                g = np.cumsum(la[b, c0:c1, h])
-                gam = np.exp(g)
-                G = np.exp(g[:, None] - g[None, :])
-                n_c = c1 - c0
-                low = np.tril(np.ones((n_c, n_c)), -1)
-                inc = np.tril(np.ones((n_c, n_c)))
-                A = bt[:, None] * (K @ K.T) * G * low
-                Tm = np.linalg.inv(np.eye(n_c) + A)
-                Kl = [np.nan_to_num(kl[b, c0:c1, h, l]) for l in range(L)]
-                Dl = [np.nan_to_num(dl[b, c0:c1, h, l]) for l in range(L)]
-                R = sum(((K @ Kl[l].T) * G * low) @ Dl[l] for l in range(L)) if L else 0.0
-                W = Tm @ ((bt * gam)[:, None] * K)
-                U = Tm @ (bt[:, None] * (V - R))
-                E = U - W @ S.T
-                O = gam[:, None] * (Q @ S.T) + ((Q @ K.T) * G * inc) @ E
-                for l in range(L):
-                    O += ((Q @ Kl[l].T) * G * inc) @ Dl[l]
-                dec = np.exp(g[-1] - g)
-                Snew = np.exp(g[-1]) * S + E.T @ (dec[:, None] * K)
-                for l in range(L):
-                    Snew += Dl[l].T @ (dec[:, None] * Kl[l])
+                O, S, _, _ = one_chunk(S, *_chunk_inputs(inp, kl, dl, b, h, c0, c1))
                 out[b, c0:c1, h] = O
-                S = Snew
             fs[b, h] = S
     return out, fs
 
@@ -76,3 +91,45 @@ def test_chunk_form_matches_oracle(L, C, ragged):
     scale_o = np.max(np.abs(out))
     np.testing.assert_allclose(co, out, atol=1e-12 * scale_o, rtol=0)
     np.testing.assert_allclose(cs, fs, atol=1e-12 * np.max(np.abs(fs)), rtol=0)
+
+
+@pytest.mark.parametrize("L,C,cuts", [(0, 8, (16, 40)), (2, 8, (24,)), (3, 6, (12, 18, 36))])
+def test_sequence_split_affine_combine(L, C, cuts):
+    """Sequence split: each segment's affine map S_end = S_start M + c is built from its own
+    chunks starting from nothing; an exclusive scan with (M1, c1) o (M2, c2) =
+    (M1 M2, c1 M2 + c2) gives every segment's entering state, which equals the oracle's
+    state after the prefix; the segment's outputs recomputed from that state equal the
+    oracle's."""
+    B, T, H, dk, dv = 1, 45, 2, 6, 7
+    inp = random_small(B, T, H, dk, dv, L, 4, seed=60 + L)
+    out, fs, tr = oracle.forward(inp, trace=True)
+    bounds = [0, *cuts, T]
+    for h in range(H):
+        maps = []
+        for s0, s1 in zip(bounds[:-1], bounds[1:]):
+            M, c = np.eye(dk), np.zeros((dv, dk))
+            for c0 in range(s0, s1, C):
+                _, _, Mc, cc = one_chunk(np.zeros((dv, dk)),
+                                         *_chunk_inputs(inp, tr["kl"], tr["dl"], 0, h, c0,
+                                                        min(c0 + C, s1)))
+                M, c = M @ Mc, c @ Mc + cc
+            maps.append((M, c))
+        S = np.zeros((dv, dk))
+        for i, (s0, s1) in enumerate(zip(bounds[:-1], bounds[1:])):
+            if s0 > 0:
+                pre = {n: (v[:, :s0].contiguous() if n in ("q", "k", "v", "log_alpha", "beta")
+                           else v) for n, v in inp.items()}
+                _, fs_pre, _ = oracle.forward(pre)
+                np.testing.assert_allclose(S, fs_pre[0, h], rtol=0,
+                                           atol=1e-12 * np.max(np.abs(fs_pre[0, h])))
+            Sseg = S.copy()
+            for c0 in range(s0, s1, C):
+                c1 = min(c0 + C, s1)
+                O, Sseg, _, _ = one_chunk(Sseg, *_chunk_inputs(inp, tr["kl"], tr["dl"], 0, h,
+                                                               c0, c1))
+                np.testing.assert_allclose(O, out[0, c0:c1, h], rtol=0,
+                                           atol=1e-12 * np.max(np.abs(out)))
+            M, c = maps[i]
+            S = S @ M + c
+            np.testing.assert_allclose(S, Sseg, rtol=0, atol=1e-12 * np.max(np.abs(Sseg)))
+        np.testing.assert_allclose(S, fs[0, h], rtol=0, atol=1e-12 * np.max(np.abs(fs[0, h])))
