@@ -150,6 +150,20 @@ PRISM_API int prism_forward_from(const prism_dims* dims,
                                  float* out, float* final_state, const int32_t* seq_lens,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
+/* The device status word of the last prism_forward / prism_forward_from /
+ * prism_prepare + prism_scan call that used this workspace (same dims).  Every
+ * wait those kernels make on an mbarrier is bounded; one that gives up writes a
+ * nonzero word instead of hanging, and that call's outputs are then invalid.
+ *   *status = 0 when every wait completed; nonzero otherwise.
+ * Waits for `stream` (it copies 4 bytes from the workspace and synchronises), so
+ * call it on the stream the forward pass ran on, after it.  The word is cleared
+ * at the start of each forward call.  Errors: as for prism_forward's dims and
+ * workspace checks; PRISM_ERR_INVALID_ARG for a NULL status; PRISM_ERR_CUDA when
+ * the copy or the synchronisation fails.  prism_forward_static keeps its word in
+ * the library's own scratch and is not covered. */
+PRISM_API int prism_device_status(const prism_dims* dims, const void* workspace,
+                                  size_t workspace_bytes, int* status, void* stream);
+
 /* One token of every sequence (dims->T must be 1; chunk is ignored): the
  * recurrence of §2.1-2.2 of "Technical Summary: PRISM" applied to a single token,
  * for streaming generation after a prism_forward_from / prism_forward prefix.

@@ -391,6 +391,24 @@ extern "C" PRISM_API int prism_forward(const prism_dims* dims, const void* q, co
                             out, final_state, seq_lens, workspace, workspace_bytes, stream);
 }
 
+extern "C" PRISM_API int prism_device_status(const prism_dims* dims, const void* workspace,
+                                             size_t workspace_bytes, int* status, void* stream) {
+  const int rc = check_dims(dims);
+  if (rc != PRISM_OK) return rc;
+  if (!status) return PRISM_ERR_INVALID_ARG;
+  if (workspace && !aligned(workspace, 256)) return PRISM_ERR_MISALIGNED;
+  const Layout Lo = layout(dims);
+  if (!workspace || workspace_bytes < Lo.total) return PRISM_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  const int* src = region<const int>(const_cast<void*>(workspace), Lo, PRISM_WS_STATUS);
+  if (cudaMemcpyAsync(&word, src, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return PRISM_ERR_CUDA;
+  *status = word;
+  return PRISM_OK;
+}
+
 extern "C" PRISM_API int prism_decode_step(const prism_dims* dims, const void* q, const void* k,
                                            const void* v, const float* log_alpha,
                                            const float* beta, const float* conv_w,

@@ -25,7 +25,8 @@ ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
 STATIC_SCRATCH_BYTES = 32 << 20
 EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "prism_prepare",
            "prism_scan", "prism_forward_static", "prism_strerror", "prism_forward_from",
-           "prism_decode_step", "prism_backward_workspace_bytes", "prism_backward")
+           "prism_decode_step", "prism_backward_workspace_bytes", "prism_backward",
+           "prism_device_status")
 WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC")
 
 
@@ -81,6 +82,9 @@ def load():
             lib.prism_backward_workspace_bytes.restype = ctypes.c_size_t
             lib.prism_backward.argtypes = [ctypes.POINTER(Dims)] + [_vp] * 21 + [ctypes.c_size_t, _vp]
             lib.prism_backward.restype = ctypes.c_int
+            lib.prism_device_status.argtypes = [ctypes.POINTER(Dims), _vp, ctypes.c_size_t,
+                                                 ctypes.POINTER(ctypes.c_int), _vp]
+            lib.prism_device_status.restype = ctypes.c_int
             lib.prism_strerror.argtypes = [ctypes.c_int]
             lib.prism_strerror.restype = ctypes.c_char_p
             _lib = lib
@@ -142,6 +146,15 @@ def _dims_for(q, v, conv_w, L, chunk, no_gelu=False, flags=0) -> Dims:
 
 def alloc_workspace(dims: Dims, device) -> torch.Tensor:
     return torch.empty(max(workspace_bytes(dims), 1), dtype=torch.uint8, device=device)
+
+
+def device_status(dims: Dims, workspace, stream=None) -> int:
+    """The device status word a forward call left in ``workspace`` (0: every bounded wait
+    completed).  Synchronises ``stream``."""
+    word = ctypes.c_int(-1)
+    _check(load().prism_device_status(ctypes.byref(dims), _ptr(workspace), workspace.numel(),
+                                      ctypes.byref(word), _stream_ptr(stream)))
+    return word.value
 
 
 def prism_forward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, out=None,

@@ -141,3 +141,22 @@ def test_backward_argument_errors(lib):
     p[12] = 0x1004                                 # dk misaligned
     assert call(d, p) == 3
     assert call(d, ok, wsb=nbytes - 1) == 4        # workspace too small
+
+
+def test_device_status_argument_errors(lib):
+    """prism_device_status rejects bad dims, a NULL result pointer and a missing, misaligned
+    or short workspace before touching the device."""
+    d = prism.make_dims(2, 64, 2, 32, 32, 4, 2, 32, prism.PRISM_BF16)
+    need = prism.workspace_bytes(d)
+    word = ctypes.c_int(-1)
+
+    def call(dims, ws, nbytes, out=ctypes.byref(word)):
+        return lib.prism_device_status(ctypes.byref(dims), ws, nbytes, out, None)
+
+    bad = prism.make_dims(2, 64, 2, 32, 32, 4, 2, 48, prism.PRISM_BF16)       # chunk 48
+    assert call(bad, 0x100000, need) == 2
+    assert call(d, 0x100000, need, None) == 1
+    assert call(d, 0x100010, need) == 3
+    assert call(d, None, need) == 4
+    assert call(d, 0x100000, need - 1) == 4
+    assert word.value == -1

@@ -258,3 +258,16 @@ def test_boundary_errors_on_device():
     with pytest.raises(prism.PrismError) as e:
         prism.forward_inputs(d, 2, 48)
     assert e.value.code == 2
+
+
+@pytest.mark.parametrize("dtype,D,C", [("bf16", 128, 64), ("bf16", 32, 16), ("f32", 16, 16)])
+def test_device_status_after_forward(dtype, D, C):
+    """Every bounded wait completed: the workspace's status word, filled with a nonzero
+    pattern beforehand, reads 0 through prism_device_status after a forward call."""
+    wl = I.Workload("case", dtype, 2, 100, 2, D, D, 2, 4, C, seed=8)
+    d = prism.inputs_to_device(I.generate(wl))
+    dims = prism.make_dims(2, 100, 2, D, D, 4, 2, C, d["q"].dtype)
+    ws = prism.alloc_workspace(dims, "cuda")
+    ws.fill_(0xA5)
+    prism.forward_inputs(d, wl.L, wl.chunk, workspace=ws)
+    assert prism.device_status(dims, ws) == 0
