@@ -64,6 +64,31 @@ def _refine_forward(u, v, Wk, Wp, wb, identity_act):
     return st
 
 
+def refine_backward(st, dD, dkl, u, Wk, Wp, wb, g, h, identity_act):
+    """The refinement chain of one token backwards, from the cotangents dD[l] of the write
+    values D_l and dkl[l] of the directions k_l.  Adds the weight gradients of head h to
+    ``g`` and returns (dr_1, du): the cotangent of r^(1) and the projections' share of the
+    anchor's cotangent."""
+    dv = u.shape[0]
+    dr = np.zeros(dv)
+    du = np.zeros(dv)
+    for l in range(len(st) - 1, -1, -1):
+        s = st[l]
+        gd = s["b"] * dD[l] - dr
+        gp = np.ones(dv) if identity_act else \
+            scipy.stats.norm.cdf(s["x"]) + s["x"] * scipy.stats.norm.pdf(s["x"])
+        dx = gd * gp
+        dp = dx * s["r"]
+        dr = dr + dx * s["p"]
+        dz = (s["delta"] @ dD[l]) * s["b"] * (1.0 - s["b"])
+        dkh = s["n"] * (dkl[l] - s["k"] * (s["k"] @ dkl[l]))
+        du += Wk[l].T @ dkh + Wp[l].T @ dp + dz * wb[l]
+        g["Wk"][h, l] += np.outer(dkh, u)
+        g["Wp"][h, l] += np.outer(dp, u)
+        g["wbeta"][h, l] += dz * u
+    return dr, du
+
+
 def adjoint(inp, d_out, d_fs, *, identity_act=False, block=16, rs=1):
     f = {n: (np.asarray(inp[n], dtype=np.float64) if inp[n] is not None else None)
          for n in G.GRAD_KEYS}
@@ -138,22 +163,8 @@ def adjoint(inp, d_out, d_fs, *, identity_act=False, block=16, rs=1):
                     g["beta"][b, t, h] = acc["dbeta"]
                     g["log_alpha"][b, t, h] = acc["dla"]
                     # refinement chain backwards
-                    dr = np.zeros(dv)
-                    dut = np.zeros(dv)
-                    for l in range(len(ref[t]) - 1, -1, -1):
-                        s = ref[t][l]
-                        gd = s["b"] * dD[l] - dr
-                        gp = np.ones(dv) if identity_act else \
-                            scipy.stats.norm.cdf(s["x"]) + s["x"] * scipy.stats.norm.pdf(s["x"])
-                        dx = gd * gp
-                        dp = dx * s["r"]
-                        dr = dr + dx * s["p"]
-                        dz = (s["delta"] @ dD[l]) * s["b"] * (1.0 - s["b"])
-                        dkh = s["n"] * (acc["dkl"][l] - s["k"] * (s["k"] @ acc["dkl"][l]))
-                        dut += Wk[h, l].T @ dkh + Wp[h, l].T @ dp + dz * wb[h, l]
-                        g["Wk"][h, l] += np.outer(dkh, u[t])
-                        g["Wp"][h, l] += np.outer(dp, u[t])
-                        g["wbeta"][h, l] += dz * u[t]
+                    dr, dut = refine_backward(ref[t], dD, acc["dkl"], u[t], Wk[h], Wp[h], wb[h],
+                                              g, h, identity_act)
                     dv_t += dr
                     dut -= dr
                     g["v"][b, t, h] += dv_t
