@@ -263,6 +263,53 @@ PRISM_API int prism_backward(const prism_dims* dims,
                              const int32_t* seq_lens, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* ---- Host-to-host forward pass ----
+ * prism_forward on HOST buffers: q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta,
+ * seq_lens are read from host memory and out, final_state written to host memory
+ * (same shapes and meaning as prism_forward; final_state and seq_lens may be NULL,
+ * conv_w and the weights too when L = 0).  The work is cut into pieces, and piece i's
+ * kernels run while piece i+1 is copied in and piece i-1 copied out:
+ *   streams[0] copies in, streams[1] runs the kernels, streams[2] copies out
+ *   (caller-owned cudaStream_t handles; streams = NULL runs all on the legacy default
+ *   stream; a single piece runs on streams[2] alone).
+ * Pieces are groups of whole sequences when B > 1 and chunk-aligned token segments
+ * when B = 1 (a segment starts from the previous one's final state and reads the v rows
+ * before it as the anchor's history, so the result equals one prism_forward call).  At
+ * most max_pieces (1..PRISM_HOST_MAX_PIECES) pieces, each moving at least
+ * min_piece_bytes of q, k, v and out (0: no minimum).
+ *   arena  DEVICE buffer of at least prism_host_arena_bytes(dims, max_pieces,
+ *          min_piece_bytes) bytes, 256-byte aligned: device copies of the inputs and
+ *          outputs and a workspace; its contents are scratch.
+ * Ordering: the call's work starts after the work already enqueued on all three
+ * streams and is complete when streams[2] gets past it (synchronise on streams[2], or
+ * wait on an event recorded there, before reading out or final_state).  Overlap needs
+ * page-locked host memory; pageable buffers work but the copies then block.  When
+ * B = 1, seq_lens[0] is read on the host during the call.  Errors: those of
+ * prism_forward's dims checks; PRISM_ERR_INVALID_ARG for a NULL required pointer,
+ * max_pieces out of range or PRISM_FLAG_VHIST_TOKEN_MAJOR in dims->flags;
+ * PRISM_ERR_WORKSPACE / PRISM_ERR_MISALIGNED for the arena; PRISM_ERR_CUDA when a copy,
+ * event or stream call fails (part of the work may then be enqueued and the outputs are
+ * undefined).  The pages describe the layer, not its data movement: this entry point
+ * has no counterpart there. */
+#define PRISM_HOST_MAX_PIECES 16
+
+/* The pieces prism_forward_host cuts these dims into: *n_pieces and their boundaries
+ * bounds[0] = 0 < bounds[1] < ... < bounds[*n_pieces] (= B when B > 1, else T); bounds
+ * must hold max_pieces + 1 ints. */
+PRISM_API int prism_host_plan(const prism_dims* dims, int max_pieces, size_t min_piece_bytes,
+                              int* n_pieces, int* bounds);
+/* Device arena bytes for prism_forward_host (0 if the arguments are invalid). */
+PRISM_API size_t prism_host_arena_bytes(const prism_dims* dims, int max_pieces,
+                                        size_t min_piece_bytes);
+PRISM_API int prism_forward_host(const prism_dims* dims,
+                                 const void* q, const void* k, const void* v,
+                                 const float* log_alpha, const float* beta,
+                                 const float* conv_w, const float* Wk, const float* Wp,
+                                 const float* wbeta,
+                                 float* out, float* final_state, const int32_t* seq_lens,
+                                 int max_pieces, size_t min_piece_bytes,
+                                 void* arena, size_t arena_bytes, void* const* streams);
+
 /* Static description of an error code. */
 PRISM_API const char* prism_strerror(int code);
 

@@ -23,10 +23,12 @@ ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
           3: "PRISM_ERR_MISALIGNED", 4: "PRISM_ERR_WORKSPACE", 5: "PRISM_ERR_LAUNCH",
           6: "PRISM_ERR_CUDA", 7: "PRISM_ERR_SCRATCH_LIMIT"}
 STATIC_SCRATCH_BYTES = 32 << 20
+PRISM_HOST_MAX_PIECES = 16
 EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "prism_prepare",
            "prism_scan", "prism_forward_static", "prism_strerror", "prism_forward_from",
            "prism_decode_step", "prism_backward_workspace_bytes", "prism_backward",
-           "prism_device_status")
+           "prism_device_status", "prism_host_plan", "prism_host_arena_bytes",
+           "prism_forward_host")
 WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC")
 
 
@@ -85,6 +87,15 @@ def load():
             lib.prism_device_status.argtypes = [ctypes.POINTER(Dims), _vp, ctypes.c_size_t,
                                                  ctypes.POINTER(ctypes.c_int), _vp]
             lib.prism_device_status.restype = ctypes.c_int
+            lib.prism_host_plan.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_size_t,
+                                            ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+            lib.prism_host_plan.restype = ctypes.c_int
+            lib.prism_host_arena_bytes.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_size_t]
+            lib.prism_host_arena_bytes.restype = ctypes.c_size_t
+            lib.prism_forward_host.argtypes = ([ctypes.POINTER(Dims)] + [_vp] * 12
+                                               + [ctypes.c_int, ctypes.c_size_t, _vp, ctypes.c_size_t,
+                                                  ctypes.POINTER(ctypes.c_void_p)])
+            lib.prism_forward_host.restype = ctypes.c_int
             lib.prism_strerror.argtypes = [ctypes.c_int]
             lib.prism_strerror.restype = ctypes.c_char_p
             _lib = lib
@@ -337,73 +348,50 @@ def forward_inputs(inp: dict, L: int, chunk: int, **kw):
                          seq_lens=inp.get("seq_lens"), **kw)
 
 
-def plan_pieces(B, T, chunk, w, moved_bytes, pieces=8, min_piece_bytes=32 << 20):
-    """How HostPipeline cuts the work: a list of (start, end) ranges of sequences when B > 1,
-    or of chunk-aligned token ranges when B = 1 (each at least max(chunk, w) tokens so the
-    next segment's history lies inside its predecessor), at most ``pieces`` of them and,
-    when ``min_piece_bytes`` > 0, none moving fewer bytes than that."""
-    if min_piece_bytes > 0:
-        pieces = max(1, min(pieces, moved_bytes // min_piece_bytes))
-    if B > 1:
-        n = min(pieces, B)
-        step = -(-B // n)
-        return [(b0, min(b0 + step, B)) for b0 in range(0, B, step)]
-    n = max(1, min(pieces, T // max(chunk, w)))
-    step = -(-T // n)
-    step = -(-step // chunk) * chunk
-    return [(t0, min(t0 + step, T)) for t0 in range(0, T, step)]
+def plan_pieces(dims: Dims, pieces=8, min_piece_bytes=32 << 20):
+    """How prism_forward_host cuts the work for these dims: a list of (start, end) ranges of
+    sequences when B > 1, or of chunk-aligned token ranges when B = 1 (each at least
+    max(chunk, w) tokens so the next segment's history lies inside its predecessor), at
+    most ``pieces`` of them and, when ``min_piece_bytes`` > 0, none moving fewer bytes
+    than that."""
+    n = ctypes.c_int(0)
+    bounds = (ctypes.c_int * (pieces + 1))()
+    _check(load().prism_host_plan(ctypes.byref(dims), pieces, min_piece_bytes, ctypes.byref(n), bounds))
+    return [(bounds[i], bounds[i + 1]) for i in range(n.value)]
+
+
+def host_arena_bytes(dims: Dims, pieces=8, min_piece_bytes=32 << 20) -> int:
+    return int(load().prism_host_arena_bytes(ctypes.byref(dims), pieces, min_piece_bytes))
+
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.is_cuda or not t.is_contiguous():
+        raise PrismError(1, "host buffers must be contiguous CPU tensors")
+    return t.data_ptr()
 
 
 class HostPipeline:
-    """The forward pass from host (pinned) inputs to host outputs, with the copies overlapped
-    with the kernels: the work is cut into pieces (groups of sequences when B > 1; token
-    segments when B = 1, each resumed from the previous segment's final state and its last
-    w v rows with prism_forward_from), copied in on one stream, computed on a second and
-    copied out on a third.  Device buffers, streams and the workspace are kept across calls.
+    """The forward pass from host (pinned) inputs to host outputs through prism_forward_host:
+    the library cuts the work into pieces (groups of sequences when B > 1; token segments
+    when B = 1, each resumed from the previous segment's final state and its last w v rows)
+    and overlaps the copies in, the kernels and the copies out on three streams.  The device
+    arena and the streams are kept across calls.
     """
 
     def __init__(self, shapes: dict, dtype, L, chunk, *, pieces=8, device="cuda", no_gelu=False,
                  min_piece_bytes=32 << 20):
-        self.L, self.chunk, self.no_gelu = L, chunk, no_gelu
-        self.dev = torch.device(device)
         B, T, H, D = shapes["q"]
-        # pieces small enough to overlap, large enough that copies and launches stay efficient
-        moved = B * T * H * D * (3 * torch.tensor([], dtype=dtype).element_size() + 4)
-        self.pieces = plan_pieces(B, T, chunk, shapes["conv_w"][1], moved, pieces, min_piece_bytes)
-        step = max(a1 - a0 for a0, a1 in self.pieces)
-        self.B, self.T, self.H, self.D = B, T, H, D
-        self.w = shapes["conv_w"][1]
-        self.buf = {n: torch.empty(shp, dtype=(dtype if n in ("q", "k", "v") else torch.float32),
-                                   device=self.dev) for n, shp in shapes.items() if n != "seq_lens"}
-        self.out = torch.empty((B, T, H, D), dtype=torch.float32, device=self.dev)
-        self.states = [torch.empty((B, H, D, D), dtype=torch.float32, device=self.dev) for _ in range(2)]
-        if B > 1:
-            pdims = make_dims(step, T, H, D, D, self.w, L, chunk, dtype, no_gelu)
-        else:
-            pdims = make_dims(1, step, H, D, D, self.w, L, chunk, dtype, no_gelu, PRISM_FLAG_VHIST_TOKEN_MAJOR)
-        self.ws = alloc_workspace(pdims, self.dev)
-        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(self.dev) for _ in range(3))
-        self.ev_in = [torch.cuda.Event() for _ in self.pieces]
-        self.ev_comp = [torch.cuda.Event() for _ in self.pieces]
-        self.lens_dev = None                        # one buffer per piece (16-byte aligned)
-
-    def _run_one(self, host, host_out, host_fs, stream):
-        b = self.buf
-        with torch.cuda.stream(stream):
-            for n in ("q", "k", "v", "log_alpha", "beta", "conv_w", "Wk", "Wp", "wbeta"):
-                b[n].copy_(host[n], non_blocking=True)
-            lens = host.get("seq_lens")
-            lv = None
-            if lens is not None:
-                if self.lens_dev is None:
-                    self.lens_dev = [torch.empty(tuple(lens.shape), dtype=torch.int32, device=self.dev)]
-                self.lens_dev[0].copy_(lens, non_blocking=True)
-                lv = self.lens_dev[0]
-            prism_forward(b["q"], b["k"], b["v"], b["log_alpha"], b["beta"], b["conv_w"], b["Wk"],
-                          b["Wp"], b["wbeta"], self.L, self.chunk, out=self.out, final_state=self.states[0],
-                          seq_lens=lv, workspace=self.ws, stream=stream, no_gelu=self.no_gelu)
-            host_out.copy_(self.out, non_blocking=True)
-            host_fs.copy_(self.states[0], non_blocking=True)
+        self.dev = torch.device(device)
+        self.dims = make_dims(B, T, H, D, D, shapes["conv_w"][1], L, chunk, dtype, no_gelu)
+        self.max_pieces, self.min_piece_bytes = pieces, min_piece_bytes
+        self.pieces = plan_pieces(self.dims, pieces, min_piece_bytes)
+        nbytes = host_arena_bytes(self.dims, pieces, min_piece_bytes)
+        if nbytes == 0:
+            raise PrismError(2, "HostPipeline: unsupported dims")
+        self.arena = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+        self.streams = [torch.cuda.Stream(self.dev) for _ in range(3)]
 
     def h2d_bytes(self, host: dict) -> int:
         return sum(t.numel() * t.element_size() for n, t in host.items() if t is not None)
@@ -413,54 +401,20 @@ class HostPipeline:
         host_fs [B,H,D,D] fp32 pinned.  Ordered after ``stream`` (default: current) and
         finished before later work on it."""
         caller = stream or torch.cuda.current_stream(self.dev)
-        if len(self.pieces) == 1:                  # nothing to overlap: one stream, no events
-            return self._run_one(host, host_out, host_fs, caller)
-        start = torch.cuda.Event()
-        start.record(caller)
-        for s in (self.s_in, self.s_comp, self.s_out):
-            s.wait_event(start)
-        b = self.buf
-        lens = host.get("seq_lens")
-        with torch.cuda.stream(self.s_in):
-            for n in ("conv_w", "Wk", "Wp", "wbeta"):
-                b[n].copy_(host[n], non_blocking=True)
-            if lens is not None and self.B > 1:
-                if self.lens_dev is None:
-                    self.lens_dev = [torch.empty((a1 - a0,), dtype=torch.int32, device=self.dev)
-                                     for a0, a1 in self.pieces]
-                for (a0, a1), buf in zip(self.pieces, self.lens_dev):
-                    buf.copy_(lens[a0:a1], non_blocking=True)
-        for i, (a0, a1) in enumerate(self.pieces):
-            sl = (slice(a0, a1),) if self.B > 1 else (slice(None), slice(a0, a1))
-            with torch.cuda.stream(self.s_in):
-                for n in ("q", "k", "v", "log_alpha", "beta"):
-                    b[n][sl].copy_(host[n][sl], non_blocking=True)
-                self.ev_in[i].record(self.s_in)
-            self.s_comp.wait_event(self.ev_in[i])
-            with torch.cuda.stream(self.s_comp):
-                if self.B > 1:
-                    lv = self.lens_dev[i] if lens is not None else None
-                    prism_forward(b["q"][sl], b["k"][sl], b["v"][sl], b["log_alpha"][sl], b["beta"][sl],
-                                  b["conv_w"], b["Wk"], b["Wp"], b["wbeta"], self.L, self.chunk,
-                                  out=self.out[sl], final_state=self.states[0][a0:a1], seq_lens=lv,
-                                  workspace=self.ws, stream=self.s_comp, no_gelu=self.no_gelu)
-                else:
-                    if lens is not None:
-                        raise PrismError(1, "HostPipeline: seq_lens with B = 1 is not supported")
-                    hist = b["v"][:, a0 - self.w:a0] if a0 >= self.w else None
-                    prism_forward_from(b["q"][sl], b["k"][sl], b["v"][sl], b["log_alpha"][sl],
-                                       b["beta"][sl], b["conv_w"], b["Wk"], b["Wp"], b["wbeta"],
-                                       self.L, self.chunk,
-                                       initial_state=self.states[i % 2] if i > 0 else None,
-                                       v_hist=hist, v_hist_token_major=True, out=self.out[sl],
-                                       final_state=self.states[(i + 1) % 2], workspace=self.ws,
-                                       stream=self.s_comp, no_gelu=self.no_gelu)
-                self.ev_comp[i].record(self.s_comp)
-            self.s_out.wait_event(self.ev_comp[i])
-            with torch.cuda.stream(self.s_out):
-                host_out[sl].copy_(self.out[sl], non_blocking=True)
-        with torch.cuda.stream(self.s_out):
-            fs = self.states[0] if self.B > 1 else self.states[len(self.pieces) % 2]
-            host_fs.copy_(fs, non_blocking=True)
-        for s in (self.s_in, self.s_comp, self.s_out):
-            caller.wait_stream(s)
+        if len(self.pieces) == 1:                  # one piece: everything on the caller's stream
+            handles = (ctypes.c_void_p * 3)(*([caller.cuda_stream] * 3))
+        else:
+            for s in self.streams:
+                s.wait_stream(caller)
+            handles = (ctypes.c_void_p * 3)(*[s.cuda_stream for s in self.streams])
+        with torch.cuda.device(self.dev):         # the library's events live on this device
+            rc = load().prism_forward_host(
+                ctypes.byref(self.dims), _host_ptr(host["q"]), _host_ptr(host["k"]), _host_ptr(host["v"]),
+                _host_ptr(host["log_alpha"]), _host_ptr(host["beta"]), _host_ptr(host.get("conv_w")),
+                _host_ptr(host.get("Wk")), _host_ptr(host.get("Wp")), _host_ptr(host.get("wbeta")),
+                _host_ptr(host_out), _host_ptr(host_fs), _host_ptr(host.get("seq_lens")),
+                self.max_pieces, self.min_piece_bytes, self.arena.data_ptr(), self.arena.numel(),
+                handles)
+        _check(rc)
+        if len(self.pieces) > 1:
+            caller.wait_stream(self.streams[2])
