@@ -275,3 +275,32 @@ def test_chunk_adjoint_dot_product():
     an = sum(np.sum(r[key] * dx[key]) for key in x)
     an += sum(np.sum(r["Kl"][l] * dKl[l]) + np.sum(r["Dl"][l] * dDl[l]) for l in range(L))
     assert abs(fd - an) <= 1e-7 * max(abs(an), 1.0), (fd, an)
+
+
+def test_reverse_chain_has_the_forward_scan_form():
+    """The serial part of the chunked backward is the forward scan's state update run
+    backwards with the same per-chunk factors: with W = T diag(beta gamma) K,
+    Qt = diag(gamma) Q - tril(Q K^T (.) Gamma) W and Kt = diag(lambda) K (the factors the
+    forward's prepare stage computes),
+        dS0 = gamma_C dS1 - (Kt dS1^T)^T W + dO^T Qt,
+    i.e. dS0 = dS1 M^T + dO^T Qt with M = gamma_C I - W^T Kt the forward chunk map.  Every
+    other gradient of the chunk is then state-parallel given S0 and dS1."""
+    rng = np.random.default_rng(9)
+    for n, dk, dv, L in [(8, 4, 5, 2), (16, 6, 6, 0), (5, 3, 4, 3)]:
+        Q, K = rng.standard_normal((n, dk)), rng.standard_normal((n, dk)) / 2
+        V = rng.standard_normal((n, dv))
+        be = 1 / (1 + np.exp(-rng.standard_normal(n)))
+        la = -np.log1p(np.exp(rng.standard_normal(n))) / 8
+        Kl = [rng.standard_normal((n, dk)) / 2 for _ in range(L)]
+        Dl = [rng.standard_normal((n, dv)) for _ in range(L)]
+        S0 = rng.standard_normal((dv, dk))
+        dO, dS1 = rng.standard_normal((n, dv)), rng.standard_normal((dv, dk))
+        r = chunk_backward(S0, Q, K, V, be, la, Kl, Dl, dO, dS1)
+        _, _, f = chunk_forward(S0, Q, K, V, be, la, Kl, Dl)
+        W, gam, lam = f["W"], f["gam"], f["lam"]
+        Qt = gam[:, None] * Q - f["QK"] @ W
+        Kt = lam[:, None] * K
+        dS0 = gam[-1] * dS1 - (Kt @ dS1.T).T @ W + dO.T @ Qt
+        np.testing.assert_allclose(r["S0"], dS0, rtol=0, atol=1e-12 * np.max(np.abs(dS0)))
+        M = gam[-1] * np.eye(dk) - W.T @ Kt
+        np.testing.assert_allclose(dS1 @ M.T + dO.T @ Qt, dS0, rtol=0, atol=1e-12 * np.max(np.abs(dS0)))
