@@ -47,6 +47,10 @@ def make(name, shape, seed, lens, identity_act, resumed):
         extra["v_hist"] = g.standard_normal((B, H, w, dv))
     out, fs, _ = oracle.forward(inp, identity_act=identity_act, **extra)
     rec = {
+        "source": ("written by tests/golden/make_golden.py from the fp64 oracle (oracle.forward"
+                   + ("" if resumed else ", oracle.grad.backward") + "); the method is the PRISM "
+                   "mixer of 'Technical Summary: PRISM (Parallel Residual Iterative Sequence "
+                   "Model)', sections 2.1 and 2.2, which prints no worked example"),
         "shape": dict(zip(("B", "T", "H", "dk", "dv", "L", "w"), shape)),
         "identity_act": identity_act,
         "inputs": {k: (v.tolist() if k == "seq_lens" else _listed(v.numpy()))

@@ -37,9 +37,11 @@ def _load(path):
     return rec, inp
 
 
-def test_fixtures_present():
+def test_fixtures_present_and_cited():
     names = {os.path.basename(p) for p in GOLDEN}
     assert {"prism_tiny.json", "prism_tiny_no_gelu.json", "prism_tiny_resumed.json"} <= names
+    for p in GOLDEN:
+        assert "Technical Summary: PRISM" in json.load(open(p))["source"]
 
 
 @pytest.mark.parametrize("path", GOLDEN, ids=os.path.basename)
