@@ -87,6 +87,19 @@ MUTANTS = [
     ("padding_processed", "if (t >= len) {", "if (0) {"),
     ("r1_without_anchor", "r[i] = vt[i] - u[i];", "r[i] = vt[i];"),
     ("output_before_update", _UPDATE + _READOUT, _READOUT + _UPDATE),
+    ("padding_output_not_zeroed", "for (int i = 0; i < dv; ++i) o[i] = 0.0;\n            continue;",
+     "continue;"),
+    ("initial_state_of_other_pair", "P->initial_state + ((size_t)b * P->H + h) * dv * dk",
+     "P->initial_state + ((size_t)h * P->B + b) * dv * dk"),
+    ("final_state_to_other_pair", "P->final_state + ((size_t)b * P->H + h) * dv * dk",
+     "P->final_state + ((size_t)h * P->B + b) * dv * dk"),
+    ("norm_eps_1e-12", "#define NORM_EPS 1e-6", "#define NORM_EPS 1e-12"),
+    ("history_of_head_zero", "(((size_t)b * P->H + h) * w + (w + t - j)) * dv",
+     "(((size_t)b * P->H + 0) * w + (w + t - j)) * dv"),
+    ("gate_with_bias", "const double bl = sigmoid(z);", "const double bl = sigmoid(z + 0.5);"),
+    ("residual_added", "r[i] -= dl[i];", "r[i] += dl[i];"),
+    ("direction_normalised_twice", "for (int a = 0; a < dk; ++a) kk[a] *= inv;",
+     "for (int a = 0; a < dk; ++a) kk[a] *= inv * inv;"),
 ]
 
 
