@@ -84,3 +84,38 @@ def test_arena_and_argument_errors(_lib):
     assert call(host, 0x100000, n_ok - 1) == 4
     assert call(host, None, n_ok) == 4
     assert call(host, 0x100080, n_ok) == 3
+
+
+def test_plan_properties_over_random_dims():
+    """For random supported dims: the pieces tile the work, stay within max_pieces, groups
+    of sequences start 16-byte aligned in the gate arrays, token segments are chunk-aligned
+    and hold at least max(chunk, w) tokens (but the last), and the arena is at least the
+    full-size inputs and outputs."""
+    hyp = pytest.importorskip("hypothesis")
+    st = pytest.importorskip("hypothesis.strategies")
+
+    @hyp.settings(max_examples=300, deadline=None)
+    @hyp.given(B=st.integers(1, 64), T=st.integers(1, 5000), H=st.integers(1, 8),
+               D=st.sampled_from([16, 32, 64, 128]), chunk=st.sampled_from([16, 32, 64]),
+               w=st.integers(1, 8), L=st.integers(0, 8), pieces=st.integers(1, 16),
+               floor=st.sampled_from([0, 1 << 16, 32 << 20]), f32=st.booleans())
+    def check(B, T, H, D, chunk, w, L, pieces, floor, f32):
+        if f32 and D > 64:
+            D = 64
+        d = prism.make_dims(B, T, H, D, D, w, L, chunk, prism.PRISM_F32 if f32 else prism.PRISM_BF16)
+        p = prism.plan_pieces(d, pieces, floor)
+        n = B if B > 1 else T
+        _covers(p, n)
+        assert 1 <= len(p) <= pieces
+        if B > 1:
+            for a0, _ in p:
+                assert (a0 * T * H * 4) % 16 == 0
+        else:
+            for a0, a1 in p[:-1]:
+                assert (a1 - a0) % chunk == 0 and a1 - a0 >= max(chunk, w)
+        esz = 4 if f32 else 2
+        arena = prism.host_arena_bytes(d, pieces, floor)
+        assert arena % 256 == 0
+        assert arena >= B * T * H * D * (3 * esz + 4) + B * T * H * 8
+
+    check()
