@@ -60,6 +60,8 @@ typedef enum { PRISM_F32 = 0, PRISM_BF16 = 1 } prism_dtype;
 #define PRISM_FLAG_VHIST_TOKEN_MAJOR 2u  /* prism_forward_from: v_hist is [B,w,H,d_v], the layout of
                                             v itself (so the last w token rows of the previous
                                             segment's v serve directly when B = 1) */
+#define PRISM_FLAG_NO_SEQ_SPLIT 4u  /* run the scan as one serial chain per sequence even where
+                                       prism_scan_segments() would cut it (see there) */
 
 typedef struct {
     int B, T, H;          /* batch, sequence length, heads */
@@ -97,7 +99,10 @@ enum {
     PRISM_WS_OI = 7,       /*   O_intra = P U + O_l                              [C,d]  fp32 */
     PRISM_WS_N = 8,        /*   N^T, N = sum_l D_l^T diag(gamma_C/gamma) K_l     [d,d]  fp32 */
     PRISM_WS_GC = 9,       /*   gamma_C, [B,H,NC]                                       fp32 */
-    PRISM_WS_COUNT = 10
+    PRISM_WS_SEG = 10,     /* sequence split only (prism_scan_segments() = P > 1): three arrays
+                              [B,H,P,d,d] fp32 — each segment's entering state, and the c and M
+                              of its affine map S_end = S_start M + c */
+    PRISM_WS_COUNT = 11
 };
 
 /* Inside one chunk, the PRISM_BF16 per-chunk arrays (R rows x d features) are
@@ -108,7 +113,10 @@ enum {
  * Qt hi (resp. Kt), so W(r, f) is at ((f / 8) * 2C + r) * 8 + f % 8 and
  * Qt_hi(r, f) at ((f / 8) * 2C + C + r) * 8 + f % 8. */
 
-/* Bytes of device workspace for these dims (0 if the dims are invalid). */
+/* Bytes of device workspace for these dims (0 if the dims are invalid).  The
+ * workspace holds each chunk's factored state map: the chunkwise form of the
+ * recurrence S_t = S_{t-1} A_t + B_t ("Technical Summary: PRISM", §2.1), whose
+ * state-independent part (§2.2, last paragraph) is what allows a parallel scan. */
 PRISM_API size_t prism_workspace_bytes(const prism_dims* dims);
 
 /* Byte offset of each PRISM_WS_* region inside the workspace (SIZE_MAX when the
@@ -150,7 +158,8 @@ PRISM_API int prism_forward_from(const prism_dims* dims,
                                  float* out, float* final_state, const int32_t* seq_lens,
                                  void* workspace, size_t workspace_bytes, void* stream);
 
-/* The device status word of the last prism_forward / prism_forward_from /
+/* (No counterpart in the pages: failure detection of this library.)
+ * The device status word of the last prism_forward / prism_forward_from /
  * prism_prepare + prism_scan call that used this workspace (same dims).  Every
  * wait those kernels make on an mbarrier is bounded; one that gives up writes a
  * nonzero word instead of hanging, and that call's outputs are then invalid.
@@ -183,7 +192,9 @@ PRISM_API int prism_decode_step(const prism_dims* dims,
                                 const float* wbeta,
                                 float* state, void* v_hist, float* out, void* stream);
 
-/* State-independent stage (fully parallel over chunks): anchor, refinement and,
+/* State-independent stage (fully parallel over chunks; "Technical Summary:
+ * PRISM", §2.2 stages 1-2 and the state-independence noted at its end):
+ * anchor, refinement and,
  * on the PRISM_BF16 path, each chunk's factored affine state map; results go
  * to the workspace regions listed above. */
 PRISM_API int prism_prepare(const prism_dims* dims,
@@ -193,7 +204,22 @@ PRISM_API int prism_prepare(const prism_dims* dims,
                             const float* wbeta, const int32_t* seq_lens,
                             void* workspace, size_t workspace_bytes, void* stream);
 
-/* Serial stage: the chunk-to-chunk state chain and the outputs, from a
+/* Number of segments P the scan cuts each sequence into (1: one serial chain).
+ * The chunk chain is serial in time, so few long sequences (a small B*H) leave most
+ * of the GPU idle.  Each chunk acts on the state as an affine map S1 = S0 M + c
+ * ("Technical Summary: PRISM", §2.2, last paragraph: the update is state-independent,
+ * the condition for parallel prefix scanning), so a segment of chunks composes to
+ * one such map.  With P > 1 the scan runs: segment 0 in full and, in parallel, the
+ * (M, c) of every later segment; the entering states chained segment to segment;
+ * segments 1..P-1 in full from them.  About twice the chain work, P-fold shorter.
+ * P > 1 only on the PRISM_BF16 path with d = 128 and chunk 32 or 64, without
+ * PRISM_FLAG_NO_SEQ_SPLIT, when the first pass fits one wave of CTAs
+ * (B*H*4*(2P-1) <= 152) with P >= 3 and at least 8 chunks per segment; P <= 16.
+ * A function of the dims alone.  Returns 0 for invalid dims. */
+PRISM_API int prism_scan_segments(const prism_dims* dims);
+
+/* Serial stage ("Technical Summary: PRISM", §2.1: S_t = S_{t-1} A_t + B_t,
+ * composed chunk to chunk): the state chain and the outputs, from a
  * workspace filled by prism_prepare with the same dims and inputs. */
 PRISM_API int prism_scan(const prism_dims* dims,
                          const void* q, const void* k, const void* v,
@@ -216,9 +242,13 @@ PRISM_API int prism_scan(const prism_dims* dims,
  *   - Dims whose prism_workspace_bytes() exceeds PRISM_STATIC_SCRATCH_BYTES
  *     are rejected with PRISM_ERR_SCRATCH_LIMIT before anything is launched.
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on each device looks up the array's device address with
- *     that device current (cudaGetSymbolAddress); make that first call before
- *     any stream capture on the device.
+ *   - Every call looks up the array's device address with the caller's device
+ *     current (cudaGetSymbolAddress; not cached, so a device reset or a new
+ *     context cannot leave a stale address behind).  The first call on a
+ *     device may load the library's device code: make it before any stream
+ *     capture on that device.
+ *   - The bounded-wait status word of these calls lives in the library's own
+ *     array; prism_device_status does not read it.
  *   - All calls on a device share the array and it keeps the last call's
  *     contents.  Calls that overlap on the GPU (other streams, or threads
  *     without ordering between their launches) race on it: serialise them. */

@@ -30,13 +30,35 @@ cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// The scan: one chain per sequence (a.nseg <= 1), or the sequence split in three
+// launches (affine maps, entering states, final pass; see scan_tc.cuh).
 template <int C>
 cudaError_t launch_scan_tc_t(const ScanTcArgs& a, cudaStream_t s) {
   using S = ScanTcSmem<C>;
   auto fn = scan_tc_kernel<C>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
   if (e != cudaSuccess) return e;
-  fn<<<a.B * a.H * (S::D / S::BV), S::NT, S::bytes, s>>>(a);
+  const int NSL = S::D / S::BV, BH = a.B * a.H;
+  if (a.nseg <= 1) {
+    ScanTcArgs p0 = a;
+    p0.phase = 0;
+    fn<<<BH * NSL, S::NT, S::bytes, s>>>(p0);
+    return cudaGetLastError();
+  }
+  ScanTcArgs p1 = a;
+  p1.phase = 1;
+  fn<<<BH * NSL * (1 + 2 * (a.nseg - 1)), S::NT, S::bytes, s>>>(p1);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.nseg > 2) {
+    auto fc = scan_seg_chain_kernel<S::D>;
+    e = cudaFuncSetAttribute(fc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SegChainSmem<S::D>::bytes);
+    if (e != cudaSuccess) return e;
+    fc<<<BH * (S::D / kSegRows), 256, SegChainSmem<S::D>::bytes, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  ScanTcArgs p3 = a;
+  p3.phase = 3;
+  fn<<<BH * NSL * (a.nseg - 1), S::NT, S::bytes, s>>>(p3);
   return cudaGetLastError();
 }
 

@@ -126,7 +126,8 @@ int check_dims(const prism_dims* d) {
   if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->d_k <= 0 || d->d_v <= 0 || d->L < 0 ||
       d->conv_width <= 0 || d->chunk <= 0)
     return PRISM_ERR_INVALID_ARG;
-  if (d->flags & ~(PRISM_FLAG_NO_GELU | PRISM_FLAG_VHIST_TOKEN_MAJOR)) return PRISM_ERR_INVALID_ARG;
+  if (d->flags & ~(PRISM_FLAG_NO_GELU | PRISM_FLAG_VHIST_TOKEN_MAJOR | PRISM_FLAG_NO_SEQ_SPLIT))
+    return PRISM_ERR_INVALID_ARG;
   if (d->d_k != d->d_v) return PRISM_ERR_UNSUPPORTED;
   const int D = d->d_k, C = d->chunk;
   if (D != 16 && D != 32 && D != 64 && D != 128) return PRISM_ERR_UNSUPPORTED;
@@ -147,6 +148,22 @@ struct Layout {
   size_t off[PRISM_WS_COUNT];
   size_t total;
 };
+
+// Segments of the sequence split (1: none).  The first pass runs B*H*4*(2P-1) CTAs of
+// one per SM (segment 0 in full, the c and M rows of every later one): it must fit one
+// wave of the 152 SMs, and each segment keeps at least kMinSegChunks chunks.  Time goes
+// as about 2/P of the serial chain's, so P = 2 gains nothing and is not taken.
+constexpr int kScanSMs = 152, kMaxSeg = 16, kMinSegChunks = 8;
+int scan_segments(const prism_dims* d) {
+  if (d->dtype != PRISM_BF16 || d->d_k != 128 || (d->chunk != 32 && d->chunk != 64)) return 1;
+  if (d->flags & PRISM_FLAG_NO_SEQ_SPLIT) return 1;
+  const long long ctas = (long long)d->B * d->H * 4;
+  const int NC = (d->T + d->chunk - 1) / d->chunk;
+  int P = 1;
+  for (int q = 3; q <= kMaxSeg; ++q)
+    if (ctas * (2 * q - 1) <= kScanSMs && NC >= q * kMinSegChunks) P = q;
+  return P;
+}
 
 Layout layout(const prism_dims* d) {
   Layout Lo;
@@ -173,6 +190,8 @@ Layout layout(const prism_dims* d) {
     take(PRISM_WS_OI, per * 4);
     if (d->L > 0) take(PRISM_WS_N, (size_t)d->B * d->H * NC * D * D * 4);
     take(PRISM_WS_GC, (size_t)d->B * d->H * NC * 4);
+    const int P = scan_segments(d);
+    if (P > 1) take(PRISM_WS_SEG, 3 * (size_t)d->B * d->H * P * D * D * 4);
   }
   Lo.total = cur;
   return Lo;
@@ -211,6 +230,11 @@ int pick_bv(const prism_dims* d) {
 extern "C" PRISM_API size_t prism_workspace_bytes(const prism_dims* dims) {
   if (check_dims(dims) != PRISM_OK) return 0;
   return layout(dims).total;
+}
+
+extern "C" PRISM_API int prism_scan_segments(const prism_dims* dims) {
+  if (check_dims(dims) != PRISM_OK) return 0;
+  return scan_segments(dims);
 }
 
 extern "C" PRISM_API int prism_workspace_layout(const prism_dims* dims, size_t* offsets, int n) {
@@ -337,6 +361,14 @@ int scan_impl(const prism_dims* dims, const void* q, const void* k, const void* 
     a.gC = region<const float>(workspace, Lo, PRISM_WS_GC);
     a.seq_lens = seq_lens; a.out = out; a.final_state = final_state; a.initial_state = initial_state;
     a.status = region<int>(workspace, Lo, PRISM_WS_STATUS);
+    a.nseg = scan_segments(dims);
+    a.phase = 0;
+    a.seg_chunks = (int)(((dims->T + C - 1) / C + a.nseg - 1) / a.nseg);
+    float* seg = region<float>(workspace, Lo, PRISM_WS_SEG);
+    const size_t per = (size_t)dims->B * dims->H * a.nseg * D * D;
+    a.seg_start = seg;
+    a.seg_c = seg ? seg + per : nullptr;
+    a.seg_M = seg ? seg + 2 * per : nullptr;
     return prism::launch_scan_tc_128(C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
   }
   prism::ScanArgs a;

@@ -14,31 +14,22 @@
 // ordering) race on it and must be serialised by the caller.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "../../include/prism.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_scratch[PRISM_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_ptr[kMaxDevices] = {};
-
-// Device address of g_scratch on the current device (looked up once per
-// device, with that device current).  In host code g_scratch itself only
-// names a host-side stand-in, so the address must come from the runtime.
+// Device address of g_scratch on the current device, looked up on every call with
+// that device current.  In host code g_scratch only names a host-side stand-in, so
+// the address must come from the runtime; it is not cached, because the module can
+// be loaded again at another address (after cudaDeviceReset, or in another context
+// on the same device) and a stale address would send the kernels to memory this
+// library no longer owns.  Once the module is loaded the lookup is a table read.
 int scratch_for_current_device(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PRISM_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return PRISM_ERR_CUDA;
-    g_ptr[dev] = p;
-  }
-  *out = g_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return PRISM_ERR_CUDA;
+  *out = p;
   return PRISM_OK;
 }
 

@@ -15,6 +15,17 @@
 // which is exactly the K-major (resp. MN-major) operand layout, so every chunk is
 // five bulk copies into a double buffer.
 //
+// Sequence split (long sequences with few (b, h) pairs): the chunk chain of a sequence
+// is cut into nseg segments of seg_chunks chunks.  Because each chunk acts on the state
+// as an affine map, S1 = S0 M + c with M = gamma_C I - W^T Kt and c = U^T Kt + N (the
+// state independence of "Technical Summary: PRISM", §2.2, last paragraph), a segment
+// composes to one such map.  Phase 1 runs segment 0 in full (its end state is segment
+// 1's entering state) and, for every later segment, the same chain twice over: from a
+// zero state with U and N (the rows of c) and from the identity without them (the rows
+// of M, which evolve exactly like state rows).  scan_seg_chain_kernel then chains the
+// entering states S_(s+1) = S_s M_s + c_s, and phase 3 runs segments 1.. in full from
+// them.  Rows of the state are independent, so the M rows split over CTAs like S rows.
+//
 // Threads: warps 0..7 read TMEM lane quarter w % 4 and column half w / 4 (16 of the
 // slice's BV = 32 columns); thread (k, half) keeps those 16 entries of row k of S^T in
 // fp32 registers across chunks.  Warp 8 issues the copies and the MMAs.
@@ -38,6 +49,13 @@ struct ScanTcArgs {
   float* final_state;    // [B][H][d_v][d_k] or null
   const float* initial_state;   // [B][H][d_v][d_k] entering state, or null (zero)
   int* status;           // device error word (bounded waits)
+  // Sequence split.  phase 0: one chain per sequence (nseg = 1); phase 1: segment 0 in
+  // full plus the affine maps of segments 1..nseg-1; phase 3: segments 1..nseg-1 in full
+  // from seg_start.  Arrays [B][H][nseg][D][D], rows d_v (or, for seg_M, d_k) by d_k.
+  int nseg, seg_chunks, phase;
+  float* seg_start;      // entering state of each segment (slot 0 unused)
+  float* seg_c;          // c of each segment (slot 0 unused)
+  float* seg_M;          // M of each segment (slot 0 unused)
 };
 
 template <int C>
@@ -80,14 +98,32 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
   float* sX = reinterpret_cast<float*>(sm + S::oX);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slice = blockIdx.x % NSL, bh = blockIdx.x / NSL;
+  // kind 0: the chain with outputs; 1: the rows of a segment's c; 2: the rows of its M
+  int slice = blockIdx.x % NSL, bh = blockIdx.x / NSL, seg = 0, kind = 0;
+  const int nseg = p.phase == 0 ? 1 : p.nseg;
+  if (p.phase == 1 && bh >= p.B * p.H) {
+    const int r = bh - p.B * p.H;
+    kind = 1 + r % 2;
+    seg = 1 + (r / 2) % (nseg - 1);
+    bh = (r / 2) / (nseg - 1);
+  } else if (p.phase == 3) {
+    seg = 1 + bh % (nseg - 1);
+    bh = bh / (nseg - 1);
+  }
+  const bool outputs = kind == 0, useU = kind != 2;
   const int h = bh % p.H, b = bh / p.H;
   const int v0 = slice * BV;
   const int H = p.H, T_ = p.T;
   const int NC = (T_ + C - 1) / C;
   const int len = p.seq_lens ? min(max(p.seq_lens[b], 0), T_) : T_;
-  const int nchunks = (len + C - 1) / C;
-  const size_t cb0 = ((size_t)b * H + h) * NC;
+  const int nchunks_seq = (len + C - 1) / C;
+  const int c_lo = p.phase == 0 ? 0 : min(seg * p.seg_chunks, nchunks_seq);
+  const int c_hi = p.phase == 0 ? nchunks_seq : min(c_lo + p.seg_chunks, nchunks_seq);
+  const int nchunks = c_hi - c_lo;             // chunks of this CTA's chain
+  const size_t cb0 = ((size_t)b * H + h) * NC + c_lo;
+  const bool last_seg = seg == nseg - 1;
+  const size_t seg_off = (((size_t)b * H + h) * nseg + seg) * D * D;
+  const float* useN = useU ? p.Nt : nullptr;
 
   if (tid == 0) {
     tc::bar_init(bar_full, 1);
@@ -113,12 +149,15 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
       auto load = [&](int c, int buf) {
         unsigned char* base = sm + (buf ? S::oBuf1 : S::oBuf0);
         const size_t cb = cb0 + c;
-        tc::bar_expect_tx(bar_full + buf, 2 * S::kMap + 2 * S::kU + (p.Nt ? S::kN : 0));
+        tc::bar_expect_tx(bar_full + buf, 2 * S::kMap + (useU ? S::kU : 0) + (outputs ? S::kU : 0) +
+                                              (useN ? S::kN : 0));
         tc::bulk_g2s(base + S::oWQ, p.WQ + cb * 2 * C * D, S::kMap, bar_full + buf);
         tc::bulk_g2s(base + S::oQK, p.QK + cb * 2 * C * D, S::kMap, bar_full + buf);
-        tc::bulk_g2s(base + S::oU, p.U + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, bar_full + buf);
-        tc::bulk_g2s(base + S::oOi, p.Oi + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, bar_full + buf);
-        if (p.Nt) tc::bulk_g2s(base + S::oN, p.Nt + cb * D * D + (size_t)(v0 / 4) * D * 4, S::kN, bar_full + buf);
+        if (useU)
+          tc::bulk_g2s(base + S::oU, p.U + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, bar_full + buf);
+        if (outputs)
+          tc::bulk_g2s(base + S::oOi, p.Oi + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, bar_full + buf);
+        if (useN) tc::bulk_g2s(base + S::oN, useN + cb * D * D + (size_t)(v0 / 4) * D * 4, S::kN, bar_full + buf);
       };
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         ok &= tc::bar_wait(bar, parity);
@@ -146,10 +185,12 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
           tc::mma(t_d3, tc::desc(base + S::oQK + C * 16 + kk * 256, 128, 2 * C * 16),
                   tc::desc(sE + kk * 256, 128, 16 * C), idesc_k, kk > 0);
         tc::commit(bar_mma2);
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma(t_d2, tc::desc(base + S::oQK + kk * 2 * (2 * C * 16), 2 * C * 16, 128),
-                  tc::desc(sS + kk * 256, 128, 16 * D), idesc_q1, kk > 0);
-        tc::commit(bar_mma1b);
+        if (outputs) {
+          for (int kk = 0; kk < D / 16; ++kk)
+            tc::mma(t_d2, tc::desc(base + S::oQK + kk * 2 * (2 * C * 16), 2 * C * 16, 128),
+                    tc::desc(sS + kk * 256, 128, 16 * D), idesc_q1, kk > 0);
+          tc::commit(bar_mma1b);
+        }
       }
     }
     __syncwarp();
@@ -159,9 +200,12 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
     const int hf = warp >> 2;                  // column half: slice columns hf*16 .. hf*16+15
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     float st[HB];                              // S^T[k][v0 + hf*16 ..]
-    const float* s0 = p.initial_state ? p.initial_state + ((size_t)b * H + h) * D * D : nullptr;
+    const float* s0 = kind != 0 ? nullptr
+                      : seg == 0 ? (p.initial_state ? p.initial_state + ((size_t)b * H + h) * D * D : nullptr)
+                                 : p.seg_start + seg_off;
 #pragma unroll
-    for (int v = 0; v < HB; ++v) st[v] = s0 ? s0[(size_t)(v0 + hf * HB + v) * D + k] : 0.f;
+    for (int v = 0; v < HB; ++v)
+      st[v] = s0 ? s0[(size_t)(v0 + hf * HB + v) * D + k] : (kind == 2 && v0 + hf * HB + v == k) ? 1.f : 0.f;
     auto write_state = [&]() {                 // [S_hi | S_lo]^T rows: (k, n) at (n/8)*16D + k*16 + (n%8)*2
 #pragma unroll
       for (int g = 0; g < HB / 8; ++g) {
@@ -187,7 +231,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
       const float* sOi = reinterpret_cast<const float*>(base + S::oOi);
       const float* sN = reinterpret_cast<const float*>(base + S::oN);
       const size_t cbase = cb0 + c;
-      const int t0 = c * C, nv = min(C, len - t0);
+      const int t0 = (c_lo + c) * C, nv = min(C, len - t0);
       const float gC = tc::ldg_early(p.gC + cbase);
       ok &= tc::bar_wait(bar_mma1, c & 1);
       tc::fence_after();
@@ -208,8 +252,8 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
             tc::pin(d1[2 + g]);
             const int pc = 4 * hf + 2 * g;     // U piece (4 columns) of this group
             float uu[8], e8[8];
-            const float4 u0 = *reinterpret_cast<const float4*>(sU + (pc * C + k) * 4);
-            const float4 u1 = *reinterpret_cast<const float4*>(sU + ((pc + 1) * C + k) * 4);
+            const float4 u0 = useU ? *reinterpret_cast<const float4*>(sU + (pc * C + k) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 u1 = useU ? *reinterpret_cast<const float4*>(sU + ((pc + 1) * C + k) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
             uu[0] = u0.x; uu[1] = u0.y; uu[2] = u0.z; uu[3] = u0.w;
             uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
 #pragma unroll
@@ -222,7 +266,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
             *reinterpret_cast<uint4*>(sE + n8 * (16u * C) + k * 16u) = hi;
             *reinterpret_cast<uint4*>(sE + (BV / 8 + n8) * (16u * C) + k * 16u) = lo;
           }
-        } else if (k < 2 * C) {
+        } else if (outputs && k < 2 * C) {
           const int r = k - C;
 #pragma unroll
           for (int g = 0; g < 2; ++g) {
@@ -258,7 +302,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
           tc::pin(d3[g]);
           tc::pin(d3[2 + g]);
           float nn[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (p.Nt) {
+          if (useN) {
             const int pc = 4 * hf + 2 * g;
             const float4 n0 = *reinterpret_cast<const float4*>(sN + (pc * D + k) * 4);
             const float4 n1 = *reinterpret_cast<const float4*>(sN + ((pc + 1) * D + k) * 4);
@@ -270,6 +314,10 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
             st[8 * g + j] = fmaf(gC, st[8 * g + j],
                                  (__uint_as_float(d3[g][j]) + __uint_as_float(d3[2 + g][j])) + nn[j]);
         }
+      }
+      if (!outputs) {                          // affine maps: state rows only
+        write_state();
+        continue;
       }
       // MMA1b (Qt_lo S0_hi^T) has read the state tile: the new state may replace it; the
       // Qt_lo rows go to the output rows through sX
@@ -305,13 +353,23 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
         }
       }
     }
-    // padded tokens: zero output columns of this slice
-    for (size_t idx = tid; idx < (size_t)(T_ - len) * BV; idx += NW * 32) {
-      const int t = len + (int)(idx / BV), col = (int)(idx % BV);
-      p.out[(((size_t)b * T_ + t) * H + h) * D + v0 + col] = 0.f;
+    // padded tokens of this chain's token range: zero output columns of this slice
+    if (outputs) {
+      const int t_lo = max(len, p.phase == 0 ? 0 : seg * p.seg_chunks * C);
+      const int t_hi = (p.phase == 0 || last_seg) ? T_ : min(T_, (seg + 1) * p.seg_chunks * C);
+      for (size_t idx = tid; idx < (size_t)max(t_hi - t_lo, 0) * BV; idx += NW * 32) {
+        const int t = t_lo + (int)(idx / BV), col = (int)(idx % BV);
+        p.out[(((size_t)b * T_ + t) * H + h) * D + v0 + col] = 0.f;
+      }
     }
-    if (p.final_state) {
-      float* fs = p.final_state + ((size_t)b * H + h) * D * D;
+    // end state: the final state (last segment), segment 1's entering state (segment 0 of
+    // phase 1), or the rows of c or M
+    float* fs = kind == 1 ? p.seg_c + seg_off
+              : kind == 2 ? p.seg_M + seg_off
+              : (p.phase == 0 || last_seg) ? (p.final_state ? p.final_state + ((size_t)b * H + h) * D * D : nullptr)
+              : p.phase == 1 ? p.seg_start + seg_off + (size_t)D * D
+              : nullptr;
+    if (fs) {
 #pragma unroll
       for (int v = 0; v < HB; ++v) fs[(size_t)(v0 + hf * HB + v) * D + k] = st[v];
     }
@@ -320,6 +378,57 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, 256);
+}
+
+// Phase 2 of the sequence split: the entering state of each segment,
+// S_(s+1) = S_s M_s + c_s for s = 1..nseg-2 (S_1 comes from phase 1's segment 0).
+// One CTA per (b, h) and 32 rows of the state (rows are independent); the rows stay
+// in shared memory from one segment to the next, M_s is staged whole.  fp32 FMA.
+constexpr int kSegRows = 32;
+template <int D>
+struct SegChainSmem {
+  static constexpr int LDS = D + 4;            // padded rows: the 4 rows of a warp hit 4 bank groups
+  static constexpr size_t bytes = (size_t)(kSegRows * LDS + D * D) * 4;
+};
+template <int D>
+__global__ void __launch_bounds__(256) scan_seg_chain_kernel(ScanTcArgs p) {
+  constexpr int LDS = SegChainSmem<D>::LDS, NSL = D / kSegRows;
+  extern __shared__ __align__(16) float smc[];
+  float* sS = smc;                             // [kSegRows][LDS]
+  float* sM = smc + kSegRows * LDS;            // [D][D]
+  const int slice = blockIdx.x % NSL, bh = blockIdx.x / NSL;
+  const int r0 = slice * kSegRows, tid = threadIdx.x;
+  const int row = tid / 8, cg = tid % 8;       // row r0 + row, columns cg + 8 i
+  const size_t base = (size_t)bh * p.nseg * D * D;
+  for (int i = tid; i < kSegRows * D / 4; i += 256) {
+    const int rr = i / (D / 4), c4 = i % (D / 4);
+    *reinterpret_cast<float4*>(sS + rr * LDS + 4 * c4) = *reinterpret_cast<const float4*>(
+        p.seg_start + base + (size_t)D * D + (size_t)(r0 + rr) * D + 4 * c4);
+  }
+  for (int s = 1; s + 1 < p.nseg; ++s) {
+    const float* M = p.seg_M + base + (size_t)s * D * D;
+    const float* cc = p.seg_c + base + (size_t)s * D * D + (size_t)r0 * D;
+    __syncthreads();                           // sS complete; the previous sM fully read
+    for (int i = tid; i < D * D / 4; i += 256)
+      reinterpret_cast<float4*>(sM)[i] = reinterpret_cast<const float4*>(M)[i];
+    __syncthreads();
+    float acc[D / 8];
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) acc[i] = cc[(size_t)row * D + cg + 8 * i];
+#pragma unroll 4
+    for (int j = 0; j < D; ++j) {
+      const float sv = sS[row * LDS + j];
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) acc[i] = fmaf(sv, sM[j * D + cg + 8 * i], acc[i]);
+    }
+    __syncthreads();                           // every thread has read its sS row
+    float* dst = p.seg_start + base + (size_t)(s + 1) * D * D + (size_t)r0 * D;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      sS[row * LDS + cg + 8 * i] = acc[i];
+      dst[(size_t)row * D + cg + 8 * i] = acc[i];
+    }
+  }
 }
 
 }  // namespace prism

@@ -72,6 +72,9 @@ WORKLOADS = {
                         chunk=64, seed=3, note="LM-shaped"),
     "longctx_bf16": Workload("longctx_bf16", "bf16", B=1, T=65536, H=32, dk=128, dv=128,
                              L=4, w=4, chunk=64, seed=4, note="long context"),
+    "longctx_h4_bf16": Workload("longctx_h4_bf16", "bf16", B=1, T=65536, H=4, dk=128, dv=128,
+                                L=4, w=4, chunk=64, seed=5,
+                                note="long context with few heads (the sequence-split scan)"),
 }
 
 

@@ -19,6 +19,7 @@ from . import build as _build
 PRISM_F32, PRISM_BF16 = 0, 1
 PRISM_FLAG_NO_GELU = 1
 PRISM_FLAG_VHIST_TOKEN_MAJOR = 2
+PRISM_FLAG_NO_SEQ_SPLIT = 4
 ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
           3: "PRISM_ERR_MISALIGNED", 4: "PRISM_ERR_WORKSPACE", 5: "PRISM_ERR_LAUNCH",
           6: "PRISM_ERR_CUDA", 7: "PRISM_ERR_SCRATCH_LIMIT"}
@@ -28,8 +29,8 @@ EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "
            "prism_scan", "prism_forward_static", "prism_strerror", "prism_forward_from",
            "prism_decode_step", "prism_backward_workspace_bytes", "prism_backward",
            "prism_device_status", "prism_host_plan", "prism_host_arena_bytes",
-           "prism_forward_host")
-WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC")
+           "prism_forward_host", "prism_scan_segments")
+WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC", "seg")
 
 
 class PrismError(RuntimeError):
@@ -96,6 +97,8 @@ def load():
                                                + [ctypes.c_int, ctypes.c_size_t, _vp, ctypes.c_size_t,
                                                   ctypes.POINTER(ctypes.c_void_p)])
             lib.prism_forward_host.restype = ctypes.c_int
+            lib.prism_scan_segments.argtypes = [ctypes.POINTER(Dims)]
+            lib.prism_scan_segments.restype = ctypes.c_int
             lib.prism_strerror.argtypes = [ctypes.c_int]
             lib.prism_strerror.restype = ctypes.c_char_p
             _lib = lib
@@ -127,6 +130,11 @@ def make_dims(B, T, H, d_k, d_v, conv_width, L, chunk, dtype, no_gelu=False, fla
 
 def workspace_bytes(dims: Dims) -> int:
     return int(load().prism_workspace_bytes(ctypes.byref(dims)))
+
+
+def scan_segments(dims: Dims) -> int:
+    """Segments the scan cuts each sequence of these dims into (1: one serial chain)."""
+    return int(load().prism_scan_segments(ctypes.byref(dims)))
 
 
 def _ptr(t):
@@ -170,7 +178,7 @@ def device_status(dims: Dims, workspace, stream=None) -> int:
 
 def prism_forward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, out=None,
                   final_state=None, seq_lens=None, workspace=None, stream=None,
-                  no_gelu=False, want_state=True):
+                  no_gelu=False, want_state=True, flags=0):
     """The mixer forward pass on CUDA tensors laid out as in include/prism.h.
 
     Returns ``(out, final_state)`` (out is fp32); ``final_state`` is None when
@@ -178,7 +186,7 @@ def prism_forward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, 
     """
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu)
+    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu, flags)
     if out is None:
         out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
     if final_state is None and want_state:
@@ -196,14 +204,14 @@ def prism_forward(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, 
 def prism_forward_from(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *,
                        initial_state=None, v_hist=None, out=None, final_state=None,
                        seq_lens=None, workspace=None, stream=None, no_gelu=False, want_state=True,
-                       v_hist_token_major=False):
+                       v_hist_token_major=False, flags=0):
     """prism_forward resuming from ``initial_state`` [B,H,dv,dk] fp32 and ``v_hist``
     [B,H,w,dv] (I/O dtype; the v rows of the w tokens before t = 0, oldest first), or
     [B,w,H,dv] (the layout of v) with ``v_hist_token_major``."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dims = _dims_for(q, v, conv_w, L, chunk, no_gelu,
-                     PRISM_FLAG_VHIST_TOKEN_MAJOR if v_hist_token_major else 0)
+                     (PRISM_FLAG_VHIST_TOKEN_MAJOR if v_hist_token_major else 0) | flags)
     if out is None:
         out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
     if final_state is None and want_state:
@@ -308,9 +316,9 @@ def prism_forward_static(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chu
 
 
 def prism_prepare(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, workspace, *,
-                  seq_lens=None, stream=None, no_gelu=False):
+                  seq_lens=None, stream=None, no_gelu=False, flags=0):
     """State-independent stage into ``workspace`` (see include/prism.h)."""
-    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu)
+    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu, flags)
     rc = load().prism_prepare(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                               _ptr(beta), _ptr(conv_w), _ptr(Wk), _ptr(Wp), _ptr(wbeta),
                               _ptr(seq_lens), _ptr(workspace), workspace.numel(),
@@ -320,11 +328,12 @@ def prism_prepare(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, wor
 
 
 def prism_scan(q, k, v, log_alpha, beta, L, chunk, conv_width, workspace, *, out=None,
-               final_state=None, seq_lens=None, stream=None, want_state=True, no_gelu=False):
+               final_state=None, seq_lens=None, stream=None, want_state=True, no_gelu=False,
+               flags=0):
     """Serial stage from a prepared workspace; returns (out, final_state)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    dims = make_dims(B, T, H, dk, dv, conv_width, L, chunk, q.dtype, no_gelu)
+    dims = make_dims(B, T, H, dk, dv, conv_width, L, chunk, q.dtype, no_gelu, flags)
     if out is None:
         out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
     if final_state is None and want_state:

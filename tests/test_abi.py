@@ -62,7 +62,7 @@ def _fwd(lib, dims, ptrs, ws=0):
 
 @pytest.mark.parametrize("field,value,code", [
     ("B", 0, 1), ("T", -1, 1), ("d_k", 48, 2), ("chunk", 48, 2), ("L", 9, 2),
-    ("conv_width", 9, 2), ("conv_width", 0, 1), ("dtype", 7, 1), ("flags", 4, 1)])
+    ("conv_width", 9, 2), ("conv_width", 0, 1), ("dtype", 7, 1), ("flags", 8, 1)])
 def test_bad_dims(lib, field, value, code):
     d = prism.make_dims(2, 64, 2, 64, 64, 4, 2, 64, prism.PRISM_BF16)
     if field == "d_k":
@@ -160,3 +160,39 @@ def test_device_status_argument_errors(lib):
     assert call(d, None, need) == 4
     assert call(d, 0x100000, need - 1) == 4
     assert word.value == -1
+
+
+def test_scan_segments_rule(lib):
+    """The sequence split is a function of the dims alone: taken only for the tcgen05
+    scan (bf16, d = 128, chunk 32 or 64) when the first pass of B*H*4*(2P-1) CTAs fits
+    the 152 SMs with P >= 3 and at least 8 chunks per segment; the workspace then
+    holds three [B,H,P,d,d] fp32 arrays."""
+    bf = prism.PRISM_BF16
+    seg = lambda *a, **k: prism.scan_segments(prism.make_dims(*a, **k))
+    assert seg(1, 65536, 32, 128, 128, 4, 4, 64, bf) == 1          # 128 scan CTAs: no room
+    assert seg(8, 4096, 16, 128, 128, 4, 2, 64, bf) == 1
+    assert seg(1, 65536, 4, 128, 128, 4, 4, 64, bf) == 5           # 16 x 9 = 144 <= 152
+    assert seg(1, 65536, 1, 128, 128, 4, 4, 64, bf) == 16          # capped
+    assert seg(1, 4096, 2, 128, 128, 4, 2, 64, bf) == 8            # 64 chunks / 8
+    assert seg(1, 1000, 1, 128, 128, 4, 2, 64, bf) == 1            # 16 chunks: too short
+    assert seg(1, 65536, 4, 128, 128, 4, 4, 64, bf, flags=prism.PRISM_FLAG_NO_SEQ_SPLIT) == 1
+    assert seg(1, 65536, 4, 64, 64, 4, 4, 64, bf) == 1             # d < 128: other scan kernel
+    assert seg(1, 65536, 4, 128, 128, 4, 4, 16, bf) == 1           # chunk 16: other scan kernel
+    assert seg(1, 4096, 1, 32, 32, 4, 2, 16, prism.PRISM_F32) == 1
+    assert seg(1, 64, 1, 100, 100, 4, 2, 16, bf) == 0              # invalid dims
+    for B, T, H in ((1, 65536, 4), (2, 3000, 1), (1, 4096, 2), (8, 4096, 16)):
+        for C in (32, 64):
+            d = prism.make_dims(B, T, H, 128, 128, 4, 2, C, bf)
+            P = prism.scan_segments(d)
+            NC = -(-T // C)
+            assert P == 1 or (P >= 3 and B * H * 4 * (2 * P - 1) <= 152 and NC >= 8 * P and P <= 16)
+            lay = prism.workspace_layout(d)
+            if P == 1:
+                assert lay["seg"] is None
+            else:
+                assert lay["seg"] % 256 == 0
+                assert prism.workspace_bytes(d) >= lay["seg"] + 3 * B * H * P * 128 * 128 * 4
+                nosplit = prism.make_dims(B, T, H, 128, 128, 4, 2, C, bf,
+                                          flags=prism.PRISM_FLAG_NO_SEQ_SPLIT)
+                assert prism.workspace_layout(nosplit)["seg"] is None
+                assert prism.workspace_bytes(nosplit) == lay["seg"]

@@ -65,3 +65,37 @@ def test_scan_bytes_are_the_workspace_maps(name, L):
     written = th * 4 * wl.dv + wl.B * wl.H * wl.dv * wl.dk * 4      # out and final state
     # regions are padded to 256 bytes each
     assert abs((scan_bytes - written) - maps) <= 6 * 256
+
+
+@pytest.mark.parametrize("name", sorted(I.WORKLOADS))
+@pytest.mark.parametrize("L", [0, 2, 4])
+def test_method_counts(name, L):
+    """The roofline numerators of the method's own work: the two kernels' flops add up to
+    F_scan + F_anchor, the same as the whole path's; the path moves (2 d_k + 2 d_v) e + 8
+    bytes per token-head (1032 at d = 128 in bf16) plus the weights and the final state."""
+    wl = I.WORKLOADS[name]
+    m = bench.method_counts(wl, L)
+    th = wl.B * wl.T * wl.H
+    d, e = wl.dk, (4 if wl.dtype == "f32" else 2)
+    expect = th * (_f_scan(wl.chunk, d, L) + _f_anchor(wl.w, d, L))
+    assert m["prepare"][1] + m["scan"][1] == pytest.approx(expect, rel=1e-12)
+    assert m["path"][1] == pytest.approx(expect, rel=1e-12)
+    assert m["scan"][1] == pytest.approx(th * 6 * d * d, rel=1e-12)
+    weights = wl.H * (L * (2 * d * d + d) + wl.w * d) * 4
+    state = wl.B * wl.H * d * d * 4
+    per = (m["path"][0] - weights - state) / th
+    assert per == pytest.approx(4 * d * e + 8, rel=1e-12)
+    if d == 128 and e == 2:
+        assert per == 1032
+
+
+def test_longctx_method_figures():
+    """Long context: 740,693 flops per token-head for the prepare kernel (1.553 TFLOP per
+    launch) and 838,997 for the path (1.760 TFLOP): tensor-bound at the measured peaks."""
+    wl = I.WORKLOADS["longctx_bf16"]
+    m = bench.method_counts(wl, 4)
+    th = wl.B * wl.T * wl.H
+    assert m["prepare"][1] / th == pytest.approx(740693.33, rel=1e-6)
+    assert m["path"][1] / th == pytest.approx(838997.33, rel=1e-6)
+    r = bench.roofline_of(*m["prepare"], 7.126, 6775.3, 1915.6)
+    assert r["bound"] == "tensor" and r["frac"] == pytest.approx(1.5533e12 / 7.126e-3 / 1915.6e12, rel=1e-3)
