@@ -15,8 +15,17 @@ cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
   auto fn = prep_tc_kernel<D, C>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.T + C - 1) / C, a.H, a.B);
-  fn<<<grid, S::NTA, S::bytes, s>>>(a);
+  // Where the next chunk's tiles can come in during a tail (S::kPrefetch), one persistent CTA
+  // per SM walks the chunks; otherwise one CTA per chunk.
+  const long long chunks = (long long)a.B * a.H * ((a.T + C - 1) / C);
+  long long grid = chunks;
+  if (S::kPrefetch) {
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (grid > sms) grid = sms;
+  }
+  fn<<<(unsigned)grid, S::NTA, S::bytes, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -2,8 +2,11 @@
 // summaries, on tcgen05 tensor cores.  ("Technical Summary: PRISM", §2.2
 // stages 1-2 and the injection B_t = sum_l beta^(l) delta^(l) k^(l)^T.)
 //
-// Everything here is state-independent, so it runs fully parallel: one CTA per
-// (chunk, head, batch).  For the chunk's C tokens it computes the anchor u, the
+// Everything here is state-independent, so it runs fully parallel over chunks.  The
+// kernel is persistent: one CTA per SM walks the chunks (b, h, chunk) with a stride of
+// the grid size; while a chunk's tail runs, the next chunk's K, Q and v tiles are
+// already being copied in and its gates loaded, so a chunk starts without waiting on
+// memory.  For the chunk's C tokens it computes the anchor u, the
 // L refinement steps (directions K_l = k^(l), write values D_l = beta^(l) delta^(l))
 // and reduces them at once to what the state scan needs:
 //   R   = sum_l strict_tril(K K_l^T (.) Gamma) D_l      (C x d_v)  value-side correction
@@ -157,8 +160,9 @@ struct PrepSmem {
   static constexpr uint32_t oInv = oBeta + 4 * C;        // f32 1/|k_hat| [C] (0 past the sequence end)
   static constexpr uint32_t oPart = oInv + 4 * C;        // f32 per-quarter partial sums, quarters 1..3:
                                                          //   [3][2][C] (|k_hat|^2, w_beta . u)
+  static constexpr uint32_t oBtok = oPart + 24 * C;      // f32 beta_t [C] (0 past the sequence end)
   static constexpr int kBars = 13;
-  static constexpr uint32_t oBar = oPart + 24 * C;       // mbarriers
+  static constexpr uint32_t oBar = oBtok + 4 * C;        // mbarriers
   static constexpr uint32_t oSlot = oBar + 8 * kBars;
   static constexpr uint32_t oTiles = ((oSlot + 8 + 127) / 128) * 128;
   // refinement-loop tiles
@@ -190,11 +194,15 @@ struct PrepSmem {
   static constexpr uint32_t tTB = p6.where(sTB);         // f16 T (B operand)
   static constexpr Place p7 = p6.at(sTB);
   static constexpr uint32_t bytes = p7.o2 > loop_end ? p7.o2 : loop_end;
-  // N^T leaves through a shared-memory staging area and an asynchronous bulk store
-  // (draining while the tail computes) where the tail's own buffers leave the K_l / D /
-  // Dt region free.
+  // Where the tail's buffers leave the K_l and D regions free, the next chunk's K, Q rows
+  // and v window are copied there while the tail runs; otherwise after it.
+  static constexpr bool kPrefetch = p7.o2 <= oKl;
+  // N^T (D x D fp32) leaves through the K_l and D regions (staged by the consumers, copied
+  // out by the producer with one bulk store) where the tail leaves them free.
   static constexpr uint32_t kNT = D * D * 4;
-  static constexpr bool kStageN = p7.o2 <= oKl && oKl + kNT <= loop_end;
+  static constexpr bool kStageN = kPrefetch && oKl + kNT <= loop_end;
+  static_assert((uint32_t)(2 * C * D * 2) <= 2 * kF && (uint32_t)((C + 8) * D * 2) <= 2 * kF,
+                "input tiles fit the K_l and D regions");
   // TMEM columns: k_hat of even / odd steps | p (the u hi and u lo products side by side; the
   // scores [G;P] of K_l hi and lo once p has been read) | [R;O_l] | N_l, and in the tail [W | U] over the first 4C columns
   // (or W over N_l and U after it when D > 2C).
@@ -374,6 +382,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   float* sbl = reinterpret_cast<float*>(sm + S::oBeta);
   float* sinv = reinterpret_cast<float*>(sm + S::oInv);
   float* spart = reinterpret_cast<float*>(sm + S::oPart);
+  float* sbt = reinterpret_cast<float*>(sm + S::oBtok);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::oBar);
   // mbarriers.  Tile copies: bar_wk (W_k into X), bar_wp (W_p into Y), bar_in (K, Q, v).
   // MMA completion (tcgen05.commit): bar_k[l % 2] (k_hat^(l)), bar_p (p^(l)), bar_gp (scores
@@ -400,62 +409,54 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   const int row = quarter * 32 + lane;         // this thread's TMEM lane
   const int tb0 = cg * NTH;                    // first of this thread's token columns
   const int fb0 = cg * NFD;                    // first of this thread's feature columns
-  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int H = p.H, T_ = p.T, L = p.L, w = p.w;
   const int NC = (T_ + C - 1) / C;
-  const int len = p.seq_lens ? min(max(p.seq_lens[b], 0), T_) : T_;
-  const int t0 = chunk * C;
-  const int nv = min(C, len - t0);
-  if (nv <= 0) return;                         // chunk entirely padding: never read
+  const int total = p.B * H * NC;
   const bool need_lo = *p.wflag != 0;
-  const unsigned char* wsrc = p.wblocks;
-  auto wblock = [&](int l, int which, int part) {
-    return wsrc + WeightBlock<D>::index(h, l, L, which, part) * S::kW;
-  };
-
-  // ---- setup: warp 0 starts every tile copy (K, Q rows and the v window by TMA, W_k^(0)
-  //      and W_p^(0) by bulk copy) and allocates TMEM; meanwhile the consumers fetch
-  //      their small parameters and warp 1 scans the gates ----
+  const bool cvalid = row < D && !producer;
+  constexpr int NG = (C + 31) / 32;
   __nv_bfloat16* kqraw = reinterpret_cast<__nv_bfloat16*>(sKl);   // [2C][D]: K rows, then Q rows
   __nv_bfloat16* vwin = reinterpret_cast<__nv_bfloat16*>(sD);     // [C + 8][D]: tokens t0-8 .. t0+C-1
-  if (warp == 0) {
-    if (lane == 0) {
-      for (int i = 0; i < S::kBars; ++i)
-        tc::bar_init(bars + i, (bars + i == bar_u || bars + i == bar_rb || bars + i == bar_r5) ? NW : 1);
-      tc::bar_fence_init();
-      tc::bar_expect_tx(bar_in, (uint32_t)(3 * C + 8) * D * 2);
-      tc::tma_load_4d(kqraw, &p.tm_k, 0, h, t0, b, bar_in);
-      tc::tma_load_4d(kqraw + C * D, &p.tm_q, 0, h, t0, b, bar_in);
-      tc::tma_load_4d(vwin, &p.tm_v, 0, h, t0 - 8, b, bar_in);
-      if (L > 0) {                             // W^(0) streams in while the anchor is built
-        tc::bar_expect_tx(bar_wk, S::kW);
-        tc::bulk_g2s(sX, wblock(0, 0, 0), S::kW, bar_wk);
-        tc::bar_expect_tx(bar_wp, S::kW);
-        tc::bulk_g2s(sY, wblock(0, 1, 0), S::kW, bar_wp);
-      }
+  // Chunks are numbered (b, h, chunk) with a head's chunks consecutive; chunk_of gives the
+  // coordinates and the count of tokens before the sequence end (<= 0: padding only).
+  auto chunk_of = [&](int id, int& b_, int& h_, int& c_, int& nv_) {
+    c_ = id % NC;
+    h_ = (id / NC) % H;
+    b_ = id / (NC * H);
+    const int len_ = p.seq_lens ? min(max(p.seq_lens[b_], 0), T_) : T_;
+    nv_ = min(C, len_ - c_ * C);
+  };
+  auto next_chunk = [&](int id) {              // this CTA's next chunk with tokens, from id on
+    for (; id < total; id += gridDim.x) {
+      int b_, h_, c_, nv_;
+      chunk_of(id, b_, h_, c_, nv_);
+      if (nv_ > 0) break;
     }
-    __syncwarp();
-    tc::alloc(tslot, S::tmem_cols);
-  }
-  // small per-thread parameters: conv taps (ca[m] multiplies v_{t-8+m}), w_beta^(0) of
-  // this thread's feature, beta of token tid (used in the tail)
-  const bool cvalid = row < D && !producer;
-  float ca[8];
-#pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    const int j = 8 - m;
-    ca[m] = (cvalid && j <= w) ? tc::ldg_early(p.conv_w + ((size_t)h * w + (j - 1)) * D + row) : 0.f;
-  }
-  float wb_next = (L > 0 && cvalid) ? tc::ldg_early(p.wbeta + (size_t)h * L * D + row) : 0.f;
-  const float beta_tok = (tid < nv) ? tc::ldg_early(p.beta + ((size_t)b * T_ + t0 + tid) * H + h) : 0.f;
-  if (warp == 1) {
-    // inclusive scan of log alpha over the chunk (all loads issued first)
-    constexpr int NG = (C + 31) / 32;
-    float la[NG];
+    return id;
+  };
+  // One thread: TMA copies of a chunk's K and Q rows and its v window (C + 8 tokens;
+  // out-of-range rows arrive as zeros) into the K_l and D regions.
+  auto load_inputs = [&](int id) {
+    int b_, h_, c_, nv_;
+    chunk_of(id, b_, h_, c_, nv_);
+    tc::bar_expect_tx(bar_in, (uint32_t)(3 * C + 8) * D * 2);
+    tc::tma_load_4d(kqraw, &p.tm_k, 0, h_, c_ * C, b_, bar_in);
+    tc::tma_load_4d(kqraw + C * D, &p.tm_q, 0, h_, c_ * C, b_, bar_in);
+    tc::tma_load_4d(vwin, &p.tm_v, 0, h_, c_ * C - 8, b_, bar_in);
+  };
+  // A chunk's gates into shared memory, by the producer warp: log alpha scanned over the
+  // chunk (sg) and beta_t (sbt), zero past the sequence end.  The decay factors sdec
+  // follow at the chunk's start (the previous chunk's tail still reads its own).
+  auto gates_to_smem = [&](int id) {
+    int b_, h_, c_, nv_;
+    chunk_of(id, b_, h_, c_, nv_);
+    float la[NG], be[NG];
 #pragma unroll
     for (int q = 0; q < NG; ++q) {
       const int i = q * 32 + lane;
-      la[q] = (i < nv) ? tc::ldg_early(p.log_alpha + ((size_t)b * T_ + t0 + i) * H + h) : 0.f;
+      const size_t g = ((size_t)b_ * T_ + c_ * C + i) * H + h_;
+      la[q] = (i < nv_) ? tc::ldg_early(p.log_alpha + g) : 0.f;
+      be[q] = (i < nv_) ? tc::ldg_early(p.beta + g) : 0.f;
     }
     float run = 0.f;
 #pragma unroll
@@ -469,12 +470,29 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       }
       x += run;
       run = __shfl_sync(0xffffffffu, x, 31);
-      if (i < C) sg[i] = x;
+      if (i < C) {
+        sg[i] = x;
+        sbt[i] = be[q];
+      }
     }
     __syncwarp();
-    for (int i = lane; i < C; i += 32) sdec[i] = expf(sg[C - 1] - sg[i]);
+  };
+
+  // ---- once per CTA: barriers, TMEM, the first chunk's tile copies and gates ----
+  int cur = next_chunk(blockIdx.x);
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < S::kBars; ++i)
+        tc::bar_init(bars + i, (bars + i == bar_u || bars + i == bar_rb || bars + i == bar_r5) ? NW : 1);
+      tc::bar_fence_init();
+      if (cur < total) load_inputs(cur);
+    }
+    __syncwarp();
+    tc::alloc(tslot, S::tmem_cols);
   }
-  // rows D..127 of the scaled-write tiles stay zero (A operand of the injection)
+  if (producer && cur < total) gates_to_smem(cur);
+  // rows D..127 of the scaled-write tiles stay zero (A operand of the injection); nothing
+  // else ever writes them
   if constexpr (D < 128)
     for (int idx = tid; idx < (128 - D) * (C / 8) * 2; idx += S::NTA) {
       const int part = idx / ((128 - D) * (C / 8));
@@ -482,6 +500,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       const int r = D + rem % (128 - D), s8 = rem / (128 - D);
       *reinterpret_cast<uint4*>(sDt + part * S::kF128 + s8 * 2048u + r * 16u) = make_uint4(0u, 0u, 0u, 0u);
     }
+  tc::fence_smem_to_async();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -498,10 +517,56 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   constexpr uint32_t S_s = (D / 8) * 128;      // token step of the feature x token tiles
   bool ok = true;
 
+  // One loop over this CTA's chunks for both roles; the producer warp and the consumer
+  // warps split inside it.
+  bool have_gates = true;                      // producer: the chunk's gates are in sg / sbt
+  for (uint32_t it = 0; cur < total; ++it) {
+  int b, h, chunk, nv;
+  chunk_of(cur, b, h, chunk, nv);
+  const int t0 = chunk * C;
+  const int len = p.seq_lens ? min(max(p.seq_lens[b], 0), T_) : T_;
+  const int nxt = next_chunk(cur + gridDim.x);
+  // parities: bar_k[0] completes ceil(L/2) times per chunk, bar_k[1] floor(L/2) times,
+  // bar_p, bar_gp and bar_6 L times, bar_in and bar_u once
+  const uint32_t kb0 = it * (uint32_t)((L + 1) / 2), kb1 = it * (uint32_t)(L / 2), sb = it * (uint32_t)L;
+  auto kpar = [&](int l) { return (((l & 1) ? kb1 : kb0) + (uint32_t)(l >> 1)) & 1u; };
+  auto spar = [&](int l) { return (sb + (uint32_t)l) & 1u; };
+  const unsigned char* wsrc = p.wblocks;
+  auto wblock = [&](int l, int which, int part) {
+    return wsrc + WeightBlock<D>::index(h, l, L, which, part) * S::kW;
+  };
+  // ---- chunk start: the producer streams W^(0) in (the previous tail is done with X and
+  //      Y) and forms the decay factors from the gates it brought in; the consumers fetch
+  //      their small parameters ----
+  if (producer && lane == 0 && L > 0) {
+    tc::bar_expect_tx(bar_wk, S::kW);
+    tc::bulk_g2s(sX, wblock(0, 0, 0), S::kW, bar_wk);
+    tc::bar_expect_tx(bar_wp, S::kW);
+    tc::bulk_g2s(sY, wblock(0, 1, 0), S::kW, bar_wp);
+  }
+  if (producer) {
+    if (!have_gates) gates_to_smem(cur);      // first chunk, or no prefetch
+    have_gates = false;
+    for (int i = lane; i < C; i += 32) sdec[i] = expf(sg[C - 1] - sg[i]);
+  }
+  // conv taps (ca[m] multiplies v_{t-8+m}) and w_beta^(0) of this thread's feature
+  float ca[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int j = 8 - m;
+    ca[m] = (cvalid && j <= w) ? tc::ldg_early(p.conv_w + ((size_t)h * w + (j - 1)) * D + row) : 0.f;
+  }
+  float wb_next = (L > 0 && cvalid) ? tc::ldg_early(p.wbeta + (size_t)h * L * D + row) : 0.f;
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
   if (producer) {
     // ================= producer: tile copies and MMAs of the refinement loop =================
     if (lane == 0 && L > 0) {
-      uint32_t ph_wk = 0, ph_wp = 0, ph_rb = 0, ph_r5 = 0, ph_x = 0;
+      // phase counts: per chunk bar_wk and bar_wp complete L times (2L with the lo halves),
+      // bar_x 2L times (lo halves only), bar_rb and bar_r5 L times
+      const uint32_t nw = need_lo ? 2u * L : (uint32_t)L;
+      uint32_t ph_wk = it * nw, ph_wp = it * nw, ph_rb = it * L, ph_r5 = it * L, ph_x = need_lo ? it * 2u * L : 0u;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         ok &= tc::bar_wait(bar, parity);
         tc::fence_after();
@@ -535,7 +600,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
         }
         tc::commit(done);
       };
-      wait(bar_u, 0);
+      wait(bar_u, it & 1);
       wait(bar_wk, ph_wk++ & 1);
       proj(0, 0, t_k0, sX, bar_wk, ph_wk, bar_k);
       wait(bar_wp, ph_wp++ & 1);
@@ -545,11 +610,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
         if (l + 1 < L) {
           // W_p^(l+1) into Y once p^(l) is done; W_k^(l+1) into X once k_hat^(l) is done and
           // step l-1's [G;P] tiles have been read; then k_hat^(l+1) into the other columns
-          wait(bar_p, l & 1);
+          wait(bar_p, spar(l));
           tc::bar_expect_tx(bar_wp, S::kW);
           tc::bulk_g2s(sY, wblock(l + 1, 1, 0), S::kW, bar_wp);
-          wait(bar_k + (l & 1), (l >> 1) & 1);
-          if (l > 0) wait(bar_6, (l - 1) & 1);
+          wait(bar_k + (l & 1), kpar(l));
+          if (l > 0) wait(bar_6, spar(l - 1));
           tc::bar_expect_tx(bar_wk, S::kW);
           tc::bulk_g2s(sX, wblock(l + 1, 0, 0), S::kW, bar_wk);
           wait(bar_wk, ph_wk++ & 1);
@@ -587,9 +652,30 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       }
     }
     __syncwarp();
+    if constexpr (S::kStageN) {
+      // the consumers have staged N^T in the K_l / D regions: copy it out, and once the copy
+      // has read it, bring the next chunk's tiles in (they land in the same regions)
+      asm volatile("bar.sync 10, %0;\n" ::"n"(S::NTA) : "memory");
+      if (lane == 0) {
+        const size_t cbase = ((size_t)b * H + h) * NC + chunk;
+        if (L > 0) {
+          tc::bulk_s2g(p.Nt + cbase * D * D, sKl, S::kNT);
+          tc::bulk_commit();
+          tc::bulk_wait_read();
+        }
+        if (nxt < total) load_inputs(nxt);
+      }
+      __syncwarp();
+      // the consumers have also read this chunk's sg and sbt (sdec stays theirs until the
+      // chunk ends): the next chunk's gates come in now
+      if (nxt < total) {
+        gates_to_smem(nxt);
+        have_gates = true;
+      }
+    }
   } else {
   // ================= consumers =================
-  ok = tc::bar_wait(bar_in, 0);
+  ok &= tc::bar_wait(bar_in, it & 1);
   // v rows past the sequence end are cleared.
   if (t0 + C > len) {
     const int r0 = len - (t0 - 8);             // first v-window row past the end (>= 9)
@@ -686,7 +772,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   const bool gelu = !(p.flags & 1u);
   for (int l = 0; l < L; ++l) {
     const uint32_t t_kl = t_k0 + (l & 1) * C;  // k_hat^(l)
-    ok &= tc::bar_wait(bar_k + (l & 1), (l >> 1) & 1);
+    ok &= tc::bar_wait(bar_k + (l & 1), kpar(l));
     tc::fence_after();
     // [3] epilogue.  Pass A: per token |k_hat|^2 and the gate logit w_beta . u,
     //     summed over this warp's 32 features (reduce-scatter over 8-token groups); the
@@ -772,8 +858,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       }
       asm volatile("bar.sync %0, 128;\n" ::"r"(2 + cg) : "memory");
       // p^(l) ready, and step l-1's MMAs have read the K_l, D_l tiles about to be rewritten
-      ok &= tc::bar_wait(bar_p, l & 1);
-      if (l > 0) ok &= tc::bar_wait(bar_6, (l - 1) & 1);
+      ok &= tc::bar_wait(bar_p, spar(l));
+      if (l > 0) ok &= tc::bar_wait(bar_6, spar(l - 1));
       tc::fence_after();
       // Pass B: directions, residual step, factor tiles
       if (fwarp) {
@@ -821,7 +907,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     tc::fence_before();
     __syncwarp();
     if (lane == 0) tc::bar_arrive(bar_rb);
-    ok &= tc::bar_wait(bar_gp, l & 1);
+    ok &= tc::bar_wait(bar_gp, spar(l));
     tc::fence_after();
     // [5] epilogue: decay and causal mask, then hi/lo split; rows < C are G, C..2C-1 are P
     if (quarter * 32 < 2 * C) {
@@ -852,10 +938,10 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     if (lane == 0) tc::bar_arrive(bar_r5);
   }
   if (L > 0) {
-    ok &= tc::bar_wait(bar_6, (L - 1) & 1);
+    ok &= tc::bar_wait(bar_6, spar(L - 1));
     tc::fence_after();
   }
-  uint32_t ph_mma = 0;
+  uint32_t ph_mma = it * 3u;                   // bar_mma completes three times per chunk
   auto wait_mma = [&]() {
     ok &= tc::bar_wait(bar_mma, ph_mma & 1);
     ++ph_mma;
@@ -886,10 +972,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   for (int g = 0; g < NFD / 8; ++g)
     vr[g] = tok_valid ? tc::ldg_early(reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t0 + s_tok) * H + h) * D + fb0 + 8 * g))
                       : make_uint4(0u, 0u, 0u, 0u);
-  // (a) N^T to global (its TMEM columns are reused below)
+  // (a) N^T to global (its TMEM columns are reused below), piece-major over v:
+  //     (k, v) at ((v/4)*D + k)*4 + v%4, so a warp's lanes (consecutive k) write 512
+  //     contiguous bytes per piece
   if (L > 0 && fwarp) {
-    // piece-major over v: (k, v) at ((v/4)*D + k)*4 + v%4, staged in shared memory when room
-    float* nbase = S::kStageN ? reinterpret_cast<float*>(sm + S::oKl) : p.Nt + cbase * D * D;
+    float* nbase = S::kStageN ? reinterpret_cast<float*>(sKl) : p.Nt + cbase * D * D;
     uint32_t nr[NFD / 8][8];
 #pragma unroll
     for (int g = 0; g < NFD / 8; ++g) tc::ld8a(t_n + lane_base + fb0 + 8 * g, nr[g]);
@@ -907,17 +994,24 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     }
   }
   if (tid < C) {
-    tbeta[tid] = beta_tok;
+    tbeta[tid] = sbt[tid];
     tgam[tid] = expf(sg[tid]);
   }
-  if constexpr (S::kStageN) tc::fence_smem_to_async();
+  tc::fence_smem_to_async();
   tc::fence_before();
-  csync<NT>();
-  if constexpr (S::kStageN)
-    if (L > 0 && tid == 0) {                 // N^T out while the tail runs
-      tc::bulk_s2g(p.Nt + cbase * D * D, sm + S::oKl, S::kNT);
-      tc::bulk_commit();
+  // every read of this chunk's K_l / D regions is done (the last step's MMAs have
+  // completed, the raw K/Q rows and the v window were read before the loop): with N^T
+  // staged there, the producer copies it out and then brings the next chunk's tiles and
+  // gates in, while this tail runs
+  if constexpr (S::kStageN) {
+    asm volatile("bar.sync 10, %0;\n" ::"n"(S::NTA) : "memory");
+  } else {
+    csync<NT>();
+    if (S::kPrefetch && tid == 0) {
+      const int nxt = next_chunk(cur + gridDim.x);
+      if (nxt < total) load_inputs(nxt);
     }
+  }
   // (b) [K K^T ; Q K^T] = [K ; Q] K^T   (B = the K rows of the same tile, K-major)
   if (tid == 0) {
     tc::fence_after();
@@ -1105,9 +1199,15 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     }
   }
   if (tid == 0) p.gC[cbase] = tgam[C - 1];
-  if constexpr (S::kStageN)                  // the copy must have read N^T before the CTA exits
-    if (tid == 0) tc::bulk_wait_read();
   }  // consumers
+  // end of chunk: every role is done with this chunk's shared memory and TMEM
+  tc::fence_smem_to_async();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (!S::kPrefetch && nxt < total && tid == 0) load_inputs(nxt);
+  cur = nxt;
+  }  // chunks
   if (!ok) atomicExch(p.status, 1);
   tc::fence_before();
   __syncthreads();
