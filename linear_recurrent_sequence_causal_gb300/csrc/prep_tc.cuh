@@ -161,7 +161,7 @@ struct PrepSmem {
   static constexpr uint32_t oPart = oInv + 4 * C;        // f32 per-quarter partial sums, quarters 1..3:
                                                          //   [3][2][C] (|k_hat|^2, w_beta . u)
   static constexpr uint32_t oBtok = oPart + 24 * C;      // f32 beta_t [C] (0 past the sequence end)
-  static constexpr int kBars = 13;
+  static constexpr int kBars = 14;
   static constexpr uint32_t oBar = oBtok + 4 * C;        // mbarriers
   static constexpr uint32_t oSlot = oBar + 8 * kBars;
   static constexpr uint32_t oTiles = ((oSlot + 8 + 127) / 128) * 128;
@@ -387,8 +387,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   // mbarriers.  Tile copies: bar_wk (W_k into X), bar_wp (W_p into Y), bar_in (K, Q, v).
   // MMA completion (tcgen05.commit): bar_k[l % 2] (k_hat^(l)), bar_p (p^(l)), bar_gp (scores
   // of step l), bar_6 (step l's [R;O_l], N_l updates), bar_x (internal), bar_mma (tail).
-  // Consumer warps -> producer (one arrival per warp): bar_u (u tiles written), bar_rb
-  // (pass B done: K_l, D_l tiles written, k_hat and p read), bar_r5 ([G;P] tiles written).
+  // Consumer warps -> producer (one arrival per warp): bar_u (u tiles written), bar_ra
+  // (pass A done: K_l tile written, k_hat read), bar_rb (pass B done: D_l tiles written, p
+  // read), bar_r5 ([G;P] tiles written).
   uint64_t* bar_mma = bars + 0;
   uint64_t* bar_wk = bars + 1;
   uint64_t* bar_wp = bars + 2;
@@ -401,6 +402,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   uint64_t* bar_r5 = bars + 10;
   uint64_t* bar_x = bars + 11;
   uint64_t* bar_u = bars + 12;
+  uint64_t* bar_ra = bars + 13;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::oSlot);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -483,7 +485,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   if (warp == 0) {
     if (lane == 0) {
       for (int i = 0; i < S::kBars; ++i)
-        tc::bar_init(bars + i, (bars + i == bar_u || bars + i == bar_rb || bars + i == bar_r5) ? NW : 1);
+        tc::bar_init(bars + i,
+                     (bars + i == bar_u || bars + i == bar_ra || bars + i == bar_rb || bars + i == bar_r5) ? NW : 1);
       tc::bar_fence_init();
       if (cur < total) load_inputs(cur);
     }
@@ -511,7 +514,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   constexpr uint32_t idesc_proj = tc::idesc_f16(C, false, true);   // B = U, MN-major
   constexpr uint32_t idesc_proj2 = tc::idesc_f16(2 * C, false, true);   // B = [u_hi | u_lo]
-  constexpr uint32_t idesc_gp2 = tc::idesc_f16(2 * C, false, true);
+  constexpr uint32_t idesc_gs = tc::idesc_f16(C, false, true);      // B = K_l (MN-major)
   constexpr uint32_t idesc_cc = tc::idesc_f16(C, false, false);
   constexpr uint32_t idesc_dd = tc::idesc_f16(D, false, false);
   constexpr uint32_t S_s = (D / 8) * 128;      // token step of the feature x token tiles
@@ -564,9 +567,10 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     // ================= producer: tile copies and MMAs of the refinement loop =================
     if (lane == 0 && L > 0) {
       // phase counts: per chunk bar_wk and bar_wp complete L times (2L with the lo halves),
-      // bar_x 2L times (lo halves only), bar_rb and bar_r5 L times
+      // bar_x 2L times (lo halves only), bar_ra, bar_rb and bar_r5 L times
       const uint32_t nw = need_lo ? 2u * L : (uint32_t)L;
-      uint32_t ph_wk = it * nw, ph_wp = it * nw, ph_rb = it * L, ph_r5 = it * L, ph_x = need_lo ? it * 2u * L : 0u;
+      uint32_t ph_wk = it * nw, ph_wp = it * nw, ph_ra = it * L, ph_rb = it * L, ph_r5 = it * L;
+      uint32_t ph_x = need_lo ? it * 2u * L : 0u;
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         ok &= tc::bar_wait(bar, parity);
         tc::fence_after();
@@ -620,13 +624,22 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
           wait(bar_wk, ph_wk++ & 1);
           proj(l + 1, 0, t_k0 + ((l + 1) & 1) * C, sX, bar_wk, ph_wk, bar_k + ((l + 1) & 1));
         }
-        // [4] scores [G ; P] = [K ; Q] [K_l,hi | K_l,lo]^T into the p columns (pass B has read
-        //     p^(l)) as one N = 2C operand; the epilogue adds the two halves
-        wait(bar_rb, ph_rb++ & 1);
+        // [4] scores [G ; P] = [K ; Q] K_l^T into k_hat^(l)'s columns once pass A has read
+        //     them and written the K_l tile; the hi and lo halves of K_l accumulate in one set
+        //     of C columns, so the scores compute while pass B runs
+        wait(bar_ra, ph_ra++ & 1);
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma(t_p, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKl + kk * 256, 128, S_s), idesc_gp2, kk > 0);
+          for (int part = 0; part < 2; ++part)
+            tc::mma(t_kl, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKl + part * S::kF + kk * 256, 128, S_s),
+                    idesc_gs, kk > 0 || part > 0);
         tc::commit(bar_gp);
+        // once pass B has read p^(l) and written the D tiles: p^(l+1) into the p columns, then
         // [6a] N_l^T += K_l^T Dt_l (3 passes; rows of N^T are k features, columns v features)
+        wait(bar_rb, ph_rb++ & 1);
+        if (l + 1 < L) {
+          wait(bar_wp, ph_wp++ & 1);
+          proj(l + 1, 1, t_p, sY, bar_wp, ph_wp, bar_p);
+        }
         {
           const int ap[3] = {0, 1, 0}, bp[3] = {0, 0, 1};
           for (int ps = 0; ps < 3; ++ps)
@@ -634,13 +647,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
               tc::mma(t_n, tc::desc(sKl + ap[ps] * S::kF + kk * 2 * S_s, S_s, 128),
                       tc::desc(sDt + bp[ps] * S::kF128 + kk * 4096, 2048, 128), idesc_dd, l > 0 || ps > 0 || kk > 0);
         }
-        // [6b] [R ; O_l] += [G ; P] D_l (3 passes) once the [G;P] tiles are in X; before it
-        //      p^(l+1) into the p columns, which the [5] epilogue has read
+        // [6b] [R ; O_l] += [G ; P] D_l (3 passes) once the [G;P] tiles are in X
         wait(bar_r5, ph_r5++ & 1);
-        if (l + 1 < L) {
-          wait(bar_wp, ph_wp++ & 1);
-          proj(l + 1, 1, t_p, sY, bar_wp, ph_wp, bar_p);
-        }
         {
           const int ap[3] = {0, 0, 1}, bp[3] = {0, 1, 0};
           for (int ps = 0; ps < 3; ++ps)
@@ -781,6 +789,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       const float wb = wb_next;
       if (l + 1 < L && cvalid) wb_next = tc::ldg_early(p.wbeta + ((size_t)h * L + l + 1) * D + c);   // next step's
       float keep_n[NTH / 8], keep_z[NTH / 8];
+      float kh[NTH];                           // k_hat of this thread's feature and tokens
       if (fwarp) {
 #pragma unroll
         for (int j8 = 0; j8 < NTH; j8 += 8) {
@@ -802,7 +811,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
           float rn[8], rz[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            rn[jj] = u2f(kr[jj]) * u2f(kr[jj]);
+            kh[j8 + jj] = u2f(kr[jj]);
+            rn[jj] = kh[j8 + jj] * kh[j8 + jj];
             rz[jj] = wb * uf[jj];
           }
           int n = 8;
@@ -857,28 +867,47 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
         }
       }
       asm volatile("bar.sync %0, 128;\n" ::"r"(2 + cg) : "memory");
-      // p^(l) ready, and step l-1's MMAs have read the K_l, D_l tiles about to be rewritten
-      ok &= tc::bar_wait(bar_p, spar(l));
+      // directions k^(l) = k_hat / |k_hat| into the K_l tile (hi, lo) once step l-1's MMAs
+      // have read the tiles about to be rewritten; then the producer may score against it
       if (l > 0) ok &= tc::bar_wait(bar_6, spar(l - 1));
       tc::fence_after();
-      // Pass B: directions, residual step, factor tiles
+      if (fwarp && cvalid) {
+#pragma unroll
+        for (int j8 = 0; j8 < NTH; j8 += 8) {
+          const int tb = tb0 + j8;
+          float si[8], kd[8];
+          ld_f8(sinv + tb, si);
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) kd[jj] = kh[j8 + jj] * si[jj];
+          uint4 hi, lo;
+          // feature x token tiles: (f, s) at (s/8)*S_s + f*16 + (s%8)*2  (f < D)
+          const uint32_t off = (tb / 8) * S_s + c * 16u;
+          tc::split8(kd, hi, lo);
+          *reinterpret_cast<uint4*>(sKl + off) = hi;
+          *reinterpret_cast<uint4*>(sKl + S::kF + off) = lo;
+        }
+      }
+      tc::fence_smem_to_async();
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) tc::bar_arrive(bar_ra);
+      ok &= tc::bar_wait(bar_p, spar(l));       // p^(l) ready
+      tc::fence_after();
+      // Pass B: residual step and the write values
       if (fwarp) {
 #pragma unroll
         for (int j8 = 0; j8 < NTH; j8 += 8) {
-          uint32_t kr[8], pr[8], pl[8];
-          tc::ld8a(t_kl + lane_base + tb0 + j8, kr);
+          uint32_t pr[8], pl[8];
           tc::ld8a(t_p + lane_base + tb0 + j8, pr);
           tc::ld8a(t_p + C + lane_base + tb0 + j8, pl);
           const int tb = tb0 + j8;
-          float si[8], sb[8], sd[8];
-          ld_f8(sinv + tb, si);
+          float sb[8], sd[8];
           ld_f8(sbl + tb, sb);
           ld_f8(sdec + tb, sd);
-          tc::wait_ld(kr, pr, pl);
-          float kd[8], dv[8], dt[8];
+          tc::wait_ld(pr, pl);
+          float dv[8], dt[8];
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
-            kd[jj] = u2f(kr[jj]) * si[jj];
             const float x = (u2f(pr[jj]) + u2f(pl[jj])) * rres[j8 + jj];
             const float dl = gelu ? gelu_erf(x) : x;
             rres[j8 + jj] -= dl;
@@ -890,9 +919,6 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
             // feature x token tiles: (f, s) at (s/8)*S_s + f*16 + (s%8)*2  (f < D)
             const uint32_t off = (tb / 8) * S_s + c * 16u;
             const uint32_t off128 = (tb / 8) * 2048u + c * 16u;
-            tc::split8(kd, hi, lo);
-            *reinterpret_cast<uint4*>(sKl + off) = hi;
-            *reinterpret_cast<uint4*>(sKl + S::kF + off) = lo;
             tc::split8(dv, hi, lo);
             *reinterpret_cast<uint4*>(sD + off) = hi;
             *reinterpret_cast<uint4*>(sD + S::kF + off) = lo;
@@ -911,20 +937,16 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     tc::fence_after();
     // [5] epilogue: decay and causal mask, then hi/lo split; rows < C are G, C..2C-1 are P
     if (quarter * 32 < 2 * C) {
-      uint32_t gr[NTH / 8][8], gl[NTH / 8][8];
+      uint32_t gr[NTH / 8][8];
 #pragma unroll
-      for (int g = 0; g < NTH / 8; ++g) {
-        tc::ld8a(t_p + lane_base + tb0 + 8 * g, gr[g]);
-        tc::ld8a(t_p + C + lane_base + tb0 + 8 * g, gl[g]);
-      }
+      for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_kl + lane_base + tb0 + 8 * g, gr[g]);
       tc::wait_ld();
 #pragma unroll
       for (int g = 0; g < NTH / 8; ++g) {
         tc::pin(gr[g]);
-        tc::pin(gl[g]);
         float val[8];
 #pragma unroll
-        for (int jj = 0; jj < 8; ++jj) val[jj] = gm[8 * g + jj] * (u2f(gr[g][jj]) + u2f(gl[g][jj]));
+        for (int jj = 0; jj < 8; ++jj) val[jj] = gm[8 * g + jj] * u2f(gr[g][jj]);
         uint4 hi, lo;
         tc::split8(val, hi, lo);
         const uint32_t off = ((tb0 + 8 * g) / 8) * 2048u + row * 16u;
