@@ -178,11 +178,14 @@ struct PrepSmem {
   static constexpr uint32_t sKX = 4 * C * D, sSq = 4 * C * (C + 4), sB = 8 * C;
   static constexpr uint32_t sZ = 4 * 32 * 36;            // block-solve scratch
   static constexpr uint32_t sTB = 2 * C * C;             // f16 T as B operand (C x C)
-  static constexpr Place p0{oX, oKQ, oKl};
-  static constexpr uint32_t tKX = p0.where(sKX);         // f16 [Kb | X] MN-major, C x 2D
-  static constexpr Place p1 = p0.at(sKX);
-  static constexpr uint32_t tTP = p1.where(kF128);       // f16 [I ; P], then [T ; PT], 128 x C
-  static constexpr Place p2 = p1.at(kF128);
+  // The solve's buffers go where the refinement loop leaves memory free first (W_p and the
+  // u tiles: Y and U), so the solve can run while the last step's MMAs still read X, K_l,
+  // D and Dt; [Kb | X] is built in X once those MMAs are done.
+  static constexpr Place p0{oY, oKQ, oKl};
+  static constexpr uint32_t tKX = oX;                    // f16 [Kb | X] MN-major, C x 2D
+  static_assert(sKX <= kX, "[Kb | X] fits the X region");
+  static constexpr uint32_t tTP = p0.where(kF128);       // f16 [I ; P], then [T ; PT], 128 x C
+  static constexpr Place p2 = p0.at(kF128);
   static constexpr uint32_t tA = p2.where(sSq);          // f32 A [C][C+4]
   static constexpr Place p3 = p2.at(sSq);
   static constexpr uint32_t tT = p3.where(sSq);          // f32 T [C][C+4]
@@ -197,6 +200,8 @@ struct PrepSmem {
   // Where the tail's buffers leave the K_l and D regions free, the next chunk's K, Q rows
   // and v window are copied there while the tail runs; otherwise after it.
   static constexpr bool kPrefetch = p7.o2 <= oKl;
+  // the same condition lets the solve start before the last step's MMAs complete
+  static constexpr bool kEarlyTail = kPrefetch;
   // N^T (D x D fp32) leaves through the K_l and D regions (staged by the consumers, copied
   // out by the producer with one bulk store) where the tail leaves them free.
   static constexpr uint32_t kNT = D * D * 4;
@@ -959,10 +964,6 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
     __syncwarp();
     if (lane == 0) tc::bar_arrive(bar_r5);
   }
-  if (L > 0) {
-    ok &= tc::bar_wait(bar_6, spar(L - 1));
-    tc::fence_after();
-  }
   uint32_t ph_mma = it * 3u;                   // bar_mma completes three times per chunk
   auto wait_mma = [&]() {
     ok &= tc::bar_wait(bar_mma, ph_mma & 1);
@@ -988,50 +989,18 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
   const int s_tok = row;
   const bool tok = s_tok < C;
   const bool tok_valid = tok && s_tok < nv;
-  // v rows for (d), fetched now so the latency overlaps (a)
+  // v rows for (d), fetched now so their latency overlaps the solve
   uint4 vr[NFD / 8];
 #pragma unroll
   for (int g = 0; g < NFD / 8; ++g)
     vr[g] = tok_valid ? tc::ldg_early(reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t0 + s_tok) * H + h) * D + fb0 + 8 * g))
                       : make_uint4(0u, 0u, 0u, 0u);
-  // (a) N^T to global (its TMEM columns are reused below), piece-major over v:
-  //     (k, v) at ((v/4)*D + k)*4 + v%4, so a warp's lanes (consecutive k) write 512
-  //     contiguous bytes per piece
-  if (L > 0 && fwarp) {
-    float* nbase = S::kStageN ? reinterpret_cast<float*>(sKl) : p.Nt + cbase * D * D;
-    uint32_t nr[NFD / 8][8];
-#pragma unroll
-    for (int g = 0; g < NFD / 8; ++g) tc::ld8a(t_n + lane_base + fb0 + 8 * g, nr[g]);
-    tc::wait_ld();
-#pragma unroll
-    for (int g = 0; g < NFD / 8; ++g) {
-      tc::pin(nr[g]);
-      if (cvalid) {
-        const int a0 = fb0 + 8 * g;
-        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4) * D + row) * 4) =
-            make_float4(u2f(nr[g][0]), u2f(nr[g][1]), u2f(nr[g][2]), u2f(nr[g][3]));
-        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4 + 1) * D + row) * 4) =
-            make_float4(u2f(nr[g][4]), u2f(nr[g][5]), u2f(nr[g][6]), u2f(nr[g][7]));
-      }
-    }
-  }
-  if (tid < C) {
-    tbeta[tid] = sbt[tid];
-    tgam[tid] = expf(sg[tid]);
-  }
-  tc::fence_smem_to_async();
-  tc::fence_before();
-  // every read of this chunk's K_l / D regions is done (the last step's MMAs have
-  // completed, the raw K/Q rows and the v window were read before the loop): with N^T
-  // staged there, the producer copies it out and then brings the next chunk's tiles and
-  // gates in, while this tail runs
-  if constexpr (S::kStageN) {
-    asm volatile("bar.sync 10, %0;\n" ::"n"(S::NTA) : "memory");
-  } else {
-    csync<NT>();
-    if (S::kPrefetch && tid == 0) {
-      const int nxt = next_chunk(cur + gridDim.x);
-      if (nxt < total) load_inputs(nxt);
+  // Where the solve's buffers avoid the tiles the last step's MMAs read (kEarlyTail), the
+  // solve runs before those MMAs are waited for; otherwise after.
+  if constexpr (!S::kEarlyTail) {
+    if (L > 0) {
+      ok &= tc::bar_wait(bar_6, spar(L - 1));
+      tc::fence_after();
     }
   }
   // (b) [K K^T ; Q K^T] = [K ; Q] K^T   (B = the K rows of the same tile, K-major)
@@ -1042,41 +1011,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
               idesc_cc, kk > 0);
     tc::commit(bar_mma);
   }
-  // (d) meanwhile: X = beta (V - R) and Kb = beta gamma K as the MN-major B tile [Kb | X]:
-  //     (s, f) at (f/8)*(16C) + s*16 + (f%8)*2,  f < D: Kb,  f >= D: X
-  if (quarter * 32 < C) {
-    const float bs = tok ? tbeta[s_tok] : 0.f, gs = tok ? tgam[s_tok] : 0.f;
-    uint32_t rr[NFD / 8][8];
-    if (L > 0) {
-#pragma unroll
-      for (int g = 0; g < NFD / 8; ++g) tc::ld8a(t_ro + lane_base + fb0 + 8 * g, rr[g]);
-      tc::wait_ld();
-#pragma unroll
-      for (int g = 0; g < NFD / 8; ++g) tc::pin(rr[g]);
-    } else {
-#pragma unroll
-      for (int g = 0; g < NFD / 8; ++g)
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) rr[g][jj] = 0u;
-    }
-    if (tok) {
-#pragma unroll
-      for (int g = 0; g < NFD / 8; ++g) {
-        const int f0 = fb0 + 8 * g;
-        const __nv_bfloat16* ve = reinterpret_cast<const __nv_bfloat16*>(&vr[g]);
-        const uint4 kraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + s_tok * 16u);
-        const __half* ke = reinterpret_cast<const __half*>(&kraw);
-        float xf[8], kf[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj) {
-          xf[jj] = tok_valid ? bs * (__bfloat162float(ve[jj]) - u2f(rr[g][jj])) : 0.f;
-          kf[jj] = bs * gs * __half2float(ke[jj]);
-        }
-        *reinterpret_cast<uint4*>(sKX + ((D + f0) / 8) * (16u * C) + s_tok * 16u) = tc::cvt8(xf);
-        *reinterpret_cast<uint4*>(sKX + (f0 / 8) * (16u * C) + s_tok * 16u) = tc::cvt8(kf);
-      }
-    }
+  if (tid < C) {
+    tbeta[tid] = sbt[tid];
+    tgam[tid] = expf(sg[tid]);
   }
+  csync<NT>();
   wait_mma();
   // (c) A = strict_tril(beta (K K^T) (.) Gamma) (fp32) and the A tile [I ; P] of the
   //     [T ; PT] product (fp16, K-major (r, s) at (s/8)*2048 + r*16 + (s%8)*2; rows >= 2C zero)
@@ -1110,6 +1049,48 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
       *reinterpret_cast<uint4*>(sTP + ((tb0 + 8 * g) / 8) * 2048u + row * 16u) = make_uint4(0u, 0u, 0u, 0u);
   }
   csync<NT>();
+  if constexpr (S::kEarlyTail) {
+    if (L > 0) {
+      ok &= tc::bar_wait(bar_6, spar(L - 1));
+      tc::fence_after();
+    }
+  }
+  // (a) N^T to global (its TMEM columns are reused below), piece-major over v:
+  //     (k, v) at ((v/4)*D + k)*4 + v%4, so a warp's lanes (consecutive k) write 512
+  //     contiguous bytes per piece
+  if (L > 0 && fwarp) {
+    float* nbase = S::kStageN ? reinterpret_cast<float*>(sKl) : p.Nt + cbase * D * D;
+    uint32_t nr[NFD / 8][8];
+#pragma unroll
+    for (int g = 0; g < NFD / 8; ++g) tc::ld8a(t_n + lane_base + fb0 + 8 * g, nr[g]);
+    tc::wait_ld();
+#pragma unroll
+    for (int g = 0; g < NFD / 8; ++g) {
+      tc::pin(nr[g]);
+      if (cvalid) {
+        const int a0 = fb0 + 8 * g;
+        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4) * D + row) * 4) =
+            make_float4(u2f(nr[g][0]), u2f(nr[g][1]), u2f(nr[g][2]), u2f(nr[g][3]));
+        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4 + 1) * D + row) * 4) =
+            make_float4(u2f(nr[g][4]), u2f(nr[g][5]), u2f(nr[g][6]), u2f(nr[g][7]));
+      }
+    }
+  }
+  tc::fence_smem_to_async();
+  tc::fence_before();
+  // every read of this chunk's K_l / D regions is done (the last step's MMAs have
+  // completed, the raw K/Q rows and the v window were read before the loop): with N^T
+  // staged there, the producer copies it out and then brings the next chunk's tiles and
+  // gates in, while this tail runs
+  if constexpr (S::kStageN) {
+    asm volatile("bar.sync 10, %0;\n" ::"n"(S::NTA) : "memory");
+  } else {
+    csync<NT>();
+    if (S::kPrefetch && tid == 0) {
+      const int nxt = next_chunk(cur + gridDim.x);
+      if (nxt < total) load_inputs(nxt);
+    }
+  }
   // (e) T = (I + A)^-1 (fp32, and the fp16 B tile); then [T ; PT] = [I ; P] T on the tensor core
   solve_tri<C, NT>(tAf, tTf, sTB, tZf);
   tc::fence_smem_to_async();
@@ -1136,6 +1117,53 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const _
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) v8[jj] = u2f(tr[g][jj]);
       *reinterpret_cast<uint4*>(sTP + ((tb0 + 8 * g) / 8) * 2048u + row * 16u) = tc::cvt8(v8);
+    }
+  }
+  tc::fence_smem_to_async();
+  tc::fence_before();
+  csync<NT>();
+  // (d) [Kb | X] as the MN-major B tile: (s, f) at (f/8)*(16C) + s*16 + (f%8)*2, f < D: Kb,
+  //     f >= D: X.  Rows < C (which hold R in TMEM) write X = beta (V - R) of token row;
+  //     rows C..2C-1 write Kb = beta gamma K of token row - C.
+  if (quarter * 32 < C) {                      // warps holding rows of R (TMEM loads are warp-wide)
+    uint32_t rr[NFD / 8][8];
+    if (L > 0) {
+#pragma unroll
+      for (int g = 0; g < NFD / 8; ++g) tc::ld8a(t_ro + lane_base + fb0 + 8 * g, rr[g]);
+      tc::wait_ld();
+#pragma unroll
+      for (int g = 0; g < NFD / 8; ++g) tc::pin(rr[g]);
+    } else {
+#pragma unroll
+      for (int g = 0; g < NFD / 8; ++g)
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) rr[g][jj] = 0u;
+    }
+    if (row < C) {
+      const float bs = tbeta[row];
+#pragma unroll
+      for (int g = 0; g < NFD / 8; ++g) {
+        const int f0 = fb0 + 8 * g;
+        const __nv_bfloat16* ve = reinterpret_cast<const __nv_bfloat16*>(&vr[g]);
+        float xf[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) xf[jj] = tok_valid ? bs * (__bfloat162float(ve[jj]) - u2f(rr[g][jj])) : 0.f;
+        *reinterpret_cast<uint4*>(sKX + ((D + f0) / 8) * (16u * C) + row * 16u) = tc::cvt8(xf);
+      }
+    }
+  }
+  if (row >= C && row < 2 * C) {
+    const int sk = row - C;
+    const float bg = tbeta[sk] * tgam[sk];
+#pragma unroll
+    for (int g = 0; g < NFD / 8; ++g) {
+      const int f0 = fb0 + 8 * g;
+      const uint4 kraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + sk * 16u);
+      const __half* ke = reinterpret_cast<const __half*>(&kraw);
+      float kf[8];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) kf[jj] = bg * __half2float(ke[jj]);
+      *reinterpret_cast<uint4*>(sKX + (f0 / 8) * (16u * C) + sk * 16u) = tc::cvt8(kf);
     }
   }
   tc::fence_smem_to_async();
