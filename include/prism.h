@@ -62,6 +62,14 @@ typedef enum { PRISM_F32 = 0, PRISM_BF16 = 1 } prism_dtype;
                                             segment's v serve directly when B = 1) */
 #define PRISM_FLAG_NO_SEQ_SPLIT 4u  /* run the scan as one serial chain per sequence even where
                                        prism_scan_segments() would cut it (see there) */
+#define PRISM_FLAG_CHECK_WAIT_TIMEOUT 8u  /* diagnostic of the failure path: on the PRISM_BF16 path
+                                             with d = 128, chunk 32 or 64, every CTA of the scan
+                                             first waits, with a short poll limit, on an mbarrier
+                                             that nothing completes (no copy or MMA is in flight
+                                             then); the wait gives up and the status word is set,
+                                             as a real timeout would set it, and the outputs are
+                                             then computed as without the flag.  prism_device_status
+                                             must read nonzero after such a call. */
 
 typedef struct {
     int B, T, H;          /* batch, sequence length, heads */

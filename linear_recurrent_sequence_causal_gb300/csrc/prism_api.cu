@@ -126,7 +126,8 @@ int check_dims(const prism_dims* d) {
   if (d->B <= 0 || d->T <= 0 || d->H <= 0 || d->d_k <= 0 || d->d_v <= 0 || d->L < 0 ||
       d->conv_width <= 0 || d->chunk <= 0)
     return PRISM_ERR_INVALID_ARG;
-  if (d->flags & ~(PRISM_FLAG_NO_GELU | PRISM_FLAG_VHIST_TOKEN_MAJOR | PRISM_FLAG_NO_SEQ_SPLIT))
+  if (d->flags & ~(PRISM_FLAG_NO_GELU | PRISM_FLAG_VHIST_TOKEN_MAJOR | PRISM_FLAG_NO_SEQ_SPLIT |
+                   PRISM_FLAG_CHECK_WAIT_TIMEOUT))
     return PRISM_ERR_INVALID_ARG;
   if (d->d_k != d->d_v) return PRISM_ERR_UNSUPPORTED;
   const int D = d->d_k, C = d->chunk;
@@ -363,6 +364,7 @@ int scan_impl(const prism_dims* dims, const void* q, const void* k, const void* 
     a.status = region<int>(workspace, Lo, PRISM_WS_STATUS);
     a.nseg = scan_segments(dims);
     a.phase = 0;
+    a.check_timeout = (dims->flags & PRISM_FLAG_CHECK_WAIT_TIMEOUT) ? 1 : 0;
     a.seg_chunks = (int)(((dims->T + C - 1) / C + a.nseg - 1) / a.nseg);
     float* seg = region<float>(workspace, Lo, PRISM_WS_SEG);
     const size_t per = (size_t)dims->B * dims->H * a.nseg * D * D;

@@ -53,6 +53,7 @@ struct ScanTcArgs {
   // full plus the affine maps of segments 1..nseg-1; phase 3: segments 1..nseg-1 in full
   // from seg_start.  Arrays [B][H][nseg][D][D], rows d_v (or, for seg_M, d_k) by d_k.
   int nseg, seg_chunks, phase;
+  int check_timeout;     // nonzero: a wait that cannot complete first (the failure path, exercised)
   float* seg_start;      // entering state of each segment (slot 0 unused)
   float* seg_c;          // c of each segment (slot 0 unused)
   float* seg_M;          // M of each segment (slot 0 unused)
@@ -74,8 +75,8 @@ struct ScanTcSmem {
   static constexpr int LDX = BV + 4;                     // padded row (conflict-free 16-byte accesses)
   static constexpr uint32_t oX = oE + kE;                // Qt_lo S0_hi^T rows, handed to the output rows
   static constexpr uint32_t kX = C * LDX * 4;
-  static constexpr uint32_t oBar = oX + kX;              // full[2], mma1, e_ready, mma2, s_ready, mma1b
-  static constexpr uint32_t oSlot = oBar + 7 * 8;
+  static constexpr uint32_t oBar = oX + kX;              // full[2], mma1, e_ready, mma2, s_ready, mma1b, never
+  static constexpr uint32_t oSlot = oBar + 8 * 8;
   static constexpr uint32_t bytes = oSlot + 16;
   static constexpr int NW = 8;                          // epilogue warps
   static constexpr int NT = (NW + 1) * 32;
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
   uint64_t* bar_mma2 = bar_full + 4;
   uint64_t* bar_s = bar_full + 5;
   uint64_t* bar_mma1b = bar_full + 6;
+  uint64_t* bar_never = bar_full + 7;          // no arrival ever: the timeout check waits on it
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + S::oSlot);
   unsigned char* sS = sm + S::oS;
   unsigned char* sE = sm + S::oE;
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
     tc::bar_init(bar_mma2, 1);
     tc::bar_init(bar_s, NW);
     tc::bar_init(bar_mma1b, 1);
+    tc::bar_init(bar_never, 1);
     tc::bar_fence_init();
   }
   if (warp == 0) tc::alloc(tslot, 256);
@@ -142,6 +145,9 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
   const uint32_t tmem = *tslot;
   const uint32_t t_d1 = tmem, t_d2 = tmem + 2 * BV, t_d3 = tmem + 128;   // 64, 32 and 64 columns
   bool ok = true;
+  // The failure path on request: nothing is in flight yet (no copy issued, no MMA), so a
+  // wait that gives up here leaves nothing behind; it records the error like any other.
+  if (p.check_timeout) ok &= tc::bar_wait(bar_never, 0, 1u << 10);
 
   if (warp == NW) {
     // ================= issuer: chunk copies and MMAs =================

@@ -20,6 +20,7 @@ PRISM_F32, PRISM_BF16 = 0, 1
 PRISM_FLAG_NO_GELU = 1
 PRISM_FLAG_VHIST_TOKEN_MAJOR = 2
 PRISM_FLAG_NO_SEQ_SPLIT = 4
+PRISM_FLAG_CHECK_WAIT_TIMEOUT = 8
 ERRORS = {0: "PRISM_OK", 1: "PRISM_ERR_INVALID_ARG", 2: "PRISM_ERR_UNSUPPORTED",
           3: "PRISM_ERR_MISALIGNED", 4: "PRISM_ERR_WORKSPACE", 5: "PRISM_ERR_LAUNCH",
           6: "PRISM_ERR_CUDA", 7: "PRISM_ERR_SCRATCH_LIMIT"}

@@ -62,7 +62,7 @@ def _fwd(lib, dims, ptrs, ws=0):
 
 @pytest.mark.parametrize("field,value,code", [
     ("B", 0, 1), ("T", -1, 1), ("d_k", 48, 2), ("chunk", 48, 2), ("L", 9, 2),
-    ("conv_width", 9, 2), ("conv_width", 0, 1), ("dtype", 7, 1), ("flags", 8, 1)])
+    ("conv_width", 9, 2), ("conv_width", 0, 1), ("dtype", 7, 1), ("flags", 16, 1)])
 def test_bad_dims(lib, field, value, code):
     d = prism.make_dims(2, 64, 2, 64, 64, 4, 2, 64, prism.PRISM_BF16)
     if field == "d_k":
