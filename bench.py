@@ -120,7 +120,7 @@ def load_peaks():
 # Sources of each forward kernel (the backward and decode kernels do not change them).
 _COMMON = ("tc_common.cuh", "prism_common.cuh", "kernels_tc.cuh", "inst_tc_16.cu", "inst_tc_32.cu",
            "inst_tc_64.cu", "inst_tc_128.cu")
-KERNEL_SOURCES = {"prepare": ("prep_tc.cuh",) + _COMMON, "scan": ("scan_tc.cuh", "scan_affine.cuh") + _COMMON}
+KERNEL_SOURCES = {"prepare": ("prep_tc.cuh",) + _COMMON, "scan": ("scan_tc.cuh",) + _COMMON}
 
 
 def kernel_source_hash(kernel):

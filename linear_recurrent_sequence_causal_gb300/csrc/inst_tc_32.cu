@@ -1,4 +1,4 @@
-// bf16-path instantiations for head dim 32: prep (tcgen05) and scan kernels.
+// bf16-path instantiations for head dim 32: prep and scan kernels (tcgen05).
 #include "kernels_tc.cuh"
 
 namespace prism {
@@ -15,15 +15,6 @@ cudaError_t launch_weights_32(const float* Wk, const float* Wp, int H, int L, un
   prep_weights_kernel<32><<<H * L * 2, 256, 0, s>>>(Wk, Wp, H, L, blocks, flag);
   return cudaGetLastError();
 }
-cudaError_t launch_scan_32(int C, int BV, const ScanArgs& a, cudaStream_t s) {
-  if (C == 16 && BV == 16) return launch_scan_t<32, 16, 16>(a, s);
-  if (C == 16 && BV == 32) return launch_scan_t<32, 16, 32>(a, s);
-  if (C == 32 && BV == 16) return launch_scan_t<32, 32, 16>(a, s);
-  if (C == 32 && BV == 32) return launch_scan_t<32, 32, 32>(a, s);
-  if (C == 64 && BV == 16) return launch_scan_t<32, 64, 16>(a, s);
-  if (C == 64 && BV == 32) return launch_scan_t<32, 64, 32>(a, s);
-  return cudaErrorInvalidValue;
-}
 size_t prep_smem_32(int C) {
   switch (C) {
     case 16: return PrepSmem<32, 16>::bytes;
@@ -31,5 +22,13 @@ size_t prep_smem_32(int C) {
     case 64: return PrepSmem<32, 64>::bytes;
   }
   return 0;
+}
+cudaError_t launch_scan_tc_32(int C, const ScanTcArgs& a, cudaStream_t s) {
+  switch (C) {
+    case 16: return launch_scan_tc_t<32, 16>(a, s);
+    case 32: return launch_scan_tc_t<32, 32>(a, s);
+    case 64: return launch_scan_tc_t<32, 64>(a, s);
+  }
+  return cudaErrorInvalidValue;
 }
 }  // namespace prism

@@ -4,7 +4,6 @@
 #include <cuda_runtime.h>
 
 #include "prep_tc.cuh"
-#include "scan_affine.cuh"
 #include "scan_tc.cuh"
 
 namespace prism {
@@ -29,22 +28,12 @@ cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int D, int C, int BV>
-cudaError_t launch_scan_t(const ScanArgs& a, cudaStream_t s) {
-  using S = ScanSmem<D, C, BV>;
-  auto fn = scan_affine_kernel<D, C, BV>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
-  if (e != cudaSuccess) return e;
-  fn<<<a.B * a.H * (D / BV), S::NW * 32, S::bytes, s>>>(a);
-  return cudaGetLastError();
-}
-
 // The scan: one chain per sequence (a.nseg <= 1), or the sequence split in three
 // launches (affine maps, entering states, final pass; see scan_tc.cuh).
-template <int C>
+template <int D, int C>
 cudaError_t launch_scan_tc_t(const ScanTcArgs& a, cudaStream_t s) {
-  using S = ScanTcSmem<C>;
-  auto fn = scan_tc_kernel<C>;
+  using S = ScanTcSmem<D, C>;
+  auto fn = scan_tc_kernel<D, C>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
   if (e != cudaSuccess) return e;
   const int NSL = S::D / S::BV, BH = a.B * a.H;

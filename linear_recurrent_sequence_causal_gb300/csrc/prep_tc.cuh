@@ -140,10 +140,13 @@ struct PrepSmem {
   // Consumer threads: 4 warps per TMEM lane quarter when the column counts allow it;
   // warp w reads lane quarter w % 4 and column group w / 4 of every TMEM tile.  One more
   // warp (the producer) issues the tile copies and the MMAs of the refinement loop.
-  static constexpr int CG = (C % 32 == 0 && D % 32 == 0) ? 4 : 2;   // column groups
+  // column groups; at d <= 32 one lane quarter holds every feature, so two column groups (8
+  // consumer warps) keep the rest of the CTA small enough for two CTAs per SM
+  static constexpr int CG = (D <= 32 && C <= 32) ? 2 : (C % 32 == 0 && D % 32 == 0) ? 4 : 2;
   static constexpr int NW = 4 * CG;                      // consumer warps
   static constexpr int NT = 32 * NW;                     // consumer threads
   static constexpr int NTA = NT + 32;                    // all threads (with the producer warp)
+  static constexpr int kMinBlocks = NTA <= 288 ? 2 : 1;   // CTAs per SM the registers must allow
   static constexpr int NTH = C / CG;                     // token columns per thread
   static constexpr int NFD = D / CG;                     // feature columns per thread
   static constexpr int NQ = (D + 31) / 32;               // lane quarters that hold features
@@ -371,7 +374,8 @@ __device__ __forceinline__ void h8_to_f(uint4 x, float (&f)[8]) {
 }
 
 template <int D, int C>
-__global__ void __launch_bounds__(PrepSmem<D, C>::NTA, 1) prep_tc_kernel(const __grid_constant__ PrepArgs p) {
+__global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlocks)
+    prep_tc_kernel(const __grid_constant__ PrepArgs p) {
   using S = PrepSmem<D, C>;
   constexpr int NT = S::NT, NW = S::NW, NTH = S::NTH, NFD = S::NFD, NQ = S::NQ;
   extern __shared__ __align__(1024) unsigned char sm[];

@@ -21,14 +21,25 @@ cudaError_t launch_k2_f32_64(int C, const K2Args& a, cudaStream_t s);
   cudaError_t launch_prep_##D(int C, const PrepArgs& a, cudaStream_t s);                       \
   cudaError_t launch_weights_##D(const float* Wk, const float* Wp, int H, int L,                \
                                  unsigned char* blocks, int* flag, cudaStream_t s);             \
-  cudaError_t launch_scan_##D(int C, int BV, const ScanArgs& a, cudaStream_t s);                \
   size_t prep_smem_##D(int C);
 PRISM_DECL_TC(16)
 PRISM_DECL_TC(32)
 PRISM_DECL_TC(64)
 PRISM_DECL_TC(128)
 #undef PRISM_DECL_TC
+cudaError_t launch_scan_tc_16(int C, const ScanTcArgs& a, cudaStream_t s);
+cudaError_t launch_scan_tc_32(int C, const ScanTcArgs& a, cudaStream_t s);
+cudaError_t launch_scan_tc_64(int C, const ScanTcArgs& a, cudaStream_t s);
 cudaError_t launch_scan_tc_128(int C, const ScanTcArgs& a, cudaStream_t s);
+static cudaError_t launch_scan_tc(int D, int C, const ScanTcArgs& a, cudaStream_t s) {
+  switch (D) {
+    case 16: return launch_scan_tc_16(C, a, s);
+    case 32: return launch_scan_tc_32(C, a, s);
+    case 64: return launch_scan_tc_64(C, a, s);
+    case 128: return launch_scan_tc_128(C, a, s);
+  }
+  return cudaErrorInvalidValue;
+}
 cudaError_t launch_decode(int dtype, int D, const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_backward(int dtype, int D, const BwdArgs& a, cudaStream_t s);
 
@@ -66,15 +77,6 @@ static cudaError_t launch_weights(int D, const float* Wk, const float* Wp, int H
     case 32: return launch_weights_32(Wk, Wp, H, L, blocks, flag, s);
     case 64: return launch_weights_64(Wk, Wp, H, L, blocks, flag, s);
     case 128: return launch_weights_128(Wk, Wp, H, L, blocks, flag, s);
-  }
-  return cudaErrorInvalidValue;
-}
-static cudaError_t launch_scan(int D, int C, int BV, const ScanArgs& a, cudaStream_t s) {
-  switch (D) {
-    case 16: return launch_scan_16(C, BV, a, s);
-    case 32: return launch_scan_32(C, BV, a, s);
-    case 64: return launch_scan_64(C, BV, a, s);
-    case 128: return launch_scan_128(C, BV, a, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -216,15 +218,6 @@ T* region(void* ws, const Layout& Lo, int r) {
                               : reinterpret_cast<T*>(static_cast<unsigned char*>(ws) + Lo.off[r]);
 }
 
-// Scan tile height (rows of S per CTA): 16-row tiles while the whole grid fits in
-// one wave of CTAs, else 32-row tiles (fewer waves, less re-reading of the
-// chunk maps shared by a head's tiles).
-int pick_bv(const prism_dims* d) {
-  const int D = d->d_k;
-  if (D < 32) return 16;
-  const long long seqs = (long long)d->B * d->H;
-  return seqs * (D / 16) > 152 ? 32 : 16;
-}
 
 }  // namespace
 
@@ -351,7 +344,8 @@ int scan_impl(const prism_dims* dims, const void* q, const void* k, const void* 
     a.seq_lens = seq_lens; a.out = out; a.final_state = final_state; a.initial_state = initial_state;
     return prism::launch_k2(0, D, C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
   }
-  if (D == 128 && (C == 32 || C == 64)) {   // tensor-core scan
+  // tensor-core scan (every bf16 head dim and chunk)
+  {
     prism::ScanTcArgs a;
     a.B = dims->B; a.T = dims->T; a.H = dims->H;
     a.WQ = region<const __half>(workspace, Lo, PRISM_WS_WQ);
@@ -371,19 +365,8 @@ int scan_impl(const prism_dims* dims, const void* q, const void* k, const void* 
     a.seg_start = seg;
     a.seg_c = seg ? seg + per : nullptr;
     a.seg_M = seg ? seg + 2 * per : nullptr;
-    return prism::launch_scan_tc_128(C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
+    return prism::launch_scan_tc(D, C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
   }
-  prism::ScanArgs a;
-  a.B = dims->B; a.T = dims->T; a.H = dims->H; a.L = dims->L;
-  a.WQ = region<const __half>(workspace, Lo, PRISM_WS_WQ);
-  a.QK = region<const __half>(workspace, Lo, PRISM_WS_QK);
-  a.U = region<const float>(workspace, Lo, PRISM_WS_U);
-  a.Oi = region<const float>(workspace, Lo, PRISM_WS_OI);
-  a.Nt = region<const float>(workspace, Lo, PRISM_WS_N);
-  a.gC = region<const float>(workspace, Lo, PRISM_WS_GC);
-  a.seq_lens = seq_lens; a.out = out; a.final_state = final_state; a.initial_state = initial_state;
-  return prism::launch_scan(D, C, pick_bv(dims), a, s) == cudaSuccess ? PRISM_OK
-                                                                      : PRISM_ERR_LAUNCH;
 }
 }  // namespace
 

@@ -1,19 +1,16 @@
-// Shared device helpers for the PRISM kernels: element types, the warp-level
-// tile product used by both kernels, and small numeric helpers.
+// Shared device helpers for the PRISM kernels: element types, the warp-level fp32
+// tile product of the fp32 I/O path, and small numeric helpers.
 //
-// The tile product computes a warp's share of C[M x N] += A[M x K] * B[K x N]
-// in 16 x 16 output tiles held in the register layout of the m16n8k16 MMA
-// (thread (g = lane/4, c = lane%4) owns rows g, g+8 and columns 2c, 2c+1 of
-// each 16 x 8 half).  bf16 operands go through ldmatrix + mma.sync; fp32
-// operands use the same register layout with FMA (exact fp32 products, for
-// the fp32 I/O workloads whose tolerance bf16 cannot meet).
+// The tile product computes a warp's share of C[M x N] += A[M x K] * B[K x N] in
+// 16 x 16 output tiles (thread (g = lane/4, c = lane%4) owns rows g, g+8 and columns
+// 2c, 2c+1 of each 16 x 8 half) with exact fp32 FMA products, for the fp32 workloads
+// whose tolerance 16-bit operands cannot meet.
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
-#include <type_traits>
 
 namespace prism {
 
@@ -34,33 +31,6 @@ template <> struct Elem<__nv_bfloat16> {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                               uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 // Accumulator of one 16 x 16 output tile: acc[h][e], h = which 8-column half,
@@ -85,76 +55,7 @@ __device__ __forceinline__ int acc_col(int h, int e) {
 //   A_T == true : A(m,k) = a[k*lda + m]   (stored transposed)
 //   B_NK == true : B(k,n) = b[n*ldb + k]  (stored N x K, "K-major")
 //   B_NK == false: B(k,n) = b[k*ldb + n]  (stored K x N, row-major)
-// Offsets m0, n0 are multiples of 16; K is a multiple of 16; all row strides
-// are multiples of 8 elements and the bases 16-byte aligned.
-template <bool A_T, bool B_NK, class H16>
-__device__ __forceinline__ void tile_mma16(Acc16& acc, const H16* a, int lda, const H16* b, int ldb,
-                                           int m0, int n0, int K) {
-  const int lane = threadIdx.x & 31;
-  const int j = lane >> 3;      // which 8x8 matrix this lane addresses
-  const int r = lane & 7;       // which row of it
-  for (int k0 = 0; k0 < K; k0 += 16) {
-    uint32_t af[4], bf[4];
-    if (!A_T) {
-      // matrices: (m+0,k+0) (m+8,k+0) (m+0,k+8) (m+8,k+8)
-      const H16* p = a + (size_t)(m0 + r + 8 * (j & 1)) * lda + k0 + 8 * (j >> 1);
-      ldsm_x4(smem_u32(p), af);
-    } else {
-      // stored [k][m]; same four blocks, rows of the stored matrix are k
-      const H16* p = a + (size_t)(k0 + r + 8 * (j >> 1)) * lda + m0 + 8 * (j & 1);
-      ldsm_x4_t(smem_u32(p), af);
-    }
-    if (B_NK) {
-      // matrices: (n+0,k+0) (n+0,k+8) (n+8,k+0) (n+8,k+8)
-      const H16* p = b + (size_t)(n0 + r + 8 * (j >> 1)) * ldb + k0 + 8 * (j & 1);
-      ldsm_x4(smem_u32(p), bf);
-    } else {
-      // stored [k][n]: matrices (k+0,n+0) (k+8,n+0) (k+0,n+8) (k+8,n+8)
-      const H16* p = b + (size_t)(k0 + r + 8 * (j & 1)) * ldb + n0 + 8 * (j >> 1);
-      ldsm_x4_t(smem_u32(p), bf);
-    }
-    if constexpr (sizeof(H16) == 2 && std::is_same<H16, __half>::value) {
-      mma_f16_16816(acc.v[0], af, bf[0], bf[1]);
-      mma_f16_16816(acc.v[1], af, bf[2], bf[3]);
-    } else {
-      mma_bf16_16816(acc.v[0], af, bf[0], bf[1]);
-      mma_bf16_16816(acc.v[1], af, bf[2], bf[3]);
-    }
-  }
-}
-
-// Same product with operands addressed through functors: a(m0_row, k_col) and
-// b(...) return the shared address of the 16-byte ldmatrix row the lane loads.
-//   AMode 0: A row-major,  address of (row m, cols k..k+7)    -> ldmatrix
-//   AMode 1: A transposed, address of (row k, cols m..m+7)    -> ldmatrix.trans
-//   BMode 0: B stored N x K, address of (row n, cols k..k+7)  -> ldmatrix
-//   BMode 1: B stored K x N, address of (row k, cols n..n+7)  -> ldmatrix.trans
-template <int AMode, int BMode, class AF, class BF>
-__device__ __forceinline__ void tile_mma_f16(Acc16& acc, AF a, BF b, int m0, int n0, int K) {
-  const int lane = threadIdx.x & 31;
-  const int j = lane >> 3, r = lane & 7;
-  for (int k0 = 0; k0 < K; k0 += 16) {
-    uint32_t af[4], bf[4];
-    if (AMode == 0) ldsm_x4(a(m0 + r + 8 * (j & 1), k0 + 8 * (j >> 1)), af);
-    else            ldsm_x4_t(a(k0 + r + 8 * (j >> 1), m0 + 8 * (j & 1)), af);
-    if (BMode == 0) ldsm_x4(b(n0 + r + 8 * (j >> 1), k0 + 8 * (j & 1)), bf);
-    else            ldsm_x4_t(b(k0 + r + 8 * (j & 1), n0 + 8 * (j >> 1)), bf);
-    mma_f16_16816(acc.v[0], af, bf[0], bf[1]);
-    mma_f16_16816(acc.v[1], af, bf[2], bf[3]);
-  }
-}
-
-template <bool A_T, bool B_NK>
-__device__ __forceinline__ void tile_mma(Acc16& acc, const __nv_bfloat16* a, int lda,
-                                         const __nv_bfloat16* b, int ldb, int m0, int n0, int K) {
-  tile_mma16<A_T, B_NK>(acc, a, lda, b, ldb, m0, n0, K);
-}
-template <bool A_T, bool B_NK>
-__device__ __forceinline__ void tile_mma(Acc16& acc, const __half* a, int lda, const __half* b,
-                                         int ldb, int m0, int n0, int K) {
-  tile_mma16<A_T, B_NK>(acc, a, lda, b, ldb, m0, n0, K);
-}
-
+// Offsets m0, n0 are multiples of 16.
 template <bool A_T, bool B_NK>
 __device__ __forceinline__ void tile_mma(Acc16& acc, const float* a, int lda, const float* b,
                                          int ldb, int m0, int n0, int K) {

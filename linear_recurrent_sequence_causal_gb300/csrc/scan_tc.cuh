@@ -1,4 +1,4 @@
-// Kernel B on tcgen05 (bf16 I/O path, d = 128, chunk 32 or 64): the serial chain of
+// Kernel B on tcgen05 (bf16 I/O path, any supported d and chunk): the serial chain of
 // the chunkwise scan ("Technical Summary: PRISM", §2.1, S_t = S_{t-1} A_t + B_t
 // composed over a chunk), one CTA per (b, h, BV-wide slice of d_v):
 //   E   = U - W S0^T                      (C x BV)
@@ -26,9 +26,11 @@
 // entering states S_(s+1) = S_s M_s + c_s, and phase 3 runs segments 1.. in full from
 // them.  Rows of the state are independent, so the M rows split over CTAs like S rows.
 //
-// Threads: warps 0..7 read TMEM lane quarter w % 4 and column half w / 4 (16 of the
-// slice's BV = 32 columns); thread (k, half) keeps those 16 entries of row k of S^T in
-// fp32 registers across chunks.  Warp 8 issues the copies and the MMAs.
+// Threads: warps 0..7 read TMEM lane quarter w % 4 and column half w / 4 (BV / 2 of the
+// slice's BV = min(32, d) columns); thread (k, half) keeps those entries of row k of S^T
+// (k < d) in fp32 registers across chunks.  Warp 8 issues the copies and the MMAs.  The
+// MMAs are M = 128 throughout: where 2C or d is smaller, the extra rows read on into the
+// shared memory that follows (the allocation covers it) and their TMEM lanes are ignored.
 #pragma once
 
 #include "prism_common.cuh"
@@ -59,9 +61,9 @@ struct ScanTcArgs {
   float* seg_M;          // M of each segment (slot 0 unused)
 };
 
-template <int C>
+template <int D_, int C>
 struct ScanTcSmem {
-  static constexpr int D = 128, BV = 32;
+  static constexpr int D = D_, BV = D < 32 ? D : 32;      // BV columns of d_v (rows of S) per CTA
   static constexpr uint32_t kMap = 2 * C * D * 2;        // one interleaved fp16 map (WQ or QK)
   static constexpr uint32_t kU = C * BV * 4;             // BV columns of U (or O_intra)
   static constexpr uint32_t kN = BV * D * 4;             // BV rows of N
@@ -77,15 +79,26 @@ struct ScanTcSmem {
   static constexpr uint32_t kX = C * LDX * 4;
   static constexpr uint32_t oBar = oX + kX;              // full[2], mma1, e_ready, mma2, s_ready, mma1b, never
   static constexpr uint32_t oSlot = oBar + 8 * 8;
-  static constexpr uint32_t bytes = oSlot + 16;
+  // The MMAs run with M = 128; where 2C or d_k is smaller, the rows past them read on into
+  // the following shared memory (their TMEM lanes are never read).  The farthest such read:
+  // K-major [W ; Qt] or [Qt_lo ; Kt] (128 rows, K = d_k) and MN-major Kt^T (M = 128, K = C)
+  // from a chunk map of the second buffer.
+  static constexpr uint32_t kRowsA = (D / 8 - 1) * (32u * C) + 128 * 16;
+  static constexpr uint32_t kRowsKt = C * 16 + 15 * (32u * C) + (C / 8) * 128;
+  static constexpr uint32_t kReach = oBuf1 + oQK + (kRowsA > kRowsKt ? kRowsA : kRowsKt);
+  static constexpr uint32_t bytes = (oSlot + 16 > kReach ? oSlot + 16 : kReach);
   static constexpr int NW = 8;                          // epilogue warps
   static constexpr int NT = (NW + 1) * 32;
+  // TMEM: the MMA1 and MMA2 accumulators share columns (MMA2 of a chunk is issued once the E
+  // epilogue has read MMA1's), then MMA1b's: 3 BV columns; below d = 128 two CTAs share an SM.
+  static constexpr uint32_t kTmemCols = 3 * BV <= 64 ? 64 : 3 * BV <= 128 ? 128 : 256;
+  static constexpr int kMinBlocks = D < 128 ? 2 : 1;
 };
 
-template <int C>
-__global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArgs p) {
-  using S = ScanTcSmem<C>;
-  constexpr int D = S::D, BV = S::BV, NSL = D / BV, NW = S::NW, HB = BV / 2;
+template <int D_, int C>
+__global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMinBlocks) scan_tc_kernel(ScanTcArgs p) {
+  using S = ScanTcSmem<D_, C>;
+  constexpr int D = S::D, BV = S::BV, NSL = D / BV, NW = S::NW, HB = BV / 2, G8 = HB / 8;
   extern __shared__ __align__(1024) unsigned char sm[];
   uint64_t* bar_full = reinterpret_cast<uint64_t*>(sm + S::oBar);   // [2]
   uint64_t* bar_mma1 = bar_full + 2;
@@ -138,12 +151,12 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
     tc::bar_init(bar_never, 1);
     tc::bar_fence_init();
   }
-  if (warp == 0) tc::alloc(tslot, 256);
+  if (warp == 0) tc::alloc(tslot, S::kTmemCols);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t t_d1 = tmem, t_d2 = tmem + 2 * BV, t_d3 = tmem + 128;   // 64, 32 and 64 columns
+  const uint32_t t_d1 = tmem, t_d3 = tmem, t_d2 = tmem + 2 * BV;   // 2BV (MMA1, then MMA2) and BV columns
   bool ok = true;
   // The failure path on request: nothing is in flight yet (no copy issued, no MMA), so a
   // wait that gives up here leaves nothing behind; it records the error like any other.
@@ -205,13 +218,16 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
     const int k = (warp & 3) * 32 + lane;      // TMEM lane: row of [W;Qt], of E, of S^T
     const int hf = warp >> 2;                  // column half: slice columns hf*16 .. hf*16+15
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    float st[HB];                              // S^T[k][v0 + hf*16 ..]
+    const bool krow = k < D;                   // this lane holds a row of S^T
+    float st[HB];                              // S^T[k][v0 + hf*HB ..]
     const float* s0 = kind != 0 ? nullptr
                       : seg == 0 ? (p.initial_state ? p.initial_state + ((size_t)b * H + h) * D * D : nullptr)
                                  : p.seg_start + seg_off;
 #pragma unroll
     for (int v = 0; v < HB; ++v)
-      st[v] = s0 ? s0[(size_t)(v0 + hf * HB + v) * D + k] : (kind == 2 && v0 + hf * HB + v == k) ? 1.f : 0.f;
+      st[v] = !krow ? 0.f
+              : s0  ? s0[(size_t)(v0 + hf * HB + v) * D + k]
+                    : (kind == 2 && v0 + hf * HB + v == k) ? 1.f : 0.f;
     auto write_state = [&]() {                 // [S_hi | S_lo]^T rows: (k, n) at (n/8)*16D + k*16 + (n%8)*2
 #pragma unroll
       for (int g = 0; g < HB / 8; ++g) {
@@ -220,9 +236,11 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
         for (int j = 0; j < 8; ++j) x[j] = st[8 * g + j];
         uint4 hi, lo;
         tc::split8(x, hi, lo);
-        const int n8 = 2 * hf + g;             // column group of the slice
-        *reinterpret_cast<uint4*>(sS + n8 * (16u * D) + k * 16u) = hi;
-        *reinterpret_cast<uint4*>(sS + (BV / 8 + n8) * (16u * D) + k * 16u) = lo;
+        const int n8 = G8 * hf + g;            // column group of the slice
+        if (krow) {
+          *reinterpret_cast<uint4*>(sS + n8 * (16u * D) + k * 16u) = hi;
+          *reinterpret_cast<uint4*>(sS + (BV / 8 + n8) * (16u * D) + k * 16u) = lo;
+        }
       }
       tc::fence_smem_to_async();
       tc::fence_before();
@@ -244,19 +262,19 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
       // ---- E = U - W S0^T (lanes < C); O = O_intra + Qt_hi S0^T (lanes C..2C-1) ----
       float ov[HB];
       if ((warp & 3) * 32 < 2 * C) {
-        uint32_t d1[4][8];                     // hi columns hf*16.., lo columns 32 + hf*16..
+        uint32_t d1[2 * G8][8];                // hi columns hf*HB.., lo columns BV + hf*HB..
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < G8; ++g) {
           tc::ld8a(t_d1 + lane_base + hf * HB + 8 * g, d1[g]);
-          tc::ld8a(t_d1 + lane_base + BV + hf * HB + 8 * g, d1[2 + g]);
+          tc::ld8a(t_d1 + lane_base + BV + hf * HB + 8 * g, d1[G8 + g]);
         }
         tc::wait_ld();
         if (k < C) {
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
+          for (int g = 0; g < G8; ++g) {
             tc::pin(d1[g]);
-            tc::pin(d1[2 + g]);
-            const int pc = 4 * hf + 2 * g;     // U piece (4 columns) of this group
+            tc::pin(d1[G8 + g]);
+            const int pc = (HB / 4) * hf + 2 * g;   // U piece (4 columns) of this group
             float uu[8], e8[8];
             const float4 u0 = useU ? *reinterpret_cast<const float4*>(sU + (pc * C + k) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
             const float4 u1 = useU ? *reinterpret_cast<const float4*>(sU + ((pc + 1) * C + k) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -264,27 +282,27 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
             uu[4] = u1.x; uu[5] = u1.y; uu[6] = u1.z; uu[7] = u1.w;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              e8[j] = uu[j] - (__uint_as_float(d1[g][j]) + __uint_as_float(d1[2 + g][j]));
+              e8[j] = uu[j] - (__uint_as_float(d1[g][j]) + __uint_as_float(d1[G8 + g][j]));
             uint4 hi, lo;
             tc::split8(e8, hi, lo);
             // [E_hi | E_lo]: (r, n) at (n/8)*16C + r*16 + (n%8)*2
-            const int n8 = 2 * hf + g;
+            const int n8 = G8 * hf + g;
             *reinterpret_cast<uint4*>(sE + n8 * (16u * C) + k * 16u) = hi;
             *reinterpret_cast<uint4*>(sE + (BV / 8 + n8) * (16u * C) + k * 16u) = lo;
           }
         } else if (outputs && k < 2 * C) {
           const int r = k - C;
 #pragma unroll
-          for (int g = 0; g < 2; ++g) {
+          for (int g = 0; g < G8; ++g) {
             tc::pin(d1[g]);
-            tc::pin(d1[2 + g]);
-            const int pc = 4 * hf + 2 * g;
+            tc::pin(d1[G8 + g]);
+            const int pc = (HB / 4) * hf + 2 * g;
             const float4 o0 = *reinterpret_cast<const float4*>(sOi + (pc * C + r) * 4);
             const float4 o1 = *reinterpret_cast<const float4*>(sOi + ((pc + 1) * C + r) * 4);
             const float oi[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              ov[8 * g + j] = oi[j] + (__uint_as_float(d1[g][j]) + __uint_as_float(d1[2 + g][j]));
+              ov[8 * g + j] = oi[j] + (__uint_as_float(d1[g][j]) + __uint_as_float(d1[G8 + g][j]));
           }
         }
       }
@@ -295,21 +313,21 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
       // ---- S1^T = gamma_C S0^T + Kt^T E + N^T  (lane k, this column half) ----
       ok &= tc::bar_wait(bar_mma2, c & 1);
       tc::fence_after();
-      {
-        uint32_t d3[4][8];
+      if ((warp & 3) * 32 < D) {                // warps holding rows of S^T (TMEM loads are warp-wide)
+        uint32_t d3[2 * G8][8];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < G8; ++g) {
           tc::ld8a(t_d3 + lane_base + hf * HB + 8 * g, d3[g]);
-          tc::ld8a(t_d3 + lane_base + BV + hf * HB + 8 * g, d3[2 + g]);
+          tc::ld8a(t_d3 + lane_base + BV + hf * HB + 8 * g, d3[G8 + g]);
         }
         tc::wait_ld();
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < G8; ++g) {
           tc::pin(d3[g]);
-          tc::pin(d3[2 + g]);
+          tc::pin(d3[G8 + g]);
           float nn[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (useN) {
-            const int pc = 4 * hf + 2 * g;
+          if (useN && krow) {
+            const int pc = (HB / 4) * hf + 2 * g;
             const float4 n0 = *reinterpret_cast<const float4*>(sN + (pc * D + k) * 4);
             const float4 n1 = *reinterpret_cast<const float4*>(sN + ((pc + 1) * D + k) * 4);
             nn[0] = n0.x; nn[1] = n0.y; nn[2] = n0.z; nn[3] = n0.w;
@@ -318,7 +336,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             st[8 * g + j] = fmaf(gC, st[8 * g + j],
-                                 (__uint_as_float(d3[g][j]) + __uint_as_float(d3[2 + g][j])) + nn[j]);
+                                 (__uint_as_float(d3[g][j]) + __uint_as_float(d3[G8 + g][j])) + nn[j]);
         }
       }
       if (!outputs) {                          // affine maps: state rows only
@@ -329,14 +347,15 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
       // Qt_lo rows go to the output rows through sX
       ok &= tc::bar_wait(bar_mma1b, c & 1);
       tc::fence_after();
-      if ((warp & 3) * 32 < C && k < C) {
-        uint32_t d2[2][8];
+      if ((warp & 3) * 32 < C) {                // TMEM loads are warp-wide; rows k < C are kept
+        uint32_t d2[G8][8];
 #pragma unroll
-        for (int g = 0; g < 2; ++g) tc::ld8a(t_d2 + lane_base + hf * HB + 8 * g, d2[g]);
+        for (int g = 0; g < G8; ++g) tc::ld8a(t_d2 + lane_base + hf * HB + 8 * g, d2[g]);
         tc::wait_ld();
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < G8; ++g) {
           tc::pin(d2[g]);
+          if (k >= C) continue;
           float* xr = sX + k * S::LDX + hf * HB + 8 * g;
           *reinterpret_cast<float4*>(xr) =
               make_float4(__uint_as_float(d2[g][0]), __uint_as_float(d2[g][1]), __uint_as_float(d2[g][2]), __uint_as_float(d2[g][3]));
@@ -375,7 +394,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
               : (p.phase == 0 || last_seg) ? (p.final_state ? p.final_state + ((size_t)b * H + h) * D * D : nullptr)
               : p.phase == 1 ? p.seg_start + seg_off + (size_t)D * D
               : nullptr;
-    if (fs) {
+    if (fs && krow) {
 #pragma unroll
       for (int v = 0; v < HB; ++v) fs[(size_t)(v0 + hf * HB + v) * D + k] = st[v];
     }
@@ -383,7 +402,7 @@ __global__ void __launch_bounds__(ScanTcSmem<C>::NT, 1) scan_tc_kernel(ScanTcArg
   if (!ok) atomicExch(p.status, 1);
   tc::fence_before();
   __syncthreads();
-  if (warp == 0) tc::dealloc(tmem, 256);
+  if (warp == 0) tc::dealloc(tmem, S::kTmemCols);
 }
 
 // Phase 2 of the sequence split: the entering state of each segment,
