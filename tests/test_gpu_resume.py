@@ -70,14 +70,19 @@ def test_forward_from_given_state_and_history(dtype, D, chunk, L):
     check(out, fs, ro, rs, dtype, what="given state")
 
 
-@pytest.mark.parametrize("dtype,D,L,no_gelu", [("bf16", 128, 2, False), ("bf16", 64, 4, False),
-                                               ("f32", 32, 2, False), ("bf16", 16, 0, False),
-                                               ("bf16", 32, 3, True)])
-def test_decode_steps_match_oracle(dtype, D, L, no_gelu):
+@pytest.mark.parametrize("dtype,D,L,no_gelu,B,H,T0,n", [
+    ("bf16", 128, 2, False, 2, 3, 37, 6), ("bf16", 64, 4, False, 2, 3, 37, 6),
+    ("f32", 32, 2, False, 2, 3, 37, 6), ("bf16", 16, 0, False, 2, 3, 37, 6),
+    ("bf16", 32, 3, True, 2, 3, 37, 6),
+    # an odd batch (sequences are grouped in pairs per CTA), a single sequence
+    ("bf16", 128, 2, False, 3, 2, 21, 3), ("bf16", 128, 4, False, 1, 2, 21, 3),
+    # enough CTAs that the weight ring holds fewer slices than the 2L of a step
+    ("bf16", 128, 8, False, 48, 8, 5, 2), ("f32", 64, 8, True, 96, 8, 5, 2)])
+def test_decode_steps_match_oracle(dtype, D, L, no_gelu, B, H, T0, n):
     """A chunked prefix, then one token at a time: outputs and state of the oracle's
     single run over all tokens."""
-    T0, n, chunk = 37, 6, 16
-    wl = I.Workload("case", dtype, 2, T0 + n, 3, D, D, L, 4, chunk, seed=80 + D + L)
+    chunk = 16
+    wl = I.Workload("case", dtype, B, T0 + n, H, D, D, L, 4, chunk, seed=80 + D + L + B)
     inp = I.generate(wl)
     ro, rs, _ = oracle.forward(inp, identity_act=no_gelu)
     d = prism.inputs_to_device(inp)
@@ -85,7 +90,7 @@ def test_decode_steps_match_oracle(dtype, D, L, no_gelu):
     hist = prism.v_history(d["v"], wl.w, T0)
     outs = [out0]
     for t in range(T0, T0 + n):
-        tok = {k: d[k][:, t].contiguous() for k in TOKEN_KEYS}
+        tok = {k: d[k][:, t].clone() for k in TOKEN_KEYS}   # own storage: 16-byte aligned
         o = prism.prism_decode_step(tok["q"], tok["k"], tok["v"], tok["log_alpha"], tok["beta"],
                                     d["conv_w"], d["Wk"], d["Wp"], d["wbeta"], L, state, hist,
                                     no_gelu=no_gelu)
