@@ -63,7 +63,8 @@ typedef enum { PRISM_F32 = 0, PRISM_BF16 = 1 } prism_dtype;
 #define PRISM_FLAG_NO_SEQ_SPLIT 4u  /* run the scan as one serial chain per sequence even where
                                        prism_scan_segments() would cut it (see there) */
 #define PRISM_FLAG_CHECK_WAIT_TIMEOUT 8u  /* diagnostic of the failure path: on the PRISM_BF16 path
-                                             with d = 128, chunk 32 or 64, every CTA of the scan
+                                             (ignored on the PRISM_F32 path, refused by
+                                             prism_decode_step), every CTA of the scan
                                              first waits, with a short poll limit, on an mbarrier
                                              that nothing completes (no copy or MMA is in flight
                                              then); the wait gives up and the status word is set,
