@@ -255,10 +255,13 @@ extern "C" PRISM_API const char* prism_strerror(int code) {
 }
 
 namespace {
+// weights_ready: the workspace already holds these weights in the prepare kernel's fp16
+// blocks (and the flag saying whether their lo halves matter), converted by an earlier
+// call on the same stream; the conversion is skipped and the flag kept.
 int prepare_impl(const prism_dims* dims, const void* q, const void* k, const void* v,
                  const float* log_alpha, const float* beta, const float* conv_w, const float* Wk,
                  const float* Wp, const float* wbeta, const int32_t* seq_lens, const void* v_hist,
-                 void* workspace, size_t workspace_bytes, void* stream) {
+                 void* workspace, size_t workspace_bytes, void* stream, bool weights_ready = false) {
   int rc = check_dims(dims);
   if (rc != PRISM_OK) return rc;
   rc = check_inputs(dims, q, k, v, log_alpha, beta, seq_lens, workspace, workspace_bytes);
@@ -270,7 +273,8 @@ int prepare_impl(const prism_dims* dims, const void* q, const void* k, const voi
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Layout Lo = layout(dims);
   int* status = region<int>(workspace, Lo, PRISM_WS_STATUS);
-  if (cudaMemsetAsync(status, 0, 8, s) != cudaSuccess) return PRISM_ERR_CUDA;
+  const bool keep_weights = weights_ready && dims->dtype == PRISM_BF16 && dims->L > 0;
+  if (cudaMemsetAsync(status, 0, keep_weights ? 4 : 8, s) != cudaSuccess) return PRISM_ERR_CUDA;
   const int D = dims->d_k, C = dims->chunk;
   if (dims->dtype == PRISM_F32) {
     if (dims->L == 0) return PRISM_OK;
@@ -284,7 +288,7 @@ int prepare_impl(const prism_dims* dims, const void* q, const void* k, const voi
     return prism::launch_k1(0, D, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
   }
   unsigned char* wblocks = region<unsigned char>(workspace, Lo, PRISM_WS_WBLOCKS);
-  if (dims->L > 0 &&
+  if (dims->L > 0 && !keep_weights &&
       prism::launch_weights(D, Wk, Wp, dims->H, dims->L, wblocks, status + 1, s) != cudaSuccess)
     return PRISM_ERR_LAUNCH;
   prism::PrepArgs a;
@@ -379,6 +383,27 @@ extern "C" PRISM_API int prism_scan(const prism_dims* dims, const void* q, const
                    out, final_state, stream);
 }
 
+namespace prism {
+// prism_forward_from; with weights_ready the weight conversion of an earlier call into the
+// same workspace is reused (the host pipeline's pieces after the first).
+int forward_from_impl(const prism_dims* dims, const void* q, const void* k, const void* v,
+                      const float* log_alpha, const float* beta, const float* conv_w,
+                      const float* Wk, const float* Wp, const float* wbeta,
+                      const float* initial_state, const void* v_hist, float* out,
+                      float* final_state, const int32_t* seq_lens, void* workspace,
+                      size_t workspace_bytes, void* stream, bool weights_ready) {
+  int rc = check_dims(dims);
+  if (rc != PRISM_OK) return rc;
+  if (!out) return PRISM_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || (final_state && !aligned(final_state, 16))) return PRISM_ERR_MISALIGNED;
+  rc = prepare_impl(dims, q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, seq_lens, v_hist,
+                    workspace, workspace_bytes, stream, weights_ready);
+  if (rc != PRISM_OK) return rc;
+  return scan_impl(dims, q, k, v, log_alpha, beta, seq_lens, initial_state, workspace,
+                   workspace_bytes, out, final_state, stream);
+}
+}  // namespace prism
+
 extern "C" PRISM_API int prism_forward_from(const prism_dims* dims, const void* q, const void* k,
                                             const void* v, const float* log_alpha,
                                             const float* beta, const float* conv_w,
@@ -387,15 +412,9 @@ extern "C" PRISM_API int prism_forward_from(const prism_dims* dims, const void* 
                                             float* out, float* final_state,
                                             const int32_t* seq_lens, void* workspace,
                                             size_t workspace_bytes, void* stream) {
-  int rc = check_dims(dims);
-  if (rc != PRISM_OK) return rc;
-  if (!out) return PRISM_ERR_INVALID_ARG;
-  if (!aligned(out, 16) || (final_state && !aligned(final_state, 16))) return PRISM_ERR_MISALIGNED;
-  rc = prepare_impl(dims, q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, seq_lens, v_hist,
-                    workspace, workspace_bytes, stream);
-  if (rc != PRISM_OK) return rc;
-  return scan_impl(dims, q, k, v, log_alpha, beta, seq_lens, initial_state, workspace,
-                   workspace_bytes, out, final_state, stream);
+  return prism::forward_from_impl(dims, q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta,
+                                  initial_state, v_hist, out, final_state, seq_lens, workspace,
+                                  workspace_bytes, stream, false);
 }
 
 extern "C" PRISM_API int prism_forward(const prism_dims* dims, const void* q, const void* k,

@@ -15,6 +15,15 @@
 
 #include "prism.h"
 
+namespace prism {
+int forward_from_impl(const prism_dims* dims, const void* q, const void* k, const void* v,
+                      const float* log_alpha, const float* beta, const float* conv_w,
+                      const float* Wk, const float* Wp, const float* wbeta,
+                      const float* initial_state, const void* v_hist, float* out,
+                      float* final_state, const int32_t* seq_lens, void* workspace,
+                      size_t workspace_bytes, void* stream, bool weights_ready);
+}
+
 namespace {
 
 size_t r256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -194,6 +203,7 @@ extern "C" PRISM_API int prism_forward_host(const prism_dims* dims, const void* 
   // B = 1 with a length: the tokens past it are padding; segments are cut there.
   const int len1 = (B == 1 && seq_lens) ? std::max(0, std::min(seq_lens[0], T)) : T;
   int cur = -1;                                  // state buffer holding S (B = 1), -1 = zero
+  bool weights_ready = false;                    // the workspace holds the converted weights
   unsigned char* st[2] = {at(A.st0), at(A.st1)};
 
   for (int i = 0; i < P; ++i) {
@@ -227,11 +237,13 @@ extern "C" PRISM_API int prism_forward_host(const prism_dims* dims, const void* 
       prism_dims pd = *dims;
       pd.B = a1 - a0;
       float* fs = reinterpret_cast<float*>(at(A.st0) + (size_t)a0 * state_b);
-      rc = prism_forward(&pd, at(A.q) + r0 * row_in, at(A.k) + r0 * row_in, at(A.v) + r0 * row_in,
-                         reinterpret_cast<const float*>(at(A.la) + r0 * row_g),
-                         reinterpret_cast<const float*>(at(A.be) + r0 * row_g), d_cw, d_wk, d_wp, d_wb,
-                         d_out, final_state ? fs : nullptr, d_lens, at(A.ws), A.ws_bytes, s_comp);
+      rc = prism::forward_from_impl(&pd, at(A.q) + r0 * row_in, at(A.k) + r0 * row_in, at(A.v) + r0 * row_in,
+                                    reinterpret_cast<const float*>(at(A.la) + r0 * row_g),
+                                    reinterpret_cast<const float*>(at(A.be) + r0 * row_g), d_cw, d_wk, d_wp,
+                                    d_wb, nullptr, nullptr, d_out, final_state ? fs : nullptr, d_lens,
+                                    at(A.ws), A.ws_bytes, s_comp, weights_ready);
       if (rc != PRISM_OK) return rc;
+      weights_ready = true;
     } else {
       const int e = std::min(a1, len1);          // valid tokens of this segment: [a0, e)
       if (e > a0) {
@@ -240,13 +252,14 @@ extern "C" PRISM_API int prism_forward_host(const prism_dims* dims, const void* 
         pd.flags |= PRISM_FLAG_VHIST_TOKEN_MAJOR;
         const int nxt = cur == 0 ? 1 : 0;
         const void* hist = a0 > 0 ? at(A.v) + ((size_t)a0 - w) * row_in : nullptr;
-        rc = prism_forward_from(&pd, at(A.q) + r0 * row_in, at(A.k) + r0 * row_in, at(A.v) + r0 * row_in,
-                                reinterpret_cast<const float*>(at(A.la) + r0 * row_g),
-                                reinterpret_cast<const float*>(at(A.be) + r0 * row_g), d_cw, d_wk, d_wp,
-                                d_wb, cur >= 0 ? reinterpret_cast<const float*>(st[cur]) : nullptr, hist,
-                                d_out, reinterpret_cast<float*>(st[nxt]), nullptr, at(A.ws), A.ws_bytes,
-                                s_comp);
+        rc = prism::forward_from_impl(&pd, at(A.q) + r0 * row_in, at(A.k) + r0 * row_in, at(A.v) + r0 * row_in,
+                                      reinterpret_cast<const float*>(at(A.la) + r0 * row_g),
+                                      reinterpret_cast<const float*>(at(A.be) + r0 * row_g), d_cw, d_wk,
+                                      d_wp, d_wb, cur >= 0 ? reinterpret_cast<const float*>(st[cur]) : nullptr,
+                                      hist, d_out, reinterpret_cast<float*>(st[nxt]), nullptr, at(A.ws),
+                                      A.ws_bytes, s_comp, weights_ready);
         if (rc != PRISM_OK) return rc;
+        weights_ready = true;
         cur = nxt;
       }
       if (e < a1) {                              // padding rows of this segment read 0

@@ -358,7 +358,7 @@ def forward_inputs(inp: dict, L: int, chunk: int, **kw):
                          seq_lens=inp.get("seq_lens"), **kw)
 
 
-def plan_pieces(dims: Dims, pieces=8, min_piece_bytes=32 << 20):
+def plan_pieces(dims: Dims, pieces=12, min_piece_bytes=8 << 20):
     """How prism_forward_host cuts the work for these dims: a list of (start, end) ranges of
     sequences when B > 1, or of chunk-aligned token ranges when B = 1 (each at least
     max(chunk, w) tokens so the next segment's history lies inside its predecessor), at
@@ -370,7 +370,7 @@ def plan_pieces(dims: Dims, pieces=8, min_piece_bytes=32 << 20):
     return [(bounds[i], bounds[i + 1]) for i in range(n.value)]
 
 
-def host_arena_bytes(dims: Dims, pieces=8, min_piece_bytes=32 << 20) -> int:
+def host_arena_bytes(dims: Dims, pieces=12, min_piece_bytes=8 << 20) -> int:
     return int(load().prism_host_arena_bytes(ctypes.byref(dims), pieces, min_piece_bytes))
 
 
@@ -390,8 +390,8 @@ class HostPipeline:
     arena and the streams are kept across calls.
     """
 
-    def __init__(self, shapes: dict, dtype, L, chunk, *, pieces=8, device="cuda", no_gelu=False,
-                 min_piece_bytes=32 << 20):
+    def __init__(self, shapes: dict, dtype, L, chunk, *, pieces=12, device="cuda", no_gelu=False,
+                 min_piece_bytes=8 << 20):
         B, T, H, D = shapes["q"]
         self.dev = torch.device(device)
         self.dims = make_dims(B, T, H, D, D, shapes["conv_w"][1], L, chunk, dtype, no_gelu)
