@@ -90,7 +90,9 @@ struct WeightBlock {
 
 // Converts W_k, W_p (fp32 [H][L][D][D]) into fp16 hi/lo blocks; sets *flag if
 // any lo half is significant (|lo| > 2^-22 of its row norm), in which case the
-// projections take a third pass with the lo halves.
+// projections take a third pass with the lo halves.  For 32 <= d < 128 the D rows repeat
+// down the block's 128 rows, so the projections land in every TMEM lane quarter (the
+// epilogue spreads a chunk's tokens over the copies).
 template <int D>
 __global__ void prep_weights_kernel(const float* Wk, const float* Wp, int H, int L,
                                     unsigned char* blocks, int* flag) {
@@ -103,13 +105,14 @@ __global__ void prep_weights_kernel(const float* Wk, const float* Wp, int H, int
   bool need = false;
   for (int row = warp; row < 128; row += nwarp) {
     float n2 = 0.f;
-    if (row < D)
-      for (int c = lane; c < D; c += 32) { const float x = W[(size_t)row * D + c]; n2 = fmaf(x, x, n2); }
+    const bool live = D >= 32 || row < D;      // d = 16: one copy (rows 16..127 zero)
+    if (live)
+      for (int c = lane; c < D; c += 32) { const float x = W[(size_t)(row % D) * D + c]; n2 = fmaf(x, x, n2); }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
     const float tol = sqrtf(n2) * 0x1p-22f;
     for (int c = lane; c < D; c += 32) {
-      const float x = row < D ? W[(size_t)row * D + c] : 0.f;
+      const float x = live ? W[(size_t)(row % D) * D + c] : 0.f;
       __half h, l;
       tc::split_f16(x, h, l);
       const uint32_t off = (c / 8) * 2048u + row * 16u + (c % 8) * 2u;
@@ -148,6 +151,12 @@ struct PrepSmem {
   static constexpr int NTA = NT + 32;                    // all threads (with the producer warp)
   static constexpr int kMinBlocks = NTA <= 288 ? 2 : 1;   // CTAs per SM the registers must allow
   static constexpr int NTH = C / CG;                     // token columns per thread
+  // Feature role (anchor, passes A and B): the projections arrive RF times over in TMEM
+  // (the weight rows repeat), in whole lane quarters when d >= 32, so replica rf of a
+  // feature takes NTF = C / (CG RF) of its column group's tokens (at least 8).
+  static constexpr int NQF = D >= 32 ? D / 32 : 1;       // lane quarters per replica
+  static constexpr int RF = (D >= 32 && D < 128) ? (128 / D < C / (8 * CG) ? 128 / D : C / (8 * CG)) : 1;
+  static constexpr int NTF = C / (CG * RF);
   static constexpr int NFD = D / CG;                     // feature columns per thread
   static constexpr int NQ = (D + 31) / 32;               // lane quarters that hold features
   static constexpr uint32_t kW = WeightBlock<D>::bytes;  // 128 x D
@@ -219,7 +228,7 @@ struct PrepSmem {
   static constexpr uint32_t tmem_cols =
       tmem_cols_needed <= 32 ? 32 : tmem_cols_needed <= 64 ? 64 : tmem_cols_needed <= 128 ? 128
                                   : tmem_cols_needed <= 256 ? 256 : 512;
-  static_assert(NTH % 8 == 0 && NFD % 8 == 0, "column groups of 8");
+  static_assert(NTH % 8 == 0 && NFD % 8 == 0 && NTF % 8 == 0 && RF >= 1, "column groups of 8");
   static_assert(tmem_cols_needed <= 512, "TMEM");
 };
 
@@ -378,6 +387,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
     prep_tc_kernel(const __grid_constant__ PrepArgs p) {
   using S = PrepSmem<D, C>;
   constexpr int NT = S::NT, NW = S::NW, NTH = S::NTH, NFD = S::NFD, NQ = S::NQ;
+  constexpr int RF = S::RF, NTF = S::NTF, NQF = S::NQF;
   extern __shared__ __align__(1024) unsigned char sm[];
   unsigned char* sX = sm + S::oX;
   unsigned char* sY = sm + S::oY;
@@ -425,6 +435,13 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
   const int total = p.B * H * NC;
   const bool need_lo = *p.wflag != 0;
   const bool cvalid = row < D && !producer;
+  // feature role: lane row holds feature cf, replica rf (quarter qf of it) and takes tokens
+  // tf0 .. tf0+NTF-1 of its column group
+  const int cf = row % D;
+  const int rf = D >= 32 ? quarter / NQF : 0, qf = D >= 32 ? quarter % NQF : 0;
+  const bool fwarp_f = !producer && quarter < (D >= 32 ? NQF * RF : 1);   // warp-uniform
+  const bool fvalid = fwarp_f && (D >= 32 || row < D);
+  const int tf0 = (cg * RF + rf) * NTF;
   constexpr int NG = (C + 31) / 32;
   __nv_bfloat16* kqraw = reinterpret_cast<__nv_bfloat16*>(sKl);   // [2C][D]: K rows, then Q rows
   __nv_bfloat16* vwin = reinterpret_cast<__nv_bfloat16*>(sD);     // [C + 8][D]: tokens t0-8 .. t0+C-1
@@ -566,9 +583,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
     const int j = 8 - m;
-    ca[m] = (cvalid && j <= w) ? tc::ldg_early(p.conv_w + ((size_t)h * w + (j - 1)) * D + row) : 0.f;
+    ca[m] = (fvalid && j <= w) ? tc::ldg_early(p.conv_w + ((size_t)h * w + (j - 1)) * D + cf) : 0.f;
   }
-  float wb_next = (L > 0 && cvalid) ? tc::ldg_early(p.wbeta + (size_t)h * L * D + row) : 0.f;
+  float wb_next = (L > 0 && fvalid) ? tc::ldg_early(p.wbeta + (size_t)h * L * D + cf) : 0.f;
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -708,32 +725,32 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
     }
   }
   csync<NT>();
-  const int c = row;
-  const bool fwarp = quarter < NQ;             // warp holds feature rows
+  const int c = cf;
+  const bool fwarp = quarter < NQ;             // warp holds feature rows (token-row role: N^T)
 
   // ---- anchor u = sum_j c_j (.) v_{t-j} (the U tile, hi + lo) and residual r = v - u
-  //      (registers); thread (feature c, column group) owns tokens tb0 .. tb0+NTH-1 ----
-  float rres[NTH];
+  //      (registers); thread (feature c, replica, column group) owns tokens tf0 .. tf0+NTF-1 ----
+  float rres[NTF];
   {
 #pragma unroll
-    for (int j8 = 0; j8 < NTH; j8 += 8) {
-      if (fwarp) {
+    for (int j8 = 0; j8 < NTF; j8 += 8) {
+      if (fwarp_f) {
         float win[16], uu[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) win[i] = cvalid ? __bfloat162float(vwin[(tb0 + j8 + i) * D + c]) : 0.f;
+        for (int i = 0; i < 16; ++i) win[i] = fvalid ? __bfloat162float(vwin[(tf0 + j8 + i) * D + c]) : 0.f;
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
           float u = 0.f;
 #pragma unroll
           for (int m = 0; m < 8; ++m) u = fmaf(ca[m], win[jj + m], u);
           uu[jj] = u;
-          rres[j8 + jj] = (tb0 + j8 + jj < nv) ? win[jj + 8] - u : 0.f;
+          rres[j8 + jj] = (tf0 + j8 + jj < nv) ? win[jj + 8] - u : 0.f;
         }
-        if (cvalid) {
+        if (fvalid) {
           // U tile, MN-major B operand (K = features, N = tokens): (c, t) at (t/8)*16D + c*16 + (t%8)*2
           uint4 uh, ul;
           tc::split8(uu, uh, ul);
-          const uint32_t off = ((tb0 + j8) / 8) * (16u * D) + c * 16u;
+          const uint32_t off = ((tf0 + j8) / 8) * (16u * D) + c * 16u;
           *reinterpret_cast<uint4*>(sU + off) = uh;
           *reinterpret_cast<uint4*>(sU + S::kU + off) = ul;
         }
@@ -796,17 +813,17 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
     //     quarter-0 warps keep their sums, the others leave them in shared memory.
     {
       const float wb = wb_next;
-      if (l + 1 < L && cvalid) wb_next = tc::ldg_early(p.wbeta + ((size_t)h * L + l + 1) * D + c);   // next step's
-      float keep_n[NTH / 8], keep_z[NTH / 8];
-      float kh[NTH];                           // k_hat of this thread's feature and tokens
-      if (fwarp) {
+      if (l + 1 < L && fvalid) wb_next = tc::ldg_early(p.wbeta + ((size_t)h * L + l + 1) * D + c);   // next step's
+      float keep_n[NTF / 8], keep_z[NTF / 8];
+      float kh[NTF];                           // k_hat of this thread's feature and tokens
+      if (fwarp_f) {
 #pragma unroll
-        for (int j8 = 0; j8 < NTH; j8 += 8) {
+        for (int j8 = 0; j8 < NTF; j8 += 8) {
           uint32_t kr[8];
-          tc::ld8a(t_kl + lane_base + tb0 + j8, kr);
+          tc::ld8a(t_kl + lane_base + tf0 + j8, kr);
           float uf[8];                            // u = hi + lo from the U tile
-          if (cvalid) {
-            const uint32_t off = ((tb0 + j8) / 8) * (16u * D) + c * 16u;
+          if (fvalid) {
+            const uint32_t off = ((tf0 + j8) / 8) * (16u * D) + c * 16u;
             float uh[8], ul[8];
             h8_to_f(*reinterpret_cast<const uint4*>(sU + off), uh);
             h8_to_f(*reinterpret_cast<const uint4*>(sU + S::kU + off), ul);
@@ -846,13 +863,13 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
             }
           }
           if ((lane & 3) == 0) {                // lane holds token j8 + lane/4 of its group
-            const int t = tb0 + j8 + (lane >> 2);
-            if (quarter == 0) {
+            const int t = tf0 + j8 + (lane >> 2);
+            if (qf == 0) {
               keep_n[j8 / 8] = rn[0];
               keep_z[j8 / 8] = rz[0];
             } else {
-              spart[(quarter - 1) * 2 * C + t] = rn[0];
-              spart[(quarter - 1) * 2 * C + C + t] = rz[0];
+              spart[(qf - 1) * 2 * C + t] = rn[0];
+              spart[(qf - 1) * 2 * C + C + t] = rz[0];
             }
           }
         }
@@ -860,13 +877,13 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       // the four warps of this column group (one per lane quarter) hold all partial sums
       // of its tokens: they synchronise among themselves
       asm volatile("bar.sync %0, 128;\n" ::"r"(2 + cg) : "memory");
-      if (quarter == 0 && (lane & 3) == 0) {   // sums over the quarters, in quarter order
+      if (fwarp_f && qf == 0 && (lane & 3) == 0) {   // sums over the quarters, in quarter order
 #pragma unroll
-        for (int g = 0; g < NTH / 8; ++g) {
-          const int t = tb0 + 8 * g + (lane >> 2);
+        for (int g = 0; g < NTF / 8; ++g) {
+          const int t = tf0 + 8 * g + (lane >> 2);
           float ss = keep_n[g], zz = keep_z[g];
 #pragma unroll
-          for (int q = 1; q < NQ; ++q) {
+          for (int q = 1; q < NQF; ++q) {
             ss += spart[(q - 1) * 2 * C + t];
             zz += spart[(q - 1) * 2 * C + C + t];
           }
@@ -880,10 +897,10 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       // have read the tiles about to be rewritten; then the producer may score against it
       if (l > 0) ok &= tc::bar_wait(bar_6, spar(l - 1));
       tc::fence_after();
-      if (fwarp && cvalid) {
+      if (fvalid) {
 #pragma unroll
-        for (int j8 = 0; j8 < NTH; j8 += 8) {
-          const int tb = tb0 + j8;
+        for (int j8 = 0; j8 < NTF; j8 += 8) {
+          const int tb = tf0 + j8;
           float si[8], kd[8];
           ld_f8(sinv + tb, si);
 #pragma unroll
@@ -903,13 +920,13 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       ok &= tc::bar_wait(bar_p, spar(l));       // p^(l) ready
       tc::fence_after();
       // Pass B: residual step and the write values
-      if (fwarp) {
+      if (fwarp_f) {
 #pragma unroll
-        for (int j8 = 0; j8 < NTH; j8 += 8) {
+        for (int j8 = 0; j8 < NTF; j8 += 8) {
           uint32_t pr[8], pl[8];
-          tc::ld8a(t_p + lane_base + tb0 + j8, pr);
-          tc::ld8a(t_p + C + lane_base + tb0 + j8, pl);
-          const int tb = tb0 + j8;
+          tc::ld8a(t_p + lane_base + tf0 + j8, pr);
+          tc::ld8a(t_p + C + lane_base + tf0 + j8, pl);
+          const int tb = tf0 + j8;
           float sb[8], sd[8];
           ld_f8(sbl + tb, sb);
           ld_f8(sdec + tb, sd);
@@ -923,7 +940,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
             dv[jj] = sb[jj] * dl;
             dt[jj] = dv[jj] * sd[jj];
           }
-          if (cvalid) {
+          if (fvalid) {
             uint4 hi, lo;
             // feature x token tiles: (f, s) at (s/8)*S_s + f*16 + (s%8)*2  (f < D)
             const uint32_t off = (tb / 8) * S_s + c * 16u;

@@ -417,7 +417,7 @@ struct SegChainSmem {
 };
 template <int D>
 __global__ void __launch_bounds__(256) scan_seg_chain_kernel(ScanTcArgs p) {
-  constexpr int LDS = SegChainSmem<D>::LDS, NSL = D / kSegRows;
+  constexpr int LDS = SegChainSmem<D>::LDS, NSL = D >= kSegRows ? D / kSegRows : 1;   // (split only at d = 128)
   extern __shared__ __align__(16) float smc[];
   float* sS = smc;                             // [kSegRows][LDS]
   float* sM = smc + kSegRows * LDS;            // [D][D]
