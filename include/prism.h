@@ -182,6 +182,20 @@ PRISM_API int prism_forward_from(const prism_dims* dims,
 PRISM_API int prism_device_status(const prism_dims* dims, const void* workspace,
                                   size_t workspace_bytes, int* status, void* stream);
 
+/* (No counterpart in the pages: a debugging aid of this library.)
+ * In the bounds-checked debug build of the library (every translation unit compiled
+ * with -DPRISM_DEBUG_BOUNDS; build.py's build_debug() makes _build/debug/libprism.so),
+ * the tensor-core forward kernels (prepare, scan, the sequence split's chain) and the
+ * decode kernel check each index of their plain loads and stores, of their shared-memory
+ * tile writes and of the source ranges of their bulk copies against the extent of the
+ * array it addresses; an access that would fall outside is skipped and bit value 2 of a
+ * library-wide word is set.  This call synchronises the device and returns that word in
+ * *word (0: no violation since the last clear), clearing it when `clear` is nonzero.  In
+ * the normal build it writes 0 and returns PRISM_ERR_UNSUPPORTED.  Errors:
+ * PRISM_ERR_INVALID_ARG for a NULL word; PRISM_ERR_CUDA when the synchronisation or the
+ * copy fails.  Not covered: the fp32 path's kernels and the backward pass. */
+PRISM_API int prism_debug_bounds(int* word, int clear);
+
 /* One token of every sequence (dims->T must be 1; chunk is ignored): the
  * recurrence of §2.1-2.2 of "Technical Summary: PRISM" applied to a single token,
  * for streaming generation after a prism_forward_from / prism_forward prefix.

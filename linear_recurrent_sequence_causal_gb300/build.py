@@ -44,16 +44,30 @@ def stale() -> bool:
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
+DEBUG_LIB = os.path.join(BUILD, "debug", "libprism.so")
+
+
+def build_debug(force: bool = False, jobs: int | None = None) -> str:
+    """The bounds-checked debug build (-DPRISM_DEBUG_BOUNDS) in _build/debug/."""
+    if not force and os.path.exists(DEBUG_LIB) and not any(
+            os.path.getmtime(p) > os.path.getmtime(DEBUG_LIB) for p in _deps()):
+        return DEBUG_LIB
+    return _compile(DEBUG_LIB, os.path.join(BUILD, "debug", "obj"), ["-DPRISM_DEBUG_BOUNDS"], jobs)
+
+
 def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -> str:
     if not force and not stale():
         return LIB
+    return _compile(LIB, os.path.join(BUILD, "obj"), [], jobs, verbose)
+
+
+def _compile(lib: str, obj_dir: str, extra: list, jobs: int | None = None, verbose: bool = False) -> str:
     nvcc = _nvcc()
-    obj_dir = os.path.join(BUILD, "obj")
     os.makedirs(obj_dir, exist_ok=True)
 
     def compile_one(src):
         obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
@@ -65,12 +79,12 @@ def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -
     jobs = jobs or min(len(srcs), os.cpu_count() or 4)
     with concurrent.futures.ThreadPoolExecutor(max_workers=jobs) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -47,6 +47,7 @@ struct DecodeArgs {
   float* state;             // [B][H][D][D] in/out
   void* vhist;              // [B][H][w][D] in/out (I/O dtype), oldest first
   float* out;               // [B][H][D]
+  int* bounds;              // debug build: word of out-of-bounds accesses (else null)
 };
 
 constexpr int kDecodeMaxW = 8;   // longest conv history the entry point accepts
@@ -136,16 +137,19 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
 // W_p^(l) for m = 2l + 1) into ring slot m % nbuf, as one cp.async group.
 template <int D, int BB>
 __device__ __forceinline__ void decode_issue_slice(const DecodeArgs& p, int h, int m, int r0,
-                                                   float* ring) {
+                                                   float* ring, size_t smem_n) {
   using G = DecodeGeom<D, BB>;
   const int l = m >> 1;
-  const float* g = ((m & 1) ? p.Wp : p.Wk) + (((size_t)h * p.L + l) * D + r0) * D;
+  const float* W = (m & 1) ? p.Wp : p.Wk;
+  const float* g = W + (((size_t)h * p.L + l) * D + r0) * D;
   float* dst = ring + (size_t)(m % p.nbuf) * G::kSlice;
+  const size_t wbytes = (size_t)p.H * p.L * D * D * sizeof(float);
 #pragma unroll
   for (int j = 0; j < G::J; ++j) {
     const int f = threadIdx.x + G::NT * j;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst + 4 * f)),
-                 "l"(g + 4 * (size_t)f) : "memory");
+    if (PRISM_IN_BOUNDS(within(g + 4 * (size_t)f, 16, W, wbytes) && within(dst + 4 * f, 16, ring, smem_n), p.bounds))
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(dst + 4 * f)),
+                   "l"(g + 4 * (size_t)f) : "memory");
   }
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
@@ -196,6 +200,11 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
 
   const int nslice = 2 * L;
   const int nfirst = nslice < nbuf ? nslice : nbuf;
+  // extents of the arrays this CTA touches (the debug build checks every access)
+  int* bw = p.bounds;
+  const size_t smem_n = dyn_smem_bytes(), nBH = (size_t)p.B * p.H;
+  const size_t tok_bytes = nBH * D * sizeof(T), hist_bytes = nBH * w * D * sizeof(T);
+  const size_t state_bytes = nBH * D * D * sizeof(float);
   // another CTA's shared memory may be written only once that CTA runs: this barrier
   // phase (waited for before the first such store) says so
   cluster_arrive_relaxed();
@@ -212,12 +221,13 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
 #pragma unroll
     for (int t = 0; t < kDecodeMaxW; ++t)
       if (t < w) {
-        hx[t] = Elem<T>::to_f(hist[(size_t)t * D]);
-        cx[t] = p.conv_w[((size_t)h * w + (w - 1 - t)) * D + vc];   // tap j = w - t
+        hx[t] = Elem<T>::to_f(get(hist + (size_t)t * D, p.vhist, hist_bytes, bw));
+        cx[t] = get(p.conv_w + ((size_t)h * w + (w - 1 - t)) * D + vc, p.conv_w,
+                    (size_t)p.H * w * D * sizeof(float), bw);   // tap j = w - t
       }
-    kv = Elem<T>::to_f(static_cast<const T*>(p.k)[vbh * D + vc]);
-    qv = Elem<T>::to_f(static_cast<const T*>(p.q)[vbh * D + vc]);
-    vv = Elem<T>::to_f(static_cast<const T*>(p.v)[vbh * D + vc]);
+    kv = Elem<T>::to_f(get(static_cast<const T*>(p.k) + vbh * D + vc, p.k, tok_bytes, bw));
+    qv = Elem<T>::to_f(get(static_cast<const T*>(p.q) + vbh * D + vc, p.q, tok_bytes, bw));
+    vv = Elem<T>::to_f(get(static_cast<const T*>(p.v) + vbh * D + vc, p.v, tok_bytes, bw));
   }
   bool valid[BB];
   float la[BB], be[BB];
@@ -225,17 +235,20 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
   for (int bb = 0; bb < BB; ++bb) {
     valid[bb] = b0 + bb < p.B;
     const size_t bh = (size_t)(b0 + bb) * p.H + h;
-    la[bb] = valid[bb] ? p.log_alpha[bh] : 0.f;
-    be[bb] = valid[bb] ? p.beta[bh] : 0.f;
+    la[bb] = valid[bb] ? get(p.log_alpha + bh, p.log_alpha, nBH * sizeof(float), bw) : 0.f;
+    be[bb] = valid[bb] ? get(p.beta + bh, p.beta, nBH * sizeof(float), bw) : 0.f;
   }
   __syncthreads();
   // cp.async groups, oldest first: w_beta | the first nfirst weight slices | this CTA's
   // rows of S (each thread copies the float4s it later reads) | refills of the ring
   for (int i = tid; i < L * D / 4; i += NT)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(swb + 4 * i)),
-                 "l"(p.wbeta + (size_t)h * L * D + 4 * (size_t)i) : "memory");
+    if (PRISM_IN_BOUNDS(within(p.wbeta + (size_t)h * L * D + 4 * (size_t)i, 16, p.wbeta,
+                               (size_t)p.H * L * D * sizeof(float)) &&
+                        within(swb + 4 * i, 16, smf, smem_n), bw))
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(swb + 4 * i)),
+                   "l"(p.wbeta + (size_t)h * L * D + 4 * (size_t)i) : "memory");
   asm volatile("cp.async.commit_group;\n" ::: "memory");
-  for (int m = 0; m < nfirst; ++m) decode_issue_slice<D, BB>(p, h, m, r0, ring);
+  for (int m = 0; m < nfirst; ++m) decode_issue_slice<D, BB>(p, h, m, r0, ring, smem_n);
 #pragma unroll
   for (int bb = 0; bb < BB; ++bb)
     if (valid[bb]) {
@@ -243,8 +256,10 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
 #pragma unroll
       for (int j = 0; j < J; ++j) {
         const int f = tid + NT * j;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(sS + bb * G::kSlice + 4 * f)),
-                     "l"(st + 4 * (size_t)f) : "memory");
+        if (PRISM_IN_BOUNDS(within(st + 4 * (size_t)f, 16, p.state, state_bytes) &&
+                            within(sS + bb * G::kSlice + 4 * f, 16, smf, smem_n), bw))
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(sS + bb * G::kSlice + 4 * f)),
+                       "l"(st + 4 * (size_t)f) : "memory");
       }
     }
   asm volatile("cp.async.commit_group;\n" ::: "memory");
@@ -259,13 +274,13 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
       for (int t = kDecodeMaxW - 1; t >= 0; --t)   // j = 1 .. w: the newest row first
         if (t < w) {
           u = fmaf(cx[t], hx[t], u);
-          if (own) shs[(vb * w + t) * RB + (vc - r0)] = hx[t];
+          if (own) put(shs + (vb * w + t) * RB + (vc - r0), hx[t], smf, smem_n, bw);
         }
     }
-    vec[vc] = u;
-    vec[D + vc] = kv;
-    vec[2 * D + vc] = qv;
-    vec[3 * D + vc] = vv;
+    put(vec + vc, u, smf, smem_n, bw);
+    put(vec + D + vc, kv, smf, smem_n, bw);
+    put(vec + 2 * D + vc, qv, smf, smem_n, bw);
+    put(vec + 3 * D + vc, vv, smf, smem_n, bw);
   }
   cp_async_wait_upto(nfirst + 1);                  // w_beta is in (the rest may still fly)
   __syncthreads();
@@ -280,8 +295,9 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
   const bool writer = g % (GW / NV) == 0;
   float4 u4[BB];
 #pragma unroll
-  for (int bb = 0; bb < BB; ++bb) u4[bb] = *reinterpret_cast<const float4*>(svec + bb * 4 * D + c0);
-  float r = svec[bb_own * 4 * D + 3 * D + r0 + row_own] - svec[bb_own * 4 * D + r0 + row_own];
+  for (int bb = 0; bb < BB; ++bb) u4[bb] = get(reinterpret_cast<const float4*>(svec + bb * 4 * D + c0), smf, smem_n, bw);
+  float r = get(svec + bb_own * 4 * D + 3 * D + r0 + row_own, smf, smem_n, bw) -
+            get(svec + bb_own * 4 * D + r0 + row_own, smf, smem_n, bw);
 
   const bool gelu = !(p.flags & 1u);
   cluster_wait();                                  // every CTA of the cluster has started
@@ -300,15 +316,15 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
       const float* slp = ring + (size_t)((2 * (l + s) + 1) % nbuf) * G::kSlice;
 #pragma unroll
       for (int j = 0; j < J; ++j) {
-        const float4 wk = *reinterpret_cast<const float4*>(slk + 4 * (tid + NT * j));
-        const float4 wp = *reinterpret_cast<const float4*>(slp + 4 * (tid + NT * j));
+        const float4 wk = get(reinterpret_cast<const float4*>(slk + 4 * (tid + NT * j)), smf, smem_n, bw);
+        const float4 wp = get(reinterpret_cast<const float4*>(slp + 4 * (tid + NT * j)), smf, smem_n, bw);
 #pragma unroll
         for (int bb = 0; bb < BB; ++bb) {
           xk[s][bb * J + j] = dot4(wk, u4[bb]);
           xp[s][bb * J + j] = dot4(wp, u4[bb]);
         }
       }
-      const float4 wb4 = *reinterpret_cast<const float4*>(swb + (l + s) * D + c0);
+      const float4 wb4 = get(reinterpret_cast<const float4*>(swb + (l + s) * D + c0), smf, smem_n, bw);
 #pragma unroll
       for (int bb = 0; bb < BB; ++bb) z[s][bb] = dot4(wb4, u4[bb]);
     }
@@ -323,7 +339,7 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
     // same thread refills them
 #pragma unroll
     for (int s = 0; s < 2 * NL; ++s)
-      if (2 * l + s + nbuf < nslice) decode_issue_slice<D, BB>(p, h, 2 * l + s + nbuf, r0, ring);
+      if (2 * l + s + nbuf < nslice) decode_issue_slice<D, BB>(p, h, 2 * l + s + nbuf, r0, ring, smem_n);
 #pragma unroll
     for (int s = 0; s < NL; ++s) {
       const float x = pr[s] * r;
@@ -332,9 +348,10 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
       if (writer) {
         // this CTA's entry of k_hat^(l) into every CTA of the cluster (itself included)
         const int at = ((l + s) * BB + bb_own) * D + r0 + row_own;
+        if (PRISM_IN_BOUNDS(at >= 0 && at < L * BB * D && within(skh + at, 4, smf, smem_n), bw))
 #pragma unroll
-        for (int c = 0; c < NCL; ++c) cluster_map_mut(skh, (uint32_t)c)[at] = kh[s];
-        sdl[((l + s) * BB + bb_own) * RB + row_own] = bl[s] * dl;
+          for (int c = 0; c < NCL; ++c) cluster_map_mut(skh, (uint32_t)c)[at] = kh[s];
+        put(sdl + ((l + s) * BB + bb_own) * RB + row_own, bl[s] * dl, smf, smem_n, bw);
       }
     }
   };
@@ -354,7 +371,8 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
   for (int bb = 0; bb < BB; ++bb)
 #pragma unroll
     for (int j = 0; j < J; ++j)
-      S[bb][j] = valid[bb] ? *reinterpret_cast<const float4*>(sS + bb * G::kSlice + 4 * (tid + NT * j))
+      S[bb][j] = valid[bb] ? get(reinterpret_cast<const float4*>(sS + bb * G::kSlice + 4 * (tid + NT * j)), smf,
+                                 smem_n, bw)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
 
   // S <- alpha (S - beta (S k) k^T) + beta v k^T = alpha S + a k^T with
@@ -364,7 +382,7 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
     float x[NV];
 #pragma unroll
     for (int bb = 0; bb < BB; ++bb) {
-      k4[bb] = *reinterpret_cast<const float4*>(svec + bb * 4 * D + D + c0);
+      k4[bb] = get(reinterpret_cast<const float4*>(svec + bb * 4 * D + D + c0), smf, smem_n, bw);
 #pragma unroll
       for (int j = 0; j < J; ++j) x[bb * J + j] = dot4(S[bb][j], k4[bb]);
     }
@@ -373,7 +391,7 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
 #pragma unroll
     for (int bb = 1; bb < BB; ++bb)
       if (bb_own == bb) { al_own = la[bb]; be_own = be[bb]; }
-    const float a_own = be_own * (svec[bb_own * 4 * D + 3 * D + r0 + row_own] - expf(al_own) * sk);
+    const float a_own = be_own * (get(svec + bb_own * 4 * D + 3 * D + r0 + row_own, smf, smem_n, bw) - expf(al_own) * sk);
     const int base = (threadIdx.x & 31) - g;                      // the row group's first lane
 #pragma unroll
     for (int bb = 0; bb < BB; ++bb) {
@@ -394,11 +412,11 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
 #pragma unroll
     for (int bb = 0; bb < BB; ++bb) {
       const int lb = l * BB + bb;
-      const float4 kl = *reinterpret_cast<const float4*>(skh + lb * D + c0);
+      const float4 kl = get(reinterpret_cast<const float4*>(skh + lb * D + c0), smf, smem_n, bw);
       const float inv = rsqrtf(row_sum<GW>(dot4(kl, kl)) + 1e-6f);
 #pragma unroll
       for (int j = 0; j < J; ++j) {
-        const float dl = sdl[lb * RB + row0 + G::RSTEP * j] * inv;
+        const float dl = get(sdl + lb * RB + row0 + G::RSTEP * j, smf, smem_n, bw) * inv;
         S[bb][j].x = fmaf(dl, kl.x, S[bb][j].x);
         S[bb][j].y = fmaf(dl, kl.y, S[bb][j].y);
         S[bb][j].z = fmaf(dl, kl.z, S[bb][j].z);
@@ -413,16 +431,17 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
 #pragma unroll
     for (int bb = 0; bb < BB; ++bb) {
       const size_t bh = (size_t)(b0 + bb) * p.H + h;
-      const float4 q4 = *reinterpret_cast<const float4*>(svec + bb * 4 * D + 2 * D + c0);
+      const float4 q4 = get(reinterpret_cast<const float4*>(svec + bb * 4 * D + 2 * D + c0), smf, smem_n, bw);
       float4* st = reinterpret_cast<float4*>(p.state + (bh * D + r0) * D);
 #pragma unroll
       for (int j = 0; j < J; ++j) {
-        if (valid[bb]) st[tid + NT * j] = S[bb][j];
+        if (valid[bb]) put(st + tid + NT * j, S[bb][j], p.state, state_bytes, bw);
         x[bb * J + j] = dot4(S[bb][j], q4);
       }
     }
     const float o = group_sums<NV, GW>(x);
-    if (writer && b0 + bb_own < p.B) p.out[((size_t)(b0 + bb_own) * p.H + h) * D + r0 + row_own] = o;
+    if (writer && b0 + bb_own < p.B)
+      put(p.out + ((size_t)(b0 + bb_own) * p.H + h) * D + r0 + row_own, o, p.out, nBH * D * sizeof(float), bw);
   }
   // the history moves by one token: each CTA writes its own columns (read at the start)
   for (int i = tid; i < BB * RB; i += NT) {
@@ -430,8 +449,11 @@ __global__ void __cluster_dims__(DecodeGeom<D, BB>::NCL, 1, 1)
     if (b0 + bb < p.B) {
       const size_t bh = (size_t)(b0 + bb) * p.H + h;
       T* hist = static_cast<T*>(p.vhist) + bh * w * D + r0 + c;
-      for (int t = 0; t + 1 < w; ++t) hist[(size_t)t * D] = Elem<T>::from_f(shs[(bb * w + t + 1) * RB + c]);
-      hist[(size_t)(w - 1) * D] = Elem<T>::from_f(svec[bb * 4 * D + 3 * D + r0 + c]);
+      for (int t = 0; t + 1 < w; ++t)
+        put(hist + (size_t)t * D, Elem<T>::from_f(get(shs + (bb * w + t + 1) * RB + c, smf, smem_n, bw)), p.vhist,
+            hist_bytes, bw);
+      put(hist + (size_t)(w - 1) * D, Elem<T>::from_f(get(svec + bb * 4 * D + 3 * D + r0 + c, smf, smem_n, bw)),
+          p.vhist, hist_bytes, bw);
     }
   }
 }

@@ -75,6 +75,7 @@ struct PrepArgs {
   float* Nt;                      // [D][D]  N^T (d_k x d_v), piece-major over d_v
   float* gC;                      // [1]     gamma_C
   int* status;                    // device error word (bounded waits)
+  int* bounds;                    // debug build: word of out-of-bounds accesses (else null)
 };
 
 // One weight block: 128 rows (features, zero beyond D) x D columns, fp16,
@@ -442,6 +443,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
   const bool fwarp_f = !producer && quarter < (D >= 32 ? NQF * RF : 1);   // warp-uniform
   const bool fvalid = fwarp_f && (D >= 32 || row < D);
   const int tf0 = (cg * RF + rf) * NTF;
+  // extents of the arrays the kernel addresses (the debug build checks each access)
+  int* bw = p.bounds;
+  const size_t nBTH = (size_t)p.B * T_ * H, nmaps = (size_t)p.B * H * NC;
+  const size_t wblock_bytes = (size_t)H * L * 4 * S::kW;
+  auto sm_ok = [&](const void* ptr, size_t n) { return within(ptr, n, sm, S::bytes); };
   constexpr int NG = (C + 31) / 32;
   __nv_bfloat16* kqraw = reinterpret_cast<__nv_bfloat16*>(sKl);   // [2C][D]: K rows, then Q rows
   __nv_bfloat16* vwin = reinterpret_cast<__nv_bfloat16*>(sD);     // [C + 8][D]: tokens t0-8 .. t0+C-1
@@ -483,8 +489,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
     for (int q = 0; q < NG; ++q) {
       const int i = q * 32 + lane;
       const size_t g = ((size_t)b_ * T_ + c_ * C + i) * H + h_;
-      la[q] = (i < nv_) ? tc::ldg_early(p.log_alpha + g) : 0.f;
-      be[q] = (i < nv_) ? tc::ldg_early(p.beta + g) : 0.f;
+      const bool in = i < nv_ && PRISM_IN_BOUNDS(g < nBTH, bw);
+      la[q] = in ? tc::ldg_early(p.log_alpha + g) : 0.f;
+      be[q] = in ? tc::ldg_early(p.beta + g) : 0.f;
     }
     float run = 0.f;
 #pragma unroll
@@ -564,14 +571,20 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
   auto wblock = [&](int l, int which, int part) {
     return wsrc + WeightBlock<D>::index(h, l, L, which, part) * S::kW;
   };
+  // one weight block into dst, its copy completing on bar (skipped in the debug build if
+  // the block or the destination fall outside their arrays: the wait then runs out)
+  auto wcopy = [&](unsigned char* dst, const unsigned char* src, uint64_t* bar) {
+    if (PRISM_IN_BOUNDS(within(src, S::kW, wsrc, wblock_bytes) && sm_ok(dst, S::kW), bw))
+      tc::bulk_g2s(dst, src, S::kW, bar);
+  };
   // ---- chunk start: the producer streams W^(0) in (the previous tail is done with X and
   //      Y) and forms the decay factors from the gates it brought in; the consumers fetch
   //      their small parameters ----
   if (producer && lane == 0 && L > 0) {
     tc::bar_expect_tx(bar_wk, S::kW);
-    tc::bulk_g2s(sX, wblock(0, 0, 0), S::kW, bar_wk);
+    wcopy(sX, wblock(0, 0, 0), bar_wk);
     tc::bar_expect_tx(bar_wp, S::kW);
-    tc::bulk_g2s(sY, wblock(0, 1, 0), S::kW, bar_wp);
+    wcopy(sY, wblock(0, 1, 0), bar_wp);
   }
   if (producer) {
     if (!have_gates) gates_to_smem(cur);      // first chunk, or no prefetch
@@ -583,9 +596,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
 #pragma unroll
   for (int m = 0; m < 8; ++m) {
     const int j = 8 - m;
-    ca[m] = (fvalid && j <= w) ? tc::ldg_early(p.conv_w + ((size_t)h * w + (j - 1)) * D + cf) : 0.f;
+    ca[m] = (fvalid && j <= w && PRISM_IN_BOUNDS(((size_t)h * w + (j - 1)) * D + cf < (size_t)H * w * D, bw))
+                ? tc::ldg_early(p.conv_w + ((size_t)h * w + (j - 1)) * D + cf) : 0.f;
   }
-  float wb_next = (L > 0 && fvalid) ? tc::ldg_early(p.wbeta + (size_t)h * L * D + cf) : 0.f;
+  float wb_next = (L > 0 && fvalid && PRISM_IN_BOUNDS((size_t)h * L * D + cf < (size_t)H * L * D, bw))
+                      ? tc::ldg_early(p.wbeta + (size_t)h * L * D + cf) : 0.f;
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -623,7 +638,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
           tc::commit(bar_x);
           wait(bar_x, ph_x++ & 1);
           tc::bar_expect_tx(ldbar, S::kW);
-          tc::bulk_g2s(wbuf, wblock(l, which, 1), S::kW, ldbar);
+          wcopy(wbuf, wblock(l, which, 1), ldbar);
           wait(ldbar, ldph++ & 1);
           for (int kk = 0; kk < D / 16; ++kk)
             tc::mma(dst, tc::desc(wbuf + kk * 4096, 2048, 128), tc::desc(sU + kk * 256, 128, 16 * D), idesc_proj, true);
@@ -642,11 +657,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
           // step l-1's [G;P] tiles have been read; then k_hat^(l+1) into the other columns
           wait(bar_p, spar(l));
           tc::bar_expect_tx(bar_wp, S::kW);
-          tc::bulk_g2s(sY, wblock(l + 1, 1, 0), S::kW, bar_wp);
+          wcopy(sY, wblock(l + 1, 1, 0), bar_wp);
           wait(bar_k + (l & 1), kpar(l));
           if (l > 0) wait(bar_6, spar(l - 1));
           tc::bar_expect_tx(bar_wk, S::kW);
-          tc::bulk_g2s(sX, wblock(l + 1, 0, 0), S::kW, bar_wk);
+          wcopy(sX, wblock(l + 1, 0, 0), bar_wk);
           wait(bar_wk, ph_wk++ & 1);
           proj(l + 1, 0, t_k0 + ((l + 1) & 1) * C, sX, bar_wk, ph_wk, bar_k + ((l + 1) & 1));
         }
@@ -693,7 +708,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       if (lane == 0) {
         const size_t cbase = ((size_t)b * H + h) * NC + chunk;
         if (L > 0) {
-          tc::bulk_s2g(p.Nt + cbase * D * D, sKl, S::kNT);
+          if (PRISM_IN_BOUNDS(within(p.Nt + cbase * D * D, S::kNT, p.Nt, nmaps * D * D * 4) && sm_ok(sKl, S::kNT), bw))
+            tc::bulk_s2g(p.Nt + cbase * D * D, sKl, S::kNT);
           tc::bulk_commit();
           tc::bulk_wait_read();
         }
@@ -721,7 +737,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
     for (int idx = tid; idx < w * (D / 8); idx += NT) {
       const int rr = idx / (D / 8), pc = idx % (D / 8);
       const __nv_bfloat16* src = p.vhist + (tmaj ? (((size_t)b * w + rr) * H + h) * D : (((size_t)b * H + h) * w + rr) * D) + pc * 8;
-      *reinterpret_cast<uint4*>(vwin + (8 - w + rr) * D + pc * 8) = *reinterpret_cast<const uint4*>(src);
+      if (PRISM_IN_BOUNDS(within(src, 16, p.vhist, (size_t)p.B * H * w * D * 2) && sm_ok(vwin + (8 - w + rr) * D + pc * 8, 16), bw))
+        *reinterpret_cast<uint4*>(vwin + (8 - w + rr) * D + pc * 8) = *reinterpret_cast<const uint4*>(src);
     }
   }
   csync<NT>();
@@ -751,8 +768,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
           uint4 uh, ul;
           tc::split8(uu, uh, ul);
           const uint32_t off = ((tf0 + j8) / 8) * (16u * D) + c * 16u;
-          *reinterpret_cast<uint4*>(sU + off) = uh;
-          *reinterpret_cast<uint4*>(sU + S::kU + off) = ul;
+          put(reinterpret_cast<uint4*>(sU + off), uh, sU, 2 * S::kU, bw);
+          put(reinterpret_cast<uint4*>(sU + S::kU + off), ul, sU, 2 * S::kU, bw);
         }
       } else {
 #pragma unroll
@@ -784,7 +801,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       for (int j = 0; j < 8; ++j) f[j] = __bfloat162float(e[j]);
       o = tc::cvt8(f);
     }
-    *reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u) = o;
+    put(reinterpret_cast<uint4*>(sKQ + a8 * 2048u + r * 16u), o, sKQ, S::kKQ, bw);
   }
   // Decay mask of this thread's token row for the score tiles (fixed for the
   // chunk): rows < C strictly causal (G, A), rows C..2C-1 inclusive (P).
@@ -813,7 +830,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
     //     quarter-0 warps keep their sums, the others leave them in shared memory.
     {
       const float wb = wb_next;
-      if (l + 1 < L && fvalid) wb_next = tc::ldg_early(p.wbeta + ((size_t)h * L + l + 1) * D + c);   // next step's
+      if (l + 1 < L && fvalid && PRISM_IN_BOUNDS(((size_t)h * L + l + 1) * D + c < (size_t)H * L * D, bw))
+        wb_next = tc::ldg_early(p.wbeta + ((size_t)h * L + l + 1) * D + c);   // next step's
       float keep_n[NTF / 8], keep_z[NTF / 8];
       float kh[NTF];                           // k_hat of this thread's feature and tokens
       if (fwarp_f) {
@@ -868,8 +886,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
               keep_n[j8 / 8] = rn[0];
               keep_z[j8 / 8] = rz[0];
             } else {
-              spart[(qf - 1) * 2 * C + t] = rn[0];
-              spart[(qf - 1) * 2 * C + C + t] = rz[0];
+              put(spart + (qf - 1) * 2 * C + t, rn[0], spart, 24u * C, bw);
+              put(spart + (qf - 1) * 2 * C + C + t, rz[0], spart, 24u * C, bw);
             }
           }
         }
@@ -909,8 +927,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
           // feature x token tiles: (f, s) at (s/8)*S_s + f*16 + (s%8)*2  (f < D)
           const uint32_t off = (tb / 8) * S_s + c * 16u;
           tc::split8(kd, hi, lo);
-          *reinterpret_cast<uint4*>(sKl + off) = hi;
-          *reinterpret_cast<uint4*>(sKl + S::kF + off) = lo;
+          put(reinterpret_cast<uint4*>(sKl + off), hi, sKl, 2 * S::kF, bw);
+          put(reinterpret_cast<uint4*>(sKl + S::kF + off), lo, sKl, 2 * S::kF, bw);
         }
       }
       tc::fence_smem_to_async();
@@ -946,11 +964,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
             const uint32_t off = (tb / 8) * S_s + c * 16u;
             const uint32_t off128 = (tb / 8) * 2048u + c * 16u;
             tc::split8(dv, hi, lo);
-            *reinterpret_cast<uint4*>(sD + off) = hi;
-            *reinterpret_cast<uint4*>(sD + S::kF + off) = lo;
+            put(reinterpret_cast<uint4*>(sD + off), hi, sD, 2 * S::kF, bw);
+            put(reinterpret_cast<uint4*>(sD + S::kF + off), lo, sD, 2 * S::kF, bw);
             tc::split8(dt, hi, lo);
-            *reinterpret_cast<uint4*>(sDt + off128) = hi;
-            *reinterpret_cast<uint4*>(sDt + S::kF128 + off128) = lo;
+            put(reinterpret_cast<uint4*>(sDt + off128), hi, sDt, 2 * S::kF128, bw);
+            put(reinterpret_cast<uint4*>(sDt + S::kF128 + off128), lo, sDt, 2 * S::kF128, bw);
           }
         }
       }
@@ -976,8 +994,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
         uint4 hi, lo;
         tc::split8(val, hi, lo);
         const uint32_t off = ((tb0 + 8 * g) / 8) * 2048u + row * 16u;
-        *reinterpret_cast<uint4*>(sX + off) = hi;
-        *reinterpret_cast<uint4*>(sX + S::kF128 + off) = lo;
+        put(reinterpret_cast<uint4*>(sX + off), hi, sX, S::kX, bw);
+        put(reinterpret_cast<uint4*>(sX + S::kF128 + off), lo, sX, S::kX, bw);
       }
     }
     tc::fence_smem_to_async();
@@ -1014,7 +1032,8 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
   uint4 vr[NFD / 8];
 #pragma unroll
   for (int g = 0; g < NFD / 8; ++g)
-    vr[g] = tok_valid ? tc::ldg_early(reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t0 + s_tok) * H + h) * D + fb0 + 8 * g))
+    vr[g] = (tok_valid && PRISM_IN_BOUNDS((((size_t)b * T_ + t0 + s_tok) * H + h) * D + fb0 + 8 * g + 8 <= nBTH * D, bw))
+                ? tc::ldg_early(reinterpret_cast<const uint4*>(p.v + (((size_t)b * T_ + t0 + s_tok) * H + h) * D + fb0 + 8 * g))
                       : make_uint4(0u, 0u, 0u, 0u);
   // Where the solve's buffers avoid the tiles the last step's MMAs read (kEarlyTail), the
   // solve runs before those MMAs are waited for; otherwise after.
@@ -1058,11 +1077,11 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       if (isA) {
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) {
-          tAf[t * (C + 4) + s0 + jj] = bt * v8[jj];
+          put(tAf + t * (C + 4) + s0 + jj, bt * v8[jj], tAf, (size_t)S::sSq, bw);
           v8[jj] = (s0 + jj == t) ? 1.f : 0.f;
         }
       }
-      *reinterpret_cast<uint4*>(sTP + (s0 / 8) * 2048u + row * 16u) = tc::cvt8(v8);
+      put(reinterpret_cast<uint4*>(sTP + (s0 / 8) * 2048u + row * 16u), tc::cvt8(v8), sTP, (size_t)S::kF128, bw);
     }
   } else {
 #pragma unroll
@@ -1090,10 +1109,12 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       tc::pin(nr[g]);
       if (cvalid) {
         const int a0 = fb0 + 8 * g;
-        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4) * D + row) * 4) =
-            make_float4(u2f(nr[g][0]), u2f(nr[g][1]), u2f(nr[g][2]), u2f(nr[g][3]));
-        *reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4 + 1) * D + row) * 4) =
-            make_float4(u2f(nr[g][4]), u2f(nr[g][5]), u2f(nr[g][6]), u2f(nr[g][7]));
+        const void* nb0 = S::kStageN ? static_cast<const void*>(sKl) : static_cast<const void*>(p.Nt);
+        const size_t nbn = S::kStageN ? (size_t)S::kNT : nmaps * D * D * 4;
+        put(reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4) * D + row) * 4),
+            make_float4(u2f(nr[g][0]), u2f(nr[g][1]), u2f(nr[g][2]), u2f(nr[g][3])), nb0, nbn, bw);
+        put(reinterpret_cast<float4*>(nbase + ((size_t)(a0 / 4 + 1) * D + row) * 4),
+            make_float4(u2f(nr[g][4]), u2f(nr[g][5]), u2f(nr[g][6]), u2f(nr[g][7])), nb0, nbn, bw);
       }
     }
   }
@@ -1169,7 +1190,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
         float xf[8];
 #pragma unroll
         for (int jj = 0; jj < 8; ++jj) xf[jj] = tok_valid ? bs * (__bfloat162float(ve[jj]) - u2f(rr[g][jj])) : 0.f;
-        *reinterpret_cast<uint4*>(sKX + ((D + f0) / 8) * (16u * C) + row * 16u) = tc::cvt8(xf);
+        put(reinterpret_cast<uint4*>(sKX + ((D + f0) / 8) * (16u * C) + row * 16u), tc::cvt8(xf), sKX, (size_t)S::sKX, bw);
       }
     }
   }
@@ -1184,7 +1205,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       float kf[8];
 #pragma unroll
       for (int jj = 0; jj < 8; ++jj) kf[jj] = bg * __half2float(ke[jj]);
-      *reinterpret_cast<uint4*>(sKX + (f0 / 8) * (16u * C) + sk * 16u) = tc::cvt8(kf);
+      put(reinterpret_cast<uint4*>(sKX + (f0 / 8) * (16u * C) + sk * 16u), tc::cvt8(kf), sKX, (size_t)S::sKX, bw);
     }
   }
   tc::fence_smem_to_async();
@@ -1243,12 +1264,12 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
           kt[jj] = dct * __half2float(ke[jj]);
         }
         const int o16 = ((f0 / 8) * 2 * C + tr) * 8;   // fp16 piece (8 values)
-        *reinterpret_cast<uint4*>(oWQ + o16) = tc::cvt8(wv);
-        *reinterpret_cast<uint4*>(oQK + o16 + C * 8) = tc::cvt8(kt);
-        *reinterpret_cast<float4*>(oU + ((f0 / 4) * C + tr) * 4) =
-            make_float4(u2f(xr[0]), u2f(xr[1]), u2f(xr[2]), u2f(xr[3]));
-        *reinterpret_cast<float4*>(oU + ((f0 / 4 + 1) * C + tr) * 4) =
-            make_float4(u2f(xr[4]), u2f(xr[5]), u2f(xr[6]), u2f(xr[7]));
+        put(reinterpret_cast<uint4*>(oWQ + o16), tc::cvt8(wv), p.WQ, nmaps * 2 * C * D * 2, bw);
+        put(reinterpret_cast<uint4*>(oQK + o16 + C * 8), tc::cvt8(kt), p.QK, nmaps * 2 * C * D * 2, bw);
+        put(reinterpret_cast<float4*>(oU + ((f0 / 4) * C + tr) * 4),
+            make_float4(u2f(xr[0]), u2f(xr[1]), u2f(xr[2]), u2f(xr[3])), p.U, nmaps * C * D * 4, bw);
+        put(reinterpret_cast<float4*>(oU + ((f0 / 4 + 1) * C + tr) * 4),
+            make_float4(u2f(xr[4]), u2f(xr[5]), u2f(xr[6]), u2f(xr[7])), p.U, nmaps * C * D * 4, bw);
       } else if (isPT) {
         const uint4 qraw = *reinterpret_cast<const uint4*>(sKQ + (f0 / 8) * 2048u + row * 16u);
         const __half* qe = reinterpret_cast<const __half*>(&qraw);
@@ -1258,18 +1279,18 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
         uint4 hi, lo;
         tc::split8(qv, hi, lo);
         const int o16 = ((f0 / 8) * 2 * C + tr) * 8;
-        *reinterpret_cast<uint4*>(oWQ + o16 + C * 8) = hi;
-        *reinterpret_cast<uint4*>(oQK + o16) = lo;
-        *reinterpret_cast<float4*>(oOi + ((f0 / 4) * C + tr) * 4) =
+        put(reinterpret_cast<uint4*>(oWQ + o16 + C * 8), hi, p.WQ, nmaps * 2 * C * D * 2, bw);
+        put(reinterpret_cast<uint4*>(oQK + o16), lo, p.QK, nmaps * 2 * C * D * 2, bw);
+        put(reinterpret_cast<float4*>(oOi + ((f0 / 4) * C + tr) * 4),
             make_float4(u2f(xr[0]) + u2f(orr[0]), u2f(xr[1]) + u2f(orr[1]), u2f(xr[2]) + u2f(orr[2]),
-                        u2f(xr[3]) + u2f(orr[3]));
-        *reinterpret_cast<float4*>(oOi + ((f0 / 4 + 1) * C + tr) * 4) =
+                        u2f(xr[3]) + u2f(orr[3])), p.Oi, nmaps * C * D * 4, bw);
+        put(reinterpret_cast<float4*>(oOi + ((f0 / 4 + 1) * C + tr) * 4),
             make_float4(u2f(xr[4]) + u2f(orr[4]), u2f(xr[5]) + u2f(orr[5]), u2f(xr[6]) + u2f(orr[6]),
-                        u2f(xr[7]) + u2f(orr[7]));
+                        u2f(xr[7]) + u2f(orr[7])), p.Oi, nmaps * C * D * 4, bw);
       }
     }
   }
-  if (tid == 0) p.gC[cbase] = tgam[C - 1];
+  if (tid == 0) put(p.gC + cbase, tgam[C - 1], p.gC, nmaps * 4, bw);
   }  // consumers
   // end of chunk: every role is done with this chunk's shared memory and TMEM
   tc::fence_smem_to_async();

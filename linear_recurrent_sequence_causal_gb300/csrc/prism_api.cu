@@ -82,7 +82,23 @@ static cudaError_t launch_weights(int D, const float* Wk, const float* Wp, int H
 }
 }  // namespace prism
 
+#ifdef PRISM_DEBUG_BOUNDS
+// the debug build's word of out-of-bounds accesses (prism_debug_bounds), shared by every
+// kernel of the library through the pointer each launch passes
+__device__ int g_bounds_word;
+#endif
+
 namespace {
+
+// the bounds word's device address in the debug build, null otherwise
+int* bounds_word() {
+#ifdef PRISM_DEBUG_BOUNDS
+  void* p = nullptr;
+  return cudaGetSymbolAddress(&p, g_bounds_word) == cudaSuccess ? static_cast<int*>(p) : nullptr;
+#else
+  return nullptr;
+#endif
+}
 
 constexpr size_t kMaxSmem = 232448;   // 227 KB: opt-in dynamic shared memory per CTA
 constexpr int kMaxL = 8, kMaxW = 8;
@@ -310,6 +326,7 @@ int prepare_impl(const prism_dims* dims, const void* q, const void* k, const voi
   a.Nt = region<float>(workspace, Lo, PRISM_WS_N);
   a.gC = region<float>(workspace, Lo, PRISM_WS_GC);
   a.status = status;
+  a.bounds = bounds_word();
   return prism::launch_prep(D, C, a, s) == cudaSuccess ? PRISM_OK : PRISM_ERR_LAUNCH;
 }
 }  // namespace
@@ -360,6 +377,7 @@ int scan_impl(const prism_dims* dims, const void* q, const void* k, const void* 
     a.gC = region<const float>(workspace, Lo, PRISM_WS_GC);
     a.seq_lens = seq_lens; a.out = out; a.final_state = final_state; a.initial_state = initial_state;
     a.status = region<int>(workspace, Lo, PRISM_WS_STATUS);
+    a.bounds = bounds_word();
     a.nseg = scan_segments(dims);
     a.phase = 0;
     a.check_timeout = (dims->flags & PRISM_FLAG_CHECK_WAIT_TIMEOUT) ? 1 : 0;
@@ -427,6 +445,23 @@ extern "C" PRISM_API int prism_forward(const prism_dims* dims, const void* q, co
                             out, final_state, seq_lens, workspace, workspace_bytes, stream);
 }
 
+extern "C" PRISM_API int prism_debug_bounds(int* word, int clear) {
+  if (!word) return PRISM_ERR_INVALID_ARG;
+#ifdef PRISM_DEBUG_BOUNDS
+  if (cudaDeviceSynchronize() != cudaSuccess || cudaMemcpyFromSymbol(word, g_bounds_word, sizeof(int)) != cudaSuccess)
+    return PRISM_ERR_CUDA;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_bounds_word, &zero, sizeof(int)) != cudaSuccess) return PRISM_ERR_CUDA;
+  }
+  return PRISM_OK;
+#else
+  (void)clear;
+  *word = 0;
+  return PRISM_ERR_UNSUPPORTED;
+#endif
+}
+
 extern "C" PRISM_API int prism_device_status(const prism_dims* dims, const void* workspace,
                                              size_t workspace_bytes, int* status, void* stream) {
   const int rc = check_dims(dims);
@@ -470,6 +505,7 @@ extern "C" PRISM_API int prism_decode_step(const prism_dims* dims, const void* q
   a.B = dims->B; a.H = dims->H; a.w = dims->conv_width; a.L = dims->L; a.flags = dims->flags;
   a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.conv_w = conv_w;
   a.Wk = Wk; a.Wp = Wp; a.wbeta = wbeta; a.state = state; a.vhist = v_hist; a.out = out;
+  a.bounds = bounds_word();
   return prism::launch_decode(dims->dtype == PRISM_F32 ? 0 : 1, D, a, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? PRISM_OK

@@ -29,6 +29,43 @@ template <> struct Elem<__nv_bfloat16> {
   static constexpr int kPad = 8;       // 16 bytes: ldmatrix rows land in distinct banks
 };
 
+// Bounds checks of the debug build (compiled with PRISM_DEBUG_BOUNDS): an access whose
+// index falls outside its array is skipped and bit 2 of the word `bounds` records it
+// (prism_debug_bounds reads the word).  In the normal build every check is the constant
+// true, the word is never touched and the code is the same as without the checks.
+#ifdef PRISM_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(bool ok, int* word) {
+  if (!ok && word) atomicOr(word, 2);
+  return ok;
+}
+#define PRISM_IN_BOUNDS(cond, word) ::prism::in_bounds((cond), (word))
+#else
+#define PRISM_IN_BOUNDS(cond, word) true
+#endif
+// [p, p + bytes) inside [base, base + extent)
+__device__ __forceinline__ bool within(const void* p, size_t bytes, const void* base, size_t extent) {
+  const char* a = static_cast<const char*>(p);
+  const char* o = static_cast<const char*>(base);
+  return a >= o && a + bytes <= o + extent;
+}
+
+// checked store / load: the access happens only when [ptr, ptr + sizeof(T)) lies inside
+// [base, base + extent) (always, in the normal build)
+template <class T>
+__device__ __forceinline__ void put(T* ptr, const T& v, const void* base, size_t extent, int* word) {
+  if (PRISM_IN_BOUNDS(within(ptr, sizeof(T), base, extent), word)) *ptr = v;
+}
+template <class T>
+__device__ __forceinline__ T get(const T* ptr, const void* base, size_t extent, int* word) {
+  return PRISM_IN_BOUNDS(within(ptr, sizeof(T), base, extent), word) ? *ptr : T();
+}
+// bytes of dynamic shared memory this launch has
+__device__ __forceinline__ uint32_t dyn_smem_bytes() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;\n" : "=r"(n));
+  return n;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

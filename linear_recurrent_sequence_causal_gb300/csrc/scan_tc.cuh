@@ -51,6 +51,7 @@ struct ScanTcArgs {
   float* final_state;    // [B][H][d_v][d_k] or null
   const float* initial_state;   // [B][H][d_v][d_k] entering state, or null (zero)
   int* status;           // device error word (bounded waits)
+  int* bounds;           // debug build: word of out-of-bounds accesses (else null)
   // Sequence split.  phase 0: one chain per sequence (nseg = 1); phase 1: segment 0 in
   // full plus the affine maps of segments 1..nseg-1; phase 3: segments 1..nseg-1 in full
   // from seg_start.  Arrays [B][H][nseg][D][D], rows d_v (or, for seg_M, d_k) by d_k.
@@ -138,6 +139,15 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
   const size_t cb0 = ((size_t)b * H + h) * NC + c_lo;
   const bool last_seg = seg == nseg - 1;
   const size_t seg_off = (((size_t)b * H + h) * nseg + seg) * D * D;
+  // extents of the arrays the kernel addresses (the debug build checks each access)
+  int* bw = p.bounds;
+  const size_t nmaps = (size_t)p.B * H * NC, state_bytes = (size_t)p.B * H * D * D * 4;
+  const size_t seg_bytes = (size_t)p.B * H * p.nseg * D * D * 4;
+  auto copy_in = [&](unsigned char* dst, const void* src, uint32_t bytes, const void* base, size_t extent,
+                     uint64_t* bar) {
+    if (PRISM_IN_BOUNDS(within(src, bytes, base, extent) && within(dst, bytes, sm, S::bytes), bw))
+      tc::bulk_g2s(dst, src, bytes, bar);
+  };
   const float* useN = useU ? p.Nt : nullptr;
 
   if (tid == 0) {
@@ -170,13 +180,17 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
         const size_t cb = cb0 + c;
         tc::bar_expect_tx(bar_full + buf, 2 * S::kMap + (useU ? S::kU : 0) + (outputs ? S::kU : 0) +
                                               (useN ? S::kN : 0));
-        tc::bulk_g2s(base + S::oWQ, p.WQ + cb * 2 * C * D, S::kMap, bar_full + buf);
-        tc::bulk_g2s(base + S::oQK, p.QK + cb * 2 * C * D, S::kMap, bar_full + buf);
+        copy_in(base + S::oWQ, p.WQ + cb * 2 * C * D, S::kMap, p.WQ, nmaps * 2 * C * D * 2, bar_full + buf);
+        copy_in(base + S::oQK, p.QK + cb * 2 * C * D, S::kMap, p.QK, nmaps * 2 * C * D * 2, bar_full + buf);
         if (useU)
-          tc::bulk_g2s(base + S::oU, p.U + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, bar_full + buf);
+          copy_in(base + S::oU, p.U + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, p.U, nmaps * C * D * 4,
+                  bar_full + buf);
         if (outputs)
-          tc::bulk_g2s(base + S::oOi, p.Oi + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, bar_full + buf);
-        if (useN) tc::bulk_g2s(base + S::oN, useN + cb * D * D + (size_t)(v0 / 4) * D * 4, S::kN, bar_full + buf);
+          copy_in(base + S::oOi, p.Oi + cb * C * D + (size_t)(v0 / 4) * C * 4, S::kU, p.Oi, nmaps * C * D * 4,
+                  bar_full + buf);
+        if (useN)
+          copy_in(base + S::oN, useN + cb * D * D + (size_t)(v0 / 4) * D * 4, S::kN, useN, nmaps * D * D * 4,
+                  bar_full + buf);
       };
       auto wait = [&](uint64_t* bar, uint32_t parity) {
         ok &= tc::bar_wait(bar, parity);
@@ -226,7 +240,9 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
 #pragma unroll
     for (int v = 0; v < HB; ++v)
       st[v] = !krow ? 0.f
-              : s0  ? s0[(size_t)(v0 + hf * HB + v) * D + k]
+              : s0  ? get(s0 + (size_t)(v0 + hf * HB + v) * D + k, seg == 0 ? static_cast<const void*>(p.initial_state)
+                                                                          : static_cast<const void*>(p.seg_start),
+                          seg == 0 ? state_bytes : seg_bytes, bw)
                     : (kind == 2 && v0 + hf * HB + v == k) ? 1.f : 0.f;
     auto write_state = [&]() {                 // [S_hi | S_lo]^T rows: (k, n) at (n/8)*16D + k*16 + (n%8)*2
 #pragma unroll
@@ -256,7 +272,7 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
       const float* sN = reinterpret_cast<const float*>(base + S::oN);
       const size_t cbase = cb0 + c;
       const int t0 = (c_lo + c) * C, nv = min(C, len - t0);
-      const float gC = tc::ldg_early(p.gC + cbase);
+      const float gC = PRISM_IN_BOUNDS(cbase < nmaps, bw) ? tc::ldg_early(p.gC + cbase) : 0.f;
       ok &= tc::bar_wait(bar_mma1, c & 1);
       tc::fence_after();
       // ---- E = U - W S0^T (lanes < C); O = O_intra + Qt_hi S0^T (lanes C..2C-1) ----
@@ -372,8 +388,9 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
 #pragma unroll
           for (int g = 0; g < HB / 4; ++g) {
             const float4 x = *reinterpret_cast<const float4*>(sX + r * S::LDX + hf * HB + 4 * g);
-            *reinterpret_cast<float4*>(dst + 4 * g) =
-                make_float4(ov[4 * g] + x.x, ov[4 * g + 1] + x.y, ov[4 * g + 2] + x.z, ov[4 * g + 3] + x.w);
+            put(reinterpret_cast<float4*>(dst + 4 * g),
+                make_float4(ov[4 * g] + x.x, ov[4 * g + 1] + x.y, ov[4 * g + 2] + x.z, ov[4 * g + 3] + x.w), p.out,
+                (size_t)p.B * T_ * H * D * 4, bw);
           }
         }
       }
@@ -384,7 +401,7 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
       const int t_hi = (p.phase == 0 || last_seg) ? T_ : min(T_, (seg + 1) * p.seg_chunks * C);
       for (size_t idx = tid; idx < (size_t)max(t_hi - t_lo, 0) * BV; idx += NW * 32) {
         const int t = t_lo + (int)(idx / BV), col = (int)(idx % BV);
-        p.out[(((size_t)b * T_ + t) * H + h) * D + v0 + col] = 0.f;
+        put(p.out + (((size_t)b * T_ + t) * H + h) * D + v0 + col, 0.f, p.out, (size_t)p.B * T_ * H * D * 4, bw);
       }
     }
     // end state: the final state (last segment), segment 1's entering state (segment 0 of
@@ -395,8 +412,13 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
               : p.phase == 1 ? p.seg_start + seg_off + (size_t)D * D
               : nullptr;
     if (fs && krow) {
+      const void* fbase = (kind == 0 && (p.phase == 0 || last_seg)) ? static_cast<const void*>(p.final_state)
+                          : kind == 1 ? static_cast<const void*>(p.seg_c)
+                          : kind == 2 ? static_cast<const void*>(p.seg_M)
+                                      : static_cast<const void*>(p.seg_start);
+      const size_t fext = (kind == 0 && (p.phase == 0 || last_seg)) ? state_bytes : seg_bytes;
 #pragma unroll
-      for (int v = 0; v < HB; ++v) fs[(size_t)(v0 + hf * HB + v) * D + k] = st[v];
+      for (int v = 0; v < HB; ++v) put(fs + (size_t)(v0 + hf * HB + v) * D + k, st[v], fbase, fext, bw);
     }
   }
   if (!ok) atomicExch(p.status, 1);
@@ -425,21 +447,23 @@ __global__ void __launch_bounds__(256) scan_seg_chain_kernel(ScanTcArgs p) {
   const int r0 = slice * kSegRows, tid = threadIdx.x;
   const int row = tid / 8, cg = tid % 8;       // row r0 + row, columns cg + 8 i
   const size_t base = (size_t)bh * p.nseg * D * D;
+  int* bw = p.bounds;
+  const size_t seg_bytes = (size_t)p.B * p.H * p.nseg * D * D * 4;
   for (int i = tid; i < kSegRows * D / 4; i += 256) {
     const int rr = i / (D / 4), c4 = i % (D / 4);
-    *reinterpret_cast<float4*>(sS + rr * LDS + 4 * c4) = *reinterpret_cast<const float4*>(
-        p.seg_start + base + (size_t)D * D + (size_t)(r0 + rr) * D + 4 * c4);
+    *reinterpret_cast<float4*>(sS + rr * LDS + 4 * c4) = get(reinterpret_cast<const float4*>(
+        p.seg_start + base + (size_t)D * D + (size_t)(r0 + rr) * D + 4 * c4), p.seg_start, seg_bytes, bw);
   }
   for (int s = 1; s + 1 < p.nseg; ++s) {
     const float* M = p.seg_M + base + (size_t)s * D * D;
     const float* cc = p.seg_c + base + (size_t)s * D * D + (size_t)r0 * D;
     __syncthreads();                           // sS complete; the previous sM fully read
     for (int i = tid; i < D * D / 4; i += 256)
-      reinterpret_cast<float4*>(sM)[i] = reinterpret_cast<const float4*>(M)[i];
+      reinterpret_cast<float4*>(sM)[i] = get(reinterpret_cast<const float4*>(M) + i, p.seg_M, seg_bytes, bw);
     __syncthreads();
     float acc[D / 8];
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) acc[i] = cc[(size_t)row * D + cg + 8 * i];
+    for (int i = 0; i < D / 8; ++i) acc[i] = get(cc + (size_t)row * D + cg + 8 * i, p.seg_c, seg_bytes, bw);
 #pragma unroll 4
     for (int j = 0; j < D; ++j) {
       const float sv = sS[row * LDS + j];
@@ -451,7 +475,7 @@ __global__ void __launch_bounds__(256) scan_seg_chain_kernel(ScanTcArgs p) {
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) {
       sS[row * LDS + cg + 8 * i] = acc[i];
-      dst[(size_t)row * D + cg + 8 * i] = acc[i];
+      put(dst + (size_t)row * D + cg + 8 * i, acc[i], p.seg_start, seg_bytes, bw);
     }
   }
 }

@@ -30,7 +30,7 @@ EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "
            "prism_scan", "prism_forward_static", "prism_strerror", "prism_forward_from",
            "prism_decode_step", "prism_backward_workspace_bytes", "prism_backward",
            "prism_device_status", "prism_host_plan", "prism_host_arena_bytes",
-           "prism_forward_host", "prism_scan_segments")
+           "prism_forward_host", "prism_scan_segments", "prism_debug_bounds")
 WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC", "seg")
 
 
@@ -61,7 +61,9 @@ def load():
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.LIB
+            # PRISM_LIBRARY selects another build of the same library (the bounds-checked
+            # debug build, build.build_debug())
+            path = os.environ.get("PRISM_LIBRARY") or _build.LIB
             if not os.path.exists(path):
                 raise RuntimeError(f"libprism.so not built ({path}); run __graft_entry__.build()")
             lib = ctypes.CDLL(path)
@@ -89,6 +91,8 @@ def load():
             lib.prism_device_status.argtypes = [ctypes.POINTER(Dims), _vp, ctypes.c_size_t,
                                                  ctypes.POINTER(ctypes.c_int), _vp]
             lib.prism_device_status.restype = ctypes.c_int
+            lib.prism_debug_bounds.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int]
+            lib.prism_debug_bounds.restype = ctypes.c_int
             lib.prism_host_plan.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_size_t,
                                             ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
             lib.prism_host_plan.restype = ctypes.c_int
@@ -166,6 +170,17 @@ def _dims_for(q, v, conv_w, L, chunk, no_gelu=False, flags=0) -> Dims:
 
 def alloc_workspace(dims: Dims, device) -> torch.Tensor:
     return torch.empty(max(workspace_bytes(dims), 1), dtype=torch.uint8, device=device)
+
+
+def debug_bounds(clear: bool = True):
+    """The debug build's word of out-of-bounds accesses (0: none; synchronises the
+    device), or None when the loaded library is the normal build."""
+    word = ctypes.c_int(-1)
+    rc = load().prism_debug_bounds(ctypes.byref(word), 1 if clear else 0)
+    if ERRORS.get(rc) == "PRISM_ERR_UNSUPPORTED":   # not the debug build
+        return None
+    _check(rc)
+    return word.value
 
 
 def device_status(dims: Dims, workspace, stream=None) -> int:

@@ -196,3 +196,14 @@ def test_scan_segments_rule(lib):
                                           flags=prism.PRISM_FLAG_NO_SEQ_SPLIT)
                 assert prism.workspace_layout(nosplit)["seg"] is None
                 assert prism.workspace_bytes(nosplit) == lay["seg"]
+
+
+def test_debug_bounds_word_only_in_the_debug_build(lib):
+    """The normal build answers that it is not the bounds-checked one (no GPU touched)."""
+    if os.environ.get("PRISM_LIBRARY"):
+        pytest.skip("another build of the library is loaded")
+    word = ctypes.c_int(-1)
+    assert lib.prism_debug_bounds(ctypes.byref(word), 0) == 2      # PRISM_ERR_UNSUPPORTED
+    assert word.value == 0
+    assert lib.prism_debug_bounds(None, 0) == 1                    # PRISM_ERR_INVALID_ARG
+    assert prism.debug_bounds() is None
