@@ -14,15 +14,25 @@ cudaError_t launch_prep_t(const PrepArgs& a, cudaStream_t s) {
   auto fn = prep_tc_kernel<D, C>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::bytes);
   if (e != cudaSuccess) return e;
-  // Where the next chunk's tiles can come in during a tail (S::kPrefetch), one persistent CTA
-  // per SM walks the chunks; otherwise one CTA per chunk.
+  // Persistent CTAs walk the chunks (the next chunk's tiles come in during a tail): as many
+  // as are resident at once (one or two per SM), never more than there are chunks.  With
+  // per-sequence lengths the chunks past a sequence's end are skipped, which a fixed
+  // stride shares out unevenly: there each chunk gets its own CTA and the hardware
+  // scheduler balances them.
   const long long chunks = (long long)a.B * a.H * ((a.T + C - 1) / C);
   long long grid = chunks;
-  if (S::kPrefetch) {
+  if (S::kPrefetch && !a.seq_lens) {
     int dev = 0, sms = 0;
+    static int per_sm = 0;                     // CTAs resident per SM (asked once per process)
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if (grid > sms) grid = sms;
+    if (per_sm == 0) {
+      int n = 0;
+      if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, S::NTA, S::bytes)) != cudaSuccess) return e;
+      per_sm = n;
+    }
+    const long long resident = (long long)sms * (per_sm > 0 ? per_sm : 1);
+    if (grid > resident) grid = resident;
   }
   fn<<<(unsigned)grid, S::NTA, S::bytes, s>>>(a);
   return cudaGetLastError();

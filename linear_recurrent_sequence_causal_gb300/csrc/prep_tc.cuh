@@ -192,9 +192,10 @@ struct PrepSmem {
   static constexpr uint32_t sZ = 4 * 32 * 36;            // block-solve scratch
   static constexpr uint32_t sTB = 2 * C * C;             // f16 T as B operand (C x C)
   // The solve's buffers go where the refinement loop leaves memory free first (W_p and the
-  // u tiles: Y and U), so the solve can run while the last step's MMAs still read X, K_l,
-  // D and Dt; [Kb | X] is built in X once those MMAs are done.
-  static constexpr Place p0{oY, oKQ, oKl};
+  // u tiles: Y and U), then past the loop's footprint, so the solve can run while the last
+  // step's MMAs still read X, K_l, D and Dt, and the next chunk's inputs can come into the
+  // K_l and D regions meanwhile; [Kb | X] is built in X once those MMAs are done.
+  static constexpr Place p0{oY, oKQ, loop_end};
   static constexpr uint32_t tKX = oX;                    // f16 [Kb | X] MN-major, C x 2D
   static_assert(sKX <= kX, "[Kb | X] fits the X region");
   static constexpr uint32_t tTP = p0.where(kF128);       // f16 [I ; P], then [T ; PT], 128 x C
@@ -210,9 +211,9 @@ struct PrepSmem {
   static constexpr uint32_t tTB = p6.where(sTB);         // f16 T (B operand)
   static constexpr Place p7 = p6.at(sTB);
   static constexpr uint32_t bytes = p7.o2 > loop_end ? p7.o2 : loop_end;
-  // Where the tail's buffers leave the K_l and D regions free, the next chunk's K, Q rows
-  // and v window are copied there while the tail runs; otherwise after it.
-  static constexpr bool kPrefetch = p7.o2 <= oKl;
+  // The tail's buffers leave the K_l and D regions free: the next chunk's K, Q rows and v
+  // window are copied there while the tail runs.
+  static constexpr bool kPrefetch = true;
   // the same condition lets the solve start before the last step's MMAs complete
   static constexpr bool kEarlyTail = kPrefetch;
   // N^T (D x D fp32) leaves through the K_l and D regions (staged by the consumers, copied
@@ -1043,8 +1044,12 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       tc::fence_after();
     }
   }
-  // (b) [K K^T ; Q K^T] = [K ; Q] K^T   (B = the K rows of the same tile, K-major)
+  // (b) [K K^T ; Q K^T] = [K ; Q] K^T   (B = the K rows of the same tile, K-major), into
+  //     the k_hat columns of even steps: when L is odd the last step's scores are there,
+  //     so every consumer warp's [5] must have read them (bar_r5 of the last step; without
+  //     the early tail bar_6 above already implies it)
   if (tid == 0) {
+    if (S::kEarlyTail && L > 0) ok &= tc::bar_wait(bar_r5, spar(L - 1));
     tc::fence_after();
     for (int kk = 0; kk < D / 16; ++kk)
       tc::mma(t_k0, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKQ + kk * 4096, 2048, 128),
@@ -1301,6 +1306,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
   cur = nxt;
   }  // chunks
   if (!ok) atomicExch(p.status, 1);
+  // the last N^T bulk store of this CTA has been read out of shared memory; its writes
+  // complete before the CTA exits
+  if (producer && lane == 0) tc::bulk_wait_all();
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, S::tmem_cols);

@@ -186,6 +186,8 @@ __device__ __forceinline__ void bulk_s2g(void* gdst, const void* ssrc, uint32_t 
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
+// every bulk store this thread issued has completed (its writes are done), not only read
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 
 // fp32 -> (hi, lo) fp16 pair with hi + lo ~ x to ~2^-22 relative.
 __device__ __forceinline__ void split_f16(float x, __half& hi, __half& lo) {
