@@ -1045,14 +1045,15 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
     }
   }
   // (b) [K K^T ; Q K^T] = [K ; Q] K^T   (B = the K rows of the same tile, K-major), into
-  //     the k_hat columns of even steps: when L is odd the last step's scores are there,
-  //     so every consumer warp's [5] must have read them (bar_r5 of the last step; without
-  //     the early tail bar_6 above already implies it)
+  //     the k_hat columns the last refinement step did not use: with the early tail the
+  //     last step's scores may still be being read, while the other buffer's (step L-2's)
+  //     were read by every warp before its pass A of step L-1, which the producer waited
+  //     for before the scores behind bar_gp of step L-1, and this thread has passed that.
+  const uint32_t t_kk = t_k0 + (L & 1) * C;
   if (tid == 0) {
-    if (S::kEarlyTail && L > 0) ok &= tc::bar_wait(bar_r5, spar(L - 1));
     tc::fence_after();
     for (int kk = 0; kk < D / 16; ++kk)
-      tc::mma(t_k0, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKQ + kk * 4096, 2048, 128),
+      tc::mma(t_kk, tc::desc(sKQ + kk * 4096, 2048, 128), tc::desc(sKQ + kk * 4096, 2048, 128),
               idesc_cc, kk > 0);
     tc::commit(bar_mma);
   }
@@ -1070,7 +1071,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
     const float bt = isA ? tbeta[t] : 0.f;
     uint32_t ar[NTH / 8][8];
 #pragma unroll
-    for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_k0 + lane_base + tb0 + 8 * g, ar[g]);
+    for (int g = 0; g < NTH / 8; ++g) tc::ld8a(t_kk + lane_base + tb0 + 8 * g, ar[g]);
     tc::wait_ld();
 #pragma unroll
     for (int g = 0; g < NTH / 8; ++g) {
