@@ -196,6 +196,16 @@ PRISM_API int prism_device_status(const prism_dims* dims, const void* workspace,
  * copy fails.  Not covered: the fp32 path's kernels and the backward pass. */
 PRISM_API int prism_debug_bounds(int* word, int clear);
 
+/* (No counterpart in the pages: a debugging aid of this library.)
+ * y[i] = GELU(x[i]) for i < n as the bf16 path's prepare kernel evaluates it in its
+ * refinement loop: x Phi(x) with erf by Hastings' rational approximation (Abramowitz and
+ * Stegun 7.1.26), within about 4e-7 max(|x|, 1) of the exact GELU of "Technical Summary:
+ * PRISM", §2.2.  x and y are device arrays of n fp32 values (caller-owned, may not
+ * overlap); the work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream).  Errors: PRISM_ERR_INVALID_ARG for n < 0 or a NULL array with n > 0;
+ * PRISM_ERR_CUDA when the launch fails.  n = 0 does nothing. */
+PRISM_API int prism_debug_activation(const float* x, float* y, long long n, void* stream);
+
 /* One token of every sequence (dims->T must be 1; chunk is ignored): the
  * recurrence of §2.1-2.2 of "Technical Summary: PRISM" applied to a single token,
  * for streaming generation after a prism_forward_from / prism_forward prefix.

@@ -954,7 +954,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
 #pragma unroll
           for (int jj = 0; jj < 8; ++jj) {
             const float x = (u2f(pr[jj]) + u2f(pl[jj])) * rres[j8 + jj];
-            const float dl = gelu ? gelu_erf(x) : x;
+            const float dl = gelu ? gelu_hastings(x) : x;
             rres[j8 + jj] -= dl;
             dv[jj] = sb[jj] * dl;
             dt[jj] = dv[jj] * sd[jj];

@@ -445,6 +445,22 @@ extern "C" PRISM_API int prism_forward(const prism_dims* dims, const void* q, co
                             out, final_state, seq_lens, workspace, workspace_bytes, stream);
 }
 
+namespace prism {
+// the bf16 prepare kernel's activation at n points (a diagnostic for tests)
+__global__ void debug_activation_kernel(const float* x, float* y, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    y[i] = gelu_hastings(x[i]);
+}
+}  // namespace prism
+
+extern "C" PRISM_API int prism_debug_activation(const float* x, float* y, long long n, void* stream) {
+  if (n < 0 || (n > 0 && (!x || !y))) return PRISM_ERR_INVALID_ARG;
+  if (n == 0) return PRISM_OK;
+  const long long blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+  prism::debug_activation_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? PRISM_OK : PRISM_ERR_CUDA;
+}
+
 extern "C" PRISM_API int prism_debug_bounds(int* word, int clear) {
   if (!word) return PRISM_ERR_INVALID_ARG;
 #ifdef PRISM_DEBUG_BOUNDS

@@ -136,6 +136,28 @@ struct TileMap {
 __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
 }
+
+__device__ __forceinline__ float rcp_approx(float z) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(z));
+  return r;
+}
+// x Phi(x) with erf from Hastings' rational approximation (Abramowitz and Stegun,
+// "Handbook of Mathematical Functions", 7.1.26: |error of erf(y)| <= 1.5e-7 for y >= 0, and
+// erf is odd): with y = |x| / sqrt(2), t = 1 / (1 + 0.3275911 y) and
+// h = (1 - erf(y)) / 2 = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-y^2) / 2,
+// Phi(x) = 1 - h for x >= 0 and h for x < 0.  Within about 4e-7 max(|x|, 1) of the exact
+// GELU with the approximate reciprocal and exponential (the erff form is within about the
+// same of it in fp32); fewer instructions than erff, which matters in the tensor-core
+// prepare kernel's refinement loop.
+__device__ __forceinline__ float gelu_hastings(float x) {
+  const float y = fabsf(x) * 0.70710678118654752f;
+  const float t = rcp_approx(fmaf(0.3275911f, y, 1.0f));
+  const float poly =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f), 0.254829592f);
+  const float h = 0.5f * poly * __expf(-y * y);
+  return x * (x >= 0.f ? 1.0f - h : h);
+}
 __device__ __forceinline__ float sigmoidf(float x) { return 1.0f / (1.0f + expf(-x)); }
 
 }  // namespace prism

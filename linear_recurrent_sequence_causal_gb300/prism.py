@@ -30,7 +30,8 @@ EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "
            "prism_scan", "prism_forward_static", "prism_strerror", "prism_forward_from",
            "prism_decode_step", "prism_backward_workspace_bytes", "prism_backward",
            "prism_device_status", "prism_host_plan", "prism_host_arena_bytes",
-           "prism_forward_host", "prism_scan_segments", "prism_debug_bounds")
+           "prism_forward_host", "prism_scan_segments", "prism_debug_bounds",
+           "prism_debug_activation")
 WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC", "seg")
 
 
@@ -93,6 +94,9 @@ def load():
             lib.prism_device_status.restype = ctypes.c_int
             lib.prism_debug_bounds.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.c_int]
             lib.prism_debug_bounds.restype = ctypes.c_int
+            lib.prism_debug_activation.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong,
+                                                    ctypes.c_void_p]
+            lib.prism_debug_activation.restype = ctypes.c_int
             lib.prism_host_plan.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_size_t,
                                             ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
             lib.prism_host_plan.restype = ctypes.c_int
@@ -181,6 +185,15 @@ def debug_bounds(clear: bool = True):
         return None
     _check(rc)
     return word.value
+
+
+def debug_activation(x: torch.Tensor, stream=None) -> torch.Tensor:
+    """GELU of the fp32 device tensor ``x`` as the bf16 prepare kernel evaluates it."""
+    if x.dtype != torch.float32:
+        raise PrismError(1, "x must be fp32")
+    y = torch.empty_like(x)
+    _check(load().prism_debug_activation(_ptr(x), _ptr(y), x.numel(), _stream_ptr(stream)))
+    return y
 
 
 def device_status(dims: Dims, workspace, stream=None) -> int:
