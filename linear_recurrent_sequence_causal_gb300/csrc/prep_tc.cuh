@@ -469,6 +469,9 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
     }
     return id;
   };
+  // (the chunk after `cur` is worked out where it is needed rather than kept live across
+  // the chunk: one register fewer through the refinement loop)
+  auto next_of = [&](int cur_) { return next_chunk(cur_ + gridDim.x); };
   // One thread: TMA copies of a chunk's K and Q rows and its v window (C + 8 tokens;
   // out-of-range rows arrive as zeros) into the K_l and D regions.
   auto load_inputs = [&](int id) {
@@ -562,7 +565,6 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
   chunk_of(cur, b, h, chunk, nv);
   const int t0 = chunk * C;
   const int len = p.seq_lens ? min(max(p.seq_lens[b], 0), T_) : T_;
-  const int nxt = next_chunk(cur + gridDim.x);
   // parities: bar_k[0] completes ceil(L/2) times per chunk, bar_k[1] floor(L/2) times,
   // bar_p, bar_gp and bar_6 L times, bar_in and bar_u once
   const uint32_t kb0 = it * (uint32_t)((L + 1) / 2), kb1 = it * (uint32_t)(L / 2), sb = it * (uint32_t)L;
@@ -706,6 +708,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
       // the consumers have staged N^T in the K_l / D regions: copy it out, and once the copy
       // has read it, bring the next chunk's tiles in (they land in the same regions)
       asm volatile("bar.sync 10, %0;\n" ::"n"(S::NTA) : "memory");
+      const int nxt = next_of(cur);
       if (lane == 0) {
         const size_t cbase = ((size_t)b * H + h) * NC + chunk;
         if (L > 0) {
@@ -1135,7 +1138,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
   } else {
     csync<NT>();
     if (S::kPrefetch && tid == 0) {
-      const int nxt = next_chunk(cur + gridDim.x);
+      const int nxt = next_of(cur);
       if (nxt < total) load_inputs(nxt);
     }
   }
@@ -1303,6 +1306,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
+  const int nxt = next_of(cur);
   if (!S::kPrefetch && nxt < total && tid == 0) load_inputs(nxt);
   cur = nxt;
   }  // chunks
