@@ -227,6 +227,35 @@ def test_deterministic():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
+@pytest.mark.parametrize("D,C,L,T,B,H,ragged", [(64, 32, 3, 300, 2, 2, False), (128, 64, 3, 333, 2, 2, False),
+                                                 (128, 64, 4, 1000, 2, 2, False), (32, 32, 3, 200, 64, 2, True)])
+def test_prepare_reruns_bit_identical(D, C, L, T, B, H, ragged):
+    """A race between the tensor core and the epilogue warps (an MMA overwriting TMEM
+    columns some warp still reads) shows as reruns that differ: the prepare stage's whole
+    workspace, zeroed before each call, must be bit-identical over twelve calls.  Odd L
+    puts the last refinement step's scores in the k_hat buffer of even steps."""
+    wl = I.Workload("case", "bf16", B, T, H, D, D, L, 4, C, seed=77, ragged=ragged)
+    d = prism.inputs_to_device(I.generate(wl))
+    dims = prism.make_dims(B, T, H, D, D, 4, L, C, torch.bfloat16)
+    runs = []
+    for _ in range(12):
+        ws = prism.alloc_workspace(dims, "cuda")
+        ws.zero_()
+        prism.prism_prepare(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"], d["Wk"],
+                            d["Wp"], d["wbeta"], L, C, ws, seq_lens=d.get("seq_lens"))
+        runs.append(ws.cpu())
+    assert all(torch.equal(runs[0], r) for r in runs[1:])
+
+
+def test_recsys_bf16_reruns_bit_identical():
+    wl = I.get_workload("recsys_bf16")
+    d = prism.inputs_to_device(I.generate(wl))
+    o1, s1 = prism.forward_inputs(d, wl.L, wl.chunk)
+    for _ in range(8):
+        o2, s2 = prism.forward_inputs(d, wl.L, wl.chunk)
+        assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
 def test_causality():
     wl = I.Workload("case", "bf16", 1, 256, 2, 64, 64, 2, 4, 64, seed=4)
     inp = I.generate(wl)
