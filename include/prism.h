@@ -178,7 +178,7 @@ PRISM_API int prism_forward_from(const prism_dims* dims,
  * at the start of each forward call.  Errors: as for prism_forward's dims and
  * workspace checks; PRISM_ERR_INVALID_ARG for a NULL status; PRISM_ERR_CUDA when
  * the copy or the synchronisation fails.  prism_forward_static keeps its word in
- * the library's own scratch and is not covered. */
+ * the library's own scratch: prism_static_status reads that one. */
 PRISM_API int prism_device_status(const prism_dims* dims, const void* workspace,
                                   size_t workspace_bytes, int* status, void* stream);
 
@@ -285,6 +285,15 @@ PRISM_API int prism_scan(const prism_dims* dims,
  *   - All calls on a device share the array and it keeps the last call's
  *     contents.  Calls that overlap on the GPU (other streams, or threads
  *     without ordering between their launches) race on it: serialise them. */
+/* (No counterpart in the pages: failure detection of this library.)
+ * prism_device_status for prism_forward_static: the device status word of the last
+ * static call with these dims on the current device (0: every bounded wait completed),
+ * read from the library's scratch array.  Waits for `stream` like prism_device_status.
+ * Calls on the device share the array, so the word is that of whichever static call ran
+ * last.  Errors: as for prism_forward_static's dims checks; PRISM_ERR_INVALID_ARG for a
+ * NULL status; PRISM_ERR_CUDA when the lookup, the copy or the synchronisation fails. */
+PRISM_API int prism_static_status(const prism_dims* dims, int* status, void* stream);
+
 PRISM_API int prism_forward_static(const prism_dims* dims,
                                    const void* q, const void* k, const void* v,
                                    const float* log_alpha, const float* beta,

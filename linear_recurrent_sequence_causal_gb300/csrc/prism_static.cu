@@ -53,3 +53,15 @@ extern "C" PRISM_API int prism_forward_static(const prism_dims* dims, const void
   return prism_forward(dims, q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, out, final_state,
                        seq_lens, ws, (size_t)PRISM_STATIC_SCRATCH_BYTES, stream);
 }
+
+extern "C" PRISM_API int prism_static_status(const prism_dims* dims, int* status, void* stream) {
+  size_t offsets[PRISM_WS_COUNT];
+  const int check = prism_workspace_layout(dims, offsets, PRISM_WS_COUNT);   // validates dims
+  if (check != PRISM_OK) return check;
+  if (!status) return PRISM_ERR_INVALID_ARG;
+  if (prism_workspace_bytes(dims) > (size_t)PRISM_STATIC_SCRATCH_BYTES) return PRISM_ERR_SCRATCH_LIMIT;
+  void* ws = nullptr;
+  const int rc = scratch_for_current_device(&ws);
+  if (rc != PRISM_OK) return rc;
+  return prism_device_status(dims, ws, (size_t)PRISM_STATIC_SCRATCH_BYTES, status, stream);
+}

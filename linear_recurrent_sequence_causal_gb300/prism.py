@@ -31,7 +31,7 @@ EXPORTS = ("prism_workspace_bytes", "prism_workspace_layout", "prism_forward", "
            "prism_decode_step", "prism_backward_workspace_bytes", "prism_backward",
            "prism_device_status", "prism_host_plan", "prism_host_arena_bytes",
            "prism_forward_host", "prism_scan_segments", "prism_debug_bounds",
-           "prism_debug_activation")
+           "prism_debug_activation", "prism_static_status")
 WS_REGIONS = ("status", "Kl", "Dl", "wblocks", "WQ", "QK", "U", "Oi", "N", "gC", "seg")
 
 
@@ -97,6 +97,8 @@ def load():
             lib.prism_debug_activation.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong,
                                                     ctypes.c_void_p]
             lib.prism_debug_activation.restype = ctypes.c_int
+            lib.prism_static_status.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(ctypes.c_int), ctypes.c_void_p]
+            lib.prism_static_status.restype = ctypes.c_int
             lib.prism_host_plan.argtypes = [ctypes.POINTER(Dims), ctypes.c_int, ctypes.c_size_t,
                                             ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
             lib.prism_host_plan.restype = ctypes.c_int
@@ -194,6 +196,14 @@ def debug_activation(x: torch.Tensor, stream=None) -> torch.Tensor:
     y = torch.empty_like(x)
     _check(load().prism_debug_activation(_ptr(x), _ptr(y), x.numel(), _stream_ptr(stream)))
     return y
+
+
+def static_status(dims: Dims, stream=None) -> int:
+    """The device status word of the last prism_forward_static call (0: every bounded
+    wait completed).  Synchronises ``stream``."""
+    word = ctypes.c_int(-1)
+    _check(load().prism_static_status(ctypes.byref(dims), ctypes.byref(word), _stream_ptr(stream)))
+    return word.value
 
 
 def device_status(dims: Dims, workspace, stream=None) -> int:
@@ -323,7 +333,7 @@ def v_history(v, w, end=None):
 
 def prism_forward_static(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chunk, *, out=None,
                          final_state=None, seq_lens=None, stream=None, no_gelu=False,
-                         want_state=True):
+                         want_state=True, flags=0):
     """prism_forward using the library's static device scratch (no workspace).
 
     For callers that cannot allocate device memory on their hot path; see
@@ -331,7 +341,7 @@ def prism_forward_static(q, k, v, log_alpha, beta, conv_w, Wk, Wp, wbeta, L, chu
     """
     B, T, H, dk = q.shape
     dv = v.shape[-1]
-    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu)
+    dims = _dims_for(q, v, conv_w, L, chunk, no_gelu, flags)
     if out is None:
         out = torch.empty((B, T, H, dv), dtype=torch.float32, device=q.device)
     if final_state is None and want_state:

@@ -143,6 +143,20 @@ def test_backward_argument_errors(lib):
     assert call(d, ok, wsb=nbytes - 1) == 4        # workspace too small
 
 
+def test_static_status_argument_errors(lib):
+    """prism_static_status rejects bad dims, a NULL result pointer and dims whose
+    workspace exceeds the static scratch before touching the device."""
+    word = ctypes.c_int(-1)
+    d = prism.make_dims(2, 64, 2, 32, 32, 4, 2, 32, prism.PRISM_BF16)
+    bad = prism.make_dims(2, 64, 2, 32, 32, 4, 2, 48, prism.PRISM_BF16)       # chunk 48
+    assert lib.prism_static_status(ctypes.byref(bad), ctypes.byref(word), None) == 2
+    assert lib.prism_static_status(ctypes.byref(d), None, None) == 1
+    big = prism.make_dims(64, 65536, 32, 128, 128, 4, 4, 64, prism.PRISM_BF16)
+    assert prism.workspace_bytes(big) > prism.STATIC_SCRATCH_BYTES
+    assert lib.prism_static_status(ctypes.byref(big), ctypes.byref(word), None) == 7
+    assert word.value == -1
+
+
 def test_device_status_argument_errors(lib):
     """prism_device_status rejects bad dims, a NULL result pointer and a missing, misaligned
     or short workspace before touching the device."""

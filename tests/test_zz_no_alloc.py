@@ -60,3 +60,28 @@ def test_static_scratch_rejects_oversized_dims():
     assert prism.workspace_bytes(d) > prism.STATIC_SCRATCH_BYTES
     rc = lib.prism_forward_static(ctypes.byref(d), *[0x1000] * 12, None)
     assert rc == 7 and b"STATIC_SCRATCH" in lib.prism_strerror(rc)
+
+
+@pytest.mark.gpu
+def test_static_status_word():
+    """prism_static_status reads the bounded-wait status word a static call left in the
+    library's scratch: 0 after a normal call; nonzero after a call whose diagnostic flag
+    makes a wait of each scan CTA run out (nothing in flight; the outputs are still those
+    of the normal call); 0 again after the next normal call."""
+    prism.load()
+    B, T, H, D, L, C = 2, 300, 2, 128, 2, 64
+    wl = I.Workload("static", "bf16", B, T, H, D, D, L, 4, C, seed=611)
+    d = prism.inputs_to_device(I.generate(wl))
+    dims = prism.make_dims(B, T, H, D, D, 4, L, C, torch.bfloat16)
+    chk = prism.PRISM_FLAG_CHECK_WAIT_TIMEOUT
+    dims_chk = prism.make_dims(B, T, H, D, D, 4, L, C, torch.bfloat16, flags=chk)
+    args = (d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"], d["Wk"], d["Wp"],
+            d["wbeta"], L, C)
+    o0, s0 = prism.prism_forward_static(*args)
+    assert prism.static_status(dims) == 0
+    o1, s1 = prism.prism_forward_static(*args, flags=chk)
+    assert prism.static_status(dims_chk) != 0
+    assert torch.equal(o0, o1) and torch.equal(s0, s1)
+    o2, _ = prism.prism_forward_static(*args)
+    assert prism.static_status(dims) == 0
+    assert torch.equal(o0, o2)
