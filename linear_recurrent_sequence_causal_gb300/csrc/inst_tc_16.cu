@@ -12,7 +12,7 @@ cudaError_t launch_prep_16(int C, const PrepArgs& a, cudaStream_t s) {
 }
 cudaError_t launch_weights_16(const float* Wk, const float* Wp, int H, int L, unsigned char* blocks,
                               int* flag, cudaStream_t s) {
-  prep_weights_kernel<16><<<H * L * 2, 256, 0, s>>>(Wk, Wp, H, L, blocks, flag);
+  prep_weights_kernel<16><<<H * L * 2 * WeightBlock<16>::kCtas, 256, 0, s>>>(Wk, Wp, H, L, blocks, flag);
   return cudaGetLastError();
 }
 size_t prep_smem_16(int C) {

@@ -83,6 +83,8 @@ struct PrepArgs {
 template <int D>
 struct WeightBlock {
   static constexpr uint32_t bytes = 128u * D * 2u;
+  // the conversion kernel: threads of 8 columns, 256 per CTA, kCtas CTAs per block
+  static constexpr int kPieces = D / 8, kRowsPerCta = 256 / kPieces, kCtas = 128 / kRowsPerCta;
   // block index of (h, l, which = 0 W_k / 1 W_p, part = 0 hi / 1 lo)
   static __host__ __device__ size_t index(int h, int l, int L, int which, int part) {
     return (((size_t)h * L + l) * 2 + which) * 2 + part;
@@ -95,34 +97,48 @@ struct WeightBlock {
 // down the block's 128 rows, so the projections land in every TMEM lane quarter (the
 // epilogue spreads a chunk's tokens over the copies).
 template <int D>
-__global__ void prep_weights_kernel(const float* Wk, const float* Wp, int H, int L,
-                                    unsigned char* blocks, int* flag) {
-  const int blk = blockIdx.x;              // (h*L + l)*2 + which
+__global__ void __launch_bounds__(256) prep_weights_kernel(const float* Wk, const float* Wp, int H, int L,
+                                                           unsigned char* blocks, int* flag) {
+  // thread = (row of the block, 8-column piece): two 16-byte loads of the row, one 16-byte
+  // store each of hi and lo; the row's P threads are consecutive lanes of one warp
+  constexpr int P = WeightBlock<D>::kPieces, ROWS = WeightBlock<D>::kRowsPerCta;
+  const int blk = blockIdx.x / WeightBlock<D>::kCtas;   // (h*L + l)*2 + which
+  const int row = (blockIdx.x % WeightBlock<D>::kCtas) * ROWS + threadIdx.x / P, c8 = threadIdx.x % P;
   const int which = blk & 1, hl = blk >> 1;
   const float* W = (which == 0 ? Wk : Wp) + (size_t)hl * D * D;
   unsigned char* hi = blocks + (size_t)(blk * 2 + 0) * WeightBlock<D>::bytes;
   unsigned char* lo = blocks + (size_t)(blk * 2 + 1) * WeightBlock<D>::bytes;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
-  bool need = false;
-  for (int row = warp; row < 128; row += nwarp) {
-    float n2 = 0.f;
-    const bool live = D >= 32 || row < D;      // d = 16: one copy (rows 16..127 zero)
-    if (live)
-      for (int c = lane; c < D; c += 32) { const float x = W[(size_t)(row % D) * D + c]; n2 = fmaf(x, x, n2); }
+  const bool live = D >= 32 || row < D;        // d = 16: one copy (rows 16..127 zero)
+  float x[8];
+  if (live) {
+    const float4* src = reinterpret_cast<const float4*>(W + (size_t)(row % D) * D + c8 * 8);
+    const float4 a = src[0], b = src[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
-    const float tol = sqrtf(n2) * 0x1p-22f;
-    for (int c = lane; c < D; c += 32) {
-      const float x = live ? W[(size_t)(row % D) * D + c] : 0.f;
-      __half h, l;
-      tc::split_f16(x, h, l);
-      const uint32_t off = (c / 8) * 2048u + row * 16u + (c % 8) * 2u;
-      *reinterpret_cast<__half*>(hi + off) = h;
-      *reinterpret_cast<__half*>(lo + off) = l;
-      need |= fabsf(__half2float(l)) > tol;
-    }
+    for (int j = 0; j < 8; ++j) x[j] = 0.f;
   }
-  if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr(flag, 1);
+  float n2 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) n2 = fmaf(x[j], x[j], n2);
+#pragma unroll
+  for (int o = P / 2; o > 0; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
+  const float tol = sqrtf(n2) * 0x1p-22f;
+  uint4 h, l;
+  tc::split8(x, h, l);
+  const uint32_t off = c8 * 2048u + row * 16u;
+  *reinterpret_cast<uint4*>(hi + off) = h;
+  *reinterpret_cast<uint4*>(lo + off) = l;
+  const uint32_t lw[4] = {l.x, l.y, l.z, l.w};
+  bool need = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __half2 lh;
+    memcpy(&lh, &lw[j], 4);
+    const float2 lf = __half22float2(lh);
+    need |= fabsf(lf.x) > tol || fabsf(lf.y) > tol;
+  }
+  if (__any_sync(0xffffffffu, need) && (threadIdx.x & 31) == 0) atomicOr(flag, 1);
 }
 
 // First-fit placement helper for the tail buffers: region 1 is [r1, r1_end),

@@ -194,6 +194,31 @@ def test_prepare_stage_bf16(D, C, L, ragged):
             assert err <= 5e-3, f"{name} (b={b}): normwise error {err:.3e}"
 
 
+@pytest.mark.parametrize("D,C,L", [(128, 64, 2), (64, 32, 3), (32, 32, 2), (16, 16, 1)])
+def test_weights_with_bits_below_fp16(D, C, L):
+    """Weights drawn in fp32 (not bf16-rounded) have lo halves that matter: the weight
+    conversion flags them (word 1 of the workspace's status region reads 1, against 0 for
+    bf16-rounded weights) and the projections take their third pass with the lo halves.
+    The outputs must match the oracle run on the same fp32 weights."""
+    wl = I.Workload("case", "bf16", 2, 3 * C + 5, 2, D, D, L, 4, C, seed=91 + D)
+    inp = I.generate(wl)
+    g = torch.Generator().manual_seed(92 + D)
+    inp_x = dict(inp)
+    for n in ("Wk", "Wp"):
+        inp_x[n] = torch.randn(inp[n].shape, generator=g, dtype=torch.float32) * D ** -0.5
+    dims = prism.make_dims(wl.B, wl.T, wl.H, D, D, wl.w, L, C, torch.bfloat16)
+    for src, want in ((inp, 0), (inp_x, 1)):
+        d = prism.inputs_to_device(src)
+        ws = torch.zeros(prism.workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+        prism.prism_prepare(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"], d["Wk"],
+                            d["Wp"], d["wbeta"], L, C, ws)
+        torch.cuda.synchronize()
+        assert int(ws[4:8].view(torch.int32).item()) == want
+    out, fs = gpu_forward(inp_x, L, C)
+    ro, rs, _ = oracle.forward(inp_x)
+    check(out, fs, ro, rs, "bf16", what=f"fp32 weights d={D}")
+
+
 def test_prepare_stage_f32():
     """fp32 path: the per-token factors in the workspace against the oracle trace."""
     from tests.parity import read_region
