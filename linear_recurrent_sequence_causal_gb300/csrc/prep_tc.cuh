@@ -166,7 +166,6 @@ struct PrepSmem {
   static constexpr int NW = 4 * CG;                      // consumer warps
   static constexpr int NT = 32 * NW;                     // consumer threads
   static constexpr int NTA = NT + 32;                    // all threads (with the producer warp)
-  static constexpr int kMinBlocks = NTA <= 288 ? 2 : 1;   // CTAs per SM the registers must allow
   static constexpr int NTH = C / CG;                     // token columns per thread
   // Feature role (anchor, passes A and B): the projections arrive RF times over in TMEM
   // (the weight rows repeat), in whole lane quarters when d >= 32, so replica rf of a
@@ -246,6 +245,8 @@ struct PrepSmem {
   static constexpr uint32_t tmem_cols =
       tmem_cols_needed <= 32 ? 32 : tmem_cols_needed <= 64 ? 64 : tmem_cols_needed <= 128 ? 128
                                   : tmem_cols_needed <= 256 ? 256 : 512;
+  // CTAs per SM the registers must allow: two where TMEM lets two reside
+  static constexpr int kMinBlocks = (NTA <= 288 && tmem_cols <= 256) ? 2 : 1;
   static_assert(NTH % 8 == 0 && NFD % 8 == 0 && NTF % 8 == 0 && RF >= 1, "column groups of 8");
   static_assert(tmem_cols_needed <= 512, "TMEM");
 };
