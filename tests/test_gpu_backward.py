@@ -118,3 +118,22 @@ def test_backward_short_sequences_and_an_empty_one():
         assert err <= GRAD_TOL, f"d{n}: {err:.3e}"
     for key in ("q", "k", "v", "log_alpha", "beta"):
         assert not torch.any(gg[key][1]), f"d{key} of the empty sequence"
+
+
+@pytest.mark.parametrize("D", [32, 128])
+def test_backward_every_sequence_empty(D):
+    """Every sequence of length 0: no token takes part, so every gradient, those of the
+    per-head parameters included, is exactly zero whatever the inputs and d_out hold."""
+    B, T, H, L = 3, 40, 2, 2
+    wl = I.Workload("bwd", "bf16", B, T, H, D, D, L, 4, 16, seed=6)
+    inp = I.generate(wl)
+    inp["seq_lens"] = torch.zeros(B, dtype=torch.int32)
+    d = prism.inputs_to_device(inp)
+    d_out = torch.randn(B, T, H, D, device="cuda")
+    d_fs = torch.randn(B, H, D, D, device="cuda")
+    gg = prism.prism_backward(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["conv_w"],
+                              d["Wk"], d["Wp"], d["wbeta"], L, d_out, d_final_state=d_fs,
+                              seq_lens=d["seq_lens"])
+    torch.cuda.synchronize()
+    for n in G.GRAD_KEYS:
+        assert torch.count_nonzero(gg[n]).item() == 0, f"d{n}"

@@ -137,6 +137,26 @@ def test_shapes_and_tails(dtype, B, T, H, D, L, w, chunk, ragged):
           what=f"{dtype} B{B} T{T} H{H} D{D} L{L} w{w} C{chunk}")
 
 
+@pytest.mark.parametrize("dtype,D,C,L", [("bf16", 32, 32, 3), ("bf16", 64, 64, 2), ("bf16", 128, 64, 4),
+                                         ("f32", 32, 32, 2)])
+def test_every_sequence_empty(dtype, D, C, L):
+    """A batch whose sequences all have length 0: every prepare CTA finds no chunk, the
+    outputs and final states are exactly zero whatever the (NaN) inputs hold, and the
+    device status word reads 0."""
+    B, T, H = 3, 100, 2
+    wl = I.Workload("case", dtype, B, T, H, D, D, L, 4, C, seed=77)
+    inp = I.generate(wl)
+    for name in ("q", "k", "v", "log_alpha", "beta"):
+        inp[name] = torch.full_like(inp[name], float("nan"))
+    inp["seq_lens"] = torch.zeros(B, dtype=torch.int32)
+    d = prism.inputs_to_device(inp)
+    dims = prism.make_dims(B, T, H, D, D, 4, L, C, wl.torch_dtype)
+    ws = prism.alloc_workspace(dims, "cuda")
+    out, fs = prism.forward_inputs(d, L, C, workspace=ws)
+    assert prism.device_status(dims, ws) == 0
+    assert torch.count_nonzero(out).item() == 0 and torch.count_nonzero(fs).item() == 0
+
+
 @pytest.mark.parametrize("chunk", [16, 32, 64])
 def test_chunk_size_invariance(chunk):
     wl = I.Workload("case", "bf16", 2, 300, 2, 64, 64, 3, 4, chunk, seed=77)
