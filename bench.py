@@ -557,6 +557,19 @@ def grad_oracle_sample(host, wl, L, target_s):
     return T, dt
 
 
+def backward_launches(B, T, H, D, L):
+    """Kernels one prism_backward call launches: refinement forward, state (+ the row-slice
+    reduction when a (b, h) is split over CTAs), refinement backward, dW_k / dW_p (L > 0;
+    + the token-split reduction), dw_beta / dconv (+ its reduction), the anchor's dv.  The
+    splits follow the library's own choices (bwd_pick_rs / _nsw / _nss)."""
+    ntok = B * T
+    rs_split = B * H < 152
+    nsw = min(32, max(1, ntok // 2048)) if L > 0 else 1
+    nss = min(64, max(1, ntok // 512))
+    return (5 + (1 if rs_split else 0) + (1 if L > 0 else 0) + (1 if nsw > 1 else 0)
+            + (1 if nss > 1 else 0))
+
+
 def backward_arm(args, wl, L):
     from linear_recurrent_sequence_causal_gb300 import build, prism
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -661,7 +674,7 @@ def backward_arm(args, wl, L):
             "roofline": roof, "clocks": clk,
             "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps * (5 + (1 if L > 0 else 0))}
+            "gpu_launches": args.steps * backward_launches(B, T, H, D, L)}
     if not args.no_cpu_baseline:
         Ts, dts = grad_oracle_sample(host, wl, L, args.cpu_seconds)
         line["cpu_baseline"] = {"value": Ts / dts / H, "unit": UNIT, "cores": torch.get_num_threads(),

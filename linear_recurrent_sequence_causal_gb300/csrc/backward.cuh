@@ -17,6 +17,8 @@
 //   E  bwd_conv_dv      dv_t += sum_j c_j (.) du_(t+j)  (the anchor's taps, transposed)
 #pragma once
 
+#include <algorithm>
+
 #include "prism_common.cuh"
 
 namespace prism {
@@ -34,9 +36,15 @@ inline int bwd_pick_rs(long long BH, int D) {
   return D >= 32 ? 4 : 2;
 }
 
+// Token splits of the weight-gradient sums: each split sums its share of the tokens into a
+// partial array, and a second kernel adds the partials in split order (deterministic).
+inline int bwd_pick_nsw(long long ntok) { return (int)std::min<long long>(32, std::max<long long>(1, ntok / 2048)); }
+inline int bwd_pick_nss(long long ntok) { return (int)std::min<long long>(64, std::max<long long>(1, ntok / 512)); }
+
 struct BwdArgs {
   int B, T, H, L, w;
   int rs;                         // rows-of-S slices per (b, h) in the state kernel
+  int nsw, nss;                   // token splits of dW_k / dW_p and of dw_beta / dconv
   unsigned flags;                 // bit 0: identity in place of GELU
   const void* q;                  // [B][T][H][D] (I/O dtype)
   const void* k;
@@ -79,6 +87,8 @@ struct BwdArgs {
   float* PKL;                     // [RS][n][L][D]
   float* PB;                      // [RS][n]
   float* PA;                      // [RS][n]
+  float* PW;                      // [nsw][H][2L][D][D] partial dW_k, dW_p (nsw > 1)
+  float* PSW;                     // [nss][H][L + w][D] partial dw_beta, dconv (nss > 1)
 };
 
 __device__ __forceinline__ int bwd_len(const BwdArgs& p, int b) {
@@ -797,80 +807,139 @@ __global__ void __launch_bounds__(kBwdThreads) bwd_refine_kernel(BwdArgs p) {
 }
 
 // ------------------------------------------------------------------------------------
-// D: dW_k^(l), dW_p^(l) (one CTA per TW x TW output tile: sum over the head's tokens of
-// d k_hat u^T and dp u^T), then dw_beta and the conv taps.
-
+// D: dW_k^(l), dW_p^(l): sums over the head's tokens of d k_hat u^T and dp u^T.  One CTA
+// per (TILE x TILE output tile, step and matrix, head, token split); thread (ty, tx) of
+// a (TILE/4)^2 grid keeps a 4 x 4 block of outputs in registers, and 32-token slabs of
+// the two operands pass through shared memory.
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads) bwd_weight_kernel(BwdArgs p) {
-  constexpr int TW = D < 32 ? D : 32;                // tile width
-  constexpr int OPT = TW * TW / kBwdThreads;         // outputs per thread (1 or 4)
-  __shared__ float sA[32][TW + 1], sUt[32][TW + 1];
-  const int tid = threadIdx.x;
-  const int tile = blockIdx.x, which = blockIdx.y % 2, l = blockIdx.y / 2, h = blockIdx.z;
-  const int a0 = (tile / (D / TW)) * TW, c0 = (tile % (D / TW)) * TW;
+struct BwdWTile {
+  static constexpr int TILE = D < 64 ? D : 64, NT = (TILE / 4) * (TILE / 4), TILES = (D / TILE) * (D / TILE);
+};
+template <int D>
+__global__ void __launch_bounds__(BwdWTile<D>::NT) bwd_weight_kernel(BwdArgs p) {
+  constexpr int TILE = BwdWTile<D>::TILE, NT = BwdWTile<D>::NT;
+  __shared__ __align__(16) float sA[32][TILE], sU[32][TILE];
+  const int tid = threadIdx.x, ty = tid / (TILE / 4), tx = tid % (TILE / 4);
+  const int tile = blockIdx.x, lw = blockIdx.y, which = lw % 2, l = lw / 2;
+  const int h = blockIdx.z % p.H, split = blockIdx.z / p.H;
+  const int a0 = (tile / (D / TILE)) * TILE, c0 = (tile % (D / TILE)) * TILE;
   const int H = p.H, L = p.L, NTOK = p.B * p.T;
+  const int per = ((NTOK + p.nsw - 1) / p.nsw + 31) / 32 * 32;
+  const int m_begin = split * per, m_end = min(NTOK, m_begin + per);
   const float* src = which == 0 ? p.dKH : p.DL;      // DL holds dp^(l) after kernel C
-  const int ta = tid / (TW / OPT), tc = (tid % (TW / OPT)) * OPT;   // output (a0 + ta, c0 + tc ..)
-  float acc[OPT];
+  float acc[4][4];
 #pragma unroll
-  for (int e = 0; e < OPT; ++e) acc[e] = 0.f;
-  for (int m0 = 0; m0 < NTOK; m0 += 32) {
-    for (int idx = tid; idx < 32 * TW; idx += kBwdThreads) {
-      const int i = idx / TW, j = idx % TW, m = m0 + i;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int m0 = m_begin; m0 < m_end; m0 += 32) {
+    for (int idx = tid; idx < 32 * (TILE / 4); idx += NT) {
+      const int i = idx / (TILE / 4), j4 = (idx % (TILE / 4)) * 4, m = m0 + i;
       const size_t n = (size_t)m * H + h;
-      sA[i][j] = m < NTOK ? src[(n * L + l) * D + a0 + j] : 0.f;
-      sUt[i][j] = m < NTOK ? p.U[n * D + c0 + j] : 0.f;
+      const bool in = m < m_end;
+      *reinterpret_cast<float4*>(&sA[i][j4]) =
+          in ? *reinterpret_cast<const float4*>(src + (n * L + l) * D + a0 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(&sU[i][j4]) =
+          in ? *reinterpret_cast<const float4*>(p.U + n * D + c0 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
-#pragma unroll 8
+#pragma unroll 4
     for (int i = 0; i < 32; ++i) {
-      const float av = sA[i][ta];
+      const float4 av = *reinterpret_cast<const float4*>(&sA[i][ty * 4]);
+      const float4 uv = *reinterpret_cast<const float4*>(&sU[i][tx * 4]);
+      const float a[4] = {av.x, av.y, av.z, av.w}, u[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
-      for (int e = 0; e < OPT; ++e) acc[e] = fmaf(av, sUt[i][tc + e], acc[e]);
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(a[r], u[c], acc[r][c]);
     }
     __syncthreads();
   }
-  float* dst = (which == 0 ? p.dWk : p.dWp) + (((size_t)h * L + l) * D + a0 + ta) * D + c0 + tc;
+  // one split: the sums themselves; else this split's partials, added by the reduce kernel
+  float* dst = p.nsw == 1
+                   ? (which == 0 ? p.dWk : p.dWp) + ((size_t)h * L + l) * D * D
+                   : p.PW + (((size_t)split * H + h) * 2 * L + lw) * D * D;
 #pragma unroll
-  for (int e = 0; e < OPT; ++e) dst[e] = acc[e];
+  for (int r = 0; r < 4; ++r)
+    *reinterpret_cast<float4*>(dst + (size_t)(a0 + ty * 4 + r) * D + c0 + tx * 4) =
+        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+}
+
+// dW_k, dW_p = the nsw partials added in split order.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads) bwd_weight_reduce_kernel(BwdArgs p) {
+  const size_t per = (size_t)p.H * 2 * p.L * D * D;
+  for (size_t idx = (size_t)blockIdx.x * kBwdThreads + threadIdx.x; idx < per; idx += (size_t)gridDim.x * kBwdThreads) {
+    float s = 0.f;
+    for (int q = 0; q < p.nsw; ++q) s += p.PW[(size_t)q * per + idx];
+    const size_t hl = idx / ((size_t)D * D), e = idx % ((size_t)D * D);
+    const int h = (int)(hl / (2 * p.L)), lw = (int)(hl % (2 * p.L));
+    (lw % 2 == 0 ? p.dWk : p.dWp)[((size_t)h * p.L + lw / 2) * D * D + e] = s;
+  }
 }
 
 // dw_beta^(l)[c] = sum_tokens dz^(l) u[c];  dconv[j-1][c] = sum_tokens du_t[c] v_(t-j)[c].
-// One CTA per (32 channels, head); thread (channel, token lane) over every 8th token.
+// One CTA per (32 channels, head, token split); thread (channel, token lane) over every 8th
+// token of the split's share of the flattened (b, t) axis.
 template <class T, int D>
 __global__ void __launch_bounds__(kBwdThreads) bwd_small_weight_kernel(BwdArgs p) {
   __shared__ float sRed[8][32][kBwdLmax + 8 + 1];
   const int tid = threadIdx.x, cl = tid % 32, tl = tid / 32;
-  const int c = blockIdx.x * 32 + cl, h = blockIdx.y;
+  const int c = blockIdx.x * 32 + cl, h = blockIdx.y, split = blockIdx.z;
   const int H = p.H, T_ = p.T, L = p.L, w = p.w;
+  const long long NTOK = (long long)p.B * T_;
+  const long long per = (NTOK + p.nss - 1) / p.nss;
+  const long long m_begin = split * per, m_end = m_begin + per < NTOK ? m_begin + per : NTOK;
   const T* vg = static_cast<const T*>(p.v);
   float acc[kBwdLmax + 8];
 #pragma unroll
   for (int j = 0; j < kBwdLmax + 8; ++j) acc[j] = 0.f;
-  for (int b = 0; b < p.B && c < D; ++b) {
-    const int len = bwd_len(p, b);
-    for (int t = tl; t < len; t += 8) {
-      const size_t n = ((size_t)b * T_ + t) * H + h;
-      const float uc = p.U[n * D + c], du = p.dU[n * D + c];
-      for (int l = 0; l < L; ++l) acc[l] = fmaf(p.dZ[n * L + l], uc, acc[l]);
-      for (int j = 1; j <= w && j <= t; ++j)
+  for (long long m = m_begin + tl; m < m_end && c < D; m += 8) {
+    const int b = (int)(m / T_), t = (int)(m % T_);
+    if (t >= bwd_len(p, b)) continue;
+    const size_t n = (size_t)m * H + h;
+    const float uc = p.U[n * D + c], du = p.dU[n * D + c];
+    // (fixed trip counts with predicates, so that acc stays in registers)
+#pragma unroll
+    for (int l = 0; l < kBwdLmax; ++l)
+      if (l < L) acc[l] = fmaf(p.dZ[n * L + l], uc, acc[l]);
+#pragma unroll
+    for (int j = 1; j <= 8; ++j)
+      if (j <= w && j <= t)
         acc[kBwdLmax + j - 1] = fmaf(du, Elem<T>::to_f(vg[(((size_t)b * T_ + t - j) * H + h) * D + c]), acc[kBwdLmax + j - 1]);
-    }
   }
 #pragma unroll
   for (int j = 0; j < kBwdLmax + 8; ++j) sRed[tl][cl][j] = acc[j];
   __syncthreads();
   if (tl == 0 && c < D) {
+    // one split: the sums themselves; else this split's partials [split][h][L + w][D]
+    float* part = p.PSW + ((size_t)split * H + h) * (L + w) * D;
     for (int l = 0; l < L; ++l) {
       float s = 0.f;
       for (int q = 0; q < 8; ++q) s += sRed[q][cl][l];
-      p.dwb[((size_t)h * L + l) * D + c] = s;
+      if (p.nss == 1) p.dwb[((size_t)h * L + l) * D + c] = s;
+      else part[(size_t)l * D + c] = s;
     }
     for (int j = 1; j <= w; ++j) {
       float s = 0.f;
       for (int q = 0; q < 8; ++q) s += sRed[q][cl][kBwdLmax + j - 1];
-      p.dconv[((size_t)h * w + j - 1) * D + c] = s;
+      if (p.nss == 1) p.dconv[((size_t)h * w + j - 1) * D + c] = s;
+      else part[(size_t)(L + j - 1) * D + c] = s;
     }
+  }
+}
+
+// dw_beta, dconv = the nss partials added in split order.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads) bwd_small_reduce_kernel(BwdArgs p) {
+  const int LW = p.L + p.w;
+  const size_t per = (size_t)p.H * LW * D;
+  for (size_t idx = (size_t)blockIdx.x * kBwdThreads + threadIdx.x; idx < per; idx += (size_t)gridDim.x * kBwdThreads) {
+    float s = 0.f;
+    for (int q = 0; q < p.nss; ++q) s += p.PSW[(size_t)q * per + idx];
+    const int c = (int)(idx % D), j = (int)((idx / D) % LW), h = (int)(idx / ((size_t)D * LW));
+    if (j < p.L) p.dwb[((size_t)h * p.L + j) * D + c] = s;
+    else p.dconv[((size_t)h * p.w + j - p.L) * D + c] = s;
   }
 }
 

@@ -48,12 +48,24 @@ cudaError_t launch_backward_t(const BwdArgs& a, cudaStream_t s) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (L > 0) {
-    constexpr int TW = D < 32 ? D : 32;
-    bwd_weight_kernel<D><<<dim3((D / TW) * (D / TW), 2 * L, a.H), kBwdThreads, 0, s>>>(a);
+    using WT = BwdWTile<D>;
+    bwd_weight_kernel<D><<<dim3(WT::TILES, 2 * L, a.H * a.nsw), WT::NT, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (a.nsw > 1) {
+      const size_t total = (size_t)a.H * 2 * L * D * D;
+      const size_t blocks = (total + kBwdThreads - 1) / kBwdThreads;
+      bwd_weight_reduce_kernel<D><<<(unsigned)(blocks < 4864 ? blocks : 4864), kBwdThreads, 0, s>>>(a);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  }
+  bwd_small_weight_kernel<T, D><<<dim3((D + 31) / 32, a.H, a.nss), kBwdThreads, 0, s>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.nss > 1) {
+    const size_t total = (size_t)a.H * (L + a.w) * D;
+    const size_t blocks = (total + kBwdThreads - 1) / kBwdThreads;
+    bwd_small_reduce_kernel<D><<<(unsigned)(blocks < 4864 ? blocks : 4864), kBwdThreads, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  bwd_small_weight_kernel<T, D><<<dim3((D + 31) / 32, a.H), kBwdThreads, 0, s>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
     const size_t total = (size_t)a.B * a.T * a.H * D;
     const size_t blocks = (total + kBwdThreads - 1) / kBwdThreads;

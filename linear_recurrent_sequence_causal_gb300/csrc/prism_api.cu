@@ -533,8 +533,8 @@ namespace {
 // Backward-pass workspace: per token-head factors, then the state checkpoints and the
 // block scratch.  Offsets in floats of each region, 256-byte aligned.
 struct BwdLayout {
-  size_t U, KL, DL, P, NRM, Z, dDL, dKL, dKH, dZ, dU, CK, SCR, PQ, PK, PKL, PB, PA, total;
-  int rs;
+  size_t U, KL, DL, P, NRM, Z, dDL, dKL, dKH, dZ, dU, CK, SCR, PQ, PK, PKL, PB, PA, PW, PSW, total;
+  int rs, nsw, nss;
 };
 
 BwdLayout bwd_layout(const prism_dims* d) {
@@ -567,6 +567,12 @@ BwdLayout bwd_layout(const prism_dims* d) {
   Lo.PKL = take(RSp * NTH * L * D);
   Lo.PB = take(RSp * NTH);
   Lo.PA = take(RSp * NTH);
+  // token-split partials of the weight gradients (only when split)
+  const long long ntok = (long long)d->B * d->T;
+  Lo.nsw = L > 0 ? prism::bwd_pick_nsw(ntok) : 1;
+  Lo.nss = prism::bwd_pick_nss(ntok);
+  Lo.PW = take(Lo.nsw > 1 ? (size_t)Lo.nsw * d->H * 2 * L * D * D : 0);
+  Lo.PSW = take(Lo.nss > 1 ? (size_t)Lo.nss * d->H * (L + d->conv_width) * D : 0);
   Lo.total = cur * 4;
   return Lo;
 }
@@ -628,6 +634,7 @@ extern "C" PRISM_API int prism_backward(const prism_dims* dims, const void* q, c
   a.dU = ws + Lo.dU; a.CK = ws + Lo.CK; a.SCR = ws + Lo.SCR;
   a.rs = Lo.rs;
   a.PQ = ws + Lo.PQ; a.PK = ws + Lo.PK; a.PKL = ws + Lo.PKL; a.PB = ws + Lo.PB; a.PA = ws + Lo.PA;
+  a.nsw = Lo.nsw; a.nss = Lo.nss; a.PW = ws + Lo.PW; a.PSW = ws + Lo.PSW;
   return prism::launch_backward(dims->dtype == PRISM_F32 ? 0 : 1, dims->d_k, a,
                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PRISM_OK
