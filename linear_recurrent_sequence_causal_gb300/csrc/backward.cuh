@@ -142,7 +142,9 @@ __device__ __forceinline__ float bwd_w(const float* sW, int a, int c) {
   return sW[a * D + (((c >> 2) ^ (a & (D / 4 - 1))) << 2) + (c & 3)];
 }
 
-// Y[i][a] = sum_c W[a][c] X[i][a'=c] for the NTOK token rows of X (shared memory).
+// Y[i][a] = sum_c W[a][c] X[i][a'=c] for the NTOK token rows of X (shared memory, rows
+// 16-byte aligned).  Four columns at a time: one 16-byte piece of W's row a and one of
+// each token row.
 template <int D, int NTOK>
 __device__ __forceinline__ void bwd_matvec(const float* sW, const float* X, float* Y) {
   constexpr int NG = kBwdThreads / D, TPG = NTOK / NG;
@@ -150,10 +152,14 @@ __device__ __forceinline__ void bwd_matvec(const float* sW, const float* X, floa
   float acc[TPG];
 #pragma unroll
   for (int i = 0; i < TPG; ++i) acc[i] = 0.f;
-  for (int c = 0; c < D; ++c) {
-    const float wv = bwd_w<D>(sW, a, c);
+#pragma unroll 1
+  for (int c = 0; c < D; c += 4) {
+    const float4 wv = *reinterpret_cast<const float4*>(sW + a * D + (((c >> 2) ^ (a & (D / 4 - 1))) << 2));
 #pragma unroll
-    for (int i = 0; i < TPG; ++i) acc[i] = fmaf(wv, X[(g * TPG + i) * D + c], acc[i]);
+    for (int i = 0; i < TPG; ++i) {
+      const float4 xv = *reinterpret_cast<const float4*>(X + (g * TPG + i) * D + c);
+      acc[i] = fmaf(wv.x, xv.x, fmaf(wv.y, xv.y, fmaf(wv.z, xv.z, fmaf(wv.w, xv.w, acc[i]))));
+    }
   }
 #pragma unroll
   for (int i = 0; i < TPG; ++i) Y[(g * TPG + i) * D + a] = acc[i];
