@@ -277,6 +277,7 @@ class L2Flush:
         self.buf.zero_()
 
 
+E2E_LOOPS = 5                     # timed loops of the end-to-end leg (median reported)
 L2_FLUSHED = "L2 flushed before each step (a 516 MB write outside the timed events)"
 
 
@@ -420,25 +421,30 @@ def our_arm(args, wl, L):
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
-    if small:
-        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(e2e_steps)]
-        for a, b in pairs:
-            flush()
-            a.record(stream)
-            e2e_step()
-            b.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = sum(a.elapsed_time(b) for a, b in pairs) / e2e_steps
-    else:
+
+    def e2e_loop():
+        if small:
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(e2e_steps)]
+            for a, b in pairs:
+                flush()
+                a.record(stream)
+                e2e_step()
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            return sum(a.elapsed_time(b) for a, b in pairs) / e2e_steps
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(e2e_steps):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = a.elapsed_time(b) / e2e_steps
-    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+        return a.elapsed_time(b) / e2e_steps
+
+    # The host link is shared with the machine's other GPUs, and a single loop occasionally
+    # runs 30-80 % slower: the median of E2E_LOOPS loops is reported, each loop beside it.
+    e2e_samples = [e2e_loop() for _ in range(E2E_LOOPS)]
+    e2e_ms = max_over_ranks(statistics.median(e2e_samples), dist, dev)
     e2e_value = job_throughput(B * T, world, e2e_ms)
 
     # ---- roofline of the dominant kernel, against the method's own work
@@ -495,7 +501,8 @@ def our_arm(args, wl, L):
                        "l2": L2_FLUSHED if small else "inputs larger than L2 (no flush)"},
             "roofline": roof, "kernels": kernels, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "loops_ms_per_step": e2e_samples, "steps_per_loop": e2e_steps},
             "gpu_launches": args.steps * launches_per_step}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
