@@ -172,7 +172,13 @@ PRISM_API int prism_forward_from(const prism_dims* dims,
  * prism_prepare + prism_scan call that used this workspace (same dims).  Every
  * wait those kernels make on an mbarrier is bounded; one that gives up writes a
  * nonzero word instead of hanging, and that call's outputs are then invalid.
- *   *status = 0 when every wait completed; nonzero otherwise.
+ *   *status = 0 when every wait completed and, on the PRISM_BF16 path, every value
+ *   written to out and final_state is finite.  Bit 0 (1): a wait gave up.  Bit 1 (2,
+ *   PRISM_BF16 path): a non-finite value reached out or final_state.  With finite
+ *   inputs this means a value beyond the fp16 range of the tensor-core operands: a
+ *   refinement chain that diverges until |delta^(l)| >= 65504, which long chains (L near
+ *   8) with large gains can reach.  The outputs are then invalid; the fp32 path
+ *   (PRISM_F32) is not limited this way.
  * Waits for `stream` (it copies 4 bytes from the workspace and synchronises), so
  * call it on the stream the forward pass ran on, after it.  The word is cleared
  * at the start of each forward call.  Errors: as for prism_forward's dims and

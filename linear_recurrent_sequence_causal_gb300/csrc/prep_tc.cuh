@@ -1333,7 +1333,7 @@ __global__ void __launch_bounds__(PrepSmem<D, C>::NTA, PrepSmem<D, C>::kMinBlock
   if (!S::kPrefetch && nxt < total && tid == 0) load_inputs(nxt);
   cur = nxt;
   }  // chunks
-  if (!ok) atomicExch(p.status, 1);
+  if (!ok) atomicOr(p.status, 1);
   // the last N^T bulk store of this CTA has been read out of shared memory; its writes
   // complete before the CTA exits
   if (producer && lane == 0) tc::bulk_wait_all();

@@ -168,6 +168,7 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
   const uint32_t tmem = *tslot;
   const uint32_t t_d1 = tmem, t_d3 = tmem, t_d2 = tmem + 2 * BV;   // 2BV (MMA1, then MMA2) and BV columns
   bool ok = true;
+  bool nonfinite = false;                      // a non-finite value written (status bit 1)
   // The failure path on request: nothing is in flight yet (no copy issued, no MMA), so a
   // wait that gives up here leaves nothing behind; it records the error like any other.
   if (p.check_timeout) ok &= tc::bar_wait(bar_never, 0, 1u << 10);
@@ -388,9 +389,9 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
 #pragma unroll
           for (int g = 0; g < HB / 4; ++g) {
             const float4 x = *reinterpret_cast<const float4*>(sX + r * S::LDX + hf * HB + 4 * g);
-            put(reinterpret_cast<float4*>(dst + 4 * g),
-                make_float4(ov[4 * g] + x.x, ov[4 * g + 1] + x.y, ov[4 * g + 2] + x.z, ov[4 * g + 3] + x.w), p.out,
-                (size_t)p.B * T_ * H * D * 4, bw);
+            const float4 o = make_float4(ov[4 * g] + x.x, ov[4 * g + 1] + x.y, ov[4 * g + 2] + x.z, ov[4 * g + 3] + x.w);
+            nonfinite |= !(isfinite(o.x) && isfinite(o.y) && isfinite(o.z) && isfinite(o.w));
+            put(reinterpret_cast<float4*>(dst + 4 * g), o, p.out, (size_t)p.B * T_ * H * D * 4, bw);
           }
         }
       }
@@ -418,10 +419,17 @@ __global__ void __launch_bounds__(ScanTcSmem<D_, C>::NT, ScanTcSmem<D_, C>::kMin
                                       : static_cast<const void*>(p.seg_start);
       const size_t fext = (kind == 0 && (p.phase == 0 || last_seg)) ? state_bytes : seg_bytes;
 #pragma unroll
-      for (int v = 0; v < HB; ++v) put(fs + (size_t)(v0 + hf * HB + v) * D + k, st[v], fbase, fext, bw);
+      for (int v = 0; v < HB; ++v) {
+        nonfinite |= !isfinite(st[v]);
+        put(fs + (size_t)(v0 + hf * HB + v) * D + k, st[v], fbase, fext, bw);
+      }
     }
   }
-  if (!ok) atomicExch(p.status, 1);
+  // status bit 0: a bounded wait gave up; bit 1: a non-finite value reached an output or
+  // an end state (with finite inputs: a value beyond the fp16 range of the tensor-core
+  // operands, |delta^(l)| >= 65504, as a diverging refinement chain can reach)
+  if (!ok) atomicOr(p.status, 1);
+  if (__any_sync(0xffffffffu, nonfinite) && lane == 0) atomicOr(p.status, 2);
   tc::fence_before();
   __syncthreads();
   if (warp == 0) tc::dealloc(tmem, S::kTmemCols);

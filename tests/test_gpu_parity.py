@@ -157,6 +157,75 @@ def test_every_sequence_empty(dtype, D, C, L):
     assert torch.count_nonzero(out).item() == 0 and torch.count_nonzero(fs).item() == 0
 
 
+def _random_cases(n, seed):
+    """Seeded random shapes over every supported axis (dtype, d, L, w, chunk, T, ragged)."""
+    import random
+    rnd = random.Random(seed)
+    out = []
+    for i in range(n):
+        dtype = rnd.choice(["bf16", "bf16", "f32"])
+        D = rnd.choice([16, 32, 64] if dtype == "f32" else [16, 32, 64, 128])
+        out.append((dtype, rnd.randint(1, 4), rnd.randint(1, 300), rnd.randint(1, 3), D,
+                    rnd.randint(0, 8), rnd.randint(1, 8), rnd.choice([16, 32, 64]), rnd.random() < 0.5))
+    return out
+
+
+@pytest.mark.parametrize("dtype,B,T,H,D,L,w,chunk,ragged", _random_cases(64, 2026))
+def test_random_shapes(dtype, B, T, H, D, L, w, chunk, ragged):
+    """Random combinations of the supported axes against the oracle, at the dtype's
+    tolerance (ragged batches hold an empty sequence when B > 1)."""
+    wl = I.Workload("case", dtype, B, T, H, D, D, L, w, chunk, seed=3000 + T + 7 * D + L, ragged=False)
+    inp = I.generate(wl)
+    if ragged:
+        g = torch.Generator().manual_seed(T + D)
+        lens = torch.randint(0, T + 1, (B,), generator=g, dtype=torch.int32)
+        if B > 1:
+            lens[-1] = 0
+        inp["seq_lens"] = lens
+    d = prism.inputs_to_device(inp)
+    dims = prism.make_dims(B, T, H, D, D, w, L, chunk, wl.torch_dtype)
+    ws = prism.alloc_workspace(dims, "cuda")
+    out, fs = prism.forward_inputs(d, L, chunk, workspace=ws)
+    status = prism.device_status(dims, ws)
+    ro, rs, tr = oracle.forward(inp, trace=True)
+    if status & 2:
+        # the bf16 path flagged a non-finite value: only a refinement chain that reached
+        # the fp16 range of the tensor-core operands may do that
+        assert dtype == "bf16" and L > 0, "non-finite flag on a path without fp16 operands"
+        dl = np.asarray(tr["dl"])
+        assert np.nanmax(np.abs(dl)) > 3e4, "non-finite output below the fp16 range"
+        return
+    assert status == 0
+    if ragged:
+        for b, n in enumerate(inp["seq_lens"].tolist()):
+            if n == 0:
+                rs[b] = 0.0
+    check(out, fs, ro, rs, dtype, seq_lens=inp.get("seq_lens"),
+          what=f"{dtype} B{B} T{T} H{H} D{D} L{L} w{w} C{chunk} ragged={ragged}")
+
+
+def test_refinement_beyond_fp16_range_is_flagged():
+    """A diverging refinement chain (L = 8, |delta^(l)| up to ~2e5) exceeds the fp16 range
+    of the tensor-core operands: the bf16 path sets status bit 1 instead of returning
+    non-finite outputs silently, and the fp32 path, which has no such limit, matches the
+    oracle on the same values."""
+    B, T, H, D, L, w, C = 1, 234, 2, 32, 8, 7, 16
+    wl = I.Workload("case", "bf16", B, T, H, D, D, L, w, C, seed=3000 + T + 7 * D + L)
+    inp = I.generate(wl)
+    inp["seq_lens"] = torch.tensor([186], dtype=torch.int32)
+    ro, rs, tr = oracle.forward(inp, trace=True)
+    assert np.nanmax(np.abs(np.asarray(tr["dl"]))) > 65504
+    d = prism.inputs_to_device(inp)
+    dims = prism.make_dims(B, T, H, D, D, w, L, C, torch.bfloat16)
+    ws = prism.alloc_workspace(dims, "cuda")
+    prism.forward_inputs(d, L, C, workspace=ws)
+    assert prism.device_status(dims, ws) & 2
+    # the same inputs through the fp32 path
+    f32 = {k: (v.float() if v is not None and v.dtype == torch.bfloat16 else v) for k, v in inp.items()}
+    out, fs = gpu_forward(f32, L, C)
+    check(out, fs, ro, rs, "f32", seq_lens=inp["seq_lens"], what="fp32 path, diverging chain")
+
+
 @pytest.mark.parametrize("chunk", [16, 32, 64])
 def test_chunk_size_invariance(chunk):
     wl = I.Workload("case", "bf16", 2, 300, 2, 64, 64, 3, 4, chunk, seed=77)
