@@ -137,3 +137,31 @@ def test_backward_every_sequence_empty(D):
     torch.cuda.synchronize()
     for n in G.GRAD_KEYS:
         assert torch.count_nonzero(gg[n]).item() == 0, f"d{n}"
+
+
+def _random_backward_cases(n, seed):
+    import random
+    rnd = random.Random(seed)
+    out = []
+    for _ in range(n):
+        dtype = rnd.choice(["bf16", "bf16", "f32"])
+        D = rnd.choice([16, 32, 64] if dtype == "f32" else [16, 32, 64, 128])
+        out.append((dtype, D, rnd.randint(0, 5), rnd.randint(1, 70), rnd.randint(1, 4), rnd.randint(1, 3),
+                    rnd.randint(1, 8), rnd.random() < 0.5, rnd.random() < 0.2, rnd.random() < 0.5))
+    return out
+
+
+@pytest.mark.parametrize("case", _random_backward_cases(12, 11), ids=lambda c: "-".join(map(str, c)))
+def test_backward_random_shapes(case):
+    """Seeded random shapes over every axis the backward pass supports, against the
+    gradient oracle at the same tolerance."""
+    dtype, D, L, T, B, H, w, ragged, no_gelu, with_fs = case
+    inp, ref, gg = _run(dtype, D, L, T, B, H, w, ragged, no_gelu, with_fs, seed=1500 + D + L + T)
+    for n in G.GRAD_KEYS:
+        if L == 0 and n in ("Wk", "Wp", "wbeta"):
+            continue
+        gpu = gg[n].double().cpu().numpy()
+        r = ref[n][:, :L] if n in ("Wk", "Wp", "wbeta") else ref[n]
+        assert np.all(np.isfinite(gpu)), f"d{n}: non-finite"
+        err = np.max(np.abs(gpu - r)) / max(np.max(np.abs(r)), 1e-30)
+        assert err <= GRAD_TOL, f"d{n}: {err:.3e}"

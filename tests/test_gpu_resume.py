@@ -100,3 +100,38 @@ def test_decode_steps_match_oracle(dtype, D, L, no_gelu, B, H, T0, n):
     # the history now holds the last w tokens
     np.testing.assert_array_equal(hist.float().cpu().numpy(),
                                   prism.v_history(d["v"], wl.w).float().cpu().numpy())
+
+
+def _random_decode_cases(n, seed):
+    import random
+    rnd = random.Random(seed)
+    out = []
+    for _ in range(n):
+        dtype = rnd.choice(["bf16", "bf16", "f32"])
+        D = rnd.choice([16, 32, 64] if dtype == "f32" else [16, 32, 64, 128])
+        w = rnd.randint(1, 8)
+        out.append((dtype, D, rnd.randint(0, 8), w, rnd.randint(1, 9), rnd.randint(1, 4), rnd.randint(w, 60),
+                    rnd.randint(1, 5), rnd.random() < 0.2))
+    return out
+
+
+@pytest.mark.parametrize("dtype,D,L,w,B,H,T0,n,no_gelu", _random_decode_cases(12, 5))
+def test_decode_random_shapes(dtype, D, L, w, B, H, T0, n, no_gelu):
+    """Seeded random shapes (conv widths 1..8 included): a chunked prefix, then decode
+    steps, against the oracle's single run."""
+    chunk = 16
+    wl = I.Workload("case", dtype, B, T0 + n, H, D, D, L, w, chunk, seed=900 + T0 + D + L + w)
+    inp = I.generate(wl)
+    ro, rs, _ = oracle.forward(inp, identity_act=no_gelu)
+    d = prism.inputs_to_device(inp)
+    out0, state = _run(_tokens(d, 0, T0), L, chunk, no_gelu=no_gelu)
+    hist = prism.v_history(d["v"], w, T0)
+    outs = [out0]
+    for t in range(T0, T0 + n):
+        tok = {k: d[k][:, t].clone() for k in TOKEN_KEYS}
+        o = prism.prism_decode_step(tok["q"], tok["k"], tok["v"], tok["log_alpha"], tok["beta"],
+                                    d["conv_w"], d["Wk"], d["Wp"], d["wbeta"], L, state, hist,
+                                    no_gelu=no_gelu)
+        outs.append(o[:, None])
+    torch.cuda.synchronize()
+    check(torch.cat(outs, dim=1), state, ro, rs, dtype, what="decode, random shape")
